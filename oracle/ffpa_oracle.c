@@ -1,0 +1,241 @@
+/*
+ * Float64 CPU oracle for exact scaled-dot-product attention (forward).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the package smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table
+ * or helper with the CUDA library.
+ *
+ * What it computes (FFPA API reference, "ffpa_attn.ffpa_attn_func",
+ * description of `query`/`key`/`value`, `attn_mask`, `is_causal`, `scale`,
+ * `enable_gqa` and "Returns"):
+ *
+ *   O = softmax(scale * Q K^T + mask) V            per (batch, query head)
+ *
+ *   - query head hq reads key/value head hq / (Hq / Hkv)  (grouped heads,
+ *     "Nh_q must be an integer multiple of Nh_kv");
+ *   - a boolean mask keeps an element where it is true ("True means the
+ *     element participates"); a floating mask is an additive bias;
+ *   - is_causal: query row r sees key k only when k <= r + (Nkv - Nq)
+ *     ("queries aligned to the tail of the KV sequence");
+ *   - scale defaults to 1/sqrt(D) (chosen by the caller of this file).
+ *
+ * The log-sum-exp returned beside O is the natural logarithm of
+ * sum_k exp(scale * q.k + mask) (FFPA API reference,
+ * "ffpa_attn.ffpa_attn_varlen_func", `return_lse`: fp32, "CUDA convention").
+ * A row whose every key is masked has no softmax; it is given O = 0 and
+ * LSE = -inf (the FlashAttention convention; the pages say nothing).
+ *
+ * Packed variable-length input (FFPA API reference,
+ * "ffpa_attn.ffpa_attn_varlen_func"): q is [T_q, H_q, D], k/v are
+ * [T_k, H_kv, D]; sequence s owns rows cu_q[s]..cu_q[s+1]-1 of q and
+ * cu_k[s]..cu_k[s+1]-1 of k/v, and is attended exactly like a dense
+ * problem of those lengths (causal alignment is per sequence, lower right).
+ * LSE is stored as [H_q, T_q].
+ *
+ * Inputs are read as the raw 16-bit patterns of bf16 or fp16 and widened
+ * exactly to double; every sum, exponential and logarithm is in double.
+ * No blocking, fusion or reordering beyond the definition above.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_BF16 = 0, ORACLE_FP16 = 1 };
+enum { ORACLE_MASK_NONE = 0, ORACLE_MASK_BOOL = 1, ORACLE_MASK_F32 = 2, ORACLE_MASK_QTYPE = 3 };
+
+/* bf16 is the top half of an IEEE binary32: widen by shifting. */
+static double widen_bf16(uint16_t h) {
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* IEEE binary16: sign, 5-bit exponent (bias 15), 10-bit fraction. */
+static double widen_fp16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -24);                 /* subnormal: frac * 2^-24 */
+    else if (expo == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(frac | 0x400), expo - 25); /* (1024+frac) * 2^(e-15-10) */
+    return sign ? -mag : mag;
+}
+
+static double widen(const uint16_t* p, int dtype) {
+    return dtype == ORACLE_FP16 ? widen_fp16(*p) : widen_bf16(*p);
+}
+
+/* One attention row: query vector qrow (stride 1 over D, element stride
+ * given), keys/values for n_keys rows.  mask_* describe this row's mask
+ * entries over keys (stride mk_str, elements).  causal_limit is the
+ * largest visible key index (or n_keys-1 when not causal).  Writes D
+ * doubles to out and returns the LSE. */
+static double attend_row(const uint16_t* qrow, const uint16_t* kbase, const uint16_t* vbase,
+                         int64_t k_row_stride, int64_t v_row_stride, int n_keys, int D, int dtype, double scale,
+                         int mask_kind, const void* mask_row, int64_t mk_str, int64_t causal_limit,
+                         double* s /* scratch, n_keys */, double* out) {
+    double m = -INFINITY;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        const uint16_t* krow = kbase + (int64_t)kk * k_row_stride;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += widen(qrow + d, dtype) * widen(krow + d, dtype);
+        double x = scale * dot;
+        if (mask_kind == ORACLE_MASK_BOOL) {
+            if (((const uint8_t*)mask_row)[kk * mk_str] == 0) x = -INFINITY;
+        } else if (mask_kind == ORACLE_MASK_F32) {
+            x += (double)((const float*)mask_row)[kk * mk_str];
+        } else if (mask_kind == ORACLE_MASK_QTYPE) {
+            x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);
+        }
+        if ((int64_t)kk > causal_limit) x = -INFINITY;
+        s[kk] = x;
+        if (x > m) m = x;
+    }
+    if (m == -INFINITY) {               /* every key masked: no softmax */
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        return -INFINITY;
+    }
+    double l = 0.0;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        s[kk] = exp(s[kk] - m);         /* unnormalised weight */
+        l += s[kk];
+    }
+    for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int kk = 0; kk < n_keys; ++kk)
+            acc += s[kk] * widen(vbase + (int64_t)kk * v_row_stride + d, dtype);
+        out[d] = acc / l;
+    }
+    return m + log(l);
+}
+
+/*
+ * Dense layout.  q: [B, Hq, Nq, D] with element strides q_str[4]; k, v:
+ * [B, Hkv, Nkv, D] with k_str / v_str (the D stride must be 1 for all).
+ * mask: broadcastable to [B, Hq, Nq, Nkv], element strides m_str[4]
+ * (0 on a broadcast dimension), kind ORACLE_MASK_*.
+ *
+ * rows == NULL: every row; o is [B, Hq, Nq, D] and lse [B, Hq, Nq],
+ * both contiguous.  Otherwise rows[r] is the flat index
+ * (b*Hq + hq)*Nq + i of the r-th requested row; o is [nrows, D] and lse
+ * [nrows].  Returns 0, or -1 on a bad argument.
+ */
+int oracle_attn_dense(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                      int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                      const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                      const void* mask, int mask_kind, const int64_t* m_str,
+                      double scale, int causal,
+                      const int64_t* rows, int64_t nrows,
+                      double* o, double* lse, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Nq < 0 || Nkv < 0 || D <= 0) return -1;
+    const int group = Hq / Hkv;
+    const int64_t total = rows ? nrows : (int64_t)B * Hq * Nq;
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
+        if (!s) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < total; ++r) {
+            if (!s) continue;
+            int64_t flat = rows ? rows[r] : r;
+            int64_t i = flat % Nq;
+            int64_t bh = flat / Nq;
+            int hq = (int)(bh % Hq);
+            int b = (int)(bh / Hq);
+            int hk = hq / group;
+            const uint16_t* qrow = q + b * q_str[0] + hq * q_str[1] + i * q_str[2];
+            const uint16_t* kb = k + b * k_str[0] + hk * k_str[1];
+            const uint16_t* vb = v + b * v_str[0] + hk * v_str[1];
+            const void* mrow = NULL;
+            int64_t mk = 0;
+            if (mask_kind != ORACLE_MASK_NONE) {
+                int64_t off = b * m_str[0] + hq * m_str[1] + i * m_str[2];
+                size_t esz = mask_kind == ORACLE_MASK_BOOL ? 1 : mask_kind == ORACLE_MASK_F32 ? 4 : 2;
+                mrow = (const char*)mask + off * (int64_t)esz;
+                mk = m_str[3];
+            }
+            int64_t limit = causal ? i + (int64_t)Nkv - Nq : (int64_t)Nkv - 1;
+            double* out = o + r * D;
+            lse[r] = attend_row(qrow, kb, vb, k_str[2], v_str[2], Nkv, D, dtype, scale, mask_kind, mrow,
+                                mk, limit, s, out);
+        }
+        free(s);
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Packed variable-length layout.  q: [Tq, Hq, D] (element strides
+ * q_str[3] over T, H, D); k, v: [Tk, Hkv, D].  cu_q, cu_k: nseq+1 row
+ * offsets (cu_k may equal cu_q).  o: [Tq, Hq, D] contiguous;
+ * lse: [Hq, Tq] contiguous.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                       int Hq, int Hkv, int D,
+                       const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                       const int32_t* cu_q, const int32_t* cu_k, int nseq,
+                       double scale, int causal, double* o, double* lse, int nthreads) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || nseq < 1) return -1;
+    const int group = Hq / Hkv;
+    const int64_t Tq = cu_q[nseq];
+    int64_t maxk = 1;
+    for (int sq = 0; sq < nseq; ++sq) {
+        int64_t lk = cu_k[sq + 1] - cu_k[sq];
+        if (cu_q[sq + 1] < cu_q[sq] || lk < 0) return -1;
+        if (lk > maxk) maxk = lk;
+    }
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)maxk);
+        if (!s) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < Tq * Hq; ++r) {
+            if (!s) continue;
+            int64_t t = r / Hq;         /* packed query row */
+            int hq = (int)(r % Hq);
+            int sq = 0;                 /* owning sequence */
+            while (!(t >= cu_q[sq] && t < cu_q[sq + 1])) ++sq;
+            int64_t i = t - cu_q[sq];   /* row within the sequence */
+            int64_t nq = cu_q[sq + 1] - cu_q[sq];
+            int nk = cu_k[sq + 1] - cu_k[sq];
+            int hk = hq / group;
+            const uint16_t* qrow = q + t * q_str[0] + hq * q_str[1];
+            const uint16_t* kb = k + (int64_t)cu_k[sq] * k_str[0] + hk * k_str[1];
+            const uint16_t* vb = v + (int64_t)cu_k[sq] * v_str[0] + hk * v_str[1];
+            int64_t limit = causal ? i + (int64_t)nk - nq : (int64_t)nk - 1;
+            lse[(int64_t)hq * Tq + t] =
+                attend_row(qrow, kb, vb, k_str[0], v_str[0], nk, D, dtype, scale, ORACLE_MASK_NONE, NULL,
+                           0, limit, s, o + (t * Hq + hq) * D);
+        }
+        free(s);
+    }
+    return err ? -1 : 0;
+}

@@ -1,0 +1,333 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` instance and raises
+AssertionError when the oracle disagrees with:
+
+* torch's float64 CPU ``scaled_dot_product_attention`` (a library routine
+  with the same definition: FFPA API reference, ``ffpa_attn_func`` is
+  "Signature aligned with torch.nn.functional.scaled_dot_product_attention"),
+* closed forms (softmax of known logits, Q = 0 gives a plain mean and
+  LSE = ln(#visible keys), Nkv = 1 gives V_0 and LSE = scale*q.k_0),
+* invariants of the definition (rows of softmax sum to one, GQA equals
+  repeated-KV MHA, tail-aligned causal visibility, varlen equals
+  per-sequence dense, shift and permutation invariances).
+
+They live in a plain module so that ``test_oracle_pins.py`` runs them on the
+real oracle and ``test_oracle_mutants.py`` runs them on copies of the oracle
+with planted mistakes (each mutant must fail at least one pin).
+"""
+from __future__ import annotations
+
+import math
+import zlib
+
+import torch
+import torch.nn.functional as F
+
+from exact_headdim_attention_gb300 import workloads as wl
+
+ATOL = 1e-10
+
+
+def _close(a, b, atol=ATOL, what=""):
+    a = torch.as_tensor(a, dtype=torch.float64)
+    b = torch.as_tensor(b, dtype=torch.float64)
+    assert a.shape == b.shape, f"{what}: shape {tuple(a.shape)} vs {tuple(b.shape)}"
+    fin = torch.isfinite(b)
+    assert torch.equal(torch.isfinite(a), fin), f"{what}: finiteness differs"
+    assert torch.equal(a[~fin], b[~fin]), f"{what}: infinities differ"
+    err = (a[fin] - b[fin]).abs().max().item() if fin.any() else 0.0
+    assert err <= atol, f"{what}: max |err| {err:.3e} > {atol:.1e}"
+
+
+def tail_causal_keep(Nq, Nkv):
+    """Tail-aligned causal visibility: row r keeps k <= r + (Nkv - Nq)."""
+    return torch.ones(Nq, Nkv, dtype=torch.bool).tril(diagonal=Nkv - Nq)
+
+
+def _sdpa_reference(q, k, v, mask, scale, causal):
+    """torch float64 SDPA with the causal rule expressed as an explicit mask."""
+    B, Hq, Nq, D = q.shape
+    Nkv = k.shape[2]
+    qd, kd, vd = q.double(), k.double(), v.double()
+    m = None
+    if mask is not None:
+        m = mask.double() if mask.dtype != torch.bool else mask
+    if causal:
+        keep = tail_causal_keep(Nq, Nkv)
+        if m is None:
+            m = keep
+        elif m.dtype == torch.bool:
+            m = m & keep
+        else:
+            m = m.masked_fill(~keep, -math.inf)
+    gqa = Hq != k.shape[1]
+    o = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=m, scale=scale, enable_gqa=gqa)
+    # LSE through library routines: matmul + logsumexp
+    kr = kd.repeat_interleave(Hq // k.shape[1], dim=1)
+    sc = (scale if scale is not None else 1 / math.sqrt(D)) * (qd @ kr.transpose(-1, -2))
+    if m is not None:
+        sc = sc.masked_fill(~m, -math.inf) if m.dtype == torch.bool else sc + m
+    lse = torch.logsumexp(sc, dim=-1)
+    return o, lse
+
+
+def _bool_mask(g, shape, Nq, Nkv):
+    m = torch.rand(*shape, generator=g) < 0.7
+    m = m.expand(*shape[:-2], Nq, Nkv).clone() if shape[-2] == 1 else m
+    # keep the tail diagonal so that no row is fully masked (causal or not)
+    idx = torch.arange(Nq)
+    m[..., idx, idx + (Nkv - Nq)] = True
+    return m
+
+
+SDPA_CASES = [
+    # name, B, Hq, Hkv, Nq, Nkv, D, causal, mask, dtype, scale
+    ("mha", 2, 2, 2, 5, 7, 64, False, None, torch.bfloat16, None),
+    ("gqa", 1, 4, 2, 6, 6, 32, False, None, torch.bfloat16, None),
+    ("mqa_causal_cross", 2, 3, 1, 3, 9, 16, True, None, torch.bfloat16, None),
+    ("causal_self", 1, 2, 2, 8, 8, 16, True, None, torch.bfloat16, 0.3),
+    ("bool_b1nk", 2, 2, 2, 4, 6, 16, False, ("bool", (2, 1, 4, 6)), torch.bfloat16, None),
+    ("bool_nk_causal", 1, 4, 2, 5, 7, 16, True, ("bool", (5, 7)), torch.bfloat16, None),
+    ("bool_h_bcast_q", 2, 2, 2, 3, 5, 16, False, ("bool", (1, 2, 1, 5)), torch.bfloat16, None),
+    ("add_f32", 2, 2, 1, 4, 6, 16, False, ("f32", (2, 1, 4, 6)), torch.bfloat16, 0.7),
+    ("add_qtype_causal", 1, 2, 2, 4, 6, 16, True, ("qtype", (1, 2, 4, 6)), torch.bfloat16, None),
+    ("fp16", 1, 2, 2, 5, 5, 32, False, None, torch.float16, None),
+    ("fp16_add_f32", 1, 2, 1, 3, 4, 16, True, ("f32", (3, 4)), torch.float16, 0.5),
+]
+
+
+def pin_sdpa_cases(orc, cases=SDPA_CASES):
+    for (name, B, Hq, Hkv, Nq, Nkv, D, causal, mspec, dtype, scale) in cases:
+        q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=zlib.crc32(name.encode()) % 100003, dtype=dtype)
+        mask = None
+        if mspec is not None:
+            kind, shape = mspec
+            if kind == "bool":
+                mask = _bool_mask(g, shape, Nq, Nkv)
+            elif kind == "f32":
+                mask = torch.randn(*shape, generator=g)
+            else:
+                mask = torch.randn(*shape, generator=g).to(dtype)
+        o, lse = orc.attn_dense(q, k, v, attn_mask=mask, scale=scale, is_causal=causal)
+        o_ref, lse_ref = _sdpa_reference(q, k, v, mask, scale, causal)
+        _close(o, o_ref, what=f"{name}: O")
+        _close(lse, lse_ref, what=f"{name}: LSE")
+
+
+def pin_strided_inputs(orc):
+    """Non-contiguous [B,N,H,D] views give the same result as contiguous copies."""
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn(2, 6, 4, 32, generator=g).bfloat16().transpose(1, 2)   # [B,H,N,D] view
+    k = torch.randn(2, 9, 2, 32, generator=g).bfloat16().transpose(1, 2)
+    v = torch.randn(2, 9, 2, 32, generator=g).bfloat16().transpose(1, 2)
+    o, lse = orc.attn_dense(q, k, v, is_causal=True)
+    o_ref, lse_ref = _sdpa_reference(q.contiguous(), k.contiguous(), v.contiguous(), None, None, True)
+    _close(o, o_ref, what="strided O")
+    _close(lse, lse_ref, what="strided LSE")
+
+
+def pin_closed_form_softmax(orc):
+    """Logits (0, 1, 2) on one-hot values: O = softmax(0,1,2), LSE = ln(1+e+e^2)."""
+    D = 64
+    q = torch.zeros(1, 1, 1, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, 3, D)
+    k[0, 0, :, 0] = torch.tensor([0.0, 1.0, 2.0])
+    v = torch.zeros(1, 1, 3, D)
+    for j in range(3):
+        v[0, 0, j, j] = 1.0
+    o, lse = orc.attn_dense(q.bfloat16(), k.bfloat16(), v.bfloat16(), scale=1.0)
+    z = 1 + math.e + math.e ** 2
+    want = torch.zeros(D, dtype=torch.float64)
+    want[:3] = torch.tensor([1 / z, math.e / z, math.e ** 2 / z], dtype=torch.float64)
+    _close(o[0, 0, 0], want, atol=1e-14, what="softmax(0,1,2)")
+    _close(lse[0, 0, 0], torch.tensor(math.log(z), dtype=torch.float64), atol=1e-14, what="ln(1+e+e^2)")
+
+
+def pin_zero_query(orc):
+    """Q = 0: every visible key has weight 1, O is their mean and LSE = ln(count).
+
+    With tail-aligned causal masking row r sees r + (Nkv - Nq) + 1 keys."""
+    B, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 5, 8, 16
+    _, k, v, _ = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=11)
+    q = torch.zeros(B, Hq, Nq, D, dtype=torch.bfloat16)
+    for causal in (False, True):
+        o, lse = orc.attn_dense(q, k, v, is_causal=causal)
+        for r in range(Nq):
+            n = r + (Nkv - Nq) + 1 if causal else Nkv
+            want = v[0, 0, :n].double().mean(dim=0)
+            for h in range(Hq):
+                _close(o[0, h, r], want, atol=1e-14, what=f"Q=0 mean r={r}")
+                _close(lse[0, h, r], torch.tensor(math.log(n), dtype=torch.float64), atol=1e-14,
+                       what=f"Q=0 LSE r={r}")
+
+
+def pin_single_key(orc):
+    """Nkv = 1: O equals V_0 exactly and LSE equals scale * q.k_0."""
+    q, k, v, _ = wl.draw_dense(2, 2, 2, 4, 1, 64, seed=12)
+    o, lse = orc.attn_dense(q, k, v, scale=0.25)
+    _close(o, v.double().expand(2, 2, 4, 64), atol=0.0, what="Nkv=1 O")
+    want = 0.25 * torch.einsum("bhnd,bhd->bhn", q.double(), k[:, :, 0].double())
+    _close(lse, want, atol=1e-12, what="Nkv=1 LSE")
+
+
+def pin_rows_sum_to_one(orc):
+    """V = 1 everywhere: each output element is sum_k softmax_k = 1."""
+    B, Hq, Hkv, Nq, Nkv, D = 2, 4, 2, 6, 9, 32
+    q, k, _, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=13)
+    v = torch.ones(B, Hkv, Nkv, D, dtype=torch.bfloat16)
+    mask = torch.randn(B, 1, Nq, Nkv, generator=g)
+    for causal in (False, True):
+        o, _ = orc.attn_dense(q, k, v, attn_mask=mask, is_causal=causal)
+        _close(o, torch.ones_like(o), atol=1e-13, what="rows sum to 1")
+
+
+def pin_identical_values(orc):
+    """All V rows equal to u: O = u for any logits."""
+    q, k, _, g = wl.draw_dense(1, 2, 2, 5, 7, 32, seed=14)
+    u = torch.randn(32, generator=g).bfloat16()
+    v = u.expand(1, 2, 7, 32).contiguous()
+    o, _ = orc.attn_dense(q, k, v, is_causal=True)
+    _close(o, u.double().expand_as(o), atol=1e-13, what="identical V rows")
+
+
+def pin_one_hot_logit(orc):
+    """One key with a logit 60 above the rest selects its V row (to e^-60)."""
+    D, Nkv, star = 64, 6, 3
+    q = torch.zeros(1, 1, 1, D)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, Nkv, D)
+    k[0, 0, star, 0] = 60.0
+    g = torch.Generator().manual_seed(15)
+    v = torch.randn(1, 1, Nkv, D, generator=g).bfloat16()
+    o, lse = orc.attn_dense(q.bfloat16(), k.bfloat16(), v, scale=1.0)
+    _close(o[0, 0, 0], v[0, 0, star].double(), atol=1e-20 + 1e-24, what="one-hot logit")
+    _close(lse[0, 0, 0], torch.tensor(60.0 + math.log1p((Nkv - 1) * math.exp(-60.0)),
+                                      dtype=torch.float64), atol=1e-14, what="one-hot LSE")
+
+
+def pin_causal_visibility(orc):
+    """Changing V at key t changes exactly the rows r with t <= r + (Nkv - Nq)."""
+    B, H, Nq, Nkv, D = 1, 1, 6, 10, 16
+    q, k, v, g = wl.draw_dense(B, H, H, Nq, Nkv, D, seed=16)
+    o0, _ = orc.attn_dense(q, k, v, is_causal=True)
+    for t in (Nkv - Nq, Nkv - Nq + 2, Nkv - 1):
+        v2 = v.clone()
+        v2[0, 0, t] = torch.randn(D, generator=g).bfloat16() * 4
+        o1, _ = orc.attn_dense(q, k, v2, is_causal=True)
+        for r in range(Nq):
+            same = torch.equal(o0[0, 0, r], o1[0, 0, r])
+            assert same == (t > r + (Nkv - Nq)), f"causal visibility broken at r={r}, t={t}"
+
+
+def pin_gqa_is_repeated_mha(orc):
+    """GQA equals MHA with K/V heads repeated group-wise (head hq reads hq // g)."""
+    B, Hq, Hkv, Nq, Nkv, D = 2, 6, 2, 5, 7, 32
+    q, k, v, _ = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=17)
+    o, lse = orc.attn_dense(q, k, v, is_causal=True)
+    kr = k.repeat_interleave(Hq // Hkv, dim=1).contiguous()
+    vr = v.repeat_interleave(Hq // Hkv, dim=1).contiguous()
+    o2, lse2 = orc.attn_dense(q, kr, vr, is_causal=True)
+    _close(o, o2, atol=0.0, what="GQA vs repeated MHA O")
+    _close(lse, lse2, atol=0.0, what="GQA vs repeated MHA LSE")
+
+
+def pin_shift_invariance(orc):
+    """A constant additive mask c leaves O unchanged and adds c to LSE."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 4, 6, 32, seed=18)
+    c = 1.75
+    o0, l0 = orc.attn_dense(q, k, v, is_causal=True)
+    o1, l1 = orc.attn_dense(q, k, v, attn_mask=torch.full((4, 6), c), is_causal=True)
+    _close(o1, o0, atol=1e-13, what="shift O")
+    _close(l1, l0 + c, atol=1e-13, what="shift LSE")
+
+
+def pin_all_true_mask(orc):
+    q, k, v, _ = wl.draw_dense(2, 2, 2, 4, 6, 32, seed=19)
+    o0, l0 = orc.attn_dense(q, k, v)
+    o1, l1 = orc.attn_dense(q, k, v, attn_mask=torch.ones(2, 1, 4, 6, dtype=torch.bool))
+    _close(o1, o0, atol=0.0, what="all-true mask O")
+    _close(l1, l0, atol=0.0, what="all-true mask LSE")
+
+
+def pin_kv_permutation(orc):
+    """Non-causal attention is invariant to permuting the key/value rows together."""
+    q, k, v, g = wl.draw_dense(1, 2, 2, 4, 9, 32, seed=20)
+    perm = torch.randperm(9, generator=g)
+    o0, l0 = orc.attn_dense(q, k, v)
+    o1, l1 = orc.attn_dense(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous())
+    _close(o1, o0, atol=1e-13, what="KV permutation O")
+    _close(l1, l0, atol=1e-13, what="KV permutation LSE")
+
+
+def pin_scale_fold(orc):
+    """Scaling Q by 2 (exact in bf16) with scale/2 leaves O and LSE unchanged."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 5, 6, 32, seed=21)
+    o0, l0 = orc.attn_dense(q, k, v, scale=0.3)
+    o1, l1 = orc.attn_dense(q * 2, k, v, scale=0.15)
+    _close(o1, o0, atol=1e-13, what="scale fold O")
+    _close(l1, l0, atol=1e-13, what="scale fold LSE")
+
+
+def pin_fully_masked_row(orc):
+    """A row with every key masked has O = 0 and LSE = -inf (adopted convention)."""
+    q, k, v, _ = wl.draw_dense(1, 1, 1, 3, 4, 16, seed=22)
+    mask = torch.ones(3, 4, dtype=torch.bool)
+    mask[1] = False
+    o, lse = orc.attn_dense(q, k, v, attn_mask=mask)
+    assert torch.equal(o[0, 0, 1], torch.zeros(16, dtype=torch.float64))
+    assert lse[0, 0, 1].item() == -math.inf
+    assert torch.isfinite(lse[0, 0, [0, 2]]).all()
+
+
+def pin_varlen_is_per_sequence_dense(orc):
+    """Packed varlen equals the dense definition applied to each sequence,
+    with lower-right causal alignment per sequence; also torch SDPA per sequence."""
+    lq, lk = [3, 7, 1, 5], [5, 7, 4, 2]
+    Hq, Hkv, D = 4, 2, 32
+    q, k, v, cq, ck = wl.draw_varlen(lq, lk, Hq, Hkv, D, seed=23)
+    for causal in (False, True):
+        o, lse = orc.attn_varlen(q, k, v, cq, ck, causal=causal)
+        for s in range(len(lq)):
+            qs = q[cq[s]:cq[s + 1]].transpose(0, 1).unsqueeze(0).contiguous()
+            ks = k[ck[s]:ck[s + 1]].transpose(0, 1).unsqueeze(0).contiguous()
+            vs = v[ck[s]:ck[s + 1]].transpose(0, 1).unsqueeze(0).contiguous()
+            od, ld = orc.attn_dense(qs, ks, vs, is_causal=causal)
+            _close(o[cq[s]:cq[s + 1]], od[0].transpose(0, 1), atol=0.0, what=f"varlen seq {s} O")
+            _close(lse[:, cq[s]:cq[s + 1]], ld[0], atol=0.0, what=f"varlen seq {s} LSE")
+            if causal and lk[s] < lq[s]:
+                continue   # rows with no visible key: SDPA gives NaN there
+            o_ref, l_ref = _sdpa_reference(qs, ks, vs, None, None, causal)
+            _close(od, o_ref, what=f"varlen seq {s} vs SDPA O")
+            _close(ld, l_ref, what=f"varlen seq {s} vs SDPA LSE")
+    # causal with a sequence shorter in keys than queries: early rows see nothing
+    o, lse = orc.attn_varlen(q, k, v, cq, ck, causal=True)
+    s = 3   # lq=5, lk=2: rows 0..2 see no key
+    rows = slice(int(cq[s]), int(cq[s]) + 3)
+    assert torch.equal(o[rows], torch.zeros_like(o[rows]))
+    assert bool((lse[:, rows] == -math.inf).all())
+
+
+def pin_varlen_default_cu_k(orc):
+    """cu_seqlens_k = None means cu_seqlens_q (self-attention)."""
+    lq = [4, 6]
+    q, k, v, cq, _ = wl.draw_varlen(lq, lq, 2, 2, 16, seed=24)
+    o0, l0 = orc.attn_varlen(q, k, v, cq, None, causal=True)
+    o1, l1 = orc.attn_varlen(q, k, v, cq, cq, causal=True)
+    _close(o0, o1, atol=0.0, what="cu_k default")
+    _close(l0, l1, atol=0.0, what="cu_k default LSE")
+
+
+def pin_sampled_rows(orc):
+    """The row-sampling entry returns exactly the rows of the full computation."""
+    q, k, v, g = wl.draw_dense(2, 4, 2, 7, 9, 32, seed=25)
+    mask = torch.randn(2, 1, 7, 9, generator=g)
+    o, lse = orc.attn_dense(q, k, v, attn_mask=mask, is_causal=True)
+    rows = torch.tensor([0, 5, 13, 27, 55])
+    o_r, l_r = orc.attn_dense(q, k, v, attn_mask=mask, is_causal=True, rows=rows)
+    _close(o_r, o.reshape(-1, 32)[rows], atol=0.0, what="sampled rows O")
+    _close(l_r, lse.reshape(-1)[rows], atol=0.0, what="sampled rows LSE")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
