@@ -1,0 +1,278 @@
+"""ctypes binding of libffpa (include/ffpa.h): argument marshalling only.
+
+Every step of the attention computation runs in the CUDA kernels behind
+the C ABI.  This module turns torch tensors into device pointers, element
+strides and sizes, allocates outputs with torch when the caller gives none,
+and maps status codes to the exception classes of the FFPA API reference
+("Raises": TypeError / ValueError / NotImplementedError).  There is no
+fallback: a missing library raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+FFPA_OK, FFPA_ERR_DTYPE, FFPA_ERR_INVALID, FFPA_ERR_UNSUPPORTED, FFPA_ERR_CUDA, \
+    FFPA_ERR_DEVICE_TIMEOUT = range(6)
+FFPA_BF16, FFPA_FP16 = 0, 1
+FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
+
+EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
+            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy")
+
+_lib = None
+
+
+class FFPAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class FFPATypeError(TypeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class FFPAValueError(ValueError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+class FFPANotImplementedError(NotImplementedError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+def lib_path() -> Path:
+    return _build.OUT
+
+
+def load_library(path: str | Path | None = None) -> ctypes.CDLL:
+    """Load libffpa.so; raises RuntimeError when it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path else lib_path()
+    if not p.exists():
+        raise RuntimeError(
+            f"libffpa.so not found at {p}: build it with "
+            "`python -m exact_headdim_attention_gb300.build` (no fallback path exists)")
+    lib = ctypes.CDLL(str(p))
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+    lib.ffpa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P, P, I, I, P]
+    lib.ffpa_fwd.restype = I
+    lib.ffpa_fwd_varlen.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, I, I, I, P,
+                                    I, I, P]
+    lib.ffpa_fwd_varlen.restype = I
+    lib.ffpa_status_string.argtypes = [I]
+    lib.ffpa_status_string.restype = ctypes.c_char_p
+    lib.ffpa_last_device_error.argtypes = [P]
+    lib.ffpa_last_device_error.restype = I
+    lib.ffpa_set_wait_timeout_ns.argtypes = [L]
+    lib.ffpa_set_wait_timeout_ns.restype = None
+    lib.ffpa_test_drop_first_copy.argtypes = [I]
+    lib.ffpa_test_drop_first_copy.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def ffpa_status_string(status: int) -> str:
+    return load_library().ffpa_status_string(status).decode()
+
+
+def _raise(status: int, what: str):
+    msg = f"{what}: {ffpa_status_string(status)}"
+    if status == FFPA_ERR_DTYPE:
+        raise FFPATypeError(status, msg)
+    if status == FFPA_ERR_INVALID:
+        raise FFPAValueError(status, msg)
+    if status == FFPA_ERR_UNSUPPORTED:
+        raise FFPANotImplementedError(status, msg)
+    raise FFPAError(status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FFPA_BF16
+    if t.dtype == torch.float16:
+        return FFPA_FP16
+    return -1
+
+
+def _strides(t: torch.Tensor):
+    return (ctypes.c_int64 * t.dim())(*t.stride())
+
+
+def _stream_handle(stream, t: torch.Tensor | None = None) -> int | None:
+    """cudaStream_t of `stream`, else of torch's current stream on t's device."""
+    if stream is None:
+        if t is not None and not t.is_cuda:
+            return None          # host tensors never reach a launch (the ABI rejects them)
+        stream = torch.cuda.current_stream(None if t is None else t.device)
+    return stream.cuda_stream or None
+
+
+_REJECTED = ("window_size", "softcap", "sink", "attention_mask", "block_mask", "score_mod",
+             "aux_tensors", "seqused_k", "block_table", "num_splits", "alibi_slopes")
+
+
+def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
+             dropout_p: float = 0.0, is_causal: bool = False, scale: float | None = None,
+             enable_gqa: bool = False, *, return_lse: bool = False, out=None, lse=None,
+             stream=None, **kwargs):
+    """Dense attention forward through the C ABI ``ffpa_fwd``.
+
+    q [B,Hq,Nq,D], k/v [B,Hkv,Nkv,D] (bf16 or fp16, CUDA, D stride 1);
+    attn_mask broadcastable to [B,Hq,Nq,Nkv] (bool: True participates;
+    float32 or the q dtype: additive).  Returns O [B,Hq,Nq,D], or (O, LSE
+    [B,Hq,Nq] fp32) with return_lse.  Follows the FFPA API reference,
+    ``ffpa_attn.ffpa_attn_func``."""
+    if kwargs:
+        raise TypeError(f"unexpected keyword arguments: {sorted(kwargs)}")
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout is not supported by this forward kernel")
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, D]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, Hq, Nq, D = q.shape
+    Bk, Hkv, Nkv, Dk = k.shape
+    if tuple(v.shape) != (Bk, Hkv, Nkv, Dk) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
+                            or tuple(lse.shape) != (B, Hq, Nq)):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
+    mk, mptr, mstr, keep = FFPA_MASK_NONE, None, None, None
+    if attn_mask is not None:
+        m = attn_mask
+        if m.dim() > 4:
+            raise ValueError("attn_mask has more than 4 dimensions")
+        while m.dim() < 4:
+            m = m.unsqueeze(0)
+        try:
+            m = m.expand(B, Hq, Nq, Nkv)
+        except RuntimeError as e:
+            raise ValueError(f"attn_mask {tuple(attn_mask.shape)} does not broadcast to "
+                             f"{(B, Hq, Nq, Nkv)}") from e
+        if m.device != q.device:
+            raise ValueError("attn_mask must be on the same device as q")
+        if m.dtype == torch.bool:
+            mk = FFPA_MASK_BOOL
+        elif m.dtype == torch.float32:
+            mk = FFPA_MASK_ADD_F32
+        elif m.dtype == q.dtype:
+            mk = FFPA_MASK_ADD_QTYPE
+        else:
+            raise TypeError(f"attn_mask dtype {m.dtype} not supported (bool, float32 or {q.dtype})")
+        keep, mptr, mstr = m, m.data_ptr(), _strides(m)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
+    st = lib.ffpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      None if lse is None else lse.data_ptr(), _dtype_code(q),
+                      B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v), _strides(out),
+                      mptr, mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
+                      _stream_handle(stream, q))
+    del keep
+    if st != FFPA_OK:
+        _raise(st, "ffpa_fwd")
+    return (out, lse) if return_lse else out
+
+
+def _check_cu(cu: torch.Tensor, T: int, name: str) -> list[int]:
+    if cu.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    if cu.dim() != 1 or cu.numel() < 2:
+        raise ValueError(f"{name} must be 1-D with at least 2 entries")
+    vals = cu.tolist()
+    if vals[0] != 0 or vals[-1] != T or any(b < a for a, b in zip(vals, vals[1:])):
+        raise ValueError(f"{name} must start at 0, end at {T} and be non-decreasing")
+    return vals
+
+
+def ffpa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                    cu_seqlens_k: torch.Tensor | None, max_seqlen_q: int, max_seqlen_k: int, *,
+                    dropout_p: float = 0.0, softmax_scale: float | None = None,
+                    causal: bool = False, enable_gqa: bool = False, return_lse: bool = False,
+                    out=None, lse=None, stream=None, **kwargs):
+    """Packed varlen attention forward through the C ABI ``ffpa_fwd_varlen``.
+
+    q [Tq,Hq,D], k/v [Tk,Hkv,D]; cu_seqlens_* int32 [nseq+1] (cu_seqlens_k
+    None reuses cu_seqlens_q).  Returns O [Tq,Hq,D], or (O, LSE [Hq,Tq])
+    with return_lse.  Follows the FFPA API reference,
+    ``ffpa_attn.ffpa_attn_varlen_func`` (including its rejected options)."""
+    for name in _REJECTED:
+        if kwargs.get(name) not in (None, False, (-1, -1), 0, 0.0):
+            raise NotImplementedError(f"option {name} is not supported")
+        kwargs.pop(name, None)
+    if kwargs:
+        raise TypeError(f"unexpected keyword arguments: {sorted(kwargs)}")
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout is not supported")
+    lib = load_library()
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    if _dtype_code(q) < 0:
+        raise TypeError(f"dtype {q.dtype} not supported (bf16 or fp16)")
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be 3-D [T, H, D]")
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    if tuple(v.shape) != (Tk, Hkv, Dk) or Dk != D:
+        raise ValueError("shape mismatch between q, k and v")
+    cq = _check_cu(cu_seqlens_q, Tq, "cu_seqlens_q")
+    ck = cq if cu_seqlens_k is None else _check_cu(cu_seqlens_k, Tk, "cu_seqlens_k")
+    if len(ck) != len(cq):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different batch sizes")
+    if cu_seqlens_k is None and Tk != Tq:
+        raise ValueError("cu_seqlens_k=None needs Tk == Tq")
+    if max(b - a for a, b in zip(cq, cq[1:])) > max_seqlen_q or \
+            max(b - a for a, b in zip(ck, ck[1:])) > max_seqlen_k:
+        raise ValueError("max_seqlen_* is smaller than a sequence length")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if return_lse and lse is None:
+        lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
+    cuq = cu_seqlens_q.to(q.device)
+    cuk = None if cu_seqlens_k is None else cu_seqlens_k.to(q.device)
+    sc = None if softmax_scale is None else ctypes.byref(ctypes.c_float(float(softmax_scale)))
+    st = lib.ffpa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             None if lse is None else lse.data_ptr(), _dtype_code(q),
+                             Tq, Tk, Hq, Hkv, D, _strides(q), _strides(k), _strides(v), _strides(out),
+                             cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
+                             int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
+                             int(bool(enable_gqa)), _stream_handle(stream, q))
+    if st != FFPA_OK:
+        _raise(st, "ffpa_fwd_varlen")
+    return (out, lse) if return_lse else out
+
+
+def ffpa_last_device_error(stream=None) -> int:
+    """Checked mode: synchronise the stream and return (and clear) the device error word."""
+    return load_library().ffpa_last_device_error(_stream_handle(stream))
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load_library().ffpa_set_wait_timeout_ns(int(ns))
+
+
+def inject_dropped_copy(enable: bool) -> None:
+    """Test hook: make the next launches skip their first tensor copy (see ffpa.h)."""
+    load_library().ffpa_test_drop_first_copy(int(bool(enable)))
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

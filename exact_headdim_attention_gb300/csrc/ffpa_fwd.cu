@@ -1,0 +1,825 @@
+// Exact attention forward for large head dimensions on GB300 (sm_103a).
+//
+// Method (FFPA README, "Split-D and TiledMMA"; FFPA API reference,
+// "ffpa_attn.ffpa_attn_func" / "ffpa_attn_varlen_func"): a FlashAttention
+// style online softmax over key tiles, with the head dimension D split into
+// 64-wide chunks so that the on-chip staging of Q, K and V does not grow
+// with D ("Split-D").  On Blackwell the accumulators live in Tensor Memory
+// (TMEM, 128 lanes x 512 fp32 columns per SM) instead of registers, so the
+// pages' register-pressure problem becomes a TMEM-capacity problem: a CTA
+// owns at most 256 output columns ("output-D slice") next to two 128-column
+// S buffers.  When D > 256 the output columns are split across CTAs and
+// each CTA recomputes S for its slice.
+//
+// Per CTA (one work item = batch b, query head h, 128-row query tile,
+// output-D slice) the warps specialise:
+//   warps 0-3  softmax: row r = 32*warp + lane; read S from TMEM, mask,
+//              online max / exp2 / sum, write P (16-bit) back over S, rescale
+//              O when the running max moved by more than 2^8, epilogue.
+//   warp 4     TMA producer: Q/K D-chunk pairs and V stages into a ring of
+//              32 KB shared-memory slots (128-byte swizzle), in the exact
+//              order the MMA warp consumes them.
+//   warp 5     MMA issuer (one thread): S_j = sum_c Q_c K_{j,c}^T into TMEM
+//              (tcgen05.mma, smem x smem), O += P_j V_j (P from TMEM).
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the
+// kernel records FFPA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ffpa.h"
+#include "ptx.cuh"
+
+namespace ffpa {
+
+constexpr int BM = 128;              // query rows per tile = TMEM lanes
+constexpr int BN = 128;              // keys per S tile
+constexpr int DK = 64;               // D chunk: one 128-byte swizzle row of 16-bit values
+constexpr int DV_MAX = 256;          // output columns per CTA
+constexpr int NSLOT = 6;             // ring slots
+constexpr uint32_t SLOT_BYTES = 32768;
+constexpr uint32_t CHUNK_BYTES = BM * DK * 2;  // 16 KB: one 128x64 tile
+constexpr int NTHREADS = 192;
+constexpr int PRODUCER_WARP = 4;
+constexpr int MMA_WARP = 5;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL0 = 256;     // S buffer b occupies columns [256 + 128 b, +128)
+constexpr float RESCALE_LOG2 = 8.0f; // rescale O only when the max grows by > 2^8
+constexpr size_t SMEM_BYTES = NSLOT * SLOT_BYTES + 1024;
+
+__device__ int g_err_word;
+
+struct Params {
+  CUtensorMap tm_q;    // dense: dims (D, Nq, Hq, B); varlen: (D, Hq, Tq); box 64 x 128 rows
+  CUtensorMap tm_k;    // same over keys
+  CUtensorMap tm_v;    // box 64 x vk rows
+  void* o;
+  float* lse;
+  const void* mask;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int64_t o_str[4];    // dense (b, h, n, d); varlen (t, h, d)
+  int64_t m_str[4];
+  int mask_kind;
+  int B;               // batches (dense) or sequences (varlen)
+  int Hq, group, Nq, Nkv, D, Tq;
+  int n_qt, n_slices, nchunks, vk;
+  float scale_log2;
+  int causal, fp16, inject;
+  unsigned long long timeout_ns;
+};
+
+struct Item {
+  int b, hq, hkv, slice;
+  int q0, q_len, kv_len, q_row0, kv_row0;
+  int col_lo, dv, ntiles;
+};
+
+__device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L, Item& it) {
+  it.slice = L % p.n_slices;
+  L /= p.n_slices;
+  const int heads = p.B * p.Hq;
+  int qt;
+  if (p.causal) {                    // longest query tiles first
+    const int bh = L % heads;
+    qt = p.n_qt - 1 - L / heads;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  } else {                           // tiles of one head adjacent: K/V reuse in L2
+    qt = L % p.n_qt;
+    const int bh = L / p.n_qt;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  }
+  it.hkv = it.hq / p.group;
+  if (varlen) {
+    it.q_row0 = p.cu_q[it.b];
+    it.q_len = p.cu_q[it.b + 1] - it.q_row0;
+    it.kv_row0 = p.cu_k[it.b];
+    it.kv_len = p.cu_k[it.b + 1] - it.kv_row0;
+  } else {
+    it.q_row0 = 0;
+    it.q_len = p.Nq;
+    it.kv_row0 = 0;
+    it.kv_len = p.Nkv;
+  }
+  it.q0 = qt * BM;
+  if (it.q0 >= it.q_len) return false;
+  const int rows = min(BM, it.q_len - it.q0);
+  long long kv_end = it.kv_len;
+  if (p.causal) {
+    const long long last_visible = (long long)it.q0 + rows - 1 + (it.kv_len - it.q_len);
+    kv_end = min(kv_end, last_visible + 1);
+  }
+  it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+  const int c_lo = it.slice * p.nchunks / p.n_slices;
+  const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
+  it.col_lo = c_lo * DK;
+  it.dv = (c_hi - c_lo) * DK;
+  return true;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when this CTA has been
+// told to abort or when the limit expires (then the error word is set).
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 127u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Drain wait used on the way out: ignores the abort flag.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Masks 32 consecutive scores (log2 domain) of one row: keys past the end,
+// keys beyond the causal limit, and the caller's bool/additive mask.
+__device__ __forceinline__ void apply_mask32(float* x, int key0, int kv_len, bool causal,
+                                             long long row_limit, const uint8_t* mrow,
+                                             long long mk, int mask_kind, bool fp16) {
+  const float LOG2E = 1.4426950408889634f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const int key = key0 + c;
+    bool vis = key < kv_len && (!causal || (long long)key <= row_limit);
+    float add = 0.f;
+    if (vis && mrow != nullptr) {
+      const long long e = (long long)key * mk;
+      if (mask_kind == FFPA_MASK_BOOL) {
+        vis = mrow[e] != 0;
+      } else if (mask_kind == FFPA_MASK_ADD_F32) {
+        add = reinterpret_cast<const float*>(mrow)[e] * LOG2E;
+      } else {
+        const uint16_t hbits = reinterpret_cast<const uint16_t*>(mrow)[e];
+        const float hv = fp16 ? __half2float(__ushort_as_half(hbits))
+                              : __bfloat162float(__ushort_as_bfloat16(hbits));
+        add = hv * LOG2E;
+      }
+    }
+    x[c] = vis ? x[c] + add : -INFINITY;
+  }
+}
+
+template <bool VARLEN>
+__global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_constant__ Params p) {
+  Item it;
+  if (!decode_item(p, VARLEN, blockIdx.x, it)) return;   // uniform across the CTA
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_empty[NSLOT];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2], bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t ring_u32 = smem_u32(ring);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_s_full[b]), 1);
+      mbar_init(smem_u32(&bar_p_full[b]), 4);
+      mbar_init(smem_u32(&bar_pv_done[b]), 1);
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int T = it.ntiles;
+  const unsigned long long tmo = p.timeout_ns;
+
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && T > 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      int slot = 0;
+      uint32_t lap = 0;
+      int issued = 0;
+      bool ok = true;
+      // Test hook: the very first stage of the CTA is acquired but never
+      // armed or copied, so the MMA warp's wait on it runs out.
+      bool drop = p.inject != 0;
+      const uint32_t v_bytes = (uint32_t)p.vk * it.dv * 2;
+      // Returns 0 on abort, 1 when the slot is armed for `bytes`, 2 when dropped.
+      auto acquire = [&](uint32_t bytes) -> int {
+        if (!wait_bounded(smem_u32(&bar_empty[slot]), lap ^ 1u, &abort_flag, tmo)) return 0;
+        if (drop) {
+          drop = false;
+          return 2;
+        }
+        mbar_arrive_expect_tx(smem_u32(&bar_full[slot]), bytes);
+        return 1;
+      };
+      auto advance = [&]() {
+        ++issued;
+        if (++slot == NSLOT) { slot = 0; lap ^= 1u; }
+      };
+      auto issue_qk = [&](int j) -> bool {
+        for (int c = 0; c < p.nchunks; ++c) {
+          const int a = acquire(2 * CHUNK_BYTES);
+          if (a == 0) return false;
+          if (a == 1) {
+            const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
+            const uint32_t fb = smem_u32(&bar_full[slot]);
+            if (VARLEN) {
+              tma_load_3d(dst, &p.tm_q, fb, c * DK, it.hq, it.q_row0 + it.q0);
+              tma_load_3d(dst + CHUNK_BYTES, &p.tm_k, fb, c * DK, it.hkv, it.kv_row0 + j * BN);
+            } else {
+              tma_load_4d(dst, &p.tm_q, fb, c * DK, it.q0, it.hq, it.b);
+              tma_load_4d(dst + CHUNK_BYTES, &p.tm_k, fb, c * DK, j * BN, it.hkv, it.b);
+            }
+          }
+          advance();
+        }
+        return true;
+      };
+      auto issue_v = [&](int j) -> bool {
+        for (int h = 0; h < BN / p.vk; ++h) {
+          const int a = acquire(v_bytes);
+          if (a == 0) return false;
+          if (a == 1) {
+            const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
+            const uint32_t fb = smem_u32(&bar_full[slot]);
+            const int key = j * BN + h * p.vk;
+            for (int t = 0; t < it.dv / DK; ++t) {
+              const int col = it.col_lo + t * DK;
+              if (VARLEN)
+                tma_load_3d(dst + t * p.vk * 128, &p.tm_v, fb, col, it.hkv, it.kv_row0 + key);
+              else
+                tma_load_4d(dst + t * p.vk * 128, &p.tm_v, fb, col, key, it.hkv, it.b);
+            }
+          }
+          advance();
+        }
+        return true;
+      };
+      for (int j = 0; j < T && ok; ++j) {
+        ok = issue_qk(j);
+        if (ok && j >= 1) ok = issue_v(j - 1);
+      }
+      if (ok && T > 0) ok = issue_v(T - 1);
+      // Drain: every copy this thread started has landed before the CTA exits
+      // (the dropped test stage, the first one, was never armed).
+      const int n = issued < NSLOT ? issued : NSLOT;
+      int s = slot;
+      uint32_t lp = lap;
+      for (int i = 0; i < n; ++i) {
+        if (--s < 0) { s = NSLOT - 1; lp ^= 1u; }
+        if (p.inject != 0 && issued - 1 - i == 0) continue;
+        wait_drain(smem_u32(&bar_full[s]), lp, tmo);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_f16(!p.fp16, BM, BN, false, false);
+      const uint32_t idesc_pv = idesc_f16(!p.fp16, BM, it.dv, false, true);
+      int slot = 0;
+      uint32_t lap = 0;
+      bool ok = true;
+      auto take = [&]() -> bool {
+        if (!wait_bounded(smem_u32(&bar_full[slot]), lap, &abort_flag, tmo)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto release = [&]() {
+        umma_commit(smem_u32(&bar_empty[slot]));
+        if (++slot == NSLOT) { slot = 0; lap ^= 1u; }
+      };
+      auto do_pv = [&](int j) -> bool {
+        const int b = j & 1;
+        if (!wait_bounded(smem_u32(&bar_p_full[b]), (j >> 1) & 1, &abort_flag, tmo)) return false;
+        tc_fence_after();
+        const uint32_t p_col = tmem + S_COL0 + 128 * b;
+        for (int h = 0; h < BN / p.vk; ++h) {
+          if (!take()) return false;
+          const uint32_t base = ring_u32 + slot * SLOT_BYTES;
+          for (int kk = 0; kk < p.vk / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(base + kk * 2048, p.vk * 128, 1024);
+            umma_ts(tmem, p_col + (h * p.vk + 16 * kk) / 2, bdesc, idesc_pv,
+                    (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          }
+          release();
+        }
+        umma_commit(smem_u32(&bar_pv_done[b]));
+        return true;
+      };
+      for (int j = 0; j < T && ok; ++j) {
+        const int b = j & 1;
+        if (j >= 2) {   // S buffer b holds P_{j-2} until PV_{j-2} completes
+          ok = wait_bounded(smem_u32(&bar_pv_done[b]), ((j - 2) >> 1) & 1, &abort_flag, tmo);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t s_col = tmem + S_COL0 + 128 * b;
+        for (int c = 0; c < p.nchunks && ok; ++c) {
+          ok = take();
+          if (!ok) break;
+          const uint32_t base = ring_u32 + slot * SLOT_BYTES;
+#pragma unroll
+          for (int k = 0; k < DK / 16; ++k) {
+            const uint64_t adesc = sdesc_sw128(base + k * 32, 16, 1024);
+            const uint64_t bdesc = sdesc_sw128(base + CHUNK_BYTES + k * 32, 16, 1024);
+            umma_ss(s_col, adesc, bdesc, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+          }
+          release();
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&bar_s_full[b]));
+        if (j >= 1) ok = do_pv(j - 1);
+      }
+      if (ok && T > 0) ok = do_pv(T - 1);
+      // Drain: all MMAs issued by this thread complete before TMEM is freed.
+      umma_commit(smem_u32(&bar_drain));
+      wait_drain(smem_u32(&bar_drain), 0, tmo);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = warp * 32 + lane;                 // row within the tile = TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int row = it.q0 + r;                      // row within the sequence
+    const bool row_valid = row < it.q_len;
+    const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
+    const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
+    const uint8_t* mrow = nullptr;
+    if (p.mask_kind != FFPA_MASK_NONE && row_valid) {
+      const size_t esz = p.mask_kind == FFPA_MASK_BOOL ? 1 : p.mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
+      const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
+                            (long long)row * p.m_str[2];
+      mrow = static_cast<const uint8_t*>(p.mask) + off * (long long)esz;
+    }
+    const long long mk = p.m_str[3];
+    float m_ref = -INFINITY;
+    float l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      const int b = j & 1;
+      bool w = wait_bounded(smem_u32(&bar_s_full[b]), (j >> 1) & 1, &abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_addr = lane_base + S_COL0 + 128 * b;
+      const int kbase = j * BN;
+      const bool need_mask = (kbase + BN > it.kv_len) ||
+                             (p.causal && (long long)kbase + BN - 1 > first_limit) ||
+                             p.mask_kind != FFPA_MASK_NONE;
+      float x[BN];
+#pragma unroll
+      for (int q4 = 0; q4 < BN / 32; ++q4) {
+        uint32_t raw[32];
+        tmem_ld32(s_addr + 32 * q4, raw);
+        tmem_wait_ld();
+        reg_fence(raw);
+        float* xg = x + 32 * q4;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) xg[c] = __uint_as_float(raw[c]) * p.scale_log2;
+        if (need_mask) apply_mask32(xg, kbase + 32 * q4, it.kv_len, p.causal != 0, row_limit, mrow,
+                                    mk, p.mask_kind, p.fp16 != 0);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, x[c]);
+      bool resc = false;
+      float alpha = 1.f;
+      if (mx > m_ref + RESCALE_LOG2) {
+        if (m_ref != -INFINITY) {
+          resc = true;
+          alpha = ex2_approx(m_ref - mx);
+        }
+        m_ref = mx;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O holds PV up to tile j-1: wait for it, then scale this warp's rows.
+        w = wait_bounded(smem_u32(&bar_pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, &abort_flag, tmo);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+        for (int c0 = 0; c0 < it.dv; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + c0, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+          tmem_st32(lane_base + c0, o);
+        }
+      }
+      // P = exp2(x - m_ref) in 16-bit, written over the S columns already read.
+      const float base = m_ref == -INFINITY ? 0.f : m_ref;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int g = 0; g < BN / 32; ++g) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const int cc = 32 * g + c;
+          const float e0 = ex2_approx(x[cc] - base), e1 = ex2_approx(x[cc + 1] - base);
+          const float e2 = ex2_approx(x[cc + 2] - base), e3 = ex2_approx(x[cc + 3] - base);
+          s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+          pk[c / 2] = p.fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+          pk[c / 2 + 1] = p.fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+        }
+        tmem_st16(s_addr + 16 * g, pk);
+      }
+      l_sum = l_sum * alpha + ((s0 + s1) + (s2 + s3));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_p_full[b]));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && T > 0) {
+      const bool w = wait_bounded(smem_u32(&bar_pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1,
+                                  &abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (ok) tc_fence_after();
+    }
+    if (ok || T == 0) {
+      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      uint8_t* obase = nullptr;
+      if (row_valid) {
+        long long off;
+        if (VARLEN)
+          off = (long long)(it.q_row0 + row) * p.o_str[0] + (long long)it.hq * p.o_str[1];
+        else
+          off = (long long)it.b * p.o_str[0] + (long long)it.hq * p.o_str[1] +
+                (long long)row * p.o_str[2];
+        obase = static_cast<uint8_t*>(p.o) + (off + it.col_lo) * 2;
+      }
+      for (int c0 = 0; c0 < it.dv; c0 += 32) {
+        uint32_t o[32];
+        if (T > 0) {
+          tmem_ld32(lane_base + c0, o);
+          tmem_wait_ld();
+          reg_fence(o);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
+        uint32_t pkd[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = __uint_as_float(o[2 * c]) * inv_l;
+          const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
+          pkd[c] = p.fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+        }
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+        }
+      }
+      if (row_valid && p.lse != nullptr && it.slice == 0) {
+        const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+        long long li;
+        if (VARLEN)
+          li = (long long)it.hq * p.Tq + it.q_row0 + row;
+        else
+          li = ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
+        p.lse[li] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace ffpa
+
+// =====================================================================
+// Host side: validation, planning, tensor maps, launch.
+// =====================================================================
+namespace {
+
+using namespace ffpa;
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_drop_first_copy{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Element strides of every non-unit dimension but the last must be a
+// multiple of 8 elements (16 bytes for 16-bit types); the last must be 1.
+bool strides_ok(const int64_t* str, const int64_t* size, int rank) {
+  if (str[rank - 1] != 1) return false;
+  for (int i = 0; i < rank - 1; ++i) {
+    if (size[i] <= 1) continue;
+    if (str[i] <= 0 || (str[i] % 8) != 0) return false;
+  }
+  return true;
+}
+
+// Tensor map over (D, dims[1], dims[2], ...) with byte strides; size-1
+// dimensions get a harmless stride so their (unused) value never fails the
+// encoder's alignment checks.
+ffpa_status encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const int64_t* elem_strides, uint32_t box_rows,
+                       int row_dim) {
+  auto enc = encode_fn();
+  if (!enc) return FFPA_ERR_CUDA;
+  cuuint64_t gdim[5];
+  cuuint64_t gstr[4];
+  cuuint32_t box[5];
+  cuuint32_t es[5];
+  uint64_t prev_bytes = dims[0] * 2;   // bytes spanned by the dimensions inside this one
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    box[i] = 1;
+    es[i] = 1;
+  }
+  box[0] = DK;
+  box[row_dim] = box_rows;
+  for (int i = 1; i < rank; ++i) {
+    uint64_t s = static_cast<uint64_t>(elem_strides[i]) * 2;
+    if (dims[i] <= 1) s = (prev_bytes + 15) & ~uint64_t(15);
+    gstr[i - 1] = s;
+    prev_bytes = s * dims[i];
+  }
+  CUresult r = enc(m, dt, rank, const_cast<void*>(base), gdim, gstr, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FFPA_OK : FFPA_ERR_INVALID;
+}
+
+// Makes the device that owns `ptr` current for this library's runtime (the
+// runtime is linked statically, so its current device is not the caller's),
+// then requires compute capability 10.3 (sm_103).
+ffpa_status check_device(const void* ptr, int* dev_out) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return FFPA_ERR_CUDA;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return FFPA_ERR_INVALID;
+  const int dev = attr.device;
+  if (cudaSetDevice(dev) != cudaSuccess) return FFPA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FFPA_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  return FFPA_OK;
+}
+
+void plan_slices(int D, Params* P) {
+  P->nchunks = D / DK;
+  P->n_slices = (D + DV_MAX - 1) / DV_MAX;
+  // widest slice: ceil(nchunks / n_slices) chunks
+  const int max_dv = ((P->nchunks + P->n_slices - 1) / P->n_slices) * DK;
+  P->vk = max_dv > 128 ? 64 : 128;
+}
+
+template <bool VARLEN>
+ffpa_status launch(const Params& P, int items, cudaStream_t stream) {
+  auto kern = ffpa_fwd_kernel<VARLEN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  kern<<<items, NTHREADS, SMEM_BYTES, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ffpa_status_string(ffpa_status s) {
+  switch (s) {
+    case FFPA_OK: return "FFPA_OK";
+    case FFPA_ERR_DTYPE: return "FFPA_ERR_DTYPE: inputs must be bf16 or fp16";
+    case FFPA_ERR_INVALID: return "FFPA_ERR_INVALID: invalid shape, stride, pointer or option";
+    case FFPA_ERR_UNSUPPORTED: return "FFPA_ERR_UNSUPPORTED: head dim or device not supported";
+    case FFPA_ERR_CUDA: return "FFPA_ERR_CUDA: a CUDA runtime call failed";
+    case FFPA_ERR_DEVICE_TIMEOUT: return "FFPA_ERR_DEVICE_TIMEOUT: a kernel wait ran out of time";
+  }
+  return "FFPA: unknown status";
+}
+
+void ffpa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
+
+void ffpa_test_drop_first_copy(int enable) { g_drop_first_copy.store(enable ? 1 : 0); }
+
+ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, ffpa::g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(ffpa::g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
+    return static_cast<ffpa_status>(word);
+  }
+  return FFPA_OK;
+}
+
+ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                     const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
+  if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (B == 0 || Nq == 0) return FFPA_OK;          // nothing to read or write
+  if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  if (mask_kind != FFPA_MASK_NONE && Nkv > 0) {
+    if (!mask || !mask_str) return FFPA_ERR_INVALID;
+    for (int i = 0; i < 4; ++i)
+      if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+  }
+  const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
+  if (!strides_ok(q_str, qsz, 4) || !strides_ok(o_str, qsz, 4)) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!strides_ok(k_str, ksz, 4) || !strides_ok(v_str, ksz, 4))) return FFPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || (Nkv > 0 && (!aligned16(k) || !aligned16(v))))
+    return FFPA_ERR_INVALID;
+  int dev = 0;
+  ffpa_status st = check_device(q, &dev);
+  if (st != FFPA_OK) return st;
+
+  Params P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  plan_slices(D, &P);
+  {
+    const uint64_t dq[4] = {(uint64_t)D, (uint64_t)Nq, (uint64_t)Hq, (uint64_t)B};
+    const int64_t sq[4] = {1, q_str[2], q_str[1], q_str[0]};
+    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq, sq, BM, 1)) != FFPA_OK) return st;
+  }
+  if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
+    const uint64_t dk[4] = {(uint64_t)D, (uint64_t)Nkv, (uint64_t)Hkv, (uint64_t)B};
+    const int64_t sk[4] = {1, k_str[2], k_str[1], k_str[0]};
+    if ((st = encode_map(&P.tm_k, tdt, 4, k, dk, sk, BN, 1)) != FFPA_OK) return st;
+    const int64_t sv[4] = {1, v_str[2], v_str[1], v_str[0]};
+    if ((st = encode_map(&P.tm_v, tdt, 4, v, dk, sv, P.vk, 1)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.lse = lse;
+  P.mask = mask_kind != FFPA_MASK_NONE ? mask : nullptr;
+  P.mask_kind = mask_kind;
+  for (int i = 0; i < 4; ++i) {
+    P.o_str[i] = o_str[i];
+    P.m_str[i] = mask_kind != FFPA_MASK_NONE ? mask_str[i] : 0;
+  }
+  P.B = B;
+  P.Hq = Hq;
+  P.group = Hq / Hkv;
+  P.Nq = Nq;
+  P.Nkv = Nkv;
+  P.D = D;
+  P.Tq = 0;
+  P.n_qt = (Nq + BM - 1) / BM;
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = is_causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.inject = g_drop_first_copy.load();
+  P.timeout_ns = g_timeout_ns.load();
+  const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
+  if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch<false>(P, static_cast<int>(items), reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3],
+                            const int64_t v_str[3], const int64_t o_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (nseq < 1 || max_seqlen_q < 0 || max_seqlen_k < 0) return FFPA_ERR_INVALID;
+  if (!cu_seqlens_q) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (Tq == 0 || max_seqlen_q == 0) return FFPA_OK;   // nothing to read or write
+  if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
+  if (Tk > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  const int64_t qsz[3] = {Tq, Hq, D}, ksz[3] = {Tk, Hkv, D};
+  if (!strides_ok(q_str, qsz, 3) || !strides_ok(o_str, qsz, 3)) return FFPA_ERR_INVALID;
+  if (Tk > 0 && (!strides_ok(k_str, ksz, 3) || !strides_ok(v_str, ksz, 3))) return FFPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
+    return FFPA_ERR_INVALID;
+  int dev = 0;
+  ffpa_status st = check_device(q, &dev);
+  if (st != FFPA_OK) return st;
+
+  Params P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  plan_slices(D, &P);
+  {
+    const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)Tq};
+    const int64_t sq[3] = {1, q_str[1], q_str[0]};
+    if ((st = encode_map(&P.tm_q, tdt, 3, q, dq, sq, BM, 2)) != FFPA_OK) return st;
+  }
+  if (Tk > 0) {
+    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)Tk};
+    const int64_t sk[3] = {1, k_str[1], k_str[0]};
+    if ((st = encode_map(&P.tm_k, tdt, 3, k, dk, sk, BN, 2)) != FFPA_OK) return st;
+    const int64_t sv[3] = {1, v_str[1], v_str[0]};
+    if ((st = encode_map(&P.tm_v, tdt, 3, v, dk, sv, P.vk, 2)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.lse = lse;
+  P.mask = nullptr;
+  P.mask_kind = FFPA_MASK_NONE;
+  P.o_str[0] = o_str[0];
+  P.o_str[1] = o_str[1];
+  P.o_str[2] = o_str[2];
+  P.cu_q = cu_seqlens_q;
+  P.cu_k = cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q;
+  P.B = nseq;
+  P.Hq = Hq;
+  P.group = Hq / Hkv;
+  P.Nq = 0;
+  P.Nkv = 0;
+  P.D = D;
+  P.Tq = Tq;
+  P.n_qt = (max_seqlen_q + BM - 1) / BM;
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.inject = g_drop_first_copy.load();
+  P.timeout_ns = g_timeout_ns.load();
+  (void)max_seqlen_k;
+  const long long items = (long long)nseq * Hq * P.n_qt * P.n_slices;
+  if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch<true>(P, static_cast<int>(items), reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+/*
+ * ffpa.h -- C ABI of libffpa: exact scaled-dot-product attention forward for
+ * large head dimensions (D = 64..1024) on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (FFPA API reference, "ffpa_attn.ffpa_attn_func", parameters
+ * `query`, `key`, `value`, `attn_mask`, `is_causal`, `scale`, `enable_gqa`
+ * and "Returns"; README, "Split-D and TiledMMA"):
+ *
+ *     O[b,h,i,:] = sum_k softmax_k( scale * Q[b,h,i,:].K[b,h/g,k,:] + M[b,h,i,k] ) V[b,h/g,k,:]
+ *
+ * with g = Hq / Hkv query heads per key/value head, M an optional boolean
+ * (true keeps, false removes) or additive mask broadcast to [B,Hq,Nq,Nkv],
+ * and, when causal, key k visible to query row i only if k <= i + (Nkv - Nq)
+ * (queries aligned to the tail of the keys).  The optional LSE output is the
+ * natural logarithm of sum_k exp(scale * q.k + M), in fp32 ("CUDA
+ * convention", FFPA API reference, "ffpa_attn_varlen_func", `return_lse`).
+ * A row with no visible key gets O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named q, k, v, o, lse, mask, cu_seqlens_* are DEVICE pointers
+ *    (memory the caller allocated on the current CUDA device).  `scale` is a
+ *    HOST pointer.  The library never allocates, frees or synchronises on the
+ *    caller's behalf (ffpa_last_device_error excepted); work is enqueued on
+ *    `stream` and runs asynchronously.  The caller owns every buffer and
+ *    must keep it alive until the stream has passed this work.
+ *  - Strides are in ELEMENTS.  The last (D) stride must be 1.  For q, k and
+ *    v every other stride times the element size must be a multiple of 16
+ *    bytes and the base pointer 16-byte aligned (tensor-memory-accelerator
+ *    loads); o must satisfy the same rules (16-byte vector stores).
+ *  - Inputs are bf16 or fp16 (all three the same type); O has the input type.
+ *  - Return codes: FFPA_OK, or the first failed check; nothing is enqueued
+ *    when the result is not FFPA_OK.
+ *
+ * Thread safety: the entry points keep no per-call state; they may be called
+ * concurrently from several host threads on different streams.
+ */
+#ifndef FFPA_H_
+#define FFPA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ffpa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  FFPA_OK = 0,
+  FFPA_ERR_DTYPE = 1,          /* input dtype other than bf16/fp16 (API reference: TypeError) */
+  FFPA_ERR_INVALID = 2,        /* bad shape, stride, pointer or option (API reference: ValueError) */
+  FFPA_ERR_UNSUPPORTED = 3,    /* head dim or device not covered (API reference: NotImplementedError) */
+  FFPA_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, attribute, device query) */
+  FFPA_ERR_DEVICE_TIMEOUT = 5  /* a kernel pipeline wait exceeded its time limit (see below) */
+} ffpa_status;
+
+typedef enum { FFPA_BF16 = 0, FFPA_FP16 = 1 } ffpa_dtype;
+
+typedef enum {
+  FFPA_MASK_NONE = 0,
+  FFPA_MASK_BOOL = 1,      /* uint8, nonzero = the element participates */
+  FFPA_MASK_ADD_F32 = 2,   /* float32 additive bias (may hold -inf) */
+  FFPA_MASK_ADD_QTYPE = 3  /* additive bias in the input dtype (bf16/fp16) */
+} ffpa_mask_kind;
+
+/*
+ * Dense attention forward (FFPA API reference, "ffpa_attn.ffpa_attn_func").
+ *
+ *   q   [B, Hq,  Nq,  D]   strides q_str  = (b, h, n, d)
+ *   k   [B, Hkv, Nkv, D]   strides k_str
+ *   v   [B, Hkv, Nkv, D]   strides v_str
+ *   o   [B, Hq,  Nq,  D]   strides o_str  (written)
+ *   lse [B, Hq, Nq] fp32 contiguous, or NULL when not wanted (written)
+ *   mask: NULL with FFPA_MASK_NONE, else broadcastable to [B, Hq, Nq, Nkv]
+ *         with element strides mask_str (0 on a broadcast dimension).
+ *   scale: NULL selects 1/sqrt(D) (API reference, `scale`).
+ *   is_causal: tail-aligned causal masking; requires Nkv >= Nq.
+ *   enable_gqa: must be nonzero when Hq != Hkv (API reference, `enable_gqa`).
+ *
+ * Checks, in order: dt (FFPA_ERR_DTYPE); sizes >= 0, Hq, Hkv >= 1
+ * (INVALID); 64 <= D <= 1024 and D % 64 == 0 (UNSUPPORTED); Hq % Hkv,
+ * enable_gqa, causal with Nkv < Nq, null pointers, strides, alignment, mask
+ * kind, non-finite scale (INVALID); device is sm_103 (UNSUPPORTED).  An
+ * empty problem (B, Hq or Nq zero) returns FFPA_OK without launching; Nkv
+ * = 0 writes O = 0 and LSE = -inf.
+ */
+ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                     const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream);
+
+/*
+ * Packed variable-length attention forward (FFPA API reference,
+ * "ffpa_attn.ffpa_attn_varlen_func").
+ *
+ *   q [Tq, Hq, D], k and v [Tk, Hkv, D] with strides (t, h, d); o like q.
+ *   cu_seqlens_q: int32 device array [nseq+1], cu[0] = 0, cu[nseq] = Tq,
+ *   non-decreasing; sequence s owns rows cu[s] .. cu[s+1]-1.
+ *   cu_seqlens_k: same for keys, or NULL to reuse cu_seqlens_q.
+ *   max_seqlen_q / max_seqlen_k: upper bounds of the per-sequence lengths
+ *   (a caller precondition: rows beyond max_seqlen_q are not computed).
+ *   lse: [Hq, Tq] fp32 contiguous, or NULL.
+ *   causal: lower-right (tail) alignment within each sequence.
+ *
+ * cu_seqlens live on the device and are not read by the host: a malformed
+ * array is a caller precondition (the Python binding checks it on the host).
+ * Other checks and error codes as for ffpa_fwd; nseq < 1 or max_seqlen_* < 0
+ * is FFPA_ERR_INVALID.
+ */
+ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3],
+                            const int64_t v_str[3], const int64_t o_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* ffpa_status_string(ffpa_status status);
+
+/*
+ * Checked mode: synchronises `stream`, then reads and clears the device error
+ * word that the kernels set when a pipeline wait runs past its time limit
+ * (every wait on the GPU is bounded; on expiry the kernel records
+ * FFPA_ERR_DEVICE_TIMEOUT, drains its own copies, frees its tensor memory and
+ * returns).  Returns FFPA_OK, FFPA_ERR_DEVICE_TIMEOUT, or FFPA_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+ffpa_status ffpa_last_device_error(ffpa_stream_t stream);
+
+/*
+ * Time limit of every in-kernel wait, in nanoseconds (default 2e9 = 2 s;
+ * 0 restores the default).  Applies to launches made after the call.
+ */
+void ffpa_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * TEST HOOK, not for production use: when nonzero, the next launches skip
+ * the first tensor copy of each CTA, so that the pipeline wait depending on
+ * it runs out and reports FFPA_ERR_DEVICE_TIMEOUT (no fault, no hang).
+ */
+void ffpa_test_drop_first_copy(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFPA_H_ */

@@ -1,0 +1,148 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+declared symbol, and every argument check returns the documented status
+without touching a GPU (no compute call is made)."""
+import ctypes
+import json
+import re
+import subprocess
+from pathlib import Path
+
+import pytest
+import torch
+
+import exact_headdim_attention_gb300 as pkg
+from exact_headdim_attention_gb300 import build as bld
+
+ROOT = Path(__file__).resolve().parent.parent
+GOLDEN = json.loads((Path(__file__).parent / "golden" / "api_errors.json").read_text())
+
+FAKE = 0x7F0000000000          # 16-byte aligned, never dereferenced by host checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bld.build()
+    return pkg.load_library()
+
+
+def declared_symbols():
+    text = (ROOT / "include" / "ffpa.h").read_text()
+    return sorted(set(re.findall(r"\b(ffpa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_symbols() == sorted(pkg.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(pkg.lib_path())], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ffpa_[a-z_]+)\b", out))
+    for name in declared_symbols():
+        assert name in exported, f"{name} not exported"
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        txt = pkg.ffpa_status_string(s)
+        assert txt.startswith("FFPA_")
+    assert "unknown" in pkg.ffpa_status_string(99)
+
+
+def _arr(vals):
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
+def dense_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,
+               q=FAKE, qs=None, mask=None, mask_kind=0, mask_str=None, scale=None, o=FAKE):
+    def st(H, N):
+        return _arr([H * N * D, N * D, D, 1])
+    qs = qs or st(Hq, Nq)
+    ks = st(Hkv, Nkv)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
+    return lib.ffpa_fwd(q, FAKE, FAKE, o, None, dt, B, Hq, Hkv, Nq, Nkv, D, qs, ks, ks, st(Hq, Nq),
+                        mask, mask_kind, mask_str, sc, causal, enable_gqa, None)
+
+
+def varlen_call(lib, dt=0, Tq=256, Tk=256, Hq=2, Hkv=2, D=64, nseq=2, causal=0, enable_gqa=0,
+                cu=FAKE, max_q=128, max_k=128):
+    def st(H):
+        return _arr([H * D, D, 1])
+    return lib.ffpa_fwd_varlen(FAKE, FAKE, FAKE, FAKE, None, dt, Tq, Tk, Hq, Hkv, D, st(Hq), st(Hkv),
+                               st(Hkv), st(Hq), cu, None, nseq, max_q, max_k, None, causal,
+                               enable_gqa, None)
+
+
+@pytest.mark.parametrize("case", GOLDEN["dense"], ids=lambda c: c["case"])
+def test_dense_documented_errors(lib, case):
+    assert dense_call(lib, **case["override"]) == case["status"]
+
+
+@pytest.mark.parametrize("case", GOLDEN["varlen"], ids=lambda c: c["case"])
+def test_varlen_documented_errors(lib, case):
+    assert varlen_call(lib, **case["override"]) == case["status"]
+
+
+def test_dense_layout_and_pointer_checks(lib):
+    INVALID = pkg.FFPA_ERR_INVALID
+    assert dense_call(lib, q=None) == INVALID
+    assert dense_call(lib, q=FAKE + 8) == INVALID                      # misaligned base
+    assert dense_call(lib, o=FAKE + 2) == INVALID
+    assert dense_call(lib, qs=_arr([2 * 128 * 64, 128 * 64, 64, 2])) == INVALID   # D stride != 1
+    assert dense_call(lib, qs=_arr([2 * 128 * 68, 128 * 68, 68, 1])) == INVALID   # 136-byte rows
+    assert dense_call(lib, B=-1) == INVALID
+    assert dense_call(lib, Hkv=0) == INVALID
+    assert dense_call(lib, mask_kind=9) == INVALID
+    assert dense_call(lib, mask_kind=1, mask=None, mask_str=_arr([0, 0, 0, 1])) == INVALID
+    assert dense_call(lib, mask_kind=2, mask=FAKE, mask_str=_arr([0, -1, 0, 1])) == INVALID
+    assert dense_call(lib, scale=float("inf")) == INVALID
+    assert dense_call(lib, scale=float("nan")) == INVALID
+
+
+def test_check_order_dtype_first(lib):
+    # a bad dtype is reported even when everything else is also wrong
+    assert dense_call(lib, dt=3, D=32, Hq=3, Hkv=2, q=None) == pkg.FFPA_ERR_DTYPE
+    # an unsupported head dim is reported before layout problems
+    assert dense_call(lib, D=32, q=None) == pkg.FFPA_ERR_UNSUPPORTED
+
+
+def test_varlen_pointer_checks(lib):
+    assert varlen_call(lib, cu=None) == pkg.FFPA_ERR_INVALID
+    assert varlen_call(lib, max_q=-1) == pkg.FFPA_ERR_INVALID
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    assert dense_call(lib) == pkg.FFPA_ERR_CUDA
+
+
+def test_binding_maps_statuses_to_page_exceptions(lib):
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        pkg.ffpa_fwd(q, q, q)
+    qb = q.bfloat16()
+    with pytest.raises(NotImplementedError):
+        pkg.ffpa_fwd(qb, qb, qb, dropout_p=0.1)
+    with pytest.raises(TypeError):
+        pkg.ffpa_fwd(qb, qb, qb, window_size=(1, 1))
+    qd = torch.zeros(1, 2, 4, 32, dtype=torch.bfloat16)
+    with pytest.raises(NotImplementedError):
+        pkg.ffpa_fwd(qd, qd, qd)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd(qb, qb[:, :1].expand(1, 1, 4, 64), qb[:, :1])   # Hq != Hkv, no enable_gqa
+
+
+def test_binding_rejects_malformed_cu_seqlens(lib):
+    q = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 10], dtype=torch.int64), None, 10, 10)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 4, 3, 10], dtype=torch.int32), None, 10, 10)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 9], dtype=torch.int32), None, 10, 10)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 10], dtype=torch.int32), None, 5, 10)
+    with pytest.raises(NotImplementedError):
+        pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 10], dtype=torch.int32), None, 10, 10,
+                            softcap=1.0)

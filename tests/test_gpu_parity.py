@@ -1,0 +1,304 @@
+"""CUDA path (through the C ABI) against the float64 oracle, element by element.
+
+Small problems are compared in full (sizes that still span several 128-row
+and 128-key tiles plus a ragged tail); the full-size workloads are compared
+on sampled rows, computed one by one by the oracle.
+"""
+import math
+
+import pytest
+import torch
+
+import exact_headdim_attention_gb300 as pkg
+import oracle
+from exact_headdim_attention_gb300 import workloads as wl
+from tests.gpu_util import check, device_ok, gather_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkg.load_library()
+    pkg.set_wait_timeout_ns(0)
+    yield
+
+
+def run_dense(q, k, v, mask=None, causal=False, scale=None, out=None, lse=None):
+    gqa = q.shape[1] != k.shape[1]
+    o, l = pkg.ffpa_fwd(q.to(DEV), k.to(DEV), v.to(DEV),
+                        attn_mask=None if mask is None else mask.to(DEV), is_causal=causal,
+                        scale=scale, enable_gqa=gqa, return_lse=True, out=out, lse=lse)
+    device_ok()
+    return o, l
+
+
+def dense_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, mask=None, scale=None,
+               dtype=torch.bfloat16, std=1.0):
+    q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed, std=std, dtype=dtype)
+    m = mask(g) if callable(mask) else mask
+    o, l = run_dense(q, k, v, m, causal, scale)
+    o_ref, l_ref = oracle.attn_dense(q, k, v, attn_mask=m, scale=scale, is_causal=causal)
+    return check(o, l, o_ref, l_ref, what=f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D}")
+
+
+# ------------------------------------------------------------------ small, full
+def test_tiny_d320_with_lse():
+    w = wl.tiny_d320()
+    x = wl.materialize(w)
+    o, l = run_dense(x["q"], x["k"], x["v"])
+    o_ref, l_ref = oracle.attn_dense(x["q"], x["k"], x["v"])
+    check(o, l, o_ref, l_ref, "tiny_d320")
+
+
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 384, 448, 512, 576, 640, 768, 896, 1024])
+def test_headdims_ragged(D):
+    dense_case(1, 2, 2, 300, 300, D, seed=D)
+
+
+@pytest.mark.parametrize("Nq,Nkv", [(1, 1), (7, 7), (127, 129), (129, 127), (1, 300), (300, 1),
+                                    (64, 513), (256, 256)])
+@pytest.mark.parametrize("D", [128, 512])
+def test_odd_lengths(Nq, Nkv, D):
+    dense_case(2, 2, 2, Nq, Nkv, D, seed=Nq * 7 + Nkv)
+    if Nkv >= Nq:
+        dense_case(1, 2, 2, Nq, Nkv, D, seed=Nq + Nkv, causal=True)
+
+
+@pytest.mark.parametrize("D", [256, 512, 1024])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (4, 1), (3, 3)])
+def test_causal_cross_gqa(D, Hq, Hkv):
+    dense_case(2, Hq, Hkv, 200, 700, D, seed=D + Hq, causal=True)
+
+
+def test_noncausal_cross_gqa_scale():
+    dense_case(1, 6, 2, 333, 150, 384, seed=5, scale=0.11)
+
+
+MASKS = {
+    "bool_b1nk": lambda B, H, Nq, Nk: (lambda g: torch.rand(B, 1, Nq, Nk, generator=g) < 0.6),
+    "bool_nk": lambda B, H, Nq, Nk: (lambda g: torch.rand(Nq, Nk, generator=g) < 0.3),
+    "bool_h1k": lambda B, H, Nq, Nk: (lambda g: torch.rand(1, H, 1, Nk, generator=g) < 0.8),
+    "f32_bhnk": lambda B, H, Nq, Nk: (lambda g: torch.randn(B, H, Nq, Nk, generator=g)),
+    "f32_neg_inf": lambda B, H, Nq, Nk: (lambda g: wl.draw_additive_mask(g, B, Nq, Nk)),
+    "qtype_b1nk": lambda B, H, Nq, Nk: (lambda g: torch.randn(B, 1, Nq, Nk, generator=g).bfloat16()),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MASKS))
+@pytest.mark.parametrize("causal", [False, True])
+def test_masks(name, causal):
+    B, H, Nq, Nk, D = 2, 2, 150, 300, 320
+    dense_case(B, H, H, Nq, Nk, D, seed=len(name), causal=causal, mask=MASKS[name](B, H, Nq, Nk))
+
+
+def test_fully_masked_rows_give_zero_and_neg_inf():
+    B, H, Nq, Nk, D = 1, 2, 130, 200, 128
+    q, k, v, g = wl.draw_dense(B, H, H, Nq, Nk, D, seed=77)
+    m = torch.rand(B, H, Nq, Nk, generator=g) < 0.5
+    m[0, 0, 5] = False
+    m[0, 1, 129] = False
+    o, l = run_dense(q, k, v, m)
+    o_ref, l_ref = oracle.attn_dense(q, k, v, attn_mask=m)
+    check(o, l, o_ref, l_ref, "fully masked rows")
+    assert torch.equal(o[0, 0, 5].cpu(), torch.zeros(D, dtype=o.dtype))
+    assert l[0, 0, 5].item() == -math.inf and l[0, 1, 129].item() == -math.inf
+
+
+@pytest.mark.parametrize("D", [320, 768])
+def test_fp16(D):
+    dense_case(1, 2, 1, 200, 260, D, seed=D, causal=True, dtype=torch.float16)
+
+
+def test_fp16_qtype_mask():
+    B, H, Nq, Nk, D = 1, 2, 140, 140, 256
+    dense_case(B, H, H, Nq, Nk, D, seed=3, dtype=torch.float16,
+               mask=lambda g: torch.randn(B, 1, Nq, Nk, generator=g).half())
+
+
+def test_strided_views():
+    """[B,N,H,D] tensors viewed as [B,H,N,D] (no copy), and K/V sliced from a wider buffer."""
+    g = torch.Generator().manual_seed(9)
+    B, H, Nq, Nk, D = 2, 4, 190, 260, 512
+    qb = torch.randn(B, Nq, H, D, generator=g).bfloat16()
+    kvb = torch.randn(B, Nk, H, 2 * D, generator=g).bfloat16()
+    q = qb.transpose(1, 2)
+    k = kvb[..., :D].transpose(1, 2)
+    v = kvb[..., D:].transpose(1, 2)
+    o, l = pkg.ffpa_fwd(qb.to(DEV).transpose(1, 2), kvb.to(DEV)[..., :D].transpose(1, 2),
+                        kvb.to(DEV)[..., D:].transpose(1, 2), is_causal=True, return_lse=True)
+    device_ok()
+    o_ref, l_ref = oracle.attn_dense(q, k, v, is_causal=True)
+    check(o, l, o_ref, l_ref, "strided")
+
+
+def test_guard_bands_untouched():
+    """O rows padded to a wider pitch and LSE inside a larger buffer: the
+    padding keeps its sentinel (no write outside the output)."""
+    B, H, Nq, Nk, D = 1, 3, 200, 333, 384
+    q, k, v, _ = wl.draw_dense(B, H, H, Nq, Nk, D, seed=11)
+    pitch = D + 64
+    big = torch.full((B, H, Nq + 2, pitch), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = big[:, :, 1:Nq + 1, :D]
+    lbig = torch.full((B * H * Nq + 64,), 5.0, dtype=torch.float32, device=DEV)
+    lse = lbig[32:32 + B * H * Nq].view(B, H, Nq)
+    o, l = run_dense(q, k, v, causal=True, out=out, lse=lse)
+    o_ref, l_ref = oracle.attn_dense(q, k, v, is_causal=True)
+    check(o, l, o_ref, l_ref, "guard")
+    bigc = big.cpu()
+    assert (bigc[:, :, 0] == 7).all() and (bigc[:, :, Nq + 1] == 7).all()
+    assert (bigc[..., D:] == 7).all()
+    lc = lbig.cpu()
+    assert (lc[:32] == 5).all() and (lc[32 + B * H * Nq:] == 5).all()
+
+
+def test_empty_keys_and_queries():
+    B, H, D = 1, 2, 128
+    q = torch.randn(B, H, 50, D).bfloat16()
+    k = torch.empty(B, H, 0, D, dtype=torch.bfloat16)
+    o, l = run_dense(q, k, k)
+    assert torch.equal(o.cpu(), torch.zeros_like(q)) and bool((l == -math.inf).all())
+    o, l = run_dense(q[:, :, :0], q, q)
+    assert o.numel() == 0
+    o, l = run_dense(q[:0], q[:0], q[:0])
+    assert o.numel() == 0
+
+
+# --------------------------------------------------------- kernel invariants
+def test_invariant_rows_sum_to_one():
+    q, k, _, g = wl.draw_dense(1, 4, 2, 260, 390, 512, seed=31)
+    v = torch.ones(1, 2, 390, 512, dtype=torch.bfloat16)
+    o, _ = run_dense(q, k, v, causal=True, mask=torch.randn(1, 1, 260, 390, generator=g))
+    assert (o.float() - 1).abs().max().item() <= 1e-2
+
+
+def test_invariant_single_key_returns_v():
+    q, k, v, _ = wl.draw_dense(2, 2, 2, 129, 1, 640, seed=32)
+    o, l = run_dense(q, k, v, scale=0.25)
+    assert torch.equal(o.cpu(), v.expand(2, 2, 129, 640))
+    want = 0.25 * torch.einsum("bhnd,bhd->bhn", q.double(), k[:, :, 0].double())
+    assert (l.cpu().double() - want).abs().max().item() <= 1e-3
+
+
+def test_invariant_zero_query_lse_counts_visible_keys():
+    Nq, Nk = 150, 400
+    _, k, v, _ = wl.draw_dense(1, 2, 2, Nq, Nk, 256, seed=33)
+    q = torch.zeros(1, 2, Nq, 256, dtype=torch.bfloat16)
+    _, l = run_dense(q, k, v, causal=True)
+    want = torch.tensor([math.log(i + Nk - Nq + 1) for i in range(Nq)], dtype=torch.float64)
+    assert (l.cpu().double() - want).abs().max().item() <= 1e-3
+
+
+def test_invariant_gqa_equals_repeated_mha():
+    q, k, v, _ = wl.draw_dense(1, 8, 2, 200, 300, 512, seed=34)
+    o1, l1 = run_dense(q, k, v, causal=True)
+    o2, l2 = run_dense(q, k.repeat_interleave(4, 1), v.repeat_interleave(4, 1), causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_invariant_causal_visibility():
+    Nq, Nk, D = 200, 330, 320
+    q, k, v, g = wl.draw_dense(1, 1, 1, Nq, Nk, D, seed=35)
+    o1, _ = run_dense(q, k, v, causal=True)
+    t = 250
+    v2 = v.clone()
+    v2[0, 0, t:] = torch.randn(Nk - t, D, generator=g).bfloat16() * 3
+    o2, _ = run_dense(q, k, v2, causal=True)
+    limit = torch.arange(Nq) + (Nk - Nq)
+    unchanged = (o1 == o2).all(dim=-1).cpu()[0, 0]
+    assert bool(unchanged[limit < t].all()), "a row changed although key t is beyond its limit"
+    assert (~unchanged[limit >= t]).float().mean().item() > 0.9
+
+
+# ----------------------------------------------------------------- varlen
+@pytest.mark.parametrize("D", [128, 512])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_small(D, causal):
+    lq = [3, 130, 1, 257, 0, 64, 200]
+    lk = [5, 130, 2, 200, 7, 64, 450]
+    Hq, Hkv = 4, 2
+    q, k, v, cq, ck = wl.draw_varlen(lq, lk, Hq, Hkv, D, seed=D)
+    Tq = q.shape[0]
+    pad = 40
+    big = torch.full((Tq + 2 * pad, Hq, D), 3.0, dtype=torch.bfloat16, device=DEV)
+    out = big[pad:pad + Tq]
+    o, l = pkg.ffpa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lq),
+                               max(lk), causal=causal, enable_gqa=True, return_lse=True, out=out)
+    device_ok()
+    o_ref, l_ref = oracle.attn_varlen(q, k, v, cq, ck, causal=causal)
+    check(o, l, o_ref, l_ref, "varlen")
+    bc = big.cpu()
+    assert (bc[:pad] == 3).all() and (bc[pad + Tq:] == 3).all()
+
+
+def test_varlen_self_default_cu_k():
+    lq = [100, 300, 129]
+    q, k, v, cq, _ = wl.draw_varlen(lq, lq, 2, 2, 256, seed=3)
+    o, l = pkg.ffpa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), None, 300, 300,
+                               causal=True, return_lse=True)
+    device_ok()
+    o_ref, l_ref = oracle.attn_varlen(q, k, v, cq, None, causal=True)
+    check(o, l, o_ref, l_ref, "varlen self")
+
+
+# -------------------------------------------------------------- timeout path
+def test_bounded_wait_reports_timeout_and_context_survives():
+    x = wl.materialize(wl.tiny_d320())
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    pkg.set_wait_timeout_ns(200_000_000)
+    pkg.inject_dropped_copy(True)
+    try:
+        pkg.ffpa_fwd(q, k, v)
+        st = pkg.ffpa_last_device_error()
+    finally:
+        pkg.inject_dropped_copy(False)
+        pkg.set_wait_timeout_ns(0)
+    assert st == pkg.FFPA_ERR_DEVICE_TIMEOUT
+    o, l = run_dense(x["q"], x["k"], x["v"])
+    o_ref, l_ref = oracle.attn_dense(x["q"], x["k"], x["v"])
+    check(o, l, o_ref, l_ref, "after timeout")
+
+
+# ------------------------------------------------------- full-size workloads
+def _sampled_dense(w, n_random=48):
+    x = wl.materialize(w)
+    o, l = run_dense(x["q"], x["k"], x["v"], mask=x["mask"], causal=w.causal)
+    rows = sample_rows(w.B, w.Hq, w.Nq, n_random=n_random, seed=w.seed)
+    o_ref, l_ref = oracle.attn_dense(x["q"], x["k"], x["v"], attn_mask=x["mask"], is_causal=w.causal,
+                                     rows=rows)
+    check(gather_rows(o, rows, w.D), l.reshape(-1)[rows.to(DEV)], o_ref, l_ref, w.name)
+
+
+@pytest.mark.parametrize("D", wl.HEADDIM_SWEEP)
+def test_full_headdim_sweep_sampled(D):
+    _sampled_dense(wl.headdim_sweep(D))
+
+
+def test_full_gqa_causal_sampled():
+    _sampled_dense(wl.gqa_causal(), n_random=32)
+
+
+def test_full_cross_additive_mask_sampled():
+    _sampled_dense(wl.cross_additive_mask(), n_random=32)
+
+
+def test_full_varlen_causal_sampled():
+    w = wl.varlen_causal()
+    x = wl.materialize(w)
+    q, k, v, cq = x["q"], x["k"], x["v"], x["cu_q"]
+    o, l = pkg.ffpa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), None, x["max_q"],
+                               x["max_k"], causal=True, enable_gqa=True, return_lse=True)
+    device_ok()
+    oc, lc = o.cpu(), l.cpu()
+    for s, L in enumerate(x["seqlens"]):
+        a = int(cq[s])
+        qs = q[a:a + L].transpose(0, 1).unsqueeze(0)
+        ks = k[a:a + L].transpose(0, 1).unsqueeze(0)
+        vs = v[a:a + L].transpose(0, 1).unsqueeze(0)
+        rows = sample_rows(1, w.Hq, L, n_random=16, edge=8,
+                           heads=[(0, 0), (0, w.Hq - 1)], seed=s)
+        o_ref, l_ref = oracle.attn_dense(qs, ks, vs, is_causal=True, rows=rows)
+        ok = oc[a:a + L].transpose(0, 1).reshape(-1, w.D)[rows]
+        lk = lc[:, a:a + L].reshape(-1)[rows]
+        check(ok, lk, o_ref, l_ref, f"varlen seq {s} (L={L})")
