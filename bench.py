@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Attention-forward throughput on GB300: one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one exact attention forward (softmax(scale*QK^T)V plus nothing
+else) over the self-attention workload B=1, H=16, N=4096, D=512, bf16
+inputs ~ N(0,1), non-causal (FFPA README "Quick Start" layout [B,H,N,D];
+D=512 is the head dimension the pages benchmark).  TFLOPS follow the
+pages' convention 4*B*Hq*Nq*Nkv*D (halved when causal).
+
+* value / ms_per_step: device time of exactly K back-to-back steps, CUDA
+  events on the launching stream, bracketed by barrier + synchronize; the
+  inputs (256 MiB) are larger than the 129 MB L2.
+* e2e: the same metric through the public API with pinned host buffers:
+  every step copies Q, K, V host->device and O device->host.
+* roofline: the kernel against the dense bf16 tensor peak
+  (MEASURED_PEAKS.json when present, else a recorded fallback).
+* cpu_baseline: the float64 oracle on a bounded, seeded sample of rows of
+  the same workload, on the host cores (rank 0, N = 1 only).
+* --impl reference: the oracle alone, timed per step on bounded samples.
+
+Multi-GPU (torchrun): independent replicas, one per rank (the path has no
+exchange step); value = all ranks' flops / max over ranks of the time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOPS (bf16, D=512) and % of GB300 dense BF16 peak; oracle CPU s"
+FALLBACK_BF16_TFLOPS = 1900.0      # profiling recipe fallback (one earlier GB300 measurement)
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1000 * 1000
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="selfattn_b1_h16_n4096_d512")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+def workload_by_name(name):
+    from exact_headdim_attention_gb300 import workloads as wl
+    for w in wl.all_workloads():
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def config_of(w, flops):
+    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv,
+           "D": w.D, "causal": w.causal, "mask": "additive f32" if w.additive_mask else None,
+           "varlen": w.varlen, "flops_per_step": flops,
+           "l2": "inputs larger than L2 (no flush between steps)"}
+    return cfg
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            bf16 = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
+            if bf16:
+                return float(bf16), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback (profiling recipe: 1.9 PFLOP/s bf16 burst)"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not win and self.samples:     # very short timed region: nearest sample
+            mid = 0.5 * (t0 + t1)
+            win = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        reasons = sorted({name for p in win for name, val in zip(self.NAMES, p[5:9])
+                          if val.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device_index)
+
+
+# --------------------------------------------------------------- our arm
+def make_step(w, x, dev):
+    """Returns (device_step, e2e_step, bytes_h2d, bytes_d2h, flops)."""
+    import torch
+    import exact_headdim_attention_gb300 as pkg
+    from exact_headdim_attention_gb300 import workloads as wl
+
+    names = ("q", "k", "v")
+    host = {n: x[n].pin_memory() for n in names}
+    devt = {n: host[n].to(dev, non_blocking=False) for n in names}
+    if w.varlen:
+        cq = x["cu_q"].to(dev)
+        out = torch.empty_like(devt["q"])
+        lse = torch.empty(w.Hq, x["q"].shape[0], dtype=torch.float32, device=dev)
+        flops = wl.useful_flops(w, x["seqlens"])
+
+        def call():
+            pkg.ffpa_fwd_varlen(devt["q"], devt["k"], devt["v"], cq, None, x["max_q"], x["max_k"],
+                                causal=w.causal, enable_gqa=w.enable_gqa, return_lse=True,
+                                out=out, lse=lse)
+    else:
+        mask = None if x.get("mask") is None else x["mask"].to(dev)
+        out = torch.empty_like(devt["q"])
+        flops = wl.useful_flops(w)
+
+        def call():
+            pkg.ffpa_fwd(devt["q"], devt["k"], devt["v"], attn_mask=mask, is_causal=w.causal,
+                         enable_gqa=w.enable_gqa, out=out)
+    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e():
+        for n in names:
+            devt[n].copy_(host[n], non_blocking=True)
+        call()
+        o_host.copy_(out, non_blocking=True)
+
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o_host.numel() * o_host.element_size()
+    return call, e2e, h2d, d2h, flops
+
+
+def time_steps(fn, steps, dist_on):
+    import torch
+    import torch.distributed as dist
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    if dist_on:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    if dist_on:
+        dist.barrier()
+    return s.elapsed_time(e) / 1e3, t0, t1
+
+
+def aggregate(elapsed_s: float, flops_per_step: float, steps: int, world: int, dist_on: bool,
+              device=None):
+    """Whole-job throughput: all ranks' flops / max over ranks of the time."""
+    import torch
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    if dist_on:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tmax = float(t.item())
+    total = flops_per_step * steps * world
+    return total / tmax / 1e12, tmax
+
+
+def cpu_baseline(w, x, target_s: float):
+    """The float64 oracle on a bounded seeded sample of rows of the workload."""
+    import torch
+    import oracle
+    cores = oracle.host_threads()
+    orc = oracle.default()
+    if w.varlen:
+        raise SystemExit("cpu baseline for varlen workloads: use the dense workloads")
+    per_row = 4.0 * w.Nkv * w.D / (2.0 if w.causal else 1.0)
+    total_rows = w.B * w.Hq * w.Nq
+    g = torch.Generator().manual_seed(w.seed + 17)
+    n = cores
+    rows = torch.randint(0, total_rows, (n,), generator=g)
+    t0 = time.perf_counter()
+    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=rows,
+                   nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(total_rows, max(cores, n * target_s / dt)))
+    n = max(cores, (n // cores) * cores)
+    rows = torch.randint(0, total_rows, (n,), generator=g)
+    t0 = time.perf_counter()
+    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=rows,
+                   nthreads=cores)
+    dt = time.perf_counter() - t0
+    flops = per_row * n
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{n} seeded random query rows of {total_rows} (all {w.Nkv} keys each), "
+                      f"{dt:.1f} s; full workload would take ~{dt * total_rows / n:.0f} s",
+            "seconds": dt, "rows": n}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import exact_headdim_attention_gb300 as pkg
+    from exact_headdim_attention_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    if dist_on:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.load_library()
+    w = workload_by_name(args.workload)
+    x = wl.materialize(w)
+    step, e2e, h2d, d2h, flops = make_step(w, x, dev)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = pkg.ffpa_last_device_error()
+    if st != pkg.FFPA_OK:
+        raise SystemExit(f"device error during warm-up: {pkg.ffpa_status_string(st)}")
+    sampler = ClockSampler(gpu_id_for(local))
+    sampler.start()
+    elapsed, t0, t1 = time_steps(step, args.steps, dist_on)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    value, tmax = aggregate(elapsed, flops, args.steps, world, dist_on, dev)
+    # end to end through the public API with host buffers
+    for _ in range(3):
+        e2e()
+    n_e2e = max(3, min(args.e2e_steps, args.steps))
+    e_el, _, _ = time_steps(e2e, n_e2e, dist_on)
+    e_value, _ = aggregate(e_el, flops, n_e2e, world, dist_on, dev)
+    st = pkg.ffpa_last_device_error()
+    if st != pkg.FFPA_OK:
+        raise SystemExit(f"device error: {pkg.ffpa_status_string(st)}")
+    peak, peak_src = read_peaks()
+    per_launch_s = elapsed / args.steps
+    achieved = flops / per_launch_s / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shapes of the pages' workloads)",
+        "config": config_of(w, flops),
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": peak_src, "kernel": "ffpa_fwd_kernel<false>",
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                "api": "exact_headdim_attention_gb300.ffpa_fwd (C ABI ffpa_fwd)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not w.varlen:
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+        line["oracle_cpu_s_full_workload_est"] = round(
+            line["cpu_baseline"]["seconds"] * (w.B * w.Hq * w.Nq) / line["cpu_baseline"]["rows"], 1)
+    traffic = measured_traffic(w.name)
+    if traffic is not None:
+        line["roofline"]["traffic"] = traffic
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        dist.destroy_process_group()
+
+
+def measured_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(name)
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from exact_headdim_attention_gb300 import workloads as wl
+    w = workload_by_name(args.workload)
+    x = wl.materialize(w)
+    flops_full = wl.useful_flops(w)
+    cores = oracle.host_threads()
+    orc = oracle.default()
+    per_row = 4.0 * w.Nkv * w.D / (2.0 if w.causal else 1.0)
+    total_rows = w.B * w.Hq * w.Nq
+    g = torch.Generator().manual_seed(w.seed + 29)
+    # size each step so that warm-up + steps take about 90 s
+    probe = torch.randint(0, total_rows, (cores,), generator=g)
+    t0 = time.perf_counter()
+    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=probe,
+                   nthreads=cores)
+    t_probe = max(time.perf_counter() - t0, 1e-6)
+    per_step = 90.0 / (args.steps + args.warmup)
+    n = max(cores, int(cores * per_step / t_probe) // cores * cores)
+    for _ in range(args.warmup):
+        orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal,
+                       rows=torch.randint(0, total_rows, (n,), generator=g), nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal,
+                       rows=torch.randint(0, total_rows, (n,), generator=g), nthreads=cores)
+    dt = time.perf_counter() - t0
+    value = per_row * n * args.steps / dt / 1e12
+    sample = (f"each step: {n} seeded random query rows of {total_rows} (all keys), "
+              f"float64 oracle on {cores} host threads")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 inputs widened to float64)",
+        "config": config_of(w, flops_full), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

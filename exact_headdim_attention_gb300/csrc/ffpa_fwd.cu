@@ -44,23 +44,28 @@ constexpr int BM = 128;              // query rows per tile = TMEM lanes
 constexpr int BN = 128;              // keys per S tile
 constexpr int DK = 64;               // D chunk: one 128-byte swizzle row of 16-bit values
 constexpr int DV_MAX = 256;          // output columns per CTA
-constexpr int NSLOT = 6;             // ring slots
-constexpr uint32_t SLOT_BYTES = 32768;
+constexpr int NSLOT_MAX = 6;         // ring slots (fewer when Q is resident)
+constexpr uint32_t SLOT_BYTES = 32768;         // one TMA box of 2 D-chunks (32 KB)
 constexpr uint32_t CHUNK_BYTES = BM * DK * 2;  // 16 KB: one 128x64 tile
+constexpr int Q_RESIDENT_MAX_CHUNKS = 8;       // Q stays in smem for D <= 512
+constexpr size_t SMEM_LIMIT = 232448;          // opt-in dynamic smem per block (sm_103)
+constexpr size_t SMEM_STATIC_RESERVE = 1024;
 constexpr int NTHREADS = 192;
 constexpr int PRODUCER_WARP = 4;
 constexpr int MMA_WARP = 5;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t S_COL0 = 256;     // S buffer b occupies columns [256 + 128 b, +128)
 constexpr float RESCALE_LOG2 = 8.0f; // rescale O only when the max grows by > 2^8
-constexpr size_t SMEM_BYTES = NSLOT * SLOT_BYTES + 1024;
 
 __device__ int g_err_word;
 
 struct Params {
-  CUtensorMap tm_q;    // dense: dims (D, Nq, Hq, B); varlen: (D, Hq, Tq); box 64 x 128 rows
-  CUtensorMap tm_k;    // same over keys
-  CUtensorMap tm_v;    // box 64 x vk rows
+  // Views with D split as (64, D/64): dense (64, N, D/64, H, B); varlen
+  // (64, T, D/64, H).  Q and K boxes: 64 x 128 rows x min(2, D/64) chunks;
+  // V box: 64 x vk rows x vchunks chunks.
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
   void* o;
   float* lse;
   const void* mask;
@@ -71,7 +76,8 @@ struct Params {
   int mask_kind;
   int B;               // batches (dense) or sequences (varlen)
   int Hq, group, Nq, Nkv, D, Tq;
-  int n_qt, n_slices, nchunks, vk;
+  int n_qt, n_slices, nchunks, vk, vchunks, kchunks;
+  int q_res, nslot;    // Q resident in smem (1) or streamed through the ring (0); ring depth
   float scale_log2;
   int causal, fp16, inject;
   unsigned long long timeout_ns;
@@ -81,7 +87,18 @@ struct Item {
   int b, hq, hkv, slice;
   int q0, q_len, kv_len, q_row0, kv_row0;
   int col_lo, dv, ntiles;
+  int rot;   // first key tile visited; tiles are visited rot, rot+1, ... (mod ntiles)
 };
+
+constexpr int PREFETCH_TILES = 2;   // L2 prefetch distance of K/V tiles
+
+// Key tile visited at step j.  Work items of one head start at different
+// tiles so that they do not all miss in L2 on the same tile at the same time;
+// the online softmax gives the same result for any visiting order.
+__device__ __forceinline__ int kv_tile(const Item& it, int j) {
+  const int t = j + it.rot;
+  return t >= it.ntiles ? t - it.ntiles : t;
+}
 
 __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L, Item& it) {
   it.slice = L % p.n_slices;
@@ -120,6 +137,9 @@ __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L,
     kv_end = min(kv_end, last_visible + 1);
   }
   it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+  it.rot = it.ntiles > 0 ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
+                                 (unsigned)it.ntiles)
+                         : 0;
   const int c_lo = it.slice * p.nchunks / p.n_slices;
   const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
   it.col_lo = c_lo * DK;
@@ -191,19 +211,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   if (!decode_item(p, VARLEN, blockIdx.x, it)) return;   // uniform across the CTA
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bar_full[NSLOT], bar_empty[NSLOT];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2], bar_drain;
+  const int qpairs = (p.nchunks + 1) >> 1;
+  const uint32_t q_region = p.q_res ? qpairs * SLOT_BYTES : 0u;
+  const uint32_t qreg_u32 = smem_u32(smem);
+  const uint32_t ring_u32 = qreg_u32 + q_region;
+  const int NS = p.nslot;
+  __shared__ __align__(8) uint64_t bar_full[NSLOT_MAX], bar_empty[NSLOT_MAX];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2], bar_drain, bar_q;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t ring_u32 = smem_u32(ring);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSLOT; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bar_full[i]), 1);
       mbar_init(smem_u32(&bar_empty[i]), 1);
     }
@@ -213,6 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       mbar_init(smem_u32(&bar_pv_done[b]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_q), 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -237,75 +262,104 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       uint32_t lap = 0;
       int issued = 0;
       bool ok = true;
-      // Test hook: the very first stage of the CTA is acquired but never
+      // Test hook: the very first ring stage of the CTA is acquired but never
       // armed or copied, so the MMA warp's wait on it runs out.
       bool drop = p.inject != 0;
-      const uint32_t v_bytes = (uint32_t)p.vk * it.dv * 2;
-      // Returns 0 on abort, 1 when the slot is armed for `bytes`, 2 when dropped.
-      auto acquire = [&](uint32_t bytes) -> int {
-        if (!wait_bounded(smem_u32(&bar_empty[slot]), lap ^ 1u, &abort_flag, tmo)) return 0;
+      const uint32_t k_bytes = (uint32_t)p.kchunks * CHUNK_BYTES;
+      const uint32_t v_bytes = (uint32_t)p.vk * p.vchunks * 128u;
+      // Returns the smem address of an armed slot, 0 when dropped, ~0u on abort.
+      auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
+        const uint32_t eb = smem_u32(&bar_empty[slot]);
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
+          return ~0u;
+        fb = smem_u32(&bar_full[slot]);
+        const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
+        ++issued;
+        if (++slot == NS) { slot = 0; lap ^= 1u; }
         if (drop) {
           drop = false;
-          return 2;
+          return 0u;
         }
-        mbar_arrive_expect_tx(smem_u32(&bar_full[slot]), bytes);
-        return 1;
+        mbar_arrive_expect_tx(fb, bytes);
+        return dst;
       };
-      auto advance = [&]() {
-        ++issued;
-        if (++slot == NSLOT) { slot = 0; lap ^= 1u; }
+      auto load_q_pair = [&](uint32_t dst, uint32_t fb, int pr) {
+        if (VARLEN)
+          tma_load_4d(dst, &p.tm_q, fb, 0, it.q_row0 + it.q0, 2 * pr, it.hq);
+        else
+          tma_load_5d(dst, &p.tm_q, fb, 0, it.q0, 2 * pr, it.hq, it.b);
       };
+      if (p.q_res) {
+        const uint32_t qb = smem_u32(&bar_q);
+        mbar_arrive_expect_tx(qb, qpairs * k_bytes);
+        for (int pr = 0; pr < qpairs; ++pr) load_q_pair(qreg_u32 + pr * SLOT_BYTES, qb, pr);
+      }
       auto issue_qk = [&](int j) -> bool {
-        for (int c = 0; c < p.nchunks; ++c) {
-          const int a = acquire(2 * CHUNK_BYTES);
-          if (a == 0) return false;
-          if (a == 1) {
-            const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
-            const uint32_t fb = smem_u32(&bar_full[slot]);
-            if (VARLEN) {
-              tma_load_3d(dst, &p.tm_q, fb, c * DK, it.hq, it.q_row0 + it.q0);
-              tma_load_3d(dst + CHUNK_BYTES, &p.tm_k, fb, c * DK, it.hkv, it.kv_row0 + j * BN);
-            } else {
-              tma_load_4d(dst, &p.tm_q, fb, c * DK, it.q0, it.hq, it.b);
-              tma_load_4d(dst + CHUNK_BYTES, &p.tm_k, fb, c * DK, j * BN, it.hkv, it.b);
-            }
+        for (int pr = 0; pr < qpairs; ++pr) {
+          uint32_t fb = 0, dst;
+          if (!p.q_res) {
+            dst = acquire(k_bytes, fb);
+            if (dst == ~0u) return false;
+            if (dst) load_q_pair(dst, fb, pr);
           }
-          advance();
+          dst = acquire(k_bytes, fb);
+          if (dst == ~0u) return false;
+          if (dst) {
+            const int key0 = kv_tile(it, j) * BN;
+            if (VARLEN)
+              tma_load_4d(dst, &p.tm_k, fb, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
+            else
+              tma_load_5d(dst, &p.tm_k, fb, 0, key0, 2 * pr, it.hkv, it.b);
+          }
         }
         return true;
       };
       auto issue_v = [&](int j) -> bool {
         for (int h = 0; h < BN / p.vk; ++h) {
-          const int a = acquire(v_bytes);
-          if (a == 0) return false;
-          if (a == 1) {
-            const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
-            const uint32_t fb = smem_u32(&bar_full[slot]);
-            const int key = j * BN + h * p.vk;
-            for (int t = 0; t < it.dv / DK; ++t) {
-              const int col = it.col_lo + t * DK;
-              if (VARLEN)
-                tma_load_3d(dst + t * p.vk * 128, &p.tm_v, fb, col, it.hkv, it.kv_row0 + key);
-              else
-                tma_load_4d(dst + t * p.vk * 128, &p.tm_v, fb, col, key, it.hkv, it.b);
-            }
+          uint32_t fb = 0;
+          const uint32_t dst = acquire(v_bytes, fb);
+          if (dst == ~0u) return false;
+          if (dst) {
+            const int key = kv_tile(it, j) * BN + h * p.vk;
+            if (VARLEN)
+              tma_load_4d(dst, &p.tm_v, fb, 0, it.kv_row0 + key, it.col_lo / DK, it.hkv);
+            else
+              tma_load_5d(dst, &p.tm_v, fb, 0, key, it.col_lo / DK, it.hkv, it.b);
           }
-          advance();
         }
         return true;
       };
+      // L2 prefetch of the K and V boxes of key tile step j.
+      auto prefetch = [&](int j) {
+        const int key0 = kv_tile(it, j) * BN;
+        for (int pr = 0; pr < qpairs; ++pr) {
+          if (VARLEN)
+            tma_prefetch_4d(&p.tm_k, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
+          else
+            tma_prefetch_5d(&p.tm_k, 0, key0, 2 * pr, it.hkv, it.b);
+        }
+        for (int h = 0; h < BN / p.vk; ++h) {
+          if (VARLEN)
+            tma_prefetch_4d(&p.tm_v, 0, it.kv_row0 + key0 + h * p.vk, it.col_lo / DK, it.hkv);
+          else
+            tma_prefetch_5d(&p.tm_v, 0, key0 + h * p.vk, it.col_lo / DK, it.hkv, it.b);
+        }
+      };
+      for (int j = 0; j < PREFETCH_TILES && j < T; ++j) prefetch(j);
       for (int j = 0; j < T && ok; ++j) {
+        if (j + PREFETCH_TILES < T) prefetch(j + PREFETCH_TILES);
         ok = issue_qk(j);
         if (ok && j >= 1) ok = issue_v(j - 1);
       }
-      if (ok && T > 0) ok = issue_v(T - 1);
+      if (ok) ok = issue_v(T - 1);
       // Drain: every copy this thread started has landed before the CTA exits
       // (the dropped test stage, the first one, was never armed).
-      const int n = issued < NSLOT ? issued : NSLOT;
+      if (p.q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
+      const int n = issued < NS ? issued : NS;
       int s = slot;
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
-        if (--s < 0) { s = NSLOT - 1; lp ^= 1u; }
+        if (--s < 0) { s = NS - 1; lp ^= 1u; }
         if (p.inject != 0 && issued - 1 - i == 0) continue;
         wait_drain(smem_u32(&bar_full[s]), lp, tmo);
       }
@@ -315,55 +369,74 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_f16(!p.fp16, BM, BN, false, false);
       const uint32_t idesc_pv = idesc_f16(!p.fp16, BM, it.dv, false, true);
+      // Descriptors advance by (byte offset >> 4) in their start-address field.
+      const uint64_t ring_desc = sdesc_sw128(ring_u32, 16, 1024);
+      const uint64_t q_desc = sdesc_sw128(qreg_u32, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(ring_u32, p.vk * 128, 1024);
       int slot = 0;
       uint32_t lap = 0;
       bool ok = true;
-      auto take = [&]() -> bool {
-        if (!wait_bounded(smem_u32(&bar_full[slot]), lap, &abort_flag, tmo)) return false;
+      auto take = [&]() -> int {
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        const int s = slot;
+        if (++slot == NS) { slot = 0; lap ^= 1u; }
         tc_fence_after();
-        return true;
+        return s;
       };
-      auto release = [&]() {
-        umma_commit(smem_u32(&bar_empty[slot]));
-        if (++slot == NSLOT) { slot = 0; lap ^= 1u; }
-      };
+      auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
       auto do_pv = [&](int j) -> bool {
         const int b = j & 1;
-        if (!wait_bounded(smem_u32(&bar_p_full[b]), (j >> 1) & 1, &abort_flag, tmo)) return false;
+        const uint32_t pb = smem_u32(&bar_p_full[b]);
+        if (!mbar_try_wait(pb, (j >> 1) & 1) && !wait_bounded(pb, (j >> 1) & 1, &abort_flag, tmo))
+          return false;
         tc_fence_after();
         const uint32_t p_col = tmem + S_COL0 + 128 * b;
         for (int h = 0; h < BN / p.vk; ++h) {
-          if (!take()) return false;
-          const uint32_t base = ring_u32 + slot * SLOT_BYTES;
-          for (int kk = 0; kk < p.vk / 16; ++kk) {
-            const uint64_t bdesc = sdesc_sw128(base + kk * 2048, p.vk * 128, 1024);
-            umma_ts(tmem, p_col + (h * p.vk + 16 * kk) / 2, bdesc, idesc_pv,
+          const int s = take();
+          if (s < 0) return false;
+          const uint64_t vd = v_desc + ((s * SLOT_BYTES) >> 4);
+          for (int kk = 0; kk < p.vk / 16; ++kk)
+            umma_ts(tmem, p_col + ((h * p.vk + 16 * kk) >> 1), vd + ((kk * 2048) >> 4), idesc_pv,
                     (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
-          }
-          release();
+          release(s);
         }
         umma_commit(smem_u32(&bar_pv_done[b]));
         return true;
       };
+      if (T > 0 && p.q_res) {
+        const uint32_t qb = smem_u32(&bar_q);
+        ok = mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo);
+      }
       for (int j = 0; j < T && ok; ++j) {
         const int b = j & 1;
         if (j >= 2) {   // S buffer b holds P_{j-2} until PV_{j-2} completes
-          ok = wait_bounded(smem_u32(&bar_pv_done[b]), ((j - 2) >> 1) & 1, &abort_flag, tmo);
+          const uint32_t db = smem_u32(&bar_pv_done[b]);
+          const uint32_t par = ((j - 2) >> 1) & 1;
+          ok = mbar_try_wait(db, par) || wait_bounded(db, par, &abort_flag, tmo);
           if (!ok) break;
           tc_fence_after();
         }
         const uint32_t s_col = tmem + S_COL0 + 128 * b;
-        for (int c = 0; c < p.nchunks && ok; ++c) {
-          ok = take();
-          if (!ok) break;
-          const uint32_t base = ring_u32 + slot * SLOT_BYTES;
-#pragma unroll
-          for (int k = 0; k < DK / 16; ++k) {
-            const uint64_t adesc = sdesc_sw128(base + k * 32, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(base + CHUNK_BYTES + k * 32, 16, 1024);
-            umma_ss(s_col, adesc, bdesc, idesc_qk, (c > 0 || k > 0) ? 1u : 0u);
+        for (int pr = 0; pr < qpairs && ok; ++pr) {
+          int sq = -1;
+          if (!p.q_res) {
+            sq = take();
+            if (sq < 0) { ok = false; break; }
           }
-          release();
+          const int sk = take();
+          if (sk < 0) { ok = false; break; }
+          const int nvalid = min(2, p.nchunks - 2 * pr);
+          for (int cc = 0; cc < nvalid; ++cc) {
+            const uint64_t ad = p.q_res ? q_desc + (((2 * pr + cc) * CHUNK_BYTES) >> 4)
+                                        : ring_desc + ((sq * SLOT_BYTES + cc * CHUNK_BYTES) >> 4);
+            const uint64_t bd = ring_desc + ((sk * SLOT_BYTES + cc * CHUNK_BYTES) >> 4);
+#pragma unroll
+            for (int k = 0; k < DK / 16; ++k)
+              umma_ss(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, (pr > 0 || cc > 0 || k > 0) ? 1u : 0u);
+          }
+          if (sq >= 0) release(sq);
+          release(sk);
         }
         if (!ok) break;
         umma_commit(smem_u32(&bar_s_full[b]));
@@ -400,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_addr = lane_base + S_COL0 + 128 * b;
-      const int kbase = j * BN;
+      const int kbase = kv_tile(it, j) * BN;
       const bool need_mask = (kbase + BN > it.kv_len) ||
                              (p.causal && (long long)kbase + BN - 1 > first_limit) ||
                              p.mask_kind != FFPA_MASK_NONE;
@@ -571,33 +644,29 @@ bool strides_ok(const int64_t* str, const int64_t* size, int rank) {
   return true;
 }
 
-// Tensor map over (D, dims[1], dims[2], ...) with byte strides; size-1
-// dimensions get a harmless stride so their (unused) value never fails the
-// encoder's alignment checks.
+// Tiled tensor map with 128-byte swizzle.  dims[0] is always 64 (one
+// 128-byte row of 16-bit values); byte strides are given for dims 1..rank-1.
+// A size-1 dimension gets a harmless stride so its (never used) value cannot
+// fail the encoder's alignment checks.
 ffpa_status encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
-                       const uint64_t* dims, const int64_t* elem_strides, uint32_t box_rows,
-                       int row_dim) {
+                       const uint64_t* dims, const uint64_t* stride_bytes, const uint32_t* box) {
   auto enc = encode_fn();
   if (!enc) return FFPA_ERR_CUDA;
   cuuint64_t gdim[5];
   cuuint64_t gstr[4];
-  cuuint32_t box[5];
+  cuuint32_t bx[5];
   cuuint32_t es[5];
-  uint64_t prev_bytes = dims[0] * 2;   // bytes spanned by the dimensions inside this one
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
-    box[i] = 1;
+    bx[i] = box[i];
     es[i] = 1;
   }
-  box[0] = DK;
-  box[row_dim] = box_rows;
   for (int i = 1; i < rank; ++i) {
-    uint64_t s = static_cast<uint64_t>(elem_strides[i]) * 2;
-    if (dims[i] <= 1) s = (prev_bytes + 15) & ~uint64_t(15);
-    gstr[i - 1] = s;
-    prev_bytes = s * dims[i];
+    uint64_t st = stride_bytes[i - 1];
+    if (dims[i] <= 1 && (st == 0 || st % 16 != 0)) st = 128;
+    gstr[i - 1] = st;
   }
-  CUresult r = enc(m, dt, rank, const_cast<void*>(base), gdim, gstr, box, es,
+  CUresult r = enc(m, dt, rank, const_cast<void*>(base), gdim, gstr, bx, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FFPA_OK : FFPA_ERR_INVALID;
@@ -625,21 +694,32 @@ ffpa_status check_device(const void* ptr, int* dev_out) {
   return FFPA_OK;
 }
 
-void plan_slices(int D, Params* P) {
+// Splits D into at most 256-column output slices, sizes the V stage, and
+// decides whether Q stays resident in shared memory (D <= 512) and how many
+// 32 KB ring slots fit beside it.  Returns the dynamic shared memory bytes.
+size_t plan(int D, Params* P) {
   P->nchunks = D / DK;
   P->n_slices = (D + DV_MAX - 1) / DV_MAX;
-  // widest slice: ceil(nchunks / n_slices) chunks
   const int max_dv = ((P->nchunks + P->n_slices - 1) / P->n_slices) * DK;
+  P->vchunks = max_dv / DK;
   P->vk = max_dv > 128 ? 64 : 128;
+  P->kchunks = P->nchunks < 2 ? P->nchunks : 2;
+  P->q_res = P->nchunks <= Q_RESIDENT_MAX_CHUNKS;
+  const size_t q_region = P->q_res ? ((P->nchunks + 1) / 2) * (size_t)SLOT_BYTES : 0;
+  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024;
+  size_t ns = (budget - q_region) / SLOT_BYTES;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  P->nslot = static_cast<int>(ns);
+  return 1024 + q_region + ns * SLOT_BYTES;
 }
 
 template <bool VARLEN>
-ffpa_status launch(const Params& P, int items, cudaStream_t stream) {
+ffpa_status launch(const Params& P, int items, size_t smem, cudaStream_t stream) {
   auto kern = ffpa_fwd_kernel<VARLEN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+                           static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;
-  kern<<<items, NTHREADS, SMEM_BYTES, stream>>>(P);
+  kern<<<items, NTHREADS, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
@@ -711,18 +791,22 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  plan_slices(D, &P);
+  const size_t smem = plan(D, &P);
+  const uint64_t nch = (uint64_t)P.nchunks;
   {
-    const uint64_t dq[4] = {(uint64_t)D, (uint64_t)Nq, (uint64_t)Hq, (uint64_t)B};
-    const int64_t sq[4] = {1, q_str[2], q_str[1], q_str[0]};
-    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq, sq, BM, 1)) != FFPA_OK) return st;
+    const uint64_t dq[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t sq[4] = {(uint64_t)q_str[2] * 2, 128, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
+    const uint32_t bq[5] = {64, BM, (uint32_t)P.kchunks, 1, 1};
+    if ((st = encode_map(&P.tm_q, tdt, 5, q, dq, sq, bq)) != FFPA_OK) return st;
   }
   if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
-    const uint64_t dk[4] = {(uint64_t)D, (uint64_t)Nkv, (uint64_t)Hkv, (uint64_t)B};
-    const int64_t sk[4] = {1, k_str[2], k_str[1], k_str[0]};
-    if ((st = encode_map(&P.tm_k, tdt, 4, k, dk, sk, BN, 1)) != FFPA_OK) return st;
-    const int64_t sv[4] = {1, v_str[2], v_str[1], v_str[0]};
-    if ((st = encode_map(&P.tm_v, tdt, 4, v, dk, sv, P.vk, 1)) != FFPA_OK) return st;
+    const uint64_t dk[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
+    const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
+    const uint32_t bk[5] = {64, BN, (uint32_t)P.kchunks, 1, 1};
+    if ((st = encode_map(&P.tm_k, tdt, 5, k, dk, sk, bk)) != FFPA_OK) return st;
+    const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
+    const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
+    if ((st = encode_map(&P.tm_v, tdt, 5, v, dk, sv, bv)) != FFPA_OK) return st;
   }
   P.o = o;
   P.lse = lse;
@@ -747,7 +831,7 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   P.timeout_ns = g_timeout_ns.load();
   const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
-  return launch<false>(P, static_cast<int>(items), reinterpret_cast<cudaStream_t>(stream));
+  return launch<false>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -781,18 +865,22 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  plan_slices(D, &P);
+  const size_t smem = plan(D, &P);
+  const uint64_t nch = (uint64_t)P.nchunks;
   {
-    const uint64_t dq[3] = {(uint64_t)D, (uint64_t)Hq, (uint64_t)Tq};
-    const int64_t sq[3] = {1, q_str[1], q_str[0]};
-    if ((st = encode_map(&P.tm_q, tdt, 3, q, dq, sq, BM, 2)) != FFPA_OK) return st;
+    const uint64_t dq[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
+    const uint64_t sq[3] = {(uint64_t)q_str[0] * 2, 128, (uint64_t)q_str[1] * 2};
+    const uint32_t bq[4] = {64, BM, (uint32_t)P.kchunks, 1};
+    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq, sq, bq)) != FFPA_OK) return st;
   }
   if (Tk > 0) {
-    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)Tk};
-    const int64_t sk[3] = {1, k_str[1], k_str[0]};
-    if ((st = encode_map(&P.tm_k, tdt, 3, k, dk, sk, BN, 2)) != FFPA_OK) return st;
-    const int64_t sv[3] = {1, v_str[1], v_str[0]};
-    if ((st = encode_map(&P.tm_v, tdt, 3, v, dk, sv, P.vk, 2)) != FFPA_OK) return st;
+    const uint64_t dk[4] = {64, (uint64_t)Tk, nch, (uint64_t)Hkv};
+    const uint64_t sk[3] = {(uint64_t)k_str[0] * 2, 128, (uint64_t)k_str[1] * 2};
+    const uint32_t bk[4] = {64, BN, (uint32_t)P.kchunks, 1};
+    if ((st = encode_map(&P.tm_k, tdt, 4, k, dk, sk, bk)) != FFPA_OK) return st;
+    const uint64_t sv[3] = {(uint64_t)v_str[0] * 2, 128, (uint64_t)v_str[1] * 2};
+    const uint32_t bv[4] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1};
+    if ((st = encode_map(&P.tm_v, tdt, 4, v, dk, sv, bv)) != FFPA_OK) return st;
   }
   P.o = o;
   P.lse = lse;
@@ -819,7 +907,7 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   (void)max_seqlen_k;
   const long long items = (long long)nseq * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
-  return launch<true>(P, static_cast<int>(items), reinterpret_cast<cudaStream_t>(stream));
+  return launch<true>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

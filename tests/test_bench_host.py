@@ -1,0 +1,64 @@
+"""Host logic of bench.py: multi-rank aggregation over gloo (world size 2,
+CPU) and the clock-record summary.  No GPU is used."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    # rank r took (r + 1) seconds for 10 steps of 1e12 flops each
+    value, tmax = bench.aggregate(float(rank + 1), 1e12, 10, world, True, torch.device("cpu"))
+    out[rank] = (value, tmax)
+    dist.destroy_process_group()
+
+
+def test_aggregate_takes_max_time_over_ranks():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    for r in range(world):
+        value, tmax = res[r]
+        assert tmax == 2.0
+        assert value == pytest.approx(1e12 * 10 * world / 2.0 / 1e12)
+
+
+def test_aggregate_single_rank():
+    value, tmax = bench.aggregate(0.5, 2e12, 4, 1, False)
+    assert tmax == 0.5 and value == pytest.approx(16.0)
+
+
+def test_clock_summary_reasons_and_window():
+    cs = bench.ClockSampler("0")
+    row = lambda sm, thr: ["0", str(sm), "2070", "900.0", "0x0", "Not Active",
+                           "Not Active", thr, "Active"]
+    cs.samples = [(0.0, row(1000, "Not Active")), (1.0, row(1900, "Not Active")),
+                  (1.1, row(1950, "Not Active")), (5.0, row(500, "Active"))]
+    s = cs.summary(0.95, 1.2)
+    assert s["samples"] == 2 and s["sm_mhz"] == 1925 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    s = cs.summary(4.9, 5.1)
+    assert "sw_thermal_slowdown" in s["reasons"]
+
+
+def test_peaks_fallback_or_measured():
+    peak, src = bench.read_peaks()
+    assert peak > 100 and ("fallback" in src or "measured" in src)
