@@ -90,8 +90,6 @@ struct Item {
   int rot;   // first key tile visited; tiles are visited rot, rot+1, ... (mod ntiles)
 };
 
-constexpr int PREFETCH_TILES = 2;   // L2 prefetch distance of K/V tiles
-
 // Key tile visited at step j.  Work items of one head start at different
 // tiles so that they do not all miss in L2 on the same tile at the same time;
 // the online softmax gives the same result for any visiting order.
@@ -151,11 +149,12 @@ __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L,
 // told to abort or when the limit expires (then the error word is set).
 __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 127u) == 0) {
+  for (uint32_t it = 0;; ++it) {
+    // Suspended waiting keeps idle warps from taking issue slots away from
+    // the MMA and TMA threads that share their SM sub-partition.
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
@@ -210,11 +209,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   Item it;
   if (!decode_item(p, VARLEN, blockIdx.x, it)) return;   // uniform across the CTA
 
+  // Scalars copied out of the parameter block once: the hot loops below run
+  // between asm statements with memory clobbers, which would otherwise force
+  // the parameter loads to be repeated.
+  const int nchunks = p.nchunks, q_res = p.q_res, vk = p.vk, vchunks = p.vchunks;
+  const int kchunks = p.kchunks, mask_kind = p.mask_kind, inject = p.inject;
+  const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
+  const float scale_log2 = p.scale_log2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int qpairs = (p.nchunks + 1) >> 1;
-  const uint32_t q_region = p.q_res ? qpairs * SLOT_BYTES : 0u;
+  const int qpairs = (nchunks + 1) >> 1;
+  const uint32_t q_region = q_res ? qpairs * SLOT_BYTES : 0u;
   const uint32_t qreg_u32 = smem_u32(smem);
   const uint32_t ring_u32 = qreg_u32 + q_region;
   const int NS = p.nslot;
@@ -264,9 +270,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       bool ok = true;
       // Test hook: the very first ring stage of the CTA is acquired but never
       // armed or copied, so the MMA warp's wait on it runs out.
-      bool drop = p.inject != 0;
-      const uint32_t k_bytes = (uint32_t)p.kchunks * CHUNK_BYTES;
-      const uint32_t v_bytes = (uint32_t)p.vk * p.vchunks * 128u;
+      bool drop = inject != 0;
+      const uint32_t k_bytes = (uint32_t)kchunks * CHUNK_BYTES;
+      const uint32_t v_bytes = (uint32_t)vk * vchunks * 128u;
       // Returns the smem address of an armed slot, 0 when dropped, ~0u on abort.
       auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         else
           tma_load_5d(dst, &p.tm_q, fb, 0, it.q0, 2 * pr, it.hq, it.b);
       };
-      if (p.q_res) {
+      if (q_res) {
         const uint32_t qb = smem_u32(&bar_q);
         mbar_arrive_expect_tx(qb, qpairs * k_bytes);
         for (int pr = 0; pr < qpairs; ++pr) load_q_pair(qreg_u32 + pr * SLOT_BYTES, qb, pr);
@@ -297,7 +303,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       auto issue_qk = [&](int j) -> bool {
         for (int pr = 0; pr < qpairs; ++pr) {
           uint32_t fb = 0, dst;
-          if (!p.q_res) {
+          if (!q_res) {
             dst = acquire(k_bytes, fb);
             if (dst == ~0u) return false;
             if (dst) load_q_pair(dst, fb, pr);
@@ -315,12 +321,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         return true;
       };
       auto issue_v = [&](int j) -> bool {
-        for (int h = 0; h < BN / p.vk; ++h) {
+        for (int h = 0; h < BN / vk; ++h) {
           uint32_t fb = 0;
           const uint32_t dst = acquire(v_bytes, fb);
           if (dst == ~0u) return false;
           if (dst) {
-            const int key = kv_tile(it, j) * BN + h * p.vk;
+            const int key = kv_tile(it, j) * BN + h * vk;
             if (VARLEN)
               tma_load_4d(dst, &p.tm_v, fb, 0, it.kv_row0 + key, it.col_lo / DK, it.hkv);
             else
@@ -329,59 +335,51 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         }
         return true;
       };
-      // L2 prefetch of the K and V boxes of key tile step j.
-      auto prefetch = [&](int j) {
-        const int key0 = kv_tile(it, j) * BN;
-        for (int pr = 0; pr < qpairs; ++pr) {
-          if (VARLEN)
-            tma_prefetch_4d(&p.tm_k, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
-          else
-            tma_prefetch_5d(&p.tm_k, 0, key0, 2 * pr, it.hkv, it.b);
-        }
-        for (int h = 0; h < BN / p.vk; ++h) {
-          if (VARLEN)
-            tma_prefetch_4d(&p.tm_v, 0, it.kv_row0 + key0 + h * p.vk, it.col_lo / DK, it.hkv);
-          else
-            tma_prefetch_5d(&p.tm_v, 0, key0 + h * p.vk, it.col_lo / DK, it.hkv, it.b);
-        }
-      };
-      for (int j = 0; j < PREFETCH_TILES && j < T; ++j) prefetch(j);
       for (int j = 0; j < T && ok; ++j) {
-        if (j + PREFETCH_TILES < T) prefetch(j + PREFETCH_TILES);
         ok = issue_qk(j);
         if (ok && j >= 1) ok = issue_v(j - 1);
       }
       if (ok) ok = issue_v(T - 1);
       // Drain: every copy this thread started has landed before the CTA exits
       // (the dropped test stage, the first one, was never armed).
-      if (p.q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
+      if (q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
       const int n = issued < NS ? issued : NS;
       int s = slot;
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = NS - 1; lp ^= 1u; }
-        if (p.inject != 0 && issued - 1 - i == 0) continue;
+        if (inject != 0 && issued - 1 - i == 0) continue;
         wait_drain(smem_u32(&bar_full[s]), lp, tmo);
       }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16(!p.fp16, BM, BN, false, false);
-      const uint32_t idesc_pv = idesc_f16(!p.fp16, BM, it.dv, false, true);
+      const uint32_t idesc_qk = idesc_f16(!fp16, BM, BN, false, false);
+      const uint32_t idesc_pv = idesc_f16(!fp16, BM, it.dv, false, true);
       // Descriptors advance by (byte offset >> 4) in their start-address field.
       const uint64_t ring_desc = sdesc_sw128(ring_u32, 16, 1024);
       const uint64_t q_desc = sdesc_sw128(qreg_u32, 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(ring_u32, p.vk * 128, 1024);
+      const uint64_t v_desc = sdesc_sw128(ring_u32, vk * 128, 1024);
       int slot = 0;
       uint32_t lap = 0;
       bool ok = true;
+      // `ready`: the full barrier of the next stage (at the cursor) has already
+      // been seen complete.  peek() probes it without blocking; it is called
+      // between the MMAs of the current stage so that the barrier round trip
+      // overlaps queued tensor work instead of draining it.
+      bool ready = false;
+      auto peek = [&]() {
+        if (!ready) ready = mbar_try_wait(smem_u32(&bar_full[slot]), lap);
+      };
       auto take = [&]() -> int {
-        const uint32_t fb = smem_u32(&bar_full[slot]);
-        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        if (!ready) {
+          const uint32_t fb = smem_u32(&bar_full[slot]);
+          if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        }
+        ready = false;
         const int s = slot;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
-        tc_fence_after();
         return s;
       };
       auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
@@ -392,19 +390,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
           return false;
         tc_fence_after();
         const uint32_t p_col = tmem + S_COL0 + 128 * b;
-        for (int h = 0; h < BN / p.vk; ++h) {
+        for (int h = 0; h < BN / vk; ++h) {
           const int s = take();
           if (s < 0) return false;
           const uint64_t vd = v_desc + ((s * SLOT_BYTES) >> 4);
-          for (int kk = 0; kk < p.vk / 16; ++kk)
-            umma_ts(tmem, p_col + ((h * p.vk + 16 * kk) >> 1), vd + ((kk * 2048) >> 4), idesc_pv,
-                    (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pc = p_col + ((h * vk) >> 1);
+          // 16 keys per MMA: +8 TMEM columns of P, +2048 bytes (>>4 = 128) of V.
+          umma_ts(tmem, pc, vd, idesc_pv, (j > 0 || h > 0) ? 1u : 0u);
+          umma_ts(tmem, pc + 8, vd + 128, idesc_pv, 1u);
+          peek();
+#pragma unroll
+          for (int kk = 2; kk < 4; ++kk) umma_ts(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, 1u);
+          if (vk == 128) {
+#pragma unroll
+            for (int kk = 4; kk < 8; ++kk) umma_ts(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, 1u);
+          }
           release(s);
         }
         umma_commit(smem_u32(&bar_pv_done[b]));
         return true;
       };
-      if (T > 0 && p.q_res) {
+      if (T > 0 && q_res) {
         const uint32_t qb = smem_u32(&bar_q);
         ok = mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo);
       }
@@ -420,20 +426,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         const uint32_t s_col = tmem + S_COL0 + 128 * b;
         for (int pr = 0; pr < qpairs && ok; ++pr) {
           int sq = -1;
-          if (!p.q_res) {
+          if (!q_res) {
             sq = take();
             if (sq < 0) { ok = false; break; }
           }
           const int sk = take();
           if (sk < 0) { ok = false; break; }
-          const int nvalid = min(2, p.nchunks - 2 * pr);
-          for (int cc = 0; cc < nvalid; ++cc) {
-            const uint64_t ad = p.q_res ? q_desc + (((2 * pr + cc) * CHUNK_BYTES) >> 4)
-                                        : ring_desc + ((sq * SLOT_BYTES + cc * CHUNK_BYTES) >> 4);
-            const uint64_t bd = ring_desc + ((sk * SLOT_BYTES + cc * CHUNK_BYTES) >> 4);
+          const uint64_t ad = q_res ? q_desc + (((2 * pr) * CHUNK_BYTES) >> 4)
+                                    : ring_desc + ((sq * SLOT_BYTES) >> 4);
+          const uint64_t bd = ring_desc + ((sk * SLOT_BYTES) >> 4);
+          // 16 D-elements per MMA: +32 bytes (>>4 = 2) within a 128-byte row;
+          // the second chunk of the pair sits 16 KB (>>4 = 1024) further.
+          umma_ss(s_col, ad, bd, idesc_qk, pr > 0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < DK / 16; ++k)
-              umma_ss(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, (pr > 0 || cc > 0 || k > 0) ? 1u : 0u);
+          for (int k = 1; k < 4; ++k) umma_ss(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, 1u);
+          peek();
+          if (2 * pr + 1 < nchunks) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_ss(s_col, ad + 1024 + 2 * k, bd + 1024 + 2 * k, idesc_qk, 1u);
           }
           if (sq >= 0) release(sq);
           release(sk);
@@ -456,13 +467,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
     const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
     const uint8_t* mrow = nullptr;
-    if (p.mask_kind != FFPA_MASK_NONE && row_valid) {
-      const size_t esz = p.mask_kind == FFPA_MASK_BOOL ? 1 : p.mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
+    if (mask_kind != FFPA_MASK_NONE && row_valid) {
+      const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
       const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
                             (long long)row * p.m_str[2];
       mrow = static_cast<const uint8_t*>(p.mask) + off * (long long)esz;
     }
     const long long mk = p.m_str[3];
+    // Scores stay unscaled (x = q.k) when possible, so that the exponent
+    // x*scale*log2(e) - m is one FFMA; additive masks (or a scale <= 0, which
+    // reverses the max) need x pre-scaled into the log2 domain.
+    const bool prescale = mask_kind == FFPA_MASK_ADD_F32 || mask_kind == FFPA_MASK_ADD_QTYPE ||
+                          !(scale_log2 > 0.f);
+    const float xs = prescale ? 1.f : scale_log2;
+    const float ld_scale = prescale ? scale_log2 : 1.f;
     float m_ref = -INFINITY;
     float l_sum = 0.f;
     bool ok = true;
@@ -475,24 +493,47 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       const uint32_t s_addr = lane_base + S_COL0 + 128 * b;
       const int kbase = kv_tile(it, j) * BN;
       const bool need_mask = (kbase + BN > it.kv_len) ||
-                             (p.causal && (long long)kbase + BN - 1 > first_limit) ||
-                             p.mask_kind != FFPA_MASK_NONE;
+                             (causal && (long long)kbase + BN - 1 > first_limit) ||
+                             mask_kind != FFPA_MASK_NONE;
       float x[BN];
-#pragma unroll
-      for (int q4 = 0; q4 < BN / 32; ++q4) {
-        uint32_t raw[32];
-        tmem_ld32(s_addr + 32 * q4, raw);
+      {
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(s_addr, r0);
+        tmem_ld32(s_addr + 32, r1);
+        tmem_ld32(s_addr + 64, r2);
+        tmem_ld32(s_addr + 96, r3);
         tmem_wait_ld();
-        reg_fence(raw);
-        float* xg = x + 32 * q4;
+        reg_fence(r0);
+        reg_fence(r1);
+        reg_fence(r2);
+        reg_fence(r3);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) xg[c] = __uint_as_float(raw[c]) * p.scale_log2;
-        if (need_mask) apply_mask32(xg, kbase + 32 * q4, it.kv_len, p.causal != 0, row_limit, mrow,
-                                    mk, p.mask_kind, p.fp16 != 0);
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0[c]) * ld_scale;
+          x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
+          x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
+          x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
+        }
       }
-      float mx = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, x[c]);
+        for (int q4 = 0; q4 < BN / 32; ++q4)
+          apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
+                       mask_kind, fp16);
+      }
+      float mx;
+      {   // tree maximum: eight independent chains, then combine
+        float m8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+        for (int c = 8; c < BN; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[c + i]);
+        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        mx *= xs;   // into the log2 domain (-inf stays -inf: xs > 0)
+      }
       bool resc = false;
       float alpha = 1.f;
       if (mx > m_ref + RESCALE_LOG2) {
@@ -527,11 +568,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
           const int cc = 32 * g + c;
-          const float e0 = ex2_approx(x[cc] - base), e1 = ex2_approx(x[cc + 1] - base);
-          const float e2 = ex2_approx(x[cc + 2] - base), e3 = ex2_approx(x[cc + 3] - base);
+          const float e0 = ex2_approx(fmaf(x[cc], xs, -base));
+          const float e1 = ex2_approx(fmaf(x[cc + 1], xs, -base));
+          const float e2 = ex2_approx(fmaf(x[cc + 2], xs, -base));
+          const float e3 = ex2_approx(fmaf(x[cc + 3], xs, -base));
           s0 += e0; s1 += e1; s2 += e2; s3 += e3;
-          pk[c / 2] = p.fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-          pk[c / 2 + 1] = p.fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+          pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+          pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
         }
         tmem_st16(s_addr + 16 * g, pk);
       }
@@ -575,7 +618,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         for (int c = 0; c < 16; ++c) {
           const float a0 = __uint_as_float(o[2 * c]) * inv_l;
           const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
-          pkd[c] = p.fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+          pkd[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
         }
         if (row_valid) {
           uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
