@@ -345,15 +345,28 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_headdim_attention_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, if it matches."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
+    or None when that capture was taken on a different kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return d.get(name)
     except (OSError, ValueError):
         return None
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d.get("dram_bytes_per_launch", {}).get(name)
 
 
 # ---------------------------------------------------------- reference arm
