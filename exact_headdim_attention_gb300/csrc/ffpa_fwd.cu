@@ -7,14 +7,14 @@
 // with D ("Split-D").  On Blackwell the accumulators live in Tensor Memory
 // (TMEM, 128 lanes x 512 fp32 columns per SM) instead of registers, so the
 // pages' register-pressure problem becomes a TMEM-capacity problem: a CTA
-// owns at most 256 output columns ("output-D slice") next to two 128-column
-// S buffers.  When D > 256 the output columns are split across CTAs and
-// each CTA recomputes S for its slice.
+// owns at most 256 output columns ("output-D slice") next to one 128-column
+// S buffer and two 64-column P buffers.  When D > 256 the output columns are
+// split across CTAs and each CTA recomputes S for its slice.
 //
 // Per CTA (one work item = batch b, query head h, 128-row query tile,
 // output-D slice) the warps specialise:
 //   warps 0-3  softmax: row r = 32*warp + lane; read S from TMEM, mask,
-//              online max / exp2 / sum, write P (16-bit) back over S, rescale
+//              online max / exp2 / sum, write P (16-bit) to a P buffer, rescale
 //              O when the running max moved by more than 2^8, epilogue.
 //   warp 4     TMA producer: Q/K D-chunk pairs and V stages into a ring of
 //              32 KB shared-memory slots (128-byte swizzle), in the exact
@@ -44,17 +44,21 @@ constexpr int BM = 128;              // query rows per tile = TMEM lanes
 constexpr int BN = 128;              // keys per S tile
 constexpr int DK = 64;               // D chunk: one 128-byte swizzle row of 16-bit values
 constexpr int DV_MAX = 256;          // output columns per CTA
-constexpr int NSLOT_MAX = 6;         // ring slots (fewer when Q is resident)
+constexpr int NSLOT_MAX = 6;         // K-ring slots (fewer when Q is resident)
+constexpr int NSLOT_V_MAX = 2;       // V-ring slots
 constexpr uint32_t SLOT_BYTES = 32768;         // one TMA box of 2 D-chunks (32 KB)
 constexpr uint32_t CHUNK_BYTES = BM * DK * 2;  // 16 KB: one 128x64 tile
 constexpr int Q_RESIDENT_MAX_CHUNKS = 8;       // Q stays in smem for D <= 512
 constexpr size_t SMEM_LIMIT = 232448;          // opt-in dynamic smem per block (sm_103)
 constexpr size_t SMEM_STATIC_RESERVE = 1024;
-constexpr int NTHREADS = 192;
-constexpr int PRODUCER_WARP = 4;
-constexpr int MMA_WARP = 5;
+constexpr int NTHREADS = 256;
+constexpr int PRODUCER_WARP = 4;     // TMA for Q and the K ring
+constexpr int MMA_WARP = 5;          // issues S = Q K^T; owns the TMEM allocation
+constexpr int PV_WARP = 6;           // issues O += P V
+constexpr int V_PRODUCER_WARP = 7;   // TMA for the V ring
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t S_COL0 = 256;     // S buffer b occupies columns [256 + 128 b, +128)
+constexpr uint32_t S_COL = 256;      // S (fp32, 128 keys) occupies columns [256, 384)
+constexpr uint32_t P_COL0 = 384;     // P buffer b (16-bit pairs, 128 keys) at [384 + 64 b, +64)
 constexpr float RESCALE_LOG2 = 8.0f; // rescale O only when the max grows by > 2^8
 
 __device__ int g_err_word;
@@ -77,7 +81,8 @@ struct Params {
   int B;               // batches (dense) or sequences (varlen)
   int Hq, group, Nq, Nkv, D, Tq;
   int n_qt, n_slices, nchunks, vk, vchunks, kchunks;
-  int q_res, nslot;    // Q resident in smem (1) or streamed through the ring (0); ring depth
+  int q_res, nslot;    // Q resident in smem (1) or streamed through the K ring (0); K-ring depth
+  int nslot_v, vslot;  // V-ring depth and slot bytes (vk keys x vchunks 64-column chunks)
   float scale_log2;
   int causal, fp16, inject;
   unsigned long long timeout_ns;
@@ -224,8 +229,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   const uint32_t qreg_u32 = smem_u32(smem);
   const uint32_t ring_u32 = qreg_u32 + q_region;
   const int NS = p.nslot;
+  const int NSV = p.nslot_v;
+  const uint32_t vslot = (uint32_t)p.vslot;
+  const uint32_t vring_u32 = ring_u32 + NS * SLOT_BYTES;
   __shared__ __align__(8) uint64_t bar_full[NSLOT_MAX], bar_empty[NSLOT_MAX];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[2], bar_pv_done[2], bar_drain, bar_q;
+  __shared__ __align__(8) uint64_t bar_vfull[NSLOT_V_MAX], bar_vempty[NSLOT_V_MAX];
+  __shared__ __align__(8) uint64_t bar_s_full, bar_s_free, bar_p_full[2], bar_pv_done[2], bar_q;
+  __shared__ __align__(8) uint64_t bar_drain[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
 
@@ -237,12 +247,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       mbar_init(smem_u32(&bar_full[i]), 1);
       mbar_init(smem_u32(&bar_empty[i]), 1);
     }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(smem_u32(&bar_vfull[i]), 1);
+      mbar_init(smem_u32(&bar_vempty[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_s_free), 4);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&bar_s_full[b]), 1);
       mbar_init(smem_u32(&bar_p_full[b]), 4);
       mbar_init(smem_u32(&bar_pv_done[b]), 1);
     }
-    mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_drain[0]), 1);
+    mbar_init(smem_u32(&bar_drain[1]), 1);
     mbar_init(smem_u32(&bar_q), 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -258,30 +274,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   const int T = it.ntiles;
   const unsigned long long tmo = p.timeout_ns;
 
-  if (warp == PRODUCER_WARP) {
-    // ------------------------------------------------------------ producer
+  if (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) {
+    // ------------------------------------------------------------ producers
+    // Two single-thread producers, each filling its own ring in the order
+    // its MMA warp consumes it: warp 4 the K ring (Q pairs when Q is not
+    // resident, then K pairs, per key tile), warp 7 the V ring (V stages per
+    // key tile).  Separate rings keep every mbarrier phase observed by its
+    // only consumer, which parity-based waits require.
     if (lane == 0 && T > 0) {
-      prefetch_tmap(&p.tm_q);
-      prefetch_tmap(&p.tm_k);
-      prefetch_tmap(&p.tm_v);
+      const bool k_role = warp == PRODUCER_WARP;
+      const int nslots = k_role ? NS : NSV;
+      const uint32_t base = k_role ? ring_u32 : vring_u32;
+      const uint32_t stride = k_role ? SLOT_BYTES : vslot;
+      uint64_t* full = k_role ? bar_full : bar_vfull;
+      uint64_t* empty = k_role ? bar_empty : bar_vempty;
+      if (k_role) {
+        prefetch_tmap(&p.tm_q);
+        prefetch_tmap(&p.tm_k);
+      } else {
+        prefetch_tmap(&p.tm_v);
+      }
       int slot = 0;
       uint32_t lap = 0;
       int issued = 0;
       bool ok = true;
-      // Test hook: the very first ring stage of the CTA is acquired but never
-      // armed or copied, so the MMA warp's wait on it runs out.
-      bool drop = inject != 0;
+      // Test hook: the very first K-ring stage of the CTA is acquired but
+      // never armed or copied, so the MMA warp's wait on it runs out.
+      bool drop = k_role && inject != 0;
       const uint32_t k_bytes = (uint32_t)kchunks * CHUNK_BYTES;
-      const uint32_t v_bytes = (uint32_t)vk * vchunks * 128u;
       // Returns the smem address of an armed slot, 0 when dropped, ~0u on abort.
       auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
-        const uint32_t eb = smem_u32(&bar_empty[slot]);
+        const uint32_t eb = smem_u32(&empty[slot]);
         if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
           return ~0u;
-        fb = smem_u32(&bar_full[slot]);
-        const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
+        fb = smem_u32(&full[slot]);
+        const uint32_t dst = base + slot * stride;
         ++issued;
-        if (++slot == NS) { slot = 0; lap ^= 1u; }
+        if (++slot == nslots) { slot = 0; lap ^= 1u; }
         if (drop) {
           drop = false;
           return 0u;
@@ -295,37 +324,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         else
           tma_load_5d(dst, &p.tm_q, fb, 0, it.q0, 2 * pr, it.hq, it.b);
       };
-      if (q_res) {
-        const uint32_t qb = smem_u32(&bar_q);
-        mbar_arrive_expect_tx(qb, qpairs * k_bytes);
-        for (int pr = 0; pr < qpairs; ++pr) load_q_pair(qreg_u32 + pr * SLOT_BYTES, qb, pr);
-      }
-      auto issue_qk = [&](int j) -> bool {
-        for (int pr = 0; pr < qpairs; ++pr) {
-          uint32_t fb = 0, dst;
-          if (!q_res) {
+      if (k_role) {
+        if (q_res) {
+          const uint32_t qb = smem_u32(&bar_q);
+          mbar_arrive_expect_tx(qb, qpairs * k_bytes);
+          for (int pr = 0; pr < qpairs; ++pr) load_q_pair(qreg_u32 + pr * SLOT_BYTES, qb, pr);
+        }
+        for (int j = 0; j < T && ok; ++j) {
+          const int key0 = kv_tile(it, j) * BN;
+          for (int pr = 0; pr < qpairs && ok; ++pr) {
+            uint32_t fb = 0, dst;
+            if (!q_res) {
+              dst = acquire(k_bytes, fb);
+              if (dst == ~0u) { ok = false; break; }
+              if (dst) load_q_pair(dst, fb, pr);
+            }
             dst = acquire(k_bytes, fb);
-            if (dst == ~0u) return false;
-            if (dst) load_q_pair(dst, fb, pr);
-          }
-          dst = acquire(k_bytes, fb);
-          if (dst == ~0u) return false;
-          if (dst) {
-            const int key0 = kv_tile(it, j) * BN;
-            if (VARLEN)
-              tma_load_4d(dst, &p.tm_k, fb, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
-            else
-              tma_load_5d(dst, &p.tm_k, fb, 0, key0, 2 * pr, it.hkv, it.b);
+            if (dst == ~0u) { ok = false; break; }
+            if (dst) {
+              if (VARLEN)
+                tma_load_4d(dst, &p.tm_k, fb, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
+              else
+                tma_load_5d(dst, &p.tm_k, fb, 0, key0, 2 * pr, it.hkv, it.b);
+            }
           }
         }
-        return true;
-      };
-      auto issue_v = [&](int j) -> bool {
-        for (int h = 0; h < BN / vk; ++h) {
-          uint32_t fb = 0;
-          const uint32_t dst = acquire(v_bytes, fb);
-          if (dst == ~0u) return false;
-          if (dst) {
+        if (q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
+      } else {
+        for (int j = 0; j < T && ok; ++j) {
+          for (int h = 0; h < BN / vk && ok; ++h) {
+            uint32_t fb = 0;
+            const uint32_t dst = acquire(vslot, fb);
+            if (dst == ~0u) { ok = false; break; }
             const int key = kv_tile(it, j) * BN + h * vk;
             if (VARLEN)
               tma_load_4d(dst, &p.tm_v, fb, 0, it.kv_row0 + key, it.col_lo / DK, it.hkv);
@@ -333,130 +363,117 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
               tma_load_5d(dst, &p.tm_v, fb, 0, key, it.col_lo / DK, it.hkv, it.b);
           }
         }
-        return true;
-      };
-      for (int j = 0; j < T && ok; ++j) {
-        ok = issue_qk(j);
-        if (ok && j >= 1) ok = issue_v(j - 1);
       }
-      if (ok) ok = issue_v(T - 1);
       // Drain: every copy this thread started has landed before the CTA exits
-      // (the dropped test stage, the first one, was never armed).
-      if (q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
-      const int n = issued < NS ? issued : NS;
+      // (the dropped test stage, the first K stage, was never armed).
+      const int n = issued < nslots ? issued : nslots;
       int s = slot;
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
-        if (--s < 0) { s = NS - 1; lp ^= 1u; }
-        if (inject != 0 && issued - 1 - i == 0) continue;
-        wait_drain(smem_u32(&bar_full[s]), lp, tmo);
+        if (--s < 0) { s = nslots - 1; lp ^= 1u; }
+        if (k_role && inject != 0 && issued - 1 - i == 0) continue;
+        wait_drain(smem_u32(&full[s]), lp, tmo);
       }
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == MMA_WARP || warp == PV_WARP) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two warps issue tensor-core work, one thread each: warp 5 the QK^T MMAs
+    // (into S), warp 6 the PV MMAs (into O).  Every mbarrier test costs an
+    // issuing thread ~100 cycles, longer than the one MMA the tensor queue
+    // holds; with two issuers the waits of one are covered by the MMAs of the
+    // other.  Each consumes its own ring (K ring / V ring) in order.
     if (lane == 0) {
-      const uint32_t idesc_qk = idesc_f16(!fp16, BM, BN, false, false);
-      const uint32_t idesc_pv = idesc_f16(!fp16, BM, it.dv, false, true);
-      // Descriptors advance by (byte offset >> 4) in their start-address field.
-      const uint64_t ring_desc = sdesc_sw128(ring_u32, 16, 1024);
-      const uint64_t q_desc = sdesc_sw128(qreg_u32, 16, 1024);
-      const uint64_t v_desc = sdesc_sw128(ring_u32, vk * 128, 1024);
+      const bool qk_role = warp == MMA_WARP;
+      const int nV = BN / vk;                       // V stages per key tile
+      const int nslots = qk_role ? NS : NSV;
+      uint64_t* full = qk_role ? bar_full : bar_vfull;
+      uint64_t* empty = qk_role ? bar_empty : bar_vempty;
       int slot = 0;
       uint32_t lap = 0;
       bool ok = true;
-      // `ready`: the full barrier of the next stage (at the cursor) has already
-      // been seen complete.  peek() probes it without blocking; it is called
-      // between the MMAs of the current stage so that the barrier round trip
-      // overlaps queued tensor work instead of draining it.
-      bool ready = false;
-      auto peek = [&]() {
-        if (!ready) ready = mbar_try_wait(smem_u32(&bar_full[slot]), lap);
-      };
       auto take = [&]() -> int {
-        if (!ready) {
-          const uint32_t fb = smem_u32(&bar_full[slot]);
-          if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
-        }
-        ready = false;
+        const uint32_t fb = smem_u32(&full[slot]);
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
         const int s = slot;
-        if (++slot == NS) { slot = 0; lap ^= 1u; }
+        if (++slot == nslots) { slot = 0; lap ^= 1u; }
         return s;
       };
-      auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
-      auto do_pv = [&](int j) -> bool {
-        const int b = j & 1;
-        const uint32_t pb = smem_u32(&bar_p_full[b]);
-        if (!mbar_try_wait(pb, (j >> 1) & 1) && !wait_bounded(pb, (j >> 1) & 1, &abort_flag, tmo))
-          return false;
+      auto release = [&](int s) { umma_commit(smem_u32(&empty[s])); };
+      auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
         tc_fence_after();
-        const uint32_t p_col = tmem + S_COL0 + 128 * b;
-        for (int h = 0; h < BN / vk; ++h) {
-          const int s = take();
-          if (s < 0) return false;
-          const uint64_t vd = v_desc + ((s * SLOT_BYTES) >> 4);
-          const uint32_t pc = p_col + ((h * vk) >> 1);
-          // 16 keys per MMA: +8 TMEM columns of P, +2048 bytes (>>4 = 128) of V.
-          umma_ts(tmem, pc, vd, idesc_pv, (j > 0 || h > 0) ? 1u : 0u);
-          umma_ts(tmem, pc + 8, vd + 128, idesc_pv, 1u);
-          peek();
-#pragma unroll
-          for (int kk = 2; kk < 4; ++kk) umma_ts(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, 1u);
-          if (vk == 128) {
-#pragma unroll
-            for (int kk = 4; kk < 8; ++kk) umma_ts(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, 1u);
-          }
-          release(s);
-        }
-        umma_commit(smem_u32(&bar_pv_done[b]));
         return true;
       };
-      if (T > 0 && q_res) {
-        const uint32_t qb = smem_u32(&bar_q);
-        ok = mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo);
-      }
-      for (int j = 0; j < T && ok; ++j) {
-        const int b = j & 1;
-        if (j >= 2) {   // S buffer b holds P_{j-2} until PV_{j-2} completes
-          const uint32_t db = smem_u32(&bar_pv_done[b]);
-          const uint32_t par = ((j - 2) >> 1) & 1;
-          ok = mbar_try_wait(db, par) || wait_bounded(db, par, &abort_flag, tmo);
+      if (qk_role) {
+        const uint32_t idesc_qk = idesc_f16(!fp16, BM, BN, false, false);
+        // Descriptors advance by (byte offset >> 4) in their start-address field.
+        const uint64_t ring_desc = sdesc_sw128(ring_u32, 16, 1024);
+        const uint64_t q_desc = sdesc_sw128(qreg_u32, 16, 1024);
+        const uint32_t s_col = tmem + S_COL;
+        if (T > 0 && q_res) ok = wait_on(smem_u32(&bar_q), 0);
+        for (int j = 0; j < T && ok; ++j) {
+          // S is free once the softmax warps have read S_{j-1}.
+          if (j >= 1 && !(ok = wait_on(smem_u32(&bar_s_free), (j - 1) & 1))) break;
+          for (int pr = 0; pr < qpairs && ok; ++pr) {
+            int sq = -1;
+            if (!q_res) {
+              sq = take();
+              if (sq < 0) { ok = false; break; }
+            }
+            const int sk = take();
+            if (sk < 0) { ok = false; break; }
+            const uint64_t ad = q_res ? q_desc + (((2 * pr) * CHUNK_BYTES) >> 4)
+                                      : ring_desc + ((sq * SLOT_BYTES) >> 4);
+            const uint64_t bd = ring_desc + ((sk * SLOT_BYTES) >> 4);
+            // 16 D-elements per MMA: +32 bytes (>>4 = 2) within a 128-byte row;
+            // the second chunk of the pair sits 16 KB (>>4 = 1024) further.
+            umma_ss(s_col, ad, bd, idesc_qk, pr > 0 ? 1u : 0u);
+#pragma unroll
+            for (int k = 1; k < 4; ++k) umma_ss(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, 1u);
+            if (2 * pr + 1 < nchunks) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_ss(s_col, ad + 1024 + 2 * k, bd + 1024 + 2 * k, idesc_qk, 1u);
+            }
+            if (sq >= 0) release(sq);
+            release(sk);
+          }
           if (!ok) break;
-          tc_fence_after();
+          umma_commit(smem_u32(&bar_s_full));
         }
-        const uint32_t s_col = tmem + S_COL0 + 128 * b;
-        for (int pr = 0; pr < qpairs && ok; ++pr) {
-          int sq = -1;
-          if (!q_res) {
-            sq = take();
-            if (sq < 0) { ok = false; break; }
-          }
-          const int sk = take();
-          if (sk < 0) { ok = false; break; }
-          const uint64_t ad = q_res ? q_desc + (((2 * pr) * CHUNK_BYTES) >> 4)
-                                    : ring_desc + ((sq * SLOT_BYTES) >> 4);
-          const uint64_t bd = ring_desc + ((sk * SLOT_BYTES) >> 4);
-          // 16 D-elements per MMA: +32 bytes (>>4 = 2) within a 128-byte row;
-          // the second chunk of the pair sits 16 KB (>>4 = 1024) further.
-          umma_ss(s_col, ad, bd, idesc_qk, pr > 0 ? 1u : 0u);
+      } else {
+        const uint32_t idesc_pv = idesc_f16(!fp16, BM, it.dv, false, true);
+        const uint64_t v_desc = sdesc_sw128(vring_u32, vk * 128, 1024);
+        for (int j = 0; j < T && ok; ++j) {
+          const int b = j & 1;
+          if (!(ok = wait_on(smem_u32(&bar_p_full[b]), (j >> 1) & 1))) break;
+          const uint32_t p_col = tmem + P_COL0 + 64 * b;
+          for (int h = 0; h < nV; ++h) {
+            const int s = take();
+            if (s < 0) { ok = false; break; }
+            const uint64_t vd = v_desc + ((s * vslot) >> 4);
+            const uint32_t pc = p_col + ((h * vk) >> 1);
+            // 16 keys per MMA: +8 TMEM columns of P, +2048 bytes (>>4 = 128) of V.
+            umma_ts(tmem, pc, vd, idesc_pv, (j > 0 || h > 0) ? 1u : 0u);
+            umma_ts(tmem, pc + 8, vd + 128, idesc_pv, 1u);
+            if (vk >= 64) {
+              umma_ts(tmem, pc + 16, vd + 256, idesc_pv, 1u);
+              umma_ts(tmem, pc + 24, vd + 384, idesc_pv, 1u);
+            }
+            if (vk == 128) {
 #pragma unroll
-          for (int k = 1; k < 4; ++k) umma_ss(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, 1u);
-          peek();
-          if (2 * pr + 1 < nchunks) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              umma_ss(s_col, ad + 1024 + 2 * k, bd + 1024 + 2 * k, idesc_qk, 1u);
+              for (int kk = 4; kk < 8; ++kk) umma_ts(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, 1u);
+            }
+            release(s);
           }
-          if (sq >= 0) release(sq);
-          release(sk);
+          if (!ok) break;
+          umma_commit(smem_u32(&bar_pv_done[b]));
         }
-        if (!ok) break;
-        umma_commit(smem_u32(&bar_s_full[b]));
-        if (j >= 1) ok = do_pv(j - 1);
       }
-      if (ok && T > 0) ok = do_pv(T - 1);
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      umma_commit(smem_u32(&bar_drain));
-      wait_drain(smem_u32(&bar_drain), 0, tmo);
+      const uint32_t db = smem_u32(&bar_drain[qk_role ? 0 : 1]);
+      umma_commit(db);
+      wait_drain(db, 0, tmo);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -486,11 +503,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       const int b = j & 1;
-      bool w = wait_bounded(smem_u32(&bar_s_full[b]), (j >> 1) & 1, &abort_flag, tmo);
+      bool w = wait_bounded(smem_u32(&bar_s_full), j & 1, &abort_flag, tmo);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_addr = lane_base + S_COL0 + 128 * b;
+      const uint32_t s_addr = lane_base + S_COL;
+      const uint32_t p_addr = lane_base + P_COL0 + 64 * b;
       const int kbase = kv_tile(it, j) * BN;
       const bool need_mask = (kbase + BN > it.kv_len) ||
                              (causal && (long long)kbase + BN - 1 > first_limit) ||
@@ -507,6 +525,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         reg_fence(r1);
         reg_fence(r2);
         reg_fence(r3);
+        // S has been read into registers: the next QK may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           x[c] = __uint_as_float(r0[c]) * ld_scale;
@@ -559,7 +581,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
           tmem_st32(lane_base + c0, o);
         }
       }
-      // P = exp2(x - m_ref) in 16-bit, written over the S columns already read.
+      if (j >= 2) {   // P buffer b was read by PV_{j-2}
+        w = wait_bounded(smem_u32(&bar_pv_done[b]), ((j - 2) >> 1) & 1, &abort_flag, tmo);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // P = exp2(x - m_ref) in 16-bit, into P buffer b.
       const float base = m_ref == -INFINITY ? 0.f : m_ref;
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
@@ -576,7 +604,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
           pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
           pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
         }
-        tmem_st16(s_addr + 16 * g, pk);
+        tmem_st16(p_addr + 16 * g, pk);
       }
       l_sum = l_sum * alpha + ((s0 + s1) + (s2 + s3));
       tmem_wait_st();
@@ -745,15 +773,23 @@ size_t plan(int D, Params* P) {
   P->n_slices = (D + DV_MAX - 1) / DV_MAX;
   const int max_dv = ((P->nchunks + P->n_slices - 1) / P->n_slices) * DK;
   P->vchunks = max_dv / DK;
-  P->vk = max_dv > 128 ? 64 : 128;
   P->kchunks = P->nchunks < 2 ? P->nchunks : 2;
   P->q_res = P->nchunks <= Q_RESIDENT_MAX_CHUNKS;
   const size_t q_region = P->q_res ? ((P->nchunks + 1) / 2) * (size_t)SLOT_BYTES : 0;
-  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024;
-  size_t ns = (budget - q_region) / SLOT_BYTES;
+  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region;
+  // V stages: up to 32 KB (vk keys x vchunks chunks of 128-byte rows), two
+  // slots; halve vk while that leaves fewer than two K-ring slots.
+  int vk = 128;
+  while (vk > 16 && (size_t)vk * P->vchunks * 128 > SLOT_BYTES) vk >>= 1;
+  P->nslot_v = NSLOT_V_MAX;
+  while (vk > 32 && budget < 2 * (size_t)SLOT_BYTES + (size_t)NSLOT_V_MAX * vk * P->vchunks * 128)
+    vk >>= 1;
+  P->vk = vk;
+  P->vslot = vk * P->vchunks * 128;
+  size_t ns = (budget - (size_t)P->nslot_v * P->vslot) / SLOT_BYTES;
   if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
   P->nslot = static_cast<int>(ns);
-  return 1024 + q_region + ns * SLOT_BYTES;
+  return 1024 + q_region + ns * SLOT_BYTES + (size_t)P->nslot_v * P->vslot;
 }
 
 template <bool VARLEN>
