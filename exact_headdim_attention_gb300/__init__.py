@@ -27,5 +27,6 @@ from ._binding import (  # noqa: F401
     lib_path,
     load_library,
     set_wait_timeout_ns,
+    set_kernel_variant,
     inject_dropped_copy,
 )

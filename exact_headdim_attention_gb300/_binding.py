@@ -23,7 +23,9 @@ FFPA_BF16, FFPA_FP16 = 0, 1
 FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
 
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
-            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy")
+            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant")
+
+KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2}
 
 _lib = None
 
@@ -81,6 +83,8 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_set_wait_timeout_ns.restype = None
     lib.ffpa_test_drop_first_copy.argtypes = [I]
     lib.ffpa_test_drop_first_copy.restype = None
+    lib.ffpa_set_kernel_variant.argtypes = [I]
+    lib.ffpa_set_kernel_variant.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -267,6 +271,13 @@ def ffpa_last_device_error(stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     load_library().ffpa_set_wait_timeout_ns(int(ns))
+
+
+def set_kernel_variant(name: str) -> None:
+    """Choose the kernel for later launches: "auto", "single" or "pair" (see ffpa.h)."""
+    if name not in KERNEL_VARIANTS:
+        raise ValueError(f"kernel variant must be one of {sorted(KERNEL_VARIANTS)}, got {name!r}")
+    load_library().ffpa_set_kernel_variant(KERNEL_VARIANTS[name])
 
 
 def inject_dropped_copy(enable: bool) -> None:

@@ -83,6 +83,7 @@ struct Params {
   int n_qt, n_slices, nchunks, vk, vchunks, kchunks;
   int q_res, nslot;    // Q resident in smem (1) or streamed through the K ring (0); K-ring depth
   int nslot_v, vslot;  // V-ring depth and slot bytes (vk keys x vchunks 64-column chunks)
+  int kslot, kc;       // pair kernel: K-ring slot bytes and D-chunks per K stage
   float scale_log2;
   int causal, fp16, inject;
   unsigned long long timeout_ns;
@@ -209,6 +210,230 @@ __device__ __forceinline__ void apply_mask32(float* x, int key0, int kv_len, boo
   }
 }
 
+// Barrier addresses seen by the softmax warps.  The arrive addresses are
+// shared::cluster addresses (the leader CTA's barriers) in pair mode and
+// plain shared-memory addresses of this CTA otherwise.
+// The two-entry barrier arrays are consecutive 8-byte objects, so entry b
+// sits at base + 8 b.
+struct SoftmaxBars {
+  uint32_t s_full;
+  uint32_t s_free_arrive;
+  uint32_t p_full_arrive;   // entry 0 of p_full[2]
+  uint32_t pv_done;         // entry 0 of pv_done[2]
+};
+
+// The softmax arrivals follow tcgen05.wait::ld (S read into registers) or
+// tcgen05.wait::st + tcgen05.fence (P written to TMEM); no generic-memory
+// write has to become visible, so the pair form is a relaxed arrive (a
+// cluster-scope release costs ~1000 cycles on this critical path).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_to(uint32_t addr) {
+  if (PAIR)
+    mbar_arrive_cluster_relaxed(addr);
+  else
+    mbar_arrive(addr);
+}
+
+// Softmax warps 0-3 and the epilogue: thread r owns query row it.q0 + r,
+// which is TMEM lane r of this CTA.
+template <bool VARLEN, bool PAIR>
+__device__ __forceinline__ void softmax_role(const Params& p, const Item& it, int T, uint32_t tmem,
+                                             int warp, int lane, const SoftmaxBars bars,
+                                             volatile int* abort_flag, unsigned long long tmo) {
+  const int mask_kind = p.mask_kind;
+  const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
+  const float scale_log2 = p.scale_log2;
+    // ------------------------------------------------------------ softmax
+  const int r = warp * 32 + lane;                 // row within the tile = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int row = it.q0 + r;                      // row within the sequence
+  const bool row_valid = row < it.q_len;
+  const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
+  const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
+  const uint8_t* mrow = nullptr;
+  if (mask_kind != FFPA_MASK_NONE && row_valid) {
+    const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
+    const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
+                          (long long)row * p.m_str[2];
+    mrow = static_cast<const uint8_t*>(p.mask) + off * (long long)esz;
+  }
+  const long long mk = p.m_str[3];
+  // Scores stay unscaled (x = q.k) when possible, so that the exponent
+  // x*scale*log2(e) - m is one FFMA; additive masks (or a scale <= 0, which
+  // reverses the max) need x pre-scaled into the log2 domain.
+  const bool prescale = mask_kind == FFPA_MASK_ADD_F32 || mask_kind == FFPA_MASK_ADD_QTYPE ||
+                        !(scale_log2 > 0.f);
+  const float xs = prescale ? 1.f : scale_log2;
+  const float ld_scale = prescale ? scale_log2 : 1.f;
+  float m_ref = -INFINITY;
+  float l_sum = 0.f;
+  bool ok = true;
+  for (int j = 0; j < T; ++j) {
+    const int b = j & 1;
+    bool w = wait_bounded(bars.s_full, j & 1, abort_flag, tmo);
+    ok = __all_sync(0xffffffffu, w);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t s_addr = lane_base + S_COL;
+    const uint32_t p_addr = lane_base + P_COL0 + 64 * b;
+    const int kbase = kv_tile(it, j) * BN;
+    const bool need_mask = (kbase + BN > it.kv_len) ||
+                           (causal && (long long)kbase + BN - 1 > first_limit) ||
+                           mask_kind != FFPA_MASK_NONE;
+    float x[BN];
+    {
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(s_addr, r0);
+      tmem_ld32(s_addr + 32, r1);
+      tmem_ld32(s_addr + 64, r2);
+      tmem_ld32(s_addr + 96, r3);
+      tmem_wait_ld();
+      reg_fence(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
+      // S has been read into registers: the next QK may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_to<PAIR>(bars.s_free_arrive);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        x[c] = __uint_as_float(r0[c]) * ld_scale;
+        x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
+        x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
+        x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
+      }
+    }
+    if (need_mask) {
+#pragma unroll
+      for (int q4 = 0; q4 < BN / 32; ++q4)
+        apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
+                     mask_kind, fp16);
+    }
+    float mx;
+    {   // tree maximum: eight independent chains, then combine
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[c + i]);
+      mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= xs;   // into the log2 domain (-inf stays -inf: xs > 0)
+    }
+    bool resc = false;
+    float alpha = 1.f;
+    if (mx > m_ref + RESCALE_LOG2) {
+      if (m_ref != -INFINITY) {
+        resc = true;
+        alpha = ex2_approx(m_ref - mx);
+      }
+      m_ref = mx;
+    }
+    if (__any_sync(0xffffffffu, resc)) {
+      // O holds PV up to tile j-1: wait for it, then scale this warp's rows.
+      w = wait_bounded(bars.pv_done + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < it.dv; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + c0, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+        tmem_st32(lane_base + c0, o);
+      }
+    }
+    if (j >= 2) {   // P buffer b was read by PV_{j-2}
+      w = wait_bounded(bars.pv_done + 8u * b, ((j - 2) >> 1) & 1, abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+    }
+    // P = exp2(x - m_ref) in 16-bit, into P buffer b.
+    const float base = m_ref == -INFINITY ? 0.f : m_ref;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int g = 0; g < BN / 32; ++g) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const int cc = 32 * g + c;
+        const float e0 = ex2_approx(fmaf(x[cc], xs, -base));
+        const float e1 = ex2_approx(fmaf(x[cc + 1], xs, -base));
+        const float e2 = ex2_approx(fmaf(x[cc + 2], xs, -base));
+        const float e3 = ex2_approx(fmaf(x[cc + 3], xs, -base));
+        s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+        pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+        pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+      }
+      tmem_st16(p_addr + 16 * g, pk);
+    }
+    l_sum = l_sum * alpha + ((s0 + s1) + (s2 + s3));
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_to<PAIR>(bars.p_full_arrive + 8u * b);
+  }
+  // ------------------------------------------------------------ epilogue
+  if (ok && T > 0) {
+    const bool w = wait_bounded(bars.pv_done + 8u * ((T - 1) & 1), ((T - 1) >> 1) & 1,
+                                abort_flag, tmo);
+    ok = __all_sync(0xffffffffu, w);
+    if (ok) tc_fence_after();
+  }
+  if (ok || T == 0) {
+    const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+    uint8_t* obase = nullptr;
+    if (row_valid) {
+      long long off;
+      if (VARLEN)
+        off = (long long)(it.q_row0 + row) * p.o_str[0] + (long long)it.hq * p.o_str[1];
+      else
+        off = (long long)it.b * p.o_str[0] + (long long)it.hq * p.o_str[1] +
+              (long long)row * p.o_str[2];
+      obase = static_cast<uint8_t*>(p.o) + (off + it.col_lo) * 2;
+    }
+    for (int c0 = 0; c0 < it.dv; c0 += 32) {
+      uint32_t o[32];
+      if (T > 0) {
+        tmem_ld32(lane_base + c0, o);
+        tmem_wait_ld();
+        reg_fence(o);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0u;
+      }
+      uint32_t pkd[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float a0 = __uint_as_float(o[2 * c]) * inv_l;
+        const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
+        pkd[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+      }
+      if (row_valid) {
+        uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+      }
+    }
+    if (row_valid && p.lse != nullptr && it.slice == 0) {
+      const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+      long long li;
+      if (VARLEN)
+        li = (long long)it.hq * p.Tq + it.q_row0 + row;
+      else
+        li = ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
+      p.lse[li] = lse;
+    }
+  }
+  }
+
 template <bool VARLEN>
 __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_constant__ Params p) {
   Item it;
@@ -217,10 +442,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   // Scalars copied out of the parameter block once: the hot loops below run
   // between asm statements with memory clobbers, which would otherwise force
   // the parameter loads to be repeated.
-  const int nchunks = p.nchunks, q_res = p.q_res, vk = p.vk, vchunks = p.vchunks;
-  const int kchunks = p.kchunks, mask_kind = p.mask_kind, inject = p.inject;
-  const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
-  const float scale_log2 = p.scale_log2;
+  const int nchunks = p.nchunks, q_res = p.q_res, vk = p.vk;
+  const int kchunks = p.kchunks, inject = p.inject;
+  const bool fp16 = p.fp16 != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -477,194 +701,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int r = warp * 32 + lane;                 // row within the tile = TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int row = it.q0 + r;                      // row within the sequence
-    const bool row_valid = row < it.q_len;
-    const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
-    const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
-    const uint8_t* mrow = nullptr;
-    if (mask_kind != FFPA_MASK_NONE && row_valid) {
-      const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
-      const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
-                            (long long)row * p.m_str[2];
-      mrow = static_cast<const uint8_t*>(p.mask) + off * (long long)esz;
-    }
-    const long long mk = p.m_str[3];
-    // Scores stay unscaled (x = q.k) when possible, so that the exponent
-    // x*scale*log2(e) - m is one FFMA; additive masks (or a scale <= 0, which
-    // reverses the max) need x pre-scaled into the log2 domain.
-    const bool prescale = mask_kind == FFPA_MASK_ADD_F32 || mask_kind == FFPA_MASK_ADD_QTYPE ||
-                          !(scale_log2 > 0.f);
-    const float xs = prescale ? 1.f : scale_log2;
-    const float ld_scale = prescale ? scale_log2 : 1.f;
-    float m_ref = -INFINITY;
-    float l_sum = 0.f;
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int b = j & 1;
-      bool w = wait_bounded(smem_u32(&bar_s_full), j & 1, &abort_flag, tmo);
-      ok = __all_sync(0xffffffffu, w);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_addr = lane_base + S_COL;
-      const uint32_t p_addr = lane_base + P_COL0 + 64 * b;
-      const int kbase = kv_tile(it, j) * BN;
-      const bool need_mask = (kbase + BN > it.kv_len) ||
-                             (causal && (long long)kbase + BN - 1 > first_limit) ||
-                             mask_kind != FFPA_MASK_NONE;
-      float x[BN];
-      {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(s_addr, r0);
-        tmem_ld32(s_addr + 32, r1);
-        tmem_ld32(s_addr + 64, r2);
-        tmem_ld32(s_addr + 96, r3);
-        tmem_wait_ld();
-        reg_fence(r0);
-        reg_fence(r1);
-        reg_fence(r2);
-        reg_fence(r3);
-        // S has been read into registers: the next QK may overwrite it.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(r0[c]) * ld_scale;
-          x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
-          x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
-          x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
-        }
-      }
-      if (need_mask) {
-#pragma unroll
-        for (int q4 = 0; q4 < BN / 32; ++q4)
-          apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
-                       mask_kind, fp16);
-      }
-      float mx;
-      {   // tree maximum: eight independent chains, then combine
-        float m8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = x[i];
-#pragma unroll
-        for (int c = 8; c < BN; c += 8)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[c + i]);
-        mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        mx *= xs;   // into the log2 domain (-inf stays -inf: xs > 0)
-      }
-      bool resc = false;
-      float alpha = 1.f;
-      if (mx > m_ref + RESCALE_LOG2) {
-        if (m_ref != -INFINITY) {
-          resc = true;
-          alpha = ex2_approx(m_ref - mx);
-        }
-        m_ref = mx;
-      }
-      if (__any_sync(0xffffffffu, resc)) {
-        // O holds PV up to tile j-1: wait for it, then scale this warp's rows.
-        w = wait_bounded(smem_u32(&bar_pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, &abort_flag, tmo);
-        ok = __all_sync(0xffffffffu, w);
-        if (!ok) break;
-        tc_fence_after();
-        for (int c0 = 0; c0 < it.dv; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + c0, o);
-          tmem_wait_ld();
-          reg_fence(o);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-          tmem_st32(lane_base + c0, o);
-        }
-      }
-      if (j >= 2) {   // P buffer b was read by PV_{j-2}
-        w = wait_bounded(smem_u32(&bar_pv_done[b]), ((j - 2) >> 1) & 1, &abort_flag, tmo);
-        ok = __all_sync(0xffffffffu, w);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      // P = exp2(x - m_ref) in 16-bit, into P buffer b.
-      const float base = m_ref == -INFINITY ? 0.f : m_ref;
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int g = 0; g < BN / 32; ++g) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const int cc = 32 * g + c;
-          const float e0 = ex2_approx(fmaf(x[cc], xs, -base));
-          const float e1 = ex2_approx(fmaf(x[cc + 1], xs, -base));
-          const float e2 = ex2_approx(fmaf(x[cc + 2], xs, -base));
-          const float e3 = ex2_approx(fmaf(x[cc + 3], xs, -base));
-          s0 += e0; s1 += e1; s2 += e2; s3 += e3;
-          pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-          pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
-        }
-        tmem_st16(p_addr + 16 * g, pk);
-      }
-      l_sum = l_sum * alpha + ((s0 + s1) + (s2 + s3));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_p_full[b]));
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && T > 0) {
-      const bool w = wait_bounded(smem_u32(&bar_pv_done[(T - 1) & 1]), ((T - 1) >> 1) & 1,
-                                  &abort_flag, tmo);
-      ok = __all_sync(0xffffffffu, w);
-      if (ok) tc_fence_after();
-    }
-    if (ok || T == 0) {
-      const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      uint8_t* obase = nullptr;
-      if (row_valid) {
-        long long off;
-        if (VARLEN)
-          off = (long long)(it.q_row0 + row) * p.o_str[0] + (long long)it.hq * p.o_str[1];
-        else
-          off = (long long)it.b * p.o_str[0] + (long long)it.hq * p.o_str[1] +
-                (long long)row * p.o_str[2];
-        obase = static_cast<uint8_t*>(p.o) + (off + it.col_lo) * 2;
-      }
-      for (int c0 = 0; c0 < it.dv; c0 += 32) {
-        uint32_t o[32];
-        if (T > 0) {
-          tmem_ld32(lane_base + c0, o);
-          tmem_wait_ld();
-          reg_fence(o);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0u;
-        }
-        uint32_t pkd[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a0 = __uint_as_float(o[2 * c]) * inv_l;
-          const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
-          pkd[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
-        }
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
-        }
-      }
-      if (row_valid && p.lse != nullptr && it.slice == 0) {
-        const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
-        long long li;
-        if (VARLEN)
-          li = (long long)it.hq * p.Tq + it.q_row0 + row;
-        else
-          li = ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
-        p.lse[li] = lse;
-      }
-    }
+    SoftmaxBars bars;
+    bars.s_full = smem_u32(&bar_s_full);
+    bars.s_free_arrive = smem_u32(&bar_s_free);
+    bars.p_full_arrive = smem_u32(&bar_p_full[0]);
+    bars.pv_done = smem_u32(&bar_pv_done[0]);
+    softmax_role<VARLEN, false>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
   }
 
   tc_fence_before();
@@ -673,6 +715,338 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+
+// =====================================================================
+// CTA-pair kernel (cta_group::2): two CTAs on two SMs share every K/V tile.
+//
+// A cluster of two CTAs owns a 256-row query tile: CTA c holds query rows
+// 128c .. 128c+127 (Q resident in its shared memory, S/O/P in its TMEM) and
+// loads only its half of each key tile (64 keys x 4 D-chunks) and of each V
+// stage (half of the slice's output columns).  The leader CTA (rank 0)
+// issues M = 256 MMAs that combine both halves, so each SM moves half the
+// K/V bytes and each MMA instruction drives both tensor cores.  The peer's
+// warps 5/6 relay its "stage landed" events to the leader's full barriers;
+// the leader's commits arrive in both CTAs (multicast).  Used when every
+// output slice is a multiple of 128 columns and Q fits in shared memory.
+// =====================================================================
+constexpr int BM_PAIR = 256;
+constexpr int KEYS_PER_CTA = BN / 2;
+
+__device__ __forceinline__ bool decode_item_pair(const Params& p, bool varlen, int L, uint32_t rank,
+                                                 Item& it) {
+  it.slice = L % p.n_slices;
+  L /= p.n_slices;
+  const int heads = p.B * p.Hq;
+  int qt;
+  if (p.causal) {
+    const int bh = L % heads;
+    qt = p.n_qt - 1 - L / heads;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  } else {
+    qt = L % p.n_qt;
+    const int bh = L / p.n_qt;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  }
+  it.hkv = it.hq / p.group;
+  if (varlen) {
+    it.q_row0 = p.cu_q[it.b];
+    it.q_len = p.cu_q[it.b + 1] - it.q_row0;
+    it.kv_row0 = p.cu_k[it.b];
+    it.kv_len = p.cu_k[it.b + 1] - it.kv_row0;
+  } else {
+    it.q_row0 = 0;
+    it.q_len = p.Nq;
+    it.kv_row0 = 0;
+    it.kv_len = p.Nkv;
+  }
+  const int q0_pair = qt * BM_PAIR;
+  if (q0_pair >= it.q_len) return false;           // same answer in both CTAs
+  it.q0 = q0_pair + BM * (int)rank;                // this CTA's rows
+  const int last_row = min(q0_pair + BM_PAIR, it.q_len) - 1;
+  long long kv_end = it.kv_len;
+  if (p.causal) kv_end = min(kv_end, (long long)last_row + (it.kv_len - it.q_len) + 1);
+  it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+  it.rot = it.ntiles > 0 ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
+                                 (unsigned)it.ntiles)
+                         : 0;
+  const int c_lo = it.slice * p.nchunks / p.n_slices;
+  const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
+  it.col_lo = c_lo * DK;
+  it.dv = (c_hi - c_lo) * DK;
+  return true;
+}
+
+template <bool VARLEN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+    ffpa_fwd_pair_kernel(const __grid_constant__ Params p) {
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  Item it;
+  if (!decode_item_pair(p, VARLEN, blockIdx.x >> 1, rank, it)) return;   // uniform across the pair
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int nchunks = p.nchunks, vk = p.vk, inject = p.inject;
+  const bool fp16 = p.fp16 != 0;
+  const int qpairs = (nchunks + 1) >> 1;
+  const int KC = p.kc;
+  const int nkst = nchunks / KC;                   // K stages per key tile
+  const uint32_t kslot = (uint32_t)p.kslot, vslot = (uint32_t)p.vslot;
+  const int NS = p.nslot, NSV = p.nslot_v;
+  const uint32_t qreg_u32 = smem_u32(smem);
+  const uint32_t kring_u32 = qreg_u32 + qpairs * SLOT_BYTES;
+  const uint32_t vring_u32 = kring_u32 + NS * kslot;
+  __shared__ __align__(8) uint64_t bar_full[NSLOT_MAX], bar_empty[NSLOT_MAX];
+  __shared__ __align__(8) uint64_t bar_vfull[NSLOT_V_MAX], bar_vempty[NSLOT_V_MAX];
+  __shared__ __align__(8) uint64_t bar_s_full, bar_s_free, bar_p_full[2], bar_pv_done[2], bar_q;
+  __shared__ __align__(8) uint64_t bar_drain[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    // Leader full barriers also count the peer's relayed arrival.
+    const uint32_t nfull = leader ? 2 : 1;
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), nfull);
+      mbar_init(smem_u32(&bar_empty[i]), 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(smem_u32(&bar_vfull[i]), nfull);
+      mbar_init(smem_u32(&bar_vempty[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_q), nfull);
+    mbar_init(smem_u32(&bar_s_full), 1);
+    mbar_init(smem_u32(&bar_s_free), 8);        // 4 softmax warps in each CTA
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bar_p_full[b]), 8);
+      mbar_init(smem_u32(&bar_pv_done[b]), 1);
+      mbar_init(smem_u32(&bar_drain[b]), 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc_pair(smem_u32(&tmem_base_sh), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();      // the peer's barriers exist before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int T = it.ntiles;
+  const unsigned long long tmo = p.timeout_ns;
+
+  if (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) {
+    // ------------------------------------------------------------ producers
+    if (lane == 0 && T > 0) {
+      const bool k_role = warp == PRODUCER_WARP;
+      const int nslots = k_role ? NS : NSV;
+      const uint32_t base = k_role ? kring_u32 : vring_u32;
+      const uint32_t stride = k_role ? kslot : vslot;
+      uint64_t* full = k_role ? bar_full : bar_vfull;
+      uint64_t* empty = k_role ? bar_empty : bar_vempty;
+      if (k_role) {
+        prefetch_tmap(&p.tm_q);
+        prefetch_tmap(&p.tm_k);
+      } else {
+        prefetch_tmap(&p.tm_v);
+      }
+      int slot = 0;
+      uint32_t lap = 0;
+      int issued = 0;
+      bool ok = true;
+      bool drop = k_role && leader && inject != 0;   // test hook (see ffpa_test_drop_first_copy)
+      auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
+        const uint32_t eb = smem_u32(&empty[slot]);
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
+          return ~0u;
+        fb = smem_u32(&full[slot]);
+        const uint32_t dst = base + slot * stride;
+        ++issued;
+        if (++slot == nslots) { slot = 0; lap ^= 1u; }
+        if (drop) {
+          drop = false;
+          return 0u;
+        }
+        mbar_arrive_expect_tx(fb, bytes);
+        return dst;
+      };
+      if (k_role) {
+        const uint32_t qb = smem_u32(&bar_q);
+        mbar_arrive_expect_tx(qb, (uint32_t)nchunks * CHUNK_BYTES);
+        for (int pr = 0; pr < qpairs; ++pr) {
+          if (VARLEN)
+            tma_load_4d(qreg_u32 + pr * SLOT_BYTES, &p.tm_q, qb, 0, it.q_row0 + it.q0, 2 * pr, it.hq);
+          else
+            tma_load_5d(qreg_u32 + pr * SLOT_BYTES, &p.tm_q, qb, 0, it.q0, 2 * pr, it.hq, it.b);
+        }
+        const int myk = KEYS_PER_CTA * (int)rank;
+        for (int j = 0; j < T && ok; ++j) {
+          const int key0 = kv_tile(it, j) * BN + myk;
+          for (int g = 0; g < nkst && ok; ++g) {
+            uint32_t fb = 0;
+            const uint32_t dst = acquire(kslot, fb);
+            if (dst == ~0u) { ok = false; break; }
+            if (dst) {
+              if (VARLEN)
+                tma_load_4d(dst, &p.tm_k, fb, 0, it.kv_row0 + key0, KC * g, it.hkv);
+              else
+                tma_load_5d(dst, &p.tm_k, fb, 0, key0, KC * g, it.hkv, it.b);
+            }
+          }
+        }
+        wait_drain(qb, 0, tmo);
+      } else {
+        const int mycol = (it.col_lo + (it.dv / 2) * (int)rank) / DK;
+        for (int j = 0; j < T && ok; ++j) {
+          for (int h = 0; h < BN / vk && ok; ++h) {
+            uint32_t fb = 0;
+            const uint32_t dst = acquire(vslot, fb);
+            if (dst == ~0u) { ok = false; break; }
+            const int key = kv_tile(it, j) * BN + h * vk;
+            if (VARLEN)
+              tma_load_4d(dst, &p.tm_v, fb, 0, it.kv_row0 + key, mycol, it.hkv);
+            else
+              tma_load_5d(dst, &p.tm_v, fb, 0, key, mycol, it.hkv, it.b);
+          }
+        }
+      }
+      const int n = issued < nslots ? issued : nslots;
+      int s = slot;
+      uint32_t lp = lap;
+      for (int i = 0; i < n; ++i) {
+        if (--s < 0) { s = nslots - 1; lp ^= 1u; }
+        if (k_role && leader && inject != 0 && issued - 1 - i == 0) continue;
+        wait_drain(smem_u32(&full[s]), lp, tmo);
+      }
+    }
+  } else if ((warp == MMA_WARP || warp == PV_WARP) && !leader) {
+    // ------------------------------------------------------------ relays
+    // Forward each landed stage of this CTA to the leader's full barrier.
+    if (lane == 0 && T > 0) {
+      const bool k_role = warp == MMA_WARP;
+      const int nslots = k_role ? NS : NSV;
+      uint64_t* full = k_role ? bar_full : bar_vfull;
+      const int per_tile = k_role ? nkst : BN / vk;
+      if (k_role) {
+        const uint32_t qb = smem_u32(&bar_q);
+        if (!(mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo))) goto relay_done;
+        mbar_arrive_cluster(mapa_shared(qb, 0));
+      }
+      {
+        int slot = 0;
+        uint32_t lap = 0;
+        for (int i = 0; i < T * per_tile; ++i) {
+          const uint32_t fb = smem_u32(&full[slot]);
+          if (!(mbar_try_wait(fb, lap) || wait_bounded(fb, lap, &abort_flag, tmo))) break;
+          mbar_arrive_cluster(mapa_shared(fb, 0));
+          if (++slot == nslots) { slot = 0; lap ^= 1u; }
+        }
+      }
+    relay_done:;
+    }
+  } else if (warp == MMA_WARP || warp == PV_WARP) {
+    // ------------------------------------------------------------ MMA issuers (leader)
+    if (lane == 0) {
+      const bool qk_role = warp == MMA_WARP;
+      const int nslots = qk_role ? NS : NSV;
+      uint64_t* full = qk_role ? bar_full : bar_vfull;
+      int slot = 0;
+      uint32_t lap = 0;
+      bool ok = true;
+      auto take = [&]() -> int {
+        const uint32_t fb = smem_u32(&full[slot]);
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        const int s = slot;
+        if (++slot == nslots) { slot = 0; lap ^= 1u; }
+        return s;
+      };
+      auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        tc_fence_after();
+        return true;
+      };
+      if (qk_role) {
+        const uint32_t idesc_qk = idesc_f16(!fp16, BM_PAIR, BN, false, false);
+        const uint64_t k_desc = sdesc_sw128(kring_u32, 16, 1024);
+        const uint64_t q_desc = sdesc_sw128(qreg_u32, 16, 1024);
+        const uint32_t s_col = tmem + S_COL;
+        const uint32_t kchunk_step = (KEYS_PER_CTA * 128) >> 4;   // one 64-key chunk
+        if (T > 0) ok = wait_on(smem_u32(&bar_q), 0);
+        for (int j = 0; j < T && ok; ++j) {
+          if (j >= 1 && !(ok = wait_on(smem_u32(&bar_s_free), (j - 1) & 1))) break;
+          for (int g = 0; g < nkst; ++g) {
+            const int sk = take();
+            if (sk < 0) { ok = false; break; }
+            const uint64_t bd0 = k_desc + ((sk * kslot) >> 4);
+            for (int cc = 0; cc < KC; ++cc) {
+              const uint64_t ad = q_desc + (((KC * g + cc) * CHUNK_BYTES) >> 4);
+              const uint64_t bd = bd0 + cc * kchunk_step;
+              umma_ss_pair(s_col, ad, bd, idesc_qk, (g > 0 || cc > 0) ? 1u : 0u);
+#pragma unroll
+              for (int k = 1; k < 4; ++k) umma_ss_pair(s_col, ad + 2 * k, bd + 2 * k, idesc_qk, 1u);
+            }
+            umma_commit_pair(smem_u32(&bar_empty[sk]));
+          }
+          if (!ok) break;
+          umma_commit_pair(smem_u32(&bar_s_full));
+        }
+      } else {
+        const uint32_t idesc_pv = idesc_f16(!fp16, BM_PAIR, it.dv, false, true);
+        const uint64_t v_desc = sdesc_sw128(vring_u32, vk * 128, 1024);
+        for (int j = 0; j < T && ok; ++j) {
+          const int b = j & 1;
+          if (!(ok = wait_on(smem_u32(&bar_p_full[b]), (j >> 1) & 1))) break;
+          const uint32_t p_col = tmem + P_COL0 + 64 * b;
+          for (int h = 0; h < BN / vk; ++h) {
+            const int s = take();
+            if (s < 0) { ok = false; break; }
+            const uint64_t vd = v_desc + ((s * vslot) >> 4);
+            const uint32_t pc = p_col + ((h * vk) >> 1);
+            for (int kk = 0; kk < vk / 16; ++kk)
+              umma_ts_pair(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
+            umma_commit_pair(smem_u32(&bar_vempty[s]));
+          }
+          if (!ok) break;
+          umma_commit_pair(smem_u32(&bar_pv_done[b]));
+        }
+      }
+      const uint32_t db = smem_u32(&bar_drain[qk_role ? 0 : 1]);
+      umma_commit_pair(db);
+      wait_drain(db, 0, tmo);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    SoftmaxBars bars;
+    bars.s_full = smem_u32(&bar_s_full);
+    bars.s_free_arrive = mapa_shared(smem_u32(&bar_s_free), 0);
+    bars.p_full_arrive = mapa_shared(smem_u32(&bar_p_full[0]), 0);
+    bars.pv_done = smem_u32(&bar_pv_done[0]);
+    softmax_role<VARLEN, true>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
+  }
+
+  // The leader's last commits also arrive in the peer: wait for them before
+  // the pair may exit, then free TMEM in both CTAs together.
+  if (!leader && threadIdx.x == 0) {
+    wait_drain(smem_u32(&bar_drain[0]), 0, tmo);
+    wait_drain(smem_u32(&bar_drain[1]), 0, tmo);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -686,6 +1060,7 @@ namespace {
 using namespace ffpa;
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_variant{FFPA_VARIANT_AUTO};
 std::atomic<int> g_drop_first_copy{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -792,6 +1167,63 @@ size_t plan(int D, Params* P) {
   return 1024 + q_region + ns * SLOT_BYTES + (size_t)P->nslot_v * P->vslot;
 }
 
+// The CTA-pair kernel needs every output slice to split into two halves of
+// whole 64-column chunks, Q resident, and K stages of equal chunk count.
+bool pair_eligible(int D) {
+  const int nchunks = D / DK;
+  if (nchunks > Q_RESIDENT_MAX_CHUNKS) return false;
+  const int n_slices = (D + DV_MAX - 1) / DV_MAX;
+  for (int sl = 0; sl < n_slices; ++sl) {
+    const int w = (sl + 1) * nchunks / n_slices - sl * nchunks / n_slices;
+    if (w % 2 != 0) return false;
+  }
+  const int kc = nchunks < 4 ? nchunks : 4;
+  return nchunks % kc == 0;
+}
+
+// Kernel choice.  Measured on GB300 (bf16, 16 heads x 4096): the pair kernel
+// wins at D=256 and D=512 on dense batches; at D=128 the single-CTA kernel's
+// shorter per-tile chain wins, and on packed varlen batches of mixed lengths
+// the 256-row pair tiles waste more rows on short sequences than they save.
+bool use_pair(int D, bool varlen) {
+  const int v = g_variant.load();
+  if (v == FFPA_VARIANT_SINGLE || !pair_eligible(D)) return false;
+  if (v == FFPA_VARIANT_PAIR) return true;
+  return D >= 256 && !varlen;
+}
+
+// Pair-kernel plan: K stages of 64 keys x kc chunks, V stages of 128 keys x
+// half the slice's columns, Q resident; returns the dynamic smem bytes.
+size_t plan_pair(int D, Params* P) {
+  plan(D, P);
+  P->q_res = 1;
+  P->kc = P->nchunks < 4 ? P->nchunks : 4;
+  P->kslot = (BN / 2) * P->kc * 128;
+  const int max_dv = P->vchunks * DK;
+  P->vchunks = max_dv / 2 / DK;
+  P->vk = BN;
+  P->vslot = P->vk * P->vchunks * 128;
+  const size_t q_region = ((P->nchunks + 1) / 2) * (size_t)SLOT_BYTES;
+  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region;
+  int nsv = NSLOT_V_MAX;
+  if (budget < (size_t)nsv * P->vslot + 2 * (size_t)P->kslot) nsv = 1;
+  size_t ns = (budget - (size_t)nsv * P->vslot) / P->kslot;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  P->nslot = static_cast<int>(ns);
+  P->nslot_v = nsv;
+  return 1024 + q_region + ns * P->kslot + (size_t)nsv * P->vslot;
+}
+
+template <bool VARLEN>
+ffpa_status launch_pair(const Params& P, int items, size_t smem, cudaStream_t stream) {
+  auto kern = ffpa_fwd_pair_kernel<VARLEN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  kern<<<2 * items, NTHREADS, smem, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
+}
+
 template <bool VARLEN>
 ffpa_status launch(const Params& P, int items, size_t smem, cudaStream_t stream) {
   auto kern = ffpa_fwd_kernel<VARLEN>;
@@ -821,6 +1253,10 @@ const char* ffpa_status_string(ffpa_status s) {
 void ffpa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
 
 void ffpa_test_drop_first_copy(int enable) { g_drop_first_copy.store(enable ? 1 : 0); }
+
+void ffpa_set_kernel_variant(int variant) {
+  if (variant >= FFPA_VARIANT_AUTO && variant <= FFPA_VARIANT_PAIR) g_variant.store(variant);
+}
 
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -870,7 +1306,10 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const size_t smem = plan(D, &P);
+  const bool pair = use_pair(D, false);
+  const size_t smem = pair ? plan_pair(D, &P) : plan(D, &P);
+  const uint32_t k_rows = pair ? BN / 2 : BN;
+  const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
   const uint64_t nch = (uint64_t)P.nchunks;
   {
     const uint64_t dq[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
@@ -881,7 +1320,7 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
     const uint64_t dk[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
     const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
-    const uint32_t bk[5] = {64, BN, (uint32_t)P.kchunks, 1, 1};
+    const uint32_t bk[5] = {64, k_rows, k_box_chunks, 1, 1};
     if ((st = encode_map(&P.tm_k, tdt, 5, k, dk, sk, bk)) != FFPA_OK) return st;
     const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
     const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
@@ -902,7 +1341,8 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   P.Nkv = Nkv;
   P.D = D;
   P.Tq = 0;
-  P.n_qt = (Nq + BM - 1) / BM;
+  const int q_tile = pair ? BM_PAIR : BM;
+  P.n_qt = (Nq + q_tile - 1) / q_tile;
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
@@ -910,6 +1350,8 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   P.timeout_ns = g_timeout_ns.load();
   const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  if (pair)
+    return launch_pair<false>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
   return launch<false>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -944,7 +1386,10 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const size_t smem = plan(D, &P);
+  const bool pair = use_pair(D, true);
+  const size_t smem = pair ? plan_pair(D, &P) : plan(D, &P);
+  const uint32_t k_rows = pair ? BN / 2 : BN;
+  const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
   const uint64_t nch = (uint64_t)P.nchunks;
   {
     const uint64_t dq[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
@@ -955,7 +1400,7 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if (Tk > 0) {
     const uint64_t dk[4] = {64, (uint64_t)Tk, nch, (uint64_t)Hkv};
     const uint64_t sk[3] = {(uint64_t)k_str[0] * 2, 128, (uint64_t)k_str[1] * 2};
-    const uint32_t bk[4] = {64, BN, (uint32_t)P.kchunks, 1};
+    const uint32_t bk[4] = {64, k_rows, k_box_chunks, 1};
     if ((st = encode_map(&P.tm_k, tdt, 4, k, dk, sk, bk)) != FFPA_OK) return st;
     const uint64_t sv[3] = {(uint64_t)v_str[0] * 2, 128, (uint64_t)v_str[1] * 2};
     const uint32_t bv[4] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1};
@@ -977,7 +1422,8 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   P.Nkv = 0;
   P.D = D;
   P.Tq = Tq;
-  P.n_qt = (max_seqlen_q + BM - 1) / BM;
+  const int q_tile = pair ? BM_PAIR : BM;
+  P.n_qt = (max_seqlen_q + q_tile - 1) / q_tile;
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
@@ -986,6 +1432,8 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   (void)max_seqlen_k;
   const long long items = (long long)nseq * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  if (pair)
+    return launch_pair<true>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
   return launch<true>(P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -137,6 +137,19 @@ ffpa_status ffpa_last_device_error(ffpa_stream_t stream);
 void ffpa_set_wait_timeout_ns(uint64_t ns);
 
 /*
+ * Kernel choice for launches made after the call.  The library has two
+ * kernels with identical results: a single-CTA kernel (any D) and a CTA-pair
+ * kernel (two SMs share each 256-query tile and each load half of every K/V
+ * tile; D in {128, 256, 512}).
+ *   FFPA_VARIANT_AUTO   (0) the faster one measured for the shape (default)
+ *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
+ *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
+ * Any other value is ignored.
+ */
+enum { FFPA_VARIANT_AUTO = 0, FFPA_VARIANT_SINGLE = 1, FFPA_VARIANT_PAIR = 2 };
+void ffpa_set_kernel_variant(int variant);
+
+/*
  * TEST HOOK, not for production use: when nonzero, the next launches skip
  * the first tensor copy of each CTA, so that the pipeline wait depending on
  * it runs out and reports FFPA_ERR_DEVICE_TIMEOUT (no fault, no hang).

@@ -146,3 +146,12 @@ def test_binding_rejects_malformed_cu_seqlens(lib):
     with pytest.raises(NotImplementedError):
         pkg.ffpa_fwd_varlen(q, q, q, torch.tensor([0, 10], dtype=torch.int32), None, 10, 10,
                             softcap=1.0)
+
+
+def test_kernel_variant_names(lib):
+    for name in ("single", "pair", "auto"):
+        pkg.set_kernel_variant(name)
+    with pytest.raises(ValueError):
+        pkg.set_kernel_variant("fastest")
+    lib.ffpa_set_kernel_variant(7)  # out of range: ignored, no effect
+    pkg.set_kernel_variant("auto")

@@ -211,6 +211,49 @@ def test_invariant_causal_visibility():
     assert (~unchanged[limit >= t]).float().mean().item() > 0.9
 
 
+# ------------------------------------------- each kernel forced, same bar
+@pytest.fixture(params=["single", "pair"])
+def variant(request):
+    pkg.set_kernel_variant(request.param)
+    yield request.param
+    pkg.set_kernel_variant("auto")
+
+
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_variant_dense(variant, D):
+    dense_case(1, 2, 2, 300, 300, D, seed=D + 1)
+    dense_case(2, 4, 1, 200, 700, D, seed=D + 2, causal=True)
+    dense_case(1, 2, 2, 65, 129, D, seed=D + 3, causal=True)
+
+
+@pytest.mark.parametrize("D", [128, 512])
+def test_variant_masks(variant, D):
+    B, H, Nq, Nk = 2, 2, 270, 300
+    dense_case(B, H, H, Nq, Nk, D, seed=D + 4, mask=MASKS["bool_b1nk"](B, H, Nq, Nk))
+    dense_case(B, H, H, Nq, Nk, D, seed=D + 5, causal=True, mask=MASKS["f32_neg_inf"](B, H, Nq, Nk))
+
+
+def test_variant_fp16(variant):
+    dense_case(1, 2, 1, 260, 260, 256, seed=9, causal=True, dtype=torch.float16)
+
+
+@pytest.mark.parametrize("D", [128, 256, 512])
+@pytest.mark.parametrize("causal", [False, True])
+def test_variant_varlen(variant, D, causal):
+    lq = [3, 130, 1, 257, 0, 64, 200, 300]
+    lk = [5, 130, 2, 300, 7, 64, 450, 300]
+    q, k, v, cq, ck = wl.draw_varlen(lq, lk, 4, 2, D, seed=D + int(causal))
+    o, l = pkg.ffpa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lq),
+                               max(lk), causal=causal, enable_gqa=True, return_lse=True)
+    device_ok()
+    o_ref, l_ref = oracle.attn_varlen(q, k, v, cq, ck, causal=causal)
+    check(o, l, o_ref, l_ref, f"varlen {variant}")
+
+
+def test_variant_full_d512_sampled(variant):
+    _sampled_dense(wl.headdim_sweep(512), n_random=24)
+
+
 # ----------------------------------------------------------------- varlen
 @pytest.mark.parametrize("D", [128, 512])
 @pytest.mark.parametrize("causal", [False, True])
@@ -258,6 +301,25 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     o, l = run_dense(x["q"], x["k"], x["v"])
     o_ref, l_ref = oracle.attn_dense(x["q"], x["k"], x["v"])
     check(o, l, o_ref, l_ref, "after timeout")
+
+
+def test_bounded_wait_pair_kernel():
+    """Same check through the CTA-pair kernel (D=512): both CTAs of the pair
+    time out, the status is reported and the next call is correct."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 256, 256, 512, seed=41)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    pkg.set_wait_timeout_ns(200_000_000)
+    pkg.inject_dropped_copy(True)
+    try:
+        pkg.ffpa_fwd(qd, kd, vd)
+        st = pkg.ffpa_last_device_error()
+    finally:
+        pkg.inject_dropped_copy(False)
+        pkg.set_wait_timeout_ns(0)
+    assert st == pkg.FFPA_ERR_DEVICE_TIMEOUT
+    o, l = run_dense(q, k, v)
+    o_ref, l_ref = oracle.attn_dense(q, k, v)
+    check(o, l, o_ref, l_ref, "pair kernel after timeout")
 
 
 # ------------------------------------------------------- full-size workloads
