@@ -25,7 +25,7 @@ FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
             "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant")
 
-KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2}
+KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
 
 _lib = None
 
@@ -274,7 +274,7 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 
 def set_kernel_variant(name: str) -> None:
-    """Choose the kernel for later launches: "auto", "single" or "pair" (see ffpa.h)."""
+    """Choose the kernel for later launches: "auto", "single", "pair" or "split" (see ffpa.h)."""
     if name not in KERNEL_VARIANTS:
         raise ValueError(f"kernel variant must be one of {sorted(KERNEL_VARIANTS)}, got {name!r}")
     load_library().ffpa_set_kernel_variant(KERNEL_VARIANTS[name])

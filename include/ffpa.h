@@ -137,16 +137,28 @@ ffpa_status ffpa_last_device_error(ffpa_stream_t stream);
 void ffpa_set_wait_timeout_ns(uint64_t ns);
 
 /*
- * Kernel choice for launches made after the call.  The library has two
- * kernels with identical results: a single-CTA kernel (any D) and a CTA-pair
- * kernel (two SMs share each 256-query tile and each load half of every K/V
- * tile; D in {128, 256, 512}).
- *   FFPA_VARIANT_AUTO   (0) the faster one measured for the shape (default)
+ * Kernel choice for launches made after the call.  The library has three
+ * kernels with identical results:
+ *   - single-CTA: one CTA per 128-row query tile and output slice of at most
+ *     256 columns (any D; S is recomputed once per slice);
+ *   - CTA pair: two SMs share each 256-query tile and each load half of every
+ *     K/V tile (D in {128, 256, 512});
+ *   - column split: two SMs share each 128-query tile, each owns half of the
+ *     output columns, key tiles alternate between them and the P tiles are
+ *     exchanged, so S is computed once (D in {128, 256, 384, 512}).
+ *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default)
  *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
  *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
+ *   FFPA_VARIANT_SPLIT  (3) the column-split kernel wherever D allows it
+ * Where the chosen kernel does not support D, the single-CTA kernel runs.
  * Any other value is ignored.
  */
-enum { FFPA_VARIANT_AUTO = 0, FFPA_VARIANT_SINGLE = 1, FFPA_VARIANT_PAIR = 2 };
+enum {
+  FFPA_VARIANT_AUTO = 0,
+  FFPA_VARIANT_SINGLE = 1,
+  FFPA_VARIANT_PAIR = 2,
+  FFPA_VARIANT_SPLIT = 3
+};
 void ffpa_set_kernel_variant(int variant);
 
 /*

@@ -212,14 +212,14 @@ def test_invariant_causal_visibility():
 
 
 # ------------------------------------------- each kernel forced, same bar
-@pytest.fixture(params=["single", "pair"])
+@pytest.fixture(params=["single", "pair", "split"])
 def variant(request):
     pkg.set_kernel_variant(request.param)
     yield request.param
     pkg.set_kernel_variant("auto")
 
 
-@pytest.mark.parametrize("D", [128, 256, 512])
+@pytest.mark.parametrize("D", [128, 256, 384, 512])
 def test_variant_dense(variant, D):
     dense_case(1, 2, 2, 300, 300, D, seed=D + 1)
     dense_case(2, 4, 1, 200, 700, D, seed=D + 2, causal=True)
@@ -320,6 +320,30 @@ def test_bounded_wait_pair_kernel():
     o, l = run_dense(q, k, v)
     o_ref, l_ref = oracle.attn_dense(q, k, v)
     check(o, l, o_ref, l_ref, "pair kernel after timeout")
+
+
+def test_bounded_wait_split_kernel():
+    """Same check through the column-split kernel: one CTA of the pair loses
+    a copy, the other one waits for its tile maxima; both time out, the
+    status is reported and the next call is correct."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 200, 400, 512, seed=43)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    pkg.set_kernel_variant("split")
+    pkg.set_wait_timeout_ns(200_000_000)
+    pkg.inject_dropped_copy(True)
+    try:
+        pkg.ffpa_fwd(qd, kd, vd)
+        st = pkg.ffpa_last_device_error()
+    finally:
+        pkg.inject_dropped_copy(False)
+        pkg.set_wait_timeout_ns(0)
+    try:
+        assert st == pkg.FFPA_ERR_DEVICE_TIMEOUT
+        o, l = run_dense(q, k, v)
+        o_ref, l_ref = oracle.attn_dense(q, k, v)
+        check(o, l, o_ref, l_ref, "split kernel after timeout")
+    finally:
+        pkg.set_kernel_variant("auto")
 
 
 # ------------------------------------------------------- full-size workloads
