@@ -1093,7 +1093,11 @@ constexpr int Q_TMEM_MAX_CHUNKS = 4;
 constexpr uint32_t P_TILE_BYTES = BM * BN * 2;   // 2 x (128 rows x 64 keys), 16-bit
 constexpr size_t SPLIT_STATIC_RESERVE = 2048;
 
-template <bool VARLEN>
+// NCH = D / 64 is a template parameter so that every MMA issue loop has a
+// compile-time trip count and is fully unrolled: the tensor pipe's
+// instruction queue is shallow, and loop overhead between MMAs leaves it
+// idle (measured: a runtime-count loop of 8 MMAs runs at about half rate).
+template <bool VARLEN, int NCH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     ffpa_fwd_split_kernel(const __grid_constant__ Params p) {
   const uint32_t rank = cluster_ctarank();
@@ -1107,8 +1111,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int nchunks = p.nchunks, vk = p.vk, inject = p.inject;
-  const int qt = p.qt_chunks;                  // Q chunks held in TMEM
+  constexpr int nchunks = NCH;
+  constexpr int qt = NCH < Q_TMEM_MAX_CHUNKS ? NCH : Q_TMEM_MAX_CHUNKS;   // Q chunks held in TMEM
+  constexpr int VCH = NCH / 2;                                           // V chunks per CTA
+  constexpr int vk = VCH * 128 * 128 <= (int)SLOT_BYTES ? 128 : 64;      // keys per V stage
+  const int inject = p.inject;
   const bool fp16 = p.fp16 != 0;
   const uint32_t vslot = (uint32_t)p.vslot;
   const int NS = p.nslot;
@@ -1278,6 +1285,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       auto qk = [&](int j) -> bool {
         (void)j;   // the producer loads tile j's stages in this order
         if (nq >= 1 && !wait_on(smem_u32(&bar_s_free), (nq - 1) & 1)) return false;
+#pragma unroll
         for (int c = 0; c < nchunks; c += 2) {
           const int sk = take();
           if (sk < 0) return false;
@@ -1306,10 +1314,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       };
       bool o_acc = false;
       auto pv = [&](uint64_t a_desc) -> bool {
+#pragma unroll
         for (int h = 0; h < BN / vk; ++h) {
           const int s = take();
           if (s < 0) return false;
           const uint64_t vd = v_desc + ((s * SLOT_BYTES) >> 4);
+#pragma unroll
           for (int kk = 0; kk < vk / 16; ++kk) {
             // 16 keys per MMA: P (K-major, 64-key chunks of 16 KB, +32 bytes
             // per 16 keys), V (MN-major, +2048 bytes per 16 keys).
@@ -1798,7 +1808,10 @@ ffpa_status launch_pair(const Params& P, int items, size_t smem, cudaStream_t st
 
 template <bool VARLEN>
 ffpa_status launch_split(const Params& P, int items, size_t smem, cudaStream_t stream) {
-  auto kern = ffpa_fwd_split_kernel<VARLEN>;
+  auto kern = P.nchunks == 8   ? ffpa_fwd_split_kernel<VARLEN, 8>
+              : P.nchunks == 6 ? ffpa_fwd_split_kernel<VARLEN, 6>
+              : P.nchunks == 4 ? ffpa_fwd_split_kernel<VARLEN, 4>
+                               : ffpa_fwd_split_kernel<VARLEN, 2>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_LIMIT - SPLIT_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;
