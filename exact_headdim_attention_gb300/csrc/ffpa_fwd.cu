@@ -795,7 +795,8 @@ __device__ __forceinline__ bool decode_item_pair(const Params& p, bool varlen, i
   return true;
 }
 
-template <bool VARLEN>
+// NCH = D / 64 as a template parameter: the MMA issue loops unroll.
+template <bool VARLEN, int NCH>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ffpa_fwd_pair_kernel(const __grid_constant__ Params p) {
   const uint32_t rank = cluster_ctarank();
@@ -806,11 +807,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int nchunks = p.nchunks, vk = p.vk, inject = p.inject;
+  constexpr int nchunks = NCH, vk = BN;
+  const int inject = p.inject;
   const bool fp16 = p.fp16 != 0;
-  const int qpairs = (nchunks + 1) >> 1;
-  const int KC = p.kc;
-  const int nkst = nchunks / KC;                   // K stages per key tile
+  constexpr int qpairs = (nchunks + 1) >> 1;
+  constexpr int KC = nchunks < 4 ? nchunks : 4;
+  constexpr int nkst = nchunks / KC;               // K stages per key tile
   const uint32_t kslot = (uint32_t)p.kslot, vslot = (uint32_t)p.vslot;
   const int NS = p.nslot, NSV = p.nslot_v;
   const uint32_t qreg_u32 = smem_u32(smem);
@@ -998,10 +1000,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         if (T > 0) ok = wait_on(smem_u32(&bar_q), 0);
         for (int j = 0; j < T && ok; ++j) {
           if (j >= 1 && !(ok = wait_on(smem_u32(&bar_s_free), (j - 1) & 1))) break;
+#pragma unroll
           for (int g = 0; g < nkst; ++g) {
             const int sk = take();
             if (sk < 0) { ok = false; break; }
             const uint64_t bd0 = k_desc + ((sk * kslot) >> 4);
+#pragma unroll
             for (int cc = 0; cc < KC; ++cc) {
               const uint64_t ad = q_desc + (((KC * g + cc) * CHUNK_BYTES) >> 4);
               const uint64_t bd = bd0 + cc * kchunk_step;
@@ -1026,6 +1030,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             if (s < 0) { ok = false; break; }
             const uint64_t vd = v_desc + ((s * vslot) >> 4);
             const uint32_t pc = p_col + ((h * vk) >> 1);
+#pragma unroll
             for (int kk = 0; kk < vk / 16; ++kk)
               umma_ts_pair(tmem, pc + 8 * kk, vd + 128 * kk, idesc_pv, (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
             umma_commit_pair(smem_u32(&bar_vempty[s]));
@@ -1798,7 +1803,9 @@ size_t plan_pair(int D, Params* P) {
 
 template <bool VARLEN>
 ffpa_status launch_pair(const Params& P, int items, size_t smem, cudaStream_t stream) {
-  auto kern = ffpa_fwd_pair_kernel<VARLEN>;
+  auto kern = P.nchunks == 8   ? ffpa_fwd_pair_kernel<VARLEN, 8>
+              : P.nchunks == 4 ? ffpa_fwd_pair_kernel<VARLEN, 4>
+                               : ffpa_fwd_pair_kernel<VARLEN, 2>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;
