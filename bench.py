@@ -82,11 +82,13 @@ def read_peaks():
             with open(path) as f:
                 d = json.load(f)
             bf16 = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
+            sus = d.get("bf16_tflops_sustained")
             if bf16:
-                return float(bf16), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+                return (float(bf16), "measured (MEASURED_PEAKS.json bf16_tflops, burst)",
+                        float(sus) if sus else None)
         except (OSError, ValueError):
             pass
-    return FALLBACK_BF16_TFLOPS, "fallback (profiling recipe: 1.9 PFLOP/s bf16 burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback (profiling recipe: 1.9 PFLOP/s bf16 burst)", None
 
 
 # ------------------------------------------------------------------ clocks
@@ -311,7 +313,11 @@ def run_ours(args):
     st = pkg.ffpa_last_device_error()
     if st != pkg.FFPA_OK:
         raise SystemExit(f"device error: {pkg.ffpa_status_string(st)}")
-    peak, peak_src = read_peaks()
+    peak, peak_src, peak_sustained = read_peaks()
+    kname = pkg.selected_kernel(w.D, w.varlen)
+    kernel = {"single": f"ffpa_fwd_kernel<{str(w.varlen).lower()}>",
+              "pair": f"ffpa_fwd_pair_kernel<{str(w.varlen).lower()}, {w.D // 64}>",
+              "split": f"ffpa_fwd_split_kernel<{str(w.varlen).lower()}, {w.D // 64}>"}[kname]
     per_launch_s = elapsed / args.steps
     achieved = flops / per_launch_s / 1e12
     line = {
@@ -323,7 +329,9 @@ def run_ours(args):
         "pct_of_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "peak_source": peak_src, "kernel": "ffpa_fwd_kernel<false>",
+                     "peak_source": peak_src, "kernel": kernel,
+                     "frac_of_sustained": (round(achieved / peak_sustained, 4)
+                                           if peak_sustained else None),
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e,

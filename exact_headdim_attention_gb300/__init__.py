@@ -28,5 +28,6 @@ from ._binding import (  # noqa: F401
     load_library,
     set_wait_timeout_ns,
     set_kernel_variant,
+    selected_kernel,
     inject_dropped_copy,
 )

@@ -23,7 +23,8 @@ FFPA_BF16, FFPA_FP16 = 0, 1
 FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
 
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
-            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant")
+            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant",
+            "ffpa_selected_kernel")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
 
@@ -85,6 +86,8 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_test_drop_first_copy.restype = None
     lib.ffpa_set_kernel_variant.argtypes = [I]
     lib.ffpa_set_kernel_variant.restype = None
+    lib.ffpa_selected_kernel.argtypes = [I, I]
+    lib.ffpa_selected_kernel.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -278,6 +281,14 @@ def set_kernel_variant(name: str) -> None:
     if name not in KERNEL_VARIANTS:
         raise ValueError(f"kernel variant must be one of {sorted(KERNEL_VARIANTS)}, got {name!r}")
     load_library().ffpa_set_kernel_variant(KERNEL_VARIANTS[name])
+
+
+def selected_kernel(D: int, varlen: bool = False) -> str:
+    """Name of the kernel ("single", "pair" or "split") a launch would use now for head dim D."""
+    v = load_library().ffpa_selected_kernel(int(D), int(bool(varlen)))
+    if v < 0:
+        raise ValueError(f"unsupported head dimension {D}")
+    return {code: name for name, code in KERNEL_VARIANTS.items()}[v]
 
 
 def inject_dropped_copy(enable: bool) -> None:

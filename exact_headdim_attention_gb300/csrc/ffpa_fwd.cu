@@ -1876,6 +1876,12 @@ void ffpa_set_kernel_variant(int variant) {
   if (variant >= FFPA_VARIANT_AUTO && variant <= FFPA_VARIANT_SPLIT) g_variant.store(variant);
 }
 
+int ffpa_selected_kernel(int D, int varlen) {
+  if (D < 64 || D > 1024 || D % 64 != 0) return -1;
+  const Kern kn = choose_kernel(D, varlen != 0);
+  return kn == Kern::PAIR ? FFPA_VARIANT_PAIR : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT : FFPA_VARIANT_SINGLE;
+}
+
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FFPA_ERR_CUDA;

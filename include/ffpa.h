@@ -162,6 +162,14 @@ enum {
 void ffpa_set_kernel_variant(int variant);
 
 /*
+ * The kernel (FFPA_VARIANT_SINGLE, _PAIR or _SPLIT) that a launch made now
+ * would run for head dimension D on a dense (varlen = 0) or packed varlen
+ * (varlen != 0) batch, under the current kernel choice.  Host only; returns
+ * -1 for a head dimension the library does not support.
+ */
+int ffpa_selected_kernel(int D, int varlen);
+
+/*
  * TEST HOOK, not for production use: when nonzero, the next launches skip
  * the first tensor copy of each CTA, so that the pipeline wait depending on
  * it runs out and reports FFPA_ERR_DEVICE_TIMEOUT (no fault, no hang).

@@ -155,3 +155,24 @@ def test_kernel_variant_names(lib):
         pkg.set_kernel_variant("fastest")
     lib.ffpa_set_kernel_variant(7)  # out of range: ignored, no effect
     pkg.set_kernel_variant("auto")
+
+
+def test_selected_kernel_follows_the_choice(lib):
+    pkg.set_kernel_variant("auto")
+    assert pkg.selected_kernel(512) == "split"
+    assert pkg.selected_kernel(512, varlen=True) == "split"
+    assert pkg.selected_kernel(256) == "pair"
+    assert pkg.selected_kernel(256, varlen=True) == "single"
+    assert pkg.selected_kernel(1024) == "single"
+    try:
+        pkg.set_kernel_variant("pair")
+        assert pkg.selected_kernel(512) == "pair"
+        assert pkg.selected_kernel(384) == "single"      # pair kernel does not take D=384
+        pkg.set_kernel_variant("split")
+        assert pkg.selected_kernel(384) == "split"
+        assert pkg.selected_kernel(640) == "single"
+    finally:
+        pkg.set_kernel_variant("auto")
+    assert lib.ffpa_selected_kernel(100, 0) == -1
+    with pytest.raises(ValueError):
+        pkg.selected_kernel(96)

@@ -60,5 +60,6 @@ def test_clock_summary_reasons_and_window():
 
 
 def test_peaks_fallback_or_measured():
-    peak, src = bench.read_peaks()
+    peak, src, sustained = bench.read_peaks()
     assert peak > 100 and ("fallback" in src or "measured" in src)
+    assert sustained is None or 100 < sustained <= peak
