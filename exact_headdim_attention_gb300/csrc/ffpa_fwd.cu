@@ -1497,6 +1497,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         }
         m_ref = mx;
       }
+      // P of the own tile (registers only: no dependence on the PV of the
+      // previous round, so this overlaps it).
+      l_sum *= alpha;
+      uint32_t pk[BN / 2];
+      if (own) {
+        const float base = m_ref == -INFINITY ? 0.f : m_ref;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          const float e0 = ex2_approx(fmaf(x[c], xs, -base));
+          const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
+          const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
+          const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
+          s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+          pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+          pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+        }
+        l_sum += (s0 + s1) + (s2 + s3);
+      }
+      if (own) {
+        // The own P area is free once the own PV of the previous own tile is
+        // done and the peer has read the previous copy (which also frees the
+        // peer's P area for this one).
+        bool w = true;
+        if (k_own >= 1)
+          w = wait_bounded(smem_u32(&bar_pown_free), (k_own - 1) & 1, &abort_flag, tmo);
+        if (w) w = wait_bounded(smem_u32(&bar_peer_free), k_own & 1, &abort_flag, tmo, true);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        // Row r of the P tile: 16 units of 8 keys, 128-byte swizzle.
+        const uint32_t prow = pown_u32 + r * 128;
+        const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+        for (int g = 0; g < BN / 8; ++g)
+          st_shared_v4(prow + (g >> 3) * CHUNK_BYTES + ((((uint32_t)g & 7u) ^ sw) << 4), pk[4 * g],
+                       pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        fence_proxy_async_smem();
+      }
       if (i >= 1) {
         // PV of round i-1 done.  Waited every round (not only before a
         // rescale) so that each phase of this barrier is observed: a parity
@@ -1518,40 +1556,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           tmem_st32(lane_base + c0, o);
         }
-      }
-      l_sum *= alpha;
-      if (own) {
-        const float base = m_ref == -INFINITY ? 0.f : m_ref;
-        uint32_t pk[BN / 2];
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN; c += 4) {
-          const float e0 = ex2_approx(fmaf(x[c], xs, -base));
-          const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
-          const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
-          const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
-          s0 += e0; s1 += e1; s2 += e2; s3 += e3;
-          pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-          pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
-        }
-        l_sum += (s0 + s1) + (s2 + s3);
-        // The own P area is free once the own PV of the previous own tile is
-        // done and the peer has read the previous copy (which also frees the
-        // peer's P area for this one).
-        bool w = true;
-        if (k_own >= 1)
-          w = wait_bounded(smem_u32(&bar_pown_free), (k_own - 1) & 1, &abort_flag, tmo);
-        if (w) w = wait_bounded(smem_u32(&bar_peer_free), k_own & 1, &abort_flag, tmo, true);
-        ok = __all_sync(0xffffffffu, w);
-        if (!ok) break;
-        // Row r of the P tile: 16 units of 8 keys, 128-byte swizzle.
-        const uint32_t prow = pown_u32 + r * 128;
-        const uint32_t sw = (uint32_t)(r & 7);
-#pragma unroll
-        for (int g = 0; g < BN / 8; ++g)
-          st_shared_v4(prow + (g >> 3) * CHUNK_BYTES + ((((uint32_t)g & 7u) ^ sw) << 4), pk[4 * g],
-                       pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-        fence_proxy_async_smem();
       }
       if (resc_warp) tmem_wait_st();
       tc_fence_before();
