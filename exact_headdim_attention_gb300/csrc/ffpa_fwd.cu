@@ -1562,15 +1562,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_pown_full));
       if (own) {
-        if (r == 0) {
-          // All four warps have written their rows: copy the tile to the peer.
-          bool w = wait_bounded(smem_u32(&bar_pown_full), i & 1, &abort_flag, tmo);
-          if (w)
-            bulk_copy_to_cta(mapa_shared(ppeer_u32, peer), pown_u32, P_TILE_BYTES,
-                             mapa_shared(smem_u32(&bar_ppeer_full), peer));
-          ok = w;
+        // This warp's 32 rows of both 64-key chunks (2 x 4 KB, each
+        // contiguous) to the peer, as soon as they are written.
+        if (lane == 0) {
+          const uint32_t pb = mapa_shared(smem_u32(&bar_ppeer_full), peer);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t off = c * CHUNK_BYTES + warp * 32 * 128;
+            bulk_copy_to_cta(mapa_shared(ppeer_u32 + off, peer), pown_u32 + off, 32 * 128, pb);
+          }
         }
-        ok = __all_sync(0xffffffffu, ok);
         ++k_own;
       }
     }
