@@ -269,6 +269,24 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
   }
 }
 
+// P = exp2(x * xs - base) for n scores, packed to 16-bit pairs; returns the
+// sum of the (unrounded) values.
+template <bool F16, int N>
+__device__ __forceinline__ float form_p(const float* x, float xs, float base, uint32_t* pk) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int c = 0; c < N; c += 4) {
+    const float e0 = ex2_approx(fmaf(x[c], xs, -base));
+    const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
+    const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
+    const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
+    s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+    pk[c / 2] = F16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+    pk[c / 2 + 1] = F16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
 // Barrier addresses seen by the softmax warps.  The arrive addresses are
 // shared::cluster addresses (the leader CTA's barriers) in pair mode and
 // plain shared-memory addresses of this CTA otherwise.
@@ -415,24 +433,15 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
     }
     // P = exp2(x - m_ref) in 16-bit, into P buffer b.
     const float base = m_ref == -INFINITY ? 0.f : m_ref;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float psum = 0.f;
 #pragma unroll
     for (int g = 0; g < BN / 32; ++g) {
       uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const int cc = 32 * g + c;
-        const float e0 = ex2_approx(fmaf(x[cc], xs, -base));
-        const float e1 = ex2_approx(fmaf(x[cc + 1], xs, -base));
-        const float e2 = ex2_approx(fmaf(x[cc + 2], xs, -base));
-        const float e3 = ex2_approx(fmaf(x[cc + 3], xs, -base));
-        s0 += e0; s1 += e1; s2 += e2; s3 += e3;
-        pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-        pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
-      }
+      psum += fp16 ? form_p<true, 32>(x + 32 * g, xs, base, pk)
+                   : form_p<false, 32>(x + 32 * g, xs, base, pk);
       tmem_st16(p_addr + 16 * g, pk);
     }
-    l_sum = l_sum * alpha + ((s0 + s1) + (s2 + s3));
+    l_sum = l_sum * alpha + psum;
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
@@ -1503,18 +1512,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       uint32_t pk[BN / 2];
       if (own) {
         const float base = m_ref == -INFINITY ? 0.f : m_ref;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN; c += 4) {
-          const float e0 = ex2_approx(fmaf(x[c], xs, -base));
-          const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
-          const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
-          const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
-          s0 += e0; s1 += e1; s2 += e2; s3 += e3;
-          pk[c / 2] = fp16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
-          pk[c / 2 + 1] = fp16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
-        }
-        l_sum += (s0 + s1) + (s2 + s3);
+        // One branch per tile, not per element: the unrolled loop then holds
+        // a single conversion per pair.
+        l_sum += fp16 ? form_p<true, BN>(x, xs, base, pk) : form_p<false, BN>(x, xs, base, pk);
       }
       if (own) {
         // The own P area is free once the own PV of the previous own tile is
