@@ -31,3 +31,4 @@ from ._binding import (  # noqa: F401
     selected_kernel,
     inject_dropped_copy,
 )
+from .torch_ops import ffpa_attn_func, ffpa_attn_varlen_func  # noqa: F401,E402
