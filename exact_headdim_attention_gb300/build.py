@@ -11,6 +11,7 @@ from __future__ import annotations
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 from pathlib import Path
 
 PKG = Path(__file__).resolve().parent
@@ -18,8 +19,10 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 OUT = PKG / "_build" / "libffpa.so"
-SOURCES = [CSRC / "ffpa_fwd.cu"]
-DEPS = SOURCES + [CSRC / "ptx.cuh", INCLUDE / "ffpa.h"]
+# One translation unit per kernel plus the host side, compiled in parallel.
+SOURCES = [CSRC / n for n in ("ffpa_split.cu", "ffpa_pair.cu", "ffpa_single.cu", "ffpa_api.cu")]
+DEPS = SOURCES + [CSRC / "ffpa_common.cuh", CSRC / "ptx.cuh", INCLUDE / "ffpa.h"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def nvcc() -> str:
@@ -28,8 +31,8 @@ def nvcc() -> str:
 
 
 def flags() -> list[str]:
-    return ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
-            "-Xcompiler", "-fPIC", "-shared", f"-I{INCLUDE}", f"-I{CSRC}"]
+    """Compile flags of every translation unit."""
+    return [*ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 
 def stale() -> bool:
@@ -42,12 +45,25 @@ def stale() -> bool:
 def build(force: bool = False, verbose: bool = False) -> Path:
     if not force and not stale():
         return OUT
-    OUT.parent.mkdir(parents=True, exist_ok=True)
-    tmp = OUT.with_suffix(".so.tmp")
-    cmd = [nvcc(), *flags(), *map(str, SOURCES), "-o", str(tmp)]
+    objdir = OUT.parent / "obj"
+    objdir.mkdir(parents=True, exist_ok=True)
+    jobs = [[nvcc(), *flags(), "-c", str(src), "-o", str(objdir / (src.stem + ".o"))]
+            for src in SOURCES]
     if verbose:
-        print(" ".join(cmd))
-    subprocess.run(cmd, check=True)
+        for cmd in jobs:
+            print(" ".join(cmd))
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs))
+    for cmd, r in zip(jobs, results):
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise subprocess.CalledProcessError(r.returncode, cmd)
+    tmp = OUT.with_suffix(".so.tmp")
+    link = [nvcc(), *ARCH, "-shared", *(str(objdir / (src.stem + ".o")) for src in SOURCES),
+            "-o", str(tmp)]
+    if verbose:
+        print(" ".join(link))
+    subprocess.run(link, check=True)
     os.replace(tmp, OUT)
     return OUT
 

@@ -1,0 +1,432 @@
+// Host side of libffpa.so: argument validation, kernel choice, planning,
+// tensor maps, launch, and the C ABI declared in include/ffpa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "ffpa_common.cuh"
+
+// =====================================================================
+// Host side: validation, planning, tensor maps, launch.
+// =====================================================================
+namespace {
+
+using namespace ffpa;
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_variant{FFPA_VARIANT_AUTO};
+std::atomic<int> g_drop_first_copy{0};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Element strides of every non-unit dimension but the last must be a
+// multiple of 8 elements (16 bytes for 16-bit types); the last must be 1.
+bool strides_ok(const int64_t* str, const int64_t* size, int rank) {
+  if (str[rank - 1] != 1) return false;
+  for (int i = 0; i < rank - 1; ++i) {
+    if (size[i] <= 1) continue;
+    if (str[i] <= 0 || (str[i] % 8) != 0) return false;
+  }
+  return true;
+}
+
+// Tiled tensor map with 128-byte swizzle.  dims[0] is always 64 (one
+// 128-byte row of 16-bit values); byte strides are given for dims 1..rank-1.
+// A size-1 dimension gets a harmless stride so its (never used) value cannot
+// fail the encoder's alignment checks.
+ffpa_status encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* stride_bytes, const uint32_t* box) {
+  auto enc = encode_fn();
+  if (!enc) return FFPA_ERR_CUDA;
+  cuuint64_t gdim[5];
+  cuuint64_t gstr[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 1; i < rank; ++i) {
+    uint64_t st = stride_bytes[i - 1];
+    if (dims[i] <= 1 && (st == 0 || st % 16 != 0)) st = 128;
+    gstr[i - 1] = st;
+  }
+  CUresult r = enc(m, dt, rank, const_cast<void*>(base), gdim, gstr, bx, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FFPA_OK : FFPA_ERR_INVALID;
+}
+
+// Makes the device that owns `ptr` current for this library's runtime (the
+// runtime is linked statically, so its current device is not the caller's),
+// then requires compute capability 10.3 (sm_103).
+ffpa_status check_device(const void* ptr, int* dev_out) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return FFPA_ERR_CUDA;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return FFPA_ERR_INVALID;
+  const int dev = attr.device;
+  if (cudaSetDevice(dev) != cudaSuccess) return FFPA_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  if (major != 10 || minor != 3) return FFPA_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  return FFPA_OK;
+}
+
+// Splits D into at most 256-column output slices, sizes the V stage, and
+// decides whether Q stays resident in shared memory (D <= 512) and how many
+// 32 KB ring slots fit beside it.  Returns the dynamic shared memory bytes.
+size_t plan(int D, Params* P) {
+  P->nchunks = D / DK;
+  P->n_slices = (D + DV_MAX - 1) / DV_MAX;
+  const int max_dv = ((P->nchunks + P->n_slices - 1) / P->n_slices) * DK;
+  P->vchunks = max_dv / DK;
+  P->kchunks = P->nchunks < 2 ? P->nchunks : 2;
+  P->q_res = P->nchunks <= Q_RESIDENT_MAX_CHUNKS;
+  const size_t q_region = P->q_res ? ((P->nchunks + 1) / 2) * (size_t)SLOT_BYTES : 0;
+  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region;
+  // V stages: up to 32 KB (vk keys x vchunks chunks of 128-byte rows), two
+  // slots; halve vk while that leaves fewer than two K-ring slots.
+  int vk = 128;
+  while (vk > 16 && (size_t)vk * P->vchunks * 128 > SLOT_BYTES) vk >>= 1;
+  P->nslot_v = NSLOT_V_MAX;
+  while (vk > 32 && budget < 2 * (size_t)SLOT_BYTES + (size_t)NSLOT_V_MAX * vk * P->vchunks * 128)
+    vk >>= 1;
+  P->vk = vk;
+  P->vslot = vk * P->vchunks * 128;
+  size_t ns = (budget - (size_t)P->nslot_v * P->vslot) / SLOT_BYTES;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  P->nslot = static_cast<int>(ns);
+  return 1024 + q_region + ns * SLOT_BYTES + (size_t)P->nslot_v * P->vslot;
+}
+
+// The CTA-pair kernel needs every output slice to split into two halves of
+// whole 64-column chunks, Q resident, and K stages of equal chunk count.
+bool pair_eligible(int D) {
+  const int nchunks = D / DK;
+  if (nchunks > Q_RESIDENT_MAX_CHUNKS) return false;
+  const int n_slices = (D + DV_MAX - 1) / DV_MAX;
+  for (int sl = 0; sl < n_slices; ++sl) {
+    const int w = (sl + 1) * nchunks / n_slices - sl * nchunks / n_slices;
+    if (w % 2 != 0) return false;
+  }
+  const int kc = nchunks < 4 ? nchunks : 4;
+  return nchunks % kc == 0;
+}
+
+enum class Kern { SINGLE, PAIR, SPLIT };
+
+// The column-split kernel needs each CTA's half of the output columns to be
+// whole 64-column chunks of at most 256 columns.
+bool split_eligible(int D) { return D >= 128 && D % 128 == 0 && D / 2 <= DV_MAX; }
+
+// Kernel choice, from measurements on GB300 (bf16): at D=512 the column-split
+// kernel wins on dense, causal and varlen batches (it does not recompute S);
+// at D=256 (no recompute anyway) the pair kernel wins on dense batches; at
+// D=128 the single-CTA kernel's shorter per-tile chain wins, and on packed
+// varlen batches of mixed lengths the 256-row pair tiles waste more rows on
+// short sequences than they save.
+Kern choose_kernel(int D, bool varlen) {
+  const int v = g_variant.load();
+  if (v == FFPA_VARIANT_SINGLE) return Kern::SINGLE;
+  if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
+  if (v == FFPA_VARIANT_SPLIT) return split_eligible(D) ? Kern::SPLIT : Kern::SINGLE;
+  if (D == 512) return Kern::SPLIT;
+  if (!varlen && D == 256) return Kern::PAIR;
+  return Kern::SINGLE;
+}
+
+// Column-split plan: Q chunks 0..3 in TMEM, the rest resident in shared
+// memory, two P tiles, V stages of vk keys x D/2 columns, 32 KB ring slots.
+size_t plan_split(int D, Params* P) {
+  P->nchunks = D / DK;
+  P->n_slices = 1;
+  P->qt_chunks = P->nchunks < Q_TMEM_MAX_CHUNKS ? P->nchunks : Q_TMEM_MAX_CHUNKS;
+  P->kchunks = 2;
+  P->kc = 2;
+  P->q_res = 1;
+  P->vchunks = D / 2 / DK;
+  int vk = 128;
+  while (vk > 16 && (size_t)vk * P->vchunks * 128 > SLOT_BYTES) vk >>= 1;
+  P->vk = vk;
+  P->vslot = vk * P->vchunks * 128;
+  P->nslot_v = 0;
+  const size_t fixed = (size_t)(P->nchunks - P->qt_chunks) * CHUNK_BYTES + 2 * (size_t)P_TILE_BYTES;
+  size_t ns = (SMEM_LIMIT - SPLIT_STATIC_RESERVE - 1024 - fixed) / SLOT_BYTES;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  P->nslot = static_cast<int>(ns);
+  return 1024 + fixed + ns * SLOT_BYTES;
+}
+
+// Pair-kernel plan: K stages of 64 keys x kc chunks, V stages of 128 keys x
+// half the slice's columns, Q resident; returns the dynamic smem bytes.
+size_t plan_pair(int D, Params* P) {
+  plan(D, P);
+  P->q_res = 1;
+  P->kc = P->nchunks < 4 ? P->nchunks : 4;
+  P->kslot = (BN / 2) * P->kc * 128;
+  const int max_dv = P->vchunks * DK;
+  P->vchunks = max_dv / 2 / DK;
+  P->vk = BN;
+  P->vslot = P->vk * P->vchunks * 128;
+  const size_t q_region = ((P->nchunks + 1) / 2) * (size_t)SLOT_BYTES;
+  const size_t budget = SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region;
+  int nsv = NSLOT_V_MAX;
+  if (budget < (size_t)nsv * P->vslot + 2 * (size_t)P->kslot) nsv = 1;
+  size_t ns = (budget - (size_t)nsv * P->vslot) / P->kslot;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  P->nslot = static_cast<int>(ns);
+  P->nslot_v = nsv;
+  return 1024 + q_region + ns * P->kslot + (size_t)nsv * P->vslot;
+}
+
+ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size_t smem,
+                          cudaStream_t stream) {
+  if (kn == Kern::PAIR) return launch_pair(varlen, P, items, smem, stream);
+  if (kn == Kern::SPLIT) return launch_split(varlen, P, items, smem, stream);
+  return launch_single(varlen, P, items, smem, stream);
+}
+
+size_t plan_for(Kern kn, int D, Params* P) {
+  if (kn == Kern::PAIR) return plan_pair(D, P);
+  if (kn == Kern::SPLIT) return plan_split(D, P);
+  return plan(D, P);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ffpa_status_string(ffpa_status s) {
+  switch (s) {
+    case FFPA_OK: return "FFPA_OK";
+    case FFPA_ERR_DTYPE: return "FFPA_ERR_DTYPE: inputs must be bf16 or fp16";
+    case FFPA_ERR_INVALID: return "FFPA_ERR_INVALID: invalid shape, stride, pointer or option";
+    case FFPA_ERR_UNSUPPORTED: return "FFPA_ERR_UNSUPPORTED: head dim or device not supported";
+    case FFPA_ERR_CUDA: return "FFPA_ERR_CUDA: a CUDA runtime call failed";
+    case FFPA_ERR_DEVICE_TIMEOUT: return "FFPA_ERR_DEVICE_TIMEOUT: a kernel wait ran out of time";
+  }
+  return "FFPA: unknown status";
+}
+
+void ffpa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
+
+void ffpa_test_drop_first_copy(int enable) { g_drop_first_copy.store(enable ? 1 : 0); }
+
+void ffpa_set_kernel_variant(int variant) {
+  if (variant >= FFPA_VARIANT_AUTO && variant <= FFPA_VARIANT_SPLIT) g_variant.store(variant);
+}
+
+int ffpa_selected_kernel(int D, int varlen) {
+  if (D < 64 || D > 1024 || D % 64 != 0) return -1;
+  const Kern kn = choose_kernel(D, varlen != 0);
+  return kn == Kern::PAIR ? FFPA_VARIANT_PAIR : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT : FFPA_VARIANT_SINGLE;
+}
+
+ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  ffpa_status (*const take[3])(int*) = {ffpa::take_err_single, ffpa::take_err_pair,
+                                        ffpa::take_err_split};
+  int first = 0;
+  for (auto fn : take) {
+    int word = 0;
+    if (fn(&word) != FFPA_OK) return FFPA_ERR_CUDA;
+    if (first == 0) first = word;
+  }
+  return static_cast<ffpa_status>(first);
+}
+
+ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                     const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
+  if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (B == 0 || Nq == 0) return FFPA_OK;          // nothing to read or write
+  if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  if (mask_kind != FFPA_MASK_NONE && Nkv > 0) {
+    if (!mask || !mask_str) return FFPA_ERR_INVALID;
+    for (int i = 0; i < 4; ++i)
+      if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+  }
+  const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
+  if (!strides_ok(q_str, qsz, 4) || !strides_ok(o_str, qsz, 4)) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!strides_ok(k_str, ksz, 4) || !strides_ok(v_str, ksz, 4))) return FFPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || (Nkv > 0 && (!aligned16(k) || !aligned16(v))))
+    return FFPA_ERR_INVALID;
+  int dev = 0;
+  ffpa_status st = check_device(q, &dev);
+  if (st != FFPA_OK) return st;
+
+  Params P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const Kern kn = choose_kernel(D, false);
+  const bool pair = kn == Kern::PAIR;
+  const size_t smem = plan_for(kn, D, &P);
+  const uint32_t k_rows = pair ? BN / 2 : BN;
+  const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
+  const uint64_t nch = (uint64_t)P.nchunks;
+  {
+    const uint64_t dq[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t sq[4] = {(uint64_t)q_str[2] * 2, 128, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
+    const uint32_t bq[5] = {64, BM, (uint32_t)P.kchunks, 1, 1};
+    if ((st = encode_map(&P.tm_q, tdt, 5, q, dq, sq, bq)) != FFPA_OK) return st;
+  }
+  if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
+    const uint64_t dk[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
+    const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
+    const uint32_t bk[5] = {64, k_rows, k_box_chunks, 1, 1};
+    if ((st = encode_map(&P.tm_k, tdt, 5, k, dk, sk, bk)) != FFPA_OK) return st;
+    const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
+    const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
+    if ((st = encode_map(&P.tm_v, tdt, 5, v, dk, sv, bv)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.lse = lse;
+  P.mask = mask_kind != FFPA_MASK_NONE ? mask : nullptr;
+  P.mask_kind = mask_kind;
+  for (int i = 0; i < 4; ++i) {
+    P.o_str[i] = o_str[i];
+    P.m_str[i] = mask_kind != FFPA_MASK_NONE ? mask_str[i] : 0;
+  }
+  P.B = B;
+  P.Hq = Hq;
+  P.group = Hq / Hkv;
+  P.Nq = Nq;
+  P.Nkv = Nkv;
+  P.D = D;
+  P.Tq = 0;
+  const int q_tile = pair ? BM_PAIR : BM;
+  P.n_qt = (Nq + q_tile - 1) / q_tile;
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = is_causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.inject = g_drop_first_copy.load();
+  P.timeout_ns = g_timeout_ns.load();
+  const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
+  if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch_kernel(kn, false, P, static_cast<int>(items), smem,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3],
+                            const int64_t v_str[3], const int64_t o_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (nseq < 1 || max_seqlen_q < 0 || max_seqlen_k < 0) return FFPA_ERR_INVALID;
+  if (!cu_seqlens_q) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (Tq == 0 || max_seqlen_q == 0) return FFPA_OK;   // nothing to read or write
+  if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
+  if (Tk > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  const int64_t qsz[3] = {Tq, Hq, D}, ksz[3] = {Tk, Hkv, D};
+  if (!strides_ok(q_str, qsz, 3) || !strides_ok(o_str, qsz, 3)) return FFPA_ERR_INVALID;
+  if (Tk > 0 && (!strides_ok(k_str, ksz, 3) || !strides_ok(v_str, ksz, 3))) return FFPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
+    return FFPA_ERR_INVALID;
+  int dev = 0;
+  ffpa_status st = check_device(q, &dev);
+  if (st != FFPA_OK) return st;
+
+  Params P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const Kern kn = choose_kernel(D, true);
+  const bool pair = kn == Kern::PAIR;
+  const size_t smem = plan_for(kn, D, &P);
+  const uint32_t k_rows = pair ? BN / 2 : BN;
+  const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
+  const uint64_t nch = (uint64_t)P.nchunks;
+  {
+    const uint64_t dq[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
+    const uint64_t sq[3] = {(uint64_t)q_str[0] * 2, 128, (uint64_t)q_str[1] * 2};
+    const uint32_t bq[4] = {64, BM, (uint32_t)P.kchunks, 1};
+    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq, sq, bq)) != FFPA_OK) return st;
+  }
+  if (Tk > 0) {
+    const uint64_t dk[4] = {64, (uint64_t)Tk, nch, (uint64_t)Hkv};
+    const uint64_t sk[3] = {(uint64_t)k_str[0] * 2, 128, (uint64_t)k_str[1] * 2};
+    const uint32_t bk[4] = {64, k_rows, k_box_chunks, 1};
+    if ((st = encode_map(&P.tm_k, tdt, 4, k, dk, sk, bk)) != FFPA_OK) return st;
+    const uint64_t sv[3] = {(uint64_t)v_str[0] * 2, 128, (uint64_t)v_str[1] * 2};
+    const uint32_t bv[4] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1};
+    if ((st = encode_map(&P.tm_v, tdt, 4, v, dk, sv, bv)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.lse = lse;
+  P.mask = nullptr;
+  P.mask_kind = FFPA_MASK_NONE;
+  P.o_str[0] = o_str[0];
+  P.o_str[1] = o_str[1];
+  P.o_str[2] = o_str[2];
+  P.cu_q = cu_seqlens_q;
+  P.cu_k = cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q;
+  P.B = nseq;
+  P.Hq = Hq;
+  P.group = Hq / Hkv;
+  P.Nq = 0;
+  P.Nkv = 0;
+  P.D = D;
+  P.Tq = Tq;
+  const int q_tile = pair ? BM_PAIR : BM;
+  P.n_qt = (max_seqlen_q + q_tile - 1) / q_tile;
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.inject = g_drop_first_copy.load();
+  P.timeout_ns = g_timeout_ns.load();
+  (void)max_seqlen_k;
+  const long long items = (long long)nseq * Hq * P.n_qt * P.n_slices;
+  if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch_kernel(kn, true, P, static_cast<int>(items), smem,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

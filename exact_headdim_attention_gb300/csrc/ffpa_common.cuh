@@ -1,0 +1,487 @@
+#pragma once
+// Exact attention forward for large head dimensions on GB300 (sm_103a):
+// device code shared by the three kernels (single-CTA, CTA pair, column
+// split), one translation unit each.
+//
+// Method (FFPA README, "Split-D and TiledMMA"; FFPA API reference,
+// "ffpa_attn.ffpa_attn_func" / "ffpa_attn_varlen_func"): a FlashAttention
+// style online softmax over key tiles, with the head dimension D split into
+// 64-wide chunks so that the on-chip staging of Q, K and V does not grow
+// with D ("Split-D").  On Blackwell the accumulators live in Tensor Memory
+// (TMEM, 128 lanes x 512 fp32 columns per SM) instead of registers, so the
+// pages' register-pressure problem becomes a TMEM-capacity problem: a CTA
+// owns at most 256 output columns ("output-D slice") next to one 128-column
+// S buffer and two 64-column P buffers.  When D > 256 the output columns are
+// split across CTAs and each CTA recomputes S for its slice.
+//
+// Per CTA (one work item = batch b, query head h, 128-row query tile,
+// output-D slice) the warps specialise:
+//   warps 0-3  softmax: row r = 32*warp + lane; read S from TMEM, mask,
+//              online max / exp2 / sum, write P (16-bit) to a P buffer, rescale
+//              O when the running max moved by more than 2^8, epilogue.
+//   warp 4     TMA producer: Q/K D-chunk pairs and V stages into a ring of
+//              32 KB shared-memory slots (128-byte swizzle), in the exact
+//              order the MMA warp consumes them.
+//   warp 5     MMA issuer (one thread): S_j = sum_c Q_c K_{j,c}^T into TMEM
+//              (tcgen05.mma, smem x smem), O += P_j V_j (P from TMEM).
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the
+// kernel records FFPA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "ffpa.h"
+#include "ptx.cuh"
+
+namespace ffpa {
+
+constexpr int BM = 128;              // query rows per tile = TMEM lanes
+constexpr int BN = 128;              // keys per S tile
+constexpr int DK = 64;               // D chunk: one 128-byte swizzle row of 16-bit values
+constexpr int DV_MAX = 256;          // output columns per CTA
+constexpr int NSLOT_MAX = 6;         // K-ring slots (fewer when Q is resident)
+constexpr int NSLOT_V_MAX = 2;       // V-ring slots
+constexpr uint32_t SLOT_BYTES = 32768;         // one TMA box of 2 D-chunks (32 KB)
+constexpr uint32_t CHUNK_BYTES = BM * DK * 2;  // 16 KB: one 128x64 tile
+constexpr int Q_RESIDENT_MAX_CHUNKS = 8;       // Q stays in smem for D <= 512
+constexpr size_t SMEM_LIMIT = 232448;          // opt-in dynamic smem per block (sm_103)
+constexpr size_t SMEM_STATIC_RESERVE = 1024;
+constexpr int NTHREADS = 256;
+constexpr int PRODUCER_WARP = 4;     // TMA for Q and the K ring
+constexpr int MMA_WARP = 5;          // issues S = Q K^T; owns the TMEM allocation
+constexpr int PV_WARP = 6;           // issues O += P V
+constexpr int V_PRODUCER_WARP = 7;   // TMA for the V ring
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 256;      // S (fp32, 128 keys) occupies columns [256, 384)
+constexpr uint32_t P_COL0 = 384;     // P buffer b (16-bit pairs, 128 keys) at [384 + 64 b, +64)
+constexpr float RESCALE_LOG2 = 8.0f; // rescale O only when the max grows by > 2^8
+
+// CTA-pair kernel: a 256-row query tile per pair, 64 keys of each K tile per CTA.
+constexpr int BM_PAIR = 256;
+constexpr int KEYS_PER_CTA = BN / 2;
+
+// Column-split kernel (see ffpa_split.cu).
+constexpr int SPLIT_THREADS = 192;
+constexpr uint32_t Q_TMEM_COL = 384;
+constexpr int Q_TMEM_MAX_CHUNKS = 4;
+constexpr uint32_t P_TILE_BYTES = BM * BN * 2;   // 2 x (128 rows x 64 keys), 16-bit
+constexpr size_t SPLIT_STATIC_RESERVE = 2048;
+
+// Device status word of this translation unit (each kernel file has its
+// own; the host reads and clears them all in ffpa_last_device_error).
+static __device__ int g_err_word;
+
+// ------------------------------------------------------------------ host
+// Launches of the three kernels (one translation unit each) and their
+// device status words.
+struct Params;
+ffpa_status launch_single(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_pair(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_split(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
+// Reads the unit's status word into *word and clears it (FFPA_ERR_CUDA if
+// the copy fails).
+ffpa_status take_err_single(int* word);
+ffpa_status take_err_pair(int* word);
+ffpa_status take_err_split(int* word);
+
+struct Params {
+  // Views with D split as (64, D/64): dense (64, N, D/64, H, B); varlen
+  // (64, T, D/64, H).  Q and K boxes: 64 x 128 rows x min(2, D/64) chunks;
+  // V box: 64 x vk rows x vchunks chunks.
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;
+  float* lse;
+  const void* mask;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int64_t o_str[4];    // dense (b, h, n, d); varlen (t, h, d)
+  int64_t m_str[4];
+  int mask_kind;
+  int B;               // batches (dense) or sequences (varlen)
+  int Hq, group, Nq, Nkv, D, Tq;
+  int n_qt, n_slices, nchunks, vk, vchunks, kchunks;
+  int q_res, nslot;    // Q resident in smem (1) or streamed through the K ring (0); K-ring depth
+  int nslot_v, vslot;  // V-ring depth and slot bytes (vk keys x vchunks 64-column chunks)
+  int kslot, kc;       // pair kernel: K-ring slot bytes and D-chunks per K stage
+  int qt_chunks;       // column-split kernel: Q chunks held in TMEM
+  float scale_log2;
+  int causal, fp16, inject;
+  unsigned long long timeout_ns;
+};
+
+struct Item {
+  int b, hq, hkv, slice;
+  int q0, q_len, kv_len, q_row0, kv_row0;
+  int col_lo, dv, ntiles;
+  int rot;   // first key tile visited; tiles are visited rot, rot+1, ... (mod ntiles)
+};
+
+// Key tile visited at step j.  Work items of one head start at different
+// tiles so that they do not all miss in L2 on the same tile at the same time;
+// the online softmax gives the same result for any visiting order.
+__device__ __forceinline__ int kv_tile(const Item& it, int j) {
+  const int t = j + it.rot;
+  return t >= it.ntiles ? t - it.ntiles : t;
+}
+
+__device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L, Item& it) {
+  it.slice = L % p.n_slices;
+  L /= p.n_slices;
+  const int heads = p.B * p.Hq;
+  int qt;
+  if (p.causal) {                    // longest query tiles first
+    const int bh = L % heads;
+    qt = p.n_qt - 1 - L / heads;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  } else {                           // tiles of one head adjacent: K/V reuse in L2
+    qt = L % p.n_qt;
+    const int bh = L / p.n_qt;
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+  }
+  it.hkv = it.hq / p.group;
+  if (varlen) {
+    it.q_row0 = p.cu_q[it.b];
+    it.q_len = p.cu_q[it.b + 1] - it.q_row0;
+    it.kv_row0 = p.cu_k[it.b];
+    it.kv_len = p.cu_k[it.b + 1] - it.kv_row0;
+  } else {
+    it.q_row0 = 0;
+    it.q_len = p.Nq;
+    it.kv_row0 = 0;
+    it.kv_len = p.Nkv;
+  }
+  it.q0 = qt * BM;
+  if (it.q0 >= it.q_len) return false;
+  const int rows = min(BM, it.q_len - it.q0);
+  long long kv_end = it.kv_len;
+  if (p.causal) {
+    const long long last_visible = (long long)it.q0 + rows - 1 + (it.kv_len - it.q_len);
+    kv_end = min(kv_end, last_visible + 1);
+  }
+  it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+  it.rot = it.ntiles > 0 ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
+                                 (unsigned)it.ntiles)
+                         : 0;
+  const int c_lo = it.slice * p.nchunks / p.n_slices;
+  const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
+  it.col_lo = c_lo * DK;
+  it.dv = (c_hi - c_lo) * DK;
+  return true;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when this CTA has been
+// told to abort or when the limit expires (then the error word is set).
+// `cluster` selects cluster-scope acquire, for phases that another CTA of
+// the cluster completes.
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long timeout_ns, bool cluster = false) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    // Suspended waiting keeps idle warps from taking issue slots away from
+    // the MMA and TMA threads that share their SM sub-partition.
+    if (cluster ? mbar_try_wait_sleep_cluster(bar, parity, 20000u)
+                : mbar_try_wait_sleep(bar, parity, 20000u))
+      return true;
+    if ((it & 7u) == 7u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Drain wait used on the way out: ignores the abort flag.
+static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Masks 32 consecutive scores (log2 domain) of one row: keys past the end,
+// keys beyond the causal limit, and the caller's bool/additive mask.
+__device__ __forceinline__ void apply_mask32(float* x, int key0, int kv_len, bool causal,
+                                             long long row_limit, const uint8_t* mrow,
+                                             long long mk, int mask_kind, bool fp16) {
+  const float LOG2E = 1.4426950408889634f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const int key = key0 + c;
+    bool vis = key < kv_len && (!causal || (long long)key <= row_limit);
+    float add = 0.f;
+    if (vis && mrow != nullptr) {
+      const long long e = (long long)key * mk;
+      if (mask_kind == FFPA_MASK_BOOL) {
+        vis = mrow[e] != 0;
+      } else if (mask_kind == FFPA_MASK_ADD_F32) {
+        add = reinterpret_cast<const float*>(mrow)[e] * LOG2E;
+      } else {
+        const uint16_t hbits = reinterpret_cast<const uint16_t*>(mrow)[e];
+        const float hv = fp16 ? __half2float(__ushort_as_half(hbits))
+                              : __bfloat162float(__ushort_as_bfloat16(hbits));
+        add = hv * LOG2E;
+      }
+    }
+    x[c] = vis ? x[c] + add : -INFINITY;
+  }
+}
+
+// Epilogue of one row: O (TMEM columns [0, it.dv), or zeros when no key
+// tile was visited) scaled by 1/l, written as 16-bit values to the output
+// columns [it.col_lo, it.col_lo + it.dv); the LSE by the CTA of slice 0.
+template <bool VARLEN>
+__device__ __forceinline__ void store_output(const Params& p, const Item& it, bool have_o,
+                                             uint32_t lane_base, int row, bool row_valid,
+                                             float l_sum, float m_ref) {
+  const bool fp16 = p.fp16 != 0;
+  const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+  uint8_t* obase = nullptr;
+  if (row_valid) {
+    long long off;
+    if (VARLEN)
+      off = (long long)(it.q_row0 + row) * p.o_str[0] + (long long)it.hq * p.o_str[1];
+    else
+      off = (long long)it.b * p.o_str[0] + (long long)it.hq * p.o_str[1] +
+            (long long)row * p.o_str[2];
+    obase = static_cast<uint8_t*>(p.o) + (off + it.col_lo) * 2;
+  }
+  for (int c0 = 0; c0 < it.dv; c0 += 32) {
+    uint32_t o[32];
+    if (have_o) {
+      tmem_ld32(lane_base + c0, o);
+      tmem_wait_ld();
+      reg_fence(o);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) o[c] = 0u;
+    }
+    uint32_t pkd[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float a0 = __uint_as_float(o[2 * c]) * inv_l;
+      const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
+      pkd[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+    }
+    if (row_valid) {
+      uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4)
+        dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+    }
+  }
+  if (row_valid && p.lse != nullptr && it.slice == 0) {
+    const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+    long long li;
+    if (VARLEN)
+      li = (long long)it.hq * p.Tq + it.q_row0 + row;
+    else
+      li = ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
+    p.lse[li] = lse;
+  }
+}
+
+// P = exp2(x * xs - base) for n scores, packed to 16-bit pairs; returns the
+// sum of the (unrounded) values.
+template <bool F16, int N>
+__device__ __forceinline__ float form_p(const float* x, float xs, float base, uint32_t* pk) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+  for (int c = 0; c < N; c += 4) {
+    const float e0 = ex2_approx(fmaf(x[c], xs, -base));
+    const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
+    const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
+    const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
+    s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+    pk[c / 2] = F16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
+    pk[c / 2 + 1] = F16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
+  }
+  return (s0 + s1) + (s2 + s3);
+}
+
+// Barrier addresses seen by the softmax warps.  The arrive addresses are
+// shared::cluster addresses (the leader CTA's barriers) in pair mode and
+// plain shared-memory addresses of this CTA otherwise.
+// The two-entry barrier arrays are consecutive 8-byte objects, so entry b
+// sits at base + 8 b.
+struct SoftmaxBars {
+  uint32_t s_full;
+  uint32_t s_free_arrive;
+  uint32_t p_full_arrive;   // entry 0 of p_full[2]
+  uint32_t pv_done;         // entry 0 of pv_done[2]
+};
+
+// The softmax arrivals follow tcgen05.wait::ld (S read into registers) or
+// tcgen05.wait::st + tcgen05.fence (P written to TMEM); no generic-memory
+// write has to become visible, so the pair form is a relaxed arrive (a
+// cluster-scope release costs ~1000 cycles on this critical path).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_to(uint32_t addr) {
+  if (PAIR)
+    mbar_arrive_cluster_relaxed(addr);
+  else
+    mbar_arrive(addr);
+}
+
+// Softmax warps 0-3 and the epilogue: thread r owns query row it.q0 + r,
+// which is TMEM lane r of this CTA.
+template <bool VARLEN, bool PAIR>
+__device__ __forceinline__ void softmax_role(const Params& p, const Item& it, int T, uint32_t tmem,
+                                             int warp, int lane, const SoftmaxBars bars,
+                                             volatile int* abort_flag, unsigned long long tmo) {
+  const int mask_kind = p.mask_kind;
+  const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
+  const float scale_log2 = p.scale_log2;
+    // ------------------------------------------------------------ softmax
+  const int r = warp * 32 + lane;                 // row within the tile = TMEM lane
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int row = it.q0 + r;                      // row within the sequence
+  const bool row_valid = row < it.q_len;
+  const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
+  const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
+  const uint8_t* mrow = nullptr;
+  if (mask_kind != FFPA_MASK_NONE && row_valid) {
+    const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
+    const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
+                          (long long)row * p.m_str[2];
+    mrow = static_cast<const uint8_t*>(p.mask) + off * (long long)esz;
+  }
+  const long long mk = p.m_str[3];
+  // Scores stay unscaled (x = q.k) when possible, so that the exponent
+  // x*scale*log2(e) - m is one FFMA; additive masks (or a scale <= 0, which
+  // reverses the max) need x pre-scaled into the log2 domain.
+  const bool prescale = mask_kind == FFPA_MASK_ADD_F32 || mask_kind == FFPA_MASK_ADD_QTYPE ||
+                        !(scale_log2 > 0.f);
+  const float xs = prescale ? 1.f : scale_log2;
+  const float ld_scale = prescale ? scale_log2 : 1.f;
+  float m_ref = -INFINITY;
+  float l_sum = 0.f;
+  bool ok = true;
+  for (int j = 0; j < T; ++j) {
+    const int b = j & 1;
+    bool w = wait_bounded(bars.s_full, j & 1, abort_flag, tmo);
+    ok = __all_sync(0xffffffffu, w);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t s_addr = lane_base + S_COL;
+    const uint32_t p_addr = lane_base + P_COL0 + 64 * b;
+    const int kbase = kv_tile(it, j) * BN;
+    const bool need_mask = (kbase + BN > it.kv_len) ||
+                           (causal && (long long)kbase + BN - 1 > first_limit) ||
+                           mask_kind != FFPA_MASK_NONE;
+    float x[BN];
+    {
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(s_addr, r0);
+      tmem_ld32(s_addr + 32, r1);
+      tmem_ld32(s_addr + 64, r2);
+      tmem_ld32(s_addr + 96, r3);
+      tmem_wait_ld();
+      reg_fence(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
+      // S has been read into registers: the next QK may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_to<PAIR>(bars.s_free_arrive);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        x[c] = __uint_as_float(r0[c]) * ld_scale;
+        x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
+        x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
+        x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
+      }
+    }
+    if (need_mask) {
+#pragma unroll
+      for (int q4 = 0; q4 < BN / 32; ++q4)
+        apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
+                     mask_kind, fp16);
+    }
+    float mx;
+    {   // tree maximum: eight independent chains, then combine
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < BN; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[c + i]);
+      mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      mx *= xs;   // into the log2 domain (-inf stays -inf: xs > 0)
+    }
+    bool resc = false;
+    float alpha = 1.f;
+    if (mx > m_ref + RESCALE_LOG2) {
+      if (m_ref != -INFINITY) {
+        resc = true;
+        alpha = ex2_approx(m_ref - mx);
+      }
+      m_ref = mx;
+    }
+    if (__any_sync(0xffffffffu, resc)) {
+      // O holds PV up to tile j-1: wait for it, then scale this warp's rows.
+      w = wait_bounded(bars.pv_done + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < it.dv; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + c0, o);
+        tmem_wait_ld();
+        reg_fence(o);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+        tmem_st32(lane_base + c0, o);
+      }
+    }
+    if (j >= 2) {   // P buffer b was read by PV_{j-2}
+      w = wait_bounded(bars.pv_done + 8u * b, ((j - 2) >> 1) & 1, abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+    }
+    // P = exp2(x - m_ref) in 16-bit, into P buffer b.
+    const float base = m_ref == -INFINITY ? 0.f : m_ref;
+    float psum = 0.f;
+#pragma unroll
+    for (int g = 0; g < BN / 32; ++g) {
+      uint32_t pk[16];
+      psum += fp16 ? form_p<true, 32>(x + 32 * g, xs, base, pk)
+                   : form_p<false, 32>(x + 32 * g, xs, base, pk);
+      tmem_st16(p_addr + 16 * g, pk);
+    }
+    l_sum = l_sum * alpha + psum;
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_to<PAIR>(bars.p_full_arrive + 8u * b);
+  }
+  // ------------------------------------------------------------ epilogue
+  if (ok && T > 0) {
+    const bool w = wait_bounded(bars.pv_done + 8u * ((T - 1) & 1), ((T - 1) >> 1) & 1,
+                                abort_flag, tmo);
+    ok = __all_sync(0xffffffffu, w);
+    if (ok) tc_fence_after();
+  }
+  if (ok || T == 0) store_output<VARLEN>(p, it, T > 0, lane_base, row, row_valid, l_sum, m_ref);
+}
+
+}  // namespace ffpa
