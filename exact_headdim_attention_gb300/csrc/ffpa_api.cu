@@ -208,9 +208,10 @@ size_t plan_pair(int D, Params* P) {
 
 ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size_t smem,
                           cudaStream_t stream) {
-  if (kn == Kern::PAIR) return launch_pair(varlen, P, items, smem, stream);
-  if (kn == Kern::SPLIT) return launch_split(varlen, P, items, smem, stream);
-  return launch_single(varlen, P, items, smem, stream);
+  const bool umask = P.mask != nullptr;
+  if (kn == Kern::PAIR) return launch_pair(varlen, umask, P, items, smem, stream);
+  if (kn == Kern::SPLIT) return launch_split(varlen, umask, P, items, smem, stream);
+  return launch_single(varlen, umask, P, items, smem, stream);
 }
 
 size_t plan_for(Kern kn, int D, Params* P) {

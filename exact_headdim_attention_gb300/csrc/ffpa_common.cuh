@@ -81,9 +81,9 @@ static __device__ int g_err_word;
 // Launches of the three kernels (one translation unit each) and their
 // device status words.
 struct Params;
-ffpa_status launch_single(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
-ffpa_status launch_pair(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
-ffpa_status launch_split(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 // Reads the unit's status word into *word and clears it (FFPA_ERR_CUDA if
 // the copy fails).
 ffpa_status take_err_single(int* word);
@@ -215,17 +215,68 @@ static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, un
 }
 
 // Masks 32 consecutive scores (log2 domain) of one row: keys past the end,
-// keys beyond the causal limit, and the caller's bool/additive mask.
+// keys beyond the causal limit, and (UMASK) the caller's bool/additive mask.
+// Kernels launched without a mask are instantiated with UMASK = false and
+// carry none of the mask-loading code.  With a mask, 32 entries that are
+// contiguous, in range and 16-byte aligned are read with 16-byte loads (8
+// for fp32, 4 for 16-bit, 2 for bool); otherwise entry by entry, only for
+// keys that are still visible.
+template <bool UMASK>
 __device__ __forceinline__ void apply_mask32(float* x, int key0, int kv_len, bool causal,
                                              long long row_limit, const uint8_t* mrow,
                                              long long mk, int mask_kind, bool fp16) {
   const float LOG2E = 1.4426950408889634f;
+  if (UMASK && mrow != nullptr && mk == 1 && key0 + 32 <= kv_len) {
+    const int esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
+    const uint8_t* mp = mrow + (long long)key0 * esz;
+    if ((reinterpret_cast<uintptr_t>(mp) & 15u) == 0) {
+      const uint4* m4 = reinterpret_cast<const uint4*>(mp);
+      if (mask_kind == FFPA_MASK_ADD_F32) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w = __ldg(m4 + v);
+          x[4 * v] += __uint_as_float(w.x) * LOG2E;
+          x[4 * v + 1] += __uint_as_float(w.y) * LOG2E;
+          x[4 * v + 2] += __uint_as_float(w.z) * LOG2E;
+          x[4 * v + 3] += __uint_as_float(w.w) * LOG2E;
+        }
+      } else if (mask_kind == FFPA_MASK_BOOL) {
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          const uint4 w = __ldg(m4 + v);
+          const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int b = 0; b < 16; ++b)
+            if (((wd[b >> 2] >> (8 * (b & 3))) & 0xffu) == 0u) x[16 * v + b] = -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w = __ldg(m4 + v);
+          const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const uint16_t hbits = (uint16_t)(wd[b >> 1] >> (16 * (b & 1)));
+            const float hv = fp16 ? __half2float(__ushort_as_half(hbits))
+                                  : __bfloat162float(__ushort_as_bfloat16(hbits));
+            x[8 * v + b] += hv * LOG2E;
+          }
+        }
+      }
+      if (causal) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if ((long long)(key0 + c) > row_limit) x[c] = -INFINITY;
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const int key = key0 + c;
     bool vis = key < kv_len && (!causal || (long long)key <= row_limit);
     float add = 0.f;
-    if (vis && mrow != nullptr) {
+    if (UMASK && vis && mrow != nullptr) {
       const long long e = (long long)key * mk;
       if (mask_kind == FFPA_MASK_BOOL) {
         vis = mrow[e] != 0;
@@ -340,7 +391,7 @@ __device__ __forceinline__ void arrive_to(uint32_t addr) {
 
 // Softmax warps 0-3 and the epilogue: thread r owns query row it.q0 + r,
 // which is TMEM lane r of this CTA.
-template <bool VARLEN, bool PAIR>
+template <bool VARLEN, bool PAIR, bool UMASK>
 __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, int T, uint32_t tmem,
                                              int warp, int lane, const SoftmaxBars bars,
                                              volatile int* abort_flag, unsigned long long tmo) {
@@ -355,7 +406,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
   const long long row_limit = (long long)row + (it.kv_len - it.q_len);   // causal
   const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
   const uint8_t* mrow = nullptr;
-  if (mask_kind != FFPA_MASK_NONE && row_valid) {
+  if (UMASK && mask_kind != FFPA_MASK_NONE && row_valid) {
     const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
     const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
                           (long long)row * p.m_str[2];
@@ -410,9 +461,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
     }
     if (need_mask) {
 #pragma unroll
-      for (int q4 = 0; q4 < BN / 32; ++q4)
-        apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
-                     mask_kind, fp16);
+      for (int q4 = 0; q4 < BN / 32; ++q4) {
+        apply_mask32<UMASK>(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
+                            mask_kind, fp16);
+        // One 32-key group at a time: keeps the mask loads of later groups
+        // from being hoisted (register pressure).
+        if (UMASK) asm volatile("" ::: "memory");
+      }
     }
     float mx;
     {   // tree maximum: eight independent chains, then combine

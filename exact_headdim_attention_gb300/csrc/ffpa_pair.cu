@@ -64,7 +64,7 @@ __device__ __forceinline__ bool decode_item_pair(const Params& p, bool varlen, i
 }
 
 // NCH = D / 64 as a template parameter: the MMA issue loops unroll.
-template <bool VARLEN, int NCH>
+template <bool VARLEN, int NCH, bool UMASK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     ffpa_fwd_pair_kernel(const __grid_constant__ Params p) {
   const uint32_t rank = cluster_ctarank();
@@ -318,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     bars.s_free_arrive = mapa_shared(smem_u32(&bar_s_free), 0);
     bars.p_full_arrive = mapa_shared(smem_u32(&bar_p_full[0]), 0);
     bars.pv_done = smem_u32(&bar_pv_done[0]);
-    softmax_role<VARLEN, true>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
+    softmax_role<VARLEN, true, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
   }
 
   // The leader's last commits also arrive in the peer: wait for them before
@@ -337,11 +337,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool UMASK>
 static ffpa_status launch_pair_t(const Params& P, int items, size_t smem, cudaStream_t stream) {
-  auto kern = P.nchunks == 8   ? ffpa_fwd_pair_kernel<VARLEN, 8>
-              : P.nchunks == 4 ? ffpa_fwd_pair_kernel<VARLEN, 4>
-                               : ffpa_fwd_pair_kernel<VARLEN, 2>;
+  auto kern = P.nchunks == 8   ? ffpa_fwd_pair_kernel<VARLEN, 8, UMASK>
+              : P.nchunks == 4 ? ffpa_fwd_pair_kernel<VARLEN, 4, UMASK>
+                               : ffpa_fwd_pair_kernel<VARLEN, 2, UMASK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;
@@ -349,9 +349,11 @@ static ffpa_status launch_pair_t(const Params& P, int items, size_t smem, cudaSt
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
-ffpa_status launch_pair(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream) {
-  return varlen ? launch_pair_t<true>(P, items, smem, stream)
-                : launch_pair_t<false>(P, items, smem, stream);
+ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem,
+                        cudaStream_t stream) {
+  return varlen  ? launch_pair_t<true, false>(P, items, smem, stream)
+         : umask ? launch_pair_t<false, true>(P, items, smem, stream)
+                 : launch_pair_t<false, false>(P, items, smem, stream);
 }
 
 ffpa_status take_err_pair(int* word) {

@@ -3,7 +3,8 @@
 
 namespace ffpa {
 
-template <bool VARLEN>
+// UMASK: launched with a caller's mask (mask-loading code present).
+template <bool VARLEN, bool UMASK>
 __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_constant__ Params p) {
   Item it;
   if (!decode_item(p, VARLEN, blockIdx.x, it)) return;   // uniform across the CTA
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     bars.s_free_arrive = smem_u32(&bar_s_free);
     bars.p_full_arrive = smem_u32(&bar_p_full[0]);
     bars.pv_done = smem_u32(&bar_pv_done[0]);
-    softmax_role<VARLEN, false>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
+    softmax_role<VARLEN, false, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
   }
 
   tc_fence_before();
@@ -287,8 +288,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   }
 }
 
-ffpa_status launch_single(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream) {
-  auto kern = varlen ? ffpa_fwd_kernel<true> : ffpa_fwd_kernel<false>;
+ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, size_t smem,
+                          cudaStream_t stream) {
+  auto kern = varlen  ? ffpa_fwd_kernel<true, false>
+              : umask ? ffpa_fwd_kernel<false, true>
+                      : ffpa_fwd_kernel<false, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;

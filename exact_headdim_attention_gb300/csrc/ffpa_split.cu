@@ -30,7 +30,7 @@ namespace ffpa {
 // compile-time trip count and is fully unrolled: the tensor pipe's
 // instruction queue is shallow, and loop overhead between MMAs leaves it
 // idle (measured: a runtime-count loop of 8 MMAs runs at about half rate).
-template <bool VARLEN, int NCH>
+template <bool VARLEN, int NCH, bool UMASK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     ffpa_fwd_split_kernel(const __grid_constant__ Params p) {
   const uint32_t rank = cluster_ctarank();
@@ -302,7 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     const long long row_limit = (long long)row + (it.kv_len - it.q_len);
     const long long first_limit = (long long)it.q0 + (it.kv_len - it.q_len);
     const uint8_t* mrow = nullptr;
-    if (mask_kind != FFPA_MASK_NONE && row_valid) {
+    if (UMASK && mask_kind != FFPA_MASK_NONE && row_valid) {
       const size_t esz = mask_kind == FFPA_MASK_BOOL ? 1 : mask_kind == FFPA_MASK_ADD_F32 ? 4 : 2;
       const long long off = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
                             (long long)row * p.m_str[2];
@@ -390,9 +390,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         }
         if (need_mask) {
 #pragma unroll
-          for (int q4 = 0; q4 < BN / 32; ++q4)
-            apply_mask32(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow, mk,
-                         mask_kind, fp16);
+          for (int q4 = 0; q4 < BN / 32; ++q4) {
+            apply_mask32<UMASK>(x + 32 * q4, kbase + 32 * q4, it.kv_len, causal, row_limit, mrow,
+                                mk, mask_kind, fp16);
+            if (UMASK) asm volatile("" ::: "memory");
+          }
         }
         float m8[8];
 #pragma unroll
@@ -528,12 +530,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
   }
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool UMASK>
 static ffpa_status launch_split_t(const Params& P, int items, size_t smem, cudaStream_t stream) {
-  auto kern = P.nchunks == 8   ? ffpa_fwd_split_kernel<VARLEN, 8>
-              : P.nchunks == 6 ? ffpa_fwd_split_kernel<VARLEN, 6>
-              : P.nchunks == 4 ? ffpa_fwd_split_kernel<VARLEN, 4>
-                               : ffpa_fwd_split_kernel<VARLEN, 2>;
+  auto kern = P.nchunks == 8   ? ffpa_fwd_split_kernel<VARLEN, 8, UMASK>
+              : P.nchunks == 6 ? ffpa_fwd_split_kernel<VARLEN, 6, UMASK>
+              : P.nchunks == 4 ? ffpa_fwd_split_kernel<VARLEN, 4, UMASK>
+                               : ffpa_fwd_split_kernel<VARLEN, 2, UMASK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_LIMIT - SPLIT_STATIC_RESERVE)) != cudaSuccess)
     return FFPA_ERR_CUDA;
@@ -541,9 +543,11 @@ static ffpa_status launch_split_t(const Params& P, int items, size_t smem, cudaS
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
-ffpa_status launch_split(bool varlen, const Params& P, int items, size_t smem, cudaStream_t stream) {
-  return varlen ? launch_split_t<true>(P, items, smem, stream)
-                : launch_split_t<false>(P, items, smem, stream);
+ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem,
+                         cudaStream_t stream) {
+  return varlen  ? launch_split_t<true, false>(P, items, smem, stream)
+         : umask ? launch_split_t<false, true>(P, items, smem, stream)
+                 : launch_split_t<false, false>(P, items, smem, stream);
 }
 
 ffpa_status take_err_split(int* word) {
