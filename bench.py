@@ -315,9 +315,10 @@ def run_ours(args):
         raise SystemExit(f"device error: {pkg.ffpa_status_string(st)}")
     peak, peak_src, peak_sustained = read_peaks()
     kname = pkg.selected_kernel(w.D, w.varlen)
-    kernel = {"single": f"ffpa_fwd_kernel<{str(w.varlen).lower()}>",
-              "pair": f"ffpa_fwd_pair_kernel<{str(w.varlen).lower()}, {w.D // 64}>",
-              "split": f"ffpa_fwd_split_kernel<{str(w.varlen).lower()}, {w.D // 64}>"}[kname]
+    vl, um = str(w.varlen).lower(), str(x.get("mask") is not None).lower()
+    kernel = {"single": f"ffpa_fwd_kernel<{vl}, {um}>",
+              "pair": f"ffpa_fwd_pair_kernel<{vl}, {w.D // 64}, {um}>",
+              "split": f"ffpa_fwd_split_kernel<{vl}, {w.D // 64}, {um}>"}[kname]
     per_launch_s = elapsed / args.steps
     achieved = flops / per_launch_s / 1e12
     line = {
