@@ -14,7 +14,8 @@ pages' convention 4*B*Hq*Nq*Nkv*D (halved when causal).
   events on the launching stream, bracketed by barrier + synchronize; the
   inputs (256 MiB) are larger than the 129 MB L2.
 * e2e: the same metric through the public API with pinned host buffers:
-  every step copies Q, K, V host->device and O device->host.
+  every step copies Q, K, V host->device and O device->host; consecutive
+  steps overlap on three streams (copy in / forward / copy out).
 * roofline: the kernel against the dense bf16 tensor peak
   (MEASURED_PEAKS.json when present, else a recorded fallback).
 * cpu_baseline: the float64 oracle on a bounded, seeded sample of rows of
@@ -170,7 +171,16 @@ def gpu_id_for(device_index: int) -> str:
 
 # --------------------------------------------------------------- our arm
 def make_step(w, x, dev):
-    """Returns (device_step, e2e_step, bytes_h2d, bytes_d2h, flops)."""
+    """Returns (device_step, e2e_step, e2e_start, e2e_finish, bytes_h2d, bytes_d2h, flops).
+
+    device_step: one forward on device-resident inputs (torch's current stream).
+    e2e_step: one end-to-end step through the public API: H2D copy of Q, K, V
+    from pinned host memory, the forward, D2H copy of O into pinned host
+    memory.  Consecutive steps are pipelined over three streams (copy in,
+    compute, copy out) and two sets of device buffers, so step i's copies
+    overlap step i-1's kernel; every step still moves all of its bytes.
+    e2e_start / e2e_finish: make the pipeline's streams wait for torch's
+    current stream / the current stream wait for all issued steps."""
     import torch
     import exact_headdim_attention_gb300 as pkg
     from exact_headdim_attention_gb300 import workloads as wl
@@ -178,38 +188,79 @@ def make_step(w, x, dev):
     names = ("q", "k", "v")
     host = {n: x[n].pin_memory() for n in names}
     devt = {n: host[n].to(dev, non_blocking=False) for n in names}
-    if w.varlen:
-        cq = x["cu_q"].to(dev)
-        out = torch.empty_like(devt["q"])
-        lse = torch.empty(w.Hq, x["q"].shape[0], dtype=torch.float32, device=dev)
-        flops = wl.useful_flops(w, x["seqlens"])
+    mask = None if w.varlen or x.get("mask") is None else x["mask"].to(dev)
+    cq = x["cu_q"].to(dev) if w.varlen else None
+    flops = wl.useful_flops(w, x["seqlens"]) if w.varlen else wl.useful_flops(w)
 
-        def call():
-            pkg.ffpa_fwd_varlen(devt["q"], devt["k"], devt["v"], cq, None, x["max_q"], x["max_k"],
+    def forward(ins, out, lse, stream=None):
+        if w.varlen:
+            pkg.ffpa_fwd_varlen(ins["q"], ins["k"], ins["v"], cq, None, x["max_q"], x["max_k"],
                                 causal=w.causal, enable_gqa=w.enable_gqa, return_lse=True,
-                                out=out, lse=lse)
-    else:
-        mask = None if x.get("mask") is None else x["mask"].to(dev)
-        out = torch.empty_like(devt["q"])
-        flops = wl.useful_flops(w)
+                                out=out, lse=lse, stream=stream)
+        else:
+            pkg.ffpa_fwd(ins["q"], ins["k"], ins["v"], attn_mask=mask, is_causal=w.causal,
+                         enable_gqa=w.enable_gqa, out=out, stream=stream)
 
-        def call():
-            pkg.ffpa_fwd(devt["q"], devt["k"], devt["v"], attn_mask=mask, is_causal=w.causal,
-                         enable_gqa=w.enable_gqa, out=out)
-    o_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    def new_lse():
+        return (torch.empty(w.Hq, x["q"].shape[0], dtype=torch.float32, device=dev)
+                if w.varlen else None)
+
+    out = torch.empty_like(devt["q"])
+    lse = new_lse()
+
+    def call():
+        forward(devt, out, lse)
+
+    # end to end: two buffer sets, three streams
+    s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ins = [devt, {n: torch.empty_like(devt[n]) for n in names}]
+    outs = [out, torch.empty_like(out)]
+    lses = [lse, new_lse()]
+    o_host = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer b landed
+    ev_c = [torch.cuda.Event() for _ in range(2)]       # forward on buffer b done
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # O of buffer b copied out
+    state = {"i": 0}
 
     def e2e():
-        for n in names:
-            devt[n].copy_(host[n], non_blocking=True)
-        call()
-        o_host.copy_(out, non_blocking=True)
+        b = state["i"] & 1
+        if state["i"] >= 2:
+            s_in.wait_event(ev_c[b])          # the forward of step i-2 has read buffer b
+        with torch.cuda.stream(s_in):
+            for n in names:
+                ins[b][n].copy_(host[n], non_blocking=True)
+        ev_in[b].record(s_in)
+        s_c.wait_event(ev_in[b])
+        if state["i"] >= 2:
+            s_c.wait_event(ev_out[b])         # O of step i-2 has left buffer b
+        forward(ins[b], outs[b], lses[b], stream=s_c)
+        ev_c[b].record(s_c)
+        s_out.wait_event(ev_c[b])
+        with torch.cuda.stream(s_out):
+            o_host[b].copy_(outs[b], non_blocking=True)
+        ev_out[b].record(s_out)
+        state["i"] += 1
+
+    def e2e_finish():
+        cur = torch.cuda.current_stream(dev)
+        for st in (s_in, s_c, s_out):
+            cur.wait_stream(st)
+
+    def e2e_start():
+        cur = torch.cuda.current_stream(dev)
+        for st in (s_in, s_c, s_out):
+            st.wait_stream(cur)
 
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = o_host.numel() * o_host.element_size()
-    return call, e2e, h2d, d2h, flops
+    d2h = o_host[0].numel() * o_host[0].element_size()
+    return call, e2e, e2e_start, e2e_finish, h2d, d2h, flops
 
 
-def time_steps(fn, steps, dist_on):
+def time_steps(fn, steps, dist_on, finish=None, start=None):
+    """Device time of `steps` calls of fn: CUDA events on torch's current
+    stream, bracketed by a barrier and a synchronize.  When fn issues work on
+    other streams, `start` makes them wait for the start event and `finish`
+    makes the current stream wait for them before the end event."""
     import torch
     import torch.distributed as dist
     s = torch.cuda.Event(enable_timing=True)
@@ -219,8 +270,12 @@ def time_steps(fn, steps, dist_on):
     torch.cuda.synchronize()
     t0 = time.monotonic()
     s.record()
+    if start is not None:
+        start()
     for _ in range(steps):
         fn()
+    if finish is not None:
+        finish()
     e.record()
     torch.cuda.synchronize()
     t1 = time.monotonic()
@@ -290,7 +345,7 @@ def run_ours(args):
     pkg.load_library()
     w = workload_by_name(args.workload)
     x = wl.materialize(w)
-    step, e2e, h2d, d2h, flops = make_step(w, x, dev)
+    step, e2e, e2e_start, e2e_finish, h2d, d2h, flops = make_step(w, x, dev)
     assert args.warmup >= 3, "at least 3 warm-up steps"
     for _ in range(args.warmup):
         step()
@@ -307,8 +362,9 @@ def run_ours(args):
     # end to end through the public API with host buffers
     for _ in range(3):
         e2e()
+    e2e_finish()
     n_e2e = max(3, min(args.e2e_steps, args.steps))
-    e_el, _, _ = time_steps(e2e, n_e2e, dist_on)
+    e_el, _, _ = time_steps(e2e, n_e2e, dist_on, finish=e2e_finish, start=e2e_start)
     e_value, _ = aggregate(e_el, flops, n_e2e, world, dist_on, dev)
     st = pkg.ffpa_last_device_error()
     if st != pkg.FFPA_OK:
@@ -336,7 +392,9 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                "api": "exact_headdim_attention_gb300.ffpa_fwd (C ABI ffpa_fwd)"},
+                "api": "exact_headdim_attention_gb300.ffpa_fwd (C ABI ffpa_fwd)",
+                "pipelining": "copy-in, forward and copy-out of consecutive steps on three "
+                              "streams with two buffer sets"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "impl": "ours",
