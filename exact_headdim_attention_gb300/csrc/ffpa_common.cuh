@@ -169,9 +169,13 @@ __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L,
     kv_end = min(kv_end, last_visible + 1);
   }
   it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
-  it.rot = it.ntiles > 0 ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
-                                 (unsigned)it.ntiles)
-                         : 0;
+  // Dense causal items all start at key tile 0 (measured on GB300, causal
+  // GQA D=512: 1032 vs 921 TFLOPS); otherwise the start is spread (non-causal
+  // D=512: 1164 vs 1132; varlen: 676 vs 650).
+  it.rot = (it.ntiles > 0 && !(p.causal && !varlen))
+               ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
+                       (unsigned)it.ntiles)
+               : 0;
   const int c_lo = it.slice * p.nchunks / p.n_slices;
   const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
   it.col_lo = c_lo * DK;

@@ -53,9 +53,11 @@ __device__ __forceinline__ bool decode_item_pair(const Params& p, bool varlen, i
   long long kv_end = it.kv_len;
   if (p.causal) kv_end = min(kv_end, (long long)last_row + (it.kv_len - it.q_len) + 1);
   it.ntiles = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
-  it.rot = it.ntiles > 0 ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
-                                 (unsigned)it.ntiles)
-                         : 0;
+  // As decode_item: dense causal items start at key tile 0.
+  it.rot = (it.ntiles > 0 && !(p.causal && !varlen))
+               ? (int)(((unsigned)qt * 37u + (unsigned)it.slice * 17u + (unsigned)it.hq * 13u) %
+                       (unsigned)it.ntiles)
+               : 0;
   const int c_lo = it.slice * p.nchunks / p.n_slices;
   const int c_hi = (it.slice + 1) * p.nchunks / p.n_slices;
   it.col_lo = c_lo * DK;
