@@ -352,17 +352,22 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
 }
 
 // P = exp2(x * xs - base) for n scores, packed to 16-bit pairs; returns the
-// sum of the (unrounded) values.
+// sum of the (unrounded) values.  The exponent arguments and the partial
+// sums use packed fp32 pair instructions.
 template <bool F16, int N>
 __device__ __forceinline__ float form_p(const float* x, float xs, float base, uint32_t* pk) {
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
   for (int c = 0; c < N; c += 4) {
-    const float e0 = ex2_approx(fmaf(x[c], xs, -base));
-    const float e1 = ex2_approx(fmaf(x[c + 1], xs, -base));
-    const float e2 = ex2_approx(fmaf(x[c + 2], xs, -base));
-    const float e3 = ex2_approx(fmaf(x[c + 3], xs, -base));
-    s0 += e0; s1 += e1; s2 += e2; s3 += e3;
+    float a0, a1, a2, a3;
+    ffma2_bc(x[c], x[c + 1], xs, -base, a0, a1);
+    ffma2_bc(x[c + 2], x[c + 3], xs, -base, a2, a3);
+    const float e0 = ex2_approx(a0);
+    const float e1 = ex2_approx(a1);
+    const float e2 = ex2_approx(a2);
+    const float e3 = ex2_approx(a3);
+    fadd2_acc(s0, s1, e0, e1);
+    fadd2_acc(s2, s3, e2, e3);
     pk[c / 2] = F16 ? pack_f16(e0, e1) : pack_bf16(e0, e1);
     pk[c / 2 + 1] = F16 ? pack_f16(e2, e3) : pack_bf16(e2, e3);
   }
@@ -457,10 +462,14 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
       if (lane == 0) arrive_to<PAIR>(bars.s_free_arrive);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        x[c] = __uint_as_float(r0[c]) * ld_scale;
-        x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
-        x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
-        x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
+        x[c] = __uint_as_float(r0[c]);
+        x[32 + c] = __uint_as_float(r1[c]);
+        x[64 + c] = __uint_as_float(r2[c]);
+        x[96 + c] = __uint_as_float(r3[c]);
+      }
+      if (prescale) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) x[c] *= ld_scale;
       }
     }
     if (need_mask) {

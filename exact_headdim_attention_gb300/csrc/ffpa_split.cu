@@ -382,10 +382,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
           if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            x[c] = __uint_as_float(r0[c]) * ld_scale;
-            x[32 + c] = __uint_as_float(r1[c]) * ld_scale;
-            x[64 + c] = __uint_as_float(r2[c]) * ld_scale;
-            x[96 + c] = __uint_as_float(r3[c]) * ld_scale;
+            x[c] = __uint_as_float(r0[c]);
+            x[32 + c] = __uint_as_float(r1[c]);
+            x[64 + c] = __uint_as_float(r2[c]);
+            x[96 + c] = __uint_as_float(r3[c]);
+          }
+          if (prescale) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c) x[c] *= ld_scale;
           }
         }
         if (need_mask) {

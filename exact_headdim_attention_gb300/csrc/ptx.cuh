@@ -76,6 +76,29 @@ __device__ __forceinline__ bool mbar_try_wait_sleep_cluster(uint32_t bar, uint32
   return ok != 0;
 }
 
+// Packed fp32 pair arithmetic (one instruction for two lanes of work).
+// (d0, d1) = (a0 * b + c, a1 * b + c)
+__device__ __forceinline__ void ffma2_bc(float a0, float a1, float b, float c, float& d0, float& d1) {
+  asm("{\n\t.reg .b64 ap, bp, cp, dp;\n\t"
+      "mov.b64 ap, {%2, %3};\n\t"
+      "mov.b64 bp, {%4, %4};\n\t"
+      "mov.b64 cp, {%5, %5};\n\t"
+      "fma.rn.f32x2 dp, ap, bp, cp;\n\t"
+      "mov.b64 {%0, %1}, dp;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (e0, e1)
+__device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float e0, float e1) {
+  asm("{\n\t.reg .b64 sp, ep;\n\t"
+      "mov.b64 sp, {%0, %1};\n\t"
+      "mov.b64 ep, {%2, %3};\n\t"
+      "add.rn.f32x2 sp, sp, ep;\n\t"
+      "mov.b64 {%0, %1}, sp;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(e0), "f"(e1));
+}
+
 // 16-byte shared-memory load / store by shared::cta address.
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
