@@ -351,6 +351,20 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
   }
 }
 
+// Maximum of n scores (n a multiple of 16): eight independent chains of
+// three-input maxima, then a small tree.
+template <int N>
+__device__ __forceinline__ float row_max(const float* x) {
+  float m8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m8[i] = fmaxf(x[i], x[8 + i]);
+#pragma unroll
+  for (int c = 16; c < N; c += 16)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m8[i] = fmax3(m8[i], x[c + i], x[c + 8 + i]);
+  return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
 // P = exp2(x * xs - base) for n scores, packed to 16-bit pairs; returns the
 // sum of the (unrounded) values.  The exponent arguments and the partial
 // sums use packed fp32 pair instructions.
@@ -482,19 +496,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
         if (UMASK) asm volatile("" ::: "memory");
       }
     }
-    float mx;
-    {   // tree maximum: eight independent chains, then combine
-      float m8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m8[i] = x[i];
-#pragma unroll
-      for (int c = 8; c < BN; c += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], x[c + i]);
-      mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      mx *= xs;   // into the log2 domain (-inf stays -inf: xs > 0)
-    }
+    const float mx = row_max<BN>(x) * xs;   // log2 domain (-inf stays -inf: xs > 0)
     bool resc = false;
     float alpha = 1.f;
     if (mx > m_ref + RESCALE_LOG2) {

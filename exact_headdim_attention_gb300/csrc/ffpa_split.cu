@@ -400,16 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
             if (UMASK) asm volatile("" ::: "memory");
           }
         }
-        float m8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) m8[u] = x[u];
-#pragma unroll
-        for (int c = 8; c < BN; c += 8)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], x[c + u]);
-        t = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        t *= xs;
+        t = row_max<BN>(x) * xs;
       }
       // Exchange the tile maxima: both CTAs then take the same decision.
       const int xb = i & 1;

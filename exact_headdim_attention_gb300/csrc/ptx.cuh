@@ -76,6 +76,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep_cluster(uint32_t bar, uint32
   return ok != 0;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 // (d0, d1) = (a0 * b + c, a1 * b + c)
 __device__ __forceinline__ void ffma2_bc(float a0, float a1, float b, float c, float& d0, float& d1) {
