@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for exact attention (forward) -- TEST INFRASTRUCTURE ONLY.
+"""Float64 CPU oracle for exact attention (forward and backward) -- TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product path (the CUDA library
@@ -56,6 +56,12 @@ class Oracle:
         self.lib.oracle_attn_dense.restype = I
         self.lib.oracle_attn_varlen.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, I, D, I, P, P, I]
         self.lib.oracle_attn_varlen.restype = I
+        self.lib.oracle_attn_bwd_dense.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P,
+                                                   D, I, P, P, P, I]
+        self.lib.oracle_attn_bwd_dense.restype = I
+        self.lib.oracle_attn_bwd_rows.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, D, I,
+                                                  P, L, P, L, P, P, P, I]
+        self.lib.oracle_attn_bwd_rows.restype = I
 
     # ------------------------------------------------------------------ dense
     def attn_dense(self, q, k, v, attn_mask=None, scale=None, is_causal=False, rows=None,
@@ -133,6 +139,81 @@ class Oracle:
         return o, lse
 
 
+    # --------------------------------------------------------------- backward
+    def attn_bwd_dense(self, q, k, v, dout, attn_mask=None, scale=None, is_causal=False,
+                       nthreads: int = 0):
+        """Gradients (dQ, dK, dV) in float64 of sum(O * dout) for the dense forward.
+
+        q, dout [B,Hq,Nq,D]; k, v [B,Hkv,Nkv,D]; same dtypes and mask rules as
+        attn_dense.  Returns dq [B,Hq,Nq,D], dk and dv [B,Hkv,Nkv,D]."""
+        dtype = _dtype_code(q)
+        assert k.dtype == q.dtype and v.dtype == q.dtype and dout.dtype == q.dtype
+        B, Hq, Nq, D = q.shape
+        _, Hkv, Nkv, _ = k.shape
+        assert dout.shape == q.shape
+        for t in (q, k, v, dout):
+            assert t.device.type == "cpu" and t.stride(-1) == 1
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
+        dq = torch.empty(B, Hq, Nq, D, dtype=torch.float64)
+        dk = torch.empty(B, Hkv, Nkv, D, dtype=torch.float64)
+        dv = torch.empty(B, Hkv, Nkv, D, dtype=torch.float64)
+        rc = self.lib.oracle_attn_bwd_dense(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dtype, B, Hq, Hkv, Nq, Nkv, D,
+            _strides(q), _strides(k), _strides(v), _strides(dout), mptr, mk, mstr, float(scale),
+            int(bool(is_causal)), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), nthreads)
+        del keep
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd_dense rejected its arguments")
+        return dq, dk, dv
+
+    def attn_bwd_rows(self, q, k, v, dout, q_rows, k_rows, scale=None, is_causal=False,
+                      nthreads: int = 0):
+        """Selected gradient rows (no mask): q_rows are flat ids (b*Hq+hq)*Nq+i of
+        dQ rows, k_rows flat ids (b*Hkv+hk)*Nkv+j of dK/dV rows.  Returns
+        (dq [len(q_rows),D], dk [len(k_rows),D], dv [len(k_rows),D]) in float64."""
+        dtype = _dtype_code(q)
+        B, Hq, Nq, D = q.shape
+        _, Hkv, Nkv, _ = k.shape
+        for t in (q, k, v, dout):
+            assert t.device.type == "cpu" and t.stride(-1) == 1
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        qr = torch.as_tensor(q_rows, dtype=torch.int64).contiguous()
+        kr = torch.as_tensor(k_rows, dtype=torch.int64).contiguous()
+        dq = torch.empty(qr.numel(), D, dtype=torch.float64)
+        dk = torch.empty(kr.numel(), D, dtype=torch.float64)
+        dv = torch.empty(kr.numel(), D, dtype=torch.float64)
+        rc = self.lib.oracle_attn_bwd_rows(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dtype, B, Hq, Hkv, Nq, Nkv, D,
+            _strides(q), _strides(k), _strides(v), _strides(dout), float(scale), int(bool(is_causal)),
+            qr.data_ptr(), qr.numel(), kr.data_ptr(), kr.numel(), dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), nthreads)
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd_rows rejected its arguments")
+        return dq, dk, dv
+
+
+def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
+    """(kind, pointer, strides, keep-alive) of a mask broadcast to [B,Hq,Nq,Nkv]."""
+    if attn_mask is None:
+        return MASK_NONE, None, (ctypes.c_int64 * 4)(0, 0, 0, 0), None
+    m = attn_mask
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    m = m.expand(B, Hq, Nq, Nkv)
+    if m.dtype == torch.bool:
+        mk = MASK_BOOL
+    elif m.dtype == torch.float32:
+        mk = MASK_F32
+    elif m.dtype == q.dtype:
+        mk = MASK_QTYPE
+    else:
+        raise TypeError(f"mask dtype {m.dtype} not supported")
+    return mk, m.data_ptr(), (ctypes.c_int64 * 4)(*m.stride()), m
+
+
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return BF16
@@ -161,6 +242,14 @@ def attn_dense(*a, **kw):
 
 def attn_varlen(*a, **kw):
     return default().attn_varlen(*a, **kw)
+
+
+def attn_bwd_dense(*a, **kw):
+    return default().attn_bwd_dense(*a, **kw)
+
+
+def attn_bwd_rows(*a, **kw):
+    return default().attn_bwd_rows(*a, **kw)
 
 
 def host_threads() -> int:

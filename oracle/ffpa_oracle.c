@@ -1,5 +1,6 @@
 /*
- * Float64 CPU oracle for exact scaled-dot-product attention (forward).
+ * Float64 CPU oracle for exact scaled-dot-product attention: the forward
+ * and, at the end of the file, its gradients.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
  * calls this file: only the tests, the package smoke check and the CPU
@@ -236,6 +237,264 @@ int oracle_attn_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v, 
                            0, limit, s, o + (t * Hq + hq) * D);
         }
         free(s);
+    }
+    return err ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ backward
+ *
+ * Gradients of the dense forward above (FFPA API reference,
+ * "ffpa_attn.ffpa_attn_func": "Backward pass is supported via
+ * FFPAAttnFunc"): for an upstream gradient dO of O, the derivatives of the
+ * scalar L = sum(O * dO) with respect to Q, K and V.  The pages give no
+ * formulas; these are the chain rule through the definition, per (batch,
+ * query head, row i) with P_i = softmax(s_i) the weights of row i:
+ *
+ *   O_i    = sum_j P_ij V_j                =>  dV_j += P_ij dO_i
+ *   dP_ij  = dO_i . V_j
+ *   dS_ij  = P_ij (dP_ij - sum_k P_ik dP_ik)    (Jacobian of the softmax)
+ *   s_ij   = scale q_i . k_j (+ mask)      =>  dQ_i  = scale sum_j dS_ij K_j
+ *                                              dK_j += scale dS_ij Q_i
+ *
+ * Query heads of one group read the same key/value head, so their dK and dV
+ * contributions add up there.  A masked score has P = 0 and contributes
+ * nothing; a fully masked row (no softmax) contributes nothing either.
+ */
+
+/* Row statistics of query row i: scores s[] (masked entries -inf), the
+ * weights P[] and dP[] over all keys, and returns sum_k P_k dP_k.  *dead is
+ * set when every key is masked (then P = 0). */
+static double grad_row(const uint16_t* qrow, const uint16_t* dorow, const uint16_t* kbase,
+                       const uint16_t* vbase, int64_t k_row_stride, int64_t v_row_stride, int n_keys,
+                       int D, int dtype, double scale, int mask_kind, const void* mask_row,
+                       int64_t mk_str, int64_t causal_limit, double* P, double* dP, int* dead) {
+    double m = -INFINITY;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        const uint16_t* krow = kbase + (int64_t)kk * k_row_stride;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += widen(qrow + d, dtype) * widen(krow + d, dtype);
+        double x = scale * dot;
+        if (mask_kind == ORACLE_MASK_BOOL) {
+            if (((const uint8_t*)mask_row)[kk * mk_str] == 0) x = -INFINITY;
+        } else if (mask_kind == ORACLE_MASK_F32) {
+            x += (double)((const float*)mask_row)[kk * mk_str];
+        } else if (mask_kind == ORACLE_MASK_QTYPE) {
+            x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);
+        }
+        if ((int64_t)kk > causal_limit) x = -INFINITY;
+        P[kk] = x;
+        if (x > m) m = x;
+    }
+    *dead = m == -INFINITY;
+    double l = 0.0;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        P[kk] = *dead ? 0.0 : exp(P[kk] - m);
+        l += P[kk];
+    }
+    double delta = 0.0;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        if (!*dead) P[kk] /= l;
+        const uint16_t* vrow = vbase + (int64_t)kk * v_row_stride;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += widen(dorow + d, dtype) * widen(vrow + d, dtype);
+        dP[kk] = dot;
+        delta += P[kk] * dot;
+    }
+    return delta;
+}
+
+/* Pointers of one dense row (b, hq, i): its query, upstream gradient, the
+ * key/value bases of its head and its mask row. */
+typedef struct {
+    const uint16_t *qrow, *dorow, *kb, *vb;
+    const void* mrow;
+    int64_t mk, limit;
+} dense_row;
+
+static dense_row dense_row_at(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              const uint16_t* dout, int Hq, int Hkv, int Nq, int Nkv,
+                              const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                              const int64_t* do_str, const void* mask, int mask_kind,
+                              const int64_t* m_str, int causal, int b, int hq, int64_t i) {
+    dense_row r;
+    int hk = hq / (Hq / Hkv);
+    r.qrow = q + b * q_str[0] + hq * q_str[1] + i * q_str[2];
+    r.dorow = dout + b * do_str[0] + hq * do_str[1] + i * do_str[2];
+    r.kb = k + b * k_str[0] + hk * k_str[1];
+    r.vb = v + b * v_str[0] + hk * v_str[1];
+    r.mrow = NULL;
+    r.mk = 0;
+    if (mask_kind != ORACLE_MASK_NONE) {
+        int64_t off = b * m_str[0] + hq * m_str[1] + i * m_str[2];
+        size_t esz = mask_kind == ORACLE_MASK_BOOL ? 1 : mask_kind == ORACLE_MASK_F32 ? 4 : 2;
+        r.mrow = (const char*)mask + off * (int64_t)esz;
+        r.mk = m_str[3];
+    }
+    r.limit = causal ? i + (int64_t)Nkv - Nq : (int64_t)Nkv - 1;
+    return r;
+}
+
+/*
+ * Full backward, dense layout.  dout has the layout of q (strides
+ * do_str[4]).  dq: [B, Hq, Nq, D]; dk, dv: [B, Hkv, Nkv, D]; all three
+ * contiguous float64.  One (batch, key/value head) per task, so the group's
+ * additions into dK and dV never race.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_attn_bwd_dense(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const uint16_t* dout, int dtype, int B, int Hq, int Hkv, int Nq, int Nkv,
+                          int D, const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                          const int64_t* do_str, const void* mask, int mask_kind,
+                          const int64_t* m_str, double scale, int causal, double* dq, double* dk,
+                          double* dv, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Nq < 0 || Nkv < 0 || D <= 0) return -1;
+    const int group = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+#pragma omp parallel
+    {
+        size_t n = (size_t)(Nkv > 0 ? Nkv : 1);
+        double* P = (double*)malloc(sizeof(double) * n);
+        double* dP = (double*)malloc(sizeof(double) * n);
+        if (!P || !dP) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < (int64_t)B * Hkv; ++u) {
+            if (!P || !dP) continue;
+            int b = (int)(u / Hkv), hk = (int)(u % Hkv);
+            double* dkh = dk + u * Nkv * (int64_t)D;
+            double* dvh = dv + u * Nkv * (int64_t)D;
+            for (int64_t e = 0; e < (int64_t)Nkv * D; ++e) dkh[e] = dvh[e] = 0.0;
+            for (int hq = hk * group; hq < (hk + 1) * group; ++hq) {
+                for (int64_t i = 0; i < Nq; ++i) {
+                    dense_row r = dense_row_at(q, k, v, dout, Hq, Hkv, Nq, Nkv, q_str, k_str, v_str,
+                                               do_str, mask, mask_kind, m_str, causal, b, hq, i);
+                    int dead;
+                    double delta = grad_row(r.qrow, r.dorow, r.kb, r.vb, k_str[2], v_str[2], Nkv, D,
+                                            dtype, scale, mask_kind, r.mrow, r.mk, r.limit, P, dP, &dead);
+                    double* dqi = dq + (((int64_t)b * Hq + hq) * Nq + i) * D;
+                    for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+                    if (dead) continue;
+                    for (int kk = 0; kk < Nkv; ++kk) {
+                        double ds = P[kk] * (dP[kk] - delta);
+                        const uint16_t* krow = r.kb + (int64_t)kk * k_str[2];
+                        for (int d = 0; d < D; ++d) {
+                            dqi[d] += scale * ds * widen(krow + d, dtype);
+                            dkh[(int64_t)kk * D + d] += scale * ds * widen(r.qrow + d, dtype);
+                            dvh[(int64_t)kk * D + d] += P[kk] * widen(r.dorow + d, dtype);
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dP);
+    }
+    return err ? -1 : 0;
+}
+
+/*
+ * Sampled backward, dense layout, for problems too large for the full
+ * routine.  q_rows[r] = (b*Hq + hq)*Nq + i selects dQ rows (dq: [nq_rows, D]);
+ * k_rows[r] = (b*Hkv + hk)*Nkv + j selects dK/dV rows (dk, dv: [nk_rows, D]).
+ * A dK/dV row needs, for every query row of its group, the row's softmax
+ * and sum_k P dP; these are recomputed per query row from the definition.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_attn_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const uint16_t* dout, int dtype, int B, int Hq, int Hkv, int Nq, int Nkv,
+                         int D, const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                         const int64_t* do_str, double scale, int causal,
+                         const int64_t* q_rows, int64_t nq_rows, const int64_t* k_rows,
+                         int64_t nk_rows, double* dq, double* dk, double* dv, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Nq < 0 || Nkv < 0 || D <= 0) return -1;
+    const int group = Hq / Hkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    int err = 0;
+    for (int64_t e = 0; e < nk_rows * D; ++e) dk[e] = dv[e] = 0.0;
+#pragma omp parallel
+    {
+        size_t n = (size_t)(Nkv > 0 ? Nkv : 1);
+        double* P = (double*)malloc(sizeof(double) * n);
+        double* dP = (double*)malloc(sizeof(double) * n);
+        double* acc = (double*)calloc((size_t)(nk_rows > 0 ? nk_rows : 1) * 2 * (size_t)D,
+                                      sizeof(double));
+        if (!P || !dP || !acc) {
+#pragma omp atomic write
+            err = 1;
+        }
+        /* dQ rows: one row's softmax at a time. */
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < nq_rows; ++r) {
+            if (!P || !dP || !acc) continue;
+            int64_t flat = q_rows[r];
+            int64_t i = flat % Nq, bh = flat / Nq;
+            int hq = (int)(bh % Hq), b = (int)(bh / Hq);
+            dense_row w = dense_row_at(q, k, v, dout, Hq, Hkv, Nq, Nkv, q_str, k_str, v_str, do_str,
+                                       NULL, ORACLE_MASK_NONE, NULL, causal, b, hq, i);
+            int dead;
+            double delta = grad_row(w.qrow, w.dorow, w.kb, w.vb, k_str[2], v_str[2], Nkv, D, dtype,
+                                    scale, ORACLE_MASK_NONE, NULL, 0, w.limit, P, dP, &dead);
+            double* dqi = dq + r * D;
+            for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+            if (dead) continue;
+            for (int kk = 0; kk < Nkv; ++kk) {
+                double ds = P[kk] * (dP[kk] - delta);
+                const uint16_t* krow = w.kb + (int64_t)kk * k_str[2];
+                for (int d = 0; d < D; ++d) dqi[d] += scale * ds * widen(krow + d, dtype);
+            }
+        }
+        /* dK/dV rows: every query row of every (batch, query head) that
+         * reads one of the selected key/value heads; each thread adds its
+         * query rows' contributions into a private accumulator. */
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t t = 0; t < (int64_t)B * Hq * Nq; ++t) {
+            if (!P || !dP || !acc) continue;
+            int64_t i = t % Nq, bh = t / Nq;
+            int hq = (int)(bh % Hq), b = (int)(bh / Hq);
+            int64_t head_kv = (int64_t)b * Hkv + hq / group;
+            int wanted = 0;
+            for (int64_t r = 0; r < nk_rows && !wanted; ++r) wanted = k_rows[r] / Nkv == head_kv;
+            if (!wanted) continue;
+            dense_row w = dense_row_at(q, k, v, dout, Hq, Hkv, Nq, Nkv, q_str, k_str, v_str, do_str,
+                                       NULL, ORACLE_MASK_NONE, NULL, causal, b, hq, i);
+            int dead;
+            double delta = grad_row(w.qrow, w.dorow, w.kb, w.vb, k_str[2], v_str[2], Nkv, D, dtype,
+                                    scale, ORACLE_MASK_NONE, NULL, 0, w.limit, P, dP, &dead);
+            if (dead) continue;
+            for (int64_t r = 0; r < nk_rows; ++r) {
+                if (k_rows[r] / Nkv != head_kv) continue;
+                int64_t j = k_rows[r] % Nkv;
+                double ds = P[j] * (dP[j] - delta);
+                double* ak = acc + r * 2 * D;
+                double* av = ak + D;
+                for (int d = 0; d < D; ++d) {
+                    ak[d] += scale * ds * widen(w.qrow + d, dtype);
+                    av[d] += P[j] * widen(w.dorow + d, dtype);
+                }
+            }
+        }
+#pragma omp critical
+        {
+            if (acc)
+                for (int64_t r = 0; r < nk_rows; ++r)
+                    for (int d = 0; d < D; ++d) {
+                        dk[r * D + d] += acc[r * 2 * D + d];
+                        dv[r * D + d] += acc[r * 2 * D + D + d];
+                    }
+        }
+        free(P);
+        free(dP);
+        free(acc);
     }
     return err ? -1 : 0;
 }

@@ -330,4 +330,125 @@ def pin_sampled_rows(orc):
     _close(l_r, lse.reshape(-1)[rows], atol=0.0, what="sampled rows LSE")
 
 
+# ------------------------------------------------------------------ backward
+def _case_mask(g, mspec, Nq, Nkv, dtype):
+    if mspec is None:
+        return None
+    kind, shape = mspec
+    if kind == "bool":
+        return _bool_mask(g, shape, Nq, Nkv)
+    if kind == "f32":
+        return torch.randn(*shape, generator=g)
+    return torch.randn(*shape, generator=g).to(dtype)
+
+
+def _sdpa_grads(q, k, v, dout, mask, scale, causal):
+    """torch float64 autograd through SDPA (the causal rule as an explicit mask)."""
+    Nq, Nkv = q.shape[2], k.shape[2]
+    qd, kd, vd = (t.double().requires_grad_() for t in (q, k, v))
+    m = None
+    if mask is not None:
+        m = mask.double() if mask.dtype != torch.bool else mask
+    if causal:
+        keep = tail_causal_keep(Nq, Nkv)
+        if m is None:
+            m = keep
+        elif m.dtype == torch.bool:
+            m = m & keep
+        else:
+            m = m.masked_fill(~keep, -math.inf)
+    o = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=m, scale=scale,
+                                       enable_gqa=q.shape[1] != k.shape[1])
+    return torch.autograd.grad(o, (qd, kd, vd), dout.double())
+
+
+def pin_bwd_sdpa_autograd(orc, cases=SDPA_CASES):
+    """dQ, dK, dV equal torch's float64 autograd of SDPA on every forward case."""
+    for (name, B, Hq, Hkv, Nq, Nkv, D, causal, mspec, dtype, scale) in cases:
+        q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=zlib.crc32(name.encode()) % 100003,
+                                   dtype=dtype)
+        mask = _case_mask(g, mspec, Nq, Nkv, dtype)
+        dout = torch.randn(B, Hq, Nq, D, generator=g).to(dtype)
+        got = orc.attn_bwd_dense(q, k, v, dout, attn_mask=mask, scale=scale, is_causal=causal)
+        ref = _sdpa_grads(q, k, v, dout, mask, scale, causal)
+        for nm, a, b in zip(("dQ", "dK", "dV"), got, ref):
+            _close(a, b, what=f"{name}: {nm}")
+
+
+def pin_bwd_finite_differences(orc):
+    """Central differences of sum(O * dO), O from an explicit float64 softmax
+    formula (no autograd), at every entry of small Q, K and V."""
+    g = torch.Generator().manual_seed(11)
+    B, Hq, Hkv, Nq, Nkv, D = 1, 2, 1, 3, 5, 8
+    q = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    k = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    v = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    dout = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    bias = torch.randn(Nq, Nkv, generator=g)
+    scale = 0.45
+    keep = tail_causal_keep(Nq, Nkv)
+
+    def loss(qd, kd, vd):
+        kr = kd.repeat_interleave(Hq // Hkv, dim=1)
+        vr = vd.repeat_interleave(Hq // Hkv, dim=1)
+        s = scale * (qd @ kr.transpose(-1, -2)) + bias.double()
+        s = s.masked_fill(~keep, -math.inf)
+        w = torch.exp(s - s.amax(-1, keepdim=True))
+        o = (w / w.sum(-1, keepdim=True)) @ vr
+        return (o * dout.double()).sum().item()
+
+    dq, dk, dv = orc.attn_bwd_dense(q, k, v, dout, attn_mask=bias, scale=scale, is_causal=True)
+    base = [q.double(), k.double(), v.double()]
+    h = 1e-5
+    for which, grad in enumerate((dq, dk, dv)):
+        t = base[which]
+        for idx in range(t.numel()):
+            plus = [x.clone() for x in base]
+            minus = [x.clone() for x in base]
+            plus[which].view(-1)[idx] += h
+            minus[which].view(-1)[idx] -= h
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            got = grad.reshape(-1)[idx].item()
+            assert abs(fd - got) <= 1e-7, f"{'QKV'[which]}[{idx}]: {got} vs central difference {fd}"
+
+
+def pin_bwd_invariants(orc):
+    """Shifting every key by one vector leaves each row's softmax unchanged, so
+    sum_j dK_j = 0 per key/value head; rows of P sum to one, so sum_j dV_j =
+    sum of dO over the group's rows; constant V gives constant O, so dQ = dK = 0."""
+    g = torch.Generator().manual_seed(5)
+    B, Hq, Hkv, Nq, Nkv, D = 2, 4, 2, 7, 11, 16
+    q = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    k = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    v = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    dout = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    for causal in (False, True):
+        dq, dk, dv = orc.attn_bwd_dense(q, k, v, dout, is_causal=causal)
+        _close(dk.sum(2), torch.zeros(B, Hkv, D), atol=1e-12, what=f"sum dK (causal={causal})")
+        want = dout.double().view(B, Hkv, Hq // Hkv, Nq, D).sum((2, 3))
+        _close(dv.sum(2), want, atol=1e-12, what=f"sum dV (causal={causal})")
+    vc = torch.randn(B, Hkv, 1, D, generator=g).bfloat16().expand(B, Hkv, Nkv, D).contiguous()
+    dq, dk, _ = orc.attn_bwd_dense(q, k, vc, dout, is_causal=True)
+    _close(dq, torch.zeros_like(dq), atol=1e-12, what="dQ for constant V")
+    _close(dk, torch.zeros_like(dk), atol=1e-12, what="dK for constant V")
+
+
+def pin_bwd_sampled_rows(orc):
+    """The sampled-row routine equals torch's float64 autograd on the rows it returns."""
+    g = torch.Generator().manual_seed(9)
+    B, Hq, Hkv, Nq, Nkv, D = 2, 4, 2, 6, 9, 16
+    q = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    k = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    v = torch.randn(B, Hkv, Nkv, D, generator=g).bfloat16()
+    dout = torch.randn(B, Hq, Nq, D, generator=g).bfloat16()
+    qr = [0, 5, 13, B * Hq * Nq - 1]
+    kr = [0, 4, 10, 17, B * Hkv * Nkv - 1]
+    for causal in (False, True):
+        dq, dk, dv = orc.attn_bwd_rows(q, k, v, dout, qr, kr, is_causal=causal)
+        gq, gk, gv = _sdpa_grads(q, k, v, dout, None, None, causal)
+        _close(dq, gq.reshape(-1, D)[qr], what=f"sampled dQ (causal={causal})")
+        _close(dk, gk.reshape(-1, D)[kr], what=f"sampled dK (causal={causal})")
+        _close(dv, gv.reshape(-1, D)[kr], what=f"sampled dV (causal={causal})")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -31,6 +31,26 @@ MUTANTS = {
     "fp16_exponent": ("expo - 25", "expo - 24"),
     "qtype_mask_ignored": ("x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);", ""),
     "masked_row_nan": ("if (m == -INFINITY) {", "if (0) {"),
+    # backward
+    "bwd_drop_delta": ("double ds = P[kk] * (dP[kk] - delta);", "double ds = P[kk] * dP[kk];"),
+    "bwd_delta_sign": ("double ds = P[kk] * (dP[kk] - delta);", "double ds = P[kk] * (dP[kk] + delta);"),
+    "bwd_dk_unscaled": ("dkh[(int64_t)kk * D + d] += scale * ds * widen(r.qrow + d, dtype);",
+                        "dkh[(int64_t)kk * D + d] += ds * widen(r.qrow + d, dtype);"),
+    "bwd_dv_with_ds": ("dvh[(int64_t)kk * D + d] += P[kk] * widen(r.dorow + d, dtype);",
+                       "dvh[(int64_t)kk * D + d] += ds * widen(r.dorow + d, dtype);"),
+    "bwd_dq_from_values": ("const uint16_t* krow = r.kb + (int64_t)kk * k_str[2];",
+                           "const uint16_t* krow = r.vb + (int64_t)kk * v_str[2];"),
+    "bwd_dp_from_keys": ("const uint16_t* vrow = vbase + (int64_t)kk * v_row_stride;",
+                         "const uint16_t* vrow = kbase + (int64_t)kk * k_row_stride;"),
+    "bwd_unnormalised_p": ("if (!*dead) P[kk] /= l;", ""),
+    "bwd_gqa_modulo": ("int hk = hq / (Hq / Hkv);", "int hk = hq % Hkv;"),
+    "bwd_causal_top_left": ("r.limit = causal ? i + (int64_t)Nkv - Nq", "r.limit = causal ? i"),
+    "bwd_mask_ignored": ("dtype, scale, mask_kind, r.mrow, r.mk, r.limit, P, dP, &dead);",
+                         "dtype, scale, ORACLE_MASK_NONE, r.mrow, r.mk, r.limit, P, dP, &dead);"),
+    "bwd_rows_dq_unscaled": ("for (int d = 0; d < D; ++d) dqi[d] += scale * ds * widen(krow + d, dtype);",
+                             "for (int d = 0; d < D; ++d) dqi[d] += ds * widen(krow + d, dtype);"),
+    "bwd_rows_dv_wrong_row": ("av[d] += P[j] * widen(w.dorow + d, dtype);",
+                              "av[d] += P[j] * widen(w.qrow + d, dtype);"),
 }
 
 
