@@ -1,4 +1,4 @@
-"""Exact scaled-dot-product attention forward for large head dimensions on GB300.
+"""Exact scaled-dot-product attention (forward and backward) for large head dimensions on GB300.
 
 The compute path is libffpa.so (hand-written sm_103a CUDA kernels behind the
 C ABI in include/ffpa.h); this package only marshals torch tensors into that
@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     FFPA_OK,
     FFPAError,
     default_scale,
+    ffpa_bwd,
     ffpa_fwd,
     ffpa_fwd_varlen,
     ffpa_last_device_error,

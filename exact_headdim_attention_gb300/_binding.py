@@ -22,7 +22,7 @@ FFPA_OK, FFPA_ERR_DTYPE, FFPA_ERR_INVALID, FFPA_ERR_UNSUPPORTED, FFPA_ERR_CUDA, 
 FFPA_BF16, FFPA_FP16 = 0, 1
 FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
 
-EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
+EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_bwd", "ffpa_status_string", "ffpa_last_device_error",
             "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant",
             "ffpa_selected_kernel")
 
@@ -76,6 +76,9 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_fwd_varlen.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, I, I, I, P,
                                     I, I, P]
     lib.ffpa_fwd_varlen.restype = I
+    lib.ffpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
+                             P, P, I, I, P]
+    lib.ffpa_bwd.restype = I
     lib.ffpa_status_string.argtypes = [I]
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_last_device_error.argtypes = [P]
@@ -197,6 +200,50 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
     if st != FFPA_OK:
         _raise(st, "ffpa_fwd")
     return (out, lse) if return_lse else out
+
+
+def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+             out: torch.Tensor, lse: torch.Tensor, is_causal: bool = False,
+             scale: float | None = None, enable_gqa: bool = False, *, dq=None, dk=None, dv=None,
+             delta=None, return_delta: bool = False, stream=None):
+    """Dense attention backward through the C ABI ``ffpa_bwd`` (no attn_mask).
+
+    dout, q, out [B,Hq,Nq,D]; k, v [B,Hkv,Nkv,D]; lse [B,Hq,Nq] fp32 from the
+    forward with the same is_causal / scale.  Returns (dq, dk, dv), plus
+    delta = rowsum(dout * out) [B,Hq,Nq] fp32 with return_delta."""
+    lib = load_library()
+    for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [B, H, N, D]")
+        if t.dtype != q.dtype:
+            raise TypeError("dout, q, k, v and out must share one dtype")
+    B, Hq, Nq, D = q.shape
+    Bk, Hkv, Nkv, Dk = k.shape
+    if (tuple(v.shape) != (Bk, Hkv, Nkv, Dk) or Bk != B or Dk != D
+            or tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape)):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}, "
+                         f"out {tuple(out.shape)}, dout {tuple(dout.shape)}")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
+    if dq is None:
+        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if dk is None:
+        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
+    if dv is None:
+        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
+    if delta is None:
+        delta = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    if delta.dtype != torch.float32 or not delta.is_contiguous() or tuple(delta.shape) != (B, Hq, Nq):
+        raise ValueError("delta must be a contiguous float32 [B, Hq, Nq] tensor")
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
+    st = lib.ffpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
+                      _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v),
+                      _strides(out), _strides(dout), _strides(dq), _strides(dk), _strides(dv), sc,
+                      int(bool(is_causal)), int(bool(enable_gqa)), _stream_handle(stream, q))
+    if st != FFPA_OK:
+        _raise(st, "ffpa_bwd")
+    return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)
 
 
 def _check_cu(cu: torch.Tensor, T: int, name: str) -> list[int]:

@@ -253,8 +253,8 @@ int ffpa_selected_kernel(int D, int varlen) {
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FFPA_ERR_CUDA;
-  ffpa_status (*const take[3])(int*) = {ffpa::take_err_single, ffpa::take_err_pair,
-                                        ffpa::take_err_split};
+  ffpa_status (*const take[4])(int*) = {ffpa::take_err_single, ffpa::take_err_pair,
+                                        ffpa::take_err_split, ffpa::take_err_bwd};
   int first = 0;
   for (auto fn : take) {
     int word = 0;
@@ -346,6 +346,113 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
   return launch_kernel(kn, false, P, static_cast<int>(items), smem,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
+                     const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
+                     const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
+                     const int64_t dv_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (B == 0 || (Nq == 0 && Nkv == 0)) return FFPA_OK;   // nothing to write
+  if (!q_str || !k_str || !v_str || !o_str || !do_str || !dq_str || !dk_str || !dv_str)
+    return FFPA_ERR_INVALID;
+  const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
+  if (Nq > 0) {
+    if (!q || !o || !dout || !dq || !lse || !delta) return FFPA_ERR_INVALID;
+    if (!strides_ok(q_str, qsz, 4) || !strides_ok(o_str, qsz, 4) || !strides_ok(do_str, qsz, 4) ||
+        !strides_ok(dq_str, qsz, 4))
+      return FFPA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq)) return FFPA_ERR_INVALID;
+  }
+  if (Nkv > 0) {
+    if (!k || !v || !dk || !dv) return FFPA_ERR_INVALID;
+    if (!strides_ok(k_str, ksz, 4) || !strides_ok(v_str, ksz, 4) || !strides_ok(dk_str, ksz, 4) ||
+        !strides_ok(dv_str, ksz, 4))
+      return FFPA_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
+  }
+  int dev = 0;
+  ffpa_status st = check_device(Nq > 0 ? q : k, &dev);
+  if (st != FFPA_OK) return st;
+
+  BwdParams P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  P.nchunks = D / DK;
+  P.npairs = (P.nchunks + 1) / 2;
+  P.kchunks = P.nchunks < 2 ? P.nchunks : 2;
+  const uint64_t nch = (uint64_t)P.nchunks;
+  const uint32_t box[5] = {64, BM, (uint32_t)P.kchunks, 1, 1};
+  // With no query rows (or no keys) no work item copies from those maps.
+  if (Nq > 0) {
+    const uint64_t dq5[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t sq[4] = {(uint64_t)q_str[2] * 2, 128, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
+    const uint64_t sd[4] = {(uint64_t)do_str[2] * 2, 128, (uint64_t)do_str[1] * 2, (uint64_t)do_str[0] * 2};
+    if ((st = encode_map(&P.tm_q, tdt, 5, q, dq5, sq, box)) != FFPA_OK) return st;
+    if ((st = encode_map(&P.tm_do, tdt, 5, dout, dq5, sd, box)) != FFPA_OK) return st;
+  }
+  if (Nkv > 0) {
+    const uint64_t dk5[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
+    const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
+    const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
+    if ((st = encode_map(&P.tm_k, tdt, 5, k, dk5, sk, box)) != FFPA_OK) return st;
+    if ((st = encode_map(&P.tm_v, tdt, 5, v, dk5, sv, box)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.dout = dout;
+  P.lse = lse;
+  P.delta = delta;
+  P.dq = dq;
+  P.dk = dk;
+  P.dv = dv;
+  for (int i = 0; i < 4; ++i) {
+    P.o_str[i] = o_str[i];
+    P.do_str[i] = do_str[i];
+    P.dq_str[i] = dq_str[i];
+    P.dk_str[i] = dk_str[i];
+    P.dv_str[i] = dv_str[i];
+  }
+  P.B = B;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.group = Hq / Hkv;
+  P.Nq = Nq;
+  P.Nkv = Nkv;
+  P.D = D;
+  P.n_qt = (Nq + BM - 1) / BM;
+  P.n_kt = (Nkv + BN - 1) / BN;
+  P.n_sl_dq = (D + BWD_DQ_COLS - 1) / BWD_DQ_COLS;
+  P.n_sl_kv = (D + BWD_KV_COLS - 1) / BWD_KV_COLS;
+  // Shared memory: one (dQ) or two (dK/dV) 32 KB P/dS tiles, then the ring.
+  const size_t avail = SMEM_LIMIT - BWD_STATIC_RESERVE - 1024;
+  size_t ns_dq = (avail - P_TILE_BYTES) / SLOT_BYTES;
+  size_t ns_kv = (avail - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
+  if (ns_dq > (size_t)BWD_NSLOT_MAX) ns_dq = BWD_NSLOT_MAX;
+  if (ns_kv > (size_t)BWD_NSLOT_MAX) ns_kv = BWD_NSLOT_MAX;
+  P.nslot_dq = static_cast<int>(ns_dq);
+  P.nslot_kv = static_cast<int>(ns_kv);
+  const size_t dq_smem = 1024 + P_TILE_BYTES + ns_dq * SLOT_BYTES;
+  const size_t kv_smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns_kv * SLOT_BYTES;
+  P.scale = sc;
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = is_causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.timeout_ns = g_timeout_ns.load();
+  const long long dq_items = Nq > 0 ? (long long)B * Hq * P.n_qt * P.n_sl_dq : 0;
+  const long long kv_items = Nkv > 0 ? (long long)B * Hkv * P.n_kt * P.n_sl_kv : 0;
+  if (dq_items > 0x7fffffffLL || kv_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), dq_smem, kv_smem,
+                    reinterpret_cast<cudaStream_t>(stream));
 }
 
 ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

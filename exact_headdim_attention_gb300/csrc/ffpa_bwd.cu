@@ -1,0 +1,604 @@
+// Backward of exact attention: dQ, dK and dV from Q, K, V, O, dO and the
+// forward's natural-log LSE (FFPA API reference, "ffpa_attn.ffpa_attn_func":
+// backward through FFPAAttnFunc; the Triton backend's `split_launch` option
+// issues "separate backward launches for dKdV and dQ", which is the split
+// used here).
+//
+// With P = exp(scale * Q K^T - LSE) (the forward's softmax, recomputed),
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - delta),  delta = rowsum(dO * O),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Three launches on the caller's stream:
+//   delta   one warp per query row, 16-byte loads of O and dO.
+//   dQ      one CTA per (batch, query head, 128-row query tile, <= 256 dQ
+//           columns); loops over the visible key tiles.
+//   dK/dV   one CTA per (batch, key/value head, 128-key tile, <= 128 dK and
+//           dV columns); loops over every query head of the group and the
+//           query tiles that see the key tile, so grouped heads add up in
+//           TMEM and no atomics are needed.
+// Both tensor-core kernels share one body (DQ selects the role).  Per
+// iteration the MMA thread computes two full-D contractions into TMEM
+// (S = A1 B1^T and dP = A2 B2^T: for dQ A = Q, dO and B = K, V; for dK/dV
+// A = K, V and B = Q, dO, i.e. S^T and dP^T), the elementwise warps turn
+// them into 16-bit P and dS in shared memory (128-byte swizzle, K-major),
+// and the MMA thread accumulates the output slices from them (dQ += dS K;
+// dV += P^T dO, dK += dS^T Q) with the B operand read MN-major from the
+// same 64-column boxes that serve the contractions.  TMEM holds the output
+// accumulators in columns [0, 256) and S, dP in [256, 384), [384, 512).
+// The contractions of iteration i+1 are issued before the slice MMAs of
+// iteration i, so the tensor core works while the elementwise warps run.
+// When D exceeds the output columns of one CTA, the CTAs of the other
+// column slices recompute S and dP.
+#include "ffpa_common.cuh"
+
+namespace ffpa {
+
+namespace {
+
+constexpr uint32_t BWD_S_COL = 256;
+constexpr uint32_t BWD_DP_COL = 384;
+constexpr int BWD_PRODUCER_WARP = 4;
+constexpr int BWD_MMA_WARP = 5;
+constexpr float LOG2E_F = 1.4426950408889634f;
+
+// Dot product of 8 16-bit pairs held in two uint4.
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, bool fp16) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a0, a1, b0, b1;
+    if (fp16) {
+      const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&wa[i]));
+      const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&wb[i]));
+      a0 = fa.x; a1 = fa.y; b0 = fb.x; b1 = fb.y;
+    } else {
+      a0 = __uint_as_float(wa[i] << 16);
+      a1 = __uint_as_float(wa[i] & 0xffff0000u);
+      b0 = __uint_as_float(wb[i] << 16);
+      b1 = __uint_as_float(wb[i] & 0xffff0000u);
+    }
+    s = fmaf(a0, b0, s);
+    s = fmaf(a1, b1, s);
+  }
+  return s;
+}
+
+struct BwdItem {
+  int b, hq, hkv, slice;
+  int row0;       // first row of this CTA's tile: query row (dQ) or key row (dK/dV)
+  int n_iter;     // dQ: key tiles; dK/dV: group heads x visible query tiles
+  int qt_first;   // dK/dV: first query tile that sees the key tile
+  int nq;         // dK/dV: query tiles per head
+  int col_lo, dv; // output columns [col_lo, col_lo + dv)
+};
+
+template <bool DQ>
+__device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& it) {
+  if (DQ) {
+    it.slice = L % p.n_sl_dq;
+    L /= p.n_sl_dq;
+    const int heads = p.B * p.Hq;
+    int qt, bh;
+    if (p.causal) {            // longest query tiles (most visible keys) first
+      bh = L % heads;
+      qt = p.n_qt - 1 - L / heads;
+    } else {
+      qt = L % p.n_qt;
+      bh = L / p.n_qt;
+    }
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+    it.hkv = it.hq / p.group;
+    it.row0 = qt * BM;
+    if (it.row0 >= p.Nq) return false;
+    long long kv_end = p.Nkv;
+    if (p.causal) {
+      const int rows = min(BM, p.Nq - it.row0);
+      kv_end = min(kv_end, (long long)it.row0 + rows + (p.Nkv - p.Nq));
+    }
+    it.n_iter = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+    it.qt_first = 0;
+    it.nq = 0;
+    it.col_lo = it.slice * BWD_DQ_COLS;
+    it.dv = min(BWD_DQ_COLS, p.D - it.col_lo);
+  } else {
+    it.slice = L % p.n_sl_kv;
+    L /= p.n_sl_kv;
+    const int heads = p.B * p.Hkv;
+    int kt, bh;
+    if (p.causal) {            // key tile 0 is seen by every query tile: first
+      bh = L % heads;
+      kt = L / heads;
+    } else {
+      kt = L % p.n_kt;
+      bh = L / p.n_kt;
+    }
+    it.hkv = bh % p.Hkv;
+    it.b = bh / p.Hkv;
+    it.hq = it.hkv * p.group;
+    it.row0 = kt * BN;
+    if (it.row0 >= p.Nkv) return false;
+    // Query row i sees key k when k <= i + (Nkv - Nq): the first query
+    // tile with a row that sees this tile's first key.
+    const int first_row = p.causal ? max(0, it.row0 - (p.Nkv - p.Nq)) : 0;
+    it.qt_first = first_row / BM;
+    it.nq = max(0, p.n_qt - it.qt_first);
+    it.n_iter = p.group * it.nq;
+    it.col_lo = it.slice * BWD_KV_COLS;
+    it.dv = min(BWD_KV_COLS, p.D - it.col_lo);
+  }
+  return true;
+}
+
+// Rows of a TMEM accumulator (columns [tcol, tcol + ncols) of this thread's
+// lane) times `mul`, rounded to 16 bits and stored at dst (nullptr: row out
+// of range).  have == false stores zeros.
+__device__ __forceinline__ void bwd_store_row(uint32_t taddr, int ncols, float mul, uint8_t* dst,
+                                              bool fp16, bool have) {
+  for (int c0 = 0; c0 < ncols; c0 += 32) {
+    uint32_t v[32];
+    if (have) {
+      tmem_ld32(taddr + c0, v);
+      tmem_wait_ld();
+      reg_fence(v);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) v[c] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float a0 = __uint_as_float(v[2 * c]) * mul;
+      const float a1 = __uint_as_float(v[2 * c + 1]) * mul;
+      pk[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+    }
+    if (dst != nullptr) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c0 * 2);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+}
+
+// Writes 128 16-bit values (64 packed pairs) of row r into a 128 x 128
+// K-major tile with 128-byte swizzle: two 16 KB chunks of 64 columns, 16-byte
+// unit u of row r at unit u ^ (r & 7).
+__device__ __forceinline__ void bwd_write_tile_row(uint32_t tile, int r, const uint32_t* pk) {
+  const uint32_t row = tile + (uint32_t)r * 128u;
+  const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+  for (int g = 0; g < BN / 8; ++g)
+    st_shared_v4(row + (g >> 3) * CHUNK_BYTES + ((((uint32_t)g & 7u) ^ sw) << 4), pk[4 * g],
+                 pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) ffpa_bwd_delta_kernel(const __grid_constant__ BwdParams p) {
+  const long long rows = (long long)p.B * p.Hq * p.Nq;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const long long i = row % p.Nq;
+  const long long bh = row / p.Nq;
+  const long long h = bh % p.Hq, b = bh / p.Hq;
+  const uint16_t* orow = static_cast<const uint16_t*>(p.o) + b * p.o_str[0] + h * p.o_str[1] + i * p.o_str[2];
+  const uint16_t* drow =
+      static_cast<const uint16_t*>(p.dout) + b * p.do_str[0] + h * p.do_str[1] + i * p.do_str[2];
+  const bool fp16 = p.fp16 != 0;
+  float acc = 0.f;
+  for (int d0 = lane * 8; d0 < p.D; d0 += 256)
+    acc += dot8(__ldg(reinterpret_cast<const uint4*>(orow + d0)),
+                __ldg(reinterpret_cast<const uint4*>(drow + d0)), fp16);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) p.delta[row] = acc;
+}
+
+template <bool DQ>
+__global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  BwdItem it;
+  if (!bwd_decode<DQ>(p, blockIdx.x, it)) return;   // uniform across the CTA
+
+  const int npairs = p.npairs, nchunks = p.nchunks;
+  const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
+  const int NS = DQ ? p.nslot_dq : p.nslot_kv;
+  const int T = it.n_iter;
+  const unsigned long long tmo = p.timeout_ns;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // [t1: dS (dQ) or P^T (dK/dV)] [t2: dS^T (dK/dV only)] [ring: NS x 32 KB]
+  const uint32_t t1_u32 = smem_u32(smem);
+  const uint32_t t2_u32 = t1_u32 + P_TILE_BYTES;
+  const uint32_t ring_u32 = t1_u32 + (DQ ? 1u : 2u) * P_TILE_BYTES;
+  __shared__ __align__(8) uint64_t bar_full[BWD_NSLOT_MAX], bar_empty[BWD_NSLOT_MAX];
+  __shared__ __align__(8) uint64_t bar_sd_full, bar_s_free, bar_p_full, bar_pd_done, bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+  // dK/dV: per-warp copies of the current query tile's log2-domain LSE and
+  // delta (each warp loads and reads its own, so no cross-warp barrier).
+  __shared__ __align__(16) float stat_sh[DQ ? 4 : 4 * 2 * BM];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_sd_full), 1);
+    mbar_init(smem_u32(&bar_s_free), 4);
+    mbar_init(smem_u32(&bar_p_full), 4);
+    mbar_init(smem_u32(&bar_pd_done), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == BWD_MMA_WARP) {
+    tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  // Streaming-side head and first row of iteration i (dK/dV: query head and
+  // query tile; dQ: the key tile).
+  auto stream_coords = [&](int i, int& head, int& row) {
+    if (DQ) {
+      head = it.hkv;
+      row = i * BN;
+    } else {
+      head = it.hq + i / it.nq;
+      row = (it.qt_first + i % it.nq) * BM;
+    }
+  };
+  const int nbox = (it.dv + 127) / 128;   // 64..128-column boxes of the output slice
+
+  if (warp == BWD_PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && T > 0) {
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_k);
+      prefetch_tmap(&p.tm_v);
+      prefetch_tmap(&p.tm_do);
+      const uint32_t box_bytes = (uint32_t)p.kchunks * CHUNK_BYTES;
+      int slot = 0, issued = 0;
+      uint32_t lap = 0;
+      auto load = [&](const CUtensorMap* m, int row, int chunk, int head) -> bool {
+        const uint32_t eb = smem_u32(&bar_empty[slot]);
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) return false;
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        mbar_arrive_expect_tx(fb, box_bytes);
+        tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
+        ++issued;
+        if (++slot == NS) { slot = 0; lap ^= 1u; }
+        return true;
+      };
+      const CUtensorMap* a1 = DQ ? &p.tm_q : &p.tm_k;
+      const CUtensorMap* b1 = DQ ? &p.tm_k : &p.tm_q;
+      const CUtensorMap* a2 = DQ ? &p.tm_do : &p.tm_v;
+      const CUtensorMap* b2 = DQ ? &p.tm_v : &p.tm_do;
+      const int ha = DQ ? it.hq : it.hkv;
+      auto contraction_loads = [&](int i) -> bool {
+        int hs, rs;
+        stream_coords(i, hs, rs);
+        for (int pr = 0; pr < npairs; ++pr)
+          if (!load(a1, it.row0, 2 * pr, ha) || !load(b1, rs, 2 * pr, hs)) return false;
+        for (int pr = 0; pr < npairs; ++pr)
+          if (!load(a2, it.row0, 2 * pr, ha) || !load(b2, rs, 2 * pr, hs)) return false;
+        return true;
+      };
+      auto slice_loads = [&](int i) -> bool {
+        int hs, rs;
+        stream_coords(i, hs, rs);
+        const int c0 = it.col_lo / DK;
+        if (DQ) {
+          for (int bx = 0; bx < nbox; ++bx)
+            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs)) return false;
+          return true;
+        }
+        return load(&p.tm_do, rs, c0, hs) && load(&p.tm_q, rs, c0, hs);
+      };
+      // Same order as the MMA thread consumes: contractions of iteration 0,
+      // then per iteration i the contractions of i+1 and the slices of i.
+      bool ok = contraction_loads(0);
+      for (int i = 0; i < T && ok; ++i) {
+        if (i + 1 < T) ok = contraction_loads(i + 1);
+        if (ok) ok = slice_loads(i);
+      }
+      // Drain: every copy started here has landed before the CTA exits.
+      const int n = issued < NS ? issued : NS;
+      int s = slot;
+      uint32_t lp = lap;
+      for (int i = 0; i < n; ++i) {
+        if (--s < 0) { s = NS - 1; lp ^= 1u; }
+        wait_drain(smem_u32(&bar_full[s]), lp, tmo);
+      }
+    }
+  } else if (warp == BWD_MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      int slot = 0;
+      uint32_t lap = 0;
+      auto take = [&]() -> int {
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        const int s = slot;
+        if (++slot == NS) { slot = 0; lap ^= 1u; }
+        return s;
+      };
+      auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
+      auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        tc_fence_after();
+        return true;
+      };
+      const uint32_t idesc_s = idesc_f16(!fp16, BM, BN, false, false);
+      // Both operands K-major: +32 bytes per 16 D-elements, +16 KB per chunk.
+      const uint64_t ring_k = sdesc_sw128(ring_u32, 16, 1024);
+      // MN-major B (rows = contraction index): 64-column chunks 16 KB apart,
+      // +2048 bytes per 16 rows.
+      const uint64_t ring_mn = sdesc_sw128(ring_u32, BM * 128, 1024);
+      const uint64_t t1_desc = sdesc_sw128(t1_u32, 16, 1024);
+      const uint64_t t2_desc = sdesc_sw128(t2_u32, 16, 1024);
+      auto contract = [&](uint32_t dcol) -> bool {
+        for (int pr = 0; pr < npairs; ++pr) {
+          const int sa = take();
+          if (sa < 0) return false;
+          const int sb = take();
+          if (sb < 0) return false;
+          const uint64_t ad = ring_k + ((sa * SLOT_BYTES) >> 4);
+          const uint64_t bd = ring_k + ((sb * SLOT_BYTES) >> 4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_ss(tmem + dcol, ad + 2 * k, bd + 2 * k, idesc_s, (pr > 0 || k > 0) ? 1u : 0u);
+          if (2 * pr + 1 < nchunks) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) umma_ss(tmem + dcol, ad + 1024 + 2 * k, bd + 1024 + 2 * k, idesc_s, 1u);
+          }
+          release(sa);
+          release(sb);
+        }
+        return true;
+      };
+      auto contractions = [&]() -> bool {
+        if (!contract(BWD_S_COL) || !contract(BWD_DP_COL)) return false;
+        umma_commit(smem_u32(&bar_sd_full));
+        return true;
+      };
+      // D[dcol, +n) (+)= A (128 x 128 tile, K-major) * B (box, MN-major).
+      auto slice_mma = [&](uint32_t dcol, uint64_t a_desc, int n, bool acc) -> bool {
+        const int s = take();
+        if (s < 0) return false;
+        const uint64_t bd = ring_mn + ((s * SLOT_BYTES) >> 4);
+        const uint32_t idesc = idesc_f16(!fp16, BM, n, false, true);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_ss(tmem + dcol, a_desc + (((kk >> 2) * CHUNK_BYTES) >> 4) + 2 * (kk & 3), bd + 128 * kk,
+                  idesc, (acc || kk > 0) ? 1u : 0u);
+        release(s);
+        return true;
+      };
+      bool ok = contractions();
+      for (int i = 0; i < T && ok; ++i) {
+        // S and dP of iteration i are in registers of the elementwise warps.
+        if (!(ok = wait_on(smem_u32(&bar_s_free), i & 1))) break;
+        if (i + 1 < T && !(ok = contractions())) break;
+        if (!(ok = wait_on(smem_u32(&bar_p_full), i & 1))) break;
+        if (DQ) {
+          for (int bx = 0; bx < nbox && ok; ++bx)
+            ok = slice_mma(128 * bx, t1_desc, min(128, it.dv - 128 * bx), i > 0);
+        } else {
+          ok = slice_mma(0, t1_desc, it.dv, i > 0) && slice_mma(BWD_KV_COLS, t2_desc, it.dv, i > 0);
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&bar_pd_done));
+      }
+      const uint32_t db = smem_u32(&bar_drain);
+      umma_commit(db);
+      wait_drain(db, 0, tmo);
+    }
+  } else {
+    // ------------------------------------------------------------ elementwise
+    // Thread r owns TMEM lane r: query row row0 + r (dQ) or key row row0 + r
+    // (dK/dV).  Columns are keys (dQ) or queries (dK/dV).
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    const long long off = (long long)p.Nkv - p.Nq;   // tail alignment of the causal limit
+    const int my_row = it.row0 + r;
+    float lse_r = INFINITY, delta_r = 0.f;           // dQ: this row's statistics
+    if (DQ && my_row < p.Nq) {
+      const long long li = ((long long)it.b * p.Hq + it.hq) * p.Nq + my_row;
+      const float l = p.lse[li];
+      lse_r = l > -INFINITY ? l * LOG2E_F : INFINITY;   // a row with no softmax has P = 0
+      delta_r = p.delta[li];
+    }
+    float* st = stat_sh + (DQ ? 0 : warp * 2 * BM);   // [lse(128) | delta(128)] of this warp
+    const uint32_t st_u32 = smem_u32(st);
+    bool ok = true;
+    for (int i = 0; i < T; ++i) {
+      int hs, rs;
+      stream_coords(i, hs, rs);
+      if (!DQ) {
+        // Query-tile statistics: lane l loads queries l, l+32, l+64, l+96.
+        __syncwarp();
+        const long long lbase = ((long long)it.b * p.Hq + hs) * p.Nq;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int qi = rs + 32 * q4 + lane;
+          float l2 = INFINITY, dl = 0.f;
+          if (qi < p.Nq) {
+            const float l = p.lse[lbase + qi];
+            l2 = l > -INFINITY ? l * LOG2E_F : INFINITY;
+            dl = p.delta[lbase + qi];
+          }
+          st[32 * q4 + lane] = l2;
+          st[BM + 32 * q4 + lane] = dl;
+        }
+        __syncwarp();
+      }
+      bool w = wait_bounded(smem_u32(&bar_sd_full), i & 1, &abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      // Causal limits: dQ row i sees key k <= i + off; dK/dV key row k is
+      // seen by query q >= k - off.
+      const bool need_mask = DQ ? ((long long)rs + BN > p.Nkv ||
+                                   (causal && (long long)rs + BN - 1 > (long long)it.row0 + off))
+                                : (causal && (long long)it.row0 + BM - 1 - off > (long long)rs);
+      const long long lim = DQ ? (long long)my_row + off - rs      // last visible column
+                               : (long long)my_row - off - rs;     // first visible column
+      const int kv_cols = p.Nkv - rs;                              // dQ: key columns in range
+      uint32_t ppk[DQ ? 1 : BN / 2];
+      uint32_t dpk[BN / 2];
+#pragma unroll
+      for (int g = 0; g < BN / 16; ++g) {
+        uint32_t sr[16], dr[16];
+        tmem_ld16(lane_base + BWD_S_COL + 16 * g, sr);
+        tmem_ld16(lane_base + BWD_DP_COL + 16 * g, dr);
+        tmem_wait_ld();
+        reg_fence(sr);
+        reg_fence(dr);
+        float l16[16], d16[16];
+        if (DQ) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            l16[e] = lse_r;
+            d16[e] = delta_r;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 a = ld_shared_v4(st_u32 + (uint32_t)(16 * g + 4 * q) * 4u);
+            const uint4 b = ld_shared_v4(st_u32 + (uint32_t)(BM + 16 * g + 4 * q) * 4u);
+            l16[4 * q] = __uint_as_float(a.x);
+            l16[4 * q + 1] = __uint_as_float(a.y);
+            l16[4 * q + 2] = __uint_as_float(a.z);
+            l16[4 * q + 3] = __uint_as_float(a.w);
+            d16[4 * q] = __uint_as_float(b.x);
+            d16[4 * q + 1] = __uint_as_float(b.y);
+            d16[4 * q + 2] = __uint_as_float(b.z);
+            d16[4 * q + 3] = __uint_as_float(b.w);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 16; c += 2) {
+          float pe[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 16 * g + c + e;
+            float v = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -l16[c + e]));
+            if (need_mask) {
+              const bool vis = DQ ? (col < kv_cols && (!causal || (long long)col <= lim))
+                                  : ((long long)col >= lim);
+              v = vis ? v : 0.f;
+            }
+            pe[e] = v;
+            ds[e] = v * (__uint_as_float(dr[c + e]) - d16[c + e]);
+          }
+          if (!DQ) ppk[8 * g + c / 2] = fp16 ? pack_f16(pe[0], pe[1]) : pack_bf16(pe[0], pe[1]);
+          dpk[8 * g + c / 2] = fp16 ? pack_f16(ds[0], ds[1]) : pack_bf16(ds[0], ds[1]);
+        }
+      }
+      // S and dP are in registers: the next contractions may overwrite them.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
+      // The P/dS tiles are free once the slice MMAs of iteration i-1 are done.
+      if (i >= 1) {
+        w = wait_bounded(smem_u32(&bar_pd_done), (i - 1) & 1, &abort_flag, tmo);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (DQ) {
+        bwd_write_tile_row(t1_u32, r, dpk);
+      } else {
+        bwd_write_tile_row(t1_u32, r, ppk);
+        bwd_write_tile_row(t2_u32, r, dpk);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_p_full));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && T > 0) {
+      const bool w = wait_bounded(smem_u32(&bar_pd_done), (T - 1) & 1, &abort_flag, tmo);
+      ok = __all_sync(0xffffffffu, w);
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      if (DQ) {
+        uint8_t* dst = nullptr;
+        if (my_row < p.Nq)
+          dst = static_cast<uint8_t*>(p.dq) +
+                ((long long)it.b * p.dq_str[0] + (long long)it.hq * p.dq_str[1] +
+                 (long long)my_row * p.dq_str[2] + it.col_lo) * 2;
+        bwd_store_row(lane_base, it.dv, p.scale, dst, fp16, T > 0);
+      } else {
+        uint8_t* dstv = nullptr;
+        uint8_t* dstk = nullptr;
+        if (my_row < p.Nkv) {
+          dstv = static_cast<uint8_t*>(p.dv) +
+                 ((long long)it.b * p.dv_str[0] + (long long)it.hkv * p.dv_str[1] +
+                  (long long)my_row * p.dv_str[2] + it.col_lo) * 2;
+          dstk = static_cast<uint8_t*>(p.dk) +
+                 ((long long)it.b * p.dk_str[0] + (long long)it.hkv * p.dk_str[1] +
+                  (long long)my_row * p.dk_str[2] + it.col_lo) * 2;
+        }
+        bwd_store_row(lane_base, it.dv, 1.f, dstv, fp16, T > 0);
+        bwd_store_row(lane_base + BWD_KV_COLS, it.dv, p.scale, dstk, fp16, T > 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == BWD_MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
+                       size_t kv_smem, cudaStream_t stream) {
+  const long long rows = (long long)P.B * P.Hq * P.Nq;
+  if (rows > 0) {
+    ffpa_bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+  }
+  if (dq_items > 0) {
+    if (cudaFuncSetAttribute(ffpa_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dq_smem)) != cudaSuccess)
+      return FFPA_ERR_CUDA;
+    ffpa_bwd_kernel<true><<<dq_items, BWD_THREADS, dq_smem, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+  }
+  if (kv_items > 0) {
+    if (cudaFuncSetAttribute(ffpa_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kv_smem)) != cudaSuccess)
+      return FFPA_ERR_CUDA;
+    ffpa_bwd_kernel<false><<<kv_items, BWD_THREADS, kv_smem, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+  }
+  return FFPA_OK;
+}
+
+ffpa_status take_err_bwd(int* word) {
+  *word = 0;
+  if (cudaMemcpyFromSymbol(word, g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
+  if (*word != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
+  }
+  return FFPA_OK;
+}
+
+}  // namespace ffpa

@@ -90,6 +90,41 @@ ffpa_status take_err_single(int* word);
 ffpa_status take_err_pair(int* word);
 ffpa_status take_err_split(int* word);
 
+// Backward (ffpa_bwd.cu): a delta pass, then one kernel for dK/dV (rows =
+// keys) and one for dQ (rows = queries).
+struct BwdParams;
+ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
+                       size_t kv_smem, cudaStream_t stream);
+ffpa_status take_err_bwd(int* word);
+constexpr int BWD_THREADS = 192;           // warps 0-3 elementwise, 4 TMA, 5 MMA
+constexpr int BWD_NSLOT_MAX = 6;
+constexpr size_t BWD_STATIC_RESERVE = 6144;
+constexpr int BWD_DQ_COLS = 256;           // dQ columns per CTA
+constexpr int BWD_KV_COLS = 128;           // dK and dV columns per CTA
+
+struct BwdParams {
+  // Views (64, N, D/64, H, B) of Q, K, V and dO; box 64 x 128 rows x kchunks.
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* delta;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t o_str[4], do_str[4], dq_str[4], dk_str[4], dv_str[4];
+  int B, Hq, Hkv, group, Nq, Nkv, D;
+  int nchunks, npairs, kchunks;
+  int n_qt, n_kt, n_sl_dq, n_sl_kv;
+  int nslot_dq, nslot_kv;
+  float scale, scale_log2;
+  int causal, fp16;
+  unsigned long long timeout_ns;
+};
+
 struct Params {
   // Views with D split as (64, D/64): dense (64, N, D/64, H, B); varlen
   // (64, T, D/64, H).  Q and K boxes: 64 x 128 rows x min(2, D/64) chunks;

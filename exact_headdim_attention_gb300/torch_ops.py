@@ -1,4 +1,4 @@
-"""PyTorch custom operators over the C ABI (forward only).
+"""PyTorch custom operators over the C ABI.
 
 ``torch.ops.ffpa.attn_fwd`` and ``torch.ops.ffpa.attn_varlen_fwd`` wrap
 ``ffpa_fwd`` / ``ffpa_fwd_varlen`` as opaque operators: torch.compile and
@@ -8,8 +8,9 @@ binding.  ``ffpa_attn_func`` takes the argument list of
 ``torch.nn.functional.scaled_dot_product_attention`` (the FFPA API
 reference, ``ffpa_attn.ffpa_attn_func``, uses the same list), so it can
 replace that call for the supported cases: bf16/fp16 CUDA tensors,
-64 <= D <= 1024 with D % 64 == 0, no dropout.  The operators register no
-backward: differentiating through them raises.
+64 <= D <= 1024 with D % 64 == 0, no dropout.  The dense operator is
+differentiable through ``ffpa_bwd`` (the backward kernels) when it was
+called without attn_mask; the varlen operator registers no backward.
 """
 from __future__ import annotations
 
@@ -34,6 +35,28 @@ def _attn_fwd_fake(q, k, v, attn_mask, is_causal, scale, enable_gqa):
     B, Hq, Nq, _ = q.shape
     return (torch.empty_like(q, memory_format=torch.contiguous_format),
             q.new_empty((B, Hq, Nq), dtype=torch.float32))
+
+
+def _attn_fwd_setup_context(ctx, inputs, output):
+    q, k, v, attn_mask, is_causal, scale, enable_gqa = inputs
+    o, lse = output
+    ctx.save_for_backward(q, k, v, o, lse)
+    ctx.has_mask = attn_mask is not None
+    ctx.is_causal, ctx.scale, ctx.enable_gqa = is_causal, scale, enable_gqa
+
+
+def _attn_fwd_backward(ctx, grad_o, grad_lse):
+    if ctx.has_mask:
+        raise NotImplementedError("the backward kernels take no attn_mask")
+    if grad_lse is not None and bool(torch.count_nonzero(grad_lse)):
+        raise NotImplementedError("gradients through the returned LSE are not supported")
+    q, k, v, o, lse = ctx.saved_tensors
+    dq, dk, dv = _binding.ffpa_bwd(grad_o.contiguous(), q, k, v, o, lse, is_causal=ctx.is_causal,
+                                   scale=ctx.scale, enable_gqa=ctx.enable_gqa)
+    return dq, dk, dv, None, None, None, None
+
+
+attn_fwd.register_autograd(_attn_fwd_backward, setup_context=_attn_fwd_setup_context)
 
 
 @torch.library.custom_op("ffpa::attn_varlen_fwd", mutates_args=())

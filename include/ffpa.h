@@ -117,6 +117,41 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
                             int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                             int enable_gqa, ffpa_stream_t stream);
 
+/*
+ * Backward of ffpa_fwd (dense layout, no attn_mask): the gradients dq, dk, dv
+ * of sum(O * dout) with respect to q, k and v (FFPA API reference,
+ * "ffpa_attn.ffpa_attn_func": backward through FFPAAttnFunc; the Triton
+ * backend's `split_launch` option: separate dKdV and dQ launches).  With
+ * P = exp(scale * q k^T - lse) the forward's softmax:
+ *   delta = rowsum(dout * o),  dv = P^T dout,  dS = P * (dout v^T - delta),
+ *   dq = scale * dS k,  dk = scale * dS^T q,
+ * summed over the query heads of a group for dk and dv.
+ *
+ *   q, o, dout, dq: [B, Hq, Nq, D] (strides q_str, o_str, do_str, dq_str).
+ *   k, v, dk, dv: [B, Hkv, Nkv, D] (strides k_str, v_str, dk_str, dv_str).
+ *   lse: [B, Hq, Nq] fp32 contiguous, the natural-log LSE that ffpa_fwd
+ *     returned for the same q, k, v, scale and is_causal.
+ *   delta: [B, Hq, Nq] fp32 contiguous OUTPUT (rowsum(dout * o), the
+ *     FlashAttention "softmax_d"); written first and read by the gradient
+ *     kernels, so it must not alias any input.
+ *   o, dout, dq, dk, dv: the 16-bit type of q; outputs must not alias inputs.
+ *   scale, is_causal, enable_gqa: as for ffpa_fwd (the same values as the
+ *     forward that produced o and lse).
+ *
+ * Strides follow the ffpa_fwd rules (last stride 1, others multiples of 16
+ * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd;
+ * a NULL lse or delta is FFPA_ERR_INVALID.  B == 0 or Nq == 0 with Nkv > 0
+ * writes zero dk and dv; Nkv == 0 writes zero dq.  Three launches on
+ * `stream`; no allocation, no synchronisation.
+ */
+ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
+                     const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
+                     const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
+                     const int64_t dv_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* ffpa_status_string(ffpa_status status);
 

@@ -176,3 +176,47 @@ def test_selected_kernel_follows_the_choice(lib):
     assert lib.ffpa_selected_kernel(100, 0) == -1
     with pytest.raises(ValueError):
         pkg.selected_kernel(96)
+
+
+def bwd_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,
+             lse=FAKE, delta=FAKE, dk=FAKE, qs=None, scale=None):
+    def st(H, N):
+        return _arr([H * N * D, N * D, D, 1])
+    qs = qs or st(Hq, Nq)
+    ks = st(Hkv, Nkv)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
+    return lib.ffpa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, lse, FAKE, dk, FAKE, delta, dt, B, Hq, Hkv, Nq,
+                        Nkv, D, qs, ks, ks, qs, qs, qs, ks, ks, sc, causal, enable_gqa, None)
+
+
+@pytest.mark.parametrize("case", GOLDEN["dense"], ids=lambda c: c["case"])
+def test_bwd_documented_errors(lib, case):
+    """The backward takes the forward's arguments and applies the same checks."""
+    assert bwd_call(lib, **case["override"]) == case["status"]
+
+
+def test_bwd_layout_and_pointer_checks(lib):
+    INVALID = pkg.FFPA_ERR_INVALID
+    assert bwd_call(lib, lse=None) == INVALID
+    assert bwd_call(lib, delta=None) == INVALID
+    assert bwd_call(lib, dk=FAKE + 4) == INVALID                                  # misaligned output
+    assert bwd_call(lib, qs=_arr([2 * 128 * 64, 128 * 64, 64, 2])) == INVALID     # D stride != 1
+    assert bwd_call(lib, scale=float("nan")) == INVALID
+    assert bwd_call(lib, dt=5, lse=None) == pkg.FFPA_ERR_DTYPE
+    assert bwd_call(lib, B=0, lse=None) == pkg.FFPA_OK                           # nothing to write
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_bwd_valid_call_without_gpu_reports_cuda_error(lib):
+    assert bwd_call(lib) == pkg.FFPA_ERR_CUDA
+
+
+def test_bwd_binding_checks(lib):
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 4)
+    with pytest.raises(ValueError):
+        pkg.ffpa_bwd(q, q, q, q, q, lse.double())                 # lse must be float32
+    with pytest.raises(ValueError):
+        pkg.ffpa_bwd(q, q, q, q, q[:, :, :3], lse)                # out shape
+    with pytest.raises(TypeError):
+        pkg.ffpa_bwd(q.half(), q, q, q, q, lse)                   # mixed dtypes

@@ -1,0 +1,200 @@
+"""Backward kernels (through the C ABI ``ffpa_bwd``) against the float64 oracle.
+
+The gradients are those of sum(O * dO) for a seeded upstream gradient dO;
+the CUDA path starts from its own forward's O and LSE, the oracle from the
+definition.  Small problems are compared in full (several 128-row and
+128-key tiles plus a ragged tail); large ones on sampled rows that the
+oracle computes one by one.
+
+Tolerance, from the arithmetic of the path: P and dS are rounded to 16 bits
+before the tensor-core products (relative error <= u = 2^-9 for bf16), the
+products accumulate in fp32, and dQ, dK, dV are rounded to 16 bits once
+more.  An output element is a sum of many terms with independent rounding
+errors of relative size ~u, so its error is a few u of the typical output
+magnitude: max |err| <= 2e-2 * max |ref| and mean |err| <= 1e-2 * mean |ref|
+(about 10 u and 5 u).  delta = rowsum(dO * O) is an fp32 dot product of the
+16-bit inputs: relative 1e-4 of sum |dO * O|.
+"""
+import pytest
+import torch
+
+import exact_headdim_attention_gb300 as pkg
+import oracle
+from exact_headdim_attention_gb300 import workloads as wl
+from tests.gpu_util import device_ok
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+G_MAX, G_MEAN = 2e-2, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkg.load_library()
+    pkg.set_wait_timeout_ns(0)
+    yield
+
+
+def check_grad(got, ref, what, g_max=G_MAX, g_mean=G_MEAN):
+    got = got.detach().double().cpu().reshape(ref.shape)
+    assert torch.isfinite(got).all(), f"{what}: non-finite values"
+    if ref.numel() == 0:
+        return 0.0, 0.0
+    err = (got - ref).abs()
+    rmax, rmean = ref.abs().max().item(), ref.abs().mean().item()
+    emax, emean = err.max().item(), err.mean().item()
+    print(f"{what}: max|err|/max|ref| {emax / max(rmax, 1e-300):.2e}  "
+          f"mean|err|/mean|ref| {emean / max(rmean, 1e-300):.2e}")
+    assert emax <= g_max * rmax, f"{what}: max|err| {emax:.3e} > {g_max} * {rmax:.3e}"
+    assert emean <= g_mean * rmean, f"{what}: mean|err| {emean:.3e} > {g_mean} * {rmean:.3e}"
+    return emax, emean
+
+
+def draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype=torch.bfloat16):
+    q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed, dtype=dtype)
+    dout = torch.randn(B, Hq, Nq, D, generator=g).to(dtype)
+    return q, k, v, dout
+
+
+def gpu_backward(q, k, v, dout, causal=False, scale=None):
+    """Forward then backward on the GPU, as a training step would run them."""
+    gqa = q.shape[1] != k.shape[1]
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, is_causal=causal, scale=scale, enable_gqa=gqa,
+                          return_lse=True)
+    dq, dk, dv, delta = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, is_causal=causal, scale=scale,
+                                     enable_gqa=gqa, return_delta=True)
+    device_ok()
+    return dq, dk, dv, delta, o
+
+
+def bwd_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, scale=None, dtype=torch.bfloat16):
+    q, k, v, dout = draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype)
+    dq, dk, dv, delta, o = gpu_backward(q, k, v, dout, causal, scale)
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, scale=scale, is_causal=causal)
+    tag = f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D} causal={causal} {dtype}"
+    check_grad(dq, rq, f"{tag} dQ")
+    check_grad(dk, rk, f"{tag} dK")
+    check_grad(dv, rv, f"{tag} dV")
+    # delta is rowsum(dO * O) over the CUDA path's own O
+    want = (dout.double() * o.double().cpu()).sum(-1)
+    scale_d = (dout.double() * o.double().cpu()).abs().sum(-1)
+    assert ((delta.double().cpu() - want).abs() <= 1e-4 * scale_d + 1e-6).all(), f"{tag} delta"
+
+
+# ------------------------------------------------------------------ small, full
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 512, 768, 1024])
+def test_bwd_headdims_ragged(D):
+    bwd_case(1, 2, 2, 300, 300, D, seed=100 + D)
+
+
+@pytest.mark.parametrize("D", [64, 128, 384, 512])
+def test_bwd_causal(D):
+    bwd_case(1, 2, 2, 300, 300, D, seed=200 + D, causal=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_gqa_cross(causal):
+    bwd_case(2, 4, 2, 200, 333, 128, seed=31, causal=causal)
+
+
+def test_bwd_mqa_causal_d512():
+    bwd_case(1, 4, 1, 256, 256, 512, seed=32, causal=True)
+
+
+def test_bwd_fp16_causal():
+    bwd_case(1, 2, 2, 200, 200, 256, seed=33, causal=True, dtype=torch.float16)
+
+
+def test_bwd_explicit_scale():
+    bwd_case(1, 2, 1, 150, 260, 192, seed=34, scale=0.11, causal=True)
+
+
+@pytest.mark.parametrize("Nq,Nkv,causal", [(1, 1, False), (7, 7, True), (1, 300, True), (300, 1, False),
+                                           (129, 127, False), (127, 129, True), (128, 128, True)])
+def test_bwd_lengths(Nq, Nkv, causal):
+    bwd_case(1, 2, 2, Nq, Nkv, 128, seed=Nq * 1000 + Nkv, causal=causal)
+
+
+def test_bwd_strided_views():
+    """[B, N, H, D] storage viewed as [B, H, N, D] (non-contiguous strides)."""
+    g = torch.Generator().manual_seed(35)
+    B, H, Hkv, N, D = 2, 4, 2, 190, 256
+    q = torch.randn(B, N, H, D, generator=g).bfloat16().transpose(1, 2)
+    k = torch.randn(B, N, Hkv, D, generator=g).bfloat16().transpose(1, 2)
+    v = torch.randn(B, N, Hkv, D, generator=g).bfloat16().transpose(1, 2)
+    dout = torch.randn(B, N, H, D, generator=g).bfloat16().transpose(1, 2)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, is_causal=True, enable_gqa=True, return_lse=True)
+    dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, is_causal=True, enable_gqa=True)
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, is_causal=True)
+    check_grad(dq, rq, "strided dQ")
+    check_grad(dk, rk, "strided dK")
+    check_grad(dv, rv, "strided dV")
+
+
+def test_bwd_empty_sides():
+    """No query rows: dK = dV = 0.  No keys: dQ = 0."""
+    q, k, v, dout = draw(1, 2, 2, 0, 200, 128, seed=36)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o = torch.empty_like(qd)
+    lse = torch.empty(1, 2, 0, device=DEV)
+    dk = torch.full_like(kd, float("nan"))
+    dv = torch.full_like(vd, float("nan"))
+    pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, dk=dk, dv=dv)
+    device_ok()
+    assert torch.equal(dk.float().cpu(), torch.zeros(dk.shape)) and torch.equal(dv.float().cpu(), torch.zeros(dv.shape))
+    q, k, v, dout = draw(1, 2, 2, 130, 0, 128, seed=37)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, return_lse=True)
+    dq = torch.full_like(qd, float("nan"))
+    pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, dq=dq)
+    device_ok()
+    assert torch.equal(dq.float().cpu(), torch.zeros(dq.shape))
+
+
+# ------------------------------------------------------------------ large, sampled
+def _sampled(B, Hq, Hkv, N, D, seed, causal, q_heads, kv_heads, n_rows=48):
+    q, k, v, dout = draw(B, Hq, Hkv, N, N, D, seed)
+    dq, dk, dv, _, _ = gpu_backward(q, k, v, dout, causal)
+    g = torch.Generator().manual_seed(seed)
+    edge = [0, 1, 127, 128, N - 129, N - 1]
+    qr = [h * N + i for h in q_heads for i in edge + torch.randint(0, N, (n_rows,), generator=g).tolist()]
+    kr = [h * N + j for h in kv_heads for j in edge + torch.randint(0, N, (n_rows // 2,), generator=g).tolist()]
+    rq, rk, rv = oracle.attn_bwd_rows(q, k, v, dout, qr, kr, is_causal=causal)
+    tag = f"B{B} Hq{Hq} Hkv{Hkv} N{N} D{D} causal={causal}"
+    check_grad(dq.reshape(-1, D)[torch.tensor(qr, device=DEV)], rq, f"{tag} sampled dQ")
+    check_grad(dk.reshape(-1, D)[torch.tensor(kr, device=DEV)], rk, f"{tag} sampled dK")
+    check_grad(dv.reshape(-1, D)[torch.tensor(kr, device=DEV)], rv, f"{tag} sampled dV")
+
+
+def test_bwd_full_size_d512_sampled():
+    """The self-attention workload B1 H16 N4096 D512 on sampled rows."""
+    _sampled(1, 16, 16, 4096, 512, seed=41, causal=False, q_heads=[0, 15], kv_heads=[7])
+
+
+def test_bwd_gqa_causal_d512_sampled():
+    _sampled(1, 8, 2, 2048, 512, seed=42, causal=True, q_heads=[1, 6], kv_heads=[1])
+
+
+# ------------------------------------------------------------------ autograd
+def test_autograd_through_custom_op():
+    q, k, v, dout = draw(1, 4, 2, 260, 260, 512, seed=43)
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    o = pkg.ffpa_attn_func(qd, kd, vd, is_causal=True, enable_gqa=True)
+    o.backward(dout.to(DEV))
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, is_causal=True)
+    check_grad(qd.grad, rq, "autograd dQ")
+    check_grad(kd.grad, rk, "autograd dK")
+    check_grad(vd.grad, rv, "autograd dV")
+
+
+def test_autograd_with_mask_raises():
+    q, k, v, _ = draw(1, 2, 2, 64, 64, 128, seed=44)
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    mask = torch.ones(64, 64, dtype=torch.bool, device=DEV)
+    o = pkg.ffpa_attn_func(qd, kd, vd, attn_mask=mask)
+    with pytest.raises(NotImplementedError):
+        o.sum().backward()
