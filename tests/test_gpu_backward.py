@@ -12,7 +12,10 @@ products accumulate in fp32, and dQ, dK, dV are rounded to 16 bits once
 more.  An output element is a sum of many terms with independent rounding
 errors of relative size ~u, so its error is a few u of the typical output
 magnitude: max |err| <= 2e-2 * max |ref| and mean |err| <= 1e-2 * mean |ref|
-(about 10 u and 5 u).  delta = rowsum(dO * O) is an fp32 dot product of the
+(about 10 u and 5 u), plus an absolute floor of 1e-5 (max) and 1e-6 (mean)
+for gradients that are exactly zero: with a single key the softmax is the
+constant 1, dS = 0 and so dQ = dK = 0, which the kernel reaches only up to
+the fp32 rounding of the LSE (~1e-7 relative).  delta = rowsum(dO * O) is an fp32 dot product of the
 16-bit inputs: relative 1e-4 of sum |dO * O|.
 """
 import pytest
@@ -26,6 +29,7 @@ from tests.gpu_util import device_ok
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 G_MAX, G_MEAN = 2e-2, 1e-2
+G_ABS_MAX, G_ABS_MEAN = 1e-5, 1e-6
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,8 +49,8 @@ def check_grad(got, ref, what, g_max=G_MAX, g_mean=G_MEAN):
     emax, emean = err.max().item(), err.mean().item()
     print(f"{what}: max|err|/max|ref| {emax / max(rmax, 1e-300):.2e}  "
           f"mean|err|/mean|ref| {emean / max(rmean, 1e-300):.2e}")
-    assert emax <= g_max * rmax, f"{what}: max|err| {emax:.3e} > {g_max} * {rmax:.3e}"
-    assert emean <= g_mean * rmean, f"{what}: mean|err| {emean:.3e} > {g_mean} * {rmean:.3e}"
+    assert emax <= g_max * rmax + G_ABS_MAX, f"{what}: max|err| {emax:.3e} > {g_max} * {rmax:.3e}"
+    assert emean <= g_mean * rmean + G_ABS_MEAN, f"{what}: mean|err| {emean:.3e} > {g_mean} * {rmean:.3e}"
     return emax, emean
 
 
