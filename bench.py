@@ -21,6 +21,9 @@ pages' convention 4*B*Hq*Nq*Nkv*D (halved when causal).
 * cpu_baseline: the float64 oracle on a bounded, seeded sample of rows of
   the same workload, on the host cores (rank 0, N = 1 only).
 * --impl reference: the oracle alone, timed per step on bounded samples.
+* --pass bwd: the backward instead (one ffpa_bwd call per step: the delta,
+  dQ and dK/dV kernels) on the same workload, from device-resident Q, K, V,
+  O, dO and LSE; TFLOPS in the usual 2.5x-forward convention.
 
 Multi-GPU (torchrun): independent replicas, one per rank (the path has no
 exchange step); value = all ranks' flops / max over ranks of the time.
@@ -57,6 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--pass", dest="which", choices=("fwd", "bwd"), default="fwd",
+                    help="forward (default) or backward step")
     return ap.parse_args(argv)
 
 
@@ -412,6 +417,177 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+METRIC_BWD = "attn bwd TFLOPS (bf16, D=512; 2.5x forward flops) and % of GB300 dense BF16 peak"
+
+
+def cpu_baseline_bwd(w, x, dout, target_s: float):
+    """The float64 oracle's backward on a bounded seeded sample of dQ rows (each
+    needs its row's softmax, dP and the dQ sum over all keys: 6*Nkv*D useful
+    flops of the backward's 10*Nkv*D per query row)."""
+    import torch
+    import oracle
+    cores = oracle.host_threads()
+    orc = oracle.default()
+    per_row = 6.0 * w.Nkv * w.D / (2.0 if w.causal else 1.0)
+    total_rows = w.B * w.Hq * w.Nq
+    g = torch.Generator().manual_seed(w.seed + 23)
+    n = cores
+    orc.attn_bwd_rows(x["q"], x["k"], x["v"], dout, [0], [], is_causal=w.causal, nthreads=cores)
+    t0 = time.perf_counter()
+    orc.attn_bwd_rows(x["q"], x["k"], x["v"], dout, torch.randint(0, total_rows, (n,), generator=g), [],
+                      is_causal=w.causal, nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(total_rows, max(cores, n * target_s / dt)))
+    n = max(cores, (n // cores) * cores)
+    t0 = time.perf_counter()
+    orc.attn_bwd_rows(x["q"], x["k"], x["v"], dout, torch.randint(0, total_rows, (n,), generator=g), [],
+                      is_causal=w.causal, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": per_row * n / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"dQ of {n} seeded random query rows of {total_rows} (softmax, dP and dQ over "
+                      f"all {w.Nkv} keys each), {dt:.1f} s", "seconds": dt, "rows": n}
+
+
+def run_ours_bwd(args):
+    """One backward per step; same timing, e2e and clock rules as the forward."""
+    import torch
+    import exact_headdim_attention_gb300 as pkg
+    from exact_headdim_attention_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != 1:
+        raise SystemExit("--pass bwd runs on one GPU")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkg.load_library()
+    w = workload_by_name(args.workload)
+    if w.varlen or w.additive_mask:
+        raise SystemExit("--pass bwd takes a dense workload without a mask")
+    x = wl.materialize(w)
+    g = torch.Generator().manual_seed(w.seed + 101)
+    dout = torch.randn(x["q"].shape, generator=g).to(x["q"].dtype)
+    names = ("q", "k", "v")
+    host = {n: x[n].pin_memory() for n in names}
+    host["dout"] = dout.pin_memory()
+    devt = {n: host[n].to(dev) for n in host}
+    o, lse = pkg.ffpa_fwd(devt["q"], devt["k"], devt["v"], is_causal=w.causal,
+                          enable_gqa=w.enable_gqa, return_lse=True)
+    host["o"] = o.cpu().pin_memory()
+    host["lse"] = lse.cpu().pin_memory()
+    devt["o"], devt["lse"] = o, lse
+    flops = 2.5 * wl.useful_flops(w)
+
+    def grads_like(t):
+        return {"dq": torch.empty_like(t["q"]), "dk": torch.empty_like(t["k"]),
+                "dv": torch.empty_like(t["v"]),
+                "delta": torch.empty(t["lse"].shape, dtype=torch.float32, device=dev)}
+
+    def backward(t, gr, stream=None):
+        pkg.ffpa_bwd(t["dout"], t["q"], t["k"], t["v"], t["o"], t["lse"], is_causal=w.causal,
+                     enable_gqa=w.enable_gqa, dq=gr["dq"], dk=gr["dk"], dv=gr["dv"],
+                     delta=gr["delta"], stream=stream)
+
+    gr0 = grads_like(devt)
+
+    def step():
+        backward(devt, gr0)
+
+    # end to end: inputs in, three gradients out; two buffer sets, three streams
+    s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ins = [devt, {n: torch.empty_like(devt[n]) for n in devt}]
+    grs = [gr0, grads_like(devt)]
+    out_host = [{n: torch.empty(grs[0][n].shape, dtype=grs[0][n].dtype, pin_memory=True)
+                 for n in ("dq", "dk", "dv")} for _ in range(2)]
+    ev_in, ev_c, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    state = {"i": 0}
+
+    def e2e():
+        b = state["i"] & 1
+        if state["i"] >= 2:
+            s_in.wait_event(ev_c[b])
+        with torch.cuda.stream(s_in):
+            for n in host:
+                ins[b][n].copy_(host[n], non_blocking=True)
+        ev_in[b].record(s_in)
+        s_c.wait_event(ev_in[b])
+        if state["i"] >= 2:
+            s_c.wait_event(ev_out[b])
+        backward(ins[b], grs[b], stream=s_c)
+        ev_c[b].record(s_c)
+        s_out.wait_event(ev_c[b])
+        with torch.cuda.stream(s_out):
+            for n in out_host[b]:
+                out_host[b][n].copy_(grs[b][n], non_blocking=True)
+        ev_out[b].record(s_out)
+        state["i"] += 1
+
+    def e2e_finish():
+        cur = torch.cuda.current_stream(dev)
+        for st in (s_in, s_c, s_out):
+            cur.wait_stream(st)
+
+    def e2e_start():
+        cur = torch.cuda.current_stream(dev)
+        for st in (s_in, s_c, s_out):
+            st.wait_stream(cur)
+
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host[0].values())
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = pkg.ffpa_last_device_error()
+    if st != pkg.FFPA_OK:
+        raise SystemExit(f"device error during warm-up: {pkg.ffpa_status_string(st)}")
+    sampler = ClockSampler(gpu_id_for(0))
+    sampler.start()
+    elapsed, t0, t1 = time_steps(step, args.steps, False)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    value, tmax = aggregate(elapsed, flops, args.steps, 1, False, dev)
+    for _ in range(3):
+        e2e()
+    e2e_finish()
+    n_e2e = max(3, min(args.e2e_steps, args.steps))
+    e_el, _, _ = time_steps(e2e, n_e2e, False, finish=e2e_finish, start=e2e_start)
+    e_value, _ = aggregate(e_el, flops, n_e2e, 1, False, dev)
+    st = pkg.ffpa_last_device_error()
+    if st != pkg.FFPA_OK:
+        raise SystemExit(f"device error: {pkg.ffpa_status_string(st)}")
+    peak, peak_src, peak_sustained = read_peaks()
+    achieved = value
+    cfg = config_of(w, flops)
+    cfg["pass"] = "backward (delta + dQ + dK/dV kernels)"
+    line = {
+        "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q, K, V, dO; O and LSE from the forward)",
+        "config": cfg,
+        "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": peak_src,
+                     "kernel": "ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_kernel<true> (dQ) + "
+                               "ffpa_bwd_kernel<false> (dK/dV), one C call",
+                     "frac_of_sustained": (round(achieved / peak_sustained, 4)
+                                           if peak_sustained else None),
+                     "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                "api": "exact_headdim_attention_gb300.ffpa_bwd (C ABI ffpa_bwd)",
+                "pipelining": "copy-in, backward and copy-out of consecutive steps on three "
+                              "streams with two buffer sets"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(w, x, dout, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
 def kernel_source_sha() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -490,6 +666,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.which == "bwd":
+        run_ours_bwd(args)
     else:
         run_ours(args)
 

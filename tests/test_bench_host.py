@@ -63,3 +63,15 @@ def test_peaks_fallback_or_measured():
     peak, src, sustained = bench.read_peaks()
     assert peak > 100 and ("fallback" in src or "measured" in src)
     assert sustained is None or 100 < sustained <= peak
+
+
+def test_backward_pass_flag_and_cpu_baseline():
+    import torch
+    from exact_headdim_attention_gb300 import workloads as wl
+    assert bench.parse_args([]).which == "fwd"
+    assert bench.parse_args(["--pass", "bwd"]).which == "bwd"
+    w = wl.tiny_d320()
+    x = wl.materialize(w)
+    dout = torch.randn(x["q"].shape, generator=torch.Generator().manual_seed(3)).to(x["q"].dtype)
+    cb = bench.cpu_baseline_bwd(w, x, dout, 0.05)
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["rows"] >= cb["cores"]
