@@ -120,17 +120,22 @@ def test_bwd_lengths(Nq, Nkv, causal):
 @pytest.mark.parametrize("Nq", [1, 300])
 def test_bwd_single_key(Nq):
     """Nkv = 1: the softmax is the constant 1, so dV_0 = sum_i dO_i and dQ = dK = 0.
-    The forward gives O = V_0 exactly and the recomputed P = exp2(s - lse) is 1
-    within fp32 rounding (2^-22), so the kernel's dS_i is at most 2^-21 |dP_i|:
-    |dQ_i| <= 2^-21 scale |dP_i| max|K_0| and |dK| <= 2^-21 scale sum_i |dP_i| max|Q_i|
-    (with a factor 4 of slack)."""
+    The kernel reaches the zeros up to rounding: the recomputed P = exp2(s - lse)
+    is 1 within fp32 rounding (|P - 1| <= 2^-21), and dP_i = dO_i . V_0 (tensor
+    core) and delta_i = dO_i . O_i (O = V_0 exactly) are the same D products
+    summed in fp32 in different orders, so they differ by at most
+    D * 2^-24 * sum_d |dO_id V_0d| (<= 2^-16 * that sum for D = 128).  Hence
+    |dS_i| <= e_i = 2^-21 |dP_i| + 2^-16 sum_d |dO_id V_0d|, |dQ_i| <= scale e_i
+    max|K_0| and |dK_0| <= scale sum_i e_i max|Q_i|; a factor 2 covers the final
+    16-bit rounding."""
     q, k, v, dout = draw(1, 2, 2, Nq, 1, 128, seed=38 + Nq)
     dq, dk, dv, _, _ = gpu_backward(q, k, v, dout)
     scale = 128 ** -0.5
-    dp = (dout.double() * v.double()).sum(-1).abs()                       # |dO_i . V_0|, [1,2,Nq]
-    bq = 4 * 2.0 ** -21 * scale * dp.unsqueeze(-1) * k.double().abs().amax(-1, keepdim=True)
+    prod = dout.double() * v.double()                                    # [1,2,Nq,128]
+    e = 2.0 ** -21 * prod.sum(-1).abs() + 2.0 ** -16 * prod.abs().sum(-1)   # [1,2,Nq]
+    bq = 2 * scale * e.unsqueeze(-1) * k.double().abs().amax(-1, keepdim=True)
     assert (dq.double().cpu().abs() <= bq).all(), "dQ not zero within the rounding bound"
-    bk = 4 * 2.0 ** -21 * scale * (dp * q.double().abs().amax(-1)).sum(-1)   # [1,2]
+    bk = 2 * scale * (e * q.double().abs().amax(-1)).sum(-1)               # [1,2]
     assert (dk.double().cpu().abs().amax(-1).squeeze(-1) <= bk).all(), "dK not zero within the bound"
     check_grad(dv, dout.double().sum(2, keepdim=True), f"Nq{Nq} Nkv1 dV")
 
