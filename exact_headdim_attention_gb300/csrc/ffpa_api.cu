@@ -443,10 +443,6 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.nslot_kv = static_cast<int>(ns_kv);
   const size_t dq_smem = 1024 + P_TILE_BYTES + ns_dq * SLOT_BYTES;
   const size_t kv_smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns_kv * SLOT_BYTES;
-  // Clusters of the slice CTAs of one tile (at most 8: D <= 1024); the dQ
-  // slices form one only when all have the same box count (D % 256 == 0).
-  P.cl_kv = P.n_sl_kv;
-  P.cl_dq = D % BWD_DQ_COLS == 0 ? P.n_sl_dq : 1;
   P.scale = sc;
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;

@@ -28,11 +28,7 @@
 // The contractions of iteration i+1 are issued before the slice MMAs of
 // iteration i, so the tensor core works while the elementwise warps run.
 // When D exceeds the output columns of one CTA, the CTAs of the other
-// column slices recompute S and dP.  Those CTAs form a thread-block cluster
-// (cluster rank = slice) and load the contraction operands once: box k of
-// the common sequence is fetched by rank k mod C with TMA multicast into
-// every CTA's ring, and a ring slot is refilled only after all C CTAs have
-// released it (their MMA completions arrive on every CTA's empty barrier).
+// column slices recompute S and dP.
 #include "ffpa_common.cuh"
 
 namespace ffpa {
@@ -209,9 +205,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   const int npairs = p.npairs, nchunks = p.nchunks;
   const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
   const int NS = DQ ? p.nslot_dq : p.nslot_kv;
-  const int C = DQ ? p.cl_dq : p.cl_kv;             // CTAs sharing the contraction operands
-  const uint32_t crank = C > 1 ? cluster_ctarank() : 0u;
-  const uint16_t cmask = (uint16_t)((1u << C) - 1u);
   const int T = it.n_iter;
   const unsigned long long tmo = p.timeout_ns;
   extern __shared__ uint8_t smem_raw[];
@@ -234,7 +227,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bar_full[i]), 1);
-      mbar_init(smem_u32(&bar_empty[i]), (uint32_t)C);   // one release per CTA of the cluster
+      mbar_init(smem_u32(&bar_empty[i]), 1);
     }
     mbar_init(smem_u32(&bar_sd_full), 1);
     mbar_init(smem_u32(&bar_s_free), 4);
@@ -250,7 +243,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
-  if (C > 1) cluster_sync_all();   // every CTA's barriers exist before any multicast or remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
@@ -275,26 +267,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       prefetch_tmap(&p.tm_v);
       prefetch_tmap(&p.tm_do);
       const uint32_t box_bytes = (uint32_t)p.kchunks * CHUNK_BYTES;
-      int slot = 0, issued = 0, shared_k = 0;
+      int slot = 0, issued = 0;
       uint32_t lap = 0;
-      // shared: a contraction box common to the cluster (fetched by rank
-      // k mod C, multicast); otherwise this CTA's own slice box.
-      auto load = [&](const CUtensorMap* m, int row, int chunk, int head, bool shared) -> bool {
+      auto load = [&](const CUtensorMap* m, int row, int chunk, int head) -> bool {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
-        if (C > 1) {
-          if (!wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, true)) return false;
-        } else if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) {
-          return false;
-        }
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) return false;
         const uint32_t fb = smem_u32(&bar_full[slot]);
-        const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
         mbar_arrive_expect_tx(fb, box_bytes);
-        if (!shared || C == 1) {
-          tma_load_5d(dst, m, fb, 0, row, chunk, head, it.b);
-        } else if ((uint32_t)(shared_k % C) == crank) {
-          tma_load_5d_mc(dst, m, fb, 0, row, chunk, head, it.b, cmask);
-        }
-        if (shared) ++shared_k;
+        tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
         ++issued;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return true;
@@ -308,9 +288,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         int hs, rs;
         stream_coords(i, hs, rs);
         for (int pr = 0; pr < npairs; ++pr)
-          if (!load(a1, it.row0, 2 * pr, ha, true) || !load(b1, rs, 2 * pr, hs, true)) return false;
+          if (!load(a1, it.row0, 2 * pr, ha) || !load(b1, rs, 2 * pr, hs)) return false;
         for (int pr = 0; pr < npairs; ++pr)
-          if (!load(a2, it.row0, 2 * pr, ha, true) || !load(b2, rs, 2 * pr, hs, true)) return false;
+          if (!load(a2, it.row0, 2 * pr, ha) || !load(b2, rs, 2 * pr, hs)) return false;
         return true;
       };
       auto slice_loads = [&](int i) -> bool {
@@ -319,10 +299,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         const int c0 = it.col_lo / DK;
         if (DQ) {
           for (int bx = 0; bx < nbox; ++bx)
-            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs, false)) return false;
+            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs)) return false;
           return true;
         }
-        return load(&p.tm_do, rs, c0, hs, false) && load(&p.tm_q, rs, c0, hs, false);
+        return load(&p.tm_do, rs, c0, hs) && load(&p.tm_q, rs, c0, hs);
       };
       // Same order as the MMA thread consumes: contractions of iteration 0,
       // then per iteration i the contractions of i+1 and the slices of i.
@@ -352,14 +332,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return s;
       };
-      // A slot is released to every CTA of the cluster: the next box in it
-      // may be multicast by any of them.
-      auto release = [&](int s) {
-        if (C > 1)
-          umma_commit_mc(smem_u32(&bar_empty[s]), cmask);
-        else
-          umma_commit(smem_u32(&bar_empty[s]));
-      };
+      auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
       auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
         if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
         tc_fence_after();
@@ -592,31 +565,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
-  // No CTA leaves while another may still multicast into it or arrive on
-  // its barriers.
-  if (C > 1) cluster_sync_all();
-}
-
-// One launch of `kern` over `items` CTAs in clusters of `cluster` (1: none).
-static ffpa_status launch_clustered(void (*kern)(BwdParams), const BwdParams& P, int items, int cluster,
-                                    size_t smem, cudaStream_t stream) {
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return FFPA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)items, 1, 1);
-  cfg.blockDim = dim3(BWD_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = cluster > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return FFPA_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
 ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
@@ -626,10 +574,20 @@ ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq
     ffpa_bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
-  if (dq_items > 0 && launch_clustered(ffpa_bwd_kernel<true>, P, dq_items, P.cl_dq, dq_smem, stream) != FFPA_OK)
-    return FFPA_ERR_CUDA;
-  if (kv_items > 0 && launch_clustered(ffpa_bwd_kernel<false>, P, kv_items, P.cl_kv, kv_smem, stream) != FFPA_OK)
-    return FFPA_ERR_CUDA;
+  if (dq_items > 0) {
+    if (cudaFuncSetAttribute(ffpa_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(dq_smem)) != cudaSuccess)
+      return FFPA_ERR_CUDA;
+    ffpa_bwd_kernel<true><<<dq_items, BWD_THREADS, dq_smem, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+  }
+  if (kv_items > 0) {
+    if (cudaFuncSetAttribute(ffpa_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kv_smem)) != cudaSuccess)
+      return FFPA_ERR_CUDA;
+    ffpa_bwd_kernel<false><<<kv_items, BWD_THREADS, kv_smem, stream>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+  }
   return FFPA_OK;
 }
 

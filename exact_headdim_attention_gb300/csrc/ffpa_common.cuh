@@ -120,7 +120,6 @@ struct BwdParams {
   int nchunks, npairs, kchunks;
   int n_qt, n_kt, n_sl_dq, n_sl_kv;
   int nslot_dq, nslot_kv;
-  int cl_dq, cl_kv;    // cluster sizes (the slice CTAs of one tile share the contraction operands)
   float scale, scale_log2;
   int causal, fp16;
   unsigned long long timeout_ns;

@@ -169,18 +169,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* m, 
 }
 
 // L2 prefetch of a tensor box (no shared-memory destination, no barrier).
-// As tma_load_5d, multicast: the box lands at the same shared-memory offset
-// in every CTA of the cluster named in cta_mask, and each destination's
-// mbarrier at offset `bar` receives the completed bytes.
-__device__ __forceinline__ void tma_load_5d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                               int c1, int c2, int c3, int c4, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-      "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* m, int c0, int c1, int c2, int c3) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
