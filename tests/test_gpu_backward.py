@@ -84,7 +84,7 @@ def bwd_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, scale=None, dtype=torch
 
 
 # ------------------------------------------------------------------ small, full
-@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 512, 768, 1024])
+@pytest.mark.parametrize("D", [64, 128, 192, 256, 320, 448, 512, 640, 768, 1024])
 def test_bwd_headdims_ragged(D):
     bwd_case(1, 2, 2, 300, 300, D, seed=100 + D)
 
