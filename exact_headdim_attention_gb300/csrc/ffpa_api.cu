@@ -103,7 +103,7 @@ ffpa_status check_device(const void* ptr, int* dev_out) {
 // decides whether Q stays resident in shared memory (D <= 512) and how many
 // 32 KB ring slots fit beside it.  Returns the dynamic shared memory bytes.
 size_t plan(int D, Params* P) {
-  P->nchunks = D / DK;
+  P->nchunks = (D + DK - 1) / DK;   // a head dim below a multiple of 64 is zero-padded
   P->n_slices = (D + DV_MAX - 1) / DV_MAX;
   const int max_dv = ((P->nchunks + P->n_slices - 1) / P->n_slices) * DK;
   P->vchunks = max_dv / DK;
@@ -129,6 +129,7 @@ size_t plan(int D, Params* P) {
 // The CTA-pair kernel needs every output slice to split into two halves of
 // whole 64-column chunks, Q resident, and K stages of equal chunk count.
 bool pair_eligible(int D) {
+  if (D % DK != 0) return false;
   const int nchunks = D / DK;
   if (nchunks > Q_RESIDENT_MAX_CHUNKS) return false;
   const int n_slices = (D + DV_MAX - 1) / DV_MAX;
@@ -153,6 +154,7 @@ bool split_eligible(int D) { return D >= 128 && D % 128 == 0 && D / 2 <= DV_MAX;
 // varlen batches of mixed lengths the 256-row pair tiles waste more rows on
 // short sequences than they save.
 Kern choose_kernel(int D, bool varlen) {
+  if (D % DK != 0) return Kern::SINGLE;   // only the single-CTA kernel takes zero-padded chunks
   const int v = g_variant.load();
   if (v == FFPA_VARIANT_SINGLE) return Kern::SINGLE;
   if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
@@ -245,7 +247,7 @@ void ffpa_set_kernel_variant(int variant) {
 }
 
 int ffpa_selected_kernel(int D, int varlen) {
-  if (D < 64 || D > 1024 || D % 64 != 0) return -1;
+  if (D < 64 || D > 1024 || D % (varlen ? 64 : 8) != 0) return -1;
   const Kern kn = choose_kernel(D, varlen != 0);
   return kn == Kern::PAIR ? FFPA_VARIANT_PAIR : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT : FFPA_VARIANT_SINGLE;
 }
@@ -272,7 +274,7 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
                      ffpa_stream_t stream) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
-  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (D < 64 || D > 1024 || D % 8 != 0) return FFPA_ERR_UNSUPPORTED;
   if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
@@ -305,20 +307,37 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   const uint32_t k_rows = pair ? BN / 2 : BN;
   const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
   const uint64_t nch = (uint64_t)P.nchunks;
-  {
+  P.dfine = D % DK != 0;
+  if (P.dfine) {
+    // (D, N, H, B) views with one 64-column box per chunk: the TMA unit
+    // zero-fills the columns past D of the last chunk.
+    const uint64_t dq4[4] = {(uint64_t)D, (uint64_t)Nq, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t sq[3] = {(uint64_t)q_str[2] * 2, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
+    const uint32_t bq[4] = {64, BM, 1, 1};
+    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq4, sq, bq)) != FFPA_OK) return st;
+    if (Nkv > 0) {
+      const uint64_t dk4[4] = {(uint64_t)D, (uint64_t)Nkv, (uint64_t)Hkv, (uint64_t)B};
+      const uint64_t sk[3] = {(uint64_t)k_str[2] * 2, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
+      const uint64_t sv[3] = {(uint64_t)v_str[2] * 2, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
+      const uint32_t bk[4] = {64, BN, 1, 1};
+      const uint32_t bv[4] = {64, (uint32_t)P.vk, 1, 1};
+      if ((st = encode_map(&P.tm_k, tdt, 4, k, dk4, sk, bk)) != FFPA_OK) return st;
+      if ((st = encode_map(&P.tm_v, tdt, 4, v, dk4, sv, bv)) != FFPA_OK) return st;
+    }
+  } else {
     const uint64_t dq[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
     const uint64_t sq[4] = {(uint64_t)q_str[2] * 2, 128, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
     const uint32_t bq[5] = {64, BM, (uint32_t)P.kchunks, 1, 1};
     if ((st = encode_map(&P.tm_q, tdt, 5, q, dq, sq, bq)) != FFPA_OK) return st;
-  }
-  if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
-    const uint64_t dk[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
-    const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
-    const uint32_t bk[5] = {64, k_rows, k_box_chunks, 1, 1};
-    if ((st = encode_map(&P.tm_k, tdt, 5, k, dk, sk, bk)) != FFPA_OK) return st;
-    const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
-    const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
-    if ((st = encode_map(&P.tm_v, tdt, 5, v, dk, sv, bv)) != FFPA_OK) return st;
+    if (Nkv > 0) {   // with no keys no work item issues a copy; the maps stay unused
+      const uint64_t dk[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
+      const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
+      const uint32_t bk[5] = {64, k_rows, k_box_chunks, 1, 1};
+      if ((st = encode_map(&P.tm_k, tdt, 5, k, dk, sk, bk)) != FFPA_OK) return st;
+      const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
+      const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
+      if ((st = encode_map(&P.tm_v, tdt, 5, v, dk, sv, bv)) != FFPA_OK) return st;
+    }
   }
   P.o = o;
   P.lse = lse;

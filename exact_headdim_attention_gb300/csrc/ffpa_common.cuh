@@ -149,6 +149,10 @@ struct Params {
   int qt_chunks;       // column-split kernel: Q chunks held in TMEM
   float scale_log2;
   int causal, fp16, inject;
+  // Dense head dims that are not a multiple of 64 (D % 8 == 0): the maps
+  // are 4-D (D, N, H, B) with one 64-column box per chunk, so columns >= D
+  // arrive as zeros (single-CTA kernel only).
+  int dfine;
   unsigned long long timeout_ns;
 };
 
@@ -351,6 +355,7 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
             (long long)row * p.o_str[2];
     obase = static_cast<uint8_t*>(p.o) + (off + it.col_lo) * 2;
   }
+  const int dcols = min(it.dv, p.D - it.col_lo);   // columns >= D are zero padding
   for (int c0 = 0; c0 < it.dv; c0 += 32) {
     uint32_t o[32];
     if (have_o) {
@@ -372,7 +377,8 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
       uint4* dst = reinterpret_cast<uint4*>(obase + c0 * 2);
 #pragma unroll
       for (int v4 = 0; v4 < 4; ++v4)
-        dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
+        if (c0 + 8 * v4 < dcols)
+          dst[v4] = make_uint4(pkd[4 * v4], pkd[4 * v4 + 1], pkd[4 * v4 + 2], pkd[4 * v4 + 3]);
     }
   }
   if (row_valid && p.lse != nullptr && it.slice == 0) {

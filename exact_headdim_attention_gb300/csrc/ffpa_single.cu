@@ -112,9 +112,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
         mbar_arrive_expect_tx(fb, bytes);
         return dst;
       };
+      // Fine head dims: one 4-D box per 64-column chunk (x = 64 c), chunks
+      // `stride` bytes apart; columns >= D are zero-filled.
+      const bool fine = !VARLEN && p.dfine != 0;
+      auto load_fine = [&](uint32_t dst, const CUtensorMap* m, uint32_t fb, int chunk0, int nch,
+                           uint32_t stride, int row, int head) {
+        for (int c = 0; c < nch; ++c)
+          tma_load_4d(dst + c * stride, m, fb, DK * (chunk0 + c), row, head, it.b);
+      };
       auto load_q_pair = [&](uint32_t dst, uint32_t fb, int pr) {
         if (VARLEN)
           tma_load_4d(dst, &p.tm_q, fb, 0, it.q_row0 + it.q0, 2 * pr, it.hq);
+        else if (fine)
+          load_fine(dst, &p.tm_q, fb, 2 * pr, kchunks, CHUNK_BYTES, it.q0, it.hq);
         else
           tma_load_5d(dst, &p.tm_q, fb, 0, it.q0, 2 * pr, it.hq, it.b);
       };
@@ -138,6 +148,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
             if (dst) {
               if (VARLEN)
                 tma_load_4d(dst, &p.tm_k, fb, 0, it.kv_row0 + key0, 2 * pr, it.hkv);
+              else if (fine)
+                load_fine(dst, &p.tm_k, fb, 2 * pr, kchunks, CHUNK_BYTES, key0, it.hkv);
               else
                 tma_load_5d(dst, &p.tm_k, fb, 0, key0, 2 * pr, it.hkv, it.b);
             }
@@ -153,6 +165,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
             const int key = kv_tile(it, j) * BN + h * vk;
             if (VARLEN)
               tma_load_4d(dst, &p.tm_v, fb, 0, it.kv_row0 + key, it.col_lo / DK, it.hkv);
+            else if (fine)
+              load_fine(dst, &p.tm_v, fb, it.col_lo / DK, p.vchunks, (uint32_t)vk * 128u, key, it.hkv);
             else
               tma_load_5d(dst, &p.tm_v, fb, 0, key, it.col_lo / DK, it.hkv, it.b);
           }

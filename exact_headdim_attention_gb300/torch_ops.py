@@ -8,7 +8,8 @@ binding.  ``ffpa_attn_func`` takes the argument list of
 ``torch.nn.functional.scaled_dot_product_attention`` (the FFPA API
 reference, ``ffpa_attn.ffpa_attn_func``, uses the same list), so it can
 replace that call for the supported cases: bf16/fp16 CUDA tensors,
-64 <= D <= 1024 with D % 64 == 0, no dropout.  The dense operator is
+64 <= D <= 1024 with D % 8 == 0 (D % 64 == 0 for varlen and for the
+backward), no dropout.  The dense operator is
 differentiable through ``ffpa_bwd`` (the backward kernels) when it was
 called without attn_mask; the varlen operator registers no backward.
 """

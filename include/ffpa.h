@@ -78,7 +78,10 @@ typedef enum {
  *   enable_gqa: must be nonzero when Hq != Hkv (API reference, `enable_gqa`).
  *
  * Checks, in order: dt (FFPA_ERR_DTYPE); sizes >= 0, Hq, Hkv >= 1
- * (INVALID); 64 <= D <= 1024 and D % 64 == 0 (UNSUPPORTED); Hq % Hkv,
+ * (INVALID); 64 <= D <= 1024 and D % 8 == 0 (UNSUPPORTED; a D that is not a
+ * multiple of 64 is zero-padded to whole 64-column chunks and runs on the
+ * single-CTA kernel; README "End-to-End Inference": head dims divisible by
+ * 8, e.g. 120); Hq % Hkv,
  * enable_gqa, causal with Nkv < Nq, null pointers, strides, alignment, mask
  * kind, non-finite scale (INVALID); device is sm_103 (UNSUPPORTED).  An
  * empty problem (B, Hq or Nq zero) returns FFPA_OK without launching; Nkv
@@ -106,8 +109,9 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
  *
  * cu_seqlens live on the device and are not read by the host: a malformed
  * array is a caller precondition (the Python binding checks it on the host).
- * Other checks and error codes as for ffpa_fwd; nseq < 1 or max_seqlen_* < 0
- * is FFPA_ERR_INVALID.
+ * Other checks and error codes as for ffpa_fwd, except that D must be a
+ * multiple of 64 ("large 64-aligned head dims"; else FFPA_ERR_UNSUPPORTED);
+ * nseq < 1 or max_seqlen_* < 0 is FFPA_ERR_INVALID.
  */
 ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
@@ -139,8 +143,9 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
  *     forward that produced o and lse).
  *
  * Strides follow the ffpa_fwd rules (last stride 1, others multiples of 16
- * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd;
- * a NULL lse or delta is FFPA_ERR_INVALID.  B == 0 or Nq == 0 with Nkv > 0
+ * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd,
+ * except that D must be a multiple of 64 (else FFPA_ERR_UNSUPPORTED); a NULL
+ * lse or delta is FFPA_ERR_INVALID.  B == 0 or Nq == 0 with Nkv > 0
  * writes zero dk and dv; Nkv == 0 writes zero dq.  Three launches on
  * `stream`; no allocation, no synchronisation.
  */

@@ -175,7 +175,8 @@ def test_selected_kernel_follows_the_choice(lib):
         pkg.set_kernel_variant("auto")
     assert lib.ffpa_selected_kernel(100, 0) == -1
     with pytest.raises(ValueError):
-        pkg.selected_kernel(96)
+        pkg.selected_kernel(100)                          # not a multiple of 8
+    assert pkg.selected_kernel(96) == "single"            # zero-padded to two chunks
 
 
 def bwd_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,
@@ -220,3 +221,31 @@ def test_bwd_binding_checks(lib):
         pkg.ffpa_bwd(q, q, q, q, q[:, :, :3], lse)                # out shape
     with pytest.raises(TypeError):
         pkg.ffpa_bwd(q.half(), q, q, q, q, lse)                   # mixed dtypes
+
+
+def test_fine_head_dims_dense_only(lib):
+    """Dense head dims divisible by 8 are accepted (zero-padded chunks, single-CTA
+    kernel); varlen and the backward keep whole 64-column chunks."""
+    UNSUP = pkg.FFPA_ERR_UNSUPPORTED
+    assert dense_call(lib, D=72) != UNSUP
+    assert dense_call(lib, D=1000) != UNSUP
+    assert dense_call(lib, D=100) == UNSUP
+    assert varlen_call(lib, D=72) == UNSUP
+    assert bwd_call(lib, D=72) == UNSUP
+    pkg.set_kernel_variant("auto")
+    assert pkg.selected_kernel(72) == "single"
+    assert pkg.selected_kernel(520) == "single"
+    with pytest.raises(ValueError):
+        pkg.selected_kernel(72, varlen=True)
+    try:
+        pkg.set_kernel_variant("split")
+        assert pkg.selected_kernel(120) == "single"
+        pkg.set_kernel_variant("pair")
+        assert pkg.selected_kernel(192 + 8) == "single"
+    finally:
+        pkg.set_kernel_variant("auto")
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_fine_head_dim_valid_call_without_gpu(lib):
+    assert dense_call(lib, D=120) == pkg.FFPA_ERR_CUDA

@@ -57,6 +57,33 @@ def test_headdims_ragged(D):
     dense_case(1, 2, 2, 300, 300, D, seed=D)
 
 
+@pytest.mark.parametrize("D", [72, 120, 200, 264, 520, 1000])
+def test_fine_headdims_ragged(D):
+    """Head dims divisible by 8 but not by 64: zero-padded 64-column chunks."""
+    dense_case(1, 2, 2, 300, 300, D, seed=5000 + D)
+
+
+def test_fine_headdim_causal_gqa_cross():
+    dense_case(2, 4, 2, 200, 333, 120, seed=5001, causal=True)
+
+
+def test_fine_headdim_additive_mask_fp16():
+    B, H, Nq, Nk = 1, 2, 190, 260
+    dense_case(B, H, H, Nq, Nk, 200, seed=5002, dtype=torch.float16,
+               mask=lambda g: torch.randn(B, 1, Nq, Nk, generator=g))
+
+
+def test_fine_headdim_leaves_padding_untouched():
+    """Only D columns are written: a strided O with room past D keeps its sentinel."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 150, 150, 72, seed=5003)
+    big = torch.full((1, 2, 150, 80), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = big[..., :72]
+    o, l = run_dense(q, k, v, out=out)
+    o_ref, l_ref = oracle.attn_dense(q, k, v)
+    check(out, l, o_ref, l_ref, "fine D=72 strided out")
+    assert torch.isnan(big[..., 72:].float()).all()
+
+
 @pytest.mark.parametrize("Nq,Nkv", [(1, 1), (7, 7), (127, 129), (129, 127), (1, 300), (300, 1),
                                     (64, 513), (256, 256)])
 @pytest.mark.parametrize("D", [128, 512])
