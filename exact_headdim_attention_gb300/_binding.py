@@ -77,7 +77,7 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
                                     I, I, P]
     lib.ffpa_fwd_varlen.restype = I
     lib.ffpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
-                             P, P, I, I, P]
+                             P, P, I, P, P, I, I, P]
     lib.ffpa_bwd.restype = I
     lib.ffpa_status_string.argtypes = [I]
     lib.ffpa_status_string.restype = ctypes.c_char_p
@@ -167,29 +167,7 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
     if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
                             or tuple(lse.shape) != (B, Hq, Nq)):
         raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
-    mk, mptr, mstr, keep = FFPA_MASK_NONE, None, None, None
-    if attn_mask is not None:
-        m = attn_mask
-        if m.dim() > 4:
-            raise ValueError("attn_mask has more than 4 dimensions")
-        while m.dim() < 4:
-            m = m.unsqueeze(0)
-        try:
-            m = m.expand(B, Hq, Nq, Nkv)
-        except RuntimeError as e:
-            raise ValueError(f"attn_mask {tuple(attn_mask.shape)} does not broadcast to "
-                             f"{(B, Hq, Nq, Nkv)}") from e
-        if m.device != q.device:
-            raise ValueError("attn_mask must be on the same device as q")
-        if m.dtype == torch.bool:
-            mk = FFPA_MASK_BOOL
-        elif m.dtype == torch.float32:
-            mk = FFPA_MASK_ADD_F32
-        elif m.dtype == q.dtype:
-            mk = FFPA_MASK_ADD_QTYPE
-        else:
-            raise TypeError(f"attn_mask dtype {m.dtype} not supported (bool, float32 or {q.dtype})")
-        keep, mptr, mstr = m, m.data_ptr(), _strides(m)
+    mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
     st = lib.ffpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                       None if lse is None else lse.data_ptr(), _dtype_code(q),
@@ -202,15 +180,43 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
     return (out, lse) if return_lse else out
 
 
+def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
+    """(kind, pointer, strides, keep-alive) of a mask broadcast to [B,Hq,Nq,Nkv]."""
+    if attn_mask is None:
+        return FFPA_MASK_NONE, None, None, None
+    m = attn_mask
+    if m.dim() > 4:
+        raise ValueError("attn_mask has more than 4 dimensions")
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    try:
+        m = m.expand(B, Hq, Nq, Nkv)
+    except RuntimeError as e:
+        raise ValueError(f"attn_mask {tuple(attn_mask.shape)} does not broadcast to "
+                         f"{(B, Hq, Nq, Nkv)}") from e
+    if m.device != q.device:
+        raise ValueError("attn_mask must be on the same device as q")
+    if m.dtype == torch.bool:
+        mk = FFPA_MASK_BOOL
+    elif m.dtype == torch.float32:
+        mk = FFPA_MASK_ADD_F32
+    elif m.dtype == q.dtype:
+        mk = FFPA_MASK_ADD_QTYPE
+    else:
+        raise TypeError(f"attn_mask dtype {m.dtype} not supported (bool, float32 or {q.dtype})")
+    return mk, m.data_ptr(), _strides(m), m
+
+
 def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
              out: torch.Tensor, lse: torch.Tensor, is_causal: bool = False,
-             scale: float | None = None, enable_gqa: bool = False, *, dq=None, dk=None, dv=None,
-             delta=None, return_delta: bool = False, stream=None):
-    """Dense attention backward through the C ABI ``ffpa_bwd`` (no attn_mask).
+             scale: float | None = None, enable_gqa: bool = False, attn_mask=None, *, dq=None,
+             dk=None, dv=None, delta=None, return_delta: bool = False, stream=None):
+    """Dense attention backward through the C ABI ``ffpa_bwd``.
 
     dout, q, out [B,Hq,Nq,D]; k, v [B,Hkv,Nkv,D]; lse [B,Hq,Nq] fp32 from the
-    forward with the same is_causal / scale.  Returns (dq, dk, dv), plus
-    delta = rowsum(dout * out) [B,Hq,Nq] fp32 with return_delta."""
+    forward with the same attn_mask / is_causal / scale (the mask enters the
+    recomputed scores; no gradient is formed for it).  Returns (dq, dk, dv),
+    plus delta = rowsum(dout * out) [B,Hq,Nq] fp32 with return_delta."""
     lib = load_library()
     for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
         if t.dim() != 4:
@@ -235,12 +241,15 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
         delta = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
     if delta.dtype != torch.float32 or not delta.is_contiguous() or tuple(delta.shape) != (B, Hq, Nq):
         raise ValueError("delta must be a contiguous float32 [B, Hq, Nq] tensor")
+    mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
     st = lib.ffpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
                       _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v),
-                      _strides(out), _strides(dout), _strides(dq), _strides(dk), _strides(dv), sc,
-                      int(bool(is_causal)), int(bool(enable_gqa)), _stream_handle(stream, q))
+                      _strides(out), _strides(dout), _strides(dq), _strides(dk), _strides(dv), mptr,
+                      mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
+                      _stream_handle(stream, q))
+    del keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)

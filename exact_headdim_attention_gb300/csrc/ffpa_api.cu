@@ -372,7 +372,8 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
                      const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
                      const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
-                     const int64_t dv_str[4], const float* scale, int is_causal, int enable_gqa,
+                     const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
@@ -380,9 +381,15 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
+  if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
   const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
   if (B == 0 || (Nq == 0 && Nkv == 0)) return FFPA_OK;   // nothing to write
+  if (mask_kind != FFPA_MASK_NONE && Nq > 0 && Nkv > 0) {
+    if (!mask || !mask_str) return FFPA_ERR_INVALID;
+    for (int i = 0; i < 4; ++i)
+      if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+  }
   if (!q_str || !k_str || !v_str || !o_str || !do_str || !dq_str || !dk_str || !dv_str)
     return FFPA_ERR_INVALID;
   const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
@@ -430,6 +437,10 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.o = o;
   P.dout = dout;
   P.lse = lse;
+  const bool umask = mask_kind != FFPA_MASK_NONE && Nq > 0 && Nkv > 0;
+  P.mask = umask ? mask : nullptr;
+  P.mask_kind = umask ? mask_kind : FFPA_MASK_NONE;
+  for (int i = 0; i < 4; ++i) P.m_str[i] = umask ? mask_str[i] : 0;
   P.delta = delta;
   P.dq = dq;
   P.dk = dk;

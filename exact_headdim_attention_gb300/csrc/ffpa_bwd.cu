@@ -174,6 +174,18 @@ __device__ __forceinline__ void bwd_write_tile_row(uint32_t tile, int r, const u
                  pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
 }
 
+// The caller's mask term for one score, in the log2 domain: the bool mask
+// turns the exponent argument into -inf where false; an additive mask adds
+// its value times log2(e).  off is the element offset from base.
+__device__ __forceinline__ float add_mask_term(float arg, const uint8_t* base, long long off, int kind,
+                                               bool fp16) {
+  if (kind == FFPA_MASK_BOOL) return base[off] != 0 ? arg : -INFINITY;
+  if (kind == FFPA_MASK_ADD_F32) return arg + __ldg(reinterpret_cast<const float*>(base) + off) * LOG2E_F;
+  const uint16_t h = __ldg(reinterpret_cast<const unsigned short*>(base) + off);
+  const float hv = fp16 ? __half2float(__ushort_as_half(h)) : __bfloat162float(__ushort_as_bfloat16(h));
+  return arg + hv * LOG2E_F;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(256) ffpa_bwd_delta_kernel(const __grid_constant__ BwdParams p) {
@@ -197,7 +209,8 @@ __global__ void __launch_bounds__(256) ffpa_bwd_delta_kernel(const __grid_consta
   if (lane == 0) p.delta[row] = acc;
 }
 
-template <bool DQ>
+// UMASK: launched with a caller's mask (mask-loading code present).
+template <bool DQ, bool UMASK>
 __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_constant__ BwdParams p) {
   BwdItem it;
   if (!bwd_decode<DQ>(p, blockIdx.x, it)) return;   // uniform across the CTA
@@ -420,6 +433,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       delta_r = p.delta[li];
     }
     float* st = stat_sh + (DQ ? 0 : warp * 2 * BM);   // [lse(128) | delta(128)] of this warp
+    // Caller's mask: element (query, key) at b m0 + hq m1 + query m2 + key m3.
+    const int mkind = p.mask_kind;
+    const uint8_t* mbase = static_cast<const uint8_t*>(p.mask);
+    const bool mrow_ok = DQ ? my_row < p.Nq : my_row < p.Nkv;
     const uint32_t st_u32 = smem_u32(st);
     bool ok = true;
     for (int i = 0; i < T; ++i) {
@@ -455,6 +472,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       const long long lim = DQ ? (long long)my_row + off - rs      // last visible column
                                : (long long)my_row - off - rs;     // first visible column
       const int kv_cols = p.Nkv - rs;                              // dQ: key columns in range
+      // Mask offset of this row at column 0 of the tile, step per column, and
+      // the columns in range (dQ: keys; dK/dV: queries of head hs).
+      long long moff = 0, mstep = 0;
+      int mcols = 0;
+      if (UMASK) {
+        if (DQ) {
+          moff = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
+                 (long long)my_row * p.m_str[2] + (long long)rs * p.m_str[3];
+          mstep = p.m_str[3];
+          mcols = mrow_ok ? p.Nkv - rs : 0;
+        } else {
+          moff = (long long)it.b * p.m_str[0] + (long long)hs * p.m_str[1] +
+                 (long long)rs * p.m_str[2] + (long long)my_row * p.m_str[3];
+          mstep = p.m_str[2];
+          mcols = mrow_ok ? p.Nq - rs : 0;
+        }
+      }
       uint32_t ppk[DQ ? 1 : BN / 2];
       uint32_t dpk[BN / 2];
 #pragma unroll
@@ -493,7 +527,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int col = 16 * g + c + e;
-            float v = ex2_approx(fmaf(__uint_as_float(sr[c + e]), sl2, -l16[c + e]));
+            float arg = fmaf(__uint_as_float(sr[c + e]), sl2, -l16[c + e]);
+            if (UMASK && col < mcols) arg = add_mask_term(arg, mbase, moff + col * mstep, mkind, fp16);
+            float v = ex2_approx(arg);
             if (need_mask) {
               const bool vis = DQ ? (col < kv_cols && (!causal || (long long)col <= lim))
                                   : ((long long)col >= lim);
@@ -574,18 +610,21 @@ ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq
     ffpa_bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
+  const bool umask = P.mask != nullptr;
+  auto kdq = umask ? ffpa_bwd_kernel<true, true> : ffpa_bwd_kernel<true, false>;
+  auto kkv = umask ? ffpa_bwd_kernel<false, true> : ffpa_bwd_kernel<false, false>;
   if (dq_items > 0) {
-    if (cudaFuncSetAttribute(ffpa_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(dq_smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem)) !=
+        cudaSuccess)
       return FFPA_ERR_CUDA;
-    ffpa_bwd_kernel<true><<<dq_items, BWD_THREADS, dq_smem, stream>>>(P);
+    kdq<<<dq_items, BWD_THREADS, dq_smem, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
   if (kv_items > 0) {
-    if (cudaFuncSetAttribute(ffpa_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kv_smem)) != cudaSuccess)
+    if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kv_smem)) !=
+        cudaSuccess)
       return FFPA_ERR_CUDA;
-    ffpa_bwd_kernel<false><<<kv_items, BWD_THREADS, kv_smem, stream>>>(P);
+    kkv<<<kv_items, BWD_THREADS, kv_smem, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
   return FFPA_OK;

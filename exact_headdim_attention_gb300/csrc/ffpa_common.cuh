@@ -116,6 +116,9 @@ struct BwdParams {
   void* dk;
   void* dv;
   int64_t o_str[4], do_str[4], dq_str[4], dk_str[4], dv_str[4];
+  const void* mask;     // broadcast to [B, Hq, Nq, Nkv] by m_str (0 on broadcast dims)
+  int64_t m_str[4];
+  int mask_kind;
   int B, Hq, Hkv, group, Nq, Nkv, D;
   int nchunks, npairs, kchunks;
   int n_qt, n_kt, n_sl_dq, n_sl_kv;

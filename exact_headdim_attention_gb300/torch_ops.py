@@ -10,8 +10,9 @@ reference, ``ffpa_attn.ffpa_attn_func``, uses the same list), so it can
 replace that call for the supported cases: bf16/fp16 CUDA tensors,
 64 <= D <= 1024 with D % 8 == 0 (D % 64 == 0 for varlen and for the
 backward), no dropout.  The dense operator is
-differentiable through ``ffpa_bwd`` (the backward kernels) when it was
-called without attn_mask; the varlen operator registers no backward.
+differentiable through ``ffpa_bwd`` (the backward kernels; a mask enters
+the recomputed scores, but no gradient is formed for the mask itself); the
+varlen operator registers no backward.
 """
 from __future__ import annotations
 
@@ -41,19 +42,18 @@ def _attn_fwd_fake(q, k, v, attn_mask, is_causal, scale, enable_gqa):
 def _attn_fwd_setup_context(ctx, inputs, output):
     q, k, v, attn_mask, is_causal, scale, enable_gqa = inputs
     o, lse = output
-    ctx.save_for_backward(q, k, v, o, lse)
-    ctx.has_mask = attn_mask is not None
+    ctx.save_for_backward(q, k, v, o, lse, attn_mask)
     ctx.is_causal, ctx.scale, ctx.enable_gqa = is_causal, scale, enable_gqa
 
 
 def _attn_fwd_backward(ctx, grad_o, grad_lse):
-    if ctx.has_mask:
-        raise NotImplementedError("the backward kernels take no attn_mask")
+    if ctx.needs_input_grad[3]:
+        raise NotImplementedError("no gradient is formed for attn_mask")
     if grad_lse is not None and bool(torch.count_nonzero(grad_lse)):
         raise NotImplementedError("gradients through the returned LSE are not supported")
-    q, k, v, o, lse = ctx.saved_tensors
+    q, k, v, o, lse, attn_mask = ctx.saved_tensors
     dq, dk, dv = _binding.ffpa_bwd(grad_o.contiguous(), q, k, v, o, lse, is_causal=ctx.is_causal,
-                                   scale=ctx.scale, enable_gqa=ctx.enable_gqa)
+                                   scale=ctx.scale, enable_gqa=ctx.enable_gqa, attn_mask=attn_mask)
     return dq, dk, dv, None, None, None, None
 
 

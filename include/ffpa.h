@@ -122,7 +122,7 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
                             int enable_gqa, ffpa_stream_t stream);
 
 /*
- * Backward of ffpa_fwd (dense layout, no attn_mask): the gradients dq, dk, dv
+ * Backward of ffpa_fwd (dense layout): the gradients dq, dk, dv
  * of sum(O * dout) with respect to q, k and v (FFPA API reference,
  * "ffpa_attn.ffpa_attn_func": backward through FFPAAttnFunc; the Triton
  * backend's `split_launch` option: separate dKdV and dQ launches).  With
@@ -139,8 +139,9 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
  *     FlashAttention "softmax_d"); written first and read by the gradient
  *     kernels, so it must not alias any input.
  *   o, dout, dq, dk, dv: the 16-bit type of q; outputs must not alias inputs.
- *   scale, is_causal, enable_gqa: as for ffpa_fwd (the same values as the
- *     forward that produced o and lse).
+ *   mask, mask_kind, mask_str, scale, is_causal, enable_gqa: as for ffpa_fwd
+ *     (the same values as the forward that produced o and lse).  The mask
+ *     enters the recomputed scores only: no gradient is formed for it.
  *
  * Strides follow the ffpa_fwd rules (last stride 1, others multiples of 16
  * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd,
@@ -154,7 +155,8 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
                      int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
                      const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
                      const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
-                     const int64_t dv_str[4], const float* scale, int is_causal, int enable_gqa,
+                     const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */

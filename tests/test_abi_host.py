@@ -180,14 +180,15 @@ def test_selected_kernel_follows_the_choice(lib):
 
 
 def bwd_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,
-             lse=FAKE, delta=FAKE, dk=FAKE, qs=None, scale=None):
+             lse=FAKE, delta=FAKE, dk=FAKE, qs=None, scale=None, mask=None, mask_kind=0, mask_str=None):
     def st(H, N):
         return _arr([H * N * D, N * D, D, 1])
     qs = qs or st(Hq, Nq)
     ks = st(Hkv, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
     return lib.ffpa_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, lse, FAKE, dk, FAKE, delta, dt, B, Hq, Hkv, Nq,
-                        Nkv, D, qs, ks, ks, qs, qs, qs, ks, ks, sc, causal, enable_gqa, None)
+                        Nkv, D, qs, ks, ks, qs, qs, qs, ks, ks, mask, mask_kind, mask_str, sc, causal,
+                        enable_gqa, None)
 
 
 @pytest.mark.parametrize("case", GOLDEN["dense"], ids=lambda c: c["case"])
@@ -205,6 +206,9 @@ def test_bwd_layout_and_pointer_checks(lib):
     assert bwd_call(lib, scale=float("nan")) == INVALID
     assert bwd_call(lib, dt=5, lse=None) == pkg.FFPA_ERR_DTYPE
     assert bwd_call(lib, B=0, lse=None) == pkg.FFPA_OK                           # nothing to write
+    assert bwd_call(lib, mask_kind=9) == INVALID
+    assert bwd_call(lib, mask_kind=1, mask=None, mask_str=_arr([0, 0, 0, 1])) == INVALID
+    assert bwd_call(lib, mask_kind=2, mask=FAKE, mask_str=_arr([0, -1, 0, 1])) == INVALID
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

@@ -57,22 +57,25 @@ def draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype=torch.bfloat16):
     return q, k, v, dout
 
 
-def gpu_backward(q, k, v, dout, causal=False, scale=None):
+def gpu_backward(q, k, v, dout, causal=False, scale=None, mask=None):
     """Forward then backward on the GPU, as a training step would run them."""
     gqa = q.shape[1] != k.shape[1]
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
-    o, lse = pkg.ffpa_fwd(qd, kd, vd, is_causal=causal, scale=scale, enable_gqa=gqa,
+    md = None if mask is None else mask.to(DEV)
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, attn_mask=md, is_causal=causal, scale=scale, enable_gqa=gqa,
                           return_lse=True)
     dq, dk, dv, delta = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, is_causal=causal, scale=scale,
-                                     enable_gqa=gqa, return_delta=True)
+                                     enable_gqa=gqa, attn_mask=md, return_delta=True)
     device_ok()
     return dq, dk, dv, delta, o
 
 
-def bwd_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, scale=None, dtype=torch.bfloat16):
+def bwd_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, scale=None, dtype=torch.bfloat16,
+             mask=None):
     q, k, v, dout = draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype)
-    dq, dk, dv, delta, o = gpu_backward(q, k, v, dout, causal, scale)
-    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, scale=scale, is_causal=causal)
+    m = mask(torch.Generator().manual_seed(seed + 7)) if callable(mask) else mask
+    dq, dk, dv, delta, o = gpu_backward(q, k, v, dout, causal, scale, m)
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, attn_mask=m, scale=scale, is_causal=causal)
     tag = f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D} causal={causal} {dtype}"
     check_grad(dq, rq, f"{tag} dQ")
     check_grad(dk, rk, f"{tag} dK")
@@ -138,6 +141,38 @@ def test_bwd_single_key(Nq):
     bk = 2 * scale * (e * q.double().abs().amax(-1)).sum(-1)               # [1,2]
     assert (dk.double().cpu().abs().amax(-1).squeeze(-1) <= bk).all(), "dK not zero within the bound"
     check_grad(dv, dout.double().sum(2, keepdim=True), f"Nq{Nq} Nkv1 dV")
+
+
+# ------------------------------------------------------------------ masks
+def _bool_mask_with_dead_rows(B, H, Nq, Nkv):
+    def make(g):
+        m = torch.rand(B, H, Nq, Nkv, generator=g) < 0.6
+        m[:, :, 3] = False                    # fully masked rows: LSE = -inf, no contribution
+        m[0, -1, Nq - 1] = False
+        return m
+    return make
+
+
+def test_bwd_bool_mask_with_dead_rows():
+    bwd_case(2, 2, 2, 200, 300, 128, seed=51, mask=_bool_mask_with_dead_rows(2, 2, 200, 300))
+
+
+def test_bwd_additive_f32_mask_d512():
+    B, H, Nq, Nkv = 1, 2, 190, 260
+    bwd_case(B, H, H, Nq, Nkv, 512, seed=52,
+             mask=lambda g: torch.randn(B, H, Nq, Nkv, generator=g))
+
+
+def test_bwd_qtype_mask_broadcast_causal():
+    Nq, Nkv = 150, 270
+    bwd_case(2, 4, 2, Nq, Nkv, 128, seed=53, causal=True,
+             mask=lambda g: torch.randn(1, 1, Nq, Nkv, generator=g).bfloat16())
+
+
+def test_bwd_bool_mask_fp16_gqa():
+    B, Hq, Nq, Nkv = 1, 4, 140, 140
+    bwd_case(B, Hq, 2, Nq, Nkv, 256, seed=54, dtype=torch.float16,
+             mask=lambda g: (torch.rand(B, 1, Nq, Nkv, generator=g) < 0.7) | torch.eye(Nq, Nkv, dtype=torch.bool))
 
 
 def test_bwd_strided_views():
@@ -215,10 +250,23 @@ def test_autograd_through_custom_op():
     check_grad(vd.grad, rv, "autograd dV")
 
 
-def test_autograd_with_mask_raises():
-    q, k, v, _ = draw(1, 2, 2, 64, 64, 128, seed=44)
+def test_autograd_with_bool_mask():
+    q, k, v, dout = draw(1, 2, 2, 160, 200, 128, seed=44)
+    mask = torch.rand(160, 200, generator=torch.Generator().manual_seed(45)) < 0.8
     qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
-    mask = torch.ones(64, 64, dtype=torch.bool, device=DEV)
-    o = pkg.ffpa_attn_func(qd, kd, vd, attn_mask=mask)
+    o = pkg.ffpa_attn_func(qd, kd, vd, attn_mask=mask.to(DEV))
+    o.backward(dout.to(DEV))
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, attn_mask=mask)
+    check_grad(qd.grad, rq, "autograd masked dQ")
+    check_grad(kd.grad, rk, "autograd masked dK")
+    check_grad(vd.grad, rv, "autograd masked dV")
+
+
+def test_autograd_mask_gradient_raises():
+    q, k, v, _ = draw(1, 2, 2, 64, 64, 128, seed=46)
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    bias = torch.zeros(64, 64, device=DEV, requires_grad=True)
+    o = pkg.ffpa_attn_func(qd, kd, vd, attn_mask=bias)
     with pytest.raises(NotImplementedError):
         o.sum().backward()
