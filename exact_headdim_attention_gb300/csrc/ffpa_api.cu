@@ -477,6 +477,7 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
+  P.inject = g_drop_first_copy.load();
   P.timeout_ns = g_timeout_ns.load();
   const long long dq_items = Nq > 0 ? (long long)B * Hq * P.n_qt * P.n_sl_dq : 0;
   const long long kv_items = Nkv > 0 ? (long long)B * Hkv * P.n_kt * P.n_sl_kv : 0;

@@ -282,12 +282,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       const uint32_t box_bytes = (uint32_t)p.kchunks * CHUNK_BYTES;
       int slot = 0, issued = 0;
       uint32_t lap = 0;
+      // Test hook: the CTA's first ring stage is acquired but never armed or
+      // copied, so the MMA thread's wait on it runs out.
+      bool drop = p.inject != 0;
       auto load = [&](const CUtensorMap* m, int row, int chunk, int head) -> bool {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
         if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) return false;
         const uint32_t fb = smem_u32(&bar_full[slot]);
-        mbar_arrive_expect_tx(fb, box_bytes);
-        tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
+        if (drop) {
+          drop = false;
+        } else {
+          mbar_arrive_expect_tx(fb, box_bytes);
+          tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
+        }
         ++issued;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return true;
@@ -330,6 +337,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = NS - 1; lp ^= 1u; }
+        if (p.inject != 0 && issued - 1 - i == 0) continue;   // the dropped stage was never armed
         wait_drain(smem_u32(&bar_full[s]), lp, tmo);
       }
     }

@@ -124,7 +124,7 @@ struct BwdParams {
   int n_qt, n_kt, n_sl_dq, n_sl_kv;
   int nslot_dq, nslot_kv;
   float scale, scale_log2;
-  int causal, fp16;
+  int causal, fp16, inject;
   unsigned long long timeout_ns;
 };
 

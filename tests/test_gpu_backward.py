@@ -270,3 +270,29 @@ def test_autograd_mask_gradient_raises():
     o = pkg.ffpa_attn_func(qd, kd, vd, attn_mask=bias)
     with pytest.raises(NotImplementedError):
         o.sum().backward()
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_bwd_bounded_wait_reports_timeout_and_context_survives():
+    """The first ring stage of every backward CTA is dropped (test hook): the MMA
+    thread's wait on it runs out, the kernels drain, free TMEM and report
+    FFPA_ERR_DEVICE_TIMEOUT; the next call on the same context is correct."""
+    q, k, v, dout = draw(1, 2, 2, 200, 200, 256, seed=61)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, return_lse=True)
+    device_ok()
+    pkg.set_wait_timeout_ns(200_000_000)
+    pkg.inject_dropped_copy(True)
+    try:
+        pkg.ffpa_bwd(dod, qd, kd, vd, o, lse)
+        st = pkg.ffpa_last_device_error()
+    finally:
+        pkg.inject_dropped_copy(False)
+        pkg.set_wait_timeout_ns(0)
+    assert st == pkg.FFPA_ERR_DEVICE_TIMEOUT
+    dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse)
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout)
+    check_grad(dq, rq, "dQ after timeout")
+    check_grad(dk, rk, "dK after timeout")
+    check_grad(dv, rv, "dV after timeout")
