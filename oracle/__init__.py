@@ -62,6 +62,9 @@ class Oracle:
         self.lib.oracle_attn_bwd_rows.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, D, I,
                                                   P, L, P, L, P, P, P, I]
         self.lib.oracle_attn_bwd_rows.restype = I
+        self.lib.oracle_attn_bwd_varlen.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, I, D, I,
+                                                    P, P, P, I]
+        self.lib.oracle_attn_bwd_varlen.restype = I
 
     # ------------------------------------------------------------------ dense
     def attn_dense(self, q, k, v, attn_mask=None, scale=None, is_causal=False, rows=None,
@@ -194,6 +197,31 @@ class Oracle:
             raise ValueError("oracle_attn_bwd_rows rejected its arguments")
         return dq, dk, dv
 
+    def attn_bwd_varlen(self, q, k, v, dout, cu_q, cu_k=None, scale=None, causal=False,
+                        nthreads: int = 0):
+        """Gradients (dQ [Tq,Hq,D], dK, dV [Tk,Hkv,D], float64) of sum(O * dout) for
+        the packed variable-length forward."""
+        dtype = _dtype_code(q)
+        Tq, Hq, D = q.shape
+        Tk, Hkv, _ = k.shape
+        for t in (q, k, v, dout):
+            assert t.device.type == "cpu" and t.stride(-1) == 1
+        cu_q = cu_q.to(torch.int32).contiguous()
+        cu_k = cu_q if cu_k is None else cu_k.to(torch.int32).contiguous()
+        if scale is None:
+            scale = 1.0 / math.sqrt(D)
+        dq = torch.empty(Tq, Hq, D, dtype=torch.float64)
+        dk = torch.empty(Tk, Hkv, D, dtype=torch.float64)
+        dv = torch.empty(Tk, Hkv, D, dtype=torch.float64)
+        rc = self.lib.oracle_attn_bwd_varlen(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), dout.data_ptr(), dtype, Hq, Hkv, D,
+            _strides(q), _strides(k), _strides(v), _strides(dout), cu_q.data_ptr(), cu_k.data_ptr(),
+            cu_q.numel() - 1, float(scale), int(bool(causal)), dq.data_ptr(), dk.data_ptr(),
+            dv.data_ptr(), nthreads)
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd_varlen rejected its arguments")
+        return dq, dk, dv
+
 
 def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
     """(kind, pointer, strides, keep-alive) of a mask broadcast to [B,Hq,Nq,Nkv]."""
@@ -250,6 +278,10 @@ def attn_bwd_dense(*a, **kw):
 
 def attn_bwd_rows(*a, **kw):
     return default().attn_bwd_rows(*a, **kw)
+
+
+def attn_bwd_varlen(*a, **kw):
+    return default().attn_bwd_varlen(*a, **kw)
 
 
 def host_threads() -> int:

@@ -498,3 +498,81 @@ int oracle_attn_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v
     }
     return err ? -1 : 0;
 }
+
+/*
+ * Backward of the packed variable-length forward: q, dout [Tq, Hq, D]
+ * (strides q_str[3], do_str[3] over T, H, D); k, v [Tk, Hkv, D]; cu_q,
+ * cu_k as for oracle_attn_varlen.  Sequence s is differentiated exactly like
+ * a dense problem of its own lengths (causal alignment lower right within
+ * the sequence).  dq: [Tq, Hq, D]; dk, dv: [Tk, Hkv, D]; contiguous float64.
+ * One (sequence, key/value head) per task.  Returns 0, or -1 on a bad
+ * argument.
+ */
+int oracle_attn_bwd_varlen(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint16_t* dout, int dtype, int Hq, int Hkv, int D,
+                           const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                           const int64_t* do_str, const int32_t* cu_q, const int32_t* cu_k, int nseq,
+                           double scale, int causal, double* dq, double* dk, double* dv, int nthreads) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || D <= 0 || nseq < 1) return -1;
+    const int group = Hq / Hkv;
+    int64_t maxk = 1;
+    for (int sq = 0; sq < nseq; ++sq) {
+        int64_t lk = cu_k[sq + 1] - cu_k[sq];
+        if (cu_q[sq + 1] < cu_q[sq] || lk < 0) return -1;
+        if (lk > maxk) maxk = lk;
+    }
+    const int64_t Tq = cu_q[nseq], Tk = cu_k[nseq];
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    for (int64_t e = 0; e < Tk * Hkv * D; ++e) dk[e] = dv[e] = 0.0;
+    for (int64_t e = 0; e < Tq * Hq * D; ++e) dq[e] = 0.0;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* P = (double*)malloc(sizeof(double) * (size_t)maxk);
+        double* dP = (double*)malloc(sizeof(double) * (size_t)maxk);
+        if (!P || !dP) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < (int64_t)nseq * Hkv; ++u) {
+            if (!P || !dP) continue;
+            int sq = (int)(u / Hkv), hk = (int)(u % Hkv);
+            int64_t q0 = cu_q[sq], nq = cu_q[sq + 1] - cu_q[sq];
+            int64_t k0 = cu_k[sq];
+            int nk = cu_k[sq + 1] - cu_k[sq];
+            const uint16_t* kb = k + k0 * k_str[0] + hk * k_str[1];
+            const uint16_t* vb = v + k0 * v_str[0] + hk * v_str[1];
+            for (int hq = hk * group; hq < (hk + 1) * group; ++hq) {
+                for (int64_t i = 0; i < nq; ++i) {
+                    const uint16_t* qrow = q + (q0 + i) * q_str[0] + hq * q_str[1];
+                    const uint16_t* dorow = dout + (q0 + i) * do_str[0] + hq * do_str[1];
+                    int64_t limit = causal ? i + (int64_t)nk - nq : (int64_t)nk - 1;
+                    int dead;
+                    double delta = grad_row(qrow, dorow, kb, vb, k_str[0], v_str[0], nk, D, dtype, scale,
+                                            ORACLE_MASK_NONE, NULL, 0, limit, P, dP, &dead);
+                    if (dead) continue;
+                    double* dqi = dq + ((q0 + i) * Hq + hq) * D;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        double ds = P[kk] * (dP[kk] - delta);
+                        const uint16_t* krow = kb + (int64_t)kk * k_str[0];
+                        double* dkr = dk + ((k0 + kk) * Hkv + hk) * D;
+                        double* dvr = dv + ((k0 + kk) * Hkv + hk) * D;
+                        for (int d = 0; d < D; ++d) {
+                            dqi[d] += scale * ds * widen(krow + d, dtype);
+                            dkr[d] += scale * ds * widen(qrow + d, dtype);
+                            dvr[d] += P[kk] * widen(dorow + d, dtype);
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dP);
+    }
+    return err ? -1 : 0;
+}

@@ -451,4 +451,35 @@ def pin_bwd_sampled_rows(orc):
         _close(dv, gv.reshape(-1, D)[kr], what=f"sampled dV (causal={causal})")
 
 
+def pin_bwd_varlen_equals_per_sequence(orc):
+    """Packed varlen gradients equal each sequence's dense gradients (library
+    autograd through SDPA on the unpacked sequence), causal and not, with GQA,
+    an empty query sequence and unequal query/key lengths."""
+    g = torch.Generator().manual_seed(13)
+    Hq, Hkv, D = 4, 2, 16
+    lq, lk = [5, 0, 9, 3], [7, 4, 9, 6]
+    cu_q = torch.tensor([0] + list(torch.tensor(lq).cumsum(0)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(torch.tensor(lk).cumsum(0)), dtype=torch.int32)
+    q = torch.randn(sum(lq), Hq, D, generator=g).bfloat16()
+    k = torch.randn(sum(lk), Hkv, D, generator=g).bfloat16()
+    v = torch.randn(sum(lk), Hkv, D, generator=g).bfloat16()
+    dout = torch.randn(sum(lq), Hq, D, generator=g).bfloat16()
+    for causal in (False, True):
+        dq, dk, dv = orc.attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal=causal)
+        for s_ in range(len(lq)):
+            a, b = int(cu_q[s_]), int(cu_q[s_ + 1])
+            c, d = int(cu_k[s_]), int(cu_k[s_ + 1])
+            if b - a == 0:
+                _close(dk[c:d], torch.zeros(d - c, Hkv, D), what=f"seq {s_} dK (no queries)")
+                continue
+            if causal and d - c < b - a:
+                continue
+            gq, gk, gv = _sdpa_grads(q[a:b].transpose(0, 1)[None], k[c:d].transpose(0, 1)[None],
+                                     v[c:d].transpose(0, 1)[None], dout[a:b].transpose(0, 1)[None],
+                                     None, None, causal)
+            _close(dq[a:b], gq[0].transpose(0, 1), what=f"seq {s_} dQ causal={causal}")
+            _close(dk[c:d], gk[0].transpose(0, 1), what=f"seq {s_} dK causal={causal}")
+            _close(dv[c:d], gv[0].transpose(0, 1), what=f"seq {s_} dV causal={causal}")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -51,6 +51,10 @@ MUTANTS = {
                              "for (int d = 0; d < D; ++d) dqi[d] += ds * widen(krow + d, dtype);"),
     "bwd_rows_dv_wrong_row": ("av[d] += P[j] * widen(w.dorow + d, dtype);",
                               "av[d] += P[j] * widen(w.qrow + d, dtype);"),
+    "bwd_varlen_top_left": ("int64_t limit = causal ? i + (int64_t)nk - nq : (int64_t)nk - 1;\n                    int dead;",
+                            "int64_t limit = causal ? i : (int64_t)nk - 1;\n                    int dead;"),
+    "bwd_varlen_key_base": ("const uint16_t* kb = k + k0 * k_str[0] + hk * k_str[1];\n            const uint16_t* vb = v + k0 * v_str[0]",
+                            "const uint16_t* kb = k + q0 * k_str[0] + hk * k_str[1];\n            const uint16_t* vb = v + k0 * v_str[0]"),
 }
 
 
