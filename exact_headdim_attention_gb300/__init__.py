@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     FFPAError,
     default_scale,
     ffpa_bwd,
+    ffpa_bwd_varlen,
     ffpa_fwd,
     ffpa_fwd_varlen,
     ffpa_last_device_error,

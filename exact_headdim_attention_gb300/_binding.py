@@ -22,7 +22,7 @@ FFPA_OK, FFPA_ERR_DTYPE, FFPA_ERR_INVALID, FFPA_ERR_UNSUPPORTED, FFPA_ERR_CUDA, 
 FFPA_BF16, FFPA_FP16 = 0, 1
 FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
 
-EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_bwd", "ffpa_status_string", "ffpa_last_device_error",
+EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_bwd", "ffpa_bwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
             "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant",
             "ffpa_selected_kernel")
 
@@ -79,6 +79,9 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
                              P, P, I, P, P, I, I, P]
     lib.ffpa_bwd.restype = I
+    lib.ffpa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P,
+                                    P, P, P, P, I, I, I, P, I, I, P]
+    lib.ffpa_bwd_varlen.restype = I
     lib.ffpa_status_string.argtypes = [I]
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_last_device_error.argtypes = [P]
@@ -321,6 +324,65 @@ def ffpa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     if st != FFPA_OK:
         _raise(st, "ffpa_fwd_varlen")
     return (out, lse) if return_lse else out
+
+
+def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    out: torch.Tensor, lse: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                    cu_seqlens_k: torch.Tensor | None, max_seqlen_q: int, max_seqlen_k: int, *,
+                    softmax_scale: float | None = None, causal: bool = False,
+                    enable_gqa: bool = False, dq=None, dk=None, dv=None, delta=None,
+                    return_delta: bool = False, stream=None):
+    """Packed varlen backward through the C ABI ``ffpa_bwd_varlen``.
+
+    dout, q, out [Tq,Hq,D]; k, v [Tk,Hkv,D]; lse [Hq,Tq] fp32 from
+    ffpa_fwd_varlen with the same sequences, causal and scale.  Returns
+    (dq, dk, dv), plus delta [Hq,Tq] fp32 with return_delta."""
+    lib = load_library()
+    for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dim() != 3:
+            raise ValueError(f"{name} must be 3-D [T, H, D]")
+        if t.dtype != q.dtype:
+            raise TypeError("dout, q, k, v and out must share one dtype")
+    Tq, Hq, D = q.shape
+    Tk, Hkv, Dk = k.shape
+    if (tuple(v.shape) != (Tk, Hkv, Dk) or Dk != D or tuple(out.shape) != tuple(q.shape)
+            or tuple(dout.shape) != tuple(q.shape)):
+        raise ValueError("shape mismatch between q, k, v, out and dout")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (Hq, Tq):
+        raise ValueError("lse must be a contiguous float32 [Hq, Tq] tensor")
+    cq = _check_cu(cu_seqlens_q, Tq, "cu_seqlens_q")
+    ck = cq if cu_seqlens_k is None else _check_cu(cu_seqlens_k, Tk, "cu_seqlens_k")
+    if len(ck) != len(cq):
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different batch sizes")
+    if cu_seqlens_k is None and Tk != Tq:
+        raise ValueError("cu_seqlens_k=None needs Tk == Tq")
+    if max(b - a for a, b in zip(cq, cq[1:])) > max_seqlen_q or \
+            max(b - a for a, b in zip(ck, ck[1:])) > max_seqlen_k:
+        raise ValueError("max_seqlen_* is smaller than a sequence length")
+    if dq is None:
+        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
+    if dk is None:
+        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
+    if dv is None:
+        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
+    if delta is None:
+        delta = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
+    if delta.dtype != torch.float32 or not delta.is_contiguous() or tuple(delta.shape) != (Hq, Tq):
+        raise ValueError("delta must be a contiguous float32 [Hq, Tq] tensor")
+    cuq = cu_seqlens_q.to(q.device)
+    cuk = None if cu_seqlens_k is None else cu_seqlens_k.to(q.device)
+    sc = None if softmax_scale is None else ctypes.byref(ctypes.c_float(float(softmax_scale)))
+    st = lib.ffpa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                             dv.data_ptr(), delta.data_ptr(), _dtype_code(q), Tq, Tk, Hq, Hkv, D,
+                             _strides(q), _strides(k), _strides(v), _strides(out), _strides(dout),
+                             _strides(dq), _strides(dk), _strides(dv), cuq.data_ptr(),
+                             None if cuk is None else cuk.data_ptr(), len(cq) - 1,
+                             int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
+                             int(bool(enable_gqa)), _stream_handle(stream, q))
+    if st != FFPA_OK:
+        _raise(st, "ffpa_bwd_varlen")
+    return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)
 
 
 def ffpa_last_device_error(stream=None) -> int:

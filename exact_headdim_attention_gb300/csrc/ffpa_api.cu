@@ -222,6 +222,32 @@ size_t plan_for(Kern kn, int D, Params* P) {
   return plan(D, P);
 }
 
+// Backward: output slices, ring depths, shared memory, work items; then the
+// three launches.  P's sizes, tiles, maps, pointers, scale, causal and fp16
+// are set by the caller.
+ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, cudaStream_t stream) {
+  P.nchunks = P.D / DK;
+  P.n_sl_dq = (P.D + BWD_DQ_COLS - 1) / BWD_DQ_COLS;
+  P.n_sl_kv = (P.D + BWD_KV_COLS - 1) / BWD_KV_COLS;
+  // Shared memory: one (dQ) or two (dK/dV) 32 KB P/dS tiles, then the ring.
+  const size_t avail = SMEM_LIMIT - BWD_STATIC_RESERVE - 1024;
+  size_t ns_dq = (avail - P_TILE_BYTES) / SLOT_BYTES;
+  size_t ns_kv = (avail - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
+  if (ns_dq > (size_t)BWD_NSLOT_MAX) ns_dq = BWD_NSLOT_MAX;
+  if (ns_kv > (size_t)BWD_NSLOT_MAX) ns_kv = BWD_NSLOT_MAX;
+  P.nslot_dq = static_cast<int>(ns_dq);
+  P.nslot_kv = static_cast<int>(ns_kv);
+  const size_t dq_smem = 1024 + P_TILE_BYTES + ns_dq * SLOT_BYTES;
+  const size_t kv_smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns_kv * SLOT_BYTES;
+  P.scale_log2 = P.scale * 1.4426950408889634f;
+  P.inject = g_drop_first_copy.load();
+  P.timeout_ns = g_timeout_ns.load();
+  const long long dq_items = any_q ? (long long)P.B * P.Hq * P.n_qt * P.n_sl_dq : 0;
+  const long long kv_items = any_k ? (long long)P.B * P.Hkv * P.n_kt * P.n_sl_kv : 0;
+  if (dq_items > 0x7fffffffLL || kv_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), dq_smem, kv_smem, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -461,29 +487,107 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.D = D;
   P.n_qt = (Nq + BM - 1) / BM;
   P.n_kt = (Nkv + BN - 1) / BN;
-  P.n_sl_dq = (D + BWD_DQ_COLS - 1) / BWD_DQ_COLS;
-  P.n_sl_kv = (D + BWD_KV_COLS - 1) / BWD_KV_COLS;
-  // Shared memory: one (dQ) or two (dK/dV) 32 KB P/dS tiles, then the ring.
-  const size_t avail = SMEM_LIMIT - BWD_STATIC_RESERVE - 1024;
-  size_t ns_dq = (avail - P_TILE_BYTES) / SLOT_BYTES;
-  size_t ns_kv = (avail - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
-  if (ns_dq > (size_t)BWD_NSLOT_MAX) ns_dq = BWD_NSLOT_MAX;
-  if (ns_kv > (size_t)BWD_NSLOT_MAX) ns_kv = BWD_NSLOT_MAX;
-  P.nslot_dq = static_cast<int>(ns_dq);
-  P.nslot_kv = static_cast<int>(ns_kv);
-  const size_t dq_smem = 1024 + P_TILE_BYTES + ns_dq * SLOT_BYTES;
-  const size_t kv_smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns_kv * SLOT_BYTES;
   P.scale = sc;
-  P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
-  P.inject = g_drop_first_copy.load();
-  P.timeout_ns = g_timeout_ns.load();
-  const long long dq_items = Nq > 0 ? (long long)B * Hq * P.n_qt * P.n_sl_dq : 0;
-  const long long kv_items = Nkv > 0 ? (long long)B * Hkv * P.n_kt * P.n_sl_kv : 0;
-  if (dq_items > 0x7fffffffLL || kv_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
-  return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), dq_smem, kv_smem,
-                    reinterpret_cast<cudaStream_t>(stream));
+  return bwd_launch(P, Nq > 0, Nkv > 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                            const int64_t o_str[3], const int64_t do_str[3], const int64_t dq_str[3],
+                            const int64_t dk_str[3], const int64_t dv_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
+  if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (nseq < 1 || max_seqlen_q < 0 || max_seqlen_k < 0) return FFPA_ERR_INVALID;
+  if (!cu_seqlens_q) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if ((Tq == 0 || max_seqlen_q == 0) && (Tk == 0 || max_seqlen_k == 0)) return FFPA_OK;
+  if (!q_str || !k_str || !v_str || !o_str || !do_str || !dq_str || !dk_str || !dv_str)
+    return FFPA_ERR_INVALID;
+  const int64_t qsz[3] = {Tq, Hq, D}, ksz[3] = {Tk, Hkv, D};
+  const bool any_q = Tq > 0 && max_seqlen_q > 0, any_k = Tk > 0 && max_seqlen_k > 0;
+  if (any_q) {
+    if (!q || !o || !dout || !dq || !lse || !delta) return FFPA_ERR_INVALID;
+    if (!strides_ok(q_str, qsz, 3) || !strides_ok(o_str, qsz, 3) || !strides_ok(do_str, qsz, 3) ||
+        !strides_ok(dq_str, qsz, 3))
+      return FFPA_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq)) return FFPA_ERR_INVALID;
+  }
+  if (any_k) {
+    if (!k || !v || !dk || !dv) return FFPA_ERR_INVALID;
+    if (!strides_ok(k_str, ksz, 3) || !strides_ok(v_str, ksz, 3) || !strides_ok(dk_str, ksz, 3) ||
+        !strides_ok(dv_str, ksz, 3))
+      return FFPA_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
+  }
+  int dev = 0;
+  ffpa_status st = check_device(any_q ? q : k, &dev);
+  if (st != FFPA_OK) return st;
+
+  BwdParams P{};
+  const CUtensorMapDataType tdt =
+      dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  P.D = D;
+  P.npairs = (D / DK + 1) / 2;
+  P.kchunks = D / DK < 2 ? D / DK : 2;
+  const uint64_t nch = (uint64_t)(D / DK);
+  const uint32_t box[4] = {64, BM, (uint32_t)P.kchunks, 1};
+  if (any_q) {
+    const uint64_t dq4[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
+    const uint64_t sq[3] = {(uint64_t)q_str[0] * 2, 128, (uint64_t)q_str[1] * 2};
+    const uint64_t sd[3] = {(uint64_t)do_str[0] * 2, 128, (uint64_t)do_str[1] * 2};
+    if ((st = encode_map(&P.tm_q, tdt, 4, q, dq4, sq, box)) != FFPA_OK) return st;
+    if ((st = encode_map(&P.tm_do, tdt, 4, dout, dq4, sd, box)) != FFPA_OK) return st;
+  }
+  if (any_k) {
+    const uint64_t dk4[4] = {64, (uint64_t)Tk, nch, (uint64_t)Hkv};
+    const uint64_t sk[3] = {(uint64_t)k_str[0] * 2, 128, (uint64_t)k_str[1] * 2};
+    const uint64_t sv[3] = {(uint64_t)v_str[0] * 2, 128, (uint64_t)v_str[1] * 2};
+    if ((st = encode_map(&P.tm_k, tdt, 4, k, dk4, sk, box)) != FFPA_OK) return st;
+    if ((st = encode_map(&P.tm_v, tdt, 4, v, dk4, sv, box)) != FFPA_OK) return st;
+  }
+  P.o = o;
+  P.dout = dout;
+  P.lse = lse;
+  P.delta = delta;
+  P.dq = dq;
+  P.dk = dk;
+  P.dv = dv;
+  for (int i = 0; i < 3; ++i) {
+    P.o_str[i] = o_str[i];
+    P.do_str[i] = do_str[i];
+    P.dq_str[i] = dq_str[i];
+    P.dk_str[i] = dk_str[i];
+    P.dv_str[i] = dv_str[i];
+  }
+  P.mask = nullptr;
+  P.mask_kind = FFPA_MASK_NONE;
+  P.varlen = 1;
+  P.Tq = Tq;
+  P.cu_q = cu_seqlens_q;
+  P.cu_k = cu_seqlens_k ? cu_seqlens_k : cu_seqlens_q;
+  P.B = nseq;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.group = Hq / Hkv;
+  P.Nq = max_seqlen_q;
+  P.Nkv = max_seqlen_k;
+  P.n_qt = (max_seqlen_q + BM - 1) / BM;
+  P.n_kt = (max_seqlen_k + BN - 1) / BN;
+  P.scale = sc;
+  P.causal = causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  return bwd_launch(P, any_q, any_k, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -67,12 +67,44 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, bool fp16) {
 
 struct BwdItem {
   int b, hq, hkv, slice;
+  int q_len, kv_len;       // this problem's (sequence's) lengths
+  int q_row0, kv_row0;     // varlen: first packed row of the sequence (dense: 0)
   int row0;       // first row of this CTA's tile: query row (dQ) or key row (dK/dV)
   int n_iter;     // dQ: key tiles; dK/dV: group heads x visible query tiles
   int qt_first;   // dK/dV: first query tile that sees the key tile
   int nq;         // dK/dV: query tiles per head
   int col_lo, dv; // output columns [col_lo, col_lo + dv)
 };
+
+// Lengths and packed row offsets of item it's problem (sequence it.b when
+// varlen).
+__device__ __forceinline__ void bwd_lengths(const BwdParams& p, BwdItem& it) {
+  if (p.varlen) {
+    it.q_row0 = p.cu_q[it.b];
+    it.q_len = p.cu_q[it.b + 1] - it.q_row0;
+    it.kv_row0 = p.cu_k[it.b];
+    it.kv_len = p.cu_k[it.b + 1] - it.kv_row0;
+  } else {
+    it.q_row0 = 0;
+    it.q_len = p.Nq;
+    it.kv_row0 = 0;
+    it.kv_len = p.Nkv;
+  }
+}
+
+// Index of (query head h, query row i of the item's problem) in the LSE and
+// delta arrays: dense [B, Hq, Nq], varlen [Hq, Tq].
+__device__ __forceinline__ long long bwd_stat_index(const BwdParams& p, const BwdItem& it, int h, int i) {
+  return p.varlen ? (long long)h * p.Tq + it.q_row0 + i : ((long long)it.b * p.Hq + h) * p.Nq + i;
+}
+
+// Element offset of row `row` of head h in an output tensor with strides
+// str: dense (b, h, n, d), varlen (t, h, d).
+__device__ __forceinline__ long long bwd_row_offset(const BwdParams& p, const BwdItem& it, const int64_t* str,
+                                                    int row0, int row, int h) {
+  return p.varlen ? (long long)(row0 + row) * str[0] + (long long)h * str[1]
+                  : (long long)it.b * str[0] + (long long)h * str[1] + (long long)row * str[2];
+}
 
 template <bool DQ>
 __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& it) {
@@ -91,12 +123,13 @@ __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& i
     it.hq = bh % p.Hq;
     it.b = bh / p.Hq;
     it.hkv = it.hq / p.group;
+    bwd_lengths(p, it);
     it.row0 = qt * BM;
-    if (it.row0 >= p.Nq) return false;
-    long long kv_end = p.Nkv;
+    if (it.row0 >= it.q_len) return false;
+    long long kv_end = it.kv_len;
     if (p.causal) {
-      const int rows = min(BM, p.Nq - it.row0);
-      kv_end = min(kv_end, (long long)it.row0 + rows + (p.Nkv - p.Nq));
+      const int rows = min(BM, it.q_len - it.row0);
+      kv_end = min(kv_end, (long long)it.row0 + rows + (it.kv_len - it.q_len));
     }
     it.n_iter = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
     it.qt_first = 0;
@@ -118,13 +151,14 @@ __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& i
     it.hkv = bh % p.Hkv;
     it.b = bh / p.Hkv;
     it.hq = it.hkv * p.group;
+    bwd_lengths(p, it);
     it.row0 = kt * BN;
-    if (it.row0 >= p.Nkv) return false;
+    if (it.row0 >= it.kv_len) return false;
     // Query row i sees key k when k <= i + (Nkv - Nq): the first query
     // tile with a row that sees this tile's first key.
-    const int first_row = p.causal ? max(0, it.row0 - (p.Nkv - p.Nq)) : 0;
+    const int first_row = p.causal ? max(0, it.row0 - (it.kv_len - it.q_len)) : 0;
     it.qt_first = first_row / BM;
-    it.nq = max(0, p.n_qt - it.qt_first);
+    it.nq = max(0, (it.q_len + BM - 1) / BM - it.qt_first);
     it.n_iter = p.group * it.nq;
     it.col_lo = it.slice * BWD_KV_COLS;
     it.dv = min(BWD_KV_COLS, p.D - it.col_lo);
@@ -189,16 +223,26 @@ __device__ __forceinline__ float add_mask_term(float arg, const uint8_t* base, l
 }  // namespace
 
 __global__ void __launch_bounds__(256) ffpa_bwd_delta_kernel(const __grid_constant__ BwdParams p) {
-  const long long rows = (long long)p.B * p.Hq * p.Nq;
+  // Dense: row = (b Hq + h) Nq + i.  Varlen: row = h Tq + t (the [Hq, Tq]
+  // layout of LSE and delta).
+  const long long rows = p.varlen ? (long long)p.Hq * p.Tq : (long long)p.B * p.Hq * p.Nq;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
-  const long long i = row % p.Nq;
-  const long long bh = row / p.Nq;
-  const long long h = bh % p.Hq, b = bh / p.Hq;
-  const uint16_t* orow = static_cast<const uint16_t*>(p.o) + b * p.o_str[0] + h * p.o_str[1] + i * p.o_str[2];
-  const uint16_t* drow =
-      static_cast<const uint16_t*>(p.dout) + b * p.do_str[0] + h * p.do_str[1] + i * p.do_str[2];
+  long long oo, od;
+  if (p.varlen) {
+    const long long t = row % p.Tq, h = row / p.Tq;
+    oo = t * p.o_str[0] + h * p.o_str[1];
+    od = t * p.do_str[0] + h * p.do_str[1];
+  } else {
+    const long long i = row % p.Nq;
+    const long long bh = row / p.Nq;
+    const long long h = bh % p.Hq, b = bh / p.Hq;
+    oo = b * p.o_str[0] + h * p.o_str[1] + i * p.o_str[2];
+    od = b * p.do_str[0] + h * p.do_str[1] + i * p.do_str[2];
+  }
+  const uint16_t* orow = static_cast<const uint16_t*>(p.o) + oo;
+  const uint16_t* drow = static_cast<const uint16_t*>(p.dout) + od;
   const bool fp16 = p.fp16 != 0;
   float acc = 0.f;
   for (int d0 = lane * 8; d0 < p.D; d0 += 256)
@@ -285,7 +329,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       // Test hook: the CTA's first ring stage is acquired but never armed or
       // copied, so the MMA thread's wait on it runs out.
       bool drop = p.inject != 0;
-      auto load = [&](const CUtensorMap* m, int row, int chunk, int head) -> bool {
+      // row: within the item's problem; qside: a query-side tensor (Q, dO).
+      auto load = [&](const CUtensorMap* m, int row, int chunk, int head, bool qside) -> bool {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
         if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) return false;
         const uint32_t fb = smem_u32(&bar_full[slot]);
@@ -293,7 +338,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
           drop = false;
         } else {
           mbar_arrive_expect_tx(fb, box_bytes);
-          tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
+          if (p.varlen)
+            tma_load_4d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, (qside ? it.q_row0 : it.kv_row0) + row, chunk,
+                        head);
+          else
+            tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, head, it.b);
         }
         ++issued;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
@@ -307,10 +356,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       auto contraction_loads = [&](int i) -> bool {
         int hs, rs;
         stream_coords(i, hs, rs);
+        // dQ: A = Q, dO (query side), B = K, V; dK/dV the other way round.
         for (int pr = 0; pr < npairs; ++pr)
-          if (!load(a1, it.row0, 2 * pr, ha) || !load(b1, rs, 2 * pr, hs)) return false;
+          if (!load(a1, it.row0, 2 * pr, ha, DQ) || !load(b1, rs, 2 * pr, hs, !DQ)) return false;
         for (int pr = 0; pr < npairs; ++pr)
-          if (!load(a2, it.row0, 2 * pr, ha) || !load(b2, rs, 2 * pr, hs)) return false;
+          if (!load(a2, it.row0, 2 * pr, ha, DQ) || !load(b2, rs, 2 * pr, hs, !DQ)) return false;
         return true;
       };
       auto slice_loads = [&](int i) -> bool {
@@ -319,10 +369,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         const int c0 = it.col_lo / DK;
         if (DQ) {
           for (int bx = 0; bx < nbox; ++bx)
-            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs)) return false;
+            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs, false)) return false;
           return true;
         }
-        return load(&p.tm_do, rs, c0, hs) && load(&p.tm_q, rs, c0, hs);
+        return load(&p.tm_do, rs, c0, hs, true) && load(&p.tm_q, rs, c0, hs, true);
       };
       // Same order as the MMA thread consumes: contractions of iteration 0,
       // then per iteration i the contractions of i+1 and the slices of i.
@@ -431,11 +481,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float sl2 = p.scale_log2;
-    const long long off = (long long)p.Nkv - p.Nq;   // tail alignment of the causal limit
+    const long long off = (long long)it.kv_len - it.q_len;   // tail alignment of the causal limit
     const int my_row = it.row0 + r;
     float lse_r = INFINITY, delta_r = 0.f;           // dQ: this row's statistics
-    if (DQ && my_row < p.Nq) {
-      const long long li = ((long long)it.b * p.Hq + it.hq) * p.Nq + my_row;
+    if (DQ && my_row < it.q_len) {
+      const long long li = bwd_stat_index(p, it, it.hq, my_row);
       const float l = p.lse[li];
       lse_r = l > -INFINITY ? l * LOG2E_F : INFINITY;   // a row with no softmax has P = 0
       delta_r = p.delta[li];
@@ -444,7 +494,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
     // Caller's mask: element (query, key) at b m0 + hq m1 + query m2 + key m3.
     const int mkind = p.mask_kind;
     const uint8_t* mbase = static_cast<const uint8_t*>(p.mask);
-    const bool mrow_ok = DQ ? my_row < p.Nq : my_row < p.Nkv;
+    const bool mrow_ok = DQ ? my_row < it.q_len : my_row < it.kv_len;
     const uint32_t st_u32 = smem_u32(st);
     bool ok = true;
     for (int i = 0; i < T; ++i) {
@@ -453,12 +503,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       if (!DQ) {
         // Query-tile statistics: lane l loads queries l, l+32, l+64, l+96.
         __syncwarp();
-        const long long lbase = ((long long)it.b * p.Hq + hs) * p.Nq;
+        const long long lbase = bwd_stat_index(p, it, hs, 0);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int qi = rs + 32 * q4 + lane;
           float l2 = INFINITY, dl = 0.f;
-          if (qi < p.Nq) {
+          if (qi < it.q_len) {
             const float l = p.lse[lbase + qi];
             l2 = l > -INFINITY ? l * LOG2E_F : INFINITY;
             dl = p.delta[lbase + qi];
@@ -474,12 +524,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       tc_fence_after();
       // Causal limits: dQ row i sees key k <= i + off; dK/dV key row k is
       // seen by query q >= k - off.
-      const bool need_mask = DQ ? ((long long)rs + BN > p.Nkv ||
+      const bool need_mask = DQ ? ((long long)rs + BN > it.kv_len ||
                                    (causal && (long long)rs + BN - 1 > (long long)it.row0 + off))
                                 : (causal && (long long)it.row0 + BM - 1 - off > (long long)rs);
       const long long lim = DQ ? (long long)my_row + off - rs      // last visible column
                                : (long long)my_row - off - rs;     // first visible column
-      const int kv_cols = p.Nkv - rs;                              // dQ: key columns in range
+      const int kv_cols = it.kv_len - rs;                          // dQ: key columns in range
       // Mask offset of this row at column 0 of the tile, step per column, and
       // the columns in range (dQ: keys; dK/dV: queries of head hs).
       long long moff = 0, mstep = 0;
@@ -489,12 +539,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
           moff = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] +
                  (long long)my_row * p.m_str[2] + (long long)rs * p.m_str[3];
           mstep = p.m_str[3];
-          mcols = mrow_ok ? p.Nkv - rs : 0;
+          mcols = mrow_ok ? it.kv_len - rs : 0;
         } else {
           moff = (long long)it.b * p.m_str[0] + (long long)hs * p.m_str[1] +
                  (long long)rs * p.m_str[2] + (long long)my_row * p.m_str[3];
           mstep = p.m_str[2];
-          mcols = mrow_ok ? p.Nq - rs : 0;
+          mcols = mrow_ok ? it.q_len - rs : 0;
         }
       }
       uint32_t ppk[DQ ? 1 : BN / 2];
@@ -580,21 +630,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
     if (ok) {
       if (DQ) {
         uint8_t* dst = nullptr;
-        if (my_row < p.Nq)
+        if (my_row < it.q_len)
           dst = static_cast<uint8_t*>(p.dq) +
-                ((long long)it.b * p.dq_str[0] + (long long)it.hq * p.dq_str[1] +
-                 (long long)my_row * p.dq_str[2] + it.col_lo) * 2;
+                (bwd_row_offset(p, it, p.dq_str, it.q_row0, my_row, it.hq) + it.col_lo) * 2;
         bwd_store_row(lane_base, it.dv, p.scale, dst, fp16, T > 0);
       } else {
         uint8_t* dstv = nullptr;
         uint8_t* dstk = nullptr;
-        if (my_row < p.Nkv) {
+        if (my_row < it.kv_len) {
           dstv = static_cast<uint8_t*>(p.dv) +
-                 ((long long)it.b * p.dv_str[0] + (long long)it.hkv * p.dv_str[1] +
-                  (long long)my_row * p.dv_str[2] + it.col_lo) * 2;
+                 (bwd_row_offset(p, it, p.dv_str, it.kv_row0, my_row, it.hkv) + it.col_lo) * 2;
           dstk = static_cast<uint8_t*>(p.dk) +
-                 ((long long)it.b * p.dk_str[0] + (long long)it.hkv * p.dk_str[1] +
-                  (long long)my_row * p.dk_str[2] + it.col_lo) * 2;
+                 (bwd_row_offset(p, it, p.dk_str, it.kv_row0, my_row, it.hkv) + it.col_lo) * 2;
         }
         bwd_store_row(lane_base, it.dv, 1.f, dstv, fp16, T > 0);
         bwd_store_row(lane_base + BWD_KV_COLS, it.dv, p.scale, dstk, fp16, T > 0);
@@ -613,7 +660,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
 
 ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
                        size_t kv_smem, cudaStream_t stream) {
-  const long long rows = (long long)P.B * P.Hq * P.Nq;
+  const long long rows = P.varlen ? (long long)P.Hq * P.Tq : (long long)P.B * P.Hq * P.Nq;
   if (rows > 0) {
     ffpa_bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;

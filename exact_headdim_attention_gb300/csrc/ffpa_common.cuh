@@ -119,6 +119,12 @@ struct BwdParams {
   const void* mask;     // broadcast to [B, Hq, Nq, Nkv] by m_str (0 on broadcast dims)
   int64_t m_str[4];
   int mask_kind;
+  // Packed variable-length input (varlen = 1): B sequences, rows of sequence
+  // s at cu_q[s].. / cu_k[s].. of [T, H, D] tensors; LSE and delta [Hq, Tq];
+  // Nq / Nkv are then the maximum sequence lengths.
+  int varlen, Tq;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
   int B, Hq, Hkv, group, Nq, Nkv, D;
   int nchunks, npairs, kchunks;
   int n_qt, n_kt, n_sl_dq, n_sl_kv;

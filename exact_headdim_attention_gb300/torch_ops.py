@@ -11,8 +11,8 @@ replace that call for the supported cases: bf16/fp16 CUDA tensors,
 64 <= D <= 1024 with D % 8 == 0 (D % 64 == 0 for varlen and for the
 backward), no dropout.  The dense operator is
 differentiable through ``ffpa_bwd`` (the backward kernels; a mask enters
-the recomputed scores, but no gradient is formed for the mask itself); the
-varlen operator registers no backward.
+the recomputed scores, but no gradient is formed for the mask itself), and
+the varlen operator through ``ffpa_bwd_varlen``.
 """
 from __future__ import annotations
 
@@ -77,6 +77,28 @@ def _attn_varlen_fwd_fake(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max
     Tq, Hq, _ = q.shape
     return (torch.empty_like(q, memory_format=torch.contiguous_format),
             q.new_empty((Hq, Tq), dtype=torch.float32))
+
+
+def _attn_varlen_setup_context(ctx, inputs, output):
+    (q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal, softmax_scale,
+     enable_gqa) = inputs
+    o, lse = output
+    ctx.save_for_backward(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
+    ctx.max_q, ctx.max_k = max_seqlen_q, max_seqlen_k
+    ctx.causal, ctx.scale, ctx.enable_gqa = causal, softmax_scale, enable_gqa
+
+
+def _attn_varlen_backward(ctx, grad_o, grad_lse):
+    if grad_lse is not None and bool(torch.count_nonzero(grad_lse)):
+        raise NotImplementedError("gradients through the returned LSE are not supported")
+    q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
+    dq, dk, dv = _binding.ffpa_bwd_varlen(grad_o.contiguous(), q, k, v, o, lse, cu_q, cu_k,
+                                          ctx.max_q, ctx.max_k, softmax_scale=ctx.scale,
+                                          causal=ctx.causal, enable_gqa=ctx.enable_gqa)
+    return dq, dk, dv, None, None, None, None, None, None, None
+
+
+attn_varlen_fwd.register_autograd(_attn_varlen_backward, setup_context=_attn_varlen_setup_context)
 
 
 def ffpa_attn_func(query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,

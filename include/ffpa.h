@@ -159,6 +159,32 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
                      const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream);
 
+/*
+ * Backward of ffpa_fwd_varlen (packed THD layout; FFPA API reference,
+ * "ffpa_attn.ffpa_attn_varlen_func"): dq, dk, dv of sum(O * dout), each
+ * sequence differentiated as its own dense problem (causal: lower right).
+ *
+ *   q, o, dout, dq: [Tq, Hq, D]; k, v, dk, dv: [Tk, Hkv, D] (strides over
+ *     T, H, D).
+ *   lse: [Hq, Tq] fp32 contiguous, the forward's; delta: [Hq, Tq] fp32
+ *     contiguous OUTPUT (rowsum(dout * o)).
+ *   cu_seqlens_q / cu_seqlens_k / nseq / max_seqlen_*: as for
+ *     ffpa_fwd_varlen (device arrays, caller precondition).
+ *
+ * Checks and error codes as for ffpa_fwd_varlen, plus a NULL lse or delta
+ * (FFPA_ERR_INVALID).  Three launches on `stream`; no allocation, no
+ * synchronisation.
+ */
+ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                            const int64_t o_str[3], const int64_t do_str[3], const int64_t dq_str[3],
+                            const int64_t dk_str[3], const int64_t dv_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* ffpa_status_string(ffpa_status status);
 

@@ -253,3 +253,33 @@ def test_fine_head_dims_dense_only(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
 def test_fine_head_dim_valid_call_without_gpu(lib):
     assert dense_call(lib, D=120) == pkg.FFPA_ERR_CUDA
+
+
+def bwd_varlen_call(lib, dt=0, Tq=256, Tk=256, Hq=2, Hkv=2, D=64, nseq=2, causal=0, enable_gqa=0,
+                    cu=FAKE, max_q=128, max_k=128, lse=FAKE, delta=FAKE):
+    def st(H):
+        return _arr([H * D, D, 1])
+    qs, ks = st(Hq), st(Hkv)
+    return lib.ffpa_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, lse, FAKE, FAKE, FAKE, delta, dt, Tq, Tk, Hq,
+                               Hkv, D, qs, ks, ks, qs, qs, qs, ks, ks, cu, None, nseq, max_q, max_k,
+                               None, causal, enable_gqa, None)
+
+
+@pytest.mark.parametrize("case", GOLDEN["varlen"], ids=lambda c: c["case"])
+def test_bwd_varlen_documented_errors(lib, case):
+    """The varlen backward applies the varlen forward's checks."""
+    assert bwd_varlen_call(lib, **case["override"]) == case["status"]
+
+
+def test_bwd_varlen_pointer_checks(lib):
+    INVALID = pkg.FFPA_ERR_INVALID
+    assert bwd_varlen_call(lib, cu=None) == INVALID
+    assert bwd_varlen_call(lib, lse=None) == INVALID
+    assert bwd_varlen_call(lib, delta=None) == INVALID
+    assert bwd_varlen_call(lib, max_q=-1) == INVALID
+    assert bwd_varlen_call(lib, Tq=0, Tk=0, lse=None) == pkg.FFPA_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_bwd_varlen_valid_call_without_gpu(lib):
+    assert bwd_varlen_call(lib) == pkg.FFPA_ERR_CUDA

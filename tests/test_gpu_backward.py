@@ -296,3 +296,59 @@ def test_bwd_bounded_wait_reports_timeout_and_context_survives():
     check_grad(dq, rq, "dQ after timeout")
     check_grad(dk, rk, "dK after timeout")
     check_grad(dv, rv, "dV after timeout")
+
+
+# ------------------------------------------------------------------ varlen
+def varlen_bwd_case(lq, lk, Hq, Hkv, D, seed, causal):
+    g = torch.Generator().manual_seed(seed)
+    cu_q = torch.tensor([0] + torch.tensor(lq).cumsum(0).tolist(), dtype=torch.int32)
+    cu_k = torch.tensor([0] + torch.tensor(lk).cumsum(0).tolist(), dtype=torch.int32)
+    Tq, Tk = sum(lq), sum(lk)
+    q = torch.randn(Tq, Hq, D, generator=g).bfloat16()
+    k = torch.randn(Tk, Hkv, D, generator=g).bfloat16()
+    v = torch.randn(Tk, Hkv, D, generator=g).bfloat16()
+    dout = torch.randn(Tq, Hq, D, generator=g).bfloat16()
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    cqd, ckd = cu_q.to(DEV), cu_k.to(DEV)
+    gqa = Hq != Hkv
+    o, lse = pkg.ffpa_fwd_varlen(qd, kd, vd, cqd, ckd, max(lq), max(lk), causal=causal,
+                                 enable_gqa=gqa, return_lse=True)
+    dq, dk, dv, delta = pkg.ffpa_bwd_varlen(dod, qd, kd, vd, o, lse, cqd, ckd, max(lq), max(lk),
+                                            causal=causal, enable_gqa=gqa, return_delta=True)
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal=causal)
+    tag = f"varlen lq={lq} lk={lk} Hq{Hq} Hkv{Hkv} D{D} causal={causal}"
+    check_grad(dq, rq, f"{tag} dQ")
+    check_grad(dk, rk, f"{tag} dK")
+    check_grad(dv, rv, f"{tag} dV")
+    prod = dout.double() * o.double().cpu()
+    assert ((delta.double().cpu() - prod.sum(-1).T).abs() <= 1e-4 * prod.abs().sum(-1).T + 1e-6).all()
+
+
+def test_bwd_varlen_causal_gqa():
+    varlen_bwd_case([300, 128, 1, 450], [300, 128, 1, 450], 4, 2, 128, seed=71, causal=True)
+
+
+def test_bwd_varlen_cross_d512():
+    varlen_bwd_case([100, 200, 0, 64], [150, 200, 30, 300], 2, 2, 512, seed=72, causal=False)
+
+
+def test_bwd_varlen_causal_fewer_keys():
+    """Rows that see no key (lower-right alignment with Lk < Lq) get zero gradients."""
+    varlen_bwd_case([50, 10, 257], [20, 10, 260], 2, 1, 256, seed=73, causal=True)
+
+
+def test_autograd_varlen():
+    lq = [130, 70, 260]
+    g = torch.Generator().manual_seed(74)
+    cu = torch.tensor([0] + torch.tensor(lq).cumsum(0).tolist(), dtype=torch.int32)
+    T, H, D = sum(lq), 2, 192
+    q, k, v, dout = (torch.randn(T, H, D, generator=g).bfloat16() for _ in range(4))
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    o = pkg.ffpa_attn_varlen_func(qd, kd, vd, cu.to(DEV), None, max(lq), max(lq), causal=True)
+    o.backward(dout.to(DEV))
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_varlen(q, k, v, dout, cu, causal=True)
+    check_grad(qd.grad, rq, "autograd varlen dQ")
+    check_grad(kd.grad, rk, "autograd varlen dK")
+    check_grad(vd.grad, rv, "autograd varlen dV")
