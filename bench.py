@@ -22,7 +22,7 @@ pages' convention 4*B*Hq*Nq*Nkv*D (halved when causal).
   the same workload, on the host cores (rank 0, N = 1 only).
 * --impl reference: the oracle alone, timed per step on bounded samples.
 * --pass bwd: the backward instead (one ffpa_bwd call per step: the delta,
-  dQ and dK/dV kernels) on the same workload, from device-resident Q, K, V,
+  dQ, dV and dK kernels) on the same workload, from device-resident Q, K, V,
   O, dO and LSE; TFLOPS in the usual 2.5x-forward convention.
 
 Multi-GPU (torchrun): independent replicas, one per rank (the path has no
@@ -558,7 +558,7 @@ def run_ours_bwd(args):
     peak, peak_src, peak_sustained = read_peaks()
     achieved = value
     cfg = config_of(w, flops)
-    cfg["pass"] = "backward (delta + dQ + dK/dV kernels)"
+    cfg["pass"] = "backward (delta + dQ + dV + dK kernels)"
     line = {
         "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
@@ -569,8 +569,8 @@ def run_ours_bwd(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": peak_src,
-                     "kernel": "ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_kernel<true> (dQ) + "
-                               "ffpa_bwd_kernel<false> (dK/dV), one C call",
+                     "kernel": "ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_kernel<0, false> (dQ) + "
+                               "ffpa_bwd_kernel<1, false> (dV) + ffpa_bwd_kernel<2, false> (dK), one C call",
                      "frac_of_sustained": (round(achieved / peak_sustained, 4)
                                            if peak_sustained else None),
                      "algorithmic_flops_per_launch": flops},
@@ -579,7 +579,7 @@ def run_ours_bwd(args):
                 "api": "exact_headdim_attention_gb300.ffpa_bwd (C ABI ffpa_bwd)",
                 "pipelining": "copy-in, backward and copy-out of consecutive steps on three "
                               "streams with two buffer sets"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "impl": "ours",
     }

@@ -223,29 +223,31 @@ size_t plan_for(Kern kn, int D, Params* P) {
 }
 
 // Backward: output slices, ring depths, shared memory, work items; then the
-// three launches.  P's sizes, tiles, maps, pointers, scale, causal and fp16
+// three or four launches.  P's sizes, tiles, maps, pointers, scale, causal and fp16
 // are set by the caller.
 ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, cudaStream_t stream) {
   P.nchunks = P.D / DK;
-  P.n_sl_dq = (P.D + BWD_DQ_COLS - 1) / BWD_DQ_COLS;
-  P.n_sl_kv = (P.D + BWD_KV_COLS - 1) / BWD_KV_COLS;
-  // Shared memory: one (dQ) or two (dK/dV) 32 KB P/dS tiles, then the ring.
-  const size_t avail = SMEM_LIMIT - BWD_STATIC_RESERVE - 1024;
-  size_t ns_dq = (avail - P_TILE_BYTES) / SLOT_BYTES;
-  size_t ns_kv = (avail - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
-  if (ns_dq > (size_t)BWD_NSLOT_MAX) ns_dq = BWD_NSLOT_MAX;
-  if (ns_kv > (size_t)BWD_NSLOT_MAX) ns_kv = BWD_NSLOT_MAX;
-  P.nslot_dq = static_cast<int>(ns_dq);
-  P.nslot_kv = static_cast<int>(ns_kv);
-  const size_t dq_smem = 1024 + P_TILE_BYTES + ns_dq * SLOT_BYTES;
-  const size_t kv_smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns_kv * SLOT_BYTES;
+  P.n_sl = (P.D + BWD_OUT_COLS - 1) / BWD_OUT_COLS;
+  // Shared memory: one 32 KB P/dS tile, then the ring.
+  size_t ns = (SMEM_LIMIT - BWD_STATIC_RESERVE - 1024 - P_TILE_BYTES) / SLOT_BYTES;
+  if (ns > (size_t)BWD_NSLOT_MAX) ns = BWD_NSLOT_MAX;
+  P.nslot = static_cast<int>(ns);
+  const size_t smem = 1024 + P_TILE_BYTES + ns * SLOT_BYTES;
+  // D <= 128: dV and dK from one S, dP in one kernel (measured on GB300 at
+  // D=128: 324 vs 255 TFLOPS for separate dV and dK kernels; at D=512 the
+  // separate kernels win, 324 vs 288).
+  P.kv_together = P.D <= 128;
+  size_t ns2 = (SMEM_LIMIT - BWD_STATIC_RESERVE - 1024 - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
+  if (ns2 > (size_t)BWD_NSLOT_MAX) ns2 = BWD_NSLOT_MAX;
+  P.nslot_two = static_cast<int>(ns2);
+  const size_t smem_two = 1024 + 2 * (size_t)P_TILE_BYTES + ns2 * SLOT_BYTES;
   P.scale_log2 = P.scale * 1.4426950408889634f;
   P.inject = g_drop_first_copy.load();
   P.timeout_ns = g_timeout_ns.load();
-  const long long dq_items = any_q ? (long long)P.B * P.Hq * P.n_qt * P.n_sl_dq : 0;
-  const long long kv_items = any_k ? (long long)P.B * P.Hkv * P.n_kt * P.n_sl_kv : 0;
+  const long long dq_items = any_q ? (long long)P.B * P.Hq * P.n_qt * P.n_sl : 0;
+  const long long kv_items = any_k ? (long long)P.B * P.Hkv * P.n_kt * P.n_sl : 0;
   if (dq_items > 0x7fffffffLL || kv_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
-  return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), dq_smem, kv_smem, stream);
+  return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), smem, smem_two, stream);
 }
 
 }  // namespace

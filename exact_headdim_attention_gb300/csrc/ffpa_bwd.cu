@@ -8,22 +8,26 @@
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - delta),  delta = rowsum(dO * O),
 //   dQ = scale * dS K,  dK = scale * dS^T Q.
 //
-// Three launches on the caller's stream:
+// Four launches on the caller's stream:
 //   delta   one warp per query row, 16-byte loads of O and dO.
 //   dQ      one CTA per (batch, query head, 128-row query tile, <= 256 dQ
 //           columns); loops over the visible key tiles.
-//   dK/dV   one CTA per (batch, key/value head, 128-key tile, <= 128 dK and
-//           dV columns); loops over every query head of the group and the
+//   dV, dK  one CTA per (batch, key/value head, 128-key tile, <= 256
+//           columns); loops over every query head of the group and the
 //           query tiles that see the key tile, so grouped heads add up in
 //           TMEM and no atomics are needed.
-// Both tensor-core kernels share one body (DQ selects the role).  Per
-// iteration the MMA thread computes two full-D contractions into TMEM
-// (S = A1 B1^T and dP = A2 B2^T: for dQ A = Q, dO and B = K, V; for dK/dV
-// A = K, V and B = Q, dO, i.e. S^T and dP^T), the elementwise warps turn
-// them into 16-bit P and dS in shared memory (128-byte swizzle, K-major),
-// and the MMA thread accumulates the output slices from them (dQ += dS K;
-// dV += P^T dO, dK += dS^T Q) with the B operand read MN-major from the
-// same 64-column boxes that serve the contractions.  TMEM holds the output
+// The three tensor-core kernels share one body (ROLE selects).  Per
+// iteration the MMA thread computes the full-D contractions into TMEM
+// (S = A1 B1^T, and for dQ and dK also dP = A2 B2^T: for dQ A = Q, dO and
+// B = K, V; for dV and dK A = K, V and B = Q, dO, i.e. S^T and dP^T), the
+// elementwise warps turn them into a 16-bit tile in shared memory (128-byte
+// swizzle, K-major): dS for dQ, P^T for dV, dS^T for dK; and the MMA thread
+// accumulates the output slice from it (dQ += dS K; dV += P^T dO;
+// dK += dS^T Q) with the B operand read MN-major from 64-column boxes of the
+// same tensors.  For D > 128, dV and dK are separate kernels so that each
+// holds one tile and a deeper ring, and dV needs neither dP nor delta; for
+// D <= 128 one dK/dV kernel forms both from a single S, dP (both tiles,
+// dV and dK in TMEM columns [0, 128) and [128, 256)).  TMEM holds the output
 // accumulators in columns [0, 256) and S, dP in [256, 384), [384, 512).
 // The contractions of iteration i+1 are issued before the slice MMAs of
 // iteration i, so the tensor core works while the elementwise warps run.
@@ -35,6 +39,10 @@ namespace ffpa {
 
 namespace {
 
+constexpr int BWD_ROLE_DQ = 0;   // rows = queries: dQ
+constexpr int BWD_ROLE_DV = 1;   // rows = keys: dV (P only)
+constexpr int BWD_ROLE_DK = 2;   // rows = keys: dK
+constexpr int BWD_ROLE_DKDV = 3; // rows = keys: dV and dK together (D <= 128)
 constexpr uint32_t BWD_S_COL = 256;
 constexpr uint32_t BWD_DP_COL = 384;
 constexpr int BWD_PRODUCER_WARP = 4;
@@ -109,8 +117,8 @@ __device__ __forceinline__ long long bwd_row_offset(const BwdParams& p, const Bw
 template <bool DQ>
 __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& it) {
   if (DQ) {
-    it.slice = L % p.n_sl_dq;
-    L /= p.n_sl_dq;
+    it.slice = L % p.n_sl;
+    L /= p.n_sl;
     const int heads = p.B * p.Hq;
     int qt, bh;
     if (p.causal) {            // longest query tiles (most visible keys) first
@@ -134,11 +142,11 @@ __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& i
     it.n_iter = kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
     it.qt_first = 0;
     it.nq = 0;
-    it.col_lo = it.slice * BWD_DQ_COLS;
-    it.dv = min(BWD_DQ_COLS, p.D - it.col_lo);
+    it.col_lo = it.slice * BWD_OUT_COLS;
+    it.dv = min(BWD_OUT_COLS, p.D - it.col_lo);
   } else {
-    it.slice = L % p.n_sl_kv;
-    L /= p.n_sl_kv;
+    it.slice = L % p.n_sl;
+    L /= p.n_sl;
     const int heads = p.B * p.Hkv;
     int kt, bh;
     if (p.causal) {            // key tile 0 is seen by every query tile: first
@@ -160,8 +168,8 @@ __device__ __forceinline__ bool bwd_decode(const BwdParams& p, int L, BwdItem& i
     it.qt_first = first_row / BM;
     it.nq = max(0, (it.q_len + BM - 1) / BM - it.qt_first);
     it.n_iter = p.group * it.nq;
-    it.col_lo = it.slice * BWD_KV_COLS;
-    it.dv = min(BWD_KV_COLS, p.D - it.col_lo);
+    it.col_lo = it.slice * BWD_OUT_COLS;
+    it.dv = min(BWD_OUT_COLS, p.D - it.col_lo);
   }
   return true;
 }
@@ -253,29 +261,33 @@ __global__ void __launch_bounds__(256) ffpa_bwd_delta_kernel(const __grid_consta
   if (lane == 0) p.delta[row] = acc;
 }
 
-// UMASK: launched with a caller's mask (mask-loading code present).
-template <bool DQ, bool UMASK>
+// ROLE: BWD_ROLE_DQ / DV / DK.  UMASK: launched with a caller's mask
+// (mask-loading code present).
+template <int ROLE, bool UMASK>
 __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  constexpr bool DQ = ROLE == BWD_ROLE_DQ;         // rows are queries (else keys)
+  constexpr bool NEED_DP = ROLE != BWD_ROLE_DV;    // dS needs dP and delta; dV needs only P
+  constexpr bool TWO = ROLE == BWD_ROLE_DKDV;      // two tiles (P^T, dS^T) and two outputs
   BwdItem it;
   if (!bwd_decode<DQ>(p, blockIdx.x, it)) return;   // uniform across the CTA
 
   const int npairs = p.npairs, nchunks = p.nchunks;
   const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
-  const int NS = DQ ? p.nslot_dq : p.nslot_kv;
+  const int NS = TWO ? p.nslot_two : p.nslot;
   const int T = it.n_iter;
   const unsigned long long tmo = p.timeout_ns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  // [t1: dS (dQ) or P^T (dK/dV)] [t2: dS^T (dK/dV only)] [ring: NS x 32 KB]
+  // [tile: dS (dQ), P^T (dV, dK/dV) or dS^T (dK)] [dS^T (dK/dV)] [ring: NS x 32 KB]
   const uint32_t t1_u32 = smem_u32(smem);
   const uint32_t t2_u32 = t1_u32 + P_TILE_BYTES;
-  const uint32_t ring_u32 = t1_u32 + (DQ ? 1u : 2u) * P_TILE_BYTES;
+  const uint32_t ring_u32 = t1_u32 + (TWO ? 2u : 1u) * P_TILE_BYTES;
   __shared__ __align__(8) uint64_t bar_full[BWD_NSLOT_MAX], bar_empty[BWD_NSLOT_MAX];
   __shared__ __align__(8) uint64_t bar_sd_full, bar_s_free, bar_p_full, bar_pd_done, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  // dK/dV: per-warp copies of the current query tile's log2-domain LSE and
+  // dV, dK: per-warp copies of the current query tile's log2-domain LSE and
   // delta (each warp loads and reads its own, so no cross-warp barrier).
   __shared__ __align__(16) float stat_sh[DQ ? 4 : 4 * 2 * BM];
 
@@ -359,20 +371,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         // dQ: A = Q, dO (query side), B = K, V; dK/dV the other way round.
         for (int pr = 0; pr < npairs; ++pr)
           if (!load(a1, it.row0, 2 * pr, ha, DQ) || !load(b1, rs, 2 * pr, hs, !DQ)) return false;
-        for (int pr = 0; pr < npairs; ++pr)
-          if (!load(a2, it.row0, 2 * pr, ha, DQ) || !load(b2, rs, 2 * pr, hs, !DQ)) return false;
+        if (NEED_DP)
+          for (int pr = 0; pr < npairs; ++pr)
+            if (!load(a2, it.row0, 2 * pr, ha, DQ) || !load(b2, rs, 2 * pr, hs, !DQ)) return false;
         return true;
       };
       auto slice_loads = [&](int i) -> bool {
         int hs, rs;
         stream_coords(i, hs, rs);
+        // The B operand of the slice product: K (dQ), dO (dV) or Q (dK); the
+        // dK/dV role takes dO then Q.
         const int c0 = it.col_lo / DK;
-        if (DQ) {
-          for (int bx = 0; bx < nbox; ++bx)
-            if (!load(&p.tm_k, rs, c0 + 2 * bx, hs, false)) return false;
-          return true;
-        }
-        return load(&p.tm_do, rs, c0, hs, true) && load(&p.tm_q, rs, c0, hs, true);
+        if (TWO) return load(&p.tm_do, rs, c0, hs, true) && load(&p.tm_q, rs, c0, hs, true);
+        const CUtensorMap* m = DQ ? &p.tm_k : ROLE == BWD_ROLE_DV ? &p.tm_do : &p.tm_q;
+        for (int bx = 0; bx < nbox; ++bx)
+          if (!load(m, rs, c0 + 2 * bx, hs, !DQ)) return false;
+        return true;
       };
       // Same order as the MMA thread consumes: contractions of iteration 0,
       // then per iteration i the contractions of i+1 and the slices of i.
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         return true;
       };
       auto contractions = [&]() -> bool {
-        if (!contract(BWD_S_COL) || !contract(BWD_DP_COL)) return false;
+        if (!contract(BWD_S_COL) || (NEED_DP && !contract(BWD_DP_COL))) return false;
         umma_commit(smem_u32(&bar_sd_full));
         return true;
       };
@@ -461,11 +475,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         if (!(ok = wait_on(smem_u32(&bar_s_free), i & 1))) break;
         if (i + 1 < T && !(ok = contractions())) break;
         if (!(ok = wait_on(smem_u32(&bar_p_full), i & 1))) break;
-        if (DQ) {
+        if (TWO) {
+          ok = slice_mma(0, t1_desc, it.dv, i > 0) && slice_mma(128, t2_desc, it.dv, i > 0);
+        } else {
           for (int bx = 0; bx < nbox && ok; ++bx)
             ok = slice_mma(128 * bx, t1_desc, min(128, it.dv - 128 * bx), i > 0);
-        } else {
-          ok = slice_mma(0, t1_desc, it.dv, i > 0) && slice_mma(BWD_KV_COLS, t2_desc, it.dv, i > 0);
         }
         if (!ok) break;
         umma_commit(smem_u32(&bar_pd_done));
@@ -547,16 +561,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
           mcols = mrow_ok ? it.q_len - rs : 0;
         }
       }
-      uint32_t ppk[DQ ? 1 : BN / 2];
-      uint32_t dpk[BN / 2];
+      uint32_t tpk[BN / 2];              // the 16-bit tile row: P (dV, dK/dV) or dS (dQ, dK)
+      uint32_t tpk2[TWO ? BN / 2 : 1];   // dK/dV: the dS^T row
 #pragma unroll
       for (int g = 0; g < BN / 16; ++g) {
         uint32_t sr[16], dr[16];
         tmem_ld16(lane_base + BWD_S_COL + 16 * g, sr);
-        tmem_ld16(lane_base + BWD_DP_COL + 16 * g, dr);
+        if (NEED_DP) tmem_ld16(lane_base + BWD_DP_COL + 16 * g, dr);
         tmem_wait_ld();
         reg_fence(sr);
-        reg_fence(dr);
+        if (NEED_DP) reg_fence(dr);
         float l16[16], d16[16];
         if (DQ) {
 #pragma unroll
@@ -594,29 +608,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
               v = vis ? v : 0.f;
             }
             pe[e] = v;
-            ds[e] = v * (__uint_as_float(dr[c + e]) - d16[c + e]);
+            ds[e] = NEED_DP ? v * (__uint_as_float(dr[c + e]) - d16[c + e]) : 0.f;
           }
-          if (!DQ) ppk[8 * g + c / 2] = fp16 ? pack_f16(pe[0], pe[1]) : pack_bf16(pe[0], pe[1]);
-          dpk[8 * g + c / 2] = fp16 ? pack_f16(ds[0], ds[1]) : pack_bf16(ds[0], ds[1]);
+          const bool use_p = TWO || !NEED_DP;
+          const float t0 = use_p ? pe[0] : ds[0], t1 = use_p ? pe[1] : ds[1];
+          tpk[8 * g + c / 2] = fp16 ? pack_f16(t0, t1) : pack_bf16(t0, t1);
+          if (TWO) tpk2[8 * g + c / 2] = fp16 ? pack_f16(ds[0], ds[1]) : pack_bf16(ds[0], ds[1]);
         }
       }
       // S and dP are in registers: the next contractions may overwrite them.
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
-      // The P/dS tiles are free once the slice MMAs of iteration i-1 are done.
+      // The tile is free once the slice MMAs of iteration i-1 are done.
       if (i >= 1) {
         w = wait_bounded(smem_u32(&bar_pd_done), (i - 1) & 1, &abort_flag, tmo);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
       }
-      if (DQ) {
-        bwd_write_tile_row(t1_u32, r, dpk);
-      } else {
-        bwd_write_tile_row(t1_u32, r, ppk);
-        bwd_write_tile_row(t2_u32, r, dpk);
-      }
+      bwd_write_tile_row(t1_u32, r, tpk);
+      if (TWO) bwd_write_tile_row(t2_u32, r, tpk2);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_p_full));
@@ -635,16 +647,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
                 (bwd_row_offset(p, it, p.dq_str, it.q_row0, my_row, it.hq) + it.col_lo) * 2;
         bwd_store_row(lane_base, it.dv, p.scale, dst, fp16, T > 0);
       } else {
-        uint8_t* dstv = nullptr;
-        uint8_t* dstk = nullptr;
-        if (my_row < it.kv_len) {
-          dstv = static_cast<uint8_t*>(p.dv) +
-                 (bwd_row_offset(p, it, p.dv_str, it.kv_row0, my_row, it.hkv) + it.col_lo) * 2;
-          dstk = static_cast<uint8_t*>(p.dk) +
-                 (bwd_row_offset(p, it, p.dk_str, it.kv_row0, my_row, it.hkv) + it.col_lo) * 2;
+        // dV (no scale) and/or dK (times scale): TMEM column 0, or 0 and 128
+        // for the dK/dV role.
+        const bool row_in = my_row < it.kv_len;
+        if (ROLE == BWD_ROLE_DV || TWO) {
+          uint8_t* dst = row_in ? static_cast<uint8_t*>(p.dv) +
+                                      (bwd_row_offset(p, it, p.dv_str, it.kv_row0, my_row, it.hkv) +
+                                       it.col_lo) * 2
+                                : nullptr;
+          bwd_store_row(lane_base, it.dv, 1.f, dst, fp16, T > 0);
         }
-        bwd_store_row(lane_base, it.dv, 1.f, dstv, fp16, T > 0);
-        bwd_store_row(lane_base + BWD_KV_COLS, it.dv, p.scale, dstk, fp16, T > 0);
+        if (ROLE == BWD_ROLE_DK || TWO) {
+          uint8_t* dst = row_in ? static_cast<uint8_t*>(p.dk) +
+                                      (bwd_row_offset(p, it, p.dk_str, it.kv_row0, my_row, it.hkv) +
+                                       it.col_lo) * 2
+                                : nullptr;
+          bwd_store_row(lane_base + (TWO ? 128u : 0u), it.dv, p.scale, dst, fp16, T > 0);
+        }
       }
     }
   }
@@ -658,29 +677,31 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   }
 }
 
-ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
-                       size_t kv_smem, cudaStream_t stream) {
+template <int ROLE>
+static ffpa_status launch_role(const BwdParams& P, int items, size_t smem, cudaStream_t stream) {
+  auto kern = P.mask != nullptr ? ffpa_bwd_kernel<ROLE, true> : ffpa_bwd_kernel<ROLE, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return FFPA_ERR_CUDA;
+  kern<<<items, BWD_THREADS, smem, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
+}
+
+ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t smem, size_t smem_two,
+                       cudaStream_t stream) {
   const long long rows = P.varlen ? (long long)P.Hq * P.Tq : (long long)P.B * P.Hq * P.Nq;
   if (rows > 0) {
     ffpa_bwd_delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
-  const bool umask = P.mask != nullptr;
-  auto kdq = umask ? ffpa_bwd_kernel<true, true> : ffpa_bwd_kernel<true, false>;
-  auto kkv = umask ? ffpa_bwd_kernel<false, true> : ffpa_bwd_kernel<false, false>;
-  if (dq_items > 0) {
-    if (cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dq_smem)) !=
-        cudaSuccess)
-      return FFPA_ERR_CUDA;
-    kdq<<<dq_items, BWD_THREADS, dq_smem, stream>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
-  }
+  if (dq_items > 0 && launch_role<BWD_ROLE_DQ>(P, dq_items, smem, stream) != FFPA_OK) return FFPA_ERR_CUDA;
   if (kv_items > 0) {
-    if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kv_smem)) !=
-        cudaSuccess)
-      return FFPA_ERR_CUDA;
-    kkv<<<kv_items, BWD_THREADS, kv_smem, stream>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
+    if (P.kv_together) {
+      if (launch_role<BWD_ROLE_DKDV>(P, kv_items, smem_two, stream) != FFPA_OK) return FFPA_ERR_CUDA;
+    } else {
+      if (launch_role<BWD_ROLE_DV>(P, kv_items, smem, stream) != FFPA_OK) return FFPA_ERR_CUDA;
+      if (launch_role<BWD_ROLE_DK>(P, kv_items, smem, stream) != FFPA_OK) return FFPA_ERR_CUDA;
+    }
   }
   return FFPA_OK;
 }

@@ -90,17 +90,17 @@ ffpa_status take_err_single(int* word);
 ffpa_status take_err_pair(int* word);
 ffpa_status take_err_split(int* word);
 
-// Backward (ffpa_bwd.cu): a delta pass, then one kernel for dK/dV (rows =
-// keys) and one for dQ (rows = queries).
+// Backward (ffpa_bwd.cu): a delta pass, then one kernel for dQ (rows =
+// queries) and one each for dV and dK (rows = keys; one for both when
+// D <= 128).
 struct BwdParams;
-ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t dq_smem,
-                       size_t kv_smem, cudaStream_t stream);
+ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t smem, size_t smem_two,
+                       cudaStream_t stream);
 ffpa_status take_err_bwd(int* word);
 constexpr int BWD_THREADS = 192;           // warps 0-3 elementwise, 4 TMA, 5 MMA
 constexpr int BWD_NSLOT_MAX = 6;
 constexpr size_t BWD_STATIC_RESERVE = 6144;
-constexpr int BWD_DQ_COLS = 256;           // dQ columns per CTA
-constexpr int BWD_KV_COLS = 128;           // dK and dV columns per CTA
+constexpr int BWD_OUT_COLS = 256;          // dQ, dV or dK columns per CTA
 
 struct BwdParams {
   // Views (64, N, D/64, H, B) of Q, K, V and dO; box 64 x 128 rows x kchunks.
@@ -127,8 +127,10 @@ struct BwdParams {
   const int32_t* cu_k;
   int B, Hq, Hkv, group, Nq, Nkv, D;
   int nchunks, npairs, kchunks;
-  int n_qt, n_kt, n_sl_dq, n_sl_kv;
-  int nslot_dq, nslot_kv;
+  int n_qt, n_kt, n_sl;   // query tiles, key tiles, 256-column output slices
+  int nslot;              // ring depth (one tile)
+  int kv_together;        // D <= 128: one dK/dV kernel (two tiles, ring depth nslot_two)
+  int nslot_two;
   float scale, scale_log2;
   int causal, fp16, inject;
   unsigned long long timeout_ns;
