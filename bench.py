@@ -302,6 +302,38 @@ def aggregate(elapsed_s: float, flops_per_step: float, steps: int, world: int, d
     return total / tmax / 1e12, tmax
 
 
+def cpu_model() -> str:
+    """Host CPU model (lscpu's "Model name", else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_tiny_one_core():
+    """Seconds of the float64 oracle on the tiny B1 H1 N128 D320 case on one thread."""
+    import oracle
+    from exact_headdim_attention_gb300 import workloads as wl
+    x = wl.materialize(wl.tiny_d320())
+    orc = oracle.default()
+    orc.attn_dense(x["q"], x["k"], x["v"], nthreads=1)
+    t0 = time.perf_counter()
+    orc.attn_dense(x["q"], x["k"], x["v"], nthreads=1)
+    return time.perf_counter() - t0
+
+
 def cpu_baseline(w, x, target_s: float):
     """The float64 oracle on a bounded seeded sample of rows of the workload."""
     import torch
@@ -330,7 +362,8 @@ def cpu_baseline(w, x, target_s: float):
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
             "sample": f"{n} seeded random query rows of {total_rows} (all {w.Nkv} keys each), "
                       f"{dt:.1f} s; full workload would take ~{dt * total_rows / n:.0f} s",
-            "seconds": dt, "rows": n}
+            "seconds": dt, "rows": n, "cpu_model": cpu_model(),
+            "tiny_d320_one_core_s": round(oracle_tiny_one_core(), 4)}
 
 
 def run_ours(args):
@@ -445,7 +478,8 @@ def cpu_baseline_bwd(w, x, dout, target_s: float):
     dt = time.perf_counter() - t0
     return {"value": per_row * n / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
             "sample": f"dQ of {n} seeded random query rows of {total_rows} (softmax, dP and dQ over "
-                      f"all {w.Nkv} keys each), {dt:.1f} s", "seconds": dt, "rows": n}
+                      f"all {w.Nkv} keys each), {dt:.1f} s", "seconds": dt, "rows": n,
+            "cpu_model": cpu_model()}
 
 
 def run_ours_bwd(args):
@@ -655,7 +689,7 @@ def run_reference(args):
         "data": "synthetic (seeded N(0,1) bf16 inputs widened to float64)",
         "config": config_of(w, flops_full), "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

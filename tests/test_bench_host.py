@@ -75,3 +75,8 @@ def test_backward_pass_flag_and_cpu_baseline():
     dout = torch.randn(x["q"].shape, generator=torch.Generator().manual_seed(3)).to(x["q"].dtype)
     cb = bench.cpu_baseline_bwd(w, x, dout, 0.05)
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["rows"] >= cb["cores"]
+
+
+def test_cpu_model_and_one_core_tiny_timing():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    assert bench.oracle_tiny_one_core() > 0
