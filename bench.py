@@ -622,13 +622,24 @@ def run_ours_bwd(args):
     print(json.dumps(line), flush=True)
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed (string
+    literals in these files hold no comment markers)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_sha() -> str:
+    """Hash of the kernel sources' code (comments and layout excluded), so that a
+    recorded ncu capture stays attached to the code it measured."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_headdim_attention_gb300", "csrc")
     for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            h.update(fn.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -77,10 +77,10 @@ struct BwdItem {
   int b, hq, hkv, slice;
   int q_len, kv_len;       // this problem's (sequence's) lengths
   int q_row0, kv_row0;     // varlen: first packed row of the sequence (dense: 0)
-  int row0;       // first row of this CTA's tile: query row (dQ) or key row (dK/dV)
-  int n_iter;     // dQ: key tiles; dK/dV: group heads x visible query tiles
-  int qt_first;   // dK/dV: first query tile that sees the key tile
-  int nq;         // dK/dV: query tiles per head
+  int row0;       // first row of this CTA's tile: query row (dQ) or key row (key-row roles)
+  int n_iter;     // dQ: key tiles; key-row roles (dV, dK, dK/dV): group heads x visible query tiles
+  int qt_first;   // key-row roles: first query tile that sees the key tile
+  int nq;         // key-row roles: query tiles per head
   int col_lo, dv; // output columns [col_lo, col_lo + dv)
 };
 
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  // Streaming-side head and first row of iteration i (dK/dV: query head and
+  // Streaming-side head and first row of iteration i (key-row roles: query head and
   // query tile; dQ: the key tile).
   auto stream_coords = [&](int i, int& head, int& row) {
     if (DQ) {
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       auto contraction_loads = [&](int i) -> bool {
         int hs, rs;
         stream_coords(i, hs, rs);
-        // dQ: A = Q, dO (query side), B = K, V; dK/dV the other way round.
+        // dQ: A = Q, dO (query side), B = K, V; the key-row roles the other way round.
         for (int pr = 0; pr < npairs; ++pr)
           if (!load(a1, it.row0, 2 * pr, ha, DQ) || !load(b1, rs, 2 * pr, hs, !DQ)) return false;
         if (NEED_DP)
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   } else {
     // ------------------------------------------------------------ elementwise
     // Thread r owns TMEM lane r: query row row0 + r (dQ) or key row row0 + r
-    // (dK/dV).  Columns are keys (dQ) or queries (dK/dV).
+    // (key-row roles).  Columns are keys (dQ) or queries (key-row roles).
     const int r = warp * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float sl2 = p.scale_log2;
@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
-      // Causal limits: dQ row i sees key k <= i + off; dK/dV key row k is
+      // Causal limits: dQ row i sees key k <= i + off; key row k is
       // seen by query q >= k - off.
       const bool need_mask = DQ ? ((long long)rs + BN > it.kv_len ||
                                    (causal && (long long)rs + BN - 1 > (long long)it.row0 + off))
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
                                : (long long)my_row - off - rs;     // first visible column
       const int kv_cols = it.kv_len - rs;                          // dQ: key columns in range
       // Mask offset of this row at column 0 of the tile, step per column, and
-      // the columns in range (dQ: keys; dK/dV: queries of head hs).
+      // the columns in range (dQ: keys; key-row roles: queries of head hs).
       long long moff = 0, mstep = 0;
       int mcols = 0;
       if (UMASK) {

@@ -80,3 +80,12 @@ def test_backward_pass_flag_and_cpu_baseline():
 def test_cpu_model_and_one_core_tiny_timing():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
     assert bench.oracle_tiny_one_core() > 0
+
+
+def test_kernel_source_hash_ignores_comments_not_code():
+    a = "int f(int x) {\n  return x + 1;  // one\n}\n/* block\n comment */\n"
+    b = "int f(int x) {   return x + 1; }"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    assert bench.measured_traffic("selfattn_b1_h16_n4096_d512") is not None   # record matches the sources
