@@ -147,7 +147,7 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
  * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd,
  * except that D must be a multiple of 64 (else FFPA_ERR_UNSUPPORTED); a NULL
  * lse or delta is FFPA_ERR_INVALID.  B == 0 or Nq == 0 with Nkv > 0
- * writes zero dk and dv; Nkv == 0 writes zero dq.  Three launches on
+ * writes zero dk and dv; Nkv == 0 writes zero dq.  Three (D <= 128) or four launches on
  * `stream`; no allocation, no synchronisation.
  */
 ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -172,7 +172,7 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
  *     ffpa_fwd_varlen (device arrays, caller precondition).
  *
  * Checks and error codes as for ffpa_fwd_varlen, plus a NULL lse or delta
- * (FFPA_ERR_INVALID).  Three launches on `stream`; no allocation, no
+ * (FFPA_ERR_INVALID).  Three (D <= 128) or four launches on `stream`; no allocation, no
  * synchronisation.
  */
 ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
