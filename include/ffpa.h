@@ -146,9 +146,9 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
  * Strides follow the ffpa_fwd rules (last stride 1, others multiples of 16
  * bytes, 16-byte aligned bases) for every tensor.  Errors as for ffpa_fwd,
  * except that D must be a multiple of 64 (else FFPA_ERR_UNSUPPORTED); a NULL
- * lse or delta is FFPA_ERR_INVALID.  B == 0 or Nq == 0 with Nkv > 0
- * writes zero dk and dv; Nkv == 0 writes zero dq.  Three (D <= 128) or four launches on
- * `stream`; no allocation, no synchronisation.
+ * lse or delta is FFPA_ERR_INVALID.  B == 0 writes nothing; Nq == 0 with
+ * Nkv > 0 writes zero dk and dv; Nkv == 0 writes zero dq.  Three (D <= 128) or
+ * four launches on `stream`; no allocation, no synchronisation.
  */
 ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                      const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
