@@ -1,8 +1,8 @@
 // Backward of exact attention: dQ, dK and dV from Q, K, V, O, dO and the
 // forward's natural-log LSE (FFPA API reference, "ffpa_attn.ffpa_attn_func":
 // backward through FFPAAttnFunc; the Triton backend's `split_launch` option
-// issues "separate backward launches for dKdV and dQ", which is the split
-// used here).
+// launches the dK/dV and the dQ parts separately, which is the split used
+// here).
 //
 // With P = exp(scale * Q K^T - LSE) (the forward's softmax, recomputed),
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - delta),  delta = rowsum(dO * O),

@@ -110,7 +110,7 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
  * cu_seqlens live on the device and are not read by the host: a malformed
  * array is a caller precondition (the Python binding checks it on the host).
  * Other checks and error codes as for ffpa_fwd, except that D must be a
- * multiple of 64 ("large 64-aligned head dims"; else FFPA_ERR_UNSUPPORTED);
+ * multiple of 64 (the varlen API takes head dims aligned to 64; else FFPA_ERR_UNSUPPORTED);
  * nseq < 1 or max_seqlen_* < 0 is FFPA_ERR_INVALID.
  */
 ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -14,11 +14,11 @@
  *   O = softmax(scale * Q K^T + mask) V            per (batch, query head)
  *
  *   - query head hq reads key/value head hq / (Hq / Hkv)  (grouped heads,
- *     "Nh_q must be an integer multiple of Nh_kv");
- *   - a boolean mask keeps an element where it is true ("True means the
- *     element participates"); a floating mask is an additive bias;
+ *     the query head count is a whole multiple of the key/value head count);
+ *   - a boolean mask keeps an element where it is true (a true entry takes
+ *     part in the softmax); a floating mask is an additive bias;
  *   - is_causal: query row r sees key k only when k <= r + (Nkv - Nq)
- *     ("queries aligned to the tail of the KV sequence");
+ *     (the query rows line up with the end of the key sequence);
  *   - scale defaults to 1/sqrt(D) (chosen by the caller of this file).
  *
  * The log-sum-exp returned beside O is the natural logarithm of

@@ -4,8 +4,8 @@ Each ``pin_*`` function takes an ``oracle.Oracle`` instance and raises
 AssertionError when the oracle disagrees with:
 
 * torch's float64 CPU ``scaled_dot_product_attention`` (a library routine
-  with the same definition: FFPA API reference, ``ffpa_attn_func`` is
-  "Signature aligned with torch.nn.functional.scaled_dot_product_attention"),
+  with the same definition: in the FFPA API reference, the signature of
+  ``ffpa_attn_func`` follows torch's scaled_dot_product_attention),
 * closed forms (softmax of known logits, Q = 0 gives a plain mean and
   LSE = ln(#visible keys), Nkv = 1 gives V_0 and LSE = scale*q.k_0),
 * invariants of the definition (rows of softmax sum to one, GQA equals
