@@ -617,6 +617,11 @@ def run_ours_bwd(args):
         "clocks": clocks,
         "impl": "ours",
     }
+    tb = measured_traffic_bwd(w.name)
+    if tb is not None:
+        line["roofline"]["traffic"] = tb["gradient_kernels_total"]
+        line["roofline"]["traffic_note"] = ("ncu DRAM bytes of the dQ, dV and dK launches of one step "
+                                            "(delta kernel not captured)")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_bwd(w, x, dout, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -641,6 +646,20 @@ def kernel_source_sha() -> str:
         with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(fn.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
+
+
+def measured_traffic_bwd(name):
+    """DRAM bytes of one backward step's dQ, dV and dK launches from the committed
+    ncu summary, or None when that capture was taken on different kernel code."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d.get("bwd_dram_bytes_per_step", {}).get(name)
 
 
 def measured_traffic(name):

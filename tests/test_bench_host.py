@@ -89,3 +89,9 @@ def test_kernel_source_hash_ignores_comments_not_code():
     assert bench.strip_comments(a) == bench.strip_comments(b)
     assert bench.strip_comments(a) != bench.strip_comments(c)
     assert bench.measured_traffic("selfattn_b1_h16_n4096_d512") is not None   # record matches the sources
+
+
+def test_backward_traffic_record_matches_sources():
+    tb = bench.measured_traffic_bwd("selfattn_b1_h16_n4096_d512")
+    assert tb is not None
+    assert tb["gradient_kernels_total"] == tb["dq"] + tb["dv"] + tb["dk"]
