@@ -1,6 +1,9 @@
-"""The torch custom operators over the C ABI (forward only).
+"""The torch custom operators over the C ABI (forward, and the backward kernels
+through autograd; the gradients themselves are checked on the GPU in
+test_gpu_backward.py).
 
-CPU: registration, shape-only fake implementations, rejected options.
+CPU: registration (including the autograd formulas), shape-only fake
+implementations, rejected options.
 GPU: eager calls through torch.ops against the float64 oracle, and a
 torch.compile(fullgraph=True) trace through the operator."""
 import pytest
@@ -15,6 +18,18 @@ from exact_headdim_attention_gb300 import workloads as wl
 def test_ops_registered():
     assert hasattr(torch.ops.ffpa, "attn_fwd") and hasattr(torch.ops.ffpa, "attn_varlen_fwd")
     assert pkg.ffpa_attn_func is torch_ops.ffpa_attn_func
+
+
+def test_autograd_formulas_registered():
+    """Both operators carry a backward (the binding's ffpa_bwd / ffpa_bwd_varlen)."""
+    for op, bwd, setup in ((torch_ops.attn_fwd, torch_ops._attn_fwd_backward,
+                            torch_ops._attn_fwd_setup_context),
+                           (torch_ops.attn_varlen_fwd, torch_ops._attn_varlen_backward,
+                            torch_ops._attn_varlen_setup_context)):
+        assert getattr(op, "_backward_fn", bwd) is bwd
+        assert getattr(op, "_setup_context_fn", setup) is setup
+    for name in ("ffpa::attn_fwd", "ffpa::attn_varlen_fwd"):
+        assert torch._C._dispatch_has_kernel_for_dispatch_key(name, "Autograd")
 
 
 def test_fake_shapes_dense_and_varlen():
