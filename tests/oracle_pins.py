@@ -94,7 +94,23 @@ SDPA_CASES = [
     ("add_qtype_causal", 1, 2, 2, 4, 6, 16, True, ("qtype", (1, 2, 4, 6)), torch.bfloat16, None),
     ("fp16", 1, 2, 2, 5, 5, 32, False, None, torch.float16, None),
     ("fp16_add_f32", 1, 2, 1, 3, 4, 16, True, ("f32", (3, 4)), torch.float16, 0.5),
+    # additive masks in the input dtype holding -inf (FFPA API reference, `attn_mask`: a
+    # floating mask is added to the scores; -inf removes the key)
+    ("fp16_add_qtype_neg_inf", 2, 2, 2, 5, 7, 16, False, ("qtype_inf", (2, 1, 5, 7)), torch.float16, None),
+    ("fp16_add_qtype_neg_inf_causal", 1, 4, 2, 4, 9, 32, True, ("qtype_inf", (1, 4, 4, 9)), torch.float16, 0.4),
+    ("bf16_add_qtype_neg_inf", 1, 2, 1, 6, 6, 16, False, ("qtype_inf", (6, 6)), torch.bfloat16, None),
 ]
+
+
+def _inf_mask(g, shape, Nq, Nkv, dtype):
+    """Additive mask in `dtype`: N(0,1) with ~30 % of the entries -inf; the
+    tail diagonal stays finite so that no row loses every key."""
+    m = torch.randn(*shape, generator=g)
+    m = m.masked_fill(torch.rand(*shape, generator=g) < 0.3, -math.inf)
+    m = m.expand(*shape[:-2], Nq, Nkv).clone() if shape[-2] == 1 else m
+    idx = torch.arange(Nq)
+    m[..., idx, idx + (Nkv - Nq)] = 0.5
+    return m.to(dtype)
 
 
 def pin_sdpa_cases(orc, cases=SDPA_CASES):
@@ -107,6 +123,8 @@ def pin_sdpa_cases(orc, cases=SDPA_CASES):
                 mask = _bool_mask(g, shape, Nq, Nkv)
             elif kind == "f32":
                 mask = torch.randn(*shape, generator=g)
+            elif kind == "qtype_inf":
+                mask = _inf_mask(g, shape, Nq, Nkv, dtype)
             else:
                 mask = torch.randn(*shape, generator=g).to(dtype)
         o, lse = orc.attn_dense(q, k, v, attn_mask=mask, scale=scale, is_causal=causal)
@@ -170,6 +188,31 @@ def pin_single_key(orc):
     _close(o, v.double().expand(2, 2, 4, 64), atol=0.0, what="Nkv=1 O")
     want = 0.25 * torch.einsum("bhnd,bhd->bhn", q.double(), k[:, :, 0].double())
     _close(lse, want, atol=1e-12, what="Nkv=1 LSE")
+
+
+def _same_values(a, b, what):
+    """Element-wise identity of two float64 tensors, NaN matching NaN."""
+    a = torch.as_tensor(a, dtype=torch.float64).reshape(-1)
+    b = torch.as_tensor(b, dtype=torch.float64).reshape(-1)
+    nan_a, nan_b = torch.isnan(a), torch.isnan(b)
+    assert torch.equal(nan_a, nan_b), f"{what}: NaN positions differ ({int((nan_a != nan_b).sum())})"
+    bad = (a[~nan_a] != b[~nan_b]).nonzero()
+    assert bad.numel() == 0, f"{what}: {bad.numel()} values differ, first at {int(bad[0])}"
+
+
+def pin_every_16bit_pattern(orc):
+    """Nkv = 1 passes V through unchanged (weight exp(0) / 1), so every one of
+    the 65 536 bit patterns of fp16 and of bf16 placed in V must come back as
+    torch's own widening of that pattern: normals, both zeros, every
+    subnormal, +-inf and NaN (IEEE binary16 and the top half of binary32)."""
+    pat = torch.arange(65536, dtype=torch.int32).to(torch.int16).reshape(1, 1024, 1, 64)
+    g = torch.Generator().manual_seed(16)
+    for dtype in (torch.float16, torch.bfloat16):
+        v = pat.view(dtype)
+        q = torch.randn(1, 1024, 1, 64, generator=g).to(dtype)
+        k = torch.randn(1, 1024, 1, 64, generator=g).to(dtype)
+        o, _ = orc.attn_dense(q, k, v)
+        _same_values(o, v.double(), f"{dtype} patterns")
 
 
 def pin_rows_sum_to_one(orc):

@@ -29,6 +29,10 @@ MUTANTS = {
                        "widen(kbase + (int64_t)kk * k_row_stride + d, dtype)"),
     "varlen_top_left": ("i + (int64_t)nk - nq", "i"),
     "fp16_exponent": ("expo - 25", "expo - 24"),
+    "fp16_subnormal_exponent": ("mag = ldexp((double)frac, -24);", "mag = ldexp((double)frac, -25);"),
+    "fp16_subnormal_implicit_bit": ("mag = ldexp((double)frac, -24);", "mag = ldexp((double)(frac | 0x400), -24);"),
+    "fp16_inf_as_nan": ("mag = frac ? NAN : INFINITY;", "mag = NAN;"),
+    "fp16_nan_as_inf": ("mag = frac ? NAN : INFINITY;", "mag = INFINITY;"),
     "qtype_mask_ignored": ("x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);", ""),
     "masked_row_nan": ("if (m == -INFINITY) {", "if (0) {"),
     # backward
