@@ -648,10 +648,12 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic_bwd(name):
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def measured_traffic_bwd(name, path=TRAFFIC_PATH):
     """DRAM bytes of one backward step's dQ, dV and dK launches from the committed
     ncu summary, or None when that capture was taken on different kernel code."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
@@ -662,10 +664,9 @@ def measured_traffic_bwd(name):
     return d.get("bwd_dram_bytes_per_step", {}).get(name)
 
 
-def measured_traffic(name):
+def measured_traffic(name, path=TRAFFIC_PATH):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
     or None when that capture was taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)

@@ -19,6 +19,8 @@ from ._binding import (  # noqa: F401
     FFPA_MASK_NONE,
     FFPA_OK,
     FFPAError,
+    KERNEL_VARIANTS,
+    Options,
     default_scale,
     ffpa_bwd,
     ffpa_bwd_varlen,
@@ -28,9 +30,6 @@ from ._binding import (  # noqa: F401
     ffpa_status_string,
     lib_path,
     load_library,
-    set_wait_timeout_ns,
-    set_kernel_variant,
     selected_kernel,
-    inject_dropped_copy,
 )
 from .torch_ops import ffpa_attn_func, ffpa_attn_varlen_func  # noqa: F401,E402

@@ -22,13 +22,19 @@ FFPA_OK, FFPA_ERR_DTYPE, FFPA_ERR_INVALID, FFPA_ERR_UNSUPPORTED, FFPA_ERR_CUDA, 
 FFPA_BF16, FFPA_FP16 = 0, 1
 FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4)
 
-EXPORTED = ("ffpa_fwd", "ffpa_fwd_varlen", "ffpa_bwd", "ffpa_bwd_varlen", "ffpa_status_string", "ffpa_last_device_error",
-            "ffpa_set_wait_timeout_ns", "ffpa_test_drop_first_copy", "ffpa_set_kernel_variant",
-            "ffpa_selected_kernel")
+EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", "ffpa_bwd",
+            "ffpa_bwd_ex", "ffpa_bwd_varlen", "ffpa_bwd_varlen_ex", "ffpa_status_string",
+            "ffpa_last_device_error", "ffpa_selected_kernel")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
 
 _lib = None
+
+
+class Options(ctypes.Structure):
+    """ffpa_options of include/ffpa.h (one call's status word, wait limit, kernel, test hook)."""
+    _fields_ = [("status", ctypes.c_void_p), ("wait_timeout_ns", ctypes.c_uint64),
+                ("kernel", ctypes.c_int), ("test_drop_first_copy", ctypes.c_int)]
 
 
 class FFPAError(RuntimeError):
@@ -70,29 +76,26 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
             f"libffpa.so not found at {p}: build it with "
             "`python -m exact_headdim_attention_gb300.build` (no fallback path exists)")
     lib = ctypes.CDLL(str(p))
-    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
-    lib.ffpa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P, P, I, I, P]
-    lib.ffpa_fwd.restype = I
-    lib.ffpa_fwd_varlen.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, I, I, I, P,
-                                    I, I, P]
-    lib.ffpa_fwd_varlen.restype = I
-    lib.ffpa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P,
-                             P, P, I, P, P, I, I, P]
-    lib.ffpa_bwd.restype = I
-    lib.ffpa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P,
-                                    P, P, P, P, I, I, I, P, I, I, P]
-    lib.ffpa_bwd_varlen.restype = I
+    P, I = ctypes.c_void_p, ctypes.c_int
+    O = ctypes.POINTER(Options)
+    sigs = {
+        "ffpa_fwd": [P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P, P, I, I, P],
+        "ffpa_fwd_varlen": [P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, I, I, I, P, I, I, P],
+        "ffpa_bwd": [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, I,
+                     P, P, I, I, P],
+        "ffpa_bwd_varlen": [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P,
+                            P, I, I, I, P, I, I, P],
+    }
+    for name, args in sigs.items():
+        getattr(lib, name).argtypes = args
+        getattr(lib, name).restype = I
+        getattr(lib, name + "_ex").argtypes = args + [O]
+        getattr(lib, name + "_ex").restype = I
     lib.ffpa_status_string.argtypes = [I]
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_last_device_error.argtypes = [P]
     lib.ffpa_last_device_error.restype = I
-    lib.ffpa_set_wait_timeout_ns.argtypes = [L]
-    lib.ffpa_set_wait_timeout_ns.restype = None
-    lib.ffpa_test_drop_first_copy.argtypes = [I]
-    lib.ffpa_test_drop_first_copy.restype = None
-    lib.ffpa_set_kernel_variant.argtypes = [I]
-    lib.ffpa_set_kernel_variant.restype = None
-    lib.ffpa_selected_kernel.argtypes = [I, I]
+    lib.ffpa_selected_kernel.argtypes = [I, I, I]
     lib.ffpa_selected_kernel.restype = I
     if path is None:
         _lib = lib
@@ -135,6 +138,48 @@ def _stream_handle(stream, t: torch.Tensor | None = None) -> int | None:
     return stream.cuda_stream or None
 
 
+def _options(q: torch.Tensor, kernel, status, wait_timeout_ns, test_drop_first_copy):
+    """ctypes ffpa_options for one call, or None when every field is the default."""
+    if kernel is None and status is None and not wait_timeout_ns and not test_drop_first_copy:
+        return None
+    if kernel is not None and kernel not in KERNEL_VARIANTS:
+        raise ValueError(f"kernel must be one of {sorted(KERNEL_VARIANTS)}, got {kernel!r}")
+    if status is not None:
+        if (status.dtype != torch.int32 or status.numel() != 1 or status.device != q.device):
+            raise ValueError("status must be a one-element int32 tensor on q's device")
+    return ctypes.byref(Options(None if status is None else status.data_ptr(),
+                                int(wait_timeout_ns or 0), KERNEL_VARIANTS[kernel or "auto"],
+                                int(bool(test_drop_first_copy))))
+
+
+def _check_buffer(t, name, shape, dtype, device, contiguous=False):
+    """A caller-supplied output: its shape, dtype and device must be those the
+    library writes (it sizes every write from q and k)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dim() != len(shape) or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _device_copy(cu: torch.Tensor, device, stream):
+    """cu_seqlens on the launch device, copied on the launch stream so that the
+    copy is ordered before the kernel and its memory is not reused (by torch's
+    caching allocator) while the kernel may still read it."""
+    if stream is None or not isinstance(stream, torch.cuda.Stream):
+        return cu.to(device)
+    with torch.cuda.stream(stream):
+        d = cu.to(device)
+    if d is not cu:
+        d.record_stream(stream)
+    return d
+
+
 _REJECTED = ("window_size", "softcap", "sink", "attention_mask", "block_mask", "score_mod",
              "aux_tensors", "seqused_k", "block_table", "num_splits", "alibi_slopes")
 
@@ -142,14 +187,20 @@ _REJECTED = ("window_size", "softcap", "sink", "attention_mask", "block_mask", "
 def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
              dropout_p: float = 0.0, is_causal: bool = False, scale: float | None = None,
              enable_gqa: bool = False, *, return_lse: bool = False, out=None, lse=None,
-             stream=None, **kwargs):
-    """Dense attention forward through the C ABI ``ffpa_fwd``.
+             stream=None, kernel=None, status=None, wait_timeout_ns=None,
+             test_drop_first_copy=False, **kwargs):
+    """Dense attention forward through the C ABI ``ffpa_fwd_ex``.
 
     q [B,Hq,Nq,D], k/v [B,Hkv,Nkv,D] (bf16 or fp16, CUDA, D stride 1);
     attn_mask broadcastable to [B,Hq,Nq,Nkv] (bool: True participates;
     float32 or the q dtype: additive).  Returns O [B,Hq,Nq,D], or (O, LSE
     [B,Hq,Nq] fp32) with return_lse.  Follows the FFPA API reference,
-    ``ffpa_attn.ffpa_attn_func``."""
+    ``ffpa_attn.ffpa_attn_func``.
+
+    Per-call options (ffpa_options): kernel ("auto", "single", "pair",
+    "split"), status (a one-element int32 device tensor that receives
+    FFPA_ERR_DEVICE_TIMEOUT if a wait of this call runs out; the caller
+    zeroes it), wait_timeout_ns, and the test hook test_drop_first_copy."""
     if kwargs:
         raise TypeError(f"unexpected keyword arguments: {sorted(kwargs)}")
     if dropout_p != 0.0:
@@ -165,18 +216,20 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
         raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(out, "out", q.shape, q.dtype, q.device)
     if return_lse and lse is None:
         lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
-    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()
-                            or tuple(lse.shape) != (B, Hq, Nq)):
-        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
+    if lse is not None:
+        _check_buffer(lse, "lse", (B, Hq, Nq), torch.float32, q.device, contiguous=True)
     mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
-    st = lib.ffpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                      None if lse is None else lse.data_ptr(), _dtype_code(q),
-                      B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v), _strides(out),
-                      mptr, mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
-                      _stream_handle(stream, q))
+    opts = _options(q, kernel, status, wait_timeout_ns, test_drop_first_copy)
+    st = lib.ffpa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         None if lse is None else lse.data_ptr(), _dtype_code(q),
+                         B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v), _strides(out),
+                         mptr, mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
+                         _stream_handle(stream, q), opts)
     del keep
     if st != FFPA_OK:
         _raise(st, "ffpa_fwd")
@@ -213,7 +266,8 @@ def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
 def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
              out: torch.Tensor, lse: torch.Tensor, is_causal: bool = False,
              scale: float | None = None, enable_gqa: bool = False, attn_mask=None, *, dq=None,
-             dk=None, dv=None, delta=None, return_delta: bool = False, stream=None):
+             dk=None, dv=None, delta=None, return_delta: bool = False, stream=None, status=None,
+             wait_timeout_ns=None, test_drop_first_copy=False):
     """Dense attention backward through the C ABI ``ffpa_bwd``.
 
     dout, q, out [B,Hq,Nq,D]; k, v [B,Hkv,Nkv,D]; lse [B,Hq,Nq] fp32 from the
@@ -234,28 +288,41 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
                          f"out {tuple(out.shape)}, dout {tuple(dout.shape)}")
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
         raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
-    if dq is None:
-        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
-    if dk is None:
-        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
-    if dv is None:
-        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
-    if delta is None:
-        delta = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
-    if delta.dtype != torch.float32 or not delta.is_contiguous() or tuple(delta.shape) != (B, Hq, Nq):
-        raise ValueError("delta must be a contiguous float32 [B, Hq, Nq] tensor")
+    dq, dk, dv, delta = _grad_buffers(q, k, v, dq, dk, dv, delta, (B, Hq, Nq))
     mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
-    st = lib.ffpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
-                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
-                      _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v),
-                      _strides(out), _strides(dout), _strides(dq), _strides(dk), _strides(dv), mptr,
-                      mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
-                      _stream_handle(stream, q))
+    opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
+    st = lib.ffpa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         delta.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q),
+                         _strides(k), _strides(v), _strides(out), _strides(dout), _strides(dq),
+                         _strides(dk), _strides(dv), mptr, mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
+                         _stream_handle(stream, q), opts)
     del keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)
+
+
+def _grad_buffers(q, k, v, dq, dk, dv, delta, delta_shape):
+    """The gradient outputs and delta: allocated when not given, else checked."""
+    if dq is None:
+        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(dq, "dq", q.shape, q.dtype, q.device)
+    if dk is None:
+        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(dk, "dk", k.shape, k.dtype, q.device)
+    if dv is None:
+        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(dv, "dv", v.shape, v.dtype, q.device)
+    if delta is None:
+        delta = torch.empty(delta_shape, dtype=torch.float32, device=q.device)
+    else:
+        _check_buffer(delta, "delta", delta_shape, torch.float32, q.device, contiguous=True)
+    return dq, dk, dv, delta
 
 
 def _check_cu(cu: torch.Tensor, T: int, name: str) -> list[int]:
@@ -273,7 +340,8 @@ def ffpa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     cu_seqlens_k: torch.Tensor | None, max_seqlen_q: int, max_seqlen_k: int, *,
                     dropout_p: float = 0.0, softmax_scale: float | None = None,
                     causal: bool = False, enable_gqa: bool = False, return_lse: bool = False,
-                    out=None, lse=None, stream=None, **kwargs):
+                    out=None, lse=None, stream=None, kernel=None, status=None,
+                    wait_timeout_ns=None, test_drop_first_copy=False, **kwargs):
     """Packed varlen attention forward through the C ABI ``ffpa_fwd_varlen``.
 
     q [Tq,Hq,D], k/v [Tk,Hkv,D]; cu_seqlens_* int32 [nseq+1] (cu_seqlens_k
@@ -310,17 +378,23 @@ def ffpa_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
         raise ValueError("max_seqlen_* is smaller than a sequence length")
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(out, "out", q.shape, q.dtype, q.device)
     if return_lse and lse is None:
         lse = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
-    cuq = cu_seqlens_q.to(q.device)
-    cuk = None if cu_seqlens_k is None else cu_seqlens_k.to(q.device)
+    if lse is not None:
+        _check_buffer(lse, "lse", (Hq, Tq), torch.float32, q.device, contiguous=True)
+    cuq = _device_copy(cu_seqlens_q, q.device, stream)
+    cuk = None if cu_seqlens_k is None else _device_copy(cu_seqlens_k, q.device, stream)
     sc = None if softmax_scale is None else ctypes.byref(ctypes.c_float(float(softmax_scale)))
-    st = lib.ffpa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             None if lse is None else lse.data_ptr(), _dtype_code(q),
-                             Tq, Tk, Hq, Hkv, D, _strides(q), _strides(k), _strides(v), _strides(out),
-                             cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
-                             int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
-                             int(bool(enable_gqa)), _stream_handle(stream, q))
+    opts = _options(q, kernel, status, wait_timeout_ns, test_drop_first_copy)
+    st = lib.ffpa_fwd_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                None if lse is None else lse.data_ptr(), _dtype_code(q),
+                                Tq, Tk, Hq, Hkv, D, _strides(q), _strides(k), _strides(v),
+                                _strides(out), cuq.data_ptr(),
+                                None if cuk is None else cuk.data_ptr(), len(cq) - 1,
+                                int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
+                                int(bool(enable_gqa)), _stream_handle(stream, q), opts)
     if st != FFPA_OK:
         _raise(st, "ffpa_fwd_varlen")
     return (out, lse) if return_lse else out
@@ -331,7 +405,8 @@ def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     cu_seqlens_k: torch.Tensor | None, max_seqlen_q: int, max_seqlen_k: int, *,
                     softmax_scale: float | None = None, causal: bool = False,
                     enable_gqa: bool = False, dq=None, dk=None, dv=None, delta=None,
-                    return_delta: bool = False, stream=None):
+                    return_delta: bool = False, stream=None, status=None, wait_timeout_ns=None,
+                    test_drop_first_copy=False):
     """Packed varlen backward through the C ABI ``ffpa_bwd_varlen``.
 
     dout, q, out [Tq,Hq,D]; k, v [Tk,Hkv,D]; lse [Hq,Tq] fp32 from
@@ -359,59 +434,38 @@ def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
     if max(b - a for a, b in zip(cq, cq[1:])) > max_seqlen_q or \
             max(b - a for a, b in zip(ck, ck[1:])) > max_seqlen_k:
         raise ValueError("max_seqlen_* is smaller than a sequence length")
-    if dq is None:
-        dq = torch.empty_like(q, memory_format=torch.contiguous_format)
-    if dk is None:
-        dk = torch.empty_like(k, memory_format=torch.contiguous_format)
-    if dv is None:
-        dv = torch.empty_like(v, memory_format=torch.contiguous_format)
-    if delta is None:
-        delta = torch.empty(Hq, Tq, dtype=torch.float32, device=q.device)
-    if delta.dtype != torch.float32 or not delta.is_contiguous() or tuple(delta.shape) != (Hq, Tq):
-        raise ValueError("delta must be a contiguous float32 [Hq, Tq] tensor")
-    cuq = cu_seqlens_q.to(q.device)
-    cuk = None if cu_seqlens_k is None else cu_seqlens_k.to(q.device)
+    dq, dk, dv, delta = _grad_buffers(q, k, v, dq, dk, dv, delta, (Hq, Tq))
+    cuq = _device_copy(cu_seqlens_q, q.device, stream)
+    cuk = None if cu_seqlens_k is None else _device_copy(cu_seqlens_k, q.device, stream)
     sc = None if softmax_scale is None else ctypes.byref(ctypes.c_float(float(softmax_scale)))
-    st = lib.ffpa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                             dv.data_ptr(), delta.data_ptr(), _dtype_code(q), Tq, Tk, Hq, Hkv, D,
-                             _strides(q), _strides(k), _strides(v), _strides(out), _strides(dout),
-                             _strides(dq), _strides(dk), _strides(dv), cuq.data_ptr(),
-                             None if cuk is None else cuk.data_ptr(), len(cq) - 1,
-                             int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
-                             int(bool(enable_gqa)), _stream_handle(stream, q))
+    opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
+    st = lib.ffpa_bwd_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), delta.data_ptr(), _dtype_code(q), Tq, Tk, Hq, Hkv, D,
+                                _strides(q), _strides(k), _strides(v), _strides(out),
+                                _strides(dout), _strides(dq), _strides(dk), _strides(dv),
+                                cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
+                                int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
+                                int(bool(enable_gqa)), _stream_handle(stream, q), opts)
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd_varlen")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)
 
 
 def ffpa_last_device_error(stream=None) -> int:
-    """Checked mode: synchronise the stream and return (and clear) the device error word."""
+    """Checked mode for calls made without a status word: synchronise the stream and
+    return (and clear) the device's shared fallback status word (see ffpa.h)."""
     return load_library().ffpa_last_device_error(_stream_handle(stream))
 
 
-def set_wait_timeout_ns(ns: int) -> None:
-    load_library().ffpa_set_wait_timeout_ns(int(ns))
-
-
-def set_kernel_variant(name: str) -> None:
-    """Choose the kernel for later launches: "auto", "single", "pair" or "split" (see ffpa.h)."""
-    if name not in KERNEL_VARIANTS:
-        raise ValueError(f"kernel variant must be one of {sorted(KERNEL_VARIANTS)}, got {name!r}")
-    load_library().ffpa_set_kernel_variant(KERNEL_VARIANTS[name])
-
-
-def selected_kernel(D: int, varlen: bool = False) -> str:
-    """Name of the kernel ("single", "pair" or "split") a launch would use now for head dim D."""
-    v = load_library().ffpa_selected_kernel(int(D), int(bool(varlen)))
+def selected_kernel(D: int, varlen: bool = False, kernel: str = "auto") -> str:
+    """Name of the kernel ("single", "pair" or "split") a call with `kernel` would use for head dim D."""
+    if kernel not in KERNEL_VARIANTS:
+        raise ValueError(f"kernel must be one of {sorted(KERNEL_VARIANTS)}, got {kernel!r}")
+    v = load_library().ffpa_selected_kernel(int(D), int(bool(varlen)), KERNEL_VARIANTS[kernel])
     if v < 0:
         raise ValueError(f"unsupported head dimension {D}")
     return {code: name for name, code in KERNEL_VARIANTS.items()}[v]
-
-
-def inject_dropped_copy(enable: bool) -> None:
-    """Test hook: make the next launches skip their first tensor copy (see ffpa.h)."""
-    load_library().ffpa_test_drop_first_copy(int(bool(enable)))
 
 
 def default_scale(D: int) -> float:

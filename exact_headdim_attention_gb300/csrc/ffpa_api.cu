@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -18,9 +19,141 @@ namespace {
 
 using namespace ffpa;
 
-std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
-std::atomic<int> g_variant{FFPA_VARIANT_AUTO};
-std::atomic<int> g_drop_first_copy{0};
+constexpr unsigned long long DEFAULT_TIMEOUT_NS = 2000000000ull;
+constexpr int MAX_DEVICES = 64;
+
+// Status word of calls that pass none (one per device, set by the kernels
+// when a wait runs out; read and cleared by ffpa_last_device_error).
+__device__ int g_status_fallback;
+
+// What one call asked for (ffpa_options), with the defaults filled in.
+struct CallOpts {
+  int* status;                   // device word, or NULL for the device's fallback word
+  unsigned long long timeout_ns;
+  int kernel;                    // FFPA_VARIANT_*
+  int drop;                      // test hook
+};
+
+ffpa_status read_opts(const ffpa_options* o, CallOpts* c) {
+  c->status = o ? o->status : nullptr;
+  c->timeout_ns = o && o->wait_timeout_ns ? o->wait_timeout_ns : DEFAULT_TIMEOUT_NS;
+  c->kernel = o ? o->kernel : FFPA_VARIANT_AUTO;
+  c->drop = o && o->test_drop_first_copy ? 1 : 0;
+  if (c->kernel < FFPA_VARIANT_AUTO || c->kernel > FFPA_VARIANT_SPLIT) return FFPA_ERR_INVALID;
+  return FFPA_OK;
+}
+
+// Facts about a device that never change while the process runs, looked up
+// once: whether it is an sm_103 part, and the address of its fallback word.
+struct DeviceFacts {
+  std::once_flag once;
+  ffpa_status arch = FFPA_ERR_CUDA;
+  int* fallback = nullptr;
+};
+DeviceFacts g_devices[MAX_DEVICES];
+
+// Makes `dev` the library runtime's current device for the lifetime of the
+// object and restores the previous one afterwards, so that a call leaves
+// the calling thread's current device as it found it.
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev) : dev_(dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) {
+      cudaGetLastError();
+      prev_ = -1;
+    }
+    ok_ = prev_ == dev_ || cudaSetDevice(dev_) == cudaSuccess;
+  }
+  ~DeviceScope() {
+    if (ok_ && prev_ >= 0 && prev_ != dev_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int dev_;
+  int prev_ = -1;
+  bool ok_ = false;
+};
+
+// The device's facts (computed on first use with `dev` current).
+const DeviceFacts& device_facts(int dev) {
+  DeviceFacts& f = g_devices[dev];
+  std::call_once(f.once, [&] {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      f.arch = FFPA_ERR_CUDA;
+      return;
+    }
+    f.arch = (major == 10 && minor == 3) ? FFPA_OK : FFPA_ERR_UNSUPPORTED;
+    void* addr = nullptr;
+    if (f.arch == FFPA_OK) {
+      if (cudaGetSymbolAddress(&addr, g_status_fallback) != cudaSuccess) {
+        cudaGetLastError();
+        f.arch = FFPA_ERR_CUDA;
+      }
+    }
+    f.fallback = static_cast<int*>(addr);
+  });
+  return f;
+}
+
+// The device that owns `ptr`: device or managed memory only (host memory,
+// even mapped, is rejected: the tensor-memory-accelerator copies and the
+// kernels' stores expect memory of the GPU they run on).
+ffpa_status pointer_device(const void* ptr, int* dev) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return FFPA_ERR_CUDA;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return FFPA_ERR_INVALID;
+  if (attr.device < 0 || attr.device >= MAX_DEVICES) return FFPA_ERR_UNSUPPORTED;
+  *dev = attr.device;
+  return FFPA_OK;
+}
+
+// Every non-null pointer of the call lives on the device of the first one;
+// that device is an sm_103 part.  On success *dev is that device.
+ffpa_status check_devices(std::initializer_list<const void*> ptrs, int* dev) {
+  int d0 = -1;
+  for (const void* p : ptrs) {
+    if (!p) continue;
+    int d = -1;
+    const ffpa_status st = pointer_device(p, &d);
+    if (st != FFPA_OK) return st;
+    if (d0 < 0)
+      d0 = d;
+    else if (d != d0)
+      return FFPA_ERR_INVALID;
+  }
+  if (d0 < 0) return FFPA_ERR_INVALID;
+  *dev = d0;
+  return FFPA_OK;
+}
+
+// Device set-up shared by the entry points once the arguments are valid:
+// the arch check and the status word the kernels report to.
+ffpa_status device_status_word(int dev, const CallOpts& o, int** err) {
+  const DeviceFacts& f = device_facts(dev);
+  if (f.arch != FFPA_OK) return f.arch;
+  if (o.status) {
+    int d = -1;
+    const ffpa_status st = pointer_device(o.status, &d);
+    if (st != FFPA_OK) return st;
+    if (d != dev || (reinterpret_cast<uintptr_t>(o.status) & 3u) != 0) return FFPA_ERR_INVALID;
+  }
+  *err = o.status ? o.status : f.fallback;
+  return FFPA_OK;
+}
+
+// Element size of a mask kind (bytes).
+size_t mask_esz(ffpa_mask_kind mk) {
+  return mk == FFPA_MASK_BOOL ? 1 : mk == FFPA_MASK_ADD_F32 ? 4 : 2;
+}
+
+bool aligned_to(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -77,28 +210,6 @@ ffpa_status encode_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const v
   return r == CUDA_SUCCESS ? FFPA_OK : FFPA_ERR_INVALID;
 }
 
-// Makes the device that owns `ptr` current for this library's runtime (the
-// runtime is linked statically, so its current device is not the caller's),
-// then requires compute capability 10.3 (sm_103).
-ffpa_status check_device(const void* ptr, int* dev_out) {
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return FFPA_ERR_CUDA;
-  }
-  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-    return FFPA_ERR_INVALID;
-  const int dev = attr.device;
-  if (cudaSetDevice(dev) != cudaSuccess) return FFPA_ERR_CUDA;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return FFPA_ERR_CUDA;
-  if (major != 10 || minor != 3) return FFPA_ERR_UNSUPPORTED;
-  *dev_out = dev;
-  return FFPA_OK;
-}
-
 // Splits D into at most 256-column output slices, sizes the V stage, and
 // decides whether Q stays resident in shared memory (D <= 512) and how many
 // 32 KB ring slots fit beside it.  Returns the dynamic shared memory bytes.
@@ -153,9 +264,8 @@ bool split_eligible(int D) { return D >= 128 && D % 128 == 0 && D / 2 <= DV_MAX;
 // D=128 the single-CTA kernel's shorter per-tile chain wins, and on packed
 // varlen batches of mixed lengths the 256-row pair tiles waste more rows on
 // short sequences than they save.
-Kern choose_kernel(int D, bool varlen) {
+Kern choose_kernel(int D, bool varlen, int v) {
   if (D % DK != 0) return Kern::SINGLE;   // only the single-CTA kernel takes zero-padded chunks
-  const int v = g_variant.load();
   if (v == FFPA_VARIANT_SINGLE) return Kern::SINGLE;
   if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
   if (v == FFPA_VARIANT_SPLIT) return split_eligible(D) ? Kern::SPLIT : Kern::SINGLE;
@@ -225,7 +335,7 @@ size_t plan_for(Kern kn, int D, Params* P) {
 // Backward: output slices, ring depths, shared memory, work items; then the
 // three or four launches.  P's sizes, tiles, maps, pointers, scale, causal and fp16
 // are set by the caller.
-ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, cudaStream_t stream) {
+ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, cudaStream_t stream) {
   P.nchunks = P.D / DK;
   P.n_sl = (P.D + BWD_OUT_COLS - 1) / BWD_OUT_COLS;
   // Shared memory: one 32 KB P/dS tile, then the ring.
@@ -242,8 +352,8 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, cudaStream_t stream
   P.nslot_two = static_cast<int>(ns2);
   const size_t smem_two = 1024 + 2 * (size_t)P_TILE_BYTES + ns2 * SLOT_BYTES;
   P.scale_log2 = P.scale * 1.4426950408889634f;
-  P.inject = g_drop_first_copy.load();
-  P.timeout_ns = g_timeout_ns.load();
+  P.inject = o.drop;
+  P.timeout_ns = o.timeout_ns;
   const long long dq_items = any_q ? (long long)P.B * P.Hq * P.n_qt * P.n_sl : 0;
   const long long kv_items = any_k ? (long long)P.B * P.Hkv * P.n_kt * P.n_sl : 0;
   if (dq_items > 0x7fffffffLL || kv_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
@@ -251,6 +361,35 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, cudaStream_t stream
 }
 
 }  // namespace
+
+namespace ffpa {
+
+// Kernels whose shared-memory limit was raised, per device (set-once facts).
+ffpa_status set_smem_attr_once(const void* fn, int device, int bytes) {
+  struct Entry {
+    const void* fn;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static Entry table[256];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn && table[i].device == device && table[i].bytes >= bytes) return FFPA_OK;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return FFPA_ERR_CUDA;
+  }
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn && table[i].device == device) {
+      table[i].bytes = bytes;
+      return FFPA_OK;
+    }
+  if (n < 256) table[n++] = Entry{fn, device, bytes};
+  return FFPA_OK;
+}
+
+}  // namespace ffpa
 
 extern "C" {
 
@@ -266,40 +405,44 @@ const char* ffpa_status_string(ffpa_status s) {
   return "FFPA: unknown status";
 }
 
-void ffpa_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 2000000000ull); }
-
-void ffpa_test_drop_first_copy(int enable) { g_drop_first_copy.store(enable ? 1 : 0); }
-
-void ffpa_set_kernel_variant(int variant) {
-  if (variant >= FFPA_VARIANT_AUTO && variant <= FFPA_VARIANT_SPLIT) g_variant.store(variant);
-}
-
-int ffpa_selected_kernel(int D, int varlen) {
+int ffpa_selected_kernel(int D, int varlen, int kernel) {
   if (D < 64 || D > 1024 || D % (varlen ? 64 : 8) != 0) return -1;
-  const Kern kn = choose_kernel(D, varlen != 0);
+  if (kernel < FFPA_VARIANT_AUTO || kernel > FFPA_VARIANT_SPLIT) return -1;
+  const Kern kn = choose_kernel(D, varlen != 0, kernel);
   return kn == Kern::PAIR ? FFPA_VARIANT_PAIR : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT : FFPA_VARIANT_SINGLE;
 }
 
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = -1;
+  if (cudaStreamGetDevice(s, &dev) != cudaSuccess) {
+    cudaGetLastError();
     return FFPA_ERR_CUDA;
-  ffpa_status (*const take[4])(int*) = {ffpa::take_err_single, ffpa::take_err_pair,
-                                        ffpa::take_err_split, ffpa::take_err_bwd};
-  int first = 0;
-  for (auto fn : take) {
-    int word = 0;
-    if (fn(&word) != FFPA_OK) return FFPA_ERR_CUDA;
-    if (first == 0) first = word;
   }
-  return static_cast<ffpa_status>(first);
+  if (dev < 0 || dev >= MAX_DEVICES) return FFPA_ERR_CUDA;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FFPA_ERR_CUDA;
+  const DeviceFacts& f = device_facts(dev);
+  if (f.arch == FFPA_ERR_UNSUPPORTED) return FFPA_OK;   // no kernel of this library runs there
+  if (f.arch != FFPA_OK) return FFPA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, f.fallback, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FFPA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(f.fallback, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FFPA_ERR_CUDA;
+  }
+  return static_cast<ffpa_status>(word);
 }
 
-ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                     ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
-                     const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
-                     const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
-                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
-                     ffpa_stream_t stream) {
+ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                        ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                        const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                        const int64_t mask_str[4], const float* scale, int is_causal,
+                        int enable_gqa, ffpa_stream_t stream, const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 8 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -307,29 +450,40 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
   if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
+  CallOpts opt;
+  if (read_opts(options, &opt) != FFPA_OK) return FFPA_ERR_INVALID;
   const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
   if (B == 0 || Nq == 0) return FFPA_OK;          // nothing to read or write
   if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
   if (Nkv > 0 && (!k || !v)) return FFPA_ERR_INVALID;
-  if (mask_kind != FFPA_MASK_NONE && Nkv > 0) {
+  const bool umask = mask_kind != FFPA_MASK_NONE && Nkv > 0;
+  if (umask) {
     if (!mask || !mask_str) return FFPA_ERR_INVALID;
     for (int i = 0; i < 4; ++i)
       if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+    if (!aligned_to(mask, mask_esz(mask_kind))) return FFPA_ERR_INVALID;
   }
   const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
   if (!strides_ok(q_str, qsz, 4) || !strides_ok(o_str, qsz, 4)) return FFPA_ERR_INVALID;
   if (Nkv > 0 && (!strides_ok(k_str, ksz, 4) || !strides_ok(v_str, ksz, 4))) return FFPA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(o) || (Nkv > 0 && (!aligned16(k) || !aligned16(v))))
     return FFPA_ERR_INVALID;
+  if (lse && !aligned_to(lse, 4)) return FFPA_ERR_INVALID;
   int dev = 0;
-  ffpa_status st = check_device(q, &dev);
+  ffpa_status st = check_devices({q, o, Nkv > 0 ? k : nullptr, Nkv > 0 ? v : nullptr, lse,
+                                  umask ? mask : nullptr},
+                                 &dev);
   if (st != FFPA_OK) return st;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_status_word(dev, opt, &err)) != FFPA_OK) return st;
 
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const Kern kn = choose_kernel(D, false);
+  const Kern kn = choose_kernel(D, false, opt.kernel);
   const bool pair = kn == Kern::PAIR;
   const size_t smem = plan_for(kn, D, &P);
   const uint32_t k_rows = pair ? BN / 2 : BN;
@@ -369,11 +523,11 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   }
   P.o = o;
   P.lse = lse;
-  P.mask = mask_kind != FFPA_MASK_NONE ? mask : nullptr;
-  P.mask_kind = mask_kind;
+  P.mask = umask ? mask : nullptr;
+  P.mask_kind = umask ? mask_kind : FFPA_MASK_NONE;
   for (int i = 0; i < 4; ++i) {
     P.o_str[i] = o_str[i];
-    P.m_str[i] = mask_kind != FFPA_MASK_NONE ? mask_str[i] : 0;
+    P.m_str[i] = umask ? mask_str[i] : 0;
   }
   P.B = B;
   P.Hq = Hq;
@@ -387,22 +541,35 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
-  P.inject = g_drop_first_copy.load();
-  P.timeout_ns = g_timeout_ns.load();
+  P.inject = opt.drop;
+  P.timeout_ns = opt.timeout_ns;
+  P.err = err;
+  P.device = dev;
   const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
   return launch_kernel(kn, false, P, static_cast<int>(items), smem,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                     const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
-                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
-                     const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
-                     const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
-                     const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                     const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                     const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
                      const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream) {
+  return ffpa_fwd_ex(q, k, v, o, lse, dt, B, Hq, Hkv, Nq, Nkv, D, q_str, k_str, v_str, o_str, mask,
+                     mask_kind, mask_str, scale, is_causal, enable_gqa, stream, nullptr);
+}
+
+ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                        const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
+                        const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                        ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
+                        int is_causal, int enable_gqa, ffpa_stream_t stream,
+                        const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -410,13 +577,17 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
   if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
+  CallOpts opt;
+  if (read_opts(options, &opt) != FFPA_OK) return FFPA_ERR_INVALID;
   const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
   if (B == 0 || (Nq == 0 && Nkv == 0)) return FFPA_OK;   // nothing to write
-  if (mask_kind != FFPA_MASK_NONE && Nq > 0 && Nkv > 0) {
+  const bool umask = mask_kind != FFPA_MASK_NONE && Nq > 0 && Nkv > 0;
+  if (umask) {
     if (!mask || !mask_str) return FFPA_ERR_INVALID;
     for (int i = 0; i < 4; ++i)
       if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+    if (!aligned_to(mask, mask_esz(mask_kind))) return FFPA_ERR_INVALID;
   }
   if (!q_str || !k_str || !v_str || !o_str || !do_str || !dq_str || !dk_str || !dv_str)
     return FFPA_ERR_INVALID;
@@ -427,6 +598,7 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
         !strides_ok(dq_str, qsz, 4))
       return FFPA_ERR_INVALID;
     if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq)) return FFPA_ERR_INVALID;
+    if (!aligned_to(lse, 4) || !aligned_to(delta, 4)) return FFPA_ERR_INVALID;
   }
   if (Nkv > 0) {
     if (!k || !v || !dk || !dv) return FFPA_ERR_INVALID;
@@ -436,8 +608,17 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
     if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
   }
   int dev = 0;
-  ffpa_status st = check_device(Nq > 0 ? q : k, &dev);
+  const bool any_q = Nq > 0, any_k = Nkv > 0;
+  ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,
+                                  any_q ? dq : nullptr, any_q ? lse : nullptr, any_q ? delta : nullptr,
+                                  any_k ? k : nullptr, any_k ? v : nullptr, any_k ? dk : nullptr,
+                                  any_k ? dv : nullptr, umask ? mask : nullptr},
+                                 &dev);
   if (st != FFPA_OK) return st;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_status_word(dev, opt, &err)) != FFPA_OK) return st;
 
   BwdParams P{};
   const CUtensorMapDataType tdt =
@@ -448,14 +629,14 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   const uint64_t nch = (uint64_t)P.nchunks;
   const uint32_t box[5] = {64, BM, (uint32_t)P.kchunks, 1, 1};
   // With no query rows (or no keys) no work item copies from those maps.
-  if (Nq > 0) {
+  if (any_q) {
     const uint64_t dq5[5] = {64, (uint64_t)Nq, nch, (uint64_t)Hq, (uint64_t)B};
     const uint64_t sq[4] = {(uint64_t)q_str[2] * 2, 128, (uint64_t)q_str[1] * 2, (uint64_t)q_str[0] * 2};
     const uint64_t sd[4] = {(uint64_t)do_str[2] * 2, 128, (uint64_t)do_str[1] * 2, (uint64_t)do_str[0] * 2};
     if ((st = encode_map(&P.tm_q, tdt, 5, q, dq5, sq, box)) != FFPA_OK) return st;
     if ((st = encode_map(&P.tm_do, tdt, 5, dout, dq5, sd, box)) != FFPA_OK) return st;
   }
-  if (Nkv > 0) {
+  if (any_k) {
     const uint64_t dk5[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
     const uint64_t sk[4] = {(uint64_t)k_str[2] * 2, 128, (uint64_t)k_str[1] * 2, (uint64_t)k_str[0] * 2};
     const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
@@ -465,7 +646,6 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.o = o;
   P.dout = dout;
   P.lse = lse;
-  const bool umask = mask_kind != FFPA_MASK_NONE && Nq > 0 && Nkv > 0;
   P.mask = umask ? mask : nullptr;
   P.mask_kind = umask ? mask_kind : FFPA_MASK_NONE;
   for (int i = 0; i < 4; ++i) P.m_str[i] = umask ? mask_str[i] : 0;
@@ -492,18 +672,34 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
   P.scale = sc;
   P.causal = is_causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
-  return bwd_launch(P, Nq > 0, Nkv > 0, reinterpret_cast<cudaStream_t>(stream));
+  P.err = err;
+  P.device = dev;
+  return bwd_launch(P, any_q, any_k, opt, reinterpret_cast<cudaStream_t>(stream));
 }
 
-ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
-                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                            float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
-                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
-                            const int64_t o_str[3], const int64_t do_str[3], const int64_t dq_str[3],
-                            const int64_t dk_str[3], const int64_t dv_str[3],
-                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
-                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
-                            int enable_gqa, ffpa_stream_t stream) {
+ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
+                     const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
+                     const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
+                     const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                     const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                     ffpa_stream_t stream) {
+  return ffpa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, B, Hq, Hkv, Nq, Nkv, D, q_str,
+                     k_str, v_str, o_str, do_str, dq_str, dk_str, dv_str, mask, mask_kind, mask_str,
+                     scale, is_causal, enable_gqa, stream, nullptr);
+}
+
+ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int64_t do_str[3], const int64_t dq_str[3],
+                               const int64_t dk_str[3], const int64_t dv_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -511,10 +707,14 @@ ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const v
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (nseq < 1 || max_seqlen_q < 0 || max_seqlen_k < 0) return FFPA_ERR_INVALID;
   if (!cu_seqlens_q) return FFPA_ERR_INVALID;
+  CallOpts opt;
+  if (read_opts(options, &opt) != FFPA_OK) return FFPA_ERR_INVALID;
   const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
   if ((Tq == 0 || max_seqlen_q == 0) && (Tk == 0 || max_seqlen_k == 0)) return FFPA_OK;
   if (!q_str || !k_str || !v_str || !o_str || !do_str || !dq_str || !dk_str || !dv_str)
+    return FFPA_ERR_INVALID;
+  if (!aligned_to(cu_seqlens_q, 4) || (cu_seqlens_k && !aligned_to(cu_seqlens_k, 4)))
     return FFPA_ERR_INVALID;
   const int64_t qsz[3] = {Tq, Hq, D}, ksz[3] = {Tk, Hkv, D};
   const bool any_q = Tq > 0 && max_seqlen_q > 0, any_k = Tk > 0 && max_seqlen_k > 0;
@@ -524,6 +724,7 @@ ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const v
         !strides_ok(dq_str, qsz, 3))
       return FFPA_ERR_INVALID;
     if (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq)) return FFPA_ERR_INVALID;
+    if (!aligned_to(lse, 4) || !aligned_to(delta, 4)) return FFPA_ERR_INVALID;
   }
   if (any_k) {
     if (!k || !v || !dk || !dv) return FFPA_ERR_INVALID;
@@ -533,8 +734,16 @@ ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const v
     if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
   }
   int dev = 0;
-  ffpa_status st = check_device(any_q ? q : k, &dev);
+  ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,
+                                  any_q ? dq : nullptr, any_q ? lse : nullptr, any_q ? delta : nullptr,
+                                  any_k ? k : nullptr, any_k ? v : nullptr, any_k ? dk : nullptr,
+                                  any_k ? dv : nullptr, cu_seqlens_q, cu_seqlens_k},
+                                 &dev);
   if (st != FFPA_OK) return st;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_status_word(dev, opt, &err)) != FFPA_OK) return st;
 
   BwdParams P{};
   const CUtensorMapDataType tdt =
@@ -589,16 +798,33 @@ ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const v
   P.scale = sc;
   P.causal = causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
-  return bwd_launch(P, any_q, any_k, reinterpret_cast<cudaStream_t>(stream));
+  P.err = err;
+  P.device = dev;
+  return bwd_launch(P, any_q, any_k, opt, reinterpret_cast<cudaStream_t>(stream));
 }
 
-ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                            ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
-                            const int64_t q_str[3], const int64_t k_str[3],
-                            const int64_t v_str[3], const int64_t o_str[3],
+ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3], const int64_t v_str[3],
+                            const int64_t o_str[3], const int64_t do_str[3], const int64_t dq_str[3],
+                            const int64_t dk_str[3], const int64_t dv_str[3],
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
                             int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                             int enable_gqa, ffpa_stream_t stream) {
+  return ffpa_bwd_varlen_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, Tq, Tk, Hq, Hkv, D, q_str,
+                            k_str, v_str, o_str, do_str, dq_str, dk_str, dv_str, cu_seqlens_q,
+                            cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, scale, causal,
+                            enable_gqa, stream, nullptr);
+}
+
+ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -606,24 +832,35 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
   if (nseq < 1 || max_seqlen_q < 0 || max_seqlen_k < 0) return FFPA_ERR_INVALID;
   if (!cu_seqlens_q) return FFPA_ERR_INVALID;
+  CallOpts opt;
+  if (read_opts(options, &opt) != FFPA_OK) return FFPA_ERR_INVALID;
   const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
   if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
   if (Tq == 0 || max_seqlen_q == 0) return FFPA_OK;   // nothing to read or write
   if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
   if (Tk > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  if (!aligned_to(cu_seqlens_q, 4) || (cu_seqlens_k && !aligned_to(cu_seqlens_k, 4)))
+    return FFPA_ERR_INVALID;
   const int64_t qsz[3] = {Tq, Hq, D}, ksz[3] = {Tk, Hkv, D};
   if (!strides_ok(q_str, qsz, 3) || !strides_ok(o_str, qsz, 3)) return FFPA_ERR_INVALID;
   if (Tk > 0 && (!strides_ok(k_str, ksz, 3) || !strides_ok(v_str, ksz, 3))) return FFPA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(o) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
     return FFPA_ERR_INVALID;
+  if (lse && !aligned_to(lse, 4)) return FFPA_ERR_INVALID;
   int dev = 0;
-  ffpa_status st = check_device(q, &dev);
+  ffpa_status st = check_devices({q, o, Tk > 0 ? k : nullptr, Tk > 0 ? v : nullptr, lse,
+                                  cu_seqlens_q, cu_seqlens_k},
+                                 &dev);
   if (st != FFPA_OK) return st;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_status_word(dev, opt, &err)) != FFPA_OK) return st;
 
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const Kern kn = choose_kernel(D, true);
+  const Kern kn = choose_kernel(D, true, opt.kernel);
   const bool pair = kn == Kern::PAIR;
   const size_t smem = plan_for(kn, D, &P);
   const uint32_t k_rows = pair ? BN / 2 : BN;
@@ -665,13 +902,27 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = causal ? 1 : 0;
   P.fp16 = dt == FFPA_FP16;
-  P.inject = g_drop_first_copy.load();
-  P.timeout_ns = g_timeout_ns.load();
+  P.inject = opt.drop;
+  P.timeout_ns = opt.timeout_ns;
+  P.err = err;
+  P.device = dev;
   (void)max_seqlen_k;
   const long long items = (long long)nseq * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
   return launch_kernel(kn, true, P, static_cast<int>(items), smem,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                            const int64_t q_str[3], const int64_t k_str[3],
+                            const int64_t v_str[3], const int64_t o_str[3],
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                            int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                            int enable_gqa, ffpa_stream_t stream) {
+  return ffpa_fwd_varlen_ex(q, k, v, o, lse, dt, Tq, Tk, Hq, Hkv, D, q_str, k_str, v_str, o_str,
+                            cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, scale,
+                            causal, enable_gqa, stream, nullptr);
 }
 
 }  // extern "C"

@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
   const int NS = TWO ? p.nslot_two : p.nslot;
   const int T = it.n_iter;
   const unsigned long long tmo = p.timeout_ns;
+  int* const err = p.err;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       // row: within the item's problem; qside: a query-side tensor (Q, dO).
       auto load = [&](const CUtensorMap* m, int row, int chunk, int head, bool qside) -> bool {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
-        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo)) return false;
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, err)) return false;
         const uint32_t fb = smem_u32(&bar_full[slot]);
         if (drop) {
           drop = false;
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = NS - 1; lp ^= 1u; }
         if (p.inject != 0 && issued - 1 - i == 0) continue;   // the dropped stage was never armed
-        wait_drain(smem_u32(&bar_full[s]), lp, tmo);
+        wait_drain(smem_u32(&bar_full[s]), lp, tmo, err);
       }
     }
   } else if (warp == BWD_MMA_WARP) {
@@ -412,14 +413,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       uint32_t lap = 0;
       auto take = [&]() -> int {
         const uint32_t fb = smem_u32(&bar_full[slot]);
-        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo, err)) return -1;
         const int s = slot;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return s;
       };
       auto release = [&](int s) { umma_commit(smem_u32(&bar_empty[s])); };
       auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
-        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo, err)) return false;
         tc_fence_after();
         return true;
       };
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       }
       const uint32_t db = smem_u32(&bar_drain);
       umma_commit(db);
-      wait_drain(db, 0, tmo);
+      wait_drain(db, 0, tmo, err);
     }
   } else {
     // ------------------------------------------------------------ elementwise
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
         }
         __syncwarp();
       }
-      bool w = wait_bounded(smem_u32(&bar_sd_full), i & 1, &abort_flag, tmo);
+      bool w = wait_bounded(smem_u32(&bar_sd_full), i & 1, &abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
@@ -622,7 +623,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
       if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
       // The tile is free once the slice MMAs of iteration i-1 are done.
       if (i >= 1) {
-        w = wait_bounded(smem_u32(&bar_pd_done), (i - 1) & 1, &abort_flag, tmo);
+        w = wait_bounded(smem_u32(&bar_pd_done), (i - 1) & 1, &abort_flag, tmo, err);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
     }
     // ------------------------------------------------------------ epilogue
     if (ok && T > 0) {
-      const bool w = wait_bounded(smem_u32(&bar_pd_done), (T - 1) & 1, &abort_flag, tmo);
+      const bool w = wait_bounded(smem_u32(&bar_pd_done), (T - 1) & 1, &abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (ok) tc_fence_after();
     }
@@ -680,9 +681,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) ffpa_bwd_kernel(const __grid_c
 template <int ROLE>
 static ffpa_status launch_role(const BwdParams& P, int items, size_t smem, cudaStream_t stream) {
   auto kern = P.mask != nullptr ? ffpa_bwd_kernel<ROLE, true> : ffpa_bwd_kernel<ROLE, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
-    return FFPA_ERR_CUDA;
+  const ffpa_status st =
+      set_smem_attr_once(reinterpret_cast<const void*>(kern), P.device, static_cast<int>(smem));
+  if (st != FFPA_OK) return st;
   kern<<<items, BWD_THREADS, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
@@ -706,14 +707,5 @@ ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t sm
   return FFPA_OK;
 }
 
-ffpa_status take_err_bwd(int* word) {
-  *word = 0;
-  if (cudaMemcpyFromSymbol(word, g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  if (*word != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  }
-  return FFPA_OK;
-}
 
 }  // namespace ffpa

@@ -73,22 +73,15 @@ constexpr int Q_TMEM_MAX_CHUNKS = 4;
 constexpr uint32_t P_TILE_BYTES = BM * BN * 2;   // 2 x (128 rows x 64 keys), 16-bit
 constexpr size_t SPLIT_STATIC_RESERVE = 2048;
 
-// Device status word of this translation unit (each kernel file has its
-// own; the host reads and clears them all in ffpa_last_device_error).
-static __device__ int g_err_word;
-
 // ------------------------------------------------------------------ host
-// Launches of the three kernels (one translation unit each) and their
-// device status words.
+// Launches of the three kernels (one translation unit each).
 struct Params;
 ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
-// Reads the unit's status word into *word and clears it (FFPA_ERR_CUDA if
-// the copy fails).
-ffpa_status take_err_single(int* word);
-ffpa_status take_err_pair(int* word);
-ffpa_status take_err_split(int* word);
+// Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on `device`,
+// once per (kernel, device) pair; later calls only look the pair up.
+ffpa_status set_smem_attr_once(const void* fn, int device, int bytes);
 
 // Backward (ffpa_bwd.cu): a delta pass, then one kernel for dQ (rows =
 // queries) and one each for dV and dK (rows = keys; one for both when
@@ -96,7 +89,6 @@ ffpa_status take_err_split(int* word);
 struct BwdParams;
 ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t smem, size_t smem_two,
                        cudaStream_t stream);
-ffpa_status take_err_bwd(int* word);
 constexpr int BWD_THREADS = 192;           // warps 0-3 elementwise, 4 TMA, 5 MMA
 constexpr int BWD_NSLOT_MAX = 6;
 constexpr size_t BWD_STATIC_RESERVE = 6144;
@@ -134,6 +126,8 @@ struct BwdParams {
   float scale, scale_log2;
   int causal, fp16, inject;
   unsigned long long timeout_ns;
+  int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
+  int device;   // host only: the device the launch goes to
 };
 
 struct Params {
@@ -165,6 +159,8 @@ struct Params {
   // arrive as zeros (single-CTA kernel only).
   int dfine;
   unsigned long long timeout_ns;
+  int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
+  int device;   // host only: the device the launch goes to
 };
 
 struct Item {
@@ -234,11 +230,12 @@ __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L,
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when this CTA has been
-// told to abort or when the limit expires (then the error word is set).
-// `cluster` selects cluster-scope acquire, for phases that another CTA of
-// the cluster completes.
+// told to abort or when the limit expires (then the call's status word *err
+// is set).  `cluster` selects cluster-scope acquire, for phases that another
+// CTA of the cluster completes.
 static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long timeout_ns, bool cluster = false) {
+                                          unsigned long long timeout_ns, int* err,
+                                          bool cluster = false) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     // Suspended waiting keeps idle warps from taking issue slots away from
@@ -250,7 +247,7 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > timeout_ns) {
         *abort_flag = 1;
-        atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+        atomicExch(err, (int)FFPA_ERR_DEVICE_TIMEOUT);
         return false;
       }
     }
@@ -258,11 +255,12 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
 }
 
 // Drain wait used on the way out: ignores the abort flag.
-static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                               int* err) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) {
-      atomicExch(&g_err_word, (int)FFPA_ERR_DEVICE_TIMEOUT);
+      atomicExch(err, (int)FFPA_ERR_DEVICE_TIMEOUT);
       return;
     }
   }
@@ -469,7 +467,8 @@ __device__ __forceinline__ void arrive_to(uint32_t addr) {
 template <bool VARLEN, bool PAIR, bool UMASK>
 __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, int T, uint32_t tmem,
                                              int warp, int lane, const SoftmaxBars bars,
-                                             volatile int* abort_flag, unsigned long long tmo) {
+                                             volatile int* abort_flag, unsigned long long tmo,
+                                             int* err) {
   const int mask_kind = p.mask_kind;
   const bool fp16 = p.fp16 != 0, causal = p.causal != 0;
   const float scale_log2 = p.scale_log2;
@@ -500,7 +499,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
   bool ok = true;
   for (int j = 0; j < T; ++j) {
     const int b = j & 1;
-    bool w = wait_bounded(bars.s_full, j & 1, abort_flag, tmo);
+    bool w = wait_bounded(bars.s_full, j & 1, abort_flag, tmo, err);
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after();
@@ -560,7 +559,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
     }
     if (__any_sync(0xffffffffu, resc)) {
       // O holds PV up to tile j-1: wait for it, then scale this warp's rows.
-      w = wait_bounded(bars.pv_done + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, tmo);
+      w = wait_bounded(bars.pv_done + 8u * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
@@ -575,7 +574,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
       }
     }
     if (j >= 2) {   // P buffer b was read by PV_{j-2}
-      w = wait_bounded(bars.pv_done + 8u * b, ((j - 2) >> 1) & 1, abort_flag, tmo);
+      w = wait_bounded(bars.pv_done + 8u * b, ((j - 2) >> 1) & 1, abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
@@ -599,7 +598,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, const Item& it, in
   // ------------------------------------------------------------ epilogue
   if (ok && T > 0) {
     const bool w = wait_bounded(bars.pv_done + 8u * ((T - 1) & 1), ((T - 1) >> 1) & 1,
-                                abort_flag, tmo);
+                                abort_flag, tmo, err);
     ok = __all_sync(0xffffffffu, w);
     if (ok) tc_fence_after();
   }

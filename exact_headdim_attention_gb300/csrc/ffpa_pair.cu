@@ -130,6 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = tmem_base_sh;
   const int T = it.ntiles;
   const unsigned long long tmo = p.timeout_ns;
+  int* const err = p.err;
 
   if (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) {
     // ------------------------------------------------------------ producers
@@ -153,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       bool drop = k_role && leader && inject != 0;   // test hook (see ffpa_test_drop_first_copy)
       auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
         const uint32_t eb = smem_u32(&empty[slot]);
-        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, err))
           return ~0u;
         fb = smem_u32(&full[slot]);
         const uint32_t dst = base + slot * stride;
@@ -190,7 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
             }
           }
         }
-        wait_drain(qb, 0, tmo);
+        wait_drain(qb, 0, tmo, err);
       } else {
         const int mycol = (it.col_lo + (it.dv / 2) * (int)rank) / DK;
         for (int j = 0; j < T && ok; ++j) {
@@ -212,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = nslots - 1; lp ^= 1u; }
         if (k_role && leader && inject != 0 && issued - 1 - i == 0) continue;
-        wait_drain(smem_u32(&full[s]), lp, tmo);
+        wait_drain(smem_u32(&full[s]), lp, tmo, err);
       }
     }
   } else if ((warp == MMA_WARP || warp == PV_WARP) && !leader) {
@@ -225,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       const int per_tile = k_role ? nkst : BN / vk;
       if (k_role) {
         const uint32_t qb = smem_u32(&bar_q);
-        if (!(mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo))) goto relay_done;
+        if (!(mbar_try_wait(qb, 0) || wait_bounded(qb, 0, &abort_flag, tmo, err))) goto relay_done;
         mbar_arrive_cluster(mapa_shared(qb, 0));
       }
       {
@@ -233,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
         uint32_t lap = 0;
         for (int i = 0; i < T * per_tile; ++i) {
           const uint32_t fb = smem_u32(&full[slot]);
-          if (!(mbar_try_wait(fb, lap) || wait_bounded(fb, lap, &abort_flag, tmo))) break;
+          if (!(mbar_try_wait(fb, lap) || wait_bounded(fb, lap, &abort_flag, tmo, err))) break;
           mbar_arrive_cluster(mapa_shared(fb, 0));
           if (++slot == nslots) { slot = 0; lap ^= 1u; }
         }
@@ -251,13 +252,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       auto take = [&]() -> int {
         const uint32_t fb = smem_u32(&full[slot]);
-        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo, err)) return -1;
         const int s = slot;
         if (++slot == nslots) { slot = 0; lap ^= 1u; }
         return s;
       };
       auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
-        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo, err)) return false;
         tc_fence_after();
         return true;
       };
@@ -311,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
       }
       const uint32_t db = smem_u32(&bar_drain[qk_role ? 0 : 1]);
       umma_commit_pair(db);
-      wait_drain(db, 0, tmo);
+      wait_drain(db, 0, tmo, err);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ softmax
@@ -320,14 +321,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
     bars.s_free_arrive = mapa_shared(smem_u32(&bar_s_free), 0);
     bars.p_full_arrive = mapa_shared(smem_u32(&bar_p_full[0]), 0);
     bars.pv_done = smem_u32(&bar_pv_done[0]);
-    softmax_role<VARLEN, true, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
+    softmax_role<VARLEN, true, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo, err);
   }
 
   // The leader's last commits also arrive in the peer: wait for them before
   // the pair may exit, then free TMEM in both CTAs together.
   if (!leader && threadIdx.x == 0) {
-    wait_drain(smem_u32(&bar_drain[0]), 0, tmo);
-    wait_drain(smem_u32(&bar_drain[1]), 0, tmo);
+    wait_drain(smem_u32(&bar_drain[0]), 0, tmo, err);
+    wait_drain(smem_u32(&bar_drain[1]), 0, tmo, err);
   }
   tc_fence_before();
   __syncthreads();
@@ -344,9 +345,9 @@ static ffpa_status launch_pair_t(const Params& P, int items, size_t smem, cudaSt
   auto kern = P.nchunks == 8   ? ffpa_fwd_pair_kernel<VARLEN, 8, UMASK>
               : P.nchunks == 4 ? ffpa_fwd_pair_kernel<VARLEN, 4, UMASK>
                                : ffpa_fwd_pair_kernel<VARLEN, 2, UMASK>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
-    return FFPA_ERR_CUDA;
+  const ffpa_status st =
+      set_smem_attr_once(reinterpret_cast<const void*>(kern), P.device, static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE));
+  if (st != FFPA_OK) return st;
   kern<<<2 * items, NTHREADS, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
@@ -358,14 +359,5 @@ ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, siz
                  : launch_pair_t<false, false>(P, items, smem, stream);
 }
 
-ffpa_status take_err_pair(int* word) {
-  *word = 0;
-  if (cudaMemcpyFromSymbol(word, g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  if (*word != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  }
-  return FFPA_OK;
-}
 
 }  // namespace ffpa

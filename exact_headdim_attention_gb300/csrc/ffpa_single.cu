@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
   const uint32_t tmem = tmem_base_sh;
   const int T = it.ntiles;
   const unsigned long long tmo = p.timeout_ns;
+  int* const err = p.err;
 
   if (warp == PRODUCER_WARP || warp == V_PRODUCER_WARP) {
     // ------------------------------------------------------------ producers
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       // Returns the smem address of an armed slot, 0 when dropped, ~0u on abort.
       auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
         const uint32_t eb = smem_u32(&empty[slot]);
-        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, err))
           return ~0u;
         fb = smem_u32(&full[slot]);
         const uint32_t dst = base + slot * stride;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
             }
           }
         }
-        if (q_res) wait_drain(smem_u32(&bar_q), 0, tmo);
+        if (q_res) wait_drain(smem_u32(&bar_q), 0, tmo, err);
       } else {
         for (int j = 0; j < T && ok; ++j) {
           for (int h = 0; h < BN / vk && ok; ++h) {
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = nslots - 1; lp ^= 1u; }
         if (k_role && inject != 0 && issued - 1 - i == 0) continue;
-        wait_drain(smem_u32(&full[s]), lp, tmo);
+        wait_drain(smem_u32(&full[s]), lp, tmo, err);
       }
     }
   } else if (warp == MMA_WARP || warp == PV_WARP) {
@@ -201,14 +202,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       bool ok = true;
       auto take = [&]() -> int {
         const uint32_t fb = smem_u32(&full[slot]);
-        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo, err)) return -1;
         const int s = slot;
         if (++slot == nslots) { slot = 0; lap ^= 1u; }
         return s;
       };
       auto release = [&](int s) { umma_commit(smem_u32(&empty[s])); };
       auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
-        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo, err)) return false;
         tc_fence_after();
         return true;
       };
@@ -281,7 +282,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
       // Drain: all MMAs issued by this thread complete before TMEM is freed.
       const uint32_t db = smem_u32(&bar_drain[qk_role ? 0 : 1]);
       umma_commit(db);
-      wait_drain(db, 0, tmo);
+      wait_drain(db, 0, tmo, err);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) ffpa_fwd_kernel(const __grid_cons
     bars.s_free_arrive = smem_u32(&bar_s_free);
     bars.p_full_arrive = smem_u32(&bar_p_full[0]);
     bars.pv_done = smem_u32(&bar_pv_done[0]);
-    softmax_role<VARLEN, false, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo);
+    softmax_role<VARLEN, false, UMASK>(p, it, T, tmem, warp, lane, bars, &abort_flag, tmo, err);
   }
 
   tc_fence_before();
@@ -307,21 +308,12 @@ ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, s
   auto kern = varlen  ? ffpa_fwd_kernel<true, false>
               : umask ? ffpa_fwd_kernel<false, true>
                       : ffpa_fwd_kernel<false, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE)) != cudaSuccess)
-    return FFPA_ERR_CUDA;
+  const ffpa_status st =
+      set_smem_attr_once(reinterpret_cast<const void*>(kern), P.device, static_cast<int>(SMEM_LIMIT - SMEM_STATIC_RESERVE));
+  if (st != FFPA_OK) return st;
   kern<<<items, NTHREADS, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
-ffpa_status take_err_single(int* word) {
-  *word = 0;
-  if (cudaMemcpyFromSymbol(word, g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  if (*word != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  }
-  return FFPA_OK;
-}
 
 }  // namespace ffpa

@@ -101,6 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
   const int R = (T + 1) >> 1;                  // rounds of two key tiles
   const int own0 = (int)rank, peer0 = (int)peer;   // tile of round i: 2 i + own0 / 2 i + peer0
   const unsigned long long tmo = p.timeout_ns;
+  int* const err = p.err;
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
@@ -118,7 +119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       bool drop = inject != 0 && rank == 0;   // test hook (see ffpa_test_drop_first_copy)
       auto acquire = [&](uint32_t bytes, uint32_t& fb) -> uint32_t {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
-        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo))
+        if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, err))
           return ~0u;
         fb = smem_u32(&bar_full[slot]);
         const uint32_t dst = ring_u32 + slot * SLOT_BYTES;
@@ -174,14 +175,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         if (2 * i + own0 < T && !(ok = load_v(2 * i + own0))) break;
         if (2 * i + peer0 < T && !(ok = load_v(2 * i + peer0))) break;
       }
-      wait_drain(qb, 0, tmo);
+      wait_drain(qb, 0, tmo, err);
       const int n = issued < NS ? issued : NS;
       int s = slot;
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = NS - 1; lp ^= 1u; }
         if (inject != 0 && rank == 0 && issued - 1 - i == 0) continue;   // never armed
-        wait_drain(smem_u32(&bar_full[s]), lp, tmo);
+        wait_drain(smem_u32(&bar_full[s]), lp, tmo, err);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -194,13 +195,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       bool ok = true;
       auto take = [&]() -> int {
         const uint32_t fb = smem_u32(&bar_full[slot]);
-        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo)) return -1;
+        if (!mbar_try_wait(fb, lap) && !wait_bounded(fb, lap, &abort_flag, tmo, err)) return -1;
         const int s = slot;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return s;
       };
       auto wait_on = [&](uint32_t bar, uint32_t par) -> bool {
-        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo)) return false;
+        if (!mbar_try_wait(bar, par) && !wait_bounded(bar, par, &abort_flag, tmo, err)) return false;
         tc_fence_after();
         return true;
       };
@@ -288,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       }
       const uint32_t db = smem_u32(&bar_drain);
       umma_commit(db);
-      wait_drain(db, 0, tmo);
+      wait_drain(db, 0, tmo, err);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ softmax
@@ -317,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     if (T > 0) {
       // Q chunks 0..qt-1: staging area -> TMEM (row r = lane r; the 32-bit
       // words of a row in memory order are the packed A-operand columns).
-      bool w = wait_bounded(smem_u32(&bar_q), 0, &abort_flag, tmo);
+      bool w = wait_bounded(smem_u32(&bar_q), 0, &abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (ok) {
         const uint32_t sw = (uint32_t)(r & 7);
@@ -341,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         if (r == 0) {
           // All four warps have read the staging area: the peer may copy its
           // first P tile into this CTA's P (peer) area.
-          w = wait_bounded(smem_u32(&bar_qt), 0, &abort_flag, tmo);
+          w = wait_bounded(smem_u32(&bar_qt), 0, &abort_flag, tmo, err);
           if (w) mbar_arrive_cluster(mapa_shared(smem_u32(&bar_peer_free), peer));
         }
         ok = __all_sync(0xffffffffu, w);
@@ -357,7 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       float x[BN];
       float t = -INFINITY;
       if (own) {
-        bool w = wait_bounded(smem_u32(&bar_s_full), k_own & 1, &abort_flag, tmo);
+        bool w = wait_bounded(smem_u32(&bar_s_full), k_own & 1, &abort_flag, tmo, err);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
@@ -408,7 +409,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       if (r == 0) mbar_arrive_expect_tx(xbar, BM * 4);
       st_async_b32(x_remote + xb * BM * 4, __float_as_uint(t), xbar_remote + 8u * xb);
       {
-        const bool w = wait_bounded(xbar, (i >> 1) & 1, &abort_flag, tmo, true);
+        const bool w = wait_bounded(xbar, (i >> 1) & 1, &abort_flag, tmo, err, true);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
       }
@@ -438,8 +439,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         // peer's P area for this one).
         bool w = true;
         if (k_own >= 1)
-          w = wait_bounded(smem_u32(&bar_pown_free), (k_own - 1) & 1, &abort_flag, tmo);
-        if (w) w = wait_bounded(smem_u32(&bar_peer_free), k_own & 1, &abort_flag, tmo, true);
+          w = wait_bounded(smem_u32(&bar_pown_free), (k_own - 1) & 1, &abort_flag, tmo, err);
+        if (w) w = wait_bounded(smem_u32(&bar_peer_free), k_own & 1, &abort_flag, tmo, err, true);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         // Row r of the P tile: 16 units of 8 keys, 128-byte swizzle.
@@ -455,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         // PV of round i-1 done.  Waited every round (not only before a
         // rescale) so that each phase of this barrier is observed: a parity
         // wait cannot tell phase n from phase n-2.
-        const bool w = wait_bounded(smem_u32(&bar_pv_done), (i - 1) & 1, &abort_flag, tmo);
+        const bool w = wait_bounded(smem_u32(&bar_pv_done), (i - 1) & 1, &abort_flag, tmo, err);
         ok = __all_sync(0xffffffffu, w);
         if (!ok) break;
         tc_fence_after();
@@ -493,7 +494,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     }
     // ------------------------------------------------------------ epilogue
     if (ok && R > 0) {
-      bool w = wait_bounded(smem_u32(&bar_pv_done), (R - 1) & 1, &abort_flag, tmo);
+      bool w = wait_bounded(smem_u32(&bar_pv_done), (R - 1) & 1, &abort_flag, tmo, err);
       ok = __all_sync(0xffffffffu, w);
       if (ok) {
         tc_fence_after();
@@ -502,7 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         if (r == 0) mbar_arrive_expect_tx(lbar, BM * 4);
         st_async_b32(mapa_shared(smem_u32(&lbuf[r]), peer), __float_as_uint(l_sum),
                      mapa_shared(lbar, peer));
-        w = wait_bounded(lbar, 0, &abort_flag, tmo, true);
+        w = wait_bounded(lbar, 0, &abort_flag, tmo, err, true);
         ok = __all_sync(0xffffffffu, w);
         if (ok) l_sum += ld_shared_f32(smem_u32(&lbuf[r]));
       }
@@ -511,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     if (r == 0 && ok && T > 0) {
       // Before this CTA may exit: the peer has read every P tile copied to it.
       const int n_own = (T - own0 + 1) >> 1;
-      wait_drain(smem_u32(&bar_peer_free), n_own & 1, tmo);
+      wait_drain(smem_u32(&bar_peer_free), n_own & 1, tmo, err);
     }
   }
 
@@ -531,9 +532,9 @@ static ffpa_status launch_split_t(const Params& P, int items, size_t smem, cudaS
               : P.nchunks == 6 ? ffpa_fwd_split_kernel<VARLEN, 6, UMASK>
               : P.nchunks == 4 ? ffpa_fwd_split_kernel<VARLEN, 4, UMASK>
                                : ffpa_fwd_split_kernel<VARLEN, 2, UMASK>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_LIMIT - SPLIT_STATIC_RESERVE)) != cudaSuccess)
-    return FFPA_ERR_CUDA;
+  const ffpa_status st =
+      set_smem_attr_once(reinterpret_cast<const void*>(kern), P.device, static_cast<int>(SMEM_LIMIT - SPLIT_STATIC_RESERVE));
+  if (st != FFPA_OK) return st;
   kern<<<2 * items, SPLIT_THREADS, smem, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
@@ -545,14 +546,5 @@ ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, si
                  : launch_split_t<false, false>(P, items, smem, stream);
 }
 
-ffpa_status take_err_split(int* word) {
-  *word = 0;
-  if (cudaMemcpyFromSymbol(word, g_err_word, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  if (*word != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(int)) != cudaSuccess) return FFPA_ERR_CUDA;
-  }
-  return FFPA_OK;
-}
 
 }  // namespace ffpa

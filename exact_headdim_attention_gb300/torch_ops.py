@@ -44,13 +44,22 @@ def _attn_fwd_setup_context(ctx, inputs, output):
     o, lse = output
     ctx.save_for_backward(q, k, v, o, lse, attn_mask)
     ctx.is_causal, ctx.scale, ctx.enable_gqa = is_causal, scale, enable_gqa
+    # An output the loss does not use arrives in backward as None (not as a
+    # tensor of zeros), so the LSE check below needs no device read.
+    ctx.set_materialize_grads(False)
+
+
+def _check_grads(grad_o, grad_lse):
+    if grad_lse is not None:
+        raise NotImplementedError("gradients through the returned LSE are not supported")
+    if grad_o is None:
+        raise NotImplementedError("backward without a gradient for O")
 
 
 def _attn_fwd_backward(ctx, grad_o, grad_lse):
     if ctx.needs_input_grad[3]:
         raise NotImplementedError("no gradient is formed for attn_mask")
-    if grad_lse is not None and bool(torch.count_nonzero(grad_lse)):
-        raise NotImplementedError("gradients through the returned LSE are not supported")
+    _check_grads(grad_o, grad_lse)
     q, k, v, o, lse, attn_mask = ctx.saved_tensors
     dq, dk, dv = _binding.ffpa_bwd(grad_o.contiguous(), q, k, v, o, lse, is_causal=ctx.is_causal,
                                    scale=ctx.scale, enable_gqa=ctx.enable_gqa, attn_mask=attn_mask)
@@ -86,11 +95,11 @@ def _attn_varlen_setup_context(ctx, inputs, output):
     ctx.save_for_backward(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k)
     ctx.max_q, ctx.max_k = max_seqlen_q, max_seqlen_k
     ctx.causal, ctx.scale, ctx.enable_gqa = causal, softmax_scale, enable_gqa
+    ctx.set_materialize_grads(False)
 
 
 def _attn_varlen_backward(ctx, grad_o, grad_lse):
-    if grad_lse is not None and bool(torch.count_nonzero(grad_lse)):
-        raise NotImplementedError("gradients through the returned LSE are not supported")
+    _check_grads(grad_o, grad_lse)
     q, k, v, o, lse, cu_q, cu_k = ctx.saved_tensors
     dq, dk, dv = _binding.ffpa_bwd_varlen(grad_o.contiguous(), q, k, v, o, lse, cu_q, cu_k,
                                           ctx.max_q, ctx.max_k, softmax_scale=ctx.scale,

@@ -17,9 +17,10 @@
  * A row with no visible key gets O = 0 and LSE = -inf.
  *
  * Conventions shared by every entry point:
- *  - Pointers named q, k, v, o, lse, mask, cu_seqlens_* are DEVICE pointers
- *    (memory the caller allocated on the current CUDA device).  `scale` is a
- *    HOST pointer.  The library never allocates, frees or synchronises on the
+ *  - Pointers named q, k, v, o, lse, mask, cu_seqlens_* are DEVICE pointers:
+ *    device (or managed) memory of one sm_103 GPU, all of them on the same
+ *    GPU (else FFPA_ERR_INVALID; another arch is FFPA_ERR_UNSUPPORTED).
+ *    `scale` is a HOST pointer.  The library never allocates, frees or synchronises on the
  *    caller's behalf (ffpa_last_device_error excepted); work is enqueued on
  *    `stream` and runs asynchronously.  The caller owns every buffer and
  *    must keep it alive until the stream has passed this work.
@@ -28,11 +29,30 @@
  *    bytes and the base pointer 16-byte aligned (tensor-memory-accelerator
  *    loads); o must satisfy the same rules (16-byte vector stores).
  *  - Inputs are bf16 or fp16 (all three the same type); O has the input type.
+ *    lse is 4-byte aligned; a mask is aligned to its element size.
  *  - Return codes: FFPA_OK, or the first failed check; nothing is enqueued
  *    when the result is not FFPA_OK.
  *
- * Thread safety: the entry points keep no per-call state; they may be called
- * concurrently from several host threads on different streams.
+ * Per-call options: every entry point has an `_ex` form taking a
+ * `const ffpa_options*` last (NULL = defaults; the plain form passes NULL).
+ * The options carry the call's device status word, its wait time limit,
+ * the kernel choice and a test hook; nothing the caller sets outlives the
+ * call.
+ *
+ * Thread safety and shared state.  The entry points may be called
+ * concurrently from several host threads on any streams.  What the library
+ * shares between calls is exactly:
+ *  - facts looked up once per device and never changed afterwards (compute
+ *    capability, the address of the device's fallback status word) and the
+ *    shared-memory limit raised once per kernel and device;
+ *  - one FALLBACK STATUS WORD per device, written by the kernels of every
+ *    call made without an options status word (ffpa_options.status = NULL)
+ *    when one of their waits runs out.  ffpa_last_device_error(stream) reads
+ *    and clears that word, so a timeout of such a call on one stream is
+ *    reported to whichever caller next checks any stream of that device.
+ *    Callers that need the failure of one call attributed to that call pass
+ *    their own status word in the options.
+ * A call leaves the calling thread's current CUDA device as it found it.
  */
 #ifndef FFPA_H_
 #define FFPA_H_
@@ -62,6 +82,48 @@ typedef enum {
   FFPA_MASK_ADD_F32 = 2,   /* float32 additive bias (may hold -inf) */
   FFPA_MASK_ADD_QTYPE = 3  /* additive bias in the input dtype (bf16/fp16) */
 } ffpa_mask_kind;
+
+/* Kernel choice (ffpa_options.kernel).  The library has three forward
+ * kernels with identical results:
+ *   - single-CTA: one CTA per 128-row query tile and output slice of at most
+ *     256 columns (any D; S is recomputed once per slice);
+ *   - CTA pair: two SMs share each 256-query tile and each load half of every
+ *     K/V tile (D in {128, 256, 512});
+ *   - column split: two SMs share each 128-query tile, each owns half of the
+ *     output columns, key tiles alternate between them and the P tiles are
+ *     exchanged, so S is computed once (D in {128, 256, 384, 512}).
+ *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default)
+ *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
+ *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
+ *   FFPA_VARIANT_SPLIT  (3) the column-split kernel wherever D allows it
+ * Where the chosen kernel does not support D, the single-CTA kernel runs.
+ * The backward has one kernel set and ignores the choice. */
+enum {
+  FFPA_VARIANT_AUTO = 0,
+  FFPA_VARIANT_SINGLE = 1,
+  FFPA_VARIANT_PAIR = 2,
+  FFPA_VARIANT_SPLIT = 3
+};
+
+/* Options of one call (all fields zero = the defaults). */
+typedef struct ffpa_options {
+  /* Device int (4-byte aligned, on the call's GPU) or NULL.  When a wait
+   * inside this call's kernels runs past its limit, the kernel stores
+   * FFPA_ERR_DEVICE_TIMEOUT there (drains its own copies, frees its tensor
+   * memory and returns).  The library never clears it: the caller zeroes
+   * it before the call and reads it after the stream has passed the call.
+   * NULL selects the device's shared fallback word (ffpa_last_device_error). */
+  int* status;
+  /* Time limit of every in-kernel wait, in nanoseconds; 0 = 2e9 (2 s). */
+  uint64_t wait_timeout_ns;
+  /* FFPA_VARIANT_* (forward only); any other value is FFPA_ERR_INVALID. */
+  int kernel;
+  /* TEST HOOK, not for production use: nonzero makes this call's kernels
+   * skip the first tensor copy of each CTA, so that the pipeline wait that
+   * depends on it runs out and reports FFPA_ERR_DEVICE_TIMEOUT (no fault,
+   * no hang). */
+  int test_drop_first_copy;
+} ffpa_options;
 
 /*
  * Dense attention forward (FFPA API reference, "ffpa_attn.ffpa_attn_func").
@@ -93,6 +155,12 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
                      const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
                      const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream);
+ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                        ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                        const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                        const int64_t mask_str[4], const float* scale, int is_causal,
+                        int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
 
 /*
  * Packed variable-length attention forward (FFPA API reference,
@@ -120,6 +188,13 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
                             int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                             int enable_gqa, ffpa_stream_t stream);
+ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                               ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
 
 /*
  * Backward of ffpa_fwd (dense layout): the gradients dq, dk, dv
@@ -158,6 +233,15 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
                      const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
                      const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
                      ffpa_stream_t stream);
+ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                        const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
+                        const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                        ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
+                        int is_causal, int enable_gqa, ffpa_stream_t stream,
+                        const ffpa_options* options);
 
 /*
  * Backward of ffpa_fwd_varlen (packed THD layout; FFPA API reference,
@@ -184,65 +268,37 @@ ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const v
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
                             int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                             int enable_gqa, ffpa_stream_t stream);
+ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int64_t do_str[3], const int64_t dq_str[3],
+                               const int64_t dk_str[3], const int64_t dv_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* ffpa_status_string(ffpa_status status);
 
 /*
- * Checked mode: synchronises `stream`, then reads and clears the device error
- * word that the kernels set when a pipeline wait runs past its time limit
- * (every wait on the GPU is bounded; on expiry the kernel records
- * FFPA_ERR_DEVICE_TIMEOUT, drains its own copies, frees its tensor memory and
- * returns).  Returns FFPA_OK, FFPA_ERR_DEVICE_TIMEOUT, or FFPA_ERR_CUDA if
- * the synchronisation itself failed.
+ * Checked mode for calls made without an options status word: synchronises
+ * `stream`, then reads and clears the FALLBACK status word of the stream's
+ * device (see "Thread safety and shared state" above: the word is shared
+ * by every such call on that device, on every stream).  Returns FFPA_OK,
+ * FFPA_ERR_DEVICE_TIMEOUT, or FFPA_ERR_CUDA if the synchronisation or the
+ * read failed.
  */
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream);
 
 /*
- * Time limit of every in-kernel wait, in nanoseconds (default 2e9 = 2 s;
- * 0 restores the default).  Applies to launches made after the call.
+ * The forward kernel (FFPA_VARIANT_SINGLE, _PAIR or _SPLIT) that a call
+ * with ffpa_options.kernel = `kernel` would run for head dimension D on a
+ * dense (varlen = 0) or packed varlen (varlen != 0) batch.  Host only;
+ * returns -1 for a head dimension or kernel value the library does not take.
  */
-void ffpa_set_wait_timeout_ns(uint64_t ns);
-
-/*
- * Kernel choice for launches made after the call.  The library has three
- * kernels with identical results:
- *   - single-CTA: one CTA per 128-row query tile and output slice of at most
- *     256 columns (any D; S is recomputed once per slice);
- *   - CTA pair: two SMs share each 256-query tile and each load half of every
- *     K/V tile (D in {128, 256, 512});
- *   - column split: two SMs share each 128-query tile, each owns half of the
- *     output columns, key tiles alternate between them and the P tiles are
- *     exchanged, so S is computed once (D in {128, 256, 384, 512}).
- *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default)
- *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
- *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
- *   FFPA_VARIANT_SPLIT  (3) the column-split kernel wherever D allows it
- * Where the chosen kernel does not support D, the single-CTA kernel runs.
- * Any other value is ignored.
- */
-enum {
-  FFPA_VARIANT_AUTO = 0,
-  FFPA_VARIANT_SINGLE = 1,
-  FFPA_VARIANT_PAIR = 2,
-  FFPA_VARIANT_SPLIT = 3
-};
-void ffpa_set_kernel_variant(int variant);
-
-/*
- * The kernel (FFPA_VARIANT_SINGLE, _PAIR or _SPLIT) that a launch made now
- * would run for head dimension D on a dense (varlen = 0) or packed varlen
- * (varlen != 0) batch, under the current kernel choice.  Host only; returns
- * -1 for a head dimension the library does not support.
- */
-int ffpa_selected_kernel(int D, int varlen);
-
-/*
- * TEST HOOK, not for production use: when nonzero, the next launches skip
- * the first tensor copy of each CTA, so that the pipeline wait depending on
- * it runs out and reports FFPA_ERR_DEVICE_TIMEOUT (no fault, no hang).
- */
-void ffpa_test_drop_first_copy(int enable);
+int ffpa_selected_kernel(int D, int varlen, int kernel);
 
 #ifdef __cplusplus
 }

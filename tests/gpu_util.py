@@ -34,17 +34,18 @@ def device_ok():
     assert st == pkg.FFPA_OK, pkg.ffpa_status_string(st)
 
 
-def sample_rows(B, Hq, Nq, n_random=64, edge=32, heads=None, seed=0):
-    """Flat row ids (b*Hq+h)*Nq+i: the first and last `edge` rows of a few
-    heads plus seeded random rows, so that every query tile kind (first,
-    interior, ragged last) is covered."""
+def sample_rows(B, Hq, Nq, n_random=8, tile=128, heads=None, seed=0):
+    """Flat row ids (b*Hq+h)*Nq+i of every (batch, head) pair (or of `heads`):
+    the first and last row of every `tile`-row query tile plus `n_random`
+    seeded random rows per head, so that every head, every grouped KV head
+    and every query tile kind (first, interior, ragged last) is compared."""
     g = torch.Generator().manual_seed(seed)
     if heads is None:
-        heads = sorted({(0, 0), (B - 1, Hq - 1), (B // 2, Hq // 2)})
+        heads = [(b, h) for b in range(B) for h in range(Hq)]
     rows = []
     for b, h in heads:
         base = (b * Hq + h) * Nq
-        idx = set(range(min(edge, Nq))) | set(range(max(0, Nq - edge), Nq))
+        idx = {i for t0 in range(0, Nq, tile) for i in (t0, min(Nq, t0 + tile) - 1)}
         idx |= set(torch.randint(0, Nq, (n_random,), generator=g).tolist())
         rows += [base + i for i in sorted(idx)]
     return torch.tensor(rows, dtype=torch.int64)

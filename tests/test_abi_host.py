@@ -55,14 +55,19 @@ def _arr(vals):
 
 
 def dense_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,
-               q=FAKE, qs=None, mask=None, mask_kind=0, mask_str=None, scale=None, o=FAKE):
+               q=FAKE, qs=None, mask=None, mask_kind=0, mask_str=None, scale=None, o=FAKE,
+               lse=None, options=None):
     def st(H, N):
         return _arr([H * N * D, N * D, D, 1])
     qs = qs or st(Hq, Nq)
     ks = st(Hkv, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(scale))
-    return lib.ffpa_fwd(q, FAKE, FAKE, o, None, dt, B, Hq, Hkv, Nq, Nkv, D, qs, ks, ks, st(Hq, Nq),
-                        mask, mask_kind, mask_str, sc, causal, enable_gqa, None)
+    if options is None:
+        return lib.ffpa_fwd(q, FAKE, FAKE, o, lse, dt, B, Hq, Hkv, Nq, Nkv, D, qs, ks, ks,
+                            st(Hq, Nq), mask, mask_kind, mask_str, sc, causal, enable_gqa, None)
+    return lib.ffpa_fwd_ex(q, FAKE, FAKE, o, lse, dt, B, Hq, Hkv, Nq, Nkv, D, qs, ks, ks, st(Hq, Nq),
+                           mask, mask_kind, mask_str, sc, causal, enable_gqa, None,
+                           ctypes.byref(options))
 
 
 def varlen_call(lib, dt=0, Tq=256, Tk=256, Hq=2, Hkv=2, D=64, nseq=2, causal=0, enable_gqa=0,
@@ -98,7 +103,21 @@ def test_dense_layout_and_pointer_checks(lib):
     assert dense_call(lib, mask_kind=2, mask=FAKE, mask_str=_arr([0, -1, 0, 1])) == INVALID
     assert dense_call(lib, scale=float("inf")) == INVALID
     assert dense_call(lib, scale=float("nan")) == INVALID
+    # a mask pointer not aligned to its element type, an LSE not aligned to 4 bytes
+    for kind, off in ((2, 2), (2, 1), (3, 1)):
+        assert dense_call(lib, mask_kind=kind, mask=FAKE + off, mask_str=_arr([0, 0, 0, 1])) == INVALID
+    assert dense_call(lib, lse=FAKE + 2) == INVALID
 
+
+def test_options_are_checked(lib):
+    """ffpa_options.kernel outside FFPA_VARIANT_AUTO..SPLIT is rejected; the
+    defaults (all zero) behave as the plain entry point."""
+    bad = pkg.Options(None, 0, 7, 0)
+    assert dense_call(lib, options=bad) == pkg.FFPA_ERR_INVALID
+    assert dense_call(lib, options=pkg.Options(None, 0, -1, 0)) == pkg.FFPA_ERR_INVALID
+    assert dense_call(lib, options=pkg.Options(None, 0, 0, 0), D=32) == pkg.FFPA_ERR_UNSUPPORTED
+    if not torch.cuda.is_available():
+        assert dense_call(lib, options=pkg.Options(None, 0, 3, 0)) == dense_call(lib)
 
 def test_check_order_dtype_first(lib):
     # a bad dtype is reported even when everything else is also wrong
@@ -149,31 +168,28 @@ def test_binding_rejects_malformed_cu_seqlens(lib):
 
 
 def test_kernel_variant_names(lib):
-    for name in ("single", "pair", "auto"):
-        pkg.set_kernel_variant(name)
+    for name in ("single", "pair", "split", "auto"):
+        pkg.selected_kernel(512, kernel=name)
     with pytest.raises(ValueError):
-        pkg.set_kernel_variant("fastest")
-    lib.ffpa_set_kernel_variant(7)  # out of range: ignored, no effect
-    pkg.set_kernel_variant("auto")
+        pkg.selected_kernel(512, kernel="fastest")
+    assert lib.ffpa_selected_kernel(512, 0, 7) == -1        # out of range
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd(q, q, q, kernel="fastest")
 
 
 def test_selected_kernel_follows_the_choice(lib):
-    pkg.set_kernel_variant("auto")
     assert pkg.selected_kernel(512) == "split"
     assert pkg.selected_kernel(512, varlen=True) == "split"
     assert pkg.selected_kernel(256) == "pair"
     assert pkg.selected_kernel(256, varlen=True) == "single"
     assert pkg.selected_kernel(1024) == "single"
-    try:
-        pkg.set_kernel_variant("pair")
-        assert pkg.selected_kernel(512) == "pair"
-        assert pkg.selected_kernel(384) == "single"      # pair kernel does not take D=384
-        pkg.set_kernel_variant("split")
-        assert pkg.selected_kernel(384) == "split"
-        assert pkg.selected_kernel(640) == "single"
-    finally:
-        pkg.set_kernel_variant("auto")
-    assert lib.ffpa_selected_kernel(100, 0) == -1
+    assert pkg.selected_kernel(512, kernel="pair") == "pair"
+    assert pkg.selected_kernel(384, kernel="pair") == "single"      # pair kernel does not take D=384
+    assert pkg.selected_kernel(384, kernel="split") == "split"
+    assert pkg.selected_kernel(640, kernel="split") == "single"
+    assert pkg.selected_kernel(512) == "split"                     # no choice outlives a call
+    assert lib.ffpa_selected_kernel(100, 0, 0) == -1
     with pytest.raises(ValueError):
         pkg.selected_kernel(100)                          # not a multiple of 8
     assert pkg.selected_kernel(96) == "single"            # zero-padded to two chunks
@@ -216,6 +232,37 @@ def test_bwd_valid_call_without_gpu_reports_cuda_error(lib):
     assert bwd_call(lib) == pkg.FFPA_ERR_CUDA
 
 
+def test_binding_checks_caller_outputs(lib):
+    """Caller-supplied outputs must have the shape, dtype and device the library
+    writes: the C side sizes every write from q and k."""
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    for bad in (torch.zeros(1, 2, 3, 64, dtype=torch.bfloat16),      # fewer rows
+                torch.zeros(1, 2, 4, 64, dtype=torch.float16),       # other dtype
+                torch.zeros(2, 4, 64, dtype=torch.bfloat16),         # rank 3
+                torch.zeros(1, 2, 4, 32, dtype=torch.bfloat16)):     # narrower D
+        with pytest.raises(ValueError):
+            pkg.ffpa_fwd(q, q, q, out=bad)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd(q, q, q, lse=torch.zeros(1, 2, 3))
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd(q, q, q, lse=torch.zeros(1, 2, 4, dtype=torch.float64))
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd(q, q, q, status=torch.zeros(1, dtype=torch.int64))
+    qv = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 10], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd_varlen(qv, qv, qv, cu, None, 10, 10, out=qv[:9])
+    with pytest.raises(ValueError):
+        pkg.ffpa_fwd_varlen(qv, qv, qv, cu, None, 10, 10, lse=torch.zeros(10, 2))   # [T, H] not [H, T]
+    lse = torch.zeros(1, 2, 4)
+    for name, bad in (("dq", q[:, :1]), ("dk", q.half()), ("dv", q[..., :32]),
+                      ("delta", torch.zeros(1, 2, 4, dtype=torch.float64))):
+        with pytest.raises(ValueError):
+            pkg.ffpa_bwd(q, q, q, q, q, lse, **{name: bad})
+    with pytest.raises(ValueError):
+        pkg.ffpa_bwd_varlen(qv, qv, qv, qv, qv, torch.zeros(2, 10), cu, None, 10, 10, dq=qv[:, :1])
+
+
 def test_bwd_binding_checks(lib):
     q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
     lse = torch.zeros(1, 2, 4)
@@ -236,18 +283,12 @@ def test_fine_head_dims_dense_only(lib):
     assert dense_call(lib, D=100) == UNSUP
     assert varlen_call(lib, D=72) == UNSUP
     assert bwd_call(lib, D=72) == UNSUP
-    pkg.set_kernel_variant("auto")
     assert pkg.selected_kernel(72) == "single"
     assert pkg.selected_kernel(520) == "single"
     with pytest.raises(ValueError):
         pkg.selected_kernel(72, varlen=True)
-    try:
-        pkg.set_kernel_variant("split")
-        assert pkg.selected_kernel(120) == "single"
-        pkg.set_kernel_variant("pair")
-        assert pkg.selected_kernel(192 + 8) == "single"
-    finally:
-        pkg.set_kernel_variant("auto")
+    assert pkg.selected_kernel(120, kernel="split") == "single"
+    assert pkg.selected_kernel(192 + 8, kernel="pair") == "single"
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")

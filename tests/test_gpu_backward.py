@@ -32,7 +32,6 @@ G_MAX, G_MEAN = 2e-2, 1e-2
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     pkg.load_library()
-    pkg.set_wait_timeout_ns(0)
     yield
 
 
@@ -263,6 +262,22 @@ def test_autograd_with_bool_mask():
     check_grad(vd.grad, rv, "autograd masked dV")
 
 
+def test_autograd_lse_output_unused_or_used():
+    """An LSE that is returned but not used by the loss needs no gradient (the
+    backward receives none and reads nothing from the device); a loss that
+    uses it raises, since no LSE gradient is formed."""
+    q, k, v, dout = draw(1, 2, 2, 150, 150, 128, seed=48)
+    qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
+    o, lse = pkg.ffpa_attn_func(qd, kd, vd, is_causal=True, return_lse=True)
+    o.backward(dout.to(DEV))
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, is_causal=True)
+    check_grad(qd.grad, rq, "dQ with LSE returned")
+    o, lse = pkg.ffpa_attn_func(qd, kd, vd, return_lse=True)
+    with pytest.raises(NotImplementedError):
+        (o.sum() + lse.sum()).backward()
+
+
 def test_autograd_mask_gradient_raises():
     q, k, v, _ = draw(1, 2, 2, 64, 64, 128, seed=46)
     qd, kd, vd = (t.to(DEV).requires_grad_() for t in (q, k, v))
@@ -281,15 +296,12 @@ def test_bwd_bounded_wait_reports_timeout_and_context_survives():
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
     o, lse = pkg.ffpa_fwd(qd, kd, vd, return_lse=True)
     device_ok()
-    pkg.set_wait_timeout_ns(200_000_000)
-    pkg.inject_dropped_copy(True)
-    try:
-        pkg.ffpa_bwd(dod, qd, kd, vd, o, lse)
-        st = pkg.ffpa_last_device_error()
-    finally:
-        pkg.inject_dropped_copy(False)
-        pkg.set_wait_timeout_ns(0)
-    assert st == pkg.FFPA_ERR_DEVICE_TIMEOUT
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, status=status, wait_timeout_ns=200_000_000,
+                 test_drop_first_copy=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == pkg.FFPA_ERR_DEVICE_TIMEOUT
+    assert pkg.ffpa_last_device_error() == pkg.FFPA_OK
     dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse)
     device_ok()
     rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout)
