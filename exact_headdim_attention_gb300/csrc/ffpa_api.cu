@@ -52,29 +52,6 @@ struct DeviceFacts {
 };
 DeviceFacts g_devices[MAX_DEVICES];
 
-// Makes `dev` the library runtime's current device for the lifetime of the
-// object and restores the previous one afterwards, so that a call leaves
-// the calling thread's current device as it found it.
-class DeviceScope {
- public:
-  explicit DeviceScope(int dev) : dev_(dev) {
-    if (cudaGetDevice(&prev_) != cudaSuccess) {
-      cudaGetLastError();
-      prev_ = -1;
-    }
-    ok_ = prev_ == dev_ || cudaSetDevice(dev_) == cudaSuccess;
-  }
-  ~DeviceScope() {
-    if (ok_ && prev_ >= 0 && prev_ != dev_) cudaSetDevice(prev_);
-  }
-  bool ok() const { return ok_; }
-
- private:
-  int dev_;
-  int prev_ = -1;
-  bool ok_ = false;
-};
-
 // The device's facts (computed on first use with `dev` current).
 const DeviceFacts& device_facts(int dev) {
   DeviceFacts& f = g_devices[dev];
@@ -363,6 +340,53 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, 
 }  // namespace
 
 namespace ffpa {
+
+namespace {
+struct CtxFns {
+  PFN_cuCtxGetCurrent_v4000 get = nullptr;
+  PFN_cuCtxSetCurrent_v4000 set = nullptr;
+};
+const CtxFns& ctx_fns() {
+  static CtxFns f;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* g = nullptr;
+    void* s = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &g, 4000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxSetCurrent", &s, 4000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q2 == cudaDriverEntryPointSuccess) {
+      f.get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(g);
+      f.set = reinterpret_cast<PFN_cuCtxSetCurrent_v4000>(s);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  return f;
+}
+}  // namespace
+
+DeviceScope::DeviceScope(int dev) {
+  const CtxFns& f = ctx_fns();
+  if (!f.get || !f.set || f.get(&saved_) != CUDA_SUCCESS) return;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  // Since CUDA 12, cudaSetDevice initialises the primary context and makes
+  // it current on this thread at once.
+  CUcontext now = nullptr;
+  if (f.get(&now) != CUDA_SUCCESS || now == nullptr) return;
+  restore_ = now != saved_;
+  ok_ = true;
+}
+
+DeviceScope::~DeviceScope() {
+  if (restore_) ctx_fns().set(saved_);
+}
 
 // Kernels whose shared-memory limit was raised, per device (set-once facts).
 ffpa_status set_smem_attr_once(const void* fn, int device, int bytes) {

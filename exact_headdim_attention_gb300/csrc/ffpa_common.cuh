@@ -83,6 +83,25 @@ ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, si
 // once per (kernel, device) pair; later calls only look the pair up.
 ffpa_status set_smem_attr_once(const void* fn, int device, int bytes);
 
+// Binds the primary context of `dev` to the calling thread for the lifetime
+// of the object (tensor-map encoding, symbol lookups and launches need a
+// current context; a framework's worker thread may have none), and puts the
+// thread's previous driver context back afterwards (none, if it had none),
+// so that a call leaves the caller's thread as it found it.
+class DeviceScope {
+ public:
+  explicit DeviceScope(int dev);
+  ~DeviceScope();
+  bool ok() const { return ok_; }
+  DeviceScope(const DeviceScope&) = delete;
+  DeviceScope& operator=(const DeviceScope&) = delete;
+
+ private:
+  CUcontext saved_ = nullptr;
+  bool restore_ = false;
+  bool ok_ = false;
+};
+
 // Backward (ffpa_bwd.cu): a delta pass, then one kernel for dQ (rows =
 // queries) and one each for dV and dK (rows = keys; one for both when
 // D <= 128).

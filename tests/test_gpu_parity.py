@@ -417,6 +417,38 @@ def test_pointers_on_another_device_are_rejected():
         pkg.ffpa_fwd(qd, k.to(DEV), v.to(DEV), out=torch.empty_like(q))   # out on the host
 
 
+def test_calls_from_a_thread_without_a_current_context():
+    """A fresh host thread (like a framework's backward worker) has no CUDA
+    context bound; the library binds the device's context for the call (the
+    tensor-map encoder needs one) and puts the thread back as it found it."""
+    import threading
+    q, k, v, g = wl.draw_dense(1, 4, 2, 260, 260, 512, seed=51)
+    dout = torch.randn(q.shape, generator=g).bfloat16()
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    res = {}
+
+    def work():
+        try:
+            o, l = pkg.ffpa_fwd(qd, kd, vd, is_causal=True, enable_gqa=True, return_lse=True)
+            res["fwd"] = (o, l)
+            res["bwd"] = pkg.ffpa_bwd(dod, qd, kd, vd, o, l, is_causal=True, enable_gqa=True)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported to the main thread
+            res["error"] = e
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert "error" not in res, res.get("error")
+    device_ok()
+    o_ref, l_ref = oracle.attn_dense(q, k, v, is_causal=True)
+    check(*res["fwd"], o_ref, l_ref, "forward from a fresh thread")
+    refs = oracle.attn_bwd_dense(q, k, v, dout, is_causal=True)
+    for got, ref in zip(res["bwd"], refs):
+        err = (got.double().cpu() - ref).abs().max().item()
+        assert err <= 2e-2 * ref.abs().max().item()
+
+
 def test_call_leaves_current_device_unchanged():
     before = torch.cuda.current_device()
     run_dense(*wl.draw_dense(1, 1, 1, 64, 64, 64, seed=50)[:3])
