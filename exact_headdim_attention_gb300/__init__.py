@@ -23,6 +23,8 @@ from ._binding import (  # noqa: F401
     Options,
     default_scale,
     ffpa_bwd,
+    ffpa_bwd_noalloc,
+    BWD_NOALLOC_MAX_ROWS,
     ffpa_bwd_varlen,
     ffpa_fwd,
     ffpa_fwd_varlen,

@@ -24,7 +24,7 @@ FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4
 
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", "ffpa_bwd",
             "ffpa_bwd_ex", "ffpa_bwd_varlen", "ffpa_bwd_varlen_ex", "ffpa_status_string",
-            "ffpa_last_device_error", "ffpa_selected_kernel")
+            "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
 
@@ -91,6 +91,9 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
         getattr(lib, name).restype = I
         getattr(lib, name + "_ex").argtypes = args + [O]
         getattr(lib, name + "_ex").restype = I
+    # ffpa_bwd without the delta argument
+    lib.ffpa_bwd_noalloc.argtypes = sigs["ffpa_bwd"][:9] + sigs["ffpa_bwd"][10:]
+    lib.ffpa_bwd_noalloc.restype = I
     lib.ffpa_status_string.argtypes = [I]
     lib.ffpa_status_string.restype = ctypes.c_char_p
     lib.ffpa_last_device_error.argtypes = [P]
@@ -323,6 +326,45 @@ def _grad_buffers(q, k, v, dq, dk, dv, delta, delta_shape):
     else:
         _check_buffer(delta, "delta", delta_shape, torch.float32, q.device, contiguous=True)
     return dq, dk, dv, delta
+
+
+BWD_NOALLOC_MAX_ROWS = 1048576   # FFPA_BWD_NOALLOC_MAX_ROWS of include/ffpa.h
+
+
+def ffpa_bwd_noalloc(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                     out: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+                     dv: torch.Tensor, is_causal: bool = False, scale: float | None = None,
+                     enable_gqa: bool = False, attn_mask=None, *, stream=None):
+    """Dense backward through the C ABI ``ffpa_bwd_noalloc``, for callers that
+    cannot allocate device memory: the per-row scratch of the backward lives in
+    a fixed array inside the library (at most BWD_NOALLOC_MAX_ROWS = B*Hq*Nq
+    rows), and the caller passes dq, dk and dv.  Nothing is allocated here
+    either (a broadcast mask is passed as a strided view).  Calls on one device
+    share that array: calls that overlap on the GPU race."""
+    lib = load_library()
+    B, Hq, Nq, D = q.shape
+    Nkv = k.shape[2]
+    if B * Hq * Nq > BWD_NOALLOC_MAX_ROWS:
+        raise ValueError(f"B*Hq*Nq = {B * Hq * Nq} exceeds the {BWD_NOALLOC_MAX_ROWS} rows of the "
+                         "library's fixed backward scratch; use ffpa_bwd with a delta buffer")
+    _check_buffer(dq, "dq", q.shape, q.dtype, q.device)
+    _check_buffer(dk, "dk", k.shape, k.dtype, q.device)
+    _check_buffer(dv, "dv", v.shape, v.dtype, q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Nq] tensor")
+    mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
+    st = lib.ffpa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), _dtype_code(q), B, Hq, k.shape[1], Nq, Nkv, D,
+                              _strides(q), _strides(k), _strides(v), _strides(out),
+                              _strides(dout), _strides(dq), _strides(dk), _strides(dv), mptr, mk,
+                              mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
+                              _stream_handle(stream, q))
+    del keep
+    if st != FFPA_OK:
+        _raise(st, "ffpa_bwd_noalloc")
+    return dq, dk, dv
 
 
 def _check_cu(cu: torch.Tensor, T: int, name: str) -> list[int]:

@@ -279,6 +279,41 @@ ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, cons
                                int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                                int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
 
+/*
+ * Backward for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this entry point exists for callers such as plugins that
+ * receive only their tensors' pointers from a host framework, runtimes that
+ * reserve all device memory up front, and latency-bound paths where a
+ * cudaMalloc (which may synchronise the device, or fail once memory is
+ * exhausted) is not acceptable.
+ *
+ * Same arguments, checks and results as ffpa_bwd without `delta`: the
+ * per-row values rowsum(dout * o) that the backward keeps between its first
+ * kernel and the gradient kernels live in a fixed array inside the library
+ * (FFPA_BWD_NOALLOC_MAX_ROWS fp32 values, 4 MiB, held by every GPU that
+ * loads the library until the process exits).  The caller still passes
+ * every input and the dq, dk, dv outputs; nothing is allocated or freed.
+ *  - B * Hq * Nq above FFPA_BWD_NOALLOC_MAX_ROWS: FFPA_ERR_INVALID, nothing
+ *    is enqueued (use ffpa_bwd with a caller-owned delta instead).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    values; nothing in it needs to start at zero (each call writes every
+ *    entry it reads).  Calls whose work overlaps on the GPU (on different
+ *    streams, or from different threads) race on it: serialise them.
+ */
+#define FFPA_BWD_NOALLOC_MAX_ROWS 1048576
+ffpa_status ffpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                             const int64_t q_str[4], const int64_t k_str[4],
+                             const int64_t v_str[4], const int64_t o_str[4],
+                             const int64_t do_str[4], const int64_t dq_str[4],
+                             const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                             ffpa_mask_kind mask_kind, const int64_t mask_str[4],
+                             const float* scale, int is_causal, int enable_gqa,
+                             ffpa_stream_t stream);
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* ffpa_status_string(ffpa_status status);
 
