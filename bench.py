@@ -412,7 +412,8 @@ def run_ours(args):
     vl, um = str(w.varlen).lower(), str(x.get("mask") is not None).lower()
     kernel = {"single": f"ffpa_fwd_kernel<{vl}, {um}>",
               "pair": f"ffpa_fwd_pair_kernel<{vl}, {w.D // 64}, {um}>",
-              "split": f"ffpa_fwd_split_kernel<{vl}, {w.D // 64}, {um}>"}[kname]
+              "split": (f"ffpa_fwd_split_kernel<{vl}, {w.D // 64}, {um}>" if w.D <= 512 else
+                        f"ffpa_fwd_cluster_kernel<{vl}, {w.D // 64}, {um}, {w.D // 256}>")}[kname]
     per_launch_s = elapsed / args.steps
     achieved = flops / per_launch_s / 1e12
     line = {

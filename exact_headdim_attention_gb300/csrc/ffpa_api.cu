@@ -231,42 +231,60 @@ bool pair_eligible(int D) {
 
 enum class Kern { SINGLE, PAIR, SPLIT };
 
-// The column-split kernel needs each CTA's half of the output columns to be
-// whole 64-column chunks of at most 256 columns.
-bool split_eligible(int D) { return D >= 128 && D % 128 == 0 && D / 2 <= DV_MAX; }
+// CTAs per cluster of the column-split kernel for head dimension D: each
+// CTA owns D / C output columns, whole 64-column chunks of at most 256
+// columns (0 = the kernel does not take D).  Instantiated shapes: D = 128,
+// 256, 384, 512 with C = 2; 768 with C = 3; 1024 with C = 4.
+int split_ways(int D) {
+  switch (D) {
+    case 128: case 256: case 384: case 512: return 2;
+    case 768: return 3;
+    case 1024: return 4;
+    default: return 0;
+  }
+}
 
-// Kernel choice, from measurements on GB300 (bf16): at D=512 the column-split
-// kernel wins on dense, causal and varlen batches (it does not recompute S);
-// at D=256 (no recompute anyway) the pair kernel wins on dense batches; at
-// D=128 the single-CTA kernel's shorter per-tile chain wins, and on packed
-// varlen batches of mixed lengths the 256-row pair tiles waste more rows on
-// short sequences than they save.
+bool split_eligible(int D) { return split_ways(D) != 0; }
+
+// Kernel choice, from measurements on GB300 (bf16): from D=384 up the
+// column-split kernel wins on dense, causal and varlen batches (it does not
+// recompute S; D=384: 1048 vs 732 TFLOPS for the single-CTA kernel); at D=256 (no recompute anyway) the pair kernel wins on
+// dense batches; at D=128 the single-CTA kernel's shorter per-tile chain
+// wins, and on packed varlen batches of mixed lengths the 256-row pair
+// tiles waste more rows on short sequences than they save.
 Kern choose_kernel(int D, bool varlen, int v) {
   if (D % DK != 0) return Kern::SINGLE;   // only the single-CTA kernel takes zero-padded chunks
   if (v == FFPA_VARIANT_SINGLE) return Kern::SINGLE;
   if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
   if (v == FFPA_VARIANT_SPLIT) return split_eligible(D) ? Kern::SPLIT : Kern::SINGLE;
-  if (D == 512) return Kern::SPLIT;
+  if (D == 384 || D == 512 || D == 768 || D == 1024) return Kern::SPLIT;
   if (!varlen && D == 256) return Kern::PAIR;
   return Kern::SINGLE;
 }
 
 // Column-split plan: Q chunks 0..3 in TMEM, the rest resident in shared
-// memory, two P tiles, V stages of vk keys x D/2 columns, 32 KB ring slots.
+// memory when they fit (else streamed through the ring), C P tiles, V
+// stages of vk keys x D/C columns, 32 KB ring slots.
 size_t plan_split(int D, Params* P) {
+  const int C = split_ways(D);
+  P->split_c = C;
   P->nchunks = D / DK;
   P->n_slices = 1;
   P->qt_chunks = P->nchunks < Q_TMEM_MAX_CHUNKS ? P->nchunks : Q_TMEM_MAX_CHUNKS;
   P->kchunks = 2;
   P->kc = 2;
-  P->q_res = 1;
-  P->vchunks = D / 2 / DK;
+  const bool qres = (size_t)(P->nchunks - P->qt_chunks) * CHUNK_BYTES + (size_t)C * P_TILE_BYTES +
+                        3 * (size_t)SLOT_BYTES <=
+                    SMEM_LIMIT - SPLIT_STATIC_RESERVE - 1024;
+  P->q_res = qres ? 1 : 0;
+  P->vchunks = P->nchunks / C;
   int vk = 128;
   while (vk > 16 && (size_t)vk * P->vchunks * 128 > SLOT_BYTES) vk >>= 1;
   P->vk = vk;
   P->vslot = vk * P->vchunks * 128;
   P->nslot_v = 0;
-  const size_t fixed = (size_t)(P->nchunks - P->qt_chunks) * CHUNK_BYTES + 2 * (size_t)P_TILE_BYTES;
+  const size_t fixed =
+      (qres ? (size_t)(P->nchunks - P->qt_chunks) * CHUNK_BYTES : 0) + (size_t)C * P_TILE_BYTES;
   size_t ns = (SMEM_LIMIT - SPLIT_STATIC_RESERVE - 1024 - fixed) / SLOT_BYTES;
   if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
   P->nslot = static_cast<int>(ns);
@@ -299,7 +317,9 @@ ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size
                           cudaStream_t stream) {
   const bool umask = P.mask != nullptr;
   if (kn == Kern::PAIR) return launch_pair(varlen, umask, P, items, smem, stream);
-  if (kn == Kern::SPLIT) return launch_split(varlen, umask, P, items, smem, stream);
+  if (kn == Kern::SPLIT)
+    return P.split_c == 2 ? launch_split(varlen, umask, P, items, smem, stream)
+                          : launch_cluster(varlen, umask, P, items, smem, stream);
   return launch_single(varlen, umask, P, items, smem, stream);
 }
 

@@ -71,14 +71,16 @@ constexpr int SPLIT_THREADS = 192;
 constexpr uint32_t Q_TMEM_COL = 384;
 constexpr int Q_TMEM_MAX_CHUNKS = 4;
 constexpr uint32_t P_TILE_BYTES = BM * BN * 2;   // 2 x (128 rows x 64 keys), 16-bit
-constexpr size_t SPLIT_STATIC_RESERVE = 2048;
+constexpr size_t SPLIT_STATIC_RESERVE = 2048;    // static shared memory of the column-split kernel
 
 // ------------------------------------------------------------------ host
-// Launches of the three kernels (one translation unit each).
+// Launches of the forward kernels (one translation unit each; the column
+// split has a pair kernel and a kernel for clusters of 3 or 4 CTAs).
 struct Params;
 ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_cluster(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 // Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on `device`,
 // once per (kernel, device) pair; later calls only look the pair up.
 ffpa_status set_smem_attr_once(const void* fn, int device, int bytes);
@@ -171,6 +173,7 @@ struct Params {
   int nslot_v, vslot;  // V-ring depth and slot bytes (vk keys x vchunks 64-column chunks)
   int kslot, kc;       // pair kernel: K-ring slot bytes and D-chunks per K stage
   int qt_chunks;       // column-split kernel: Q chunks held in TMEM
+  int split_c;         // column-split kernel: CTAs per cluster (output columns D / split_c each)
   float scale_log2;
   int causal, fp16, inject;
   // Dense head dims that are not a multiple of 64 (D % 8 == 0): the maps

@@ -4,7 +4,8 @@
 namespace ffpa {
 
 // =====================================================================
-// Column-split pair kernel: no recomputation of S for D up to 512.
+// Column-split pair kernel: no recomputation of S for D up to 512 (the
+// clusters of 3 and 4 CTAs for D = 768 and 1024 are in ffpa_cluster.cu).
 //
 // A cluster of two CTAs owns one 128-row query tile; CTA c owns the output
 // columns [c D/2, (c+1) D/2), so each CTA's O accumulator (D/2 <= 256 fp32
@@ -528,6 +529,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
 
 template <bool VARLEN, bool UMASK>
 static ffpa_status launch_split_t(const Params& P, int items, size_t smem, cudaStream_t stream) {
+  if (P.split_c != 2 || (P.nchunks != 2 && P.nchunks != 4 && P.nchunks != 6 && P.nchunks != 8))
+    return FFPA_ERR_UNSUPPORTED;   // only the instantiated shapes
   auto kern = P.nchunks == 8   ? ffpa_fwd_split_kernel<VARLEN, 8, UMASK>
               : P.nchunks == 6 ? ffpa_fwd_split_kernel<VARLEN, 6, UMASK>
               : P.nchunks == 4 ? ffpa_fwd_split_kernel<VARLEN, 4, UMASK>

@@ -89,10 +89,13 @@ typedef enum {
  *     256 columns (any D; S is recomputed once per slice);
  *   - CTA pair: two SMs share each 256-query tile and each load half of every
  *     K/V tile (D in {128, 256, 512});
- *   - column split: two SMs share each 128-query tile, each owns half of the
- *     output columns, key tiles alternate between them and the P tiles are
- *     exchanged, so S is computed once (D in {128, 256, 384, 512}).
- *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default)
+ *   - column split: a cluster of C SMs shares each 128-query tile, each SM
+ *     owns D/C output columns, key tiles are dealt round-robin and the P
+ *     tiles are exchanged, so S is computed once (C = 2 for D in {128, 256,
+ *     384, 512}; C = 3 for D = 768; C = 4 for D = 1024).
+ *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default:
+ *                           column split for D in {384, 512, 768, 1024}, CTA
+ *                           pair for dense D = 256, single-CTA otherwise)
  *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
  *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
  *   FFPA_VARIANT_SPLIT  (3) the column-split kernel wherever D allows it

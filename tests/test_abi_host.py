@@ -183,7 +183,11 @@ def test_selected_kernel_follows_the_choice(lib):
     assert pkg.selected_kernel(512, varlen=True) == "split"
     assert pkg.selected_kernel(256) == "pair"
     assert pkg.selected_kernel(256, varlen=True) == "single"
-    assert pkg.selected_kernel(1024) == "single"
+    assert pkg.selected_kernel(1024) == "split"                    # cluster of 4 CTAs
+    assert pkg.selected_kernel(768) == "split"                     # cluster of 3 CTAs
+    assert pkg.selected_kernel(768, varlen=True) == "split"
+    assert pkg.selected_kernel(640) == "single"
+    assert pkg.selected_kernel(1024, kernel="single") == "single"
     assert pkg.selected_kernel(512, kernel="pair") == "pair"
     assert pkg.selected_kernel(384, kernel="pair") == "single"      # pair kernel does not take D=384
     assert pkg.selected_kernel(384, kernel="split") == "split"

@@ -265,14 +265,14 @@ def variant(request):
     return request.param
 
 
-@pytest.mark.parametrize("D", [128, 256, 384, 512])
+@pytest.mark.parametrize("D", [128, 256, 384, 512, 768, 1024])
 def test_variant_dense(variant, D):
     dense_case(1, 2, 2, 300, 300, D, seed=D + 1, kernel=variant)
     dense_case(2, 4, 1, 200, 700, D, seed=D + 2, causal=True, kernel=variant)
     dense_case(1, 2, 2, 65, 129, D, seed=D + 3, causal=True, kernel=variant)
 
 
-@pytest.mark.parametrize("D", [128, 512])
+@pytest.mark.parametrize("D", [128, 512, 1024])
 def test_variant_masks(variant, D):
     B, H, Nq, Nk = 2, 2, 270, 300
     dense_case(B, H, H, Nq, Nk, D, seed=D + 4, mask=MASKS["bool_b1nk"](B, H, Nq, Nk), kernel=variant)
@@ -284,7 +284,7 @@ def test_variant_fp16(variant):
     dense_case(1, 2, 1, 260, 260, 256, seed=9, causal=True, dtype=torch.float16, kernel=variant)
 
 
-@pytest.mark.parametrize("D", [128, 256, 512])
+@pytest.mark.parametrize("D", [128, 256, 512, 768, 1024])
 @pytest.mark.parametrize("causal", [False, True])
 def test_variant_varlen(variant, D, causal):
     lq = [3, 130, 1, 257, 0, 64, 200, 300]
@@ -361,10 +361,11 @@ def test_bounded_wait_pair_kernel():
     _timeout_then_correct(q, k, v, kernel="pair")
 
 
-def test_bounded_wait_split_kernel():
-    """Through the column-split kernel: one CTA of the pair loses a copy, the
-    other one waits for its tile maxima; both time out."""
-    q, k, v, _ = wl.draw_dense(1, 2, 2, 200, 400, 512, seed=43)
+@pytest.mark.parametrize("D", [512, 768, 1024])
+def test_bounded_wait_split_kernel(D):
+    """Through the column-split kernel (clusters of 2, 3 and 4 CTAs): rank 0
+    loses a copy, the others wait for its tile maxima; all time out."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 200, 400, D, seed=43)
     _timeout_then_correct(q, k, v, kernel="split")
 
 
