@@ -65,6 +65,13 @@ class Oracle:
         self.lib.oracle_attn_bwd_varlen.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, I, D, I,
                                                     P, P, P, I]
         self.lib.oracle_attn_bwd_varlen.restype = I
+        self.lib.oracle_e4m3_encode.argtypes = [P, L, P]
+        self.lib.oracle_e4m3_encode.restype = I
+        self.lib.oracle_fp8_quantize.argtypes = [P, I, I, I, I, I, P, P, P]
+        self.lib.oracle_fp8_quantize.restype = I
+        self.lib.oracle_attn_fp8.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P, P, I, P, D, I, P, L,
+                                             P, P, I]
+        self.lib.oracle_attn_fp8.restype = I
 
     # ------------------------------------------------------------------ dense
     def attn_dense(self, q, k, v, attn_mask=None, scale=None, is_causal=False, rows=None,
@@ -74,6 +81,10 @@ class Oracle:
         attn_mask: None, bool (True keeps), float32 or q-dtype additive,
         broadcastable to [B,Hq,Nq,Nkv].  rows: optional int64 tensor of flat
         row ids (b*Hq+hq)*Nq+i.  Returns (O float64, LSE float64)."""
+        return self._attn_dense_like(self.lib.oracle_attn_dense, q, k, v, attn_mask, scale,
+                                     is_causal, rows, nthreads)
+
+    def _attn_dense_like(self, fn, q, k, v, attn_mask, scale, is_causal, rows, nthreads):
         dtype = _dtype_code(q)
         assert k.dtype == q.dtype and v.dtype == q.dtype
         B, Hq, Nq, D = q.shape
@@ -107,18 +118,17 @@ class Oracle:
             nrows = rows_t.numel()
         o = torch.empty(nrows, D, dtype=torch.float64)
         lse = torch.empty(nrows, dtype=torch.float64)
-        rc = self.lib.oracle_attn_dense(
-            q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype, B, Hq, Hkv, Nq, Nkv, D,
-            _strides(q), _strides(k), _strides(v), mptr, mk, mstr, float(scale), int(bool(is_causal)),
-            None if rows_t is None else rows_t.data_ptr(), nrows, o.data_ptr(), lse.data_ptr(), nthreads)
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype, B, Hq, Hkv, Nq, Nkv, D,
+                _strides(q), _strides(k), _strides(v), mptr, mk, mstr, float(scale),
+                int(bool(is_causal)), None if rows_t is None else rows_t.data_ptr(), nrows,
+                o.data_ptr(), lse.data_ptr(), nthreads)
         del keep
         if rc != 0:
-            raise ValueError("oracle_attn_dense rejected its arguments")
+            raise ValueError("the oracle rejected its arguments")
         if rows is None:
             return o.view(B, Hq, Nq, D), lse.view(B, Hq, Nq)
         return o, lse
 
-    # ----------------------------------------------------------------- varlen
     def attn_varlen(self, q, k, v, cu_q, cu_k=None, scale=None, causal=False, nthreads: int = 0):
         """Packed q [Tq,Hq,D], k/v [Tk,Hkv,D]; cu_* int32 [nseq+1].
 
@@ -221,6 +231,42 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_attn_bwd_varlen rejected its arguments")
         return dq, dk, dv
+
+
+def _fp8_methods():
+    """FP8 forward reference (see the FP8 section of ffpa_oracle.c)."""
+
+    def e4m3_encode(self, x: torch.Tensor) -> torch.Tensor:
+        """uint8 e4m3 codes of float32 values (clamped to [-448, 448]), nearest-even."""
+        x = x.detach().to(torch.float32).contiguous().reshape(-1)
+        out = torch.empty(x.numel(), dtype=torch.uint8)
+        if self.lib.oracle_e4m3_encode(x.data_ptr(), x.numel(), out.data_ptr()) != 0:
+            raise ValueError("NaN given to the e4m3 encoder")
+        return out
+
+    def fp8_quantize(self, x: torch.Tensor):
+        """codes uint8 [B,H,Npad,D] and scales float32 [B,H,Npad/128] of a bf16/fp16 [B,H,N,D]."""
+        B, H, N, D = x.shape
+        nblk = (N + 127) // 128
+        codes = torch.empty(B, H, nblk * 128, D, dtype=torch.uint8)
+        scales = torch.empty(B, H, nblk, dtype=torch.float32)
+        rc = self.lib.oracle_fp8_quantize(x.data_ptr(), _dtype_code(x), B, H, N, D, _strides(x),
+                                          codes.data_ptr(), scales.data_ptr())
+        if rc != 0:
+            raise ValueError("oracle_fp8_quantize rejected its arguments")
+        return codes, scales
+
+    def attn_fp8(self, q, k, v, attn_mask=None, scale=None, is_causal=False, rows=None,
+                 nthreads: int = 0):
+        """Exact attention (float64) on the per-block e4m3 quantised Q, K, V; arguments
+        and results as attn_dense."""
+        return self._attn_dense_like(self.lib.oracle_attn_fp8, q, k, v, attn_mask, scale,
+                                     is_causal, rows, nthreads)
+
+    return e4m3_encode, fp8_quantize, attn_fp8
+
+
+Oracle.e4m3_encode, Oracle.fp8_quantize, Oracle.attn_fp8 = _fp8_methods()
 
 
 def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):

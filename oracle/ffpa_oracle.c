@@ -576,3 +576,238 @@ int oracle_attn_bwd_varlen(const uint16_t* q, const uint16_t* k, const uint16_t*
     }
     return err ? -1 : 0;
 }
+
+/* ====================================================================
+ * FP8 forward (FFPA README, "Backends" and "Latest News": FP8 attention
+ * kernels for head dims 64..1024 that take bf16/fp16 tensors and return the
+ * input type; the pages name scale folding but print no quantisation
+ * formula, so the scheme below is this build's reading).
+ *
+ * Each of Q, K and V is quantised per (batch, head, block of 128 rows):
+ *   amax = max |x| over the block's rows (those below N) and all D columns;
+ *   if amax > 0 and 448 / amax is finite in float:
+ *       inv = fl(448 / amax), s = fl(amax / 448)
+ *   else inv = 0, s = 1;
+ *   code(x) = e4m3(clamp(fl(x * inv), -448, 448)), rounded to nearest,
+ *             ties to even (fl = one float operation, rounded to nearest);
+ *   dequantised x = value(code) * s.
+ * The FP8 attention is then the exact definition (in double) on the
+ * dequantised Q, K and V, with the mask, scale, causal rule and GQA map of
+ * the 16-bit path; its P is not rounded here (the kernel's e4m3 P is
+ * covered by the tolerance the tests derive).
+ * ==================================================================== */
+
+enum { ORACLE_FP8_BLOCK = 128 };
+
+/* e4m3 (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no
+ * infinities; largest finite 448 = 1.75 * 2^8; smallest subnormal 2^-9) of a
+ * finite y with |y| <= 448, rounded to nearest, ties to even. */
+static uint8_t e4m3_encode(float y) {
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    const double a = fabs((double)y);
+    if (a == 0.0) return sign;
+    int e2;
+    frexp(a, &e2);            /* a = f * 2^e2, f in [0.5, 1): a in [2^(e2-1), 2^e2) */
+    const int E = e2 - 1;     /* a = 1.m * 2^E */
+    if (E < -6) {             /* subnormal range: multiples of 2^-9 */
+        const double q = nearbyint(ldexp(a, 9));   /* ties to even (default rounding mode) */
+        return (uint8_t)(sign | (uint8_t)q);       /* q == 8 is the smallest normal, code 0x08 */
+    }
+    double q = nearbyint(ldexp(a, 3 - E));          /* eighths of 2^E: 8 .. 16 */
+    int ex = E;
+    if (q == 16.0) {
+        q = 8.0;
+        ++ex;
+    }
+    return (uint8_t)(sign | (uint8_t)((ex + 7) << 3) | (uint8_t)((int)q - 8));
+}
+
+static double e4m3_value(uint8_t c) {
+    const int ex = (c >> 3) & 0x0f, fr = c & 0x07;
+    const double mag = ex == 0 ? ldexp((double)fr, -9) : ldexp(8.0 + fr, ex - 10);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/* e4m3 codes of n floats (each clamped to [-448, 448] first). */
+int oracle_e4m3_encode(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) {
+        float y = x[i];
+        if (!(y == y)) return -1;
+        if (y > 448.0f) y = 448.0f;
+        if (y < -448.0f) y = -448.0f;
+        out[i] = e4m3_encode(y);
+    }
+    return 0;
+}
+
+/* Quantises x [B, H, N, D] (element strides x_str, D stride 1) block by
+ * block: codes [B, H, Npad, D] contiguous with Npad = N rounded up to 128
+ * (rows >= N are zero), scales s [B, H, Npad/128] contiguous. */
+int oracle_fp8_quantize(const uint16_t* x, int dtype, int B, int H, int N, int D,
+                        const int64_t* x_str, uint8_t* codes, float* scales) {
+    if (B < 0 || H <= 0 || N < 0 || D <= 0) return -1;
+    const int nblk = (N + ORACLE_FP8_BLOCK - 1) / ORACLE_FP8_BLOCK;
+    const int64_t npad = (int64_t)nblk * ORACLE_FP8_BLOCK;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int blk = 0; blk < nblk; ++blk) {
+                const int r0 = blk * ORACLE_FP8_BLOCK;
+                const int r1 = r0 + ORACLE_FP8_BLOCK < N ? r0 + ORACLE_FP8_BLOCK : N;
+                const uint16_t* base = x + b * x_str[0] + h * x_str[1];
+                float amax = 0.0f;
+                for (int r = r0; r < r1; ++r)
+                    for (int d = 0; d < D; ++d) {
+                        const float a = (float)fabs(widen(base + (int64_t)r * x_str[2] + d, dtype));
+                        if (a > amax) amax = a;
+                    }
+                float inv = 0.0f, s = 1.0f;
+                if (amax > 0.0f && isfinite(448.0f / amax)) {
+                    inv = 448.0f / amax;
+                    s = amax / 448.0f;
+                }
+                scales[((int64_t)b * H + h) * nblk + blk] = s;
+                uint8_t* out = codes + (((int64_t)b * H + h) * npad + r0) * D;
+                for (int r = r0; r < r0 + ORACLE_FP8_BLOCK; ++r)
+                    for (int d = 0; d < D; ++d) {
+                        uint8_t c = 0;
+                        if (r < r1) {
+                            float y = (float)widen(base + (int64_t)r * x_str[2] + d, dtype) * inv;
+                            if (y > 448.0f) y = 448.0f;
+                            if (y < -448.0f) y = -448.0f;
+                            c = e4m3_encode(y);
+                        }
+                        out[(int64_t)(r - r0) * D + d] = c;
+                    }
+            }
+    return 0;
+}
+
+/* Dequantised [B, H, Npad, D] doubles of a quantised tensor. */
+static double* fp8_dequantize(const uint8_t* codes, const float* scales, int B, int H, int N, int D) {
+    const int nblk = (N + ORACLE_FP8_BLOCK - 1) / ORACLE_FP8_BLOCK;
+    const int64_t npad = (int64_t)nblk * ORACLE_FP8_BLOCK;
+    double* out = (double*)malloc(sizeof(double) * (size_t)((int64_t)B * H * npad * D + 1));
+    if (!out) return NULL;
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh)
+        for (int64_t r = 0; r < npad; ++r) {
+            const double s = scales[bh * nblk + r / ORACLE_FP8_BLOCK];
+            for (int d = 0; d < D; ++d)
+                out[(bh * npad + r) * D + d] = e4m3_value(codes[(bh * npad + r) * D + d]) * s;
+        }
+    return out;
+}
+
+/* One attention row on double inputs (the definition, as attend_row). */
+static double attend_row_f64(const double* qrow, const double* kbase, const double* vbase, int n_keys,
+                             int D, double scale, int mask_kind, int dtype, const void* mask_row,
+                             int64_t mk_str, int64_t causal_limit, double* s, double* out) {
+    double m = -INFINITY;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        const double* krow = kbase + (int64_t)kk * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += qrow[d] * krow[d];
+        double x = scale * dot;
+        if (mask_kind == ORACLE_MASK_BOOL) {
+            if (((const uint8_t*)mask_row)[kk * mk_str] == 0) x = -INFINITY;
+        } else if (mask_kind == ORACLE_MASK_F32) {
+            x += (double)((const float*)mask_row)[kk * mk_str];
+        } else if (mask_kind == ORACLE_MASK_QTYPE) {
+            x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);
+        }
+        if ((int64_t)kk > causal_limit) x = -INFINITY;
+        s[kk] = x;
+        if (x > m) m = x;
+    }
+    if (m == -INFINITY) {
+        for (int d = 0; d < D; ++d) out[d] = 0.0;
+        return -INFINITY;
+    }
+    double l = 0.0;
+    for (int kk = 0; kk < n_keys; ++kk) {
+        s[kk] = exp(s[kk] - m);
+        l += s[kk];
+    }
+    for (int d = 0; d < D; ++d) {
+        double acc = 0.0;
+        for (int kk = 0; kk < n_keys; ++kk) acc += s[kk] * vbase[(int64_t)kk * D + d];
+        out[d] = acc / l;
+    }
+    return m + log(l);
+}
+
+/* The FP8 forward's reference: quantise Q, K, V as above, then exact
+ * attention on the dequantised values.  Arguments and outputs as for
+ * oracle_attn_dense.  Returns 0, or -1 on a bad argument. */
+int oracle_attn_fp8(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                    int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                    const int64_t* q_str, const int64_t* k_str, const int64_t* v_str,
+                    const void* mask, int mask_kind, const int64_t* m_str,
+                    double scale, int causal, const int64_t* rows, int64_t nrows,
+                    double* o, double* lse, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || Nq < 0 || Nkv < 0 || D <= 0) return -1;
+    const int group = Hq / Hkv;
+    const int64_t nqp = (int64_t)((Nq + ORACLE_FP8_BLOCK - 1) / ORACLE_FP8_BLOCK) * ORACLE_FP8_BLOCK;
+    const int64_t nkp = (int64_t)((Nkv + ORACLE_FP8_BLOCK - 1) / ORACLE_FP8_BLOCK) * ORACLE_FP8_BLOCK;
+    uint8_t* cq = (uint8_t*)malloc((size_t)((int64_t)B * Hq * nqp * D + 1));
+    uint8_t* ck = (uint8_t*)malloc((size_t)((int64_t)B * Hkv * nkp * D + 1));
+    uint8_t* cv = (uint8_t*)malloc((size_t)((int64_t)B * Hkv * nkp * D + 1));
+    float* sq = (float*)malloc(sizeof(float) * (size_t)((int64_t)B * Hq * (nqp / ORACLE_FP8_BLOCK) + 1));
+    float* sk = (float*)malloc(sizeof(float) * (size_t)((int64_t)B * Hkv * (nkp / ORACLE_FP8_BLOCK) + 1));
+    float* sv = (float*)malloc(sizeof(float) * (size_t)((int64_t)B * Hkv * (nkp / ORACLE_FP8_BLOCK) + 1));
+    double *dq = NULL, *dk = NULL, *dv = NULL;
+    int err = !cq || !ck || !cv || !sq || !sk || !sv;
+    if (!err)
+        err = oracle_fp8_quantize(q, dtype, B, Hq, Nq, D, q_str, cq, sq) ||
+              oracle_fp8_quantize(k, dtype, B, Hkv, Nkv, D, k_str, ck, sk) ||
+              oracle_fp8_quantize(v, dtype, B, Hkv, Nkv, D, v_str, cv, sv);
+    if (!err) {
+        dq = fp8_dequantize(cq, sq, B, Hq, Nq, D);
+        dk = fp8_dequantize(ck, sk, B, Hkv, Nkv, D);
+        dv = fp8_dequantize(cv, sv, B, Hkv, Nkv, D);
+        err = !dq || !dk || !dv;
+    }
+    const int64_t total = rows ? nrows : (int64_t)B * Hq * Nq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    if (!err) {
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
+            if (!s) {
+#pragma omp atomic write
+                err = 1;
+            }
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < total; ++r) {
+                if (!s) continue;
+                const int64_t flat = rows ? rows[r] : r;
+                const int64_t i = flat % Nq;
+                const int64_t bh = flat / Nq;
+                const int hq = (int)(bh % Hq);
+                const int b = (int)(bh / Hq);
+                const int hk = hq / group;
+                const double* qrow = dq + (((int64_t)b * Hq + hq) * nqp + i) * D;
+                const double* kb = dk + ((int64_t)b * Hkv + hk) * nkp * D;
+                const double* vb = dv + ((int64_t)b * Hkv + hk) * nkp * D;
+                const void* mrow = NULL;
+                int64_t mk = 0;
+                if (mask_kind != ORACLE_MASK_NONE) {
+                    const int64_t off = b * m_str[0] + hq * m_str[1] + i * m_str[2];
+                    const size_t esz = mask_kind == ORACLE_MASK_BOOL ? 1 : mask_kind == ORACLE_MASK_F32 ? 4 : 2;
+                    mrow = (const char*)mask + off * (int64_t)esz;
+                    mk = m_str[3];
+                }
+                const int64_t limit = causal ? i + (int64_t)Nkv - Nq : (int64_t)Nkv - 1;
+                lse[r] = attend_row_f64(qrow, kb, vb, Nkv, D, scale, mask_kind, dtype, mrow, mk, limit, s,
+                                        o + r * D);
+            }
+            free(s);
+        }
+    }
+    free(cq); free(ck); free(cv); free(sq); free(sk); free(sv);
+    free(dq); free(dk); free(dv);
+    return err ? -1 : 0;
+}

@@ -525,4 +525,111 @@ def pin_bwd_varlen_equals_per_sequence(orc):
             _close(dv[c:d], gv[0].transpose(0, 1), what=f"seq {s_} dV causal={causal}")
 
 
+
+
+# ---------------------------------------------------------------- FP8 reference
+# The FP8 forward's reference quantises Q, K and V per (batch, head, block of
+# 128 rows) to e4m3 and attends exactly to the dequantised values (a reading
+# of the FFPA README's FP8 kernels; the quantisation scheme is this build's).
+
+def _e4m3_from_torch(x):
+    """torch's own float8_e4m3fn conversion (nearest-even), after clamping to
+    the finite range as a saturating conversion does."""
+    return x.to(torch.float32).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _e4m3_values():
+    v = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    return v   # index = code; codes 0x7f and 0xff are NaN
+
+
+def pin_e4m3_encoder_matches_torch(orc):
+    """The oracle's e4m3 encoder (its own bit-level rounding) equals torch's
+    float8_e4m3fn conversion bit for bit on every bf16 value in [-448, 448],
+    on every midpoint between neighbouring e4m3 values (the ties), and on
+    random float32 values over the normal and subnormal ranges."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).to(torch.float32)
+    bits = bits[torch.isfinite(bits) & (bits.abs() <= 448)]
+    vals = _e4m3_values()
+    vals = vals[torch.isfinite(vals)].to(torch.float32).unique().sort().values
+    mids = (vals[1:] + vals[:-1]) / 2
+    g = torch.Generator().manual_seed(8)
+    rnd = (torch.rand(200000, generator=g) * 2 - 1) * 448
+    tiny = (torch.rand(50000, generator=g) * 2 - 1) * 2.0 ** -5
+    x = torch.cat([bits, mids, rnd, tiny, torch.tensor([0.0, -0.0, 448.0, -448.0, 500.0, -1e9])])
+    got = orc.e4m3_encode(x)
+    want = _e4m3_from_torch(x)
+    bad = (got != want).nonzero()
+    assert bad.numel() == 0, f"e4m3 code of {x[bad[0, 0]].item()!r}: {int(got[bad[0, 0]])} vs {int(want[bad[0, 0]])}"
+
+
+def pin_fp8_quantizer(orc):
+    """Per 128-row block of each head: the block's largest |x| gets the code of
+    +-448; every value dequantises within e4m3's rounding bound (2^-4 of |x|,
+    or 2^-10 of the scale in the subnormal range); multiplying the input by a
+    power of two multiplies only the scales; a change in one block leaves the
+    others' codes alone; a zero block gives zero codes and scale 1; rows past
+    N are zero."""
+    g = torch.Generator().manual_seed(81)
+    B, H, N, D = 2, 3, 300, 128
+    mag = torch.exp(torch.randn(B, H, 3, 1, 1, generator=g) * 3)       # blocks of very different size
+    x = (torch.randn(B, H, 384, D, generator=g).view(B, H, 3, 128, D) * mag).view(B, H, 384, D)[:, :, :N]
+    x = x.bfloat16().contiguous()
+    x[1, 2, 128:256] = 0                                                  # one zero block
+    codes, s = orc.fp8_quantize(x)
+    assert codes.shape == (B, H, 384, D) and s.shape == (B, H, 3)
+    assert bool((codes[:, :, N:] == 0).all()), "rows past N must be zero"
+    assert bool((codes[1, 2, 128:256] == 0).all()) and s[1, 2, 1].item() == 1.0
+    xf = torch.zeros(B, H, 384, D, dtype=torch.float64)
+    xf[:, :, :N] = x.double()
+    blocks = xf.view(B, H, 3, 128 * D).abs()
+    arg = blocks.argmax(dim=-1)
+    cb = codes.view(B, H, 3, 128 * D)
+    top = torch.gather(cb, -1, arg.unsqueeze(-1)).squeeze(-1)
+    nonzero = blocks.amax(dim=-1) > 0
+    assert bool(((top[nonzero] & 0x7f) == 0x7e).all()), "a block's largest |x| must map to +-448"
+    deq = _e4m3_values()[codes.long()] * s.double().repeat_interleave(128, dim=2).unsqueeze(-1)
+    bound = 2.0 ** -4 * xf.abs() + 2.0 ** -10 * s.double().repeat_interleave(128, dim=2).unsqueeze(-1)
+    err = (deq - xf).abs()
+    assert bool((err <= bound * (1 + 1e-6)).all()), f"dequantisation error {(err - bound).max().item():.3e} over the bound"
+    c8, s8 = orc.fp8_quantize((x.float() * 8).bfloat16())
+    assert torch.equal(c8, codes), "power-of-two scaling must leave the codes alone"
+    assert torch.equal(s8[nonzero], (s * 8)[nonzero]) and bool((s8[~nonzero] == 1).all()), \
+        "power-of-two scaling must multiply the scales (a zero block keeps scale 1)"
+    x2 = x.clone()
+    x2[0, 1, :128] *= 3
+    c2, s2 = orc.fp8_quantize(x2)
+    keep = torch.ones(B, H, 384, dtype=torch.bool)
+    keep[0, 1, :128] = False
+    assert torch.equal(c2[keep], codes[keep]), "blocks must be quantised independently"
+
+
+def pin_fp8_attention_is_attention_of_the_dequantised_inputs(orc):
+    """The FP8 reference equals torch's float64 SDPA applied to the
+    dequantised Q, K, V (bool and additive masks, causal, GQA, cross)."""
+    cases = [
+        ("mha", 1, 2, 2, 70, 90, 128, False, None, None),
+        ("gqa_causal_cross", 2, 4, 2, 130, 260, 128, True, None, 0.3),
+        ("bool_mask", 1, 2, 1, 40, 140, 256, False, "bool", None),
+        ("f32_mask_causal", 1, 2, 2, 60, 60, 128, True, "f32", None),
+    ]
+    vals = _e4m3_values()
+    for name, B, Hq, Hkv, Nq, Nkv, D, causal, mk, scale in cases:
+        q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed=zlib.crc32(name.encode()) % 9973)
+        mask = None
+        if mk == "bool":
+            mask = _bool_mask(g, (B, 1, Nq, Nkv), Nq, Nkv)
+        elif mk == "f32":
+            mask = torch.randn(B, Hq, Nq, Nkv, generator=g)
+        deq = []
+        for t in (q, k, v):
+            c, s = orc.fp8_quantize(t)
+            d = vals[c.long()] * s.double().repeat_interleave(128, dim=2).unsqueeze(-1)
+            deq.append(d[:, :, :t.shape[2]])
+        o, lse = orc.attn_fp8(q, k, v, attn_mask=mask, scale=scale, is_causal=causal)
+        o_ref, lse_ref = _sdpa_reference(*deq, mask, scale, causal)
+        _close(o, o_ref, what=f"fp8 {name}: O")
+        _close(lse, lse_ref, what=f"fp8 {name}: LSE")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -35,6 +35,18 @@ MUTANTS = {
     "fp16_nan_as_inf": ("mag = frac ? NAN : INFINITY;", "mag = INFINITY;"),
     "qtype_mask_ignored": ("x += widen((const uint16_t*)mask_row + kk * mk_str, dtype);", ""),
     "masked_row_nan": ("if (m == -INFINITY) {", "if (0) {"),
+    # FP8 reference
+    "fp8_ties_away": ("double q = nearbyint(ldexp(a, 3 - E));", "double q = floor(ldexp(a, 3 - E) + 0.5);"),
+    "fp8_subnormal_step": ("nearbyint(ldexp(a, 9));", "nearbyint(ldexp(a, 10));"),
+    "fp8_exponent_bias": ("((ex + 7) << 3)", "((ex + 8) << 3)"),
+    "fp8_scale_inverted": ("s = amax / 448.0f;", "s = 448.0f / amax;"),
+    "fp8_no_dequant_scale": ("out[(bh * npad + r) * D + d] = e4m3_value(codes[(bh * npad + r) * D + d]) * s;",
+                             "out[(bh * npad + r) * D + d] = e4m3_value(codes[(bh * npad + r) * D + d]);"),
+    "fp8_mask_ignored": ("lse[r] = attend_row_f64(qrow, kb, vb, Nkv, D, scale, mask_kind, dtype, mrow, mk, limit, s,",
+                         "lse[r] = attend_row_f64(qrow, kb, vb, Nkv, D, scale, ORACLE_MASK_NONE, dtype, mrow, mk, limit, s,"),
+    "fp8_values_from_keys": ("acc += s[kk] * vbase[(int64_t)kk * D + d];", "acc += s[kk] * kbase[(int64_t)kk * D + d];"),
+    "fp8_gqa_modulo": ("const int hk = hq / group;\n                const double* qrow",
+                       "const int hk = hq % Hkv;\n                const double* qrow"),
     # backward
     "bwd_drop_delta": ("double ds = P[kk] * (dP[kk] - delta);", "double ds = P[kk] * dP[kk];"),
     "bwd_delta_sign": ("double ds = P[kk] * (dP[kk] - delta);", "double ds = P[kk] * (dP[kk] + delta);"),
