@@ -27,6 +27,9 @@ from ._binding import (  # noqa: F401
     BWD_NOALLOC_MAX_ROWS,
     ffpa_bwd_varlen,
     ffpa_fwd,
+    ffpa_fwd_fp8,
+    fp8_workspace_bytes,
+    fp8_workspace_views,
     ffpa_fwd_varlen,
     ffpa_last_device_error,
     ffpa_status_string,

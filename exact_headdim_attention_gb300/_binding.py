@@ -24,7 +24,8 @@ FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4
 
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", "ffpa_bwd",
             "ffpa_bwd_ex", "ffpa_bwd_varlen", "ffpa_bwd_varlen_ex", "ffpa_status_string",
-            "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc")
+            "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc",
+            "ffpa_fwd_fp8", "ffpa_fwd_fp8_ex", "ffpa_fwd_fp8_workspace_bytes")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
 
@@ -91,6 +92,13 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
         getattr(lib, name).restype = I
         getattr(lib, name + "_ex").argtypes = args + [O]
         getattr(lib, name + "_ex").restype = I
+    fp8 = sigs["ffpa_fwd"][:-1] + [P, ctypes.c_size_t, P]   # + workspace, bytes, stream
+    lib.ffpa_fwd_fp8.argtypes = fp8
+    lib.ffpa_fwd_fp8.restype = I
+    lib.ffpa_fwd_fp8_ex.argtypes = fp8 + [O]
+    lib.ffpa_fwd_fp8_ex.restype = I
+    lib.ffpa_fwd_fp8_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.ffpa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
     # ffpa_bwd without the delta argument
     lib.ffpa_bwd_noalloc.argtypes = sigs["ffpa_bwd"][:9] + sigs["ffpa_bwd"][10:]
     lib.ffpa_bwd_noalloc.restype = I
@@ -236,6 +244,78 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
     del keep
     if st != FFPA_OK:
         _raise(st, "ffpa_fwd")
+    return (out, lse) if return_lse else out
+
+
+def fp8_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int) -> int:
+    """Bytes of the workspace ffpa_fwd_fp8 needs (0 for an unsupported shape)."""
+    return int(load_library().ffpa_fwd_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+
+
+def fp8_workspace_views(ws: torch.Tensor, B, Hq, Hkv, Nq, Nkv, D):
+    """Views of a uint8 workspace as the layout include/ffpa.h documents for
+    ffpa_fwd_fp8: e4m3 codes of Q [B,Hq,Nqp,D], K [B,Hkv,Nkp,D], V transposed
+    [B,Hkv,D,Nkp] (uint8) and the fp32 block scales of each."""
+    nqb, nkb = (Nq + 127) // 128, (Nkv + 127) // 128
+    nqp, nkp = nqb * 128, nkb * 128
+    shapes = [((B, Hq, nqp, D), torch.uint8), ((B, Hkv, nkp, D), torch.uint8),
+              ((B, Hkv, D, nkp), torch.uint8), ((B, Hq, nqb), torch.float32),
+              ((B, Hkv, nkb), torch.float32), ((B, Hkv, nkb), torch.float32)]
+    out, at = [], 0
+    for shape, dt in shapes:
+        n = math.prod(shape) * (4 if dt == torch.float32 else 1)
+        out.append(ws[at:at + n].view(dt).view(shape))
+        at += (n + 255) // 256 * 256
+    return out
+
+
+def ffpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
+                 dropout_p: float = 0.0, is_causal: bool = False, scale: float | None = None,
+                 enable_gqa: bool = False, *, return_lse: bool = False, out=None, lse=None,
+                 workspace=None, stream=None, status=None, wait_timeout_ns=None,
+                 test_drop_first_copy=False):
+    """FP8 (e4m3) attention forward through the C ABI ``ffpa_fwd_fp8_ex``.
+
+    Arguments as ffpa_fwd (bf16/fp16 in and out); D a multiple of 128.
+    workspace: a uint8 device tensor of at least fp8_workspace_bytes(...)
+    bytes (allocated here when None); after the call it holds the e4m3
+    codes and scales (fp8_workspace_views)."""
+    if dropout_p != 0.0:
+        raise NotImplementedError("dropout is not supported by this forward kernel")
+    lib = load_library()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, H, N, D]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    B, Hq, Nq, D = q.shape
+    Bk, Hkv, Nkv, Dk = k.shape
+    if tuple(v.shape) != (Bk, Hkv, Nkv, Dk) or Bk != B or Dk != D:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    else:
+        _check_buffer(out, "out", q.shape, q.dtype, q.device)
+    if return_lse and lse is None:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_buffer(lse, "lse", (B, Hq, Nq), torch.float32, q.device, contiguous=True)
+    need = int(lib.ffpa_fwd_fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    elif workspace.dtype != torch.uint8 or workspace.dim() != 1 or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous 1-D uint8 tensor")
+    mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
+    sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
+    opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
+    st = lib.ffpa_fwd_fp8_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             None if lse is None else lse.data_ptr(), _dtype_code(q),
+                             B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v),
+                             _strides(out), mptr, mk, mstr, sc, int(bool(is_causal)),
+                             int(bool(enable_gqa)), workspace.data_ptr(),
+                             workspace.numel(), _stream_handle(stream, q), opts)
+    del keep
+    if st != FFPA_OK:
+        _raise(st, "ffpa_fwd_fp8")
     return (out, lse) if return_lse else out
 
 

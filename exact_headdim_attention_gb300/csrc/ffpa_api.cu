@@ -291,6 +291,34 @@ size_t plan_split(int D, Params* P) {
   return 1024 + fixed + ns * SLOT_BYTES;
 }
 
+// FP8 workspace: e4m3 Q [B,Hq,Nqp,D], K [B,Hkv,Nkp,D], transposed V
+// [B,Hkv,D,Nkp] and the fp32 block scales of each (N rounded up to 128 in
+// Nqp / Nkp); every part 256-byte aligned.
+struct Fp8Layout {
+  size_t off[6];   // q8, k8, v8t, sq, sk, sv
+  size_t total;
+  int64_t nqp, nkp;
+  int nqb, nkb;
+};
+
+Fp8Layout fp8_layout(int B, int Hq, int Hkv, int Nq, int Nkv, int D) {
+  Fp8Layout L{};
+  L.nqb = (Nq + 127) / 128;
+  L.nkb = (Nkv + 127) / 128;
+  L.nqp = (int64_t)L.nqb * 128;
+  L.nkp = (int64_t)L.nkb * 128;
+  const size_t sizes[6] = {(size_t)B * Hq * L.nqp * D, (size_t)B * Hkv * L.nkp * D,
+                           (size_t)B * Hkv * L.nkp * D, (size_t)B * Hq * L.nqb * 4,
+                           (size_t)B * Hkv * L.nkb * 4, (size_t)B * Hkv * L.nkb * 4};
+  size_t at = 0;
+  for (int i = 0; i < 6; ++i) {
+    L.off[i] = at;
+    at += (sizes[i] + 255) & ~(size_t)255;
+  }
+  L.total = at;
+  return L;
+}
+
 // Pair-kernel plan: K stages of 64 keys x kc chunks, V stages of 128 keys x
 // half the slice's columns, Q resident; returns the dynamic smem bytes.
 size_t plan_pair(int D, Params* P) {
@@ -967,6 +995,162 @@ ffpa_status ffpa_fwd_varlen(const void* q, const void* k, const void* v, void* o
   return ffpa_fwd_varlen_ex(q, k, v, o, lse, dt, Tq, Tk, Hq, Hkv, D, q_str, k_str, v_str, o_str,
                             cu_seqlens_q, cu_seqlens_k, nseq, max_seqlen_q, max_seqlen_k, scale,
                             causal, enable_gqa, stream, nullptr);
+}
+
+size_t ffpa_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D) {
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0 || D < 128 || D > 1024 || D % 128 != 0)
+    return 0;
+  return fp8_layout(B, Hq, Hkv, Nq, Nkv, D).total;
+}
+
+ffpa_status ffpa_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                            const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                            const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                            const int64_t mask_str[4], const float* scale, int is_causal,
+                            int enable_gqa, void* workspace, size_t workspace_bytes,
+                            ffpa_stream_t stream, const ffpa_options* options) {
+  if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
+  if (D < 128 || D > 1024 || D % 128 != 0) return FFPA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0) return FFPA_ERR_INVALID;
+  if (Hq != Hkv && !enable_gqa) return FFPA_ERR_INVALID;
+  if (is_causal && Nkv < Nq) return FFPA_ERR_INVALID;
+  if (mask_kind < FFPA_MASK_NONE || mask_kind > FFPA_MASK_ADD_QTYPE) return FFPA_ERR_INVALID;
+  CallOpts opt;
+  if (read_opts(options, &opt) != FFPA_OK) return FFPA_ERR_INVALID;
+  const float sc = scale ? *scale : 1.0f / std::sqrt(static_cast<float>(D));
+  if (!std::isfinite(sc)) return FFPA_ERR_INVALID;
+  if (B == 0 || Nq == 0) return FFPA_OK;          // nothing to read or write
+  if (!q || !o || !q_str || !k_str || !v_str || !o_str) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!k || !v)) return FFPA_ERR_INVALID;
+  const bool umask = mask_kind != FFPA_MASK_NONE && Nkv > 0;
+  if (umask) {
+    if (!mask || !mask_str) return FFPA_ERR_INVALID;
+    for (int i = 0; i < 4; ++i)
+      if (mask_str[i] < 0) return FFPA_ERR_INVALID;
+    if (!aligned_to(mask, mask_esz(mask_kind))) return FFPA_ERR_INVALID;
+  }
+  const int64_t qsz[4] = {B, Hq, Nq, D}, ksz[4] = {B, Hkv, Nkv, D};
+  if (!strides_ok(q_str, qsz, 4) || !strides_ok(o_str, qsz, 4)) return FFPA_ERR_INVALID;
+  if (Nkv > 0 && (!strides_ok(k_str, ksz, 4) || !strides_ok(v_str, ksz, 4))) return FFPA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(o) || (Nkv > 0 && (!aligned16(k) || !aligned16(v))))
+    return FFPA_ERR_INVALID;
+  if (lse && !aligned_to(lse, 4)) return FFPA_ERR_INVALID;
+  const Fp8Layout L = fp8_layout(B, Hq, Hkv, Nq, Nkv, D);
+  if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < L.total) return FFPA_ERR_INVALID;
+  int dev = 0;
+  ffpa_status st = check_devices({q, o, Nkv > 0 ? k : nullptr, Nkv > 0 ? v : nullptr, lse,
+                                  umask ? mask : nullptr, workspace},
+                                 &dev);
+  if (st != FFPA_OK) return st;
+  DeviceScope scope(dev);
+  if (!scope.ok()) return FFPA_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_status_word(dev, opt, &err)) != FFPA_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8Quant Z{};
+  const void* srcs[3] = {q, k, v};
+  const int64_t* strs[3] = {q_str, k_str, v_str};
+  const int Hs[3] = {Hq, Hkv, Hkv}, Ns[3] = {Nq, Nkv, Nkv};
+  long long ctas = 0;
+  for (int t = 0; t < 3; ++t) {
+    Z.src[t] = srcs[t];
+    for (int i = 0; i < 4; ++i) Z.str[t][i] = strs[t][i];
+    Z.codes[t] = ws + L.off[t];
+    Z.scales[t] = reinterpret_cast<float*>(ws + L.off[3 + t]);
+    Z.H[t] = Hs[t];
+    Z.N[t] = Ns[t];
+    Z.npad[t] = static_cast<int>(t == 0 ? L.nqp : L.nkp);
+    Z.nblk[t] = t == 0 ? L.nqb : L.nkb;
+    ctas += (long long)B * Hs[t] * Z.nblk[t];
+    Z.cta_end[t] = ctas;
+  }
+  Z.B = B;
+  Z.D = D;
+  Z.fp16 = dt == FFPA_FP16;
+  if (ctas > 0x7fffffffLL) return FFPA_ERR_INVALID;
+
+  Params P{};
+  P.nchunks = D / DK;                        // 64-column units: output slices
+  P.n_slices = (D + DV_MAX - 1) / DV_MAX;
+  int dv_max = 0;
+  for (int sl = 0; sl < P.n_slices; ++sl) {
+    const int w = ((sl + 1) * P.nchunks / P.n_slices - sl * P.nchunks / P.n_slices) * DK;
+    dv_max = w > dv_max ? w : dv_max;
+  }
+  const int nch8 = D / 128;
+  const bool qres = nch8 <= 4;
+  const size_t q_region = qres ? (size_t)((nch8 + 1) / 2) * SLOT_BYTES : 0;
+  P.vslot = dv_max * 128;
+  P.nslot_v = NSLOT_V_MAX;
+  size_t ns = (SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region - (size_t)P.nslot_v * P.vslot) / SLOT_BYTES;
+  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+  if (ns < 2) return FFPA_ERR_UNSUPPORTED;
+  P.nslot = static_cast<int>(ns);
+  const size_t smem = 1024 + q_region + ns * SLOT_BYTES + (size_t)P.nslot_v * P.vslot;
+  const uint32_t box_ch = nch8 >= 2 ? 2u : 1u;
+  {
+    const uint64_t dq[5] = {128, (uint64_t)L.nqp, (uint64_t)nch8, (uint64_t)Hq, (uint64_t)B};
+    const uint64_t sq[4] = {(uint64_t)D, 128, (uint64_t)(L.nqp * D), (uint64_t)(Hq * L.nqp * D)};
+    const uint32_t bq[5] = {128, BM, box_ch, 1, 1};
+    if ((st = encode_map(&P.tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, ws + L.off[0], dq, sq, bq)) != FFPA_OK)
+      return st;
+  }
+  if (Nkv > 0) {
+    const uint64_t dk[5] = {128, (uint64_t)L.nkp, (uint64_t)nch8, (uint64_t)Hkv, (uint64_t)B};
+    const uint64_t sk[4] = {(uint64_t)D, 128, (uint64_t)(L.nkp * D), (uint64_t)(Hkv * L.nkp * D)};
+    const uint32_t bk[5] = {128, BN, box_ch, 1, 1};
+    if ((st = encode_map(&P.tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, ws + L.off[1], dk, sk, bk)) != FFPA_OK)
+      return st;
+    const uint64_t dv4[4] = {(uint64_t)L.nkp, (uint64_t)D, (uint64_t)Hkv, (uint64_t)B};
+    const uint64_t sv[3] = {(uint64_t)L.nkp, (uint64_t)(D * L.nkp), (uint64_t)(Hkv * D * L.nkp)};
+    const uint32_t bv[4] = {128, (uint32_t)dv_max, 1, 1};
+    if ((st = encode_map(&P.tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, ws + L.off[2], dv4, sv, bv)) != FFPA_OK)
+      return st;
+  }
+  P.o = o;
+  P.lse = lse;
+  P.mask = umask ? mask : nullptr;
+  P.mask_kind = umask ? mask_kind : FFPA_MASK_NONE;
+  for (int i = 0; i < 4; ++i) {
+    P.o_str[i] = o_str[i];
+    P.m_str[i] = umask ? mask_str[i] : 0;
+  }
+  P.B = B;
+  P.Hq = Hq;
+  P.group = Hq / Hkv;
+  P.Nq = Nq;
+  P.Nkv = Nkv;
+  P.D = D;
+  P.n_qt = L.nqb;
+  P.n_kb = L.nkb;
+  P.sq = reinterpret_cast<const float*>(ws + L.off[3]);
+  P.sk = reinterpret_cast<const float*>(ws + L.off[4]);
+  P.sv = reinterpret_cast<const float*>(ws + L.off[5]);
+  P.scale_log2 = sc * 1.4426950408889634f;
+  P.causal = is_causal ? 1 : 0;
+  P.fp16 = dt == FFPA_FP16;
+  P.inject = opt.drop;
+  P.timeout_ns = opt.timeout_ns;
+  P.err = err;
+  P.device = dev;
+  const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
+  if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  return launch_fp8(Z, P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                         ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                         const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                         const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                         const int64_t mask_str[4], const float* scale, int is_causal,
+                         int enable_gqa, void* workspace, size_t workspace_bytes,
+                         ffpa_stream_t stream) {
+  return ffpa_fwd_fp8_ex(q, k, v, o, lse, dt, B, Hq, Hkv, Nq, Nkv, D, q_str, k_str, v_str, o_str,
+                         mask, mask_kind, mask_str, scale, is_causal, enable_gqa, workspace,
+                         workspace_bytes, stream, nullptr);
 }
 
 }  // extern "C"

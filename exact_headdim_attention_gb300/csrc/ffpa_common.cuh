@@ -81,6 +81,18 @@ ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, s
 ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_cluster(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
+// FP8 forward: the quantisation of Q, K, V into the workspace, then the
+// e4m3 attention kernel (ffpa_fp8.cu).
+struct Fp8Quant {
+  const void* src[3];                          // q, k, v (16-bit)
+  int64_t str[3][4];                           // element strides (b, h, n, d)
+  uint8_t* codes[3];                           // q8, k8 [B,H,Npad,D]; v8t [B,H,D,Npad]
+  float* scales[3];                            // [B, H, Npad / 128]
+  int H[3], N[3], npad[3], nblk[3];
+  long long cta_end[3];                        // cumulative CTA counts of q, k, v
+  int B, D, fp16;
+};
+ffpa_status launch_fp8(const Fp8Quant& Qz, const Params& P, int items, size_t smem, cudaStream_t stream);
 // Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on `device`,
 // once per (kernel, device) pair; later calls only look the pair up.
 ffpa_status set_smem_attr_once(const void* fn, int device, int bytes);
@@ -183,6 +195,12 @@ struct Params {
   unsigned long long timeout_ns;
   int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
   int device;   // host only: the device the launch goes to
+  // FP8 forward: e4m3 block scales (per batch, head, 128-row block) of Q, K
+  // and V in the caller's workspace; n_kb key blocks per head.
+  const float* sq;
+  const float* sk;
+  const float* sv;
+  int n_kb;
 };
 
 struct Item {
@@ -370,12 +388,14 @@ __device__ __forceinline__ void apply_mask32(float* x, int key0, int kv_len, boo
 // Epilogue of one row: O (TMEM columns [0, it.dv), or zeros when no key
 // tile was visited) scaled by 1/l, written as 16-bit values to the output
 // columns [it.col_lo, it.col_lo + it.dv); the LSE by the CTA of slice 0.
+// o_scale multiplies the accumulator on top of 1/l (the FP8 kernel's P
+// carries a per-tile factor; 1 elsewhere).
 template <bool VARLEN>
 __device__ __forceinline__ void store_output(const Params& p, const Item& it, bool have_o,
                                              uint32_t lane_base, int row, bool row_valid,
-                                             float l_sum, float m_ref) {
+                                             float l_sum, float m_ref, float o_scale = 1.f) {
   const bool fp16 = p.fp16 != 0;
-  const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+  const float inv_l = l_sum > 0.f ? o_scale / l_sum : 0.f;
   uint8_t* obase = nullptr;
   if (row_valid) {
     long long off;

@@ -57,6 +57,7 @@
 #ifndef FFPA_H_
 #define FFPA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -198,6 +199,50 @@ ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void
                                const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
                                int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
                                int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
+
+/*
+ * FP8 forward (FFPA README, "Backends" and "Latest News": FP8 attention
+ * kernels for large head dims that take bf16/fp16 tensors and return the
+ * input type, with the quantisation scales folded into the computation).
+ * Same arguments, layouts and checks as ffpa_fwd, plus a caller workspace;
+ * the result approximates ffpa_fwd's within the e4m3 error bound.
+ *
+ * Computation (the pages give no quantisation formula; this is the
+ * library's reading): Q, K and V are quantised per (batch, head, block of
+ * 128 rows) to e4m3 with scale s = amax / 448 (codes = e4m3(x * 448 / amax),
+ * nearest-even, saturated; a zero block gets s = 1), written into the
+ * workspace; the attention then runs on the e4m3 tensor cores with s_q s_k
+ * folded into each score tile's scale and the V block scale folded into P,
+ * which is itself rounded to e4m3.  LSE is that of the scores of the
+ * dequantised Q and K.
+ *
+ *   D: 128..1024, a multiple of 128 (else FFPA_ERR_UNSUPPORTED).
+ *   workspace: device memory on q's GPU, 256-byte aligned, at least
+ *     ffpa_fwd_fp8_workspace_bytes(...) bytes (else FFPA_ERR_INVALID),
+ *     owned by the caller and not read before it is written.  Layout, with
+ *     Nqp, Nkp = Nq, Nkv rounded up to 128 and each part starting at the
+ *     next multiple of 256 bytes: e4m3 Q [B,Hq,Nqp,D], e4m3 K [B,Hkv,Nkp,D],
+ *     e4m3 V transposed [B,Hkv,D,Nkp], then fp32 scales of Q [B,Hq,Nqp/128],
+ *     of K and of V [B,Hkv,Nkp/128].  Rows past N are zero.
+ *   Inputs must be finite.  Two launches on `stream` (quantisation,
+ *   attention); no allocation, no synchronisation.
+ */
+size_t ffpa_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+ffpa_status ffpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                         ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                         const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                         const int64_t o_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                         const int64_t mask_str[4], const float* scale, int is_causal,
+                         int enable_gqa, void* workspace, size_t workspace_bytes,
+                         ffpa_stream_t stream);
+ffpa_status ffpa_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                            ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                            const int64_t q_str[4], const int64_t k_str[4],
+                            const int64_t v_str[4], const int64_t o_str[4], const void* mask,
+                            ffpa_mask_kind mask_kind, const int64_t mask_str[4],
+                            const float* scale, int is_causal, int enable_gqa, void* workspace,
+                            size_t workspace_bytes, ffpa_stream_t stream,
+                            const ffpa_options* options);
 
 /*
  * Backward of ffpa_fwd (dense layout): the gradients dq, dk, dv

@@ -27,7 +27,7 @@ def lib():
 
 def declared_symbols():
     text = (ROOT / "include" / "ffpa.h").read_text()
-    return sorted(set(re.findall(r"\b(ffpa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ffpa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():
@@ -37,7 +37,7 @@ def test_header_declares_the_abi():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", str(pkg.lib_path())], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (ffpa_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (ffpa_[a-z0-9_]+)\b", out))
     for name in declared_symbols():
         assert name in exported, f"{name} not exported"
         assert getattr(lib, name) is not None
