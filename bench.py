@@ -44,6 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attn fwd TFLOPS (bf16, D=512) and % of GB300 dense BF16 peak; oracle CPU s"
+METRIC_FP8 = "attn fwd TFLOPS (e4m3 FP8 forward incl. quantisation, D=512) and % of GB300 dense FP8 peak"
 FALLBACK_BF16_TFLOPS = 1900.0      # profiling recipe fallback (one earlier GB300 measurement)
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
@@ -60,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--precision", choices=("bf16", "fp8"), default="bf16",
+                    help="bf16 (default): the 16-bit forward; fp8: the e4m3 forward "
+                         "(quantisation + attention, ffpa_fwd_fp8) on the same bf16 inputs")
     ap.add_argument("--pass", dest="which", choices=("fwd", "bwd"), default="fwd",
                     help="forward (default) or backward step")
     return ap.parse_args(argv)
@@ -175,7 +179,7 @@ def gpu_id_for(device_index: int) -> str:
 
 
 # --------------------------------------------------------------- our arm
-def make_step(w, x, dev):
+def make_step(w, x, dev, fp8=False):
     """Returns (device_step, e2e_step, e2e_start, e2e_finish, bytes_h2d, bytes_d2h, flops).
 
     device_step: one forward on device-resident inputs (torch's current stream).
@@ -197,8 +201,19 @@ def make_step(w, x, dev):
     cq = x["cu_q"].to(dev) if w.varlen else None
     flops = wl.useful_flops(w, x["seqlens"]) if w.varlen else wl.useful_flops(w)
 
-    def forward(ins, out, lse, stream=None):
+    ws = [None, None]
+    if fp8:
         if w.varlen:
+            raise SystemExit("--precision fp8 takes a dense workload")
+        nbytes = pkg.fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.Nq, w.Nkv, w.D)
+        ws = [torch.empty(nbytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def forward(ins, out, lse, stream=None):
+        if fp8:
+            pkg.ffpa_fwd_fp8(ins["q"], ins["k"], ins["v"], attn_mask=mask, is_causal=w.causal,
+                             enable_gqa=w.enable_gqa, out=out, stream=stream,
+                             workspace=ws[0] if out is outs_ref[0] else ws[1])
+        elif w.varlen:
             pkg.ffpa_fwd_varlen(ins["q"], ins["k"], ins["v"], cq, None, x["max_q"], x["max_k"],
                                 causal=w.causal, enable_gqa=w.enable_gqa, return_lse=True,
                                 out=out, lse=lse, stream=stream)
@@ -212,6 +227,7 @@ def make_step(w, x, dev):
 
     out = torch.empty_like(devt["q"])
     lse = new_lse()
+    outs_ref = [out]
 
     def call():
         forward(devt, out, lse)
@@ -334,35 +350,44 @@ def oracle_tiny_one_core():
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, x, target_s: float):
-    """The float64 oracle on a bounded seeded sample of rows of the workload."""
+def cpu_baseline(w, x, target_s: float, fp8: bool = False):
+    """The float64 oracle (its FP8 reference with fp8) on a bounded seeded
+    sample of rows of the workload."""
     import torch
     import oracle
     cores = oracle.host_threads()
     orc = oracle.default()
+    attn = orc.attn_fp8 if fp8 else orc.attn_dense
     if w.varlen:
         raise SystemExit("cpu baseline for varlen workloads: use the dense workloads")
     per_row = 4.0 * w.Nkv * w.D / (2.0 if w.causal else 1.0)
     total_rows = w.B * w.Hq * w.Nq
     g = torch.Generator().manual_seed(w.seed + 17)
-    n = cores
-    rows = torch.randint(0, total_rows, (n,), generator=g)
-    t0 = time.perf_counter()
-    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=rows,
-                   nthreads=cores)
-    dt = max(time.perf_counter() - t0, 1e-6)
-    n = int(min(total_rows, max(cores, n * target_s / dt)))
+
+    def timed(n):
+        rows = torch.randint(0, total_rows, (n,), generator=g)
+        t0 = time.perf_counter()
+        attn(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=rows,
+             nthreads=cores)
+        return max(time.perf_counter() - t0, 1e-6)
+
+    # two calibration sizes separate the per-call cost (the FP8 reference quantises
+    # all of Q, K and V first) from the per-row cost
+    timed(cores)                                  # first call: library and thread start-up
+    n1, n2 = cores, 4 * cores
+    t1, t2 = timed(n1), timed(n2)
+    per_row_s = max((t2 - t1) / (n2 - n1), 1e-9)
+    fixed_s = max(t1 - n1 * per_row_s, 0.0)
+    n = int(min(total_rows, max(cores, max(target_s - fixed_s, 0.5 * target_s) / per_row_s)))
     n = max(cores, (n // cores) * cores)
-    rows = torch.randint(0, total_rows, (n,), generator=g)
-    t0 = time.perf_counter()
-    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=rows,
-                   nthreads=cores)
-    dt = time.perf_counter() - t0
+    dt = timed(n)
     flops = per_row * n
+    full_s = fixed_s + (dt - fixed_s) * total_rows / n
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
             "sample": f"{n} seeded random query rows of {total_rows} (all {w.Nkv} keys each), "
-                      f"{dt:.1f} s; full workload would take ~{dt * total_rows / n:.0f} s",
-            "seconds": dt, "rows": n, "cpu_model": cpu_model(),
+                      f"{dt:.1f} s; full workload would take ~{full_s:.0f} s",
+            "seconds": dt, "rows": n, "full_workload_s": round(full_s, 1),
+            "cpu_model": cpu_model(),
             "tiny_d320_one_core_s": round(oracle_tiny_one_core(), 4)}
 
 
@@ -383,7 +408,8 @@ def run_ours(args):
     pkg.load_library()
     w = workload_by_name(args.workload)
     x = wl.materialize(w)
-    step, e2e, e2e_start, e2e_finish, h2d, d2h, flops = make_step(w, x, dev)
+    fp8 = args.precision == "fp8"
+    step, e2e, e2e_start, e2e_finish, h2d, d2h, flops = make_step(w, x, dev, fp8=fp8)
     assert args.warmup >= 3, "at least 3 warm-up steps"
     for _ in range(args.warmup):
         step()
@@ -408,18 +434,25 @@ def run_ours(args):
     if st != pkg.FFPA_OK:
         raise SystemExit(f"device error: {pkg.ffpa_status_string(st)}")
     peak, peak_src, peak_sustained = read_peaks()
-    kname = pkg.selected_kernel(w.D, w.varlen)
+    if fp8:
+        # e4m3 contraction: the bf16 figure times the nominal dense ratio (4.5 / 2.25 PFLOP/s)
+        peak, peak_src = 2.0 * peak, peak_src + " x 2 (nominal e4m3 / bf16 dense ratio)"
+        peak_sustained = 2.0 * peak_sustained if peak_sustained else None
+    kname = "fp8" if fp8 else pkg.selected_kernel(w.D, w.varlen)
     vl, um = str(w.varlen).lower(), str(x.get("mask") is not None).lower()
-    kernel = {"single": f"ffpa_fwd_kernel<{vl}, {um}>",
+    kernel = {"fp8": f"ffpa_fp8_quant_kernel + ffpa_fwd_fp8_kernel<{w.D // 128}, {um}>",
+              "single": f"ffpa_fwd_kernel<{vl}, {um}>",
               "pair": f"ffpa_fwd_pair_kernel<{vl}, {w.D // 64}, {um}>",
               "split": (f"ffpa_fwd_split_kernel<{vl}, {w.D // 64}, {um}>" if w.D <= 512 else
                         f"ffpa_fwd_cluster_kernel<{vl}, {w.D // 64}, {um}, {w.D // 256}>")}[kname]
     per_launch_s = elapsed / args.steps
     achieved = flops / per_launch_s / 1e12
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC_FP8 if fp8 else METRIC, "value": round(value, 2), "unit": "TFLOPS",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tmax / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (bf16 in and out)" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shapes of the pages' workloads)",
         "config": config_of(w, flops),
         "pct_of_peak": round(100.0 * achieved / peak, 2),
@@ -431,17 +464,20 @@ def run_ours(args):
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                "api": "exact_headdim_attention_gb300.ffpa_fwd (C ABI ffpa_fwd)",
+                "api": ("exact_headdim_attention_gb300.ffpa_fwd_fp8 (C ABI ffpa_fwd_fp8)" if fp8
+                        else "exact_headdim_attention_gb300.ffpa_fwd (C ABI ffpa_fwd)"),
                 "pipelining": "copy-in, forward and copy-out of consecutive steps on three "
                               "streams with two buffer sets"},
-        "gpu_launches": args.steps,
+        "gpu_launches": (2 if fp8 else 1) * args.steps,
         "clocks": clocks,
         "impl": "ours",
     }
+    if fp8:
+        line["roofline"]["note"] = ("one step = two launches (quantisation, then attention); "
+                                    "achieved = the step's useful flops over the step time")
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not w.varlen:
-        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
-        line["oracle_cpu_s_full_workload_est"] = round(
-            line["cpu_baseline"]["seconds"] * (w.B * w.Hq * w.Nq) / line["cpu_baseline"]["rows"], 1)
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds, fp8=fp8)
+        line["oracle_cpu_s_full_workload_est"] = line["cpu_baseline"]["full_workload_s"]
     traffic = measured_traffic(w.name)
     if traffic is not None:
         line["roofline"]["traffic"] = traffic
@@ -695,7 +731,10 @@ def run_reference(args):
     per_row = 4.0 * w.Nkv * w.D / (2.0 if w.causal else 1.0)
     total_rows = w.B * w.Hq * w.Nq
     g = torch.Generator().manual_seed(w.seed + 29)
-    # size each step so that warm-up + steps take about 90 s
+    # size each step so that warm-up + steps take about 90 s (the first call, which
+    # loads the library and starts its threads, stays out of the probe)
+    orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal,
+                   rows=torch.zeros(1, dtype=torch.int64), nthreads=cores)
     probe = torch.randint(0, total_rows, (cores,), generator=g)
     t0 = time.perf_counter()
     orc.attn_dense(x["q"], x["k"], x["v"], attn_mask=x.get("mask"), is_causal=w.causal, rows=probe,
