@@ -439,9 +439,12 @@ def run_ours(args):
         peak, peak_src = 2.0 * peak, peak_src + " x 2 (nominal e4m3 / bf16 dense ratio)"
         peak_sustained = 2.0 * peak_sustained if peak_sustained else None
     kname = "fp8" if fp8 else pkg.selected_kernel(w.D, w.varlen)
+    if kname == "dual" and x.get("mask") is not None:
+        kname = "single"   # the dual-tile kernel takes no mask
     vl, um = str(w.varlen).lower(), str(x.get("mask") is not None).lower()
     kernel = {"fp8": f"ffpa_fp8_quant_kernel + ffpa_fwd_fp8_kernel<{w.D // 128}, {um}>",
               "single": f"ffpa_fwd_kernel<{vl}, {um}>",
+              "dual": f"ffpa_fwd_dual_kernel<{w.D // 64}>",
               "pair": f"ffpa_fwd_pair_kernel<{vl}, {w.D // 64}, {um}>",
               "split": (f"ffpa_fwd_split_kernel<{vl}, {w.D // 64}, {um}>" if w.D <= 512 else
                         f"ffpa_fwd_cluster_kernel<{vl}, {w.D // 64}, {um}, {w.D // 256}>")}[kname]

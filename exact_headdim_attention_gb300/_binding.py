@@ -27,7 +27,7 @@ EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", 
             "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc",
             "ffpa_fwd_fp8", "ffpa_fwd_fp8_ex", "ffpa_fwd_fp8_workspace_bytes")
 
-KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3}
+KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3, "dual": 4}
 
 _lib = None
 
@@ -209,7 +209,7 @@ def ffpa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
     ``ffpa_attn.ffpa_attn_func``.
 
     Per-call options (ffpa_options): kernel ("auto", "single", "pair",
-    "split"), status (a one-element int32 device tensor that receives
+    "split", "dual"), status (a one-element int32 device tensor that receives
     FFPA_ERR_DEVICE_TIMEOUT if a wait of this call runs out; the caller
     zeroes it), wait_timeout_ns, and the test hook test_drop_first_copy."""
     if kwargs:
@@ -581,7 +581,9 @@ def ffpa_last_device_error(stream=None) -> int:
 
 
 def selected_kernel(D: int, varlen: bool = False, kernel: str = "auto") -> str:
-    """Name of the kernel ("single", "pair" or "split") a call with `kernel` would use for head dim D."""
+    """Name of the kernel ("single", "pair", "split" or "dual") a call with `kernel` would use
+    for head dim D (an unmasked call: with a caller's mask the dual-tile choice runs the
+    single-CTA kernel)."""
     if kernel not in KERNEL_VARIANTS:
         raise ValueError(f"kernel must be one of {sorted(KERNEL_VARIANTS)}, got {kernel!r}")
     v = load_library().ffpa_selected_kernel(int(D), int(bool(varlen)), KERNEL_VARIANTS[kernel])

@@ -39,7 +39,7 @@ ffpa_status read_opts(const ffpa_options* o, CallOpts* c) {
   c->timeout_ns = o && o->wait_timeout_ns ? o->wait_timeout_ns : DEFAULT_TIMEOUT_NS;
   c->kernel = o ? o->kernel : FFPA_VARIANT_AUTO;
   c->drop = o && o->test_drop_first_copy ? 1 : 0;
-  if (c->kernel < FFPA_VARIANT_AUTO || c->kernel > FFPA_VARIANT_SPLIT) return FFPA_ERR_INVALID;
+  if (c->kernel < FFPA_VARIANT_AUTO || c->kernel > FFPA_VARIANT_DUAL) return FFPA_ERR_INVALID;
   return FFPA_OK;
 }
 
@@ -229,7 +229,10 @@ bool pair_eligible(int D) {
   return nchunks % kc == 0;
 }
 
-enum class Kern { SINGLE, PAIR, SPLIT };
+enum class Kern { SINGLE, PAIR, SPLIT, DUAL };
+
+// The dual-tile kernel: dense batches, D = 64 or 128 (instantiated shapes).
+bool dual_eligible(int D, bool varlen) { return !varlen && (D == 64 || D == 128); }
 
 // CTAs per cluster of the column-split kernel for head dimension D: each
 // CTA owns D / C output columns, whole 64-column chunks of at most 256
@@ -249,17 +252,39 @@ bool split_eligible(int D) { return split_ways(D) != 0; }
 // Kernel choice, from measurements on GB300 (bf16): from D=384 up the
 // column-split kernel wins on dense, causal and varlen batches (it does not
 // recompute S; D=384: 1048 vs 732 TFLOPS for the single-CTA kernel); at D=256 (no recompute anyway) the pair kernel wins on
-// dense batches; at D=128 the single-CTA kernel's shorter per-tile chain
-// wins, and on packed varlen batches of mixed lengths the 256-row pair
-// tiles waste more rows on short sequences than they save.
+// dense batches; at dense D=64 and D=128 the dual-tile kernel (two query
+// tiles per SM sharing K/V) wins; on packed varlen batches of mixed lengths
+// the 256-row tiles of the pair and dual kernels waste more rows on short
+// sequences than they save, and the single-CTA kernel runs.
 Kern choose_kernel(int D, bool varlen, int v) {
   if (D % DK != 0) return Kern::SINGLE;   // only the single-CTA kernel takes zero-padded chunks
   if (v == FFPA_VARIANT_SINGLE) return Kern::SINGLE;
   if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
   if (v == FFPA_VARIANT_SPLIT) return split_eligible(D) ? Kern::SPLIT : Kern::SINGLE;
+  if (v == FFPA_VARIANT_DUAL) return dual_eligible(D, varlen) ? Kern::DUAL : Kern::SINGLE;
   if (D == 384 || D == 512 || D == 768 || D == 1024) return Kern::SPLIT;
   if (!varlen && D == 256) return Kern::PAIR;
+  if (dual_eligible(D, varlen)) return Kern::DUAL;
   return Kern::SINGLE;
+}
+
+// Dual-tile plan: Q_A and Q_B resident, two P tiles, a ring of one-tile
+// slots (K or V: 128 keys x D); boxes of 128 rows x D/64 chunks.
+size_t plan_dual(int D, Params* P) {
+  P->nchunks = D / DK;
+  P->n_slices = 1;
+  P->kchunks = P->nchunks;
+  P->vchunks = P->nchunks;
+  P->vk = BN;
+  P->vslot = BN * P->vchunks * 128;
+  P->q_res = 1;
+  P->nslot_v = 0;
+  const size_t tile = (size_t)P->nchunks * CHUNK_BYTES;
+  const size_t fixed = 2 * tile + 2 * (size_t)P_TILE_BYTES;
+  size_t ns = (SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - fixed) / tile;
+  if (ns > 8) ns = 8;
+  P->nslot = static_cast<int>(ns);
+  return 1024 + fixed + ns * tile;
 }
 
 // Column-split plan: Q chunks 0..3 in TMEM, the rest resident in shared
@@ -345,6 +370,7 @@ ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size
                           cudaStream_t stream) {
   const bool umask = P.mask != nullptr;
   if (kn == Kern::PAIR) return launch_pair(varlen, umask, P, items, smem, stream);
+  if (kn == Kern::DUAL) return varlen ? FFPA_ERR_UNSUPPORTED : launch_dual(umask, P, items, smem, stream);
   if (kn == Kern::SPLIT)
     return P.split_c == 2 ? launch_split(varlen, umask, P, items, smem, stream)
                           : launch_cluster(varlen, umask, P, items, smem, stream);
@@ -354,6 +380,7 @@ ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size
 size_t plan_for(Kern kn, int D, Params* P) {
   if (kn == Kern::PAIR) return plan_pair(D, P);
   if (kn == Kern::SPLIT) return plan_split(D, P);
+  if (kn == Kern::DUAL) return plan_dual(D, P);
   return plan(D, P);
 }
 
@@ -479,9 +506,12 @@ const char* ffpa_status_string(ffpa_status s) {
 
 int ffpa_selected_kernel(int D, int varlen, int kernel) {
   if (D < 64 || D > 1024 || D % (varlen ? 64 : 8) != 0) return -1;
-  if (kernel < FFPA_VARIANT_AUTO || kernel > FFPA_VARIANT_SPLIT) return -1;
+  if (kernel < FFPA_VARIANT_AUTO || kernel > FFPA_VARIANT_DUAL) return -1;
   const Kern kn = choose_kernel(D, varlen != 0, kernel);
-  return kn == Kern::PAIR ? FFPA_VARIANT_PAIR : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT : FFPA_VARIANT_SINGLE;
+  return kn == Kern::PAIR    ? FFPA_VARIANT_PAIR
+         : kn == Kern::SPLIT ? FFPA_VARIANT_SPLIT
+         : kn == Kern::DUAL  ? FFPA_VARIANT_DUAL
+                             : FFPA_VARIANT_SINGLE;
 }
 
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream) {
@@ -555,7 +585,8 @@ ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   Params P{};
   const CUtensorMapDataType tdt =
       dt == FFPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const Kern kn = choose_kernel(D, false, opt.kernel);
+  Kern kn = choose_kernel(D, false, opt.kernel);
+  if (kn == Kern::DUAL && umask) kn = Kern::SINGLE;   // the dual-tile kernel takes no mask
   const bool pair = kn == Kern::PAIR;
   const size_t smem = plan_for(kn, D, &P);
   const uint32_t k_rows = pair ? BN / 2 : BN;
@@ -608,7 +639,7 @@ ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   P.Nkv = Nkv;
   P.D = D;
   P.Tq = 0;
-  const int q_tile = pair ? BM_PAIR : BM;
+  const int q_tile = (pair || kn == Kern::DUAL) ? 2 * BM : BM;
   P.n_qt = (Nq + q_tile - 1) / q_tile;
   P.scale_log2 = sc * 1.4426950408889634f;
   P.causal = is_causal ? 1 : 0;

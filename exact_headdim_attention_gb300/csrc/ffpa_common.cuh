@@ -81,6 +81,8 @@ ffpa_status launch_single(bool varlen, bool umask, const Params& P, int items, s
 ffpa_status launch_pair(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_split(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 ffpa_status launch_cluster(bool varlen, bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
+// Two 128-row query tiles per CTA sharing every K/V tile (ffpa_dual.cu; dense, D = 64, 128).
+ffpa_status launch_dual(bool umask, const Params& P, int items, size_t smem, cudaStream_t stream);
 // FP8 forward: the quantisation of Q, K, V into the workspace, then the
 // e4m3 attention kernel (ffpa_fp8.cu).
 struct Fp8Quant {
@@ -272,10 +274,13 @@ __device__ __forceinline__ bool decode_item(const Params& p, bool varlen, int L,
 // Bounded wait on an mbarrier phase.  Returns false when this CTA has been
 // told to abort or when the limit expires (then the call's status word *err
 // is set).  `cluster` selects cluster-scope acquire, for phases that another
-// CTA of the cluster completes.
-static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned long long timeout_ns, int* err,
-                                          bool cluster = false) {
+// CTA of the cluster completes.  The inline body serves kernels that change
+// their register budget per warpgroup (an out-of-line function cannot be
+// compiled for two budgets); the others call the out-of-line copy.
+static __device__ __forceinline__ bool wait_bounded_inl(uint32_t bar, uint32_t parity,
+                                                        volatile int* abort_flag,
+                                                        unsigned long long timeout_ns, int* err,
+                                                        bool cluster = false) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     // Suspended waiting keeps idle warps from taking issue slots away from
@@ -294,9 +299,15 @@ static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, 
   }
 }
 
+static __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 unsigned long long timeout_ns, int* err,
+                                                 bool cluster = false) {
+  return wait_bounded_inl(bar, parity, abort_flag, timeout_ns, err, cluster);
+}
+
 // Drain wait used on the way out: ignores the abort flag.
-static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
-                                               int* err) {
+static __device__ __forceinline__ void wait_drain_inl(uint32_t bar, uint32_t parity,
+                                                      unsigned long long timeout_ns, int* err) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) {
@@ -304,6 +315,11 @@ static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, un
       return;
     }
   }
+}
+
+static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long timeout_ns,
+                                               int* err) {
+  wait_drain_inl(bar, parity, timeout_ns, err);
 }
 
 // Masks 32 consecutive scores (log2 domain) of one row: keys past the end,

@@ -84,7 +84,7 @@ typedef enum {
   FFPA_MASK_ADD_QTYPE = 3  /* additive bias in the input dtype (bf16/fp16) */
 } ffpa_mask_kind;
 
-/* Kernel choice (ffpa_options.kernel).  The library has three forward
+/* Kernel choice (ffpa_options.kernel).  The library has four forward
  * kernels with identical results:
  *   - single-CTA: one CTA per 128-row query tile and output slice of at most
  *     256 columns (any D; S is recomputed once per slice);
@@ -93,20 +93,26 @@ typedef enum {
  *   - column split: a cluster of C SMs shares each 128-query tile, each SM
  *     owns D/C output columns, key tiles are dealt round-robin and the P
  *     tiles are exchanged, so S is computed once (C = 2 for D in {128, 256,
- *     384, 512}; C = 3 for D = 768; C = 4 for D = 1024).
+ *     384, 512}; C = 3 for D = 768; C = 4 for D = 1024);
+ *   - dual tile: one SM owns two 128-query tiles of a head, loads each K/V
+ *     tile once for both and overlaps one tile's softmax with the other's
+ *     products (dense batches, D in {64, 128}).
  *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default:
  *                           column split for D in {384, 512, 768, 1024}, CTA
- *                           pair for dense D = 256, single-CTA otherwise)
+ *                           pair for dense D = 256, dual tile for dense
+ *                           D in {64, 128}, single-CTA otherwise)
  *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel
  *   FFPA_VARIANT_PAIR   (2) the CTA-pair kernel wherever D allows it
  *   FFPA_VARIANT_SPLIT  (3) the column-split kernel wherever D allows it
+ *   FFPA_VARIANT_DUAL   (4) the dual-tile kernel wherever D and the layout allow it
  * Where the chosen kernel does not support D, the single-CTA kernel runs.
  * The backward has one kernel set and ignores the choice. */
 enum {
   FFPA_VARIANT_AUTO = 0,
   FFPA_VARIANT_SINGLE = 1,
   FFPA_VARIANT_PAIR = 2,
-  FFPA_VARIANT_SPLIT = 3
+  FFPA_VARIANT_SPLIT = 3,
+  FFPA_VARIANT_DUAL = 4
 };
 
 /* Options of one call (all fields zero = the defaults). */
@@ -376,7 +382,7 @@ const char* ffpa_status_string(ffpa_status status);
 ffpa_status ffpa_last_device_error(ffpa_stream_t stream);
 
 /*
- * The forward kernel (FFPA_VARIANT_SINGLE, _PAIR or _SPLIT) that a call
+ * The forward kernel (FFPA_VARIANT_SINGLE, _PAIR, _SPLIT or _DUAL) that a call
  * with ffpa_options.kernel = `kernel` would run for head dimension D on a
  * dense (varlen = 0) or packed varlen (varlen != 0) batch.  Host only;
  * returns -1 for a head dimension or kernel value the library does not take.

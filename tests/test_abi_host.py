@@ -110,10 +110,11 @@ def test_dense_layout_and_pointer_checks(lib):
 
 
 def test_options_are_checked(lib):
-    """ffpa_options.kernel outside FFPA_VARIANT_AUTO..SPLIT is rejected; the
+    """ffpa_options.kernel outside FFPA_VARIANT_AUTO..DUAL is rejected; the
     defaults (all zero) behave as the plain entry point."""
     bad = pkg.Options(None, 0, 7, 0)
     assert dense_call(lib, options=bad) == pkg.FFPA_ERR_INVALID
+    assert dense_call(lib, options=pkg.Options(None, 0, 5, 0)) == pkg.FFPA_ERR_INVALID
     assert dense_call(lib, options=pkg.Options(None, 0, -1, 0)) == pkg.FFPA_ERR_INVALID
     assert dense_call(lib, options=pkg.Options(None, 0, 0, 0), D=32) == pkg.FFPA_ERR_UNSUPPORTED
     if not torch.cuda.is_available():
@@ -168,7 +169,7 @@ def test_binding_rejects_malformed_cu_seqlens(lib):
 
 
 def test_kernel_variant_names(lib):
-    for name in ("single", "pair", "split", "auto"):
+    for name in ("single", "pair", "split", "dual", "auto"):
         pkg.selected_kernel(512, kernel=name)
     with pytest.raises(ValueError):
         pkg.selected_kernel(512, kernel="fastest")
@@ -197,6 +198,15 @@ def test_selected_kernel_follows_the_choice(lib):
     with pytest.raises(ValueError):
         pkg.selected_kernel(100)                          # not a multiple of 8
     assert pkg.selected_kernel(96) == "single"            # zero-padded to two chunks
+    # dual tile: dense D = 64 and 128 only
+    assert pkg.selected_kernel(64) == "dual"
+    assert pkg.selected_kernel(128) == "dual"
+    assert pkg.selected_kernel(128, varlen=True) == "single"
+    assert pkg.selected_kernel(128, kernel="dual") == "dual"
+    assert pkg.selected_kernel(256, kernel="dual") == "single"
+    assert pkg.selected_kernel(128, kernel="single") == "single"
+    assert pkg.selected_kernel(128, kernel="split") == "split"
+    assert pkg.selected_kernel(120, kernel="dual") == "single"
 
 
 def bwd_call(lib, dt=0, B=1, Hq=2, Hkv=2, Nq=128, Nkv=128, D=64, causal=0, enable_gqa=0,

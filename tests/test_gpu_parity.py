@@ -302,6 +302,32 @@ def test_variant_full_d512_sampled(variant):
     _sampled_dense(wl.headdim_sweep(512), n_random=8, kernel=variant)
 
 
+# ------------------------------------------- dual-tile kernel (dense, D = 64, 128)
+@pytest.mark.parametrize("D", [64, 128])
+def test_dual_dense(D):
+    """Two 128-row query tiles per CTA: ragged blocks (tile B partly or wholly
+    past Nq), GQA, causal with Nkv > Nq, exact blocks, fp16, a negative scale."""
+    dense_case(1, 2, 2, 300, 300, D, seed=D + 11, kernel="dual")        # last block: 44 rows, B empty
+    dense_case(2, 4, 1, 200, 700, D, seed=D + 12, causal=True, kernel="dual")
+    dense_case(1, 2, 2, 65, 129, D, seed=D + 13, causal=True, kernel="dual")
+    dense_case(1, 3, 3, 512, 512, D, seed=D + 14, kernel="dual")
+    dense_case(1, 2, 2, 384, 1000, D, seed=D + 15, causal=True, kernel="dual")
+    dense_case(1, 2, 1, 260, 131, D, seed=D + 16, dtype=torch.float16, kernel="dual")
+    dense_case(1, 2, 2, 257, 1, D, seed=D + 17, kernel="dual")          # one key
+    dense_case(1, 2, 2, 129, 300, D, seed=D + 18, scale=-0.2, kernel="dual")
+
+
+def test_dual_with_mask_runs_single():
+    """A caller's mask at D = 128 with the dual choice: the call runs the
+    single-CTA kernel and is exact."""
+    B, H, Nq, Nk = 2, 2, 270, 300
+    dense_case(B, H, H, Nq, Nk, 128, seed=19, mask=MASKS["bool_b1nk"](B, H, Nq, Nk), kernel="dual")
+
+
+def test_dual_full_d128_sampled():
+    _sampled_dense(wl.headdim_sweep(128), n_random=8, kernel="dual")
+
+
 # ----------------------------------------------------------------- varlen
 @pytest.mark.parametrize("D", [128, 512])
 @pytest.mark.parametrize("causal", [False, True])
@@ -367,6 +393,12 @@ def test_bounded_wait_split_kernel(D):
     loses a copy, the others wait for its tile maxima; all time out."""
     q, k, v, _ = wl.draw_dense(1, 2, 2, 200, 400, D, seed=43)
     _timeout_then_correct(q, k, v, kernel="split")
+
+
+def test_bounded_wait_dual_kernel():
+    """Through the dual-tile kernel: the MMA thread's first K stage never lands."""
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 300, 400, 128, seed=47)
+    _timeout_then_correct(q, k, v, kernel="dual")
 
 
 def test_bounded_wait_fallback_word():
