@@ -234,27 +234,38 @@ enum class Kern { SINGLE, PAIR, SPLIT, DUAL };
 // The dual-tile kernel: dense batches, D = 64 or 128 (instantiated shapes).
 bool dual_eligible(int D, bool varlen) { return !varlen && (D == 64 || D == 128); }
 
-// CTAs per cluster of the column-split kernel for head dimension D: each
-// CTA owns D / C output columns, whole 64-column chunks of at most 256
-// columns (0 = the kernel does not take D).  Instantiated shapes: D = 128,
-// 256, 384, 512 with C = 2; 768 with C = 3; 1024 with C = 4.
+// Column-split kernels for head dimension D (a multiple of 64, 128..1024):
+// the D/64 chunks are rounded up to an instantiated shape (2, 4, 6 or 8
+// chunks on clusters of C = 2 CTAs; 12 on C = 3; 16 on C = 4), each CTA
+// owning an equal share of whole chunks (at most 256 columns).  The chunks
+// past D lie beyond the tensor maps' chunk extent, so the TMA unit reads
+// them as zeros: they add nothing to S, and their output columns are not
+// stored.  0 = the kernels do not take D.
+int split_chunks(int D) {
+  if (D % DK != 0) return 0;
+  const int n = D / DK;
+  if (n < 2) return 0;
+  if (n <= 8) return (n + 1) & ~1;
+  if (n <= 12) return 12;
+  if (n <= 16) return 16;
+  return 0;
+}
+
 int split_ways(int D) {
-  switch (D) {
-    case 128: case 256: case 384: case 512: return 2;
-    case 768: return 3;
-    case 1024: return 4;
-    default: return 0;
-  }
+  const int n = split_chunks(D);
+  return n == 0 ? 0 : n <= 8 ? 2 : n == 12 ? 3 : 4;
 }
 
 bool split_eligible(int D) { return split_ways(D) != 0; }
 
-// Kernel choice, from measurements on GB300 (bf16): from D=384 up the
-// column-split kernel wins on dense, causal and varlen batches (it does not
-// recompute S; D=384: 1048 vs 732 TFLOPS for the single-CTA kernel); at D=256 (no recompute anyway) the pair kernel wins on
-// dense batches; at dense D=64 and D=128 the dual-tile kernel (two query
-// tiles per SM sharing K/V) wins; on packed varlen batches of mixed lengths
-// the 256-row tiles of the pair and dual kernels waste more rows on short
+// Kernel choice, from measurements on GB300 (bf16): above D=256 the
+// column-split kernels win on dense, causal and varlen batches (they do not
+// recompute S; D=384: 1048 vs 732 TFLOPS for the single-CTA kernel, and at
+// D=320 the split padded to 384 columns beats the single-CTA kernel's two
+// slices); at D=256 (no recompute anyway) the pair kernel wins on dense
+// batches; at dense D=64 and D=128 the dual-tile kernel (two query tiles
+// per SM sharing K/V) wins; on packed varlen batches of mixed lengths the
+// 256-row tiles of the pair and dual kernels waste more rows on short
 // sequences than they save, and the single-CTA kernel runs.
 Kern choose_kernel(int D, bool varlen, int v) {
   if (D % DK != 0) return Kern::SINGLE;   // only the single-CTA kernel takes zero-padded chunks
@@ -262,7 +273,7 @@ Kern choose_kernel(int D, bool varlen, int v) {
   if (v == FFPA_VARIANT_PAIR) return pair_eligible(D) ? Kern::PAIR : Kern::SINGLE;
   if (v == FFPA_VARIANT_SPLIT) return split_eligible(D) ? Kern::SPLIT : Kern::SINGLE;
   if (v == FFPA_VARIANT_DUAL) return dual_eligible(D, varlen) ? Kern::DUAL : Kern::SINGLE;
-  if (D == 384 || D == 512 || D == 768 || D == 1024) return Kern::SPLIT;
+  if (D > 256 && split_eligible(D)) return Kern::SPLIT;
   if (!varlen && D == 256) return Kern::PAIR;
   if (dual_eligible(D, varlen)) return Kern::DUAL;
   return Kern::SINGLE;
@@ -293,7 +304,7 @@ size_t plan_dual(int D, Params* P) {
 size_t plan_split(int D, Params* P) {
   const int C = split_ways(D);
   P->split_c = C;
-  P->nchunks = D / DK;
+  P->nchunks = split_chunks(D);
   P->n_slices = 1;
   P->qt_chunks = P->nchunks < Q_TMEM_MAX_CHUNKS ? P->nchunks : Q_TMEM_MAX_CHUNKS;
   P->kchunks = 2;
@@ -591,7 +602,9 @@ ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   const size_t smem = plan_for(kn, D, &P);
   const uint32_t k_rows = pair ? BN / 2 : BN;
   const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
-  const uint64_t nch = (uint64_t)P.nchunks;
+  // The maps span the real D/64 chunks; a column-split plan may run more
+  // (padding chunks, read as zeros past this extent).
+  const uint64_t nch = (uint64_t)(D / DK);
   P.dfine = D % DK != 0;
   if (P.dfine) {
     // (D, N, H, B) views with one 64-column box per chunk: the TMA unit
@@ -968,7 +981,7 @@ ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void
   const size_t smem = plan_for(kn, D, &P);
   const uint32_t k_rows = pair ? BN / 2 : BN;
   const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
-  const uint64_t nch = (uint64_t)P.nchunks;
+  const uint64_t nch = (uint64_t)(D / DK);   // real chunks (see ffpa_fwd_ex)
   {
     const uint64_t dq[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
     const uint64_t sq[3] = {(uint64_t)q_str[0] * 2, 128, (uint64_t)q_str[1] * 2};

@@ -38,7 +38,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
   const uint32_t peer = rank ^ 1u;
   Item it;
   if (!decode_item(p, VARLEN, blockIdx.x >> 1, it)) return;   // same answer in both CTAs
-  it.dv = p.D / 2;
+  it.dv = NCH * DK / 2;                                        // padded D: see split_chunks
   it.col_lo = it.dv * (int)rank;
   it.slice = (int)rank;                                        // rank 0 writes the LSE
 

@@ -91,14 +91,16 @@ typedef enum {
  *   - CTA pair: two SMs share each 256-query tile and each load half of every
  *     K/V tile (D in {128, 256, 512});
  *   - column split: a cluster of C SMs shares each 128-query tile, each SM
- *     owns D/C output columns, key tiles are dealt round-robin and the P
- *     tiles are exchanged, so S is computed once (C = 2 for D in {128, 256,
- *     384, 512}; C = 3 for D = 768; C = 4 for D = 1024);
+ *     owns an equal share of the output columns, key tiles are dealt
+ *     round-robin and the P tiles are exchanged, so S is computed once (D a
+ *     multiple of 64 from 128 to 1024; C = 2 up to D = 512, 3 up to 768, 4
+ *     up to 1024; D is padded with zero columns to 2, 4, 6, 8, 12 or 16
+ *     chunks of 64, which are read as zeros and not stored);
  *   - dual tile: one SM owns two 128-query tiles of a head, loads each K/V
  *     tile once for both and overlaps one tile's softmax with the other's
  *     products (dense batches, D in {64, 128}).
  *   FFPA_VARIANT_AUTO   (0) the fastest one measured for the shape (default:
- *                           column split for D in {384, 512, 768, 1024}, CTA
+ *                           column split for D > 256 (multiples of 64), CTA
  *                           pair for dense D = 256, dual tile for dense
  *                           D in {64, 128}, single-CTA otherwise)
  *   FFPA_VARIANT_SINGLE (1) always the single-CTA kernel

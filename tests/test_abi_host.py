@@ -187,12 +187,17 @@ def test_selected_kernel_follows_the_choice(lib):
     assert pkg.selected_kernel(1024) == "split"                    # cluster of 4 CTAs
     assert pkg.selected_kernel(768) == "split"                     # cluster of 3 CTAs
     assert pkg.selected_kernel(768, varlen=True) == "split"
-    assert pkg.selected_kernel(640) == "single"
+    assert pkg.selected_kernel(640) == "split"                     # padded to 12 chunks, C = 3
+    assert pkg.selected_kernel(320) == "split"                     # padded to 6 chunks, C = 2
+    assert pkg.selected_kernel(320, varlen=True) == "split"
+    assert pkg.selected_kernel(192) == "single"                    # one output slice, S once
+    assert pkg.selected_kernel(192, kernel="split") == "split"
     assert pkg.selected_kernel(1024, kernel="single") == "single"
     assert pkg.selected_kernel(512, kernel="pair") == "pair"
     assert pkg.selected_kernel(384, kernel="pair") == "single"      # pair kernel does not take D=384
     assert pkg.selected_kernel(384, kernel="split") == "split"
-    assert pkg.selected_kernel(640, kernel="split") == "single"
+    assert pkg.selected_kernel(640, kernel="split") == "split"
+    assert pkg.selected_kernel(64, kernel="split") == "single"     # the split needs two chunks
     assert pkg.selected_kernel(512) == "split"                     # no choice outlives a call
     assert lib.ffpa_selected_kernel(100, 0, 0) == -1
     with pytest.raises(ValueError):

@@ -221,10 +221,20 @@ def test_invariant_rows_sum_to_one():
     assert (o.float() - 1).abs().max().item() <= 1e-2
 
 
-def test_invariant_single_key_returns_v():
-    q, k, v, _ = wl.draw_dense(2, 2, 2, 129, 1, 640, seed=32)
-    o, l = run_dense(q, k, v, scale=0.25)
-    assert torch.equal(o.cpu(), v.expand(2, 2, 129, 640))
+@pytest.mark.parametrize("D,kernel", [(640, "single"), (512, "split"), (128, "dual"), (640, "split")])
+def test_invariant_single_key_returns_v(D, kernel):
+    """One key: O = V and LSE = scale q.k.  Exact where the running maximum is
+    the row's own fp32 maximum (P = 1); the clusters of 3 and 4 CTAs (D = 640
+    runs on 3) exchange maxima rounded up to bf16, so P is the bf16 rounding
+    of exp2(x - m) <= 1 and O equals V to within bf16 rounding."""
+    q, k, v, _ = wl.draw_dense(2, 2, 2, 129, 1, D, seed=32)
+    o, l = run_dense(q, k, v, scale=0.25, kernel=kernel)
+    want_o = v.expand(2, 2, 129, D)
+    if pkg.selected_kernel(D, kernel=kernel) == "split" and D > 512:
+        err = (o.cpu().double() - want_o.double()).abs()
+        assert bool((err <= 2.0 ** -7 * want_o.double().abs() + 1e-6).all())
+    else:
+        assert torch.equal(o.cpu(), want_o)
     want = 0.25 * torch.einsum("bhnd,bhd->bhn", q.double(), k[:, :, 0].double())
     assert (l.cpu().double() - want).abs().max().item() <= 1e-3
 
@@ -300,6 +310,36 @@ def test_variant_varlen(variant, D, causal):
 
 def test_variant_full_d512_sampled(variant):
     _sampled_dense(wl.headdim_sweep(512), n_random=8, kernel=variant)
+
+
+# -------------------- column split on head dims padded to its instantiated shapes
+@pytest.mark.parametrize("D", [192, 320, 448, 576, 640, 704, 832, 896, 960])
+def test_split_padded_headdims(D):
+    """D/64 chunks rounded up to 4, 6, 8, 12 or 16: the padding chunks are read
+    as zeros and their output columns are not stored (guard band checked)."""
+    dense_case(1, 2, 2, 300, 300, D, seed=D + 21, kernel="split")
+    dense_case(2, 4, 1, 200, 700, D, seed=D + 22, causal=True, kernel="split")
+    q, k, v, _ = wl.draw_dense(1, 2, 2, 140, 260, D, seed=D + 23)
+    big = torch.full((1, 2, 140, D + 64), 3.0, dtype=torch.bfloat16, device=DEV)
+    out = big[..., :D]
+    o, l = run_dense(q, k, v, out=out, kernel="split")
+    o_ref, l_ref = oracle.attn_dense(q, k, v)
+    check(o, l, o_ref, l_ref, f"split padded D{D}")
+    assert bool((big[..., D:] == 3.0).all()), "columns past D were written"
+
+
+@pytest.mark.parametrize("D", [320, 640])
+def test_split_padded_varlen(D):
+    lq = [3, 130, 1, 257, 0, 64, 200]
+    lk = [5, 130, 2, 300, 7, 64, 450]
+    q, k, v, cq, ck = wl.draw_varlen(lq, lk, 4, 2, D, seed=D + 24)
+    for causal in (False, True):
+        o, l = pkg.ffpa_fwd_varlen(q.to(DEV), k.to(DEV), v.to(DEV), cq.to(DEV), ck.to(DEV), max(lq),
+                                   max(lk), causal=causal, enable_gqa=True, return_lse=True,
+                                   kernel="split")
+        device_ok()
+        o_ref, l_ref = oracle.attn_varlen(q, k, v, cq, ck, causal=causal)
+        check(o, l, o_ref, l_ref, f"varlen split padded D{D}")
 
 
 # ------------------------------------------- dual-tile kernel (dense, D = 64, 128)
