@@ -442,7 +442,8 @@ def run_ours(args):
     if kname == "dual" and x.get("mask") is not None:
         kname = "single"   # the dual-tile kernel takes no mask
     vl, um = str(w.varlen).lower(), str(x.get("mask") is not None).lower()
-    kernel = {"fp8": f"ffpa_fp8_quant_kernel + ffpa_fwd_fp8_kernel<{w.D // 128}, {um}>",
+    fp8_attn = ("ffpa_fwd_fp8_split_kernel" if w.D in (384, 512) else "ffpa_fwd_fp8_kernel")
+    kernel = {"fp8": f"ffpa_fp8_quant_kernel + {fp8_attn}<{w.D // 128}, {um}>",
               "single": f"ffpa_fwd_kernel<{vl}, {um}>",
               "dual": f"ffpa_fwd_dual_kernel<{w.D // 64}>",
               "pair": f"ffpa_fwd_pair_kernel<{vl}, {w.D // 64}, {um}>",

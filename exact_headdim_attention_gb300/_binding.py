@@ -272,11 +272,13 @@ def fp8_workspace_views(ws: torch.Tensor, B, Hq, Hkv, Nq, Nkv, D):
 def ffpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=None,
                  dropout_p: float = 0.0, is_causal: bool = False, scale: float | None = None,
                  enable_gqa: bool = False, *, return_lse: bool = False, out=None, lse=None,
-                 workspace=None, stream=None, status=None, wait_timeout_ns=None,
+                 workspace=None, stream=None, kernel=None, status=None, wait_timeout_ns=None,
                  test_drop_first_copy=False):
     """FP8 (e4m3) attention forward through the C ABI ``ffpa_fwd_fp8_ex``.
 
     Arguments as ffpa_fwd (bf16/fp16 in and out); D a multiple of 128.
+    kernel: "single" forces the single-CTA FP8 kernel, "split" the column
+    split (D = 256, 384, 512); by default the split runs at D = 384 and 512.
     workspace: a uint8 device tensor of at least fp8_workspace_bytes(...)
     bytes (allocated here when None); after the call it holds the e4m3
     codes and scales (fp8_workspace_views)."""
@@ -306,7 +308,7 @@ def ffpa_fwd_fp8(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, attn_mask=No
         raise ValueError("workspace must be a contiguous 1-D uint8 tensor")
     mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
-    opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
+    opts = _options(q, kernel, status, wait_timeout_ns, test_drop_first_copy)
     st = lib.ffpa_fwd_fp8_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                              None if lse is None else lse.data_ptr(), _dtype_code(q),
                              B, Hq, Hkv, Nq, Nkv, D, _strides(q), _strides(k), _strides(v),

@@ -1125,15 +1125,40 @@ ffpa_status ffpa_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
     dv_max = w > dv_max ? w : dv_max;
   }
   const int nch8 = D / 128;
-  const bool qres = nch8 <= 4;
-  const size_t q_region = qres ? (size_t)((nch8 + 1) / 2) * SLOT_BYTES : 0;
-  P.vslot = dv_max * 128;
-  P.nslot_v = NSLOT_V_MAX;
-  size_t ns = (SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region - (size_t)P.nslot_v * P.vslot) / SLOT_BYTES;
-  if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
-  if (ns < 2) return FFPA_ERR_UNSUPPORTED;
-  P.nslot = static_cast<int>(ns);
-  const size_t smem = 1024 + q_region + ns * SLOT_BYTES + (size_t)P.nslot_v * P.vslot;
+  // Column split (a pair of CTAs per 128-row tile, each owning D/2 output
+  // columns; S once per key tile) where D/2 fits beside S in TMEM and the
+  // single-CTA FP8 kernel would recompute S (D = 384, 512; measured at
+  // D=512: 1024 vs 957 TFLOPS, at D=256, where the single-CTA kernel has
+  // one slice: 649 vs 878).  FFPA_VARIANT_SPLIT also takes D = 256;
+  // FFPA_VARIANT_SINGLE forces the single-CTA kernel.
+  const bool fsplit = opt.kernel == FFPA_VARIANT_SPLIT ? (D == 256 || D == 384 || D == 512)
+                      : opt.kernel == FFPA_VARIANT_SINGLE ? false
+                                                          : (D == 384 || D == 512);
+  size_t smem = 0;
+  if (fsplit) {
+    // Q resident (32 KB boxes of two 128-byte chunks), two e4m3 P tiles,
+    // a ring of 32 KB stages.
+    P.n_slices = 1;
+    dv_max = D / 2;
+    const size_t q_region = (size_t)((nch8 + 1) / 2) * SLOT_BYTES;
+    const size_t p_tiles = 2 * (size_t)BM * BN;
+    size_t ns = (SMEM_LIMIT - SPLIT_STATIC_RESERVE - 1024 - q_region - p_tiles) / SLOT_BYTES;
+    if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+    if (ns < 3) return FFPA_ERR_UNSUPPORTED;
+    P.nslot = static_cast<int>(ns);
+    P.split_c = 2;
+    smem = 1024 + q_region + p_tiles + ns * SLOT_BYTES;
+  } else {
+    const bool qres = nch8 <= 4;
+    const size_t q_region = qres ? (size_t)((nch8 + 1) / 2) * SLOT_BYTES : 0;
+    P.vslot = dv_max * 128;
+    P.nslot_v = NSLOT_V_MAX;
+    size_t ns = (SMEM_LIMIT - SMEM_STATIC_RESERVE - 1024 - q_region - (size_t)P.nslot_v * P.vslot) / SLOT_BYTES;
+    if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+    if (ns < 2) return FFPA_ERR_UNSUPPORTED;
+    P.nslot = static_cast<int>(ns);
+    smem = 1024 + q_region + ns * SLOT_BYTES + (size_t)P.nslot_v * P.vslot;
+  }
   const uint32_t box_ch = nch8 >= 2 ? 2u : 1u;
   {
     const uint64_t dq[5] = {128, (uint64_t)L.nqp, (uint64_t)nch8, (uint64_t)Hq, (uint64_t)B};
@@ -1182,7 +1207,7 @@ ffpa_status ffpa_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
   P.device = dev;
   const long long items = (long long)B * Hq * P.n_qt * P.n_slices;
   if (items > 0x7fffffffLL) return FFPA_ERR_INVALID;
-  return launch_fp8(Z, P, static_cast<int>(items), smem, reinterpret_cast<cudaStream_t>(stream));
+  return launch_fp8(Z, P, static_cast<int>(items), smem, fsplit, reinterpret_cast<cudaStream_t>(stream));
 }
 
 ffpa_status ffpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,

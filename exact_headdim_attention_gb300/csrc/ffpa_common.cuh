@@ -94,7 +94,10 @@ struct Fp8Quant {
   long long cta_end[3];                        // cumulative CTA counts of q, k, v
   int B, D, fp16;
 };
-ffpa_status launch_fp8(const Fp8Quant& Qz, const Params& P, int items, size_t smem, cudaStream_t stream);
+ffpa_status launch_fp8(const Fp8Quant& Qz, const Params& P, int items, size_t smem, bool split,
+                       cudaStream_t stream);
+// The FP8 attention on the column split (ffpa_fp8_split.cu; D = 256, 384, 512).
+ffpa_status launch_fp8_split(const Params& P, int items, size_t smem, cudaStream_t stream);
 // Raises kernel `fn`'s dynamic shared-memory limit to `bytes` on `device`,
 // once per (kernel, device) pair; later calls only look the pair up.
 ffpa_status set_smem_attr_once(const void* fn, int device, int bytes);

@@ -527,12 +527,14 @@ static ffpa_status launch_fp8_t(bool umask, const Params& P, int items, size_t s
   return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
 }
 
-ffpa_status launch_fp8(const Fp8Quant& Qz, const Params& P, int items, size_t smem, cudaStream_t stream) {
+ffpa_status launch_fp8(const Fp8Quant& Qz, const Params& P, int items, size_t smem, bool split,
+                       cudaStream_t stream) {
   const long long ctas = Qz.cta_end[2];
   if (ctas > 0) {
     ffpa_fp8_quant_kernel<<<(unsigned)ctas, 256, 0, stream>>>(Qz);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
+  if (split) return launch_fp8_split(P, items, smem, stream);
   const bool umask = P.mask != nullptr;
   switch (P.D / 128) {
     case 1: return launch_fp8_t<1>(umask, P, items, smem, stream);

@@ -234,6 +234,12 @@ ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void
  *     of K and of V [B,Hkv,Nkp/128].  Rows past N are zero.
  *   Inputs must be finite.  Two launches on `stream` (quantisation,
  *   attention); no allocation, no synchronisation.
+ *   Kernels (ffpa_options.kernel of ffpa_fwd_fp8_ex): the column split (two
+ *   SMs per 128-row tile, each owning D/2 output columns) by default at
+ *   D = 384 and 512, and at D = 256 with FFPA_VARIANT_SPLIT; the single-CTA
+ *   FP8 kernel otherwise or with FFPA_VARIANT_SINGLE.  Both compute the same
+ *   quantised attention (the row maximum, and so the e4m3 rounding of P,
+ *   may differ between them).
  */
 size_t ffpa_fwd_fp8_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
 ffpa_status ffpa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,

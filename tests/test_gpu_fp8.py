@@ -45,14 +45,15 @@ def _dequant(codes, scales, N):
     return d[:, :, :N]
 
 
-def run_fp8(q, k, v, mask=None, causal=False, scale=None):
+def run_fp8(q, k, v, mask=None, causal=False, scale=None, kernel=None):
     B, Hq, Nq, D = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     ws = torch.full((pkg.fp8_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D),), 0x55, dtype=torch.uint8,
                     device=DEV)
     o, lse = pkg.ffpa_fwd_fp8(q.to(DEV), k.to(DEV), v.to(DEV),
                               attn_mask=None if mask is None else mask.to(DEV), is_causal=causal,
-                              scale=scale, enable_gqa=Hq != Hkv, return_lse=True, workspace=ws)
+                              scale=scale, enable_gqa=Hq != Hkv, return_lse=True, workspace=ws,
+                              kernel=kernel)
     device_ok()
     return o, lse, pkg.fp8_workspace_views(ws, B, Hq, Hkv, Nq, Nkv, D)
 
@@ -137,11 +138,11 @@ def check_fp8(o, lse, q, k, v, mask=None, causal=False, scale=None, rows=None, w
 
 
 def fp8_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, mask=None, scale=None, dtype=torch.bfloat16,
-             std=1.0):
+             std=1.0, kernel=None):
     q, k, v, g = wl.draw_dense(B, Hq, Hkv, Nq, Nkv, D, seed, std=std, dtype=dtype)
     m = mask(g) if callable(mask) else mask
-    o, lse, views = run_fp8(q, k, v, m, causal, scale)
-    what = f"fp8 B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D}"
+    o, lse, views = run_fp8(q, k, v, m, causal, scale, kernel=kernel)
+    what = f"fp8 {kernel or 'auto'} B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D}"
     check_codes(q, k, v, views, what)
     return check_fp8(o, lse, q, k, v, m, causal, scale, what=what)
 
@@ -154,6 +155,17 @@ def test_fp8_headdims_ragged(D):
 @pytest.mark.parametrize("D", [256, 512, 1024])
 def test_fp8_causal_gqa_cross(D):
     fp8_case(2, 4, 2, 200, 460, D, seed=710 + D, causal=True)
+
+
+@pytest.mark.parametrize("D", [256, 384, 512])
+@pytest.mark.parametrize("kernel", ["single", "split"])
+def test_fp8_both_kernels(D, kernel):
+    """The column split (the default at these head dims) and the single-CTA
+    FP8 kernel, forced: dense ragged, causal GQA cross attention, a mask."""
+    fp8_case(1, 2, 2, 300, 300, D, seed=760 + D, kernel=kernel)
+    fp8_case(2, 4, 2, 200, 460, D, seed=761 + D, causal=True, kernel=kernel)
+    fp8_case(1, 2, 2, 129, 257, D, seed=762 + D, kernel=kernel,
+             mask=lambda g: torch.rand(1, 1, 129, 257, generator=g) < 0.6)
 
 
 @pytest.mark.parametrize("kind", ["bool", "f32_neg_inf", "qtype"])
@@ -203,15 +215,17 @@ def test_fp8_edges():
         pkg.ffpa_fwd_fp8(qd, qd, qd, workspace=torch.empty(1024, dtype=torch.uint8, device=DEV))
 
 
-def test_fp8_bounded_wait_reports_timeout():
+@pytest.mark.parametrize("kernel", ["single", "split"])
+def test_fp8_bounded_wait_reports_timeout(kernel):
     q, k, v, _ = wl.draw_dense(1, 2, 2, 200, 300, 512, seed=761)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    pkg.ffpa_fwd_fp8(qd, kd, vd, status=status, wait_timeout_ns=200_000_000, test_drop_first_copy=True)
+    pkg.ffpa_fwd_fp8(qd, kd, vd, status=status, wait_timeout_ns=200_000_000, test_drop_first_copy=True,
+                     kernel=kernel)
     torch.cuda.synchronize()
     assert int(status.item()) == pkg.FFPA_ERR_DEVICE_TIMEOUT
-    o, lse, views = run_fp8(q, k, v)
-    check_fp8(o, lse, q, k, v, what="after timeout")
+    o, lse, views = run_fp8(q, k, v, kernel=kernel)
+    check_fp8(o, lse, q, k, v, what=f"{kernel} after timeout")
 
 
 def test_fp8_full_d512_sampled():
