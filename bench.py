@@ -53,7 +53,7 @@ L2_BYTES = 129 * 1000 * 1000
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="selfattn_b1_h16_n4096_d512")
@@ -482,9 +482,12 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not w.varlen:
         line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds, fp8=fp8)
         line["oracle_cpu_s_full_workload_est"] = line["cpu_baseline"]["full_workload_s"]
-    traffic = measured_traffic(w.name)
+    traffic = measured_traffic(w.name, key="fp8_dram_bytes_per_launch" if fp8 else "dram_bytes_per_launch")
     if traffic is not None:
         line["roofline"]["traffic"] = traffic
+        if fp8:
+            line["roofline"]["traffic_note"] = ("ncu DRAM bytes of the attention launch; the quantisation "
+                                                "launch reads Q, K, V and writes their e4m3 codes")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist_on:
@@ -705,9 +708,10 @@ def measured_traffic_bwd(name, path=TRAFFIC_PATH):
     return d.get("bwd_dram_bytes_per_step", {}).get(name)
 
 
-def measured_traffic(name, path=TRAFFIC_PATH):
+def measured_traffic(name, path=TRAFFIC_PATH, key="dram_bytes_per_launch"):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
-    or None when that capture was taken on a different kernel source."""
+    or None when that capture was taken on a different kernel source.  key
+    "fp8_dram_bytes_per_launch" holds the FP8 attention kernel's bytes."""
     try:
         with open(path) as f:
             d = json.load(f)
@@ -715,7 +719,7 @@ def measured_traffic(name, path=TRAFFIC_PATH):
         return None
     if d.get("kernel_source_sha") != kernel_source_sha():
         return None
-    return d.get("dram_bytes_per_launch", {}).get(name)
+    return d.get(key, {}).get(name)
 
 
 # ---------------------------------------------------------- reference arm
