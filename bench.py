@@ -680,13 +680,24 @@ def strip_comments(src: str) -> str:
     return " ".join(src.split())
 
 
-def kernel_source_sha() -> str:
-    """Hash of the kernel sources' code (comments and layout excluded), so that a
-    recorded ncu capture stays attached to the code it measured."""
+# The sources each recorded capture depends on: the kernel's own file, the
+# shared device code and the host planner that sets its launch shape.
+TRAFFIC_SOURCES = {
+    "dram_bytes_per_launch": ("ffpa_split.cu", "ffpa_common.cuh", "ptx.cuh", "ffpa_api.cu"),
+    "fp8_dram_bytes_per_launch": ("ffpa_fp8_split.cu", "ffpa_fp8.cu", "ffpa_common.cuh", "ptx.cuh",
+                                  "ffpa_api.cu"),
+    "bwd_dram_bytes_per_step": ("ffpa_bwd.cu", "ffpa_common.cuh", "ptx.cuh", "ffpa_api.cu"),
+}
+
+
+def kernel_source_sha(files=None) -> str:
+    """Hash of kernel sources' code (comments and layout excluded), so that a
+    recorded ncu capture stays attached to the code it measured.  files: the
+    csrc file names to hash (all of them when None)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_headdim_attention_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(fn.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
@@ -695,31 +706,33 @@ def kernel_source_sha() -> str:
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def measured_traffic_bwd(name, path=TRAFFIC_PATH):
-    """DRAM bytes of one backward step's dQ, dV and dK launches from the committed
-    ncu summary, or None when that capture was taken on different kernel code."""
+def _traffic_section(key, path):
+    """Section `key` of the committed ncu summary (profiles/traffic.json), or None
+    when it was captured on different code than the current sources."""
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_source_sha") != kernel_source_sha():
+    sec = d.get(key)
+    if not isinstance(sec, dict) or sec.get("kernel_source_sha") != kernel_source_sha(TRAFFIC_SOURCES[key]):
         return None
-    return d.get("bwd_dram_bytes_per_step", {}).get(name)
+    return sec
+
+
+def measured_traffic_bwd(name, path=TRAFFIC_PATH):
+    """DRAM bytes of one backward step's dQ, dV and dK launches from the committed
+    ncu summary, or None when that capture was taken on different kernel code."""
+    sec = _traffic_section("bwd_dram_bytes_per_step", path)
+    return None if sec is None else sec.get(name)
 
 
 def measured_traffic(name, path=TRAFFIC_PATH, key="dram_bytes_per_launch"):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
     or None when that capture was taken on a different kernel source.  key
     "fp8_dram_bytes_per_launch" holds the FP8 attention kernel's bytes."""
-    try:
-        with open(path) as f:
-            d = json.load(f)
-    except (OSError, ValueError):
-        return None
-    if d.get("kernel_source_sha") != kernel_source_sha():
-        return None
-    return d.get(key, {}).get(name)
+    sec = _traffic_section(key, path)
+    return None if sec is None else sec.get(name)
 
 
 # ---------------------------------------------------------- reference arm

@@ -92,21 +92,31 @@ def test_kernel_source_hash_ignores_comments_not_code():
 
 
 def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path):
-    rec = {"kernel_source_sha": bench.kernel_source_sha(),
-           "dram_bytes_per_launch": {"w": 123},
-           "bwd_dram_bytes_per_step": {"w": {"dq": 1, "dv": 2, "dk": 3, "gradient_kernels_total": 6}}}
+    sha = {k: bench.kernel_source_sha(v) for k, v in bench.TRAFFIC_SOURCES.items()}
+    rec = {"dram_bytes_per_launch": {"kernel_source_sha": sha["dram_bytes_per_launch"], "w": 123},
+           "fp8_dram_bytes_per_launch": {"kernel_source_sha": sha["fp8_dram_bytes_per_launch"], "w": 45},
+           "bwd_dram_bytes_per_step": {"kernel_source_sha": sha["bwd_dram_bytes_per_step"],
+                                       "w": {"dq": 1, "dv": 2, "dk": 3, "gradient_kernels_total": 6}}}
     p = tmp_path / "traffic.json"
     p.write_text(json.dumps(rec))
     assert bench.measured_traffic("w", path=str(p)) == 123
+    assert bench.measured_traffic("w", path=str(p), key="fp8_dram_bytes_per_launch") == 45
     assert bench.measured_traffic_bwd("w", path=str(p))["gradient_kernels_total"] == 6
-    rec["kernel_source_sha"] = "0" * 16
+    # a record taken on other code is not used; the sections are independent
+    rec["dram_bytes_per_launch"]["kernel_source_sha"] = "0" * 16
+    rec["bwd_dram_bytes_per_step"]["kernel_source_sha"] = "0" * 16
     p.write_text(json.dumps(rec))
     assert bench.measured_traffic("w", path=str(p)) is None
     assert bench.measured_traffic_bwd("w", path=str(p)) is None
+    assert bench.measured_traffic("w", path=str(p), key="fp8_dram_bytes_per_launch") == 45
+    # each section hashes its own kernel's files
+    assert sha["dram_bytes_per_launch"] != sha["fp8_dram_bytes_per_launch"]
 
 
 def test_committed_traffic_record_is_consistent():
     with open(bench.TRAFFIC_PATH) as f:
         d = json.load(f)
     for name, tb in d.get("bwd_dram_bytes_per_step", {}).items():
+        if name == "kernel_source_sha":
+            continue
         assert tb["gradient_kernels_total"] == tb["dq"] + tb["dv"] + tb["dk"], name
