@@ -383,7 +383,7 @@ ffpa_status launch_kernel(Kern kn, bool varlen, const Params& P, int items, size
   if (kn == Kern::PAIR) return launch_pair(varlen, umask, P, items, smem, stream);
   if (kn == Kern::DUAL) return varlen ? FFPA_ERR_UNSUPPORTED : launch_dual(umask, P, items, smem, stream);
   if (kn == Kern::SPLIT)
-    return P.split_c == 2 ? launch_split(varlen, umask, P, items, smem, stream)
+    return (P.split_c == 2 && P.q_res != 0) ? launch_split(varlen, umask, P, items, smem, stream)
                           : launch_cluster(varlen, umask, P, items, smem, stream);
   return launch_single(varlen, umask, P, items, smem, stream);
 }
@@ -599,7 +599,18 @@ ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
   Kern kn = choose_kernel(D, false, opt.kernel);
   if (kn == Kern::DUAL && umask) kn = Kern::SINGLE;   // the dual-tile kernel takes no mask
   const bool pair = kn == Kern::PAIR;
-  const size_t smem = plan_for(kn, D, &P);
+  size_t smem = plan_for(kn, D, &P);
+  if (kn == Kern::SPLIT && is_causal && P.split_c == 2 && P.nchunks == 8) {
+    // Dense causal at D = 512: Q streamed through a five-stage ring (the
+    // cluster kernel at C = 2) instead of resident beside three stages
+    // (measured on causal GQA B2 Hq32 Hkv8 N8192: 1058 vs 1031 TFLOPS; the
+    // dense and varlen batches run faster with Q resident).
+    P.q_res = 0;
+    size_t ns = (SMEM_LIMIT - SPLIT_STATIC_RESERVE - 1024 - 2 * (size_t)P_TILE_BYTES) / SLOT_BYTES;
+    if (ns > (size_t)NSLOT_MAX) ns = NSLOT_MAX;
+    P.nslot = static_cast<int>(ns);
+    smem = 1024 + 2 * (size_t)P_TILE_BYTES + ns * SLOT_BYTES;
+  }
   const uint32_t k_rows = pair ? BN / 2 : BN;
   const uint32_t k_box_chunks = pair ? (uint32_t)P.kc : (uint32_t)P.kchunks;
   // The maps span the real D/64 chunks; a column-split plan may run more

@@ -56,7 +56,7 @@ __device__ __forceinline__ float max_from_bits(uint32_t h) { return __uint_as_fl
 template <bool VARLEN, int NCH, bool UMASK, int C>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
     ffpa_fwd_cluster_kernel(const __grid_constant__ Params p) {
-  static_assert(C >= 3 && C <= 4 && NCH % C == 0 && NCH % 2 == 0, "unsupported split");
+  static_assert(C >= 2 && C <= 4 && NCH % C == 0 && NCH % 2 == 0, "unsupported split");
   const uint32_t rank = cluster_ctarank();
   Item it;
   if (!decode_item(p, VARLEN, blockIdx.x / C, it)) return;    // same answer in every CTA
@@ -70,7 +70,10 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   constexpr int qt = NCH < Q_TMEM_MAX_CHUNKS ? NCH : Q_TMEM_MAX_CHUNKS;   // Q chunks held in TMEM
-  constexpr bool QRES = cluster_q_resident(NCH, C);
+  // Pairs (C = 2) run here only for dense causal batches at D = 512, with Q
+  // streamed so that the ring holds five stages (the pair kernel of
+  // ffpa_split.cu keeps Q resident beside three).
+  constexpr bool QRES = C == 2 ? false : cluster_q_resident(NCH, C);
   constexpr int vk = VCH * 128 * 128 <= (int)SLOT_BYTES ? 128 : 64;      // keys per V stage
   const int inject = p.inject;
   const bool fp16 = p.fp16 != 0;
@@ -609,6 +612,8 @@ static ffpa_status launch_cluster_nc(const Params& P, int items, size_t smem, cu
 
 template <bool VARLEN, bool UMASK>
 static ffpa_status launch_cluster_t(const Params& P, int items, size_t smem, cudaStream_t stream) {
+  if (!VARLEN && P.nchunks == 8 && P.split_c == 2 && P.q_res == 0)
+    return launch_cluster_nc<false, UMASK, 8, 2>(P, items, smem, stream);
   if (P.nchunks == 12 && P.split_c == 3) return launch_cluster_nc<VARLEN, UMASK, 12, 3>(P, items, smem, stream);
   if (P.nchunks == 16 && P.split_c == 4) return launch_cluster_nc<VARLEN, UMASK, 16, 4>(P, items, smem, stream);
   return FFPA_ERR_UNSUPPORTED;
