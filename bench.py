@@ -560,10 +560,17 @@ def run_ours_bwd(args):
                 "dv": torch.empty_like(t["v"]),
                 "delta": torch.empty(t["lse"].shape, dtype=torch.float32, device=dev)}
 
+    # The stored-tile workspace (P and dS of every visible tile), allocated
+    # once: the timed steps and the end-to-end steps run on one stream at a
+    # time, so they share it.
+    B, Hq, Nq, D = x["q"].shape
+    ws_bytes = pkg.bwd_workspace_bytes(B, Hq, x["k"].shape[1], Nq, x["k"].shape[2], D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+
     def backward(t, gr, stream=None):
         pkg.ffpa_bwd(t["dout"], t["q"], t["k"], t["v"], t["o"], t["lse"], is_causal=w.causal,
                      enable_gqa=w.enable_gqa, dq=gr["dq"], dk=gr["dk"], dv=gr["dv"],
-                     delta=gr["delta"], stream=stream)
+                     delta=gr["delta"], workspace=ws, stream=stream)
 
     gr0 = grads_like(devt)
 
@@ -636,7 +643,9 @@ def run_ours_bwd(args):
     peak, peak_src, peak_sustained = read_peaks()
     achieved = value
     cfg = config_of(w, flops)
-    cfg["pass"] = "backward (delta + dQ + dV + dK kernels)"
+    cfg["pass"] = ("backward (delta, scores and contraction kernels; P and dS stored once per tile)"
+                   if ws is not None else "backward (delta + dQ + dV + dK slice kernels)")
+    cfg["bwd_workspace_bytes"] = ws_bytes
     line = {
         "metric": METRIC_BWD, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 4),
@@ -647,17 +656,19 @@ def run_ours_bwd(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                      "peak_source": peak_src,
-                     "kernel": "ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_kernel<0, false> (dQ) + "
-                               "ffpa_bwd_kernel<1, false> (dV) + ffpa_bwd_kernel<2, false> (dK), one C call",
+                     "kernel": (f"ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_scores_kernel<{D // 64}, false> "
+                                f"+ ffpa_bwd_contract_kernel<{D // 64}>, one C call" if ws is not None else
+                                "ffpa_bwd step: ffpa_bwd_delta_kernel + ffpa_bwd_kernel<0, false> (dQ) + "
+                                "ffpa_bwd_kernel<1, false> (dV) + ffpa_bwd_kernel<2, false> (dK), one C call"),
                      "frac_of_sustained": (round(achieved / peak_sustained, 4)
                                            if peak_sustained else None),
                      "algorithmic_flops_per_launch": flops},
         "e2e": {"value": round(e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                "api": "exact_headdim_attention_gb300.ffpa_bwd (C ABI ffpa_bwd)",
+                "api": "exact_headdim_attention_gb300.ffpa_bwd (C ABI ffpa_bwd_ws_ex)",
                 "pipelining": "copy-in, backward and copy-out of consecutive steps on three "
                               "streams with two buffer sets"},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (3 if ws is not None else 4) * args.steps,
         "clocks": clocks,
         "impl": "ours",
     }
@@ -686,7 +697,8 @@ TRAFFIC_SOURCES = {
     "dram_bytes_per_launch": ("ffpa_split.cu", "ffpa_common.cuh", "ptx.cuh", "ffpa_api.cu"),
     "fp8_dram_bytes_per_launch": ("ffpa_fp8_split.cu", "ffpa_fp8.cu", "ffpa_common.cuh", "ptx.cuh",
                                   "ffpa_api.cu"),
-    "bwd_dram_bytes_per_step": ("ffpa_bwd.cu", "ffpa_common.cuh", "ptx.cuh", "ffpa_api.cu"),
+    "bwd_dram_bytes_per_step": ("ffpa_bwd.cu", "ffpa_bwd_tiles.cu", "ffpa_bwd_common.cuh", "ffpa_common.cuh",
+                                "ptx.cuh", "ffpa_api.cu"),
 }
 
 

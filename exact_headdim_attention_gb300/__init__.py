@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     KERNEL_VARIANTS,
     Options,
     default_scale,
+    BWD_AUTO_WORKSPACE_MAX,
+    bwd_workspace_bytes,
     ffpa_bwd,
     ffpa_bwd_noalloc,
     BWD_NOALLOC_MAX_ROWS,

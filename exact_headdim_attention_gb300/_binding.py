@@ -25,7 +25,8 @@ FFPA_MASK_NONE, FFPA_MASK_BOOL, FFPA_MASK_ADD_F32, FFPA_MASK_ADD_QTYPE = range(4
 EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", "ffpa_bwd",
             "ffpa_bwd_ex", "ffpa_bwd_varlen", "ffpa_bwd_varlen_ex", "ffpa_status_string",
             "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc",
-            "ffpa_fwd_fp8", "ffpa_fwd_fp8_ex", "ffpa_fwd_fp8_workspace_bytes")
+            "ffpa_fwd_fp8", "ffpa_fwd_fp8_ex", "ffpa_fwd_fp8_workspace_bytes", "ffpa_bwd_ws",
+            "ffpa_bwd_ws_ex", "ffpa_bwd_workspace_bytes")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3, "dual": 4}
 
@@ -99,6 +100,13 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_fwd_fp8_ex.restype = I
     lib.ffpa_fwd_fp8_workspace_bytes.argtypes = [I, I, I, I, I, I]
     lib.ffpa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+    bws = sigs["ffpa_bwd"][:-1] + [P, ctypes.c_size_t, P]   # + workspace, bytes, stream
+    lib.ffpa_bwd_ws.argtypes = bws
+    lib.ffpa_bwd_ws.restype = I
+    lib.ffpa_bwd_ws_ex.argtypes = bws + [O]
+    lib.ffpa_bwd_ws_ex.restype = I
+    lib.ffpa_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.ffpa_bwd_workspace_bytes.restype = ctypes.c_size_t
     # ffpa_bwd without the delta argument
     lib.ffpa_bwd_noalloc.argtypes = sigs["ffpa_bwd"][:9] + sigs["ffpa_bwd"][10:]
     lib.ffpa_bwd_noalloc.restype = I
@@ -348,17 +356,48 @@ def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
     return mk, m.data_ptr(), _strides(m), m
 
 
+# Largest stored-tile workspace ffpa_bwd allocates by itself (workspace="auto").
+BWD_AUTO_WORKSPACE_MAX = 4 << 30
+
+
+def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int) -> int:
+    """Bytes of the stored-tile backward's workspace (0: the shape does not take that path)."""
+    return int(load_library().ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+
+
+def _bwd_workspace(workspace, need: int, device):
+    """(pointer, bytes, tensor to keep) of the stored-tile workspace argument."""
+    if workspace is None or need == 0:
+        return None, 0, None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be None, "auto" or a uint8 device tensor')
+        if need > BWD_AUTO_WORKSPACE_MAX:
+            return None, 0, None
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if (not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8
+            or not workspace.is_contiguous() or workspace.device != device):
+        raise ValueError("workspace must be a contiguous uint8 tensor on q's device")
+    return workspace.data_ptr(), workspace.numel(), workspace
+
+
 def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
              out: torch.Tensor, lse: torch.Tensor, is_causal: bool = False,
              scale: float | None = None, enable_gqa: bool = False, attn_mask=None, *, dq=None,
-             dk=None, dv=None, delta=None, return_delta: bool = False, stream=None, status=None,
-             wait_timeout_ns=None, test_drop_first_copy=False):
-    """Dense attention backward through the C ABI ``ffpa_bwd``.
+             dk=None, dv=None, delta=None, return_delta: bool = False, workspace="auto",
+             stream=None, status=None, wait_timeout_ns=None, test_drop_first_copy=False):
+    """Dense attention backward through the C ABI ``ffpa_bwd_ws``.
 
     dout, q, out [B,Hq,Nq,D]; k, v [B,Hkv,Nkv,D]; lse [B,Hq,Nq] fp32 from the
     forward with the same attn_mask / is_causal / scale (the mask enters the
     recomputed scores; no gradient is formed for it).  Returns (dq, dk, dv),
-    plus delta = rowsum(dout * out) [B,Hq,Nq] fp32 with return_delta."""
+    plus delta = rowsum(dout * out) [B,Hq,Nq] fp32 with return_delta.
+
+    workspace: the stored-tile backward's scratch (see bwd_workspace_bytes):
+    "auto" allocates it when the shape takes that path and it needs at most
+    BWD_AUTO_WORKSPACE_MAX bytes; None runs the slice kernels (S and dP
+    recomputed per 256-column output slice); a uint8 device tensor is used
+    when it is large enough."""
     lib = load_library()
     for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
         if t.dim() != 4:
@@ -377,13 +416,15 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
     mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
     opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
-    st = lib.ffpa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
-                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                         delta.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q),
-                         _strides(k), _strides(v), _strides(out), _strides(dout), _strides(dq),
-                         _strides(dk), _strides(dv), mptr, mk, mstr, sc, int(bool(is_causal)), int(bool(enable_gqa)),
-                         _stream_handle(stream, q), opts)
-    del keep
+    need = int(lib.ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+    ws_ptr, ws_bytes, ws_keep = _bwd_workspace(workspace, need, q.device)
+    st = lib.ffpa_bwd_ws_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            delta.data_ptr(), _dtype_code(q), B, Hq, Hkv, Nq, Nkv, D, _strides(q),
+                            _strides(k), _strides(v), _strides(out), _strides(dout), _strides(dq),
+                            _strides(dk), _strides(dv), mptr, mk, mstr, sc, int(bool(is_causal)),
+                            int(bool(enable_gqa)), ws_ptr, ws_bytes, _stream_handle(stream, q), opts)
+    del keep, ws_keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)

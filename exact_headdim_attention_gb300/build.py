@@ -20,9 +20,10 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 OUT = PKG / "_build" / "libffpa.so"
 # One translation unit per kernel plus the host side, compiled in parallel.
-SOURCES = [CSRC / n for n in ("ffpa_cluster.cu", "ffpa_split.cu", "ffpa_bwd.cu", "ffpa_pair.cu",
-                              "ffpa_fp8.cu", "ffpa_fp8_split.cu", "ffpa_single.cu", "ffpa_dual.cu", "ffpa_api.cu", "ffpa_noalloc.cu")]
-DEPS = SOURCES + [CSRC / "ffpa_common.cuh", CSRC / "ptx.cuh", INCLUDE / "ffpa.h"]
+SOURCES = [CSRC / n for n in ("ffpa_cluster.cu", "ffpa_split.cu", "ffpa_bwd.cu", "ffpa_bwd_tiles.cu",
+                              "ffpa_pair.cu", "ffpa_fp8.cu", "ffpa_fp8_split.cu", "ffpa_single.cu",
+                              "ffpa_dual.cu", "ffpa_api.cu", "ffpa_noalloc.cu")]
+DEPS = SOURCES + [CSRC / "ffpa_common.cuh", CSRC / "ffpa_bwd_common.cuh", CSRC / "ptx.cuh", INCLUDE / "ffpa.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -49,6 +49,7 @@ struct DeviceFacts {
   std::once_flag once;
   ffpa_status arch = FFPA_ERR_CUDA;
   int* fallback = nullptr;
+  int sms = 0;
 };
 DeviceFacts g_devices[MAX_DEVICES];
 
@@ -64,6 +65,10 @@ const DeviceFacts& device_facts(int dev) {
       return;
     }
     f.arch = (major == 10 && minor == 3) ? FFPA_OK : FFPA_ERR_UNSUPPORTED;
+    if (cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      f.sms = 0;
+    }
     void* addr = nullptr;
     if (f.arch == FFPA_OK) {
       if (cudaGetSymbolAddress(&addr, g_status_fallback) != cudaSuccess) {
@@ -423,6 +428,74 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, 
   return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), smem, smem_two, stream);
 }
 
+// Stored-tile backward: dense, D = 256, 384 or 512, at least one query row
+// and one key.  Workspace bytes (0: the path does not apply): P and dS,
+// 16-bit, [B Hq Nqp][Nkp] each (Nqp, Nkp rounded up to 128), dS first
+// byte at half the total.
+size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D) {
+  if (!(D == 256 || D == 384 || D == 512) || B < 1 || Hq < 1 || Nq < 1 || Nkv < 1) return 0;
+  const long long nqp = ((long long)Nq + BM - 1) / BM * BM, nkp = ((long long)Nkv + BN - 1) / BN * BN;
+  const long long rows = (long long)B * Hq * nqp;
+  if (rows > 0x7fffffffLL) return 0;   // TMA row coordinates are 32-bit
+  return static_cast<size_t>(2 * rows * nkp * 2);
+}
+
+// Plans and launches the stored-tile path: the caller has set P as for
+// bwd_launch and checked the workspace (`ws`, bwd_tiles_bytes() bytes).
+ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o, cudaStream_t stream) {
+  const size_t need = bwd_tiles_bytes(P.B, P.Hq, P.Nq, P.Nkv, P.D);
+  P.nchunks = P.D / DK;
+  P.n_sl = 1;
+  const long long nqp = (long long)P.n_qt * BM, nkp = (long long)P.n_kt * BN;
+  P.ws_ld = nkp;
+  P.ws_p = ws;
+  P.ws_ds = static_cast<uint8_t*>(ws) + need / 2;
+  const CUtensorMapDataType tdt = P.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t dims[3] = {64, (uint64_t)(P.B * P.Hq * nqp), (uint64_t)(nkp / 64)};
+  const uint64_t strides[2] = {(uint64_t)nkp * 2, 128};
+  const uint32_t box[3] = {64, BM, 2};
+  ffpa_status st = encode_map(&P.tm_ws_p, tdt, 3, P.ws_p, dims, strides, box);
+  if (st == FFPA_OK) st = encode_map(&P.tm_ws_ds, tdt, 3, P.ws_ds, dims, strides, box);
+  if (st != FFPA_OK) return st;
+  // Scores kernel: dO (D/64 chunks) resident, then the ring.
+  size_t ns = (SMEM_LIMIT - TS_STATIC_RESERVE - 1024 - (size_t)P.nchunks * CHUNK_BYTES) / SLOT_BYTES;
+  if (ns > (size_t)TS_NSLOT_MAX) ns = TS_NSLOT_MAX;
+  P.ts_nslot = static_cast<int>(ns);
+  const size_t smem_s = 1024 + (size_t)P.nchunks * CHUNK_BYTES + ns * SLOT_BYTES;
+  size_t nc = (SMEM_LIMIT - TC_STATIC_RESERVE - 1024) / SLOT_BYTES;
+  if (nc > (size_t)TC_NSLOT_MAX) nc = TC_NSLOT_MAX;
+  P.tc_nslot = static_cast<int>(nc);
+  const size_t smem_c = 1024 + nc * SLOT_BYTES;
+  // Key-tile ranges per query tile (non-causal only; causal items are
+  // ordered longest first instead): the count whose last wave is fullest,
+  // keeping at least 4 key tiles per range.
+  const long long base = (long long)P.B * P.Hq * P.n_qt;
+  P.kv_parts = 1;
+  if (!P.causal && sms > 0) {
+    double best = -1.0;
+    for (int parts = 1; parts <= 4; parts *= 2) {
+      if (parts > 1 && P.n_kt / parts < 4) break;
+      const double waves = (double)(base * parts) / sms;
+      const double eff = waves / std::ceil(waves);
+      if (eff > best + 0.03) {
+        best = eff;
+        P.kv_parts = parts;
+      }
+    }
+  }
+  P.scale_log2 = P.scale * 1.4426950408889634f;
+  P.inject = o.drop;
+  P.timeout_ns = o.timeout_ns;
+  const long long score_items = base * P.kv_parts;
+  const long long n_dq = base, n_kv = (long long)P.B * P.Hkv * P.n_kt;
+  const long long contract_items = n_dq + 2 * n_kv;
+  if (score_items > 0x7fffffffLL || contract_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  P.n_dq_items = static_cast<int>(n_dq);
+  P.n_kv_items = static_cast<int>(n_kv);
+  return launch_bwd_tiles(P, static_cast<int>(score_items), static_cast<int>(contract_items), smem_s, smem_c,
+                          stream);
+}
+
 }  // namespace
 
 namespace ffpa {
@@ -688,15 +761,15 @@ ffpa_status ffpa_fwd(const void* q, const void* k, const void* v, void* o, float
                      mask_kind, mask_str, scale, is_causal, enable_gqa, stream, nullptr);
 }
 
-ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
-                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                        float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
-                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
-                        const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
-                        const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
-                        ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
-                        int is_causal, int enable_gqa, ffpa_stream_t stream,
-                        const ffpa_options* options) {
+ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                           const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                           const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
+                           const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                           ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
+                           int is_causal, int enable_gqa, void* workspace, size_t workspace_bytes,
+                           ffpa_stream_t stream, const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (B < 0 || Hq < 1 || Hkv < 1 || Nq < 0 || Nkv < 0) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -736,10 +809,16 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
   }
   int dev = 0;
   const bool any_q = Nq > 0, any_k = Nkv > 0;
+  // The stored-tile path runs when it applies and the workspace holds it;
+  // otherwise the sliced kernels run and the workspace is not touched.
+  const size_t ws_need = bwd_tiles_bytes(B, Hq, Nq, Nkv, D);
+  const bool tiles = workspace != nullptr && ws_need > 0 && workspace_bytes >= ws_need;
+  if (tiles && !aligned16(workspace)) return FFPA_ERR_INVALID;
   ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,
                                   any_q ? dq : nullptr, any_q ? lse : nullptr, any_q ? delta : nullptr,
                                   any_k ? k : nullptr, any_k ? v : nullptr, any_k ? dk : nullptr,
-                                  any_k ? dv : nullptr, umask ? mask : nullptr},
+                                  any_k ? dv : nullptr, umask ? mask : nullptr,
+                                  tiles ? workspace : nullptr},
                                  &dev);
   if (st != FFPA_OK) return st;
   DeviceScope scope(dev);
@@ -801,7 +880,40 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
   P.fp16 = dt == FFPA_FP16;
   P.err = err;
   P.device = dev;
+  if (tiles) return bwd_tiles_launch(P, workspace, device_facts(dev).sms, opt, reinterpret_cast<cudaStream_t>(stream));
   return bwd_launch(P, any_q, any_k, opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                        const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                        const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
+                        const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                        ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
+                        int is_causal, int enable_gqa, ffpa_stream_t stream,
+                        const ffpa_options* options) {
+  return ffpa_bwd_ws_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, B, Hq, Hkv, Nq, Nkv, D, q_str,
+                        k_str, v_str, o_str, do_str, dq_str, dk_str, dv_str, mask, mask_kind, mask_str,
+                        scale, is_causal, enable_gqa, nullptr, 0, stream, options);
+}
+
+size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D) {
+  if (Hkv < 1 || Hq % Hkv != 0) return 0;
+  return bwd_tiles_bytes(B, Hq, Nq, Nkv, D);
+}
+
+ffpa_status ffpa_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
+                        int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
+                        const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
+                        const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
+                        const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                        const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                        void* workspace, size_t workspace_bytes, ffpa_stream_t stream) {
+  return ffpa_bwd_ws_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, B, Hq, Hkv, Nq, Nkv, D, q_str,
+                        k_str, v_str, o_str, do_str, dq_str, dk_str, dv_str, mask, mask_kind, mask_str,
+                        scale, is_causal, enable_gqa, workspace, workspace_bytes, stream, nullptr);
 }
 
 ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

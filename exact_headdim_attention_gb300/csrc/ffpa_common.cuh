@@ -127,6 +127,20 @@ class DeviceScope {
 struct BwdParams;
 ffpa_status launch_bwd(const BwdParams& P, int dq_items, int kv_items, size_t smem, size_t smem_two,
                        cudaStream_t stream);
+// The delta pass alone (rowsum(dO * O) into P.delta).
+ffpa_status launch_bwd_delta(const BwdParams& P, cudaStream_t stream);
+// Stored-tile backward (ffpa_bwd_tiles.cu): the delta pass, the scores
+// kernel (P and dS once per query tile x key tile into the caller's
+// workspace) and the contraction kernel (dQ, dV and dK from the stored
+// tiles).  D / 64 in {4, 6, 8}.
+ffpa_status launch_bwd_tiles(const BwdParams& P, int score_items, int contract_items, size_t smem_scores,
+                             size_t smem_contract, cudaStream_t stream);
+constexpr int TS_THREADS = 320;            // scores: warps 0-7 elementwise, 8 TMA, 9 MMA
+constexpr int TC_THREADS = 192;            // contraction: warps 0-3 epilogue, 4 TMA, 5 MMA
+constexpr int TS_NSLOT_MAX = 6;
+constexpr int TC_NSLOT_MAX = 7;
+constexpr size_t TS_STATIC_RESERVE = 1024;
+constexpr size_t TC_STATIC_RESERVE = 1024;
 constexpr int BWD_THREADS = 192;           // warps 0-3 elementwise, 4 TMA, 5 MMA
 constexpr int BWD_NSLOT_MAX = 6;
 constexpr size_t BWD_STATIC_RESERVE = 6144;
@@ -166,6 +180,18 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
   int device;   // host only: the device the launch goes to
+  // Stored-tile backward: P and dS (dS times the softmax scale), 16-bit,
+  // each [B Hq n_qt 128 rows][n_kt 128 keys] row-major in the caller's
+  // workspace; views (64, B Hq n_qt 128, n_kt 2) with box 64 x 128 x 2.
+  CUtensorMap tm_ws_p;
+  CUtensorMap tm_ws_ds;
+  void* ws_p;
+  void* ws_ds;
+  long long ws_ld;   // keys per stored row (n_kt 128)
+  int kv_parts;      // scores kernel: key-tile ranges per query tile
+  int ts_nslot;      // scores kernel: ring depth
+  int tc_nslot;      // contraction kernel: ring depth
+  int n_dq_items, n_kv_items;   // contraction kernel: dQ items, and dV (= dK) items
 };
 
 struct Params {

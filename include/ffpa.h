@@ -306,6 +306,47 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
                         const ffpa_options* options);
 
 /*
+ * ffpa_bwd with a caller-owned workspace for the stored-tile backward: the
+ * same arguments, checks and results, plus
+ *
+ *   workspace, workspace_bytes: device memory of q's device, 16-byte
+ *     aligned, owned by the caller, of at least
+ *     ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D) bytes; its contents
+ *     on entry do not matter and on return are unspecified.
+ *
+ * When ffpa_bwd_workspace_bytes() is non-zero (dense layout, D = 256, 384
+ * or 512, Nq > 0, Nkv > 0) and the workspace is large enough, each
+ * (128-query, 128-key) tile's softmax P and dS (times scale) are formed
+ * once, as 16-bit values, into the workspace ([B Hq Nqp][Nkp] each, Nqp and
+ * Nkp rounded up to 128; P in the first half, dS in the second), and dq,
+ * dv, dk are contractions over the stored tiles: no product of the
+ * definition is computed twice (the ffpa_bwd kernels recompute S and dP for
+ * every 256-column output slice).  Three launches on `stream` (delta,
+ * scores, contraction).  Otherwise (workspace NULL or too small, or a shape
+ * the path does not take) this is ffpa_bwd and the workspace is not
+ * touched.  A workspace on another device, or not 16-byte aligned when it
+ * would be used, is FFPA_ERR_INVALID.  No allocation, no synchronisation.
+ */
+size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+ffpa_status ffpa_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                        const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
+                        int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],
+                        const int64_t k_str[4], const int64_t v_str[4], const int64_t o_str[4],
+                        const int64_t do_str[4], const int64_t dq_str[4], const int64_t dk_str[4],
+                        const int64_t dv_str[4], const void* mask, ffpa_mask_kind mask_kind,
+                        const int64_t mask_str[4], const float* scale, int is_causal, int enable_gqa,
+                        void* workspace, size_t workspace_bytes, ffpa_stream_t stream);
+ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           float* delta, ffpa_dtype dt, int B, int Hq, int Hkv, int Nq, int Nkv, int D,
+                           const int64_t q_str[4], const int64_t k_str[4], const int64_t v_str[4],
+                           const int64_t o_str[4], const int64_t do_str[4], const int64_t dq_str[4],
+                           const int64_t dk_str[4], const int64_t dv_str[4], const void* mask,
+                           ffpa_mask_kind mask_kind, const int64_t mask_str[4], const float* scale,
+                           int is_causal, int enable_gqa, void* workspace, size_t workspace_bytes,
+                           ffpa_stream_t stream, const ffpa_options* options);
+
+/*
  * Backward of ffpa_fwd_varlen (packed THD layout; FFPA API reference,
  * "ffpa_attn.ffpa_attn_varlen_func"): dq, dk, dv of sum(O * dout), each
  * sequence differentiated as its own dense problem (causal: lower right).

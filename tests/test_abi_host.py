@@ -251,6 +251,43 @@ def test_bwd_valid_call_without_gpu_reports_cuda_error(lib):
     assert bwd_call(lib) == pkg.FFPA_ERR_CUDA
 
 
+def test_bwd_workspace_bytes(lib):
+    """The stored-tile workspace: P and dS as 16-bit [B Hq Nqp][Nkp] with the
+    lengths rounded up to 128; zero where the path does not apply."""
+    wb = pkg.bwd_workspace_bytes
+    assert wb(1, 16, 16, 4096, 4096, 512) == 2 * 16 * 4096 * 4096 * 2
+    assert wb(2, 8, 2, 300, 129, 256) == 2 * (2 * 8 * 384) * 256 * 2
+    assert wb(1, 4, 1, 1, 1, 384) == 2 * 4 * 128 * 128 * 2
+    for D in (64, 128, 192, 320, 448, 576, 768, 1024):
+        assert wb(1, 2, 2, 256, 256, D) == 0, D          # the slice kernels only
+    assert wb(1, 2, 2, 0, 256, 512) == 0                 # no query rows
+    assert wb(1, 2, 2, 256, 0, 512) == 0                 # no keys
+    assert wb(1, 3, 2, 256, 256, 512) == 0               # not a grouping
+    assert wb(1 << 16, 1 << 8, 1, 1 << 10, 128, 512) == 0   # rows beyond 32-bit coordinates
+
+
+def bwd_ws_call(lib, ws, ws_bytes, D=512, dt=0):
+    def st(N):
+        return _arr([2 * N * D, N * D, D, 1])
+    s = st(128)
+    return lib.ffpa_bwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dt, 1, 2, 2, 128,
+                           128, D, s, s, s, s, s, s, s, s, None, 0, None, None, 0, 0, ws, ws_bytes, None)
+
+
+def test_bwd_ws_checks(lib):
+    need = pkg.bwd_workspace_bytes(1, 2, 2, 128, 128, 512)
+    # a workspace that would be used must be 16-byte aligned
+    assert bwd_ws_call(lib, FAKE + 8, need) == pkg.FFPA_ERR_INVALID
+    # argument errors come first, as for ffpa_bwd
+    assert bwd_ws_call(lib, FAKE, need, D=100) == pkg.FFPA_ERR_UNSUPPORTED
+    assert bwd_ws_call(lib, FAKE, need, dt=7) == pkg.FFPA_ERR_DTYPE
+    if not torch.cuda.is_available():
+        # a misaligned workspace that is too small is not used, so not checked
+        assert bwd_ws_call(lib, FAKE + 8, need - 1) == pkg.FFPA_ERR_CUDA
+        assert bwd_ws_call(lib, FAKE, need) == pkg.FFPA_ERR_CUDA
+        assert bwd_ws_call(lib, None, 0) == pkg.FFPA_ERR_CUDA
+
+
 def test_binding_checks_caller_outputs(lib):
     """Caller-supplied outputs must have the shape, dtype and device the library
     writes: the C side sizes every write from q and k."""

@@ -56,24 +56,27 @@ def draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype=torch.bfloat16):
     return q, k, v, dout
 
 
-def gpu_backward(q, k, v, dout, causal=False, scale=None, mask=None):
-    """Forward then backward on the GPU, as a training step would run them."""
+def gpu_backward(q, k, v, dout, causal=False, scale=None, mask=None, workspace="auto"):
+    """Forward then backward on the GPU, as a training step would run them.
+    workspace="auto" takes the stored-tile path where it applies (D = 256,
+    384, 512), None the slice kernels."""
     gqa = q.shape[1] != k.shape[1]
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
     md = None if mask is None else mask.to(DEV)
     o, lse = pkg.ffpa_fwd(qd, kd, vd, attn_mask=md, is_causal=causal, scale=scale, enable_gqa=gqa,
                           return_lse=True)
     dq, dk, dv, delta = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, is_causal=causal, scale=scale,
-                                     enable_gqa=gqa, attn_mask=md, return_delta=True)
+                                     enable_gqa=gqa, attn_mask=md, return_delta=True,
+                                     workspace=workspace)
     device_ok()
     return dq, dk, dv, delta, o
 
 
 def bwd_case(B, Hq, Hkv, Nq, Nkv, D, seed, causal=False, scale=None, dtype=torch.bfloat16,
-             mask=None):
+             mask=None, workspace="auto"):
     q, k, v, dout = draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype)
     m = mask(torch.Generator().manual_seed(seed + 7)) if callable(mask) else mask
-    dq, dk, dv, delta, o = gpu_backward(q, k, v, dout, causal, scale, m)
+    dq, dk, dv, delta, o = gpu_backward(q, k, v, dout, causal, scale, m, workspace)
     rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout, attn_mask=m, scale=scale, is_causal=causal)
     tag = f"B{B} Hq{Hq} Hkv{Hkv} Nq{Nq} Nkv{Nkv} D{D} causal={causal} {dtype}"
     check_grad(dq, rq, f"{tag} dQ")
@@ -119,27 +122,86 @@ def test_bwd_lengths(Nq, Nkv, causal):
     bwd_case(1, 2, 2, Nq, Nkv, 128, seed=Nq * 1000 + Nkv, causal=causal)
 
 
-@pytest.mark.parametrize("Nq", [1, 300])
-def test_bwd_single_key(Nq):
+@pytest.mark.parametrize("Nq,D", [(1, 128), (300, 128), (300, 256)])
+def test_bwd_single_key(Nq, D):
     """Nkv = 1: the softmax is the constant 1, so dV_0 = sum_i dO_i and dQ = dK = 0.
     The kernel reaches the zeros up to rounding: the recomputed P = exp2(s - lse)
     is 1 within fp32 rounding (|P - 1| <= 2^-21), and dP_i = dO_i . V_0 (tensor
     core) and delta_i = dO_i . O_i (O = V_0 exactly) are the same D products
     summed in fp32 in different orders, so they differ by at most
-    D * 2^-24 * sum_d |dO_id V_0d| (<= 2^-16 * that sum for D = 128).  Hence
-    |dS_i| <= e_i = 2^-21 |dP_i| + 2^-16 sum_d |dO_id V_0d|, |dQ_i| <= scale e_i
-    max|K_0| and |dK_0| <= scale sum_i e_i max|Q_i|; a factor 2 covers the final
-    16-bit rounding."""
-    q, k, v, dout = draw(1, 2, 2, Nq, 1, 128, seed=38 + Nq)
+    D * 2^-24 * sum_d |dO_id V_0d| (a factor 2 above that is taken: D 2^-23).
+    Hence |dS_i| <= e_i = 2^-21 |dP_i| + D 2^-23 sum_d |dO_id V_0d|, |dQ_i| <=
+    scale e_i max|K_0| and |dK_0| <= scale sum_i e_i max|Q_i|; a factor 2 covers
+    the 16-bit roundings of dS (stored tiles at D = 256) and of the outputs."""
+    q, k, v, dout = draw(1, 2, 2, Nq, 1, D, seed=38 + Nq + D)
     dq, dk, dv, _, _ = gpu_backward(q, k, v, dout)
-    scale = 128 ** -0.5
-    prod = dout.double() * v.double()                                    # [1,2,Nq,128]
-    e = 2.0 ** -21 * prod.sum(-1).abs() + 2.0 ** -16 * prod.abs().sum(-1)   # [1,2,Nq]
+    scale = D ** -0.5
+    prod = dout.double() * v.double()                                    # [1,2,Nq,D]
+    e = 2.0 ** -21 * prod.sum(-1).abs() + D * 2.0 ** -23 * prod.abs().sum(-1)   # [1,2,Nq]
     bq = 2 * scale * e.unsqueeze(-1) * k.double().abs().amax(-1, keepdim=True)
     assert (dq.double().cpu().abs() <= bq).all(), "dQ not zero within the rounding bound"
     bk = 2 * scale * (e * q.double().abs().amax(-1)).sum(-1)               # [1,2]
     assert (dk.double().cpu().abs().amax(-1).squeeze(-1) <= bk).all(), "dK not zero within the bound"
     check_grad(dv, dout.double().sum(2, keepdim=True), f"Nq{Nq} Nkv1 dV")
+
+
+# ------------------------------------------------------------------ stored tiles vs slices
+# D = 256, 384, 512 take the stored-tile path by default; the same cases on
+# the slice kernels (workspace=None) keep both paths checked.
+@pytest.mark.parametrize("D,causal", [(256, False), (384, True), (512, False), (512, True)])
+def test_bwd_sliced_path(D, causal):
+    bwd_case(1, 2, 2, 300, 300, D, seed=300 + D + causal, causal=causal, workspace=None)
+
+
+@pytest.mark.parametrize("Nq,Nkv,causal", [(200, 333, False), (130, 390, True), (1, 129, True),
+                                           (129, 3, False), (256, 256, True)])
+def test_bwd_tiles_lengths_gqa(Nq, Nkv, causal):
+    """Cross lengths, ragged tails on both sides, lower-right causal with more
+    keys than queries, GQA groups of 4 summed into one dK/dV tile."""
+    bwd_case(2, 4, 1, Nq, Nkv, 256, seed=Nq + 7 * Nkv, causal=causal)
+
+
+def test_bwd_tiles_masks():
+    B, H, Nq, Nkv = 1, 2, 190, 260
+    bwd_case(B, H, H, Nq, Nkv, 384, seed=57, mask=_bool_mask_with_dead_rows(B, H, Nq, Nkv))
+    bwd_case(2, 4, 2, 150, 270, 256, seed=58, causal=True,
+             mask=lambda g: torch.randn(1, 1, 150, 270, generator=g).bfloat16())
+
+
+def _sentinel_workspace(q, k, D):
+    B, Hq, Nq, _ = q.shape
+    need = pkg.bwd_workspace_bytes(B, Hq, k.shape[1], Nq, k.shape[2], D)
+    assert need == 2 * B * Hq * (-(-Nq // 128) * 128) * (-(-k.shape[2] // 128) * 128) * 2
+    return need
+
+
+def test_bwd_tiles_workspace_use():
+    """A large-enough caller workspace is written (the stored-tile path ran:
+    every stored P value is a probability, the rows of P sum to 1 over the
+    keys); one byte too small leaves it untouched (the slice kernels ran).
+    Both give the oracle's gradients."""
+    B, H, N, D = 1, 2, 200, 256
+    q, k, v, dout = draw(B, H, H, N, N, D, seed=59)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    o, lse = pkg.ffpa_fwd(qd, kd, vd, return_lse=True)
+    need = _sentinel_workspace(q, k, D)
+    rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout)
+    for extra, used in ((64, True), (-1, False)):
+        ws = torch.full((need + extra,), 0xFF, dtype=torch.uint8, device=DEV)
+        dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, workspace=ws)
+        device_ok()
+        check_grad(dq, rq, f"workspace {need + extra} dQ")
+        check_grad(dk, rk, f"workspace {need + extra} dK")
+        check_grad(dv, rv, f"workspace {need + extra} dV")
+        if not used:
+            assert bool((ws == 0xFF).all()), "a too-small workspace was written"
+            continue
+        npad = 256
+        p = ws[: need // 2].view(torch.bfloat16).reshape(B * H, npad, npad).float().cpu()
+        assert torch.isfinite(p).all() and (p >= 0).all() and (p <= 1.0001).all()
+        assert (p[:, N:, :] == 0).all() and (p[:, :, N:] == 0).all(), "padding of the stored P"
+        rowsum = p[:, :N, :N].double().sum(-1)
+        assert ((rowsum - 1).abs() < 2e-2).all(), "stored P rows do not sum to 1"
 
 
 # ------------------------------------------------------------------ masks
@@ -213,9 +275,9 @@ def test_bwd_empty_sides():
 
 
 # ------------------------------------------------------------------ large, sampled
-def _sampled(B, Hq, Hkv, N, D, seed, causal, q_heads, kv_heads, n_rows=48):
+def _sampled(B, Hq, Hkv, N, D, seed, causal, q_heads, kv_heads, n_rows=48, workspace="auto"):
     q, k, v, dout = draw(B, Hq, Hkv, N, N, D, seed)
-    dq, dk, dv, _, _ = gpu_backward(q, k, v, dout, causal)
+    dq, dk, dv, _, _ = gpu_backward(q, k, v, dout, causal, workspace=workspace)
     g = torch.Generator().manual_seed(seed)
     edge = [0, 1, 127, 128, N - 129, N - 1]
     qr = [h * N + i for h in q_heads for i in edge + torch.randint(0, N, (n_rows,), generator=g).tolist()]
@@ -227,9 +289,12 @@ def _sampled(B, Hq, Hkv, N, D, seed, causal, q_heads, kv_heads, n_rows=48):
     check_grad(dv.reshape(-1, D)[torch.tensor(kr, device=DEV)], rv, f"{tag} sampled dV")
 
 
-def test_bwd_full_size_d512_sampled():
-    """The self-attention workload B1 H16 N4096 D512 on sampled rows."""
-    _sampled(1, 16, 16, 4096, 512, seed=41, causal=False, q_heads=[0, 15], kv_heads=[7])
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_bwd_full_size_d512_sampled(workspace):
+    """The self-attention workload B1 H16 N4096 D512 on sampled rows (stored
+    tiles, as the benchmark runs it, and the slice kernels)."""
+    _sampled(1, 16, 16, 4096, 512, seed=41, causal=False, q_heads=[0, 15], kv_heads=[7],
+             workspace=workspace)
 
 
 def test_bwd_gqa_causal_d512_sampled():
@@ -288,21 +353,23 @@ def test_autograd_mask_gradient_raises():
 
 
 # ------------------------------------------------------------------ bounded waits
-def test_bwd_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_bwd_bounded_wait_reports_timeout_and_context_survives(workspace):
     """The first ring stage of every backward CTA is dropped (test hook): the MMA
     thread's wait on it runs out, the kernels drain, free TMEM and report
-    FFPA_ERR_DEVICE_TIMEOUT; the next call on the same context is correct."""
+    FFPA_ERR_DEVICE_TIMEOUT; the next call on the same context is correct.
+    Both the stored-tile kernels and the slice kernels."""
     q, k, v, dout = draw(1, 2, 2, 200, 200, 256, seed=61)
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
     o, lse = pkg.ffpa_fwd(qd, kd, vd, return_lse=True)
     device_ok()
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, status=status, wait_timeout_ns=200_000_000,
-                 test_drop_first_copy=True)
+                 test_drop_first_copy=True, workspace=workspace)
     torch.cuda.synchronize()
     assert int(status.item()) == pkg.FFPA_ERR_DEVICE_TIMEOUT
     assert pkg.ffpa_last_device_error() == pkg.FFPA_OK
-    dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse)
+    dq, dk, dv = pkg.ffpa_bwd(dod, qd, kd, vd, o, lse, workspace=workspace)
     device_ok()
     rq, rk, rv = oracle.attn_bwd_dense(q, k, v, dout)
     check_grad(dq, rq, "dQ after timeout")
