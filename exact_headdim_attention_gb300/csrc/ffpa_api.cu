@@ -429,34 +429,25 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, 
 }
 
 // Stored-tile backward: dense, D = 256, 384 or 512, at least one query row
-// and one key.  Workspace bytes (0: the path does not apply): P and dS,
-// 16-bit, [B Hq Nqp][Nkp] each (Nqp, Nkp rounded up to 128), dS first
-// byte at half the total.
+// and one key.  Workspace bytes (0: the path does not apply): a 32 KB block
+// of zeros, then P and dS, one 32 KB block (128 x 128 16-bit values) per
+// (b, hq, query tile, key tile) each.
 size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D) {
   if (!(D == 256 || D == 384 || D == 512) || B < 1 || Hq < 1 || Nq < 1 || Nkv < 1) return 0;
-  const long long nqp = ((long long)Nq + BM - 1) / BM * BM, nkp = ((long long)Nkv + BN - 1) / BN * BN;
-  const long long rows = (long long)B * Hq * nqp;
-  if (rows > 0x7fffffffLL) return 0;   // TMA row coordinates are 32-bit
-  return static_cast<size_t>(2 * rows * nkp * 2);
+  const long long blocks = (long long)B * Hq * ((Nq + BM - 1) / BM) * ((Nkv + BN - 1) / BN);
+  if (blocks > (1LL << 30)) return 0;
+  return static_cast<size_t>((2 * blocks + 1) * (long long)P_TILE_BYTES);
 }
 
 // Plans and launches the stored-tile path: the caller has set P as for
 // bwd_launch and checked the workspace (`ws`, bwd_tiles_bytes() bytes).
 ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o, cudaStream_t stream) {
-  const size_t need = bwd_tiles_bytes(P.B, P.Hq, P.Nq, P.Nkv, P.D);
   P.nchunks = P.D / DK;
   P.n_sl = 1;
-  const long long nqp = (long long)P.n_qt * BM, nkp = (long long)P.n_kt * BN;
-  P.ws_ld = nkp;
-  P.ws_p = ws;
-  P.ws_ds = static_cast<uint8_t*>(ws) + need / 2;
-  const CUtensorMapDataType tdt = P.fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t dims[3] = {64, (uint64_t)(P.B * P.Hq * nqp), (uint64_t)(nkp / 64)};
-  const uint64_t strides[2] = {(uint64_t)nkp * 2, 128};
-  const uint32_t box[3] = {64, BM, 2};
-  ffpa_status st = encode_map(&P.tm_ws_p, tdt, 3, P.ws_p, dims, strides, box);
-  if (st == FFPA_OK) st = encode_map(&P.tm_ws_ds, tdt, 3, P.ws_ds, dims, strides, box);
-  if (st != FFPA_OK) return st;
+  const long long blocks = (long long)P.B * P.Hq * P.n_qt * P.n_kt;
+  P.ws_zero = ws;
+  P.ws_p = static_cast<uint8_t*>(ws) + P_TILE_BYTES;
+  P.ws_ds = static_cast<uint8_t*>(ws) + (1 + blocks) * (long long)P_TILE_BYTES;
   // Scores kernel: dO (D/64 chunks) resident, then the ring.
   size_t ns = (SMEM_LIMIT - TS_STATIC_RESERVE - 1024 - (size_t)P.nchunks * CHUNK_BYTES) / SLOT_BYTES;
   if (ns > (size_t)TS_NSLOT_MAX) ns = TS_NSLOT_MAX;
@@ -468,13 +459,13 @@ ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o,
   const size_t smem_c = 1024 + nc * SLOT_BYTES;
   // Key-tile ranges per query tile (non-causal only; causal items are
   // ordered longest first instead): the count whose last wave is fullest,
-  // keeping at least 4 key tiles per range.
+  // keeping at least 8 key tiles per range (each range loads Q and dO once).
   const long long base = (long long)P.B * P.Hq * P.n_qt;
   P.kv_parts = 1;
   if (!P.causal && sms > 0) {
     double best = -1.0;
     for (int parts = 1; parts <= 4; parts *= 2) {
-      if (parts > 1 && P.n_kt / parts < 4) break;
+      if (parts > 1 && P.n_kt / parts < 8) break;
       const double waves = (double)(base * parts) / sms;
       const double eff = waves / std::ceil(waves);
       if (eff > best + 0.03) {
@@ -487,9 +478,11 @@ ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o,
   P.inject = o.drop;
   P.timeout_ns = o.timeout_ns;
   const long long score_items = base * P.kv_parts;
-  const long long n_dq = base, n_kv = (long long)P.B * P.Hkv * P.n_kt;
+  // Contraction: CTA pairs over two adjacent query tiles (dQ) or key tiles (dV, dK).
+  const long long n_dq = (long long)P.B * P.Hq * ((P.n_qt + 1) / 2);
+  const long long n_kv = (long long)P.B * P.Hkv * ((P.n_kt + 1) / 2);
   const long long contract_items = n_dq + 2 * n_kv;
-  if (score_items > 0x7fffffffLL || contract_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
+  if (score_items > 0x7fffffffLL || 2 * contract_items > 0x7fffffffLL) return FFPA_ERR_INVALID;
   P.n_dq_items = static_cast<int>(n_dq);
   P.n_kv_items = static_cast<int>(n_kv);
   return launch_bwd_tiles(P, static_cast<int>(score_items), static_cast<int>(contract_items), smem_s, smem_c,

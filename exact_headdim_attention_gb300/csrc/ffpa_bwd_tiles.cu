@@ -40,17 +40,19 @@ using namespace bwd;
 //   then they read dP and form dS.  Rows go to the workspace with 16-byte
 //   stores.
 //
-// Contraction kernel: one CTA per output tile of 128 rows x D columns (the
-// whole row in TMEM, up to 512 fp32 columns):
-//   dQ tile   one query tile of one query head, summed over its visible key
-//             tiles: A = stored dS tile (K-major), B = K (MN-major);
-//   dV tile   one key tile of one KV head, summed over the group's query
-//             heads and the query tiles that see it: A = stored P tile read
-//             as P^T (the same bytes, MN-major), B = dO (MN-major);
-//   dK tile   as dV with dS and Q.
-//   Warps 0-3 epilogue (TMEM -> 16-bit rows), 4 TMA producer, 5 MMA issuer.
-//   The three kinds of items are interleaved in one launch (each kind's own
-//   order puts its longest items first under causal masking).
+// Contraction kernel: CTA pairs (cta_group::2), each CTA one output tile of
+// 128 rows x D columns (the whole row in TMEM, up to 512 fp32 columns):
+//   dQ tiles  two adjacent query tiles of one query head, summed over the
+//             visible key tiles: A = stored dS tile (K-major), B = K;
+//   dV tiles  two adjacent key tiles of one KV head, summed over the group's
+//             query heads and the query tiles that see them: A = stored P
+//             tile read as P^T (the same bytes, MN-major), B = dO;
+//   dK tiles  as dV with dS and Q.
+//   B is read MN-major, each CTA loading its 128 of every 256 output columns.
+//   Warps 0-3 epilogue (TMEM -> 16-bit rows), 4 TMA producer, 5 MMA issuer
+//   (leader) or relay (peer).  The three kinds of items are interleaved in
+//   one launch (each kind's own order puts its longest items first under
+//   causal masking).
 // Every wait is bounded (FFPA_ERR_DEVICE_TIMEOUT on expiry, as elsewhere).
 // =====================================================================
 
@@ -69,6 +71,12 @@ constexpr int TC_MMA_WARP = 5;
 template <int NCH, bool UMASK>
 __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __grid_constant__ BwdParams p) {
   constexpr int NPR = NCH / 2;   // 32 KB stages per K (or V) tile
+  if (blockIdx.x == 0) {
+    // The block of zeros the contraction kernel reads for tiles outside a
+    // CTA's range.
+    uint4* z = static_cast<uint4*>(p.ws_zero);
+    for (int i = threadIdx.x; i < (int)(P_TILE_BYTES / 16); i += TS_THREADS) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const int part = blockIdx.x % p.kv_parts;
   BwdItem it;
   if (!bwd_decode<true>(p, blockIdx.x / p.kv_parts, it)) return;   // uniform across the CTA
@@ -291,12 +299,14 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
     if (UMASK)
       mrow = (long long)it.b * p.m_str[0] + (long long)it.hq * p.m_str[1] + (long long)my_row * p.m_str[2];
     const long long mstep = UMASK ? p.m_str[3] : 0;
-    // This thread's row of the stored P and dS (every row of the tile is
-    // written, zeros where the row or key is out of range).
-    const long long ws_off =
-        ((long long)(it.b * p.Hq + it.hq) * (p.n_qt * BM) + my_row) * p.ws_ld + 64 * half;
-    uint8_t* const prow = static_cast<uint8_t*>(p.ws_p) + ws_off * 2;
-    uint8_t* const dsrow = static_cast<uint8_t*>(p.ws_ds) + ws_off * 2;
+    // This thread's 16-byte units (keys 64 half + 8 q .. +7, q = 0..7) of row
+    // r in the stored blocks: every row of a block is written, zeros where
+    // the row or key is out of range.  A warp's store covers 32 consecutive
+    // rows of one unit: 512 contiguous bytes.
+    const long long blk0 = ((long long)(it.b * p.Hq + it.hq) * p.n_qt + it.row0 / BM) * p.n_kt;
+    const long long uoff = (blk0 << 15) + (long long)(8 * half) * 2048 + r * 16;
+    uint8_t* const pbase = static_cast<uint8_t*>(p.ws_p) + uoff;
+    uint8_t* const dsbase = static_cast<uint8_t*>(p.ws_ds) + uoff;
     const int c_lo = 64 * half;
     for (int jj = 0; jj < T && ok; ++jj) {
       const int rs = (j0 + jj) * BN;   // first key of the tile
@@ -335,11 +345,11 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
       {
-        uint4* dst = reinterpret_cast<uint4*>(prow + (long long)rs * 2);
+        uint8_t* const dst = pbase + ((long long)(j0 + jj) << 15);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float* x = pv + 8 * q;
-          dst[q] = fp16 ? make_uint4(pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]),
+          *reinterpret_cast<uint4*>(dst + q * 2048) = fp16 ? make_uint4(pack_f16(x[0], x[1]), pack_f16(x[2], x[3]), pack_f16(x[4], x[5]),
                                      pack_f16(x[6], x[7]))
                         : make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
                                      pack_bf16(x[6], x[7]));
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       ok = __all_sync(0xffffffffu, w);
       if (!ok) break;
       tc_fence_after();
-      uint4* dst = reinterpret_cast<uint4*>(dsrow + (long long)rs * 2);
+      uint8_t* const dst = dsbase + ((long long)(j0 + jj) << 15);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         uint32_t dr[16];
@@ -368,7 +378,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const float* y = x + 8 * q;
-          dst[2 * g + q] = fp16 ? make_uint4(pack_f16(y[0], y[1]), pack_f16(y[2], y[3]),
+          *reinterpret_cast<uint4*>(dst + (2 * g + q) * 2048) = fp16 ? make_uint4(pack_f16(y[0], y[1]), pack_f16(y[2], y[3]),
                                              pack_f16(y[4], y[5]), pack_f16(y[6], y[7]))
                                 : make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
                                              pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
@@ -386,7 +396,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
   }
 }
 
-// Role and rank of contraction item L: dQ, dV and dK items interleaved
+// Role and rank of contraction pair item L: dQ, dV and dK items interleaved
 // (rank r of each kind at 3 r, 3 r + 1, 3 r + 2), then the remaining items
 // of the more numerous kind.
 __device__ __forceinline__ void contract_role(const BwdParams& p, int L, int& role, int& rank) {
@@ -403,15 +413,86 @@ __device__ __forceinline__ void contract_role(const BwdParams& p, int L, int& ro
   }
 }
 
+// Key tiles the scores kernel writes for query tile qt (its visible key
+// tiles; 0 past the last query tile).
+__device__ __forceinline__ int written_key_tiles(const BwdParams& p, int qt) {
+  if (qt >= p.n_qt) return 0;
+  long long kv_end = p.Nkv;
+  if (p.causal) kv_end = min(kv_end, (long long)min(p.Nq, (qt + 1) * BM) + (p.Nkv - p.Nq));
+  return kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+}
+
+// One output tile pair of the contraction kernel: two adjacent query tiles
+// (dQ) or key tiles (dV, dK) of one head, rank r of the pair owning tile
+// tile0 + r.  Both CTAs walk the same contraction steps (the union of their
+// ranges; a step outside a CTA's own range contributes a zero tile).
+struct PairItem {
+  int role, b, hq, hkv;
+  int tile0, my_tile;
+  int n_iter;       // contraction steps
+  int qt_first;     // dV / dK: first query tile of the range
+  int nq;           // dV / dK: query tiles per head in the range
+};
+
+__device__ __forceinline__ void decode_pair_item(const BwdParams& p, int L, uint32_t rank, PairItem& it) {
+  int r;
+  contract_role(p, L, it.role, r);
+  if (it.role == BWD_ROLE_DQ) {
+    const int heads = p.B * p.Hq, npt = (p.n_qt + 1) >> 1;
+    int pt, bh;
+    if (p.causal) {            // longest query tiles (most visible keys) first
+      bh = r % heads;
+      pt = npt - 1 - r / heads;
+    } else {
+      pt = r % npt;
+      bh = r / npt;
+    }
+    it.hq = bh % p.Hq;
+    it.b = bh / p.Hq;
+    it.hkv = it.hq / p.group;
+    it.tile0 = 2 * pt;
+    it.n_iter = written_key_tiles(p, min(it.tile0 + 1, p.n_qt - 1));
+    it.qt_first = 0;
+    it.nq = 0;
+  } else {
+    const int heads = p.B * p.Hkv, nkp = (p.n_kt + 1) >> 1;
+    int kp, bh;
+    if (p.causal) {            // key tile 0 is seen by every query tile: first
+      bh = r % heads;
+      kp = r / heads;
+    } else {
+      kp = r % nkp;
+      bh = r / nkp;
+    }
+    it.hkv = bh % p.Hkv;
+    it.b = bh / p.Hkv;
+    it.hq = it.hkv * p.group;
+    it.tile0 = 2 * kp;
+    // Query row i sees key k when k <= i + (Nkv - Nq): the first query tile
+    // with a row that sees the pair's first key.
+    const int first_row = p.causal ? max(0, it.tile0 * BN - (p.Nkv - p.Nq)) : 0;
+    it.qt_first = first_row / BM;
+    it.nq = max(0, p.n_qt - it.qt_first);
+    it.n_iter = p.group * it.nq;
+  }
+  it.my_tile = it.tile0 + (int)rank;
+}
+
+// Contraction kernel on CTA pairs (cta_group::2): one M = 256 MMA per
+// 16-row step covers both CTAs' output tiles, and each CTA loads only half
+// of the shared B operand (its 128 of every 256 output columns), so per SM
+// the bytes per multiply-add are about 60 % of a single CTA's.  The peer's
+// warp 5 relays its "stage landed" events to the leader's full barriers; the
+// leader's commits arrive in both CTAs.
 template <int NCH>
-__global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const __grid_constant__ BwdParams p) {
-  constexpr int NPR = NCH / 2;   // 32 KB B-operand stages per contraction step (128 output columns each)
-  int role, rank;
-  contract_role(p, blockIdx.x, role, rank);
-  const bool dq_role = role == BWD_ROLE_DQ;
-  BwdItem it;
-  const bool have = dq_role ? bwd_decode<true>(p, rank, it) : bwd_decode<false>(p, rank, it);
-  if (!have) return;   // uniform across the CTA
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+    ffpa_bwd_contract_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int NG = (NCH + 3) / 4;   // 256-column groups (the last may have 128)
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  PairItem it;
+  decode_pair_item(p, blockIdx.x >> 1, rank, it);
+  const bool dq_role = it.role == BWD_ROLE_DQ;
   const int T = it.n_iter;
   const bool fp16 = p.fp16 != 0;
   const int NS = p.tc_nslot;
@@ -429,8 +510,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // Leader full barriers also count the peer's relayed arrival.
     for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_full[i]), leader ? 2 : 1);
       mbar_init(smem_u32(&bar_empty[i]), 1);
     }
     mbar_init(smem_u32(&bar_acc), 1);
@@ -439,26 +521,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
     fence_mbar_init();
   }
   if (warp == TC_MMA_WARP) {
-    tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_base_sh), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();      // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int nqp = p.n_qt * BM;
 
   if (warp == TC_PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    // Per contraction step: the stored tile (A), then the B operand's chunk pairs.
+    // Per contraction step: this CTA's stored tile (A), then its half of
+    // each 256-column group of the B operand.
     if (lane == 0 && T > 0) {
-      const CUtensorMap* amap = role == BWD_ROLE_DV ? &p.tm_ws_p : &p.tm_ws_ds;
-      const CUtensorMap* bmap = dq_role ? &p.tm_k : role == BWD_ROLE_DV ? &p.tm_do : &p.tm_q;
-      prefetch_tmap(amap);
+      const uint8_t* abase = static_cast<const uint8_t*>(it.role == BWD_ROLE_DV ? p.ws_p : p.ws_ds);
+      const CUtensorMap* bmap = dq_role ? &p.tm_k : it.role == BWD_ROLE_DV ? &p.tm_do : &p.tm_q;
       prefetch_tmap(bmap);
       int slot = 0, issued = 0;
       uint32_t lap = 0;
-      bool drop = p.inject != 0;   // test hook, as in the scores kernel
+      bool drop = leader && p.inject != 0;   // test hook, as in the scores kernel
       auto acquire = [&](uint32_t& fb) -> uint32_t {
         const uint32_t eb = smem_u32(&bar_empty[slot]);
         if (!mbar_try_wait(eb, lap ^ 1u) && !wait_bounded(eb, lap ^ 1u, &abort_flag, tmo, err)) return ~0u;
@@ -475,28 +557,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
       };
       bool ok = true;
       for (int i = 0; i < T && ok; ++i) {
-        int ws_row, ws_kc, b_row, b_head;
+        int qt, kt, head, b_row;
         if (dq_role) {
-          ws_row = (it.b * p.Hq + it.hq) * nqp + it.row0;
-          ws_kc = i * (BN / DK);
+          qt = it.my_tile;
+          kt = i;
+          head = it.hq;
           b_row = i * BN;
-          b_head = it.hkv;
         } else {
-          const int hs = it.hq + i / it.nq;
-          const int qrow = (it.qt_first + i % it.nq) * BM;
-          ws_row = (it.b * p.Hq + hs) * nqp + qrow;
-          ws_kc = it.row0 / DK;
-          b_row = qrow;
-          b_head = hs;
+          head = it.hq + i / it.nq;
+          qt = it.qt_first + i % it.nq;
+          kt = it.my_tile;
+          b_row = qt * BM;
         }
+        const bool real = kt < p.n_kt && kt < written_key_tiles(p, qt);
         uint32_t fb = 0;
         uint32_t dst = acquire(fb);
         if (dst == ~0u) { ok = false; break; }
-        if (dst) tma_load_3d(dst, amap, fb, 0, ws_row, ws_kc);
-        for (int pr = 0; pr < NPR; ++pr) {
+        if (dst) {
+          const void* src =
+              real ? static_cast<const void*>(abase + ((((long long)(it.b * p.Hq + head) * p.n_qt + qt) * p.n_kt + kt)
+                                                       << 15))
+                   : p.ws_zero;
+          bulk_load_g2s(dst, src, P_TILE_BYTES, fb);
+        }
+        const int b_head = dq_role ? it.hkv : head;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
           dst = acquire(fb);
           if (dst == ~0u) { ok = false; break; }
-          if (dst) tma_load_5d(dst, bmap, fb, 0, b_row, 2 * pr, b_head, it.b);
+          // 256-column group: chunks 4g + 2 rank, +1; a 128-column tail: chunk 4g + rank.
+          const int c0 = (4 * g + 4 <= NCH) ? 4 * g + 2 * (int)rank : 4 * g + (int)rank;
+          if (dst) tma_load_5d(dst, bmap, fb, 0, b_row, c0, b_head, it.b);
         }
       }
       const int n = issued < NS ? issued : NS;
@@ -504,12 +595,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
       uint32_t lp = lap;
       for (int i = 0; i < n; ++i) {
         if (--s < 0) { s = NS - 1; lp ^= 1u; }
-        if (p.inject != 0 && issued - 1 - i == 0) continue;   // the dropped stage was never armed
+        if (leader && p.inject != 0 && issued - 1 - i == 0) continue;   // the dropped stage was never armed
         wait_drain(smem_u32(&bar_full[s]), lp, tmo, err);
       }
     }
+  } else if (warp == TC_MMA_WARP && !leader) {
+    // ------------------------------------------------------------ relay (peer)
+    if (lane == 0 && T > 0) {
+      int slot = 0;
+      uint32_t lap = 0;
+      for (int i = 0; i < T * (1 + NG); ++i) {
+        const uint32_t fb = smem_u32(&bar_full[slot]);
+        if (!(mbar_try_wait(fb, lap) || wait_bounded(fb, lap, &abort_flag, tmo, err))) break;
+        mbar_arrive_cluster(mapa_shared(fb, 0));
+        if (++slot == NS) { slot = 0; lap ^= 1u; }
+      }
+    }
   } else if (warp == TC_MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer (leader)
     if (lane == 0 && T > 0) {
       int slot = 0;
       uint32_t lap = 0;
@@ -520,42 +623,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
         if (++slot == NS) { slot = 0; lap ^= 1u; }
         return s;
       };
-      // dQ: A = dS (rows = queries, K-major over keys).  dV / dK: A = P^T or
-      // dS^T, the stored tile read MN-major (M = keys in two 64-key chunks
-      // 16 KB apart, +2048 bytes per 16 queries).  B always MN-major.
-      const uint32_t idesc = idesc_f16(!fp16, BM, 128, !dq_role, true);
+      // The stored block without swizzle: core matrices of 8 rows x 8 keys
+      // (128 bytes), 2048 bytes apart along the keys and 128 along the rows.
+      // Without swizzle the descriptor's stride fields are: along K (leading
+      // byte offset) and along M (stride byte offset), for either major.
+      // dQ: A = dS K-major (M = queries, K = keys; +4096 bytes per 16 keys).
+      // dV / dK: A = P^T or dS^T, the same bytes MN-major (M = keys, K =
+      // queries; +256 bytes per 16 queries).  B always MN-major.
       bool ok = true;
       for (int i = 0; i < T && ok; ++i) {
         const int sa = take();
         if (sa < 0) { ok = false; break; }
         const uint32_t a_u32 = ring_u32 + sa * SLOT_BYTES;
-        const uint64_t a_desc = dq_role ? sdesc_sw128(a_u32, 16, 1024) : sdesc_sw128(a_u32, CHUNK_BYTES, 1024);
+        const uint64_t a_desc = dq_role ? sdesc_noswz(a_u32, 2048, 128) : sdesc_noswz(a_u32, 128, 2048);
 #pragma unroll
-        for (int pr = 0; pr < NPR; ++pr) {
+        for (int g = 0; g < NG; ++g) {
           const int sb = take();
           if (sb < 0) { ok = false; break; }
+          const int ng = (4 * g + 4 <= NCH) ? 256 : 128;
+          const uint32_t idesc = idesc_f16(!fp16, 2 * BM, ng, !dq_role, true);
           const uint64_t bd = sdesc_sw128(ring_u32 + sb * SLOT_BYTES, CHUNK_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t ad = dq_role ? a_desc + (((kk >> 2) * CHUNK_BYTES) >> 4) + 2 * (kk & 3)
-                                        : a_desc + 128 * kk;
-            umma_ss(tmem + 128 * pr, ad, bd + 128 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t ad = dq_role ? a_desc + 256 * kk : a_desc + 16 * kk;
+            umma_ss_pair(tmem + 256 * g, ad, bd + 128 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(smem_u32(&bar_empty[sb]));
+          umma_commit_pair(smem_u32(&bar_empty[sb]));
         }
         if (!ok) break;
-        umma_commit(smem_u32(&bar_empty[sa]));
+        umma_commit_pair(smem_u32(&bar_empty[sa]));
       }
-      if (ok) umma_commit(smem_u32(&bar_acc));
+      if (ok) umma_commit_pair(smem_u32(&bar_acc));
       const uint32_t drb = smem_u32(&bar_drain);
-      umma_commit(drb);
+      umma_commit_pair(drb);
       wait_drain(drb, 0, tmo, err);
     }
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
-    const int r = warp * 32 + lane;
+    // Warp w's 32 rows go through ring slot w (idle once the accumulator is
+    // complete): thread t writes its row's 16-bit values there (16-byte unit
+    // x of row t at unit x ^ (t & 7), conflict-free), then the warp stores
+    // the rows one by one, each warp store covering 512 contiguous bytes.
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int my_row = it.row0 + r;
     bool ok = true;
     if (T > 0) {
       const bool w = wait_bounded(smem_u32(&bar_acc), 0, &abort_flag, tmo, err);
@@ -563,25 +672,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1) ffpa_bwd_contract_kernel(const 
       if (ok) tc_fence_after();
     }
     if (ok) {
-      uint8_t* dst = nullptr;
-      if (dq_role) {
-        if (my_row < it.q_len)
-          dst = static_cast<uint8_t*>(p.dq) + bwd_row_offset(p, it, p.dq_str, it.q_row0, my_row, it.hq) * 2;
-      } else if (my_row < it.kv_len) {
-        const bool dv_role = role == BWD_ROLE_DV;
-        dst = static_cast<uint8_t*>(dv_role ? p.dv : p.dk) +
-              bwd_row_offset(p, it, dv_role ? p.dv_str : p.dk_str, it.kv_row0, my_row, it.hkv) * 2;
+      constexpr int ROWB = NCH * DK * 2;   // bytes of one output row
+      constexpr int UNITS = ROWB / 16;
+      const uint32_t stage = ring_u32 + warp * SLOT_BYTES;
+      const uint32_t sw = (uint32_t)(lane & 7);
+#pragma unroll 1
+      for (int c0 = 0; c0 < NCH * DK; c0 += 32) {
+        uint32_t v[32];
+        if (T > 0) {
+          tmem_ld32(lane_base + c0, v);
+          tmem_wait_ld();
+          reg_fence(v);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = __uint_as_float(v[2 * c]), a1 = __uint_as_float(v[2 * c + 1]);
+          pk[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t x = (uint32_t)(c0 / 8 + q);
+          st_shared_v4(stage + lane * ROWB + ((x ^ sw) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
       }
-      bwd_store_row(lane_base, p.D, 1.f, dst, fp16, T > 0);
+      __syncwarp();
+      BwdItem bi;
+      bi.b = it.b;
+      bi.q_row0 = 0;
+      bi.kv_row0 = 0;
+      const bool dv_role = it.role == BWD_ROLE_DV;
+      uint8_t* const obase = static_cast<uint8_t*>(dq_role ? p.dq : dv_role ? p.dv : p.dk);
+      const int64_t* ostr = dq_role ? p.dq_str : dv_role ? p.dv_str : p.dk_str;
+      const int head = dq_role ? it.hq : it.hkv;
+      const int rows = dq_role ? p.Nq : p.Nkv;
+      const int row0 = it.my_tile * BM + warp * 32;
+#pragma unroll 1
+      for (int rr = 0; rr < 32 && row0 + rr < rows; ++rr) {
+        uint8_t* const orow = obase + bwd_row_offset(p, bi, ostr, 0, row0 + rr, head) * 2;
+        const uint32_t srow = stage + rr * ROWB;
+        const uint32_t rsw = (uint32_t)(rr & 7);
+#pragma unroll
+        for (int x = lane; x < UNITS; x += 32) {
+          const uint4 val = ld_shared_v4(srow + (((uint32_t)x ^ rsw) << 4));
+          *reinterpret_cast<uint4*>(orow + x * 16) = val;
+        }
+      }
     }
   }
 
+  // The leader's last commits also arrive in the peer: wait for them before
+  // the pair may exit, then free TMEM in both CTAs together.
+  if (!leader && threadIdx.x == 0 && T > 0) wait_drain(smem_u32(&bar_drain), 0, tmo, err);
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == TC_MMA_WARP) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 
@@ -599,7 +751,7 @@ static ffpa_status launch_tiles_t(const BwdParams& P, int score_items, int contr
     auto kc = ffpa_bwd_contract_kernel<NCH>;
     const ffpa_status st = set_smem_attr_once(reinterpret_cast<const void*>(kc), P.device, static_cast<int>(smem_c));
     if (st != FFPA_OK) return st;
-    kc<<<contract_items, TC_THREADS, smem_c, stream>>>(P);
+    kc<<<2 * contract_items, TC_THREADS, smem_c, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
   return FFPA_OK;

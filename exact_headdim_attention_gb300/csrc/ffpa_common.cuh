@@ -180,14 +180,14 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
   int device;   // host only: the device the launch goes to
-  // Stored-tile backward: P and dS (dS times the softmax scale), 16-bit,
-  // each [B Hq n_qt 128 rows][n_kt 128 keys] row-major in the caller's
-  // workspace; views (64, B Hq n_qt 128, n_kt 2) with box 64 x 128 x 2.
-  CUtensorMap tm_ws_p;
-  CUtensorMap tm_ws_ds;
+  // Stored-tile backward: P and dS (dS times the softmax scale), 16-bit, one
+  // 32 KB block per (b, hq, query tile, key tile) in the caller's workspace,
+  // blocks ordered by (b Hq + hq, query tile, key tile); inside a block the
+  // 16-byte unit of 8 keys (8u .. 8u+7) of row r sits at byte 2048 u + 16 r
+  // (the tensor core's layout without swizzle).  ws_zero: one block of zeros.
+  void* ws_zero;
   void* ws_p;
   void* ws_ds;
-  long long ws_ld;   // keys per stored row (n_kt 128)
   int kv_parts;      // scores kernel: key-tile ranges per query tile
   int ts_nslot;      // scores kernel: ring depth
   int tc_nslot;      // contraction kernel: ring depth

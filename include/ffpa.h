@@ -317,11 +317,13 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
  * When ffpa_bwd_workspace_bytes() is non-zero (dense layout, D = 256, 384
  * or 512, Nq > 0, Nkv > 0) and the workspace is large enough, each
  * (128-query, 128-key) tile's softmax P and dS (times scale) are formed
- * once, as 16-bit values, into the workspace ([B Hq Nqp][Nkp] each, Nqp and
- * Nkp rounded up to 128; P in the first half, dS in the second), and dq,
- * dv, dk are contractions over the stored tiles: no product of the
- * definition is computed twice (the ffpa_bwd kernels recompute S and dP for
- * every 256-column output slice).  Three launches on `stream` (delta,
+ * once, as 16-bit values, into the workspace, and dq, dv, dk are
+ * contractions over the stored tiles: no product of the definition is
+ * computed twice (the ffpa_bwd kernels recompute S and dP for every
+ * 256-column output slice).  Workspace layout: a 32 KB block of zeros, then
+ * P, then dS, each one 32 KB block per (b, hq, query tile, key tile) in that
+ * order; inside a block the 8 keys 8u .. 8u+7 of tile row r are the 16 bytes
+ * at 2048 u + 16 r.  Three launches on `stream` (delta,
  * scores, contraction).  Otherwise (workspace NULL or too small, or a shape
  * the path does not take) this is ffpa_bwd and the workspace is not
  * touched.  A workspace on another device, or not 16-byte aligned when it

@@ -252,18 +252,19 @@ def test_bwd_valid_call_without_gpu_reports_cuda_error(lib):
 
 
 def test_bwd_workspace_bytes(lib):
-    """The stored-tile workspace: P and dS as 16-bit [B Hq Nqp][Nkp] with the
-    lengths rounded up to 128; zero where the path does not apply."""
+    """The stored-tile workspace: a 32 KB block of zeros, then P and dS as one
+    32 KB block (128 x 128 16-bit values) per (b, hq, query tile, key tile)
+    each; zero where the path does not apply."""
     wb = pkg.bwd_workspace_bytes
-    assert wb(1, 16, 16, 4096, 4096, 512) == 2 * 16 * 4096 * 4096 * 2
-    assert wb(2, 8, 2, 300, 129, 256) == 2 * (2 * 8 * 384) * 256 * 2
-    assert wb(1, 4, 1, 1, 1, 384) == 2 * 4 * 128 * 128 * 2
+    assert wb(1, 16, 16, 4096, 4096, 512) == (2 * 16 * 32 * 32 + 1) * 32768
+    assert wb(2, 8, 2, 300, 129, 256) == (2 * 2 * 8 * 3 * 2 + 1) * 32768
+    assert wb(1, 4, 1, 1, 1, 384) == (2 * 4 + 1) * 32768
     for D in (64, 128, 192, 320, 448, 576, 768, 1024):
         assert wb(1, 2, 2, 256, 256, D) == 0, D          # the slice kernels only
     assert wb(1, 2, 2, 0, 256, 512) == 0                 # no query rows
     assert wb(1, 2, 2, 256, 0, 512) == 0                 # no keys
     assert wb(1, 3, 2, 256, 256, 512) == 0               # not a grouping
-    assert wb(1 << 16, 1 << 8, 1, 1 << 10, 128, 512) == 0   # rows beyond 32-bit coordinates
+    assert wb(1 << 16, 1 << 8, 1, 1 << 17, 128, 512) == 0   # more than 2^30 blocks
 
 
 def bwd_ws_call(lib, ws, ws_bytes, D=512, dt=0):

@@ -171,8 +171,17 @@ def test_bwd_tiles_masks():
 def _sentinel_workspace(q, k, D):
     B, Hq, Nq, _ = q.shape
     need = pkg.bwd_workspace_bytes(B, Hq, k.shape[1], Nq, k.shape[2], D)
-    assert need == 2 * B * Hq * (-(-Nq // 128) * 128) * (-(-k.shape[2] // 128) * 128) * 2
+    assert need == (2 * B * Hq * (-(-Nq // 128)) * (-(-k.shape[2] // 128)) + 1) * 32768
     return need
+
+
+def _stored_p(ws, BH, n_qt, n_kt):
+    """The stored P of the workspace as [BH, n_qt 128, n_kt 128]: blocks of
+    32 KB per (bh, query tile, key tile) after the 32 KB zero block, 16-byte
+    unit u (keys 8u..8u+7) of row r at byte 2048 u + 16 r."""
+    blocks = ws[32768: 32768 + BH * n_qt * n_kt * 32768].view(torch.bfloat16).float().cpu()
+    t = blocks.reshape(BH, n_qt, n_kt, 16, 128, 8).permute(0, 1, 4, 2, 3, 5)
+    return t.reshape(BH, n_qt * 128, n_kt * 128)
 
 
 def test_bwd_tiles_workspace_use():
@@ -196,8 +205,8 @@ def test_bwd_tiles_workspace_use():
         if not used:
             assert bool((ws == 0xFF).all()), "a too-small workspace was written"
             continue
-        npad = 256
-        p = ws[: need // 2].view(torch.bfloat16).reshape(B * H, npad, npad).float().cpu()
+        assert bool((ws[:32768] == 0).all()), "the zero block"
+        p = _stored_p(ws, B * H, 2, 2)
         assert torch.isfinite(p).all() and (p >= 0).all() and (p <= 1.0001).all()
         assert (p[:, N:, :] == 0).all() and (p[:, :, N:] == 0).all(), "padding of the stored P"
         rowsum = p[:, :N, :N].double().sum(-1)
