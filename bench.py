@@ -672,11 +672,11 @@ def run_ours_bwd(args):
         "clocks": clocks,
         "impl": "ours",
     }
-    tb = measured_traffic_bwd(w.name)
+    tb = measured_traffic_bwd(w.name) if ws is not None else None
     if tb is not None:
         line["roofline"]["traffic"] = tb["gradient_kernels_total"]
-        line["roofline"]["traffic_note"] = ("ncu DRAM bytes of the dQ, dV and dK launches of one step "
-                                            "(delta kernel not captured)")
+        line["roofline"]["traffic_note"] = ("ncu DRAM bytes of the scores and contraction launches of one "
+                                            "step (delta kernel not captured)")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_bwd(w, x, dout, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -733,8 +733,9 @@ def _traffic_section(key, path):
 
 
 def measured_traffic_bwd(name, path=TRAFFIC_PATH):
-    """DRAM bytes of one backward step's dQ, dV and dK launches from the committed
-    ncu summary, or None when that capture was taken on different kernel code."""
+    """DRAM bytes of one stored-tile backward step's scores and contraction launches
+    from the committed ncu summary, or None when that capture was taken on
+    different kernel code."""
     sec = _traffic_section("bwd_dram_bytes_per_step", path)
     return None if sec is None else sec.get(name)
 

@@ -356,8 +356,9 @@ def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
     return mk, m.data_ptr(), _strides(m), m
 
 
-# Largest stored-tile workspace ffpa_bwd allocates by itself (workspace="auto").
-BWD_AUTO_WORKSPACE_MAX = 4 << 30
+# Largest stored-tile workspace ffpa_bwd allocates by itself (workspace="auto"):
+# at most this many bytes and at most a quarter of the device's free memory.
+BWD_AUTO_WORKSPACE_MAX = 32 << 30
 
 
 def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int) -> int:
@@ -372,7 +373,7 @@ def _bwd_workspace(workspace, need: int, device):
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be None, "auto" or a uint8 device tensor')
-        if need > BWD_AUTO_WORKSPACE_MAX:
+        if need > BWD_AUTO_WORKSPACE_MAX or need > torch.cuda.mem_get_info(device)[0] // 4:
             return None, 0, None
         workspace = torch.empty(need, dtype=torch.uint8, device=device)
     if (not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8
@@ -395,9 +396,9 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
 
     workspace: the stored-tile backward's scratch (see bwd_workspace_bytes):
     "auto" allocates it when the shape takes that path and it needs at most
-    BWD_AUTO_WORKSPACE_MAX bytes; None runs the slice kernels (S and dP
-    recomputed per 256-column output slice); a uint8 device tensor is used
-    when it is large enough."""
+    BWD_AUTO_WORKSPACE_MAX bytes and a quarter of the free device memory;
+    None runs the slice kernels (S and dP recomputed per 256-column output
+    slice); a uint8 device tensor is used when it is large enough."""
     lib = load_library()
     for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
         if t.dim() != 4:

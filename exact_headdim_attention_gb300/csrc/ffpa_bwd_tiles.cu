@@ -320,30 +320,32 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       const int kv_cols = it.kv_len - rs;                   // key columns in range
       const int mcols = (UMASK && my_row < it.q_len) ? kv_cols : 0;
       const long long moff = mrow + (long long)rs * mstep;
+      // This warp's 64 columns of S in one round trip; once they are in
+      // registers the next tile's S may overwrite them.
       float pv[64];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t sr[16];
-        tmem_ld16(lane_base + TS_S_COL + c_lo + 16 * g, sr);
+      {
+        uint32_t sa[32], sb[32];
+        tmem_ld32(lane_base + TS_S_COL + c_lo, sa);
+        tmem_ld32(lane_base + TS_S_COL + c_lo + 32, sb);
         tmem_wait_ld();
-        reg_fence(sr);
+        reg_fence(sa);
+        reg_fence(sb);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = c_lo + 16 * g + e;
-          float arg = fmaf(__uint_as_float(sr[e]), sl2, -lse_r);
+        for (int e = 0; e < 64; ++e) {
+          const int col = c_lo + e;
+          float arg = fmaf(__uint_as_float(e < 32 ? sa[e] : sb[e - 32]), sl2, -lse_r);
           if (UMASK && col < mcols) arg = add_mask_term(arg, mbase, moff + col * mstep, mkind, fp16);
           float v = ex2_approx(arg);
           if (need_mask) {
             const bool vis = col < kv_cols && (!causal || (long long)col <= lim);
             v = vis ? v : 0.f;
           }
-          pv[16 * g + e] = v;
+          pv[e] = v;
         }
       }
-      // S is in registers: the next tile's S may overwrite it.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_s_free));
       {
         uint8_t* const dst = pbase + ((long long)(j0 + jj) << 15);
 #pragma unroll
@@ -360,21 +362,24 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       if (!ok) break;
       tc_fence_after();
       uint8_t* const dst = dsbase + ((long long)(j0 + jj) << 15);
+      // dP likewise: one round trip, then the next tile's dP may overwrite it.
+      uint32_t da[32], db[32];
+      tmem_ld32(lane_base + TS_DP_COL + c_lo, da);
+      tmem_ld32(lane_base + TS_DP_COL + c_lo + 32, db);
+      tmem_wait_ld();
+      reg_fence(da);
+      reg_fence(db);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_dp_free));
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        uint32_t dr[16];
-        tmem_ld16(lane_base + TS_DP_COL + c_lo + 16 * g, dr);
-        tmem_wait_ld();
-        reg_fence(dr);
-        if (g == 3) {
-          // dP is in registers: the next tile's dP may overwrite it.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bar_dp_free));
-        }
         float x[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] = pv[16 * g + e] * sc * (__uint_as_float(dr[e]) - delta_r);
+        for (int e = 0; e < 16; ++e) {
+          const int c = 16 * g + e;
+          x[e] = pv[c] * sc * (__uint_as_float(c < 32 ? da[c] : db[c - 32]) - delta_r);
+        }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const float* y = x + 8 * q;
@@ -677,24 +682,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const uint32_t stage = ring_u32 + warp * SLOT_BYTES;
       const uint32_t sw = (uint32_t)(lane & 7);
 #pragma unroll 1
-      for (int c0 = 0; c0 < NCH * DK; c0 += 32) {
-        uint32_t v[32];
+      for (int c0 = 0; c0 < NCH * DK; c0 += 64) {   // 64 columns per TMEM round trip
+        uint32_t va[32], vb[32];
         if (T > 0) {
-          tmem_ld32(lane_base + c0, v);
+          tmem_ld32(lane_base + c0, va);
+          tmem_ld32(lane_base + c0 + 32, vb);
           tmem_wait_ld();
-          reg_fence(v);
+          reg_fence(va);
+          reg_fence(vb);
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = 0u;
+          for (int c = 0; c < 32; ++c) va[c] = vb[c] = 0u;
         }
-        uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a0 = __uint_as_float(v[2 * c]), a1 = __uint_as_float(v[2 * c + 1]);
+        for (int c = 0; c < 32; ++c) {
+          const int e = 2 * c;
+          const float a0 = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
+          const float a1 = __uint_as_float(e + 1 < 32 ? va[e + 1] : vb[e + 1 - 32]);
           pk[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
           const uint32_t x = (uint32_t)(c0 / 8 + q);
           st_shared_v4(stage + lane * ROWB + ((x ^ sw) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }

@@ -96,7 +96,7 @@ def test_traffic_record_is_used_only_for_the_sources_it_was_taken_on(tmp_path):
     rec = {"dram_bytes_per_launch": {"kernel_source_sha": sha["dram_bytes_per_launch"], "w": 123},
            "fp8_dram_bytes_per_launch": {"kernel_source_sha": sha["fp8_dram_bytes_per_launch"], "w": 45},
            "bwd_dram_bytes_per_step": {"kernel_source_sha": sha["bwd_dram_bytes_per_step"],
-                                       "w": {"dq": 1, "dv": 2, "dk": 3, "gradient_kernels_total": 6}}}
+                                       "w": {"scores": 1, "contract": 5, "gradient_kernels_total": 6}}}
     p = tmp_path / "traffic.json"
     p.write_text(json.dumps(rec))
     assert bench.measured_traffic("w", path=str(p)) == 123
@@ -119,4 +119,4 @@ def test_committed_traffic_record_is_consistent():
     for name, tb in d.get("bwd_dram_bytes_per_step", {}).items():
         if name == "kernel_source_sha":
             continue
-        assert tb["gradient_kernels_total"] == tb["dq"] + tb["dv"] + tb["dk"], name
+        assert tb["gradient_kernels_total"] == tb["scores"] + tb["contract"], name
