@@ -560,9 +560,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         mbar_arrive_expect_tx(fb, SLOT_BYTES);
         return dst;
       };
-      bool ok = true;
-      for (int i = 0; i < T && ok; ++i) {
-        int qt, kt, head, b_row;
+      // Step i's stored block (the zero block outside this CTA's range) and
+      // the B operand's rows and head.
+      auto step = [&](int i, int& b_row, int& head) -> const void* {
+        int qt, kt;
         if (dq_role) {
           qt = it.my_tile;
           kt = i;
@@ -575,16 +576,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           b_row = qt * BM;
         }
         const bool real = kt < p.n_kt && kt < written_key_tiles(p, qt);
+        return real ? static_cast<const void*>(abase + ((((long long)(it.b * p.Hq + head) * p.n_qt + qt) * p.n_kt + kt)
+                                                        << 15))
+                    : p.ws_zero;
+      };
+      // The stored blocks come from DRAM: each is requested into L2 this
+      // many steps before its copy into the ring.
+      constexpr int PF = 6;
+      for (int i = 0; i < PF && i < T; ++i) {
+        int br, hd;
+        prefetch_l2_bulk(step(i, br, hd), P_TILE_BYTES);
+      }
+      bool ok = true;
+      for (int i = 0; i < T && ok; ++i) {
+        int b_row, head;
+        const void* src = step(i, b_row, head);
+        if (i + PF < T) {
+          int br, hd;
+          prefetch_l2_bulk(step(i + PF, br, hd), P_TILE_BYTES);
+        }
         uint32_t fb = 0;
         uint32_t dst = acquire(fb);
         if (dst == ~0u) { ok = false; break; }
-        if (dst) {
-          const void* src =
-              real ? static_cast<const void*>(abase + ((((long long)(it.b * p.Hq + head) * p.n_qt + qt) * p.n_kt + kt)
-                                                       << 15))
-                   : p.ws_zero;
-          bulk_load_g2s(dst, src, P_TILE_BYTES, fb);
-        }
+        if (dst) bulk_load_g2s(dst, src, P_TILE_BYTES, fb);
         const int b_head = dq_role ? it.hkv : head;
 #pragma unroll
         for (int g = 0; g < NG; ++g) {

@@ -183,6 +183,13 @@ __device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* m, int c0, in
                : "memory");
 }
 
+// L2 prefetch of `bytes` (multiple of 16) of global memory at a 16-byte
+// aligned address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05 / TMEM
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
