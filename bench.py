@@ -564,7 +564,7 @@ def run_ours_bwd(args):
     # once: the timed steps and the end-to-end steps run on one stream at a
     # time, so they share it.
     B, Hq, Nq, D = x["q"].shape
-    ws_bytes = pkg.bwd_workspace_bytes(B, Hq, x["k"].shape[1], Nq, x["k"].shape[2], D)
+    ws_bytes = pkg.bwd_workspace_bytes(B, Hq, x["k"].shape[1], Nq, x["k"].shape[2], D, w.causal)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def backward(t, gr, stream=None):

@@ -105,7 +105,7 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_bwd_ws.restype = I
     lib.ffpa_bwd_ws_ex.argtypes = bws + [O]
     lib.ffpa_bwd_ws_ex.restype = I
-    lib.ffpa_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    lib.ffpa_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.ffpa_bwd_workspace_bytes.restype = ctypes.c_size_t
     # ffpa_bwd without the delta argument
     lib.ffpa_bwd_noalloc.argtypes = sigs["ffpa_bwd"][:9] + sigs["ffpa_bwd"][10:]
@@ -361,9 +361,10 @@ def _mask_args(attn_mask, q, B, Hq, Nq, Nkv):
 BWD_AUTO_WORKSPACE_MAX = 32 << 30
 
 
-def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int) -> int:
+def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int,
+                        is_causal: bool = False) -> int:
     """Bytes of the stored-tile backward's workspace (0: the shape does not take that path)."""
-    return int(load_library().ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+    return int(load_library().ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, int(bool(is_causal))))
 
 
 def _bwd_workspace(workspace, need: int, device):
@@ -417,7 +418,7 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
     mk, mptr, mstr, keep = _mask_args(attn_mask, q, B, Hq, Nq, Nkv)
     sc = None if scale is None else ctypes.byref(ctypes.c_float(float(scale)))
     opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
-    need = int(lib.ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D))
+    need = int(lib.ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, int(bool(is_causal))))
     ws_ptr, ws_bytes, ws_keep = _bwd_workspace(workspace, need, q.device)
     st = lib.ffpa_bwd_ws_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),

@@ -431,10 +431,12 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, 
 // Stored-tile backward: dense, D = 256, 384 or 512, at least one query row
 // and one key.  Workspace bytes (0: the path does not apply): a 32 KB block
 // of zeros, then P and dS, one 32 KB block (128 x 128 16-bit values) per
-// (b, hq, query tile, key tile) each.
-size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D) {
+// (b, hq, query tile, stored key tile) each (causal: only the key tiles the
+// query tile sees).
+size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D, int causal) {
   if (!(D == 256 || D == 384 || D == 512) || B < 1 || Hq < 1 || Nq < 1 || Nkv < 1) return 0;
-  const long long blocks = (long long)B * Hq * ((Nq + BM - 1) / BM) * ((Nkv + BN - 1) / BN);
+  if (causal && Nkv < Nq) return 0;
+  const long long blocks = (long long)B * Hq * bwd_stored_before((Nq + BM - 1) / BM, Nq, Nkv, causal);
   if (blocks > (1LL << 30)) return 0;
   return static_cast<size_t>((2 * blocks + 1) * (long long)P_TILE_BYTES);
 }
@@ -444,7 +446,8 @@ size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D) {
 ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o, cudaStream_t stream) {
   P.nchunks = P.D / DK;
   P.n_sl = 1;
-  const long long blocks = (long long)P.B * P.Hq * P.n_qt * P.n_kt;
+  P.ws_head = bwd_stored_before(P.n_qt, P.Nq, P.Nkv, P.causal);
+  const long long blocks = (long long)P.B * P.Hq * P.ws_head;
   P.ws_zero = ws;
   P.ws_p = static_cast<uint8_t*>(ws) + P_TILE_BYTES;
   P.ws_ds = static_cast<uint8_t*>(ws) + (1 + blocks) * (long long)P_TILE_BYTES;
@@ -804,7 +807,7 @@ ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const vo
   const bool any_q = Nq > 0, any_k = Nkv > 0;
   // The stored-tile path runs when it applies and the workspace holds it;
   // otherwise the sliced kernels run and the workspace is not touched.
-  const size_t ws_need = bwd_tiles_bytes(B, Hq, Nq, Nkv, D);
+  const size_t ws_need = bwd_tiles_bytes(B, Hq, Nq, Nkv, D, is_causal ? 1 : 0);
   const bool tiles = workspace != nullptr && ws_need > 0 && workspace_bytes >= ws_need;
   if (tiles && !aligned16(workspace)) return FFPA_ERR_INVALID;
   ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,
@@ -891,9 +894,9 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
                         scale, is_causal, enable_gqa, nullptr, 0, stream, options);
 }
 
-size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D) {
+size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int is_causal) {
   if (Hkv < 1 || Hq % Hkv != 0) return 0;
-  return bwd_tiles_bytes(B, Hq, Nq, Nkv, D);
+  return bwd_tiles_bytes(B, Hq, Nq, Nkv, D, is_causal ? 1 : 0);
 }
 
 ffpa_status ffpa_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dout,

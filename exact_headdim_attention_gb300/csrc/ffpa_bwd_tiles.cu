@@ -303,7 +303,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
     // r in the stored blocks: every row of a block is written, zeros where
     // the row or key is out of range.  A warp's store covers 32 consecutive
     // rows of one unit: 512 contiguous bytes.
-    const long long blk0 = ((long long)(it.b * p.Hq + it.hq) * p.n_qt + it.row0 / BM) * p.n_kt;
+    const long long blk0 = (long long)(it.b * p.Hq + it.hq) * p.ws_head +
+                           bwd_stored_before(it.row0 / BM, p.Nq, p.Nkv, p.causal);
     const long long uoff = (blk0 << 15) + (long long)(8 * half) * 2048 + r * 16;
     uint8_t* const pbase = static_cast<uint8_t*>(p.ws_p) + uoff;
     uint8_t* const dsbase = static_cast<uint8_t*>(p.ws_ds) + uoff;
@@ -418,15 +419,6 @@ __device__ __forceinline__ void contract_role(const BwdParams& p, int L, int& ro
   }
 }
 
-// Key tiles the scores kernel writes for query tile qt (its visible key
-// tiles; 0 past the last query tile).
-__device__ __forceinline__ int written_key_tiles(const BwdParams& p, int qt) {
-  if (qt >= p.n_qt) return 0;
-  long long kv_end = p.Nkv;
-  if (p.causal) kv_end = min(kv_end, (long long)min(p.Nq, (qt + 1) * BM) + (p.Nkv - p.Nq));
-  return kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
-}
-
 // One output tile pair of the contraction kernel: two adjacent query tiles
 // (dQ) or key tiles (dV, dK) of one head, rank r of the pair owning tile
 // tile0 + r.  Both CTAs walk the same contraction steps (the union of their
@@ -456,7 +448,7 @@ __device__ __forceinline__ void decode_pair_item(const BwdParams& p, int L, uint
     it.b = bh / p.Hq;
     it.hkv = it.hq / p.group;
     it.tile0 = 2 * pt;
-    it.n_iter = written_key_tiles(p, min(it.tile0 + 1, p.n_qt - 1));
+    it.n_iter = bwd_stored_tiles(min(it.tile0 + 1, p.n_qt - 1), p.Nq, p.Nkv, p.causal);
     it.qt_first = 0;
     it.nq = 0;
   } else {
@@ -575,14 +567,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           kt = it.my_tile;
           b_row = qt * BM;
         }
-        const bool real = kt < p.n_kt && kt < written_key_tiles(p, qt);
-        return real ? static_cast<const void*>(abase + ((((long long)(it.b * p.Hq + head) * p.n_qt + qt) * p.n_kt + kt)
-                                                        << 15))
-                    : p.ws_zero;
+        const bool real = qt < p.n_qt && kt < bwd_stored_tiles(qt, p.Nq, p.Nkv, p.causal);
+        const long long blk = (long long)(it.b * p.Hq + head) * p.ws_head + bwd_stored_before(qt, p.Nq, p.Nkv, p.causal) + kt;
+        return real ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
       };
-      // The stored blocks come from DRAM: each is requested into L2 this
-      // many steps before its copy into the ring.
-      constexpr int PF = 6;
+      // The stored blocks come from DRAM: for D >= 384 each is requested into
+      // L2 this many steps before its copy into the ring (measured at D = 512:
+      // 743 -> 725 us per launch; none at D = 256, whose steps are half as long).
+      constexpr int PF = NCH >= 6 ? 6 : 0;
       for (int i = 0; i < PF && i < T; ++i) {
         int br, hd;
         prefetch_l2_bulk(step(i, br, hd), P_TILE_BYTES);

@@ -146,6 +146,31 @@ constexpr int BWD_NSLOT_MAX = 6;
 constexpr size_t BWD_STATIC_RESERVE = 6144;
 constexpr int BWD_OUT_COLS = 256;          // dQ, dV or dK columns per CTA
 
+// Stored-tile backward: key tiles kept for query tile qt (those its rows
+// see: every key tile, or under causal masking (lower right, Nkv >= Nq) the
+// tiles up to its last row's limit), and the blocks of query tiles
+// 0 .. qt-1 of one head, in closed form: full query tiles t keep
+// min(n_kt, t + 1 + c) tiles with c = ceil((Nkv - Nq) / 128), the last one n_kt.
+__host__ __device__ inline int bwd_stored_tiles(int qt, int Nq, int Nkv, int causal) {
+  const int n_kt = (Nkv + BN - 1) / BN;
+  if (!causal) return n_kt;
+  const int rows_end = (qt + 1) * BM < Nq ? (qt + 1) * BM : Nq;
+  const long long kv_end0 = (long long)rows_end + (Nkv - Nq);
+  const long long kv_end = kv_end0 < Nkv ? kv_end0 : Nkv;
+  return kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
+}
+__host__ __device__ inline long long bwd_stored_before(int qt, int Nq, int Nkv, int causal) {
+  const long long n_kt = (Nkv + BN - 1) / BN, n_qt = (Nq + BM - 1) / BM;
+  if (!causal) return (long long)qt * n_kt;
+  const long long c = ((long long)(Nkv - Nq) + BN - 1) / BN;
+  const long long full = (long long)qt < n_qt - 1 ? qt : n_qt - 1;   // full query tiles below qt
+  const long long cap = n_kt - c > 0 ? n_kt - c : 0;                // tiles t < cap keep t + 1 + c
+  const long long a = full < cap ? full : cap;
+  long long s = a * (a + 1) / 2 + c * a + (full - a) * n_kt;
+  if ((long long)qt > n_qt - 1) s += n_kt;
+  return s;
+}
+
 struct BwdParams {
   // Views (64, N, D/64, H, B) of Q, K, V and dO; box 64 x 128 rows x kchunks.
   CUtensorMap tm_q;
@@ -181,13 +206,15 @@ struct BwdParams {
   int* err;     // device status word of this call (set to FFPA_ERR_DEVICE_TIMEOUT on expiry)
   int device;   // host only: the device the launch goes to
   // Stored-tile backward: P and dS (dS times the softmax scale), 16-bit, one
-  // 32 KB block per (b, hq, query tile, key tile) in the caller's workspace,
-  // blocks ordered by (b Hq + hq, query tile, key tile); inside a block the
-  // 16-byte unit of 8 keys (8u .. 8u+7) of row r sits at byte 2048 u + 16 r
-  // (the tensor core's layout without swizzle).  ws_zero: one block of zeros.
+  // 32 KB block per (b, hq, query tile, stored key tile) in the caller's
+  // workspace: block (b Hq + hq) ws_head + bwd_stored_before(qt) + kt; inside
+  // a block the 16-byte unit of 8 keys (8u .. 8u+7) of row r sits at byte
+  // 2048 u + 16 r (the tensor core's layout without swizzle).  ws_zero: one
+  // block of zeros.
   void* ws_zero;
   void* ws_p;
   void* ws_ds;
+  long long ws_head;   // stored blocks per head
   int kv_parts;      // scores kernel: key-tile ranges per query tile
   int ts_nslot;      // scores kernel: ring depth
   int tc_nslot;      // contraction kernel: ring depth

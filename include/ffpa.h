@@ -311,8 +311,8 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
  *
  *   workspace, workspace_bytes: device memory of q's device, 16-byte
  *     aligned, owned by the caller, of at least
- *     ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D) bytes; its contents
- *     on entry do not matter and on return are unspecified.
+ *     ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, is_causal) bytes; its
+ *     contents on entry do not matter and on return are unspecified.
  *
  * When ffpa_bwd_workspace_bytes() is non-zero (dense layout, D = 256, 384
  * or 512, Nq > 0, Nkv > 0) and the workspace is large enough, each
@@ -322,14 +322,15 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
  * computed twice (the ffpa_bwd kernels recompute S and dP for every
  * 256-column output slice).  Workspace layout: a 32 KB block of zeros, then
  * P, then dS, each one 32 KB block per (b, hq, query tile, key tile) in that
- * order; inside a block the 8 keys 8u .. 8u+7 of tile row r are the 16 bytes
- * at 2048 u + 16 r.  Three launches on `stream` (delta,
+ * order, where with is_causal only the key tiles that some row of the query
+ * tile sees are stored (about half the blocks when Nq = Nkv); inside a block
+ * the 8 keys 8u .. 8u+7 of tile row r are the 16 bytes at 2048 u + 16 r.  Three launches on `stream` (delta,
  * scores, contraction).  Otherwise (workspace NULL or too small, or a shape
  * the path does not take) this is ffpa_bwd and the workspace is not
  * touched.  A workspace on another device, or not 16-byte aligned when it
  * would be used, is FFPA_ERR_INVALID.  No allocation, no synchronisation.
  */
-size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D);
+size_t ffpa_bwd_workspace_bytes(int B, int Hq, int Hkv, int Nq, int Nkv, int D, int is_causal);
 ffpa_status ffpa_bwd_ws(const void* q, const void* k, const void* v, const void* o, const void* dout,
                         const float* lse, void* dq, void* dk, void* dv, float* delta, ffpa_dtype dt,
                         int B, int Hq, int Hkv, int Nq, int Nkv, int D, const int64_t q_str[4],

@@ -267,6 +267,30 @@ def test_bwd_workspace_bytes(lib):
     assert wb(1 << 16, 1 << 8, 1, 1 << 17, 128, 512) == 0   # more than 2^30 blocks
 
 
+def _stored_tiles_brute(Nq, Nkv):
+    """Key tiles of each query tile that some row sees (lower-right causal), summed."""
+    total = 0
+    for qt in range(-(-Nq // 128)):
+        last_row = min(Nq, (qt + 1) * 128) - 1
+        last_key = min(Nkv - 1, last_row + (Nkv - Nq))
+        total += last_key // 128 + 1
+    return total
+
+
+def test_bwd_workspace_bytes_causal(lib):
+    """Under causal masking only the visible key tiles are stored: the block
+    count is the brute-force sum over query tiles; non-causal keeps all."""
+    wb = pkg.bwd_workspace_bytes
+    for Nq, Nkv in ((4096, 4096), (300, 300), (129, 1000), (1, 1), (1, 129), (127, 129), (256, 1024),
+                    (1000, 1000), (640, 641)):
+        for B, Hq in ((1, 1), (2, 8)):
+            want = (2 * B * Hq * _stored_tiles_brute(Nq, Nkv) + 1) * 32768
+            assert wb(B, Hq, Hq, Nq, Nkv, 512, True) == want, (Nq, Nkv)
+            assert wb(B, Hq, Hq, Nq, Nkv, 512, False) == (2 * B * Hq * (-(-Nq // 128)) * (-(-Nkv // 128)) + 1) * 32768
+    assert wb(1, 2, 2, 300, 200, 512, True) == 0      # causal needs Nkv >= Nq
+    assert wb(1, 16, 16, 4096, 4096, 512, True) == (2 * 16 * (32 * 33 // 2) + 1) * 32768
+
+
 def bwd_ws_call(lib, ws, ws_bytes, D=512, dt=0):
     def st(N):
         return _arr([2 * N * D, N * D, D, 1])

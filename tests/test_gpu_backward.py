@@ -170,7 +170,7 @@ def test_bwd_tiles_masks():
 
 def _sentinel_workspace(q, k, D):
     B, Hq, Nq, _ = q.shape
-    need = pkg.bwd_workspace_bytes(B, Hq, k.shape[1], Nq, k.shape[2], D)
+    need = pkg.bwd_workspace_bytes(B, Hq, k.shape[1], Nq, k.shape[2], D, False)
     assert need == (2 * B * Hq * (-(-Nq // 128)) * (-(-k.shape[2] // 128)) + 1) * 32768
     return need
 
