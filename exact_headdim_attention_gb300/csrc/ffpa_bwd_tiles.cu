@@ -583,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       for (int i = 0; i < T && ok; ++i) {
         int b_row, head;
         const void* src = step(i, b_row, head);
-        if (i + PF < T) {
+        if (PF > 0 && i + PF < T) {
           int br, hd;
           prefetch_l2_bulk(step(i + PF, br, hd), P_TILE_BYTES);
         }
