@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     default_scale,
     BWD_AUTO_WORKSPACE_MAX,
     bwd_workspace_bytes,
+    varlen_bwd_workspace_bytes,
     ffpa_bwd,
     ffpa_bwd_noalloc,
     BWD_NOALLOC_MAX_ROWS,

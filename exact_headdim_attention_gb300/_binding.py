@@ -26,7 +26,8 @@ EXPORTED = ("ffpa_fwd", "ffpa_fwd_ex", "ffpa_fwd_varlen", "ffpa_fwd_varlen_ex", 
             "ffpa_bwd_ex", "ffpa_bwd_varlen", "ffpa_bwd_varlen_ex", "ffpa_status_string",
             "ffpa_last_device_error", "ffpa_selected_kernel", "ffpa_bwd_noalloc",
             "ffpa_fwd_fp8", "ffpa_fwd_fp8_ex", "ffpa_fwd_fp8_workspace_bytes", "ffpa_bwd_ws",
-            "ffpa_bwd_ws_ex", "ffpa_bwd_workspace_bytes")
+            "ffpa_bwd_ws_ex", "ffpa_bwd_workspace_bytes", "ffpa_bwd_varlen_ws", "ffpa_bwd_varlen_ws_ex",
+            "ffpa_bwd_varlen_workspace_bytes")
 
 KERNEL_VARIANTS = {"auto": 0, "single": 1, "pair": 2, "split": 3, "dual": 4}
 
@@ -107,6 +108,13 @@ def load_library(path: str | Path | None = None) -> ctypes.CDLL:
     lib.ffpa_bwd_ws_ex.restype = I
     lib.ffpa_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     lib.ffpa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    bvws = sigs["ffpa_bwd_varlen"][:-1] + [P, ctypes.c_size_t, P]   # + workspace, bytes, stream
+    lib.ffpa_bwd_varlen_ws.argtypes = bvws
+    lib.ffpa_bwd_varlen_ws.restype = I
+    lib.ffpa_bwd_varlen_ws_ex.argtypes = bvws + [O]
+    lib.ffpa_bwd_varlen_ws_ex.restype = I
+    lib.ffpa_bwd_varlen_workspace_bytes.argtypes = [P, P, I, I, I, I, I]
+    lib.ffpa_bwd_varlen_workspace_bytes.restype = ctypes.c_size_t
     # ffpa_bwd without the delta argument
     lib.ffpa_bwd_noalloc.argtypes = sigs["ffpa_bwd"][:9] + sigs["ffpa_bwd"][10:]
     lib.ffpa_bwd_noalloc.restype = I
@@ -367,6 +375,15 @@ def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int,
     return int(load_library().ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, int(bool(is_causal))))
 
 
+def varlen_bwd_workspace_bytes(cu_q, cu_k, Hq: int, Hkv: int, D: int, causal: bool = False) -> int:
+    """Bytes of the varlen stored-tile backward's workspace for these sequences
+    (cu_q, cu_k: host sequences of cumulative lengths; 0: the path does not apply)."""
+    cq = (ctypes.c_int32 * len(cu_q))(*[int(x) for x in cu_q])
+    ck = (ctypes.c_int32 * len(cu_k))(*[int(x) for x in cu_k])
+    return int(load_library().ffpa_bwd_varlen_workspace_bytes(cq, ck, len(cu_q) - 1, Hq, Hkv, D,
+                                                              int(bool(causal))))
+
+
 def _bwd_workspace(workspace, need: int, device):
     """(pointer, bytes, tensor to keep) of the stored-tile workspace argument."""
     if workspace is None or need == 0:
@@ -572,13 +589,14 @@ def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                     cu_seqlens_k: torch.Tensor | None, max_seqlen_q: int, max_seqlen_k: int, *,
                     softmax_scale: float | None = None, causal: bool = False,
                     enable_gqa: bool = False, dq=None, dk=None, dv=None, delta=None,
-                    return_delta: bool = False, stream=None, status=None, wait_timeout_ns=None,
-                    test_drop_first_copy=False):
-    """Packed varlen backward through the C ABI ``ffpa_bwd_varlen``.
+                    return_delta: bool = False, workspace="auto", stream=None, status=None,
+                    wait_timeout_ns=None, test_drop_first_copy=False):
+    """Packed varlen backward through the C ABI ``ffpa_bwd_varlen_ws``.
 
     dout, q, out [Tq,Hq,D]; k, v [Tk,Hkv,D]; lse [Hq,Tq] fp32 from
     ffpa_fwd_varlen with the same sequences, causal and scale.  Returns
-    (dq, dk, dv), plus delta [Hq,Tq] fp32 with return_delta."""
+    (dq, dk, dv), plus delta [Hq,Tq] fp32 with return_delta.  workspace: as
+    for ffpa_bwd, sized by varlen_bwd_workspace_bytes of these sequences."""
     lib = load_library()
     for name, t in (("dout", dout), ("q", q), ("k", k), ("v", v), ("out", out)):
         if t.dim() != 3:
@@ -602,18 +620,21 @@ def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
             max(b - a for a, b in zip(ck, ck[1:])) > max_seqlen_k:
         raise ValueError("max_seqlen_* is smaller than a sequence length")
     dq, dk, dv, delta = _grad_buffers(q, k, v, dq, dk, dv, delta, (Hq, Tq))
+    need = varlen_bwd_workspace_bytes(cq, ck, Hq, Hkv, D, causal)
+    ws_ptr, ws_bytes, ws_keep = _bwd_workspace(workspace, need, q.device)
     cuq = _device_copy(cu_seqlens_q, q.device, stream)
     cuk = None if cu_seqlens_k is None else _device_copy(cu_seqlens_k, q.device, stream)
     sc = None if softmax_scale is None else ctypes.byref(ctypes.c_float(float(softmax_scale)))
     opts = _options(q, None, status, wait_timeout_ns, test_drop_first_copy)
-    st = lib.ffpa_bwd_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                dv.data_ptr(), delta.data_ptr(), _dtype_code(q), Tq, Tk, Hq, Hkv, D,
-                                _strides(q), _strides(k), _strides(v), _strides(out),
-                                _strides(dout), _strides(dq), _strides(dk), _strides(dv),
-                                cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
-                                int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
-                                int(bool(enable_gqa)), _stream_handle(stream, q), opts)
+    st = lib.ffpa_bwd_varlen_ws_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), delta.data_ptr(), _dtype_code(q), Tq, Tk, Hq, Hkv, D,
+                                   _strides(q), _strides(k), _strides(v), _strides(out),
+                                   _strides(dout), _strides(dq), _strides(dk), _strides(dv),
+                                   cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
+                                   int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
+                                   int(bool(enable_gqa)), ws_ptr, ws_bytes, _stream_handle(stream, q), opts)
+    del ws_keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd_varlen")
     return (dq, dk, dv, delta) if return_delta else (dq, dk, dv)

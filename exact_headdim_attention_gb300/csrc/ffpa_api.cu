@@ -441,16 +441,49 @@ size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D, int causal) {
   return static_cast<size_t>((2 * blocks + 1) * (long long)P_TILE_BYTES);
 }
 
+// Varlen stored-tile workspace: the per-sequence block bases (nseq + 1
+// int64, rounded up to 1 KB), a 32 KB block of zeros, then P and dS blocks.
+size_t bwd_varlen_header_bytes(int nseq) { return (((size_t)nseq + 1) * 8 + 1023) / 1024 * 1024; }
+
+size_t bwd_varlen_tiles_bytes(const int32_t* cu_q, const int32_t* cu_k, int nseq, int Hq, int D, int causal) {
+  if (!(D == 256 || D == 384 || D == 512) || !cu_q || nseq < 1 || Hq < 1) return 0;
+  if (!cu_k) cu_k = cu_q;
+  long long blocks = 0;
+  for (int s = 0; s < nseq; ++s) {
+    const int lq = cu_q[s + 1] - cu_q[s], lk = cu_k[s + 1] - cu_k[s];
+    if (lq < 0 || lk < 0) return 0;
+    blocks += (long long)Hq * bwd_stored_before((lq + BM - 1) / BM, lq, lk, causal);
+    if (blocks > (1LL << 30)) return 0;
+  }
+  if (blocks == 0) return 0;
+  return bwd_varlen_header_bytes(nseq) + static_cast<size_t>((2 * blocks + 1) * (long long)P_TILE_BYTES);
+}
+
 // Plans and launches the stored-tile path: the caller has set P as for
-// bwd_launch and checked the workspace (`ws`, bwd_tiles_bytes() bytes).
-ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o, cudaStream_t stream) {
+// bwd_launch and checked the workspace (`ws`, `ws_bytes`: dense, at least
+// bwd_tiles_bytes(); varlen, at least the header and three blocks, the
+// kernels checking every block index against what it holds).
+ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, size_t ws_bytes, int sms, const CallOpts& o,
+                             cudaStream_t stream) {
   P.nchunks = P.D / DK;
   P.n_sl = 1;
-  P.ws_head = bwd_stored_before(P.n_qt, P.Nq, P.Nkv, P.causal);
-  const long long blocks = (long long)P.B * P.Hq * P.ws_head;
-  P.ws_zero = ws;
-  P.ws_p = static_cast<uint8_t*>(ws) + P_TILE_BYTES;
-  P.ws_ds = static_cast<uint8_t*>(ws) + (1 + blocks) * (long long)P_TILE_BYTES;
+  long long blocks;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (P.varlen) {
+    const size_t hdr = bwd_varlen_header_bytes(P.B);
+    P.ws_head = 0;
+    P.ws_base = reinterpret_cast<const long long*>(w);
+    w += hdr;
+    blocks = (long long)((ws_bytes - hdr - P_TILE_BYTES) / (2 * (size_t)P_TILE_BYTES));
+  } else {
+    P.ws_head = bwd_stored_before(P.n_qt, P.Nq, P.Nkv, P.causal);
+    P.ws_base = nullptr;
+    blocks = (long long)P.B * P.Hq * P.ws_head;
+  }
+  P.ws_blocks = blocks;
+  P.ws_zero = w;
+  P.ws_p = w + P_TILE_BYTES;
+  P.ws_ds = w + (1 + blocks) * (long long)P_TILE_BYTES;
   // Scores kernel: dO (D/64 chunks) resident, then the ring.
   size_t ns = (SMEM_LIMIT - TS_STATIC_RESERVE - 1024 - (size_t)P.nchunks * CHUNK_BYTES) / SLOT_BYTES;
   if (ns > (size_t)TS_NSLOT_MAX) ns = TS_NSLOT_MAX;
@@ -465,7 +498,7 @@ ffpa_status bwd_tiles_launch(BwdParams& P, void* ws, int sms, const CallOpts& o,
   // keeping at least 8 key tiles per range (each range loads Q and dO once).
   const long long base = (long long)P.B * P.Hq * P.n_qt;
   P.kv_parts = 1;
-  if (!P.causal && sms > 0) {
+  if (!P.causal && !P.varlen && sms > 0) {
     double best = -1.0;
     for (int parts = 1; parts <= 4; parts *= 2) {
       if (parts > 1 && P.n_kt / parts < 8) break;
@@ -876,7 +909,9 @@ ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const vo
   P.fp16 = dt == FFPA_FP16;
   P.err = err;
   P.device = dev;
-  if (tiles) return bwd_tiles_launch(P, workspace, device_facts(dev).sms, opt, reinterpret_cast<cudaStream_t>(stream));
+  if (tiles)
+    return bwd_tiles_launch(P, workspace, workspace_bytes, device_facts(dev).sms, opt,
+                            reinterpret_cast<cudaStream_t>(stream));
   return bwd_launch(P, any_q, any_k, opt, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -925,16 +960,17 @@ ffpa_status ffpa_bwd(const void* q, const void* k, const void* v, const void* o,
                      scale, is_causal, enable_gqa, stream, nullptr);
 }
 
-ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
-                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
-                               const int64_t q_str[3], const int64_t k_str[3],
-                               const int64_t v_str[3], const int64_t o_str[3],
-                               const int64_t do_str[3], const int64_t dq_str[3],
-                               const int64_t dk_str[3], const int64_t dv_str[3],
-                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
-                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
-                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options) {
+ffpa_status ffpa_bwd_varlen_ws_ex(const void* q, const void* k, const void* v, const void* o,
+                                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                  float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                                  const int64_t q_str[3], const int64_t k_str[3],
+                                  const int64_t v_str[3], const int64_t o_str[3],
+                                  const int64_t do_str[3], const int64_t dq_str[3],
+                                  const int64_t dk_str[3], const int64_t dv_str[3],
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                                  int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                                  int enable_gqa, void* workspace, size_t workspace_bytes,
+                                  ffpa_stream_t stream, const ffpa_options* options) {
   if (dt != FFPA_BF16 && dt != FFPA_FP16) return FFPA_ERR_DTYPE;
   if (Tq < 0 || Tk < 0 || Hq < 1 || Hkv < 1) return FFPA_ERR_INVALID;
   if (D < 64 || D > 1024 || D % 64 != 0) return FFPA_ERR_UNSUPPORTED;
@@ -969,10 +1005,17 @@ ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, cons
     if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
   }
   int dev = 0;
+  // The stored-tile path: D = 256, 384 or 512, both sides present, and a
+  // workspace of at least the header and three blocks (the kernels check
+  // every block index against the blocks it holds).
+  const bool tiles = workspace != nullptr && (D == 256 || D == 384 || D == 512) && any_q && any_k &&
+                     workspace_bytes >= bwd_varlen_header_bytes(nseq) + 3 * (size_t)P_TILE_BYTES;
+  if (tiles && !aligned16(workspace)) return FFPA_ERR_INVALID;
   ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,
                                   any_q ? dq : nullptr, any_q ? lse : nullptr, any_q ? delta : nullptr,
                                   any_k ? k : nullptr, any_k ? v : nullptr, any_k ? dk : nullptr,
-                                  any_k ? dv : nullptr, cu_seqlens_q, cu_seqlens_k},
+                                  any_k ? dv : nullptr, cu_seqlens_q, cu_seqlens_k,
+                                  tiles ? workspace : nullptr},
                                  &dev);
   if (st != FFPA_OK) return st;
   DeviceScope scope(dev);
@@ -1035,7 +1078,49 @@ ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, cons
   P.fp16 = dt == FFPA_FP16;
   P.err = err;
   P.device = dev;
+  if (tiles)
+    return bwd_tiles_launch(P, workspace, workspace_bytes, device_facts(dev).sms, opt,
+                            reinterpret_cast<cudaStream_t>(stream));
   return bwd_launch(P, any_q, any_k, opt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int64_t do_str[3], const int64_t dq_str[3],
+                               const int64_t dk_str[3], const int64_t dv_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, ffpa_stream_t stream, const ffpa_options* options) {
+  return ffpa_bwd_varlen_ws_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, Tq, Tk, Hq, Hkv, D, q_str, k_str,
+                               v_str, o_str, do_str, dq_str, dk_str, dv_str, cu_seqlens_q, cu_seqlens_k, nseq,
+                               max_seqlen_q, max_seqlen_k, scale, causal, enable_gqa, nullptr, 0, stream,
+                               options);
+}
+
+size_t ffpa_bwd_varlen_workspace_bytes(const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_k_host,
+                                       int nseq, int Hq, int Hkv, int D, int is_causal) {
+  if (Hkv < 1 || Hq % Hkv != 0) return 0;
+  return bwd_varlen_tiles_bytes(cu_seqlens_q_host, cu_seqlens_k_host, nseq, Hq, D, is_causal ? 1 : 0);
+}
+
+ffpa_status ffpa_bwd_varlen_ws(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int64_t do_str[3], const int64_t dq_str[3],
+                               const int64_t dk_str[3], const int64_t dv_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, void* workspace, size_t workspace_bytes,
+                               ffpa_stream_t stream) {
+  return ffpa_bwd_varlen_ws_ex(q, k, v, o, dout, lse, dq, dk, dv, delta, dt, Tq, Tk, Hq, Hkv, D, q_str, k_str,
+                               v_str, o_str, do_str, dq_str, dk_str, dv_str, cu_seqlens_q, cu_seqlens_k, nseq,
+                               max_seqlen_q, max_seqlen_k, scale, causal, enable_gqa, workspace,
+                               workspace_bytes, stream, nullptr);
 }
 
 ffpa_status ffpa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,

@@ -67,6 +67,56 @@ constexpr int TC_MMA_WARP = 5;
 
 }  // namespace
 
+// Block of the stored P (or dS) for (batch or sequence b, query head h, query
+// tile qt, key tile kt) of a problem with q_len queries and kv_len keys.
+__device__ __forceinline__ long long stored_block(const BwdParams& p, int b, int h, int q_len, int kv_len, int qt,
+                                                  int kt) {
+  if (p.varlen) {
+    const long long per_head = bwd_stored_before((q_len + BM - 1) / BM, q_len, kv_len, p.causal);
+    return p.ws_base[b] + (long long)h * per_head + bwd_stored_before(qt, q_len, kv_len, p.causal) + kt;
+  }
+  return (long long)(b * p.Hq + h) * p.ws_head + bwd_stored_before(qt, p.Nq, p.Nkv, p.causal) + kt;
+}
+
+// A block index past the caller's workspace: recorded as an invalid
+// argument in the call's status word (a varlen workspace smaller than the
+// sequences need); the block is then neither written nor read.
+__device__ __forceinline__ bool block_in_workspace(const BwdParams& p, long long blk) {
+  if (blk < p.ws_blocks) return true;
+  atomicExch(p.err, (int)FFPA_ERR_INVALID);
+  return false;
+}
+
+// Varlen: the first stored block of every sequence (an exclusive scan of
+// Hq x blocks per head over the sequences), and the total at index nseq.
+__global__ void __launch_bounds__(1024) ffpa_bwd_bases_kernel(const __grid_constant__ BwdParams p) {
+  __shared__ long long part[1024];
+  const int n = p.B, t = threadIdx.x;
+  const int per = (n + 1023) / 1024;
+  const int s0 = min(n, t * per), s1 = min(n, s0 + per);
+  auto blocks = [&](int s) -> long long {
+    const int lq = p.cu_q[s + 1] - p.cu_q[s], lk = p.cu_k[s + 1] - p.cu_k[s];
+    return (long long)p.Hq * bwd_stored_before((lq + BM - 1) / BM, lq, lk, p.causal);
+  };
+  long long sum = 0;
+  for (int s = s0; s < s1; ++s) sum += blocks(s);
+  part[t] = sum;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {
+    const long long v = t >= d ? part[t - d] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  long long base = part[t] - sum;
+  long long* out = const_cast<long long*>(p.ws_base);
+  for (int s = s0; s < s1; ++s) {
+    out[s] = base;
+    base += blocks(s);
+  }
+  if (t == 1023) out[n] = part[1023];
+}
+
 // NCH = D / 64 (4, 6 or 8): every MMA issue loop has a compile-time trip count.
 template <int NCH, bool UMASK>
 __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __grid_constant__ BwdParams p) {
@@ -147,7 +197,10 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
           drop = false;
         } else {
           mbar_arrive_expect_tx(fb, SLOT_BYTES);
-          tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, it.hkv, it.b);
+          if (p.varlen)
+            tma_load_4d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, it.kv_row0 + row, chunk, it.hkv);
+          else
+            tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, it.hkv, it.b);
         }
         ++issued;
         if (++slot == NS) { slot = 0; lap ^= 1u; }
@@ -175,8 +228,15 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       prefetch_tmap(&p.tm_do);
       const uint32_t db = smem_u32(&bar_do);
       mbar_arrive_expect_tx(qb, (uint32_t)NCH * CHUNK_BYTES);
-      for (int pr = 0; pr < NPR; ++pr)
-        tma_load_5d(do_u32 + pr * SLOT_BYTES, &p.tm_q, qb, 0, it.row0, 2 * pr, it.hq, it.b);
+      auto qload = [&](const CUtensorMap* m, uint32_t bar) {
+        for (int pr = 0; pr < NPR; ++pr) {
+          if (p.varlen)
+            tma_load_4d(do_u32 + pr * SLOT_BYTES, m, bar, 0, it.q_row0 + it.row0, 2 * pr, it.hq);
+          else
+            tma_load_5d(do_u32 + pr * SLOT_BYTES, m, bar, 0, it.row0, 2 * pr, it.hq, it.b);
+        }
+      };
+      qload(&p.tm_q, qb);
       int slot = 0;
       uint32_t lap = 0;
       auto take = [&]() -> int {
@@ -196,8 +256,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       const bool do_issued = ok;
       if (ok) {
         mbar_arrive_expect_tx(db, (uint32_t)NCH * CHUNK_BYTES);
-        for (int pr = 0; pr < NPR; ++pr)
-          tma_load_5d(do_u32 + pr * SLOT_BYTES, &p.tm_do, db, 0, it.row0, 2 * pr, it.hq, it.b);
+        qload(&p.tm_do, db);
       }
       const uint32_t idesc = idesc_f16(!fp16, BM, BN, false, false);
       // K-major operands: +32 bytes per 16 D-elements, +16 KB per chunk.
@@ -303,8 +362,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
     // r in the stored blocks: every row of a block is written, zeros where
     // the row or key is out of range.  A warp's store covers 32 consecutive
     // rows of one unit: 512 contiguous bytes.
-    const long long blk0 = (long long)(it.b * p.Hq + it.hq) * p.ws_head +
-                           bwd_stored_before(it.row0 / BM, p.Nq, p.Nkv, p.causal);
+    const long long blk0 = stored_block(p, it.b, it.hq, it.q_len, it.kv_len, it.row0 / BM, 0);
     const long long uoff = (blk0 << 15) + (long long)(8 * half) * 2048 + r * 16;
     uint8_t* const pbase = static_cast<uint8_t*>(p.ws_p) + uoff;
     uint8_t* const dsbase = static_cast<uint8_t*>(p.ws_ds) + uoff;
@@ -347,7 +405,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
           pv[e] = v;
         }
       }
-      {
+      const bool in_ws = block_in_workspace(p, blk0 + j0 + jj);
+      if (in_ws) {
         uint8_t* const dst = pbase + ((long long)(j0 + jj) << 15);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -374,7 +433,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_dp_free));
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
+      for (int g = 0; g < 4 && in_ws; ++g) {
         float x[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -425,54 +484,70 @@ __device__ __forceinline__ void contract_role(const BwdParams& p, int L, int& ro
 // ranges; a step outside a CTA's own range contributes a zero tile).
 struct PairItem {
   int role, b, hq, hkv;
+  int q_len, kv_len;       // this problem's (sequence's) lengths
+  int q_row0, kv_row0;     // varlen: first packed row of the sequence (dense: 0)
+  int n_qt, n_kt;          // its query and key tiles
   int tile0, my_tile;
   int n_iter;       // contraction steps
   int qt_first;     // dV / dK: first query tile of the range
   int nq;           // dV / dK: query tiles per head in the range
 };
 
-__device__ __forceinline__ void decode_pair_item(const BwdParams& p, int L, uint32_t rank, PairItem& it) {
+// False for a pair past the end of its sequence (varlen; same answer in
+// both CTAs).
+__device__ __forceinline__ bool decode_pair_item(const BwdParams& p, int L, uint32_t rank, PairItem& it) {
   int r;
   contract_role(p, L, it.role, r);
-  if (it.role == BWD_ROLE_DQ) {
-    const int heads = p.B * p.Hq, npt = (p.n_qt + 1) >> 1;
-    int pt, bh;
-    if (p.causal) {            // longest query tiles (most visible keys) first
-      bh = r % heads;
-      pt = npt - 1 - r / heads;
-    } else {
-      pt = r % npt;
-      bh = r / npt;
-    }
+  const bool dq = it.role == BWD_ROLE_DQ;
+  const int heads = p.B * (dq ? p.Hq : p.Hkv);
+  const int npairs = dq ? (p.n_qt + 1) >> 1 : (p.n_kt + 1) >> 1;
+  int pi, bh;
+  if (p.causal) {            // dQ: longest query tiles first; dV / dK: key tile 0 (seen by all) first
+    bh = r % heads;
+    pi = dq ? npairs - 1 - r / heads : r / heads;
+  } else {
+    pi = r % npairs;
+    bh = r / npairs;
+  }
+  if (dq) {
     it.hq = bh % p.Hq;
     it.b = bh / p.Hq;
     it.hkv = it.hq / p.group;
-    it.tile0 = 2 * pt;
-    it.n_iter = bwd_stored_tiles(min(it.tile0 + 1, p.n_qt - 1), p.Nq, p.Nkv, p.causal);
-    it.qt_first = 0;
-    it.nq = 0;
   } else {
-    const int heads = p.B * p.Hkv, nkp = (p.n_kt + 1) >> 1;
-    int kp, bh;
-    if (p.causal) {            // key tile 0 is seen by every query tile: first
-      bh = r % heads;
-      kp = r / heads;
-    } else {
-      kp = r % nkp;
-      bh = r / nkp;
-    }
     it.hkv = bh % p.Hkv;
     it.b = bh / p.Hkv;
     it.hq = it.hkv * p.group;
-    it.tile0 = 2 * kp;
+  }
+  if (p.varlen) {
+    it.q_row0 = p.cu_q[it.b];
+    it.q_len = p.cu_q[it.b + 1] - it.q_row0;
+    it.kv_row0 = p.cu_k[it.b];
+    it.kv_len = p.cu_k[it.b + 1] - it.kv_row0;
+  } else {
+    it.q_row0 = 0;
+    it.q_len = p.Nq;
+    it.kv_row0 = 0;
+    it.kv_len = p.Nkv;
+  }
+  it.n_qt = (it.q_len + BM - 1) / BM;
+  it.n_kt = (it.kv_len + BN - 1) / BN;
+  it.tile0 = 2 * pi;
+  it.my_tile = it.tile0 + (int)rank;
+  if (dq) {
+    if (it.tile0 >= it.n_qt) return false;
+    it.n_iter = bwd_stored_tiles(min(it.tile0 + 1, it.n_qt - 1), it.q_len, it.kv_len, p.causal);
+    it.qt_first = 0;
+    it.nq = 0;
+  } else {
+    if (it.tile0 >= it.n_kt) return false;
     // Query row i sees key k when k <= i + (Nkv - Nq): the first query tile
     // with a row that sees the pair's first key.
-    const int first_row = p.causal ? max(0, it.tile0 * BN - (p.Nkv - p.Nq)) : 0;
+    const int first_row = p.causal ? max(0, it.tile0 * BN - (it.kv_len - it.q_len)) : 0;
     it.qt_first = first_row / BM;
-    it.nq = max(0, p.n_qt - it.qt_first);
+    it.nq = max(0, it.n_qt - it.qt_first);
     it.n_iter = p.group * it.nq;
   }
-  it.my_tile = it.tile0 + (int)rank;
+  return true;
 }
 
 // Contraction kernel on CTA pairs (cta_group::2): one M = 256 MMA per
@@ -488,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   PairItem it;
-  decode_pair_item(p, blockIdx.x >> 1, rank, it);
+  if (!decode_pair_item(p, blockIdx.x >> 1, rank, it)) return;   // same answer in both CTAs
   const bool dq_role = it.role == BWD_ROLE_DQ;
   const int T = it.n_iter;
   const bool fp16 = p.fp16 != 0;
@@ -567,9 +642,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           kt = it.my_tile;
           b_row = qt * BM;
         }
-        const bool real = qt < p.n_qt && kt < bwd_stored_tiles(qt, p.Nq, p.Nkv, p.causal);
-        const long long blk = (long long)(it.b * p.Hq + head) * p.ws_head + bwd_stored_before(qt, p.Nq, p.Nkv, p.causal) + kt;
-        return real ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
+        const bool real = qt < it.n_qt && kt < bwd_stored_tiles(qt, it.q_len, it.kv_len, p.causal);
+        if (!real) return p.ws_zero;
+        const long long blk = stored_block(p, it.b, head, it.q_len, it.kv_len, qt, kt);
+        return block_in_workspace(p, blk) ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
       };
       // The stored blocks come from DRAM: for D >= 384 each is requested into
       // L2 this many steps before its copy into the ring (measured at D = 512:
@@ -598,7 +674,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           if (dst == ~0u) { ok = false; break; }
           // 256-column group: chunks 4g + 2 rank, +1; a 128-column tail: chunk 4g + rank.
           const int c0 = (4 * g + 4 <= NCH) ? 4 * g + 2 * (int)rank : 4 * g + (int)rank;
-          if (dst) tma_load_5d(dst, bmap, fb, 0, b_row, c0, b_head, it.b);
+          if (dst) {
+            if (p.varlen)
+              tma_load_4d(dst, bmap, fb, 0, (dq_role ? it.kv_row0 : it.q_row0) + b_row, c0, b_head);
+            else
+              tma_load_5d(dst, bmap, fb, 0, b_row, c0, b_head, it.b);
+          }
         }
       }
       const int n = issued < NS ? issued : NS;
@@ -717,17 +798,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       BwdItem bi;
       bi.b = it.b;
-      bi.q_row0 = 0;
-      bi.kv_row0 = 0;
+      bi.q_row0 = it.q_row0;
+      bi.kv_row0 = it.kv_row0;
       const bool dv_role = it.role == BWD_ROLE_DV;
       uint8_t* const obase = static_cast<uint8_t*>(dq_role ? p.dq : dv_role ? p.dv : p.dk);
       const int64_t* ostr = dq_role ? p.dq_str : dv_role ? p.dv_str : p.dk_str;
       const int head = dq_role ? it.hq : it.hkv;
-      const int rows = dq_role ? p.Nq : p.Nkv;
+      const int rows = dq_role ? it.q_len : it.kv_len;
+      const int seq_row0 = dq_role ? it.q_row0 : it.kv_row0;
       const int row0 = it.my_tile * BM + warp * 32;
 #pragma unroll 1
       for (int rr = 0; rr < 32 && row0 + rr < rows; ++rr) {
-        uint8_t* const orow = obase + bwd_row_offset(p, bi, ostr, 0, row0 + rr, head) * 2;
+        uint8_t* const orow = obase + bwd_row_offset(p, bi, ostr, seq_row0, row0 + rr, head) * 2;
         const uint32_t srow = stage + rr * ROWB;
         const uint32_t rsw = (uint32_t)(rr & 7);
 #pragma unroll
@@ -772,9 +854,15 @@ static ffpa_status launch_tiles_t(const BwdParams& P, int score_items, int contr
   return FFPA_OK;
 }
 
+ffpa_status launch_bwd_tiles_bases(const BwdParams& P, cudaStream_t stream) {
+  ffpa_bwd_bases_kernel<<<1, 1024, 0, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? FFPA_OK : FFPA_ERR_CUDA;
+}
+
 ffpa_status launch_bwd_tiles(const BwdParams& P, int score_items, int contract_items, size_t smem_scores,
                              size_t smem_contract, cudaStream_t stream) {
   if (launch_bwd_delta(P, stream) != FFPA_OK) return FFPA_ERR_CUDA;
+  if (P.varlen && launch_bwd_tiles_bases(P, stream) != FFPA_OK) return FFPA_ERR_CUDA;
   switch (P.nchunks) {
     case 4: return launch_tiles_t<4>(P, score_items, contract_items, smem_scores, smem_contract, stream);
     case 6: return launch_tiles_t<6>(P, score_items, contract_items, smem_scores, smem_contract, stream);

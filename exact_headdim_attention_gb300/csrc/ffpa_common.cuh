@@ -135,6 +135,9 @@ ffpa_status launch_bwd_delta(const BwdParams& P, cudaStream_t stream);
 // tiles).  D / 64 in {4, 6, 8}.
 ffpa_status launch_bwd_tiles(const BwdParams& P, int score_items, int contract_items, size_t smem_scores,
                              size_t smem_contract, cudaStream_t stream);
+// Varlen: the first stored block of every sequence (P.ws_base), from
+// cu_seqlens on the device.
+ffpa_status launch_bwd_tiles_bases(const BwdParams& P, cudaStream_t stream);
 constexpr int TS_THREADS = 320;            // scores: warps 0-7 elementwise, 8 TMA, 9 MMA
 constexpr int TC_THREADS = 192;            // contraction: warps 0-3 epilogue, 4 TMA, 5 MMA
 constexpr int TS_NSLOT_MAX = 6;
@@ -147,11 +150,12 @@ constexpr size_t BWD_STATIC_RESERVE = 6144;
 constexpr int BWD_OUT_COLS = 256;          // dQ, dV or dK columns per CTA
 
 // Stored-tile backward: key tiles kept for query tile qt (those its rows
-// see: every key tile, or under causal masking (lower right, Nkv >= Nq) the
-// tiles up to its last row's limit), and the blocks of query tiles
-// 0 .. qt-1 of one head, in closed form: full query tiles t keep
-// min(n_kt, t + 1 + c) tiles with c = ceil((Nkv - Nq) / 128), the last one n_kt.
+// see: every key tile, or under causal masking, lower right, the tiles up to
+// its last row's limit), and the blocks of query tiles 0 .. qt-1 of one head
+// in closed form: a full query tile t keeps clamp(t + 1 + c, 0, n_kt) tiles
+// with c = ceil((Nkv - Nq) / 128), the last one its own count.
 __host__ __device__ inline int bwd_stored_tiles(int qt, int Nq, int Nkv, int causal) {
+  if (Nq <= 0 || Nkv <= 0) return 0;
   const int n_kt = (Nkv + BN - 1) / BN;
   if (!causal) return n_kt;
   const int rows_end = (qt + 1) * BM < Nq ? (qt + 1) * BM : Nq;
@@ -160,14 +164,21 @@ __host__ __device__ inline int bwd_stored_tiles(int qt, int Nq, int Nkv, int cau
   return kv_end > 0 ? (int)((kv_end + BN - 1) / BN) : 0;
 }
 __host__ __device__ inline long long bwd_stored_before(int qt, int Nq, int Nkv, int causal) {
+  if (Nq <= 0 || Nkv <= 0) return 0;
   const long long n_kt = (Nkv + BN - 1) / BN, n_qt = (Nq + BM - 1) / BM;
   if (!causal) return (long long)qt * n_kt;
-  const long long c = ((long long)(Nkv - Nq) + BN - 1) / BN;
+  if (n_qt == 0) return 0;
+  const long long off = (long long)Nkv - Nq;
+  const long long c = off >= 0 ? (off + BN - 1) / BN : -((-off) / BN);
   const long long full = (long long)qt < n_qt - 1 ? qt : n_qt - 1;   // full query tiles below qt
-  const long long cap = n_kt - c > 0 ? n_kt - c : 0;                // tiles t < cap keep t + 1 + c
-  const long long a = full < cap ? full : cap;
-  long long s = a * (a + 1) / 2 + c * a + (full - a) * n_kt;
-  if ((long long)qt > n_qt - 1) s += n_kt;
+  const long long lo = c < 0 ? -c : 0;                              // first t keeping a tile
+  const long long hi = n_kt - c;                                    // t < hi: below the cap
+  const long long a0 = full < lo ? full : lo;
+  const long long lin_end = full < hi ? full : hi;
+  const long long a1 = lin_end > lo ? lin_end - lo : 0;
+  const long long a2 = full - a0 - a1;
+  long long s = a1 * (lo + 1 + c) + a1 * (a1 - 1) / 2 + a2 * n_kt;
+  if ((long long)qt > n_qt - 1) s += bwd_stored_tiles((int)(n_qt - 1), Nq, Nkv, causal);
   return s;
 }
 
@@ -214,7 +225,9 @@ struct BwdParams {
   void* ws_zero;
   void* ws_p;
   void* ws_ds;
-  long long ws_head;   // stored blocks per head
+  long long ws_head;          // dense: stored blocks per head
+  const long long* ws_base;   // varlen: first block of sequence s (device, nseq + 1 entries)
+  long long ws_blocks;        // blocks the workspace holds for P (and for dS)
   int kv_parts;      // scores kernel: key-tile ranges per query tile
   int ts_nslot;      // scores kernel: ring depth
   int tc_nslot;      // contraction kernel: ring depth

@@ -386,6 +386,55 @@ ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, cons
                                int enable_gqa, ffpa_stream_t stream, const ffpa_options* options);
 
 /*
+ * ffpa_bwd_varlen with a caller-owned workspace for the stored-tile backward
+ * (as ffpa_bwd_ws for the dense layout): the same arguments, checks and
+ * results, plus
+ *
+ *   workspace, workspace_bytes: device memory of q's device, 16-byte
+ *     aligned, owned by the caller.  The stored-tile path runs when D is
+ *     256, 384 or 512, Tq, Tk > 0, and workspace_bytes is at least
+ *     ffpa_bwd_varlen_workspace_bytes() of the same sequences (computed on
+ *     the host from host copies of cu_seqlens_q / cu_seqlens_k, which the
+ *     library cannot read there); a smaller workspace that still holds the
+ *     1 KB-rounded header of nseq + 1 int64 and three 32 KB blocks also takes
+ *     the path, and a block the sequences need past its end is neither
+ *     written nor read: the call's status word then records
+ *     FFPA_ERR_INVALID and the gradients are wrong.  Otherwise this is
+ *     ffpa_bwd_varlen and the workspace is not touched.
+ *
+ * Layout: the first stored block of every sequence (nseq + 1 int64, written
+ * by the call), a 32 KB block of zeros, then P and dS blocks as for
+ * ffpa_bwd_ws, per sequence, query head, query tile and stored key tile
+ * (causal: lower right within each sequence).  Four launches on `stream`
+ * (delta, block bases, scores, contraction); no allocation, no
+ * synchronisation.
+ */
+size_t ffpa_bwd_varlen_workspace_bytes(const int32_t* cu_seqlens_q_host, const int32_t* cu_seqlens_k_host,
+                                       int nseq, int Hq, int Hkv, int D, int is_causal);
+ffpa_status ffpa_bwd_varlen_ws(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                               const int64_t q_str[3], const int64_t k_str[3],
+                               const int64_t v_str[3], const int64_t o_str[3],
+                               const int64_t do_str[3], const int64_t dq_str[3],
+                               const int64_t dk_str[3], const int64_t dv_str[3],
+                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                               int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                               int enable_gqa, void* workspace, size_t workspace_bytes,
+                               ffpa_stream_t stream);
+ffpa_status ffpa_bwd_varlen_ws_ex(const void* q, const void* k, const void* v, const void* o,
+                                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                  float* delta, ffpa_dtype dt, int Tq, int Tk, int Hq, int Hkv, int D,
+                                  const int64_t q_str[3], const int64_t k_str[3],
+                                  const int64_t v_str[3], const int64_t o_str[3],
+                                  const int64_t do_str[3], const int64_t dq_str[3],
+                                  const int64_t dk_str[3], const int64_t dv_str[3],
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int nseq,
+                                  int max_seqlen_q, int max_seqlen_k, const float* scale, int causal,
+                                  int enable_gqa, void* workspace, size_t workspace_bytes,
+                                  ffpa_stream_t stream, const ffpa_options* options);
+
+/*
  * Backward for callers that cannot allocate device memory.  The pages have
  * no counterpart: this entry point exists for callers such as plugins that
  * receive only their tensors' pointers from a host framework, runtimes that

@@ -291,6 +291,38 @@ def test_bwd_workspace_bytes_causal(lib):
     assert wb(1, 16, 16, 4096, 4096, 512, True) == (2 * 16 * (32 * 33 // 2) + 1) * 32768
 
 
+def test_varlen_bwd_workspace_bytes(lib):
+    """Varlen: a 1 KB-rounded header of nseq + 1 int64, a zero block, and P and
+    dS blocks summed over the sequences (brute force per sequence, lower-right
+    causal within each; sequences with fewer keys than queries included)."""
+    vb = pkg.varlen_bwd_workspace_bytes
+    def want(cq, ck, Hq, causal):
+        blocks = 0
+        for s in range(len(cq) - 1):
+            lq, lk = cq[s + 1] - cq[s], ck[s + 1] - ck[s]
+            if lq == 0 or lk == 0:
+                continue
+            if not causal:
+                blocks += Hq * (-(-lq // 128)) * (-(-lk // 128))
+                continue
+            for qt in range(-(-lq // 128)):
+                last_row = min(lq, (qt + 1) * 128) - 1
+                last_key = min(lk - 1, last_row + (lk - lq))
+                blocks += Hq * (last_key // 128 + 1 if last_key >= 0 else 0)
+        hdr = -(-((len(cq)) * 8) // 1024) * 1024
+        return hdr + (2 * blocks + 1) * 32768 if blocks else 0
+    cases = [([0, 300, 428, 429, 879], None), ([0, 100, 300, 300, 364], [0, 150, 350, 380, 680]),
+             ([0, 50, 60, 317], [0, 20, 30, 290]), ([0, 4096], None), ([0, 1, 2], [0, 1, 130])]
+    for cq, ck in cases:
+        ck = ck or cq
+        for causal in (False, True):
+            for Hq in (1, 4):
+                assert vb(cq, ck, Hq, 1, 512, causal) == want(cq, ck, Hq, causal), (cq, ck, causal)
+    assert vb([0, 300], [0, 300], 2, 2, 128, False) == 0          # the slice kernels only
+    assert vb([0, 0, 0], [0, 0, 0], 2, 2, 512, False) == 0        # nothing to store
+    assert vb([0, 300], [0, 300], 3, 2, 512, False) == 0          # not a grouping
+
+
 def bwd_ws_call(lib, ws, ws_bytes, D=512, dt=0):
     def st(N):
         return _arr([2 * N * D, N * D, D, 1])

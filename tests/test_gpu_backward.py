@@ -387,7 +387,7 @@ def test_bwd_bounded_wait_reports_timeout_and_context_survives(workspace):
 
 
 # ------------------------------------------------------------------ varlen
-def varlen_bwd_case(lq, lk, Hq, Hkv, D, seed, causal):
+def varlen_bwd_case(lq, lk, Hq, Hkv, D, seed, causal, workspace="auto"):
     g = torch.Generator().manual_seed(seed)
     cu_q = torch.tensor([0] + torch.tensor(lq).cumsum(0).tolist(), dtype=torch.int32)
     cu_k = torch.tensor([0] + torch.tensor(lk).cumsum(0).tolist(), dtype=torch.int32)
@@ -402,7 +402,8 @@ def varlen_bwd_case(lq, lk, Hq, Hkv, D, seed, causal):
     o, lse = pkg.ffpa_fwd_varlen(qd, kd, vd, cqd, ckd, max(lq), max(lk), causal=causal,
                                  enable_gqa=gqa, return_lse=True)
     dq, dk, dv, delta = pkg.ffpa_bwd_varlen(dod, qd, kd, vd, o, lse, cqd, ckd, max(lq), max(lk),
-                                            causal=causal, enable_gqa=gqa, return_delta=True)
+                                            causal=causal, enable_gqa=gqa, return_delta=True,
+                                            workspace=workspace)
     device_ok()
     rq, rk, rv = oracle.attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal=causal)
     tag = f"varlen lq={lq} lk={lk} Hq{Hq} Hkv{Hkv} D{D} causal={causal}"
@@ -424,6 +425,54 @@ def test_bwd_varlen_cross_d512():
 def test_bwd_varlen_causal_fewer_keys():
     """Rows that see no key (lower-right alignment with Lk < Lq) get zero gradients."""
     varlen_bwd_case([50, 10, 257], [20, 10, 260], 2, 1, 256, seed=73, causal=True)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None])
+@pytest.mark.parametrize("D,causal", [(512, True), (384, False), (256, True)])
+def test_bwd_varlen_tiles(D, causal, workspace):
+    """Stored tiles (workspace="auto") and slice kernels on ragged packed
+    sequences: an empty sequence, one shorter than a tile, GQA groups of 2."""
+    varlen_bwd_case([300, 0, 77, 450, 129], [300, 0, 77, 450, 129], 4, 2, D, seed=80 + D, causal=causal,
+                    workspace=workspace)
+
+
+def test_bwd_varlen_tiles_cross_fewer_keys():
+    """Cross lengths per sequence, some with fewer keys than queries (lower-right
+    causal: the first rows see no key and get zero gradients)."""
+    varlen_bwd_case([200, 33, 300], [150, 40, 500], 2, 1, 512, seed=91, causal=True)
+    varlen_bwd_case([200, 33, 300], [150, 40, 500], 2, 2, 256, seed=92, causal=False)
+
+
+def test_bwd_varlen_small_workspace_reports_invalid():
+    """A workspace that holds the header and three blocks but fewer than the
+    sequences need: the kernels skip the blocks past its end (no access
+    outside it) and record FFPA_ERR_INVALID in the call's status word; the
+    next call with a workspace of the full size is correct."""
+    lq = [300, 450]
+    g = torch.Generator().manual_seed(95)
+    cu = torch.tensor([0, 300, 750], dtype=torch.int32)
+    T, H, D = 750, 2, 512
+    q, k, v, dout = (torch.randn(T, H, D, generator=g).bfloat16() for _ in range(4))
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
+    cud = cu.to(DEV)
+    o, lse = pkg.ffpa_fwd_varlen(qd, kd, vd, cud, None, 450, 450, causal=True, return_lse=True)
+    device_ok()
+    need = pkg.varlen_bwd_workspace_bytes(cu.tolist(), cu.tolist(), H, H, D, True)
+    small = torch.zeros(1024 + 3 * 32768, dtype=torch.uint8, device=DEV)
+    assert small.numel() < need
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pkg.ffpa_bwd_varlen(dod, qd, kd, vd, o, lse, cud, None, 450, 450, causal=True, workspace=small,
+                        status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == pkg.FFPA_ERR_INVALID
+    assert pkg.ffpa_last_device_error() == pkg.FFPA_OK
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    dq, dk, dv = pkg.ffpa_bwd_varlen(dod, qd, kd, vd, o, lse, cud, None, 450, 450, causal=True, workspace=ws)
+    device_ok()
+    rq, rk, rv = oracle.attn_bwd_varlen(q, k, v, dout, cu, cu, causal=True)
+    check_grad(dq, rq, "varlen dQ after a small workspace")
+    check_grad(dk, rk, "varlen dK after a small workspace")
+    check_grad(dv, rv, "varlen dV after a small workspace")
 
 
 def test_autograd_varlen():
