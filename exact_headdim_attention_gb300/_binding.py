@@ -375,6 +375,14 @@ def bwd_workspace_bytes(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int, D: int,
     return int(load_library().ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, int(bool(is_causal))))
 
 
+def _release_on(ws, workspace, stream):
+    """A workspace allocated here is freed when the call returns: on a launch
+    stream other than the current one, the caching allocator must not hand its
+    memory out again before the kernels on that stream are done with it."""
+    if ws is not None and isinstance(workspace, str) and isinstance(stream, torch.cuda.Stream):
+        ws.record_stream(stream)
+
+
 def varlen_bwd_workspace_bytes(cu_q, cu_k, Hq: int, Hkv: int, D: int, causal: bool = False) -> int:
     """Bytes of the varlen stored-tile backward's workspace for these sequences
     (cu_q, cu_k: host sequences of cumulative lengths; 0: the path does not apply)."""
@@ -443,6 +451,7 @@ def ffpa_bwd(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tens
                             _strides(k), _strides(v), _strides(out), _strides(dout), _strides(dq),
                             _strides(dk), _strides(dv), mptr, mk, mstr, sc, int(bool(is_causal)),
                             int(bool(enable_gqa)), ws_ptr, ws_bytes, _stream_handle(stream, q), opts)
+    _release_on(ws_keep, workspace, stream)
     del keep, ws_keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd")
@@ -634,6 +643,7 @@ def ffpa_bwd_varlen(dout: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: tor
                                    cuq.data_ptr(), None if cuk is None else cuk.data_ptr(), len(cq) - 1,
                                    int(max_seqlen_q), int(max_seqlen_k), sc, int(bool(causal)),
                                    int(bool(enable_gqa)), ws_ptr, ws_bytes, _stream_handle(stream, q), opts)
+    _release_on(ws_keep, workspace, stream)
     del ws_keep
     if st != FFPA_OK:
         _raise(st, "ffpa_bwd_varlen")
