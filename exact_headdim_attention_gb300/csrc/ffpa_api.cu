@@ -428,13 +428,13 @@ ffpa_status bwd_launch(BwdParams& P, bool any_q, bool any_k, const CallOpts& o, 
   return launch_bwd(P, static_cast<int>(dq_items), static_cast<int>(kv_items), smem, smem_two, stream);
 }
 
-// Stored-tile backward: dense, D = 256, 384 or 512, at least one query row
+// Stored-tile backward: dense, D = 128, 256, 384 or 512, at least one query row
 // and one key.  Workspace bytes (0: the path does not apply): a 32 KB block
 // of zeros, then P and dS, one 32 KB block (128 x 128 16-bit values) per
 // (b, hq, query tile, stored key tile) each (causal: only the key tiles the
 // query tile sees).
 size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D, int causal) {
-  if (!(D == 256 || D == 384 || D == 512) || B < 1 || Hq < 1 || Nq < 1 || Nkv < 1) return 0;
+  if (!(D == 128 || D == 256 || D == 384 || D == 512) || B < 1 || Hq < 1 || Nq < 1 || Nkv < 1) return 0;
   if (causal && Nkv < Nq) return 0;
   const long long blocks = (long long)B * Hq * bwd_stored_before((Nq + BM - 1) / BM, Nq, Nkv, causal);
   if (blocks > (1LL << 30)) return 0;
@@ -446,7 +446,7 @@ size_t bwd_tiles_bytes(int B, int Hq, int Nq, int Nkv, int D, int causal) {
 size_t bwd_varlen_header_bytes(int nseq) { return (((size_t)nseq + 1) * 8 + 1023) / 1024 * 1024; }
 
 size_t bwd_varlen_tiles_bytes(const int32_t* cu_q, const int32_t* cu_k, int nseq, int Hq, int D, int causal) {
-  if (!(D == 256 || D == 384 || D == 512) || !cu_q || nseq < 1 || Hq < 1) return 0;
+  if (!(D == 128 || D == 256 || D == 384 || D == 512) || !cu_q || nseq < 1 || Hq < 1) return 0;
   if (!cu_k) cu_k = cu_q;
   long long blocks = 0;
   for (int s = 0; s < nseq; ++s) {
@@ -1005,10 +1005,10 @@ ffpa_status ffpa_bwd_varlen_ws_ex(const void* q, const void* k, const void* v, c
     if (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv)) return FFPA_ERR_INVALID;
   }
   int dev = 0;
-  // The stored-tile path: D = 256, 384 or 512, both sides present, and a
+  // The stored-tile path: D = 128, 256, 384 or 512, both sides present, and a
   // workspace of at least the header and three blocks (the kernels check
   // every block index against the blocks it holds).
-  const bool tiles = workspace != nullptr && (D == 256 || D == 384 || D == 512) && any_q && any_k &&
+  const bool tiles = workspace != nullptr && (D == 128 || D == 256 || D == 384 || D == 512) && any_q && any_k &&
                      workspace_bytes >= bwd_varlen_header_bytes(nseq) + 3 * (size_t)P_TILE_BYTES;
   if (tiles && !aligned16(workspace)) return FFPA_ERR_INVALID;
   ffpa_status st = check_devices({any_q ? q : nullptr, any_q ? o : nullptr, any_q ? dout : nullptr,

@@ -7,7 +7,7 @@ namespace ffpa {
 using namespace bwd;
 
 // =====================================================================
-// Backward by stored score tiles (dense layout, D = 256, 384, 512).
+// Backward by stored score tiles (dense and varlen layouts, D = 128, 256, 384, 512).
 //
 // The gradients (backward of FFPAAttnFunc, FFPA API reference,
 // "ffpa_attn.ffpa_attn_func") need, per query row i and key j,
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(1024) ffpa_bwd_bases_kernel(const __grid_const
   if (t == 1023) out[n] = part[1023];
 }
 
-// NCH = D / 64 (4, 6 or 8): every MMA issue loop has a compile-time trip count.
+// NCH = D / 64 (2, 4, 6 or 8): every MMA issue loop has a compile-time trip count.
 template <int NCH, bool UMASK>
 __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __grid_constant__ BwdParams p) {
   constexpr int NPR = NCH / 2;   // 32 KB stages per K (or V) tile
@@ -864,6 +864,7 @@ ffpa_status launch_bwd_tiles(const BwdParams& P, int score_items, int contract_i
   if (launch_bwd_delta(P, stream) != FFPA_OK) return FFPA_ERR_CUDA;
   if (P.varlen && launch_bwd_tiles_bases(P, stream) != FFPA_OK) return FFPA_ERR_CUDA;
   switch (P.nchunks) {
+    case 2: return launch_tiles_t<2>(P, score_items, contract_items, smem_scores, smem_contract, stream);
     case 4: return launch_tiles_t<4>(P, score_items, contract_items, smem_scores, smem_contract, stream);
     case 6: return launch_tiles_t<6>(P, score_items, contract_items, smem_scores, smem_contract, stream);
     case 8: return launch_tiles_t<8>(P, score_items, contract_items, smem_scores, smem_contract, stream);

@@ -132,7 +132,7 @@ ffpa_status launch_bwd_delta(const BwdParams& P, cudaStream_t stream);
 // Stored-tile backward (ffpa_bwd_tiles.cu): the delta pass, the scores
 // kernel (P and dS once per query tile x key tile into the caller's
 // workspace) and the contraction kernel (dQ, dV and dK from the stored
-// tiles).  D / 64 in {4, 6, 8}.
+// tiles).  D / 64 in {2, 4, 6, 8}.
 ffpa_status launch_bwd_tiles(const BwdParams& P, int score_items, int contract_items, size_t smem_scores,
                              size_t smem_contract, cudaStream_t stream);
 // Varlen: the first stored block of every sequence (P.ws_base), from

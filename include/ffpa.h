@@ -314,8 +314,8 @@ ffpa_status ffpa_bwd_ex(const void* q, const void* k, const void* v, const void*
  *     ffpa_bwd_workspace_bytes(B, Hq, Hkv, Nq, Nkv, D, is_causal) bytes; its
  *     contents on entry do not matter and on return are unspecified.
  *
- * When ffpa_bwd_workspace_bytes() is non-zero (dense layout, D = 256, 384
- * or 512, Nq > 0, Nkv > 0) and the workspace is large enough, each
+ * When ffpa_bwd_workspace_bytes() is non-zero (dense layout, D = 128, 256,
+ * 384 or 512, Nq > 0, Nkv > 0) and the workspace is large enough, each
  * (128-query, 128-key) tile's softmax P and dS (times scale) are formed
  * once, as 16-bit values, into the workspace, and dq, dv, dk are
  * contractions over the stored tiles: no product of the definition is
@@ -392,7 +392,7 @@ ffpa_status ffpa_bwd_varlen_ex(const void* q, const void* k, const void* v, cons
  *
  *   workspace, workspace_bytes: device memory of q's device, 16-byte
  *     aligned, owned by the caller.  The stored-tile path runs when D is
- *     256, 384 or 512, Tq, Tk > 0, and workspace_bytes is at least
+ *     128, 256, 384 or 512, Tq, Tk > 0, and workspace_bytes is at least
  *     ffpa_bwd_varlen_workspace_bytes() of the same sequences (computed on
  *     the host from host copies of cu_seqlens_q / cu_seqlens_k, which the
  *     library cannot read there); a smaller workspace that still holds the

@@ -259,8 +259,9 @@ def test_bwd_workspace_bytes(lib):
     assert wb(1, 16, 16, 4096, 4096, 512) == (2 * 16 * 32 * 32 + 1) * 32768
     assert wb(2, 8, 2, 300, 129, 256) == (2 * 2 * 8 * 3 * 2 + 1) * 32768
     assert wb(1, 4, 1, 1, 1, 384) == (2 * 4 + 1) * 32768
-    for D in (64, 128, 192, 320, 448, 576, 768, 1024):
+    for D in (64, 192, 320, 448, 576, 768, 1024):
         assert wb(1, 2, 2, 256, 256, D) == 0, D          # the slice kernels only
+    assert wb(1, 2, 2, 256, 256, 128) == (2 * 2 * 2 * 2 + 1) * 32768
     assert wb(1, 2, 2, 0, 256, 512) == 0                 # no query rows
     assert wb(1, 2, 2, 256, 0, 512) == 0                 # no keys
     assert wb(1, 3, 2, 256, 256, 512) == 0               # not a grouping
@@ -318,7 +319,7 @@ def test_varlen_bwd_workspace_bytes(lib):
         for causal in (False, True):
             for Hq in (1, 4):
                 assert vb(cq, ck, Hq, 1, 512, causal) == want(cq, ck, Hq, causal), (cq, ck, causal)
-    assert vb([0, 300], [0, 300], 2, 2, 128, False) == 0          # the slice kernels only
+    assert vb([0, 300], [0, 300], 2, 2, 64, False) == 0           # the slice kernels only
     assert vb([0, 0, 0], [0, 0, 0], 2, 2, 512, False) == 0        # nothing to store
     assert vb([0, 300], [0, 300], 3, 2, 512, False) == 0          # not a grouping
 
