@@ -69,9 +69,10 @@ constexpr int TC_MMA_WARP = 5;
 
 // Block of the stored P (or dS) for (batch or sequence b, query head h, query
 // tile qt, key tile kt) of a problem with q_len queries and kv_len keys.
+template <bool VARLEN>
 __device__ __forceinline__ long long stored_block(const BwdParams& p, int b, int h, int q_len, int kv_len, int qt,
                                                   int kt) {
-  if (p.varlen) {
+  if constexpr (VARLEN) {
     const long long per_head = bwd_stored_before((q_len + BM - 1) / BM, q_len, kv_len, p.causal);
     return p.ws_base[b] + (long long)h * per_head + bwd_stored_before(qt, q_len, kv_len, p.causal) + kt;
   }
@@ -80,11 +81,17 @@ __device__ __forceinline__ long long stored_block(const BwdParams& p, int b, int
 
 // A block index past the caller's workspace: recorded as an invalid
 // argument in the call's status word (a varlen workspace smaller than the
-// sequences need); the block is then neither written nor read.
+// sequences need); the block is then neither written nor read.  The dense
+// workspace is sized by the library itself: no check.
+template <bool VARLEN>
 __device__ __forceinline__ bool block_in_workspace(const BwdParams& p, long long blk) {
-  if (blk < p.ws_blocks) return true;
-  atomicExch(p.err, (int)FFPA_ERR_INVALID);
-  return false;
+  if constexpr (!VARLEN) {
+    return true;
+  } else {
+    if (blk < p.ws_blocks) return true;
+    atomicExch(p.err, (int)FFPA_ERR_INVALID);
+    return false;
+  }
 }
 
 // Varlen: the first stored block of every sequence (an exclusive scan of
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(1024) ffpa_bwd_bases_kernel(const __grid_const
 }
 
 // NCH = D / 64 (2, 4, 6 or 8): every MMA issue loop has a compile-time trip count.
-template <int NCH, bool UMASK>
+template <int NCH, bool UMASK, bool VARLEN>
 __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __grid_constant__ BwdParams p) {
   constexpr int NPR = NCH / 2;   // 32 KB stages per K (or V) tile
   if (blockIdx.x == 0) {
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
           drop = false;
         } else {
           mbar_arrive_expect_tx(fb, SLOT_BYTES);
-          if (p.varlen)
+          if constexpr (VARLEN)
             tma_load_4d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, it.kv_row0 + row, chunk, it.hkv);
           else
             tma_load_5d(ring_u32 + slot * SLOT_BYTES, m, fb, 0, row, chunk, it.hkv, it.b);
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
       mbar_arrive_expect_tx(qb, (uint32_t)NCH * CHUNK_BYTES);
       auto qload = [&](const CUtensorMap* m, uint32_t bar) {
         for (int pr = 0; pr < NPR; ++pr) {
-          if (p.varlen)
+          if constexpr (VARLEN)
             tma_load_4d(do_u32 + pr * SLOT_BYTES, m, bar, 0, it.q_row0 + it.row0, 2 * pr, it.hq);
           else
             tma_load_5d(do_u32 + pr * SLOT_BYTES, m, bar, 0, it.row0, 2 * pr, it.hq, it.b);
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
     // r in the stored blocks: every row of a block is written, zeros where
     // the row or key is out of range.  A warp's store covers 32 consecutive
     // rows of one unit: 512 contiguous bytes.
-    const long long blk0 = stored_block(p, it.b, it.hq, it.q_len, it.kv_len, it.row0 / BM, 0);
+    const long long blk0 = stored_block<VARLEN>(p, it.b, it.hq, it.q_len, it.kv_len, it.row0 / BM, 0);
     const long long uoff = (blk0 << 15) + (long long)(8 * half) * 2048 + r * 16;
     uint8_t* const pbase = static_cast<uint8_t*>(p.ws_p) + uoff;
     uint8_t* const dsbase = static_cast<uint8_t*>(p.ws_ds) + uoff;
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1) ffpa_bwd_scores_kernel(const __
           pv[e] = v;
         }
       }
-      const bool in_ws = block_in_workspace(p, blk0 + j0 + jj);
+      const bool in_ws = block_in_workspace<VARLEN>(p, blk0 + j0 + jj);
       if (in_ws) {
         uint8_t* const dst = pbase + ((long long)(j0 + jj) << 15);
 #pragma unroll
@@ -495,6 +502,7 @@ struct PairItem {
 
 // False for a pair past the end of its sequence (varlen; same answer in
 // both CTAs).
+template <bool VARLEN>
 __device__ __forceinline__ bool decode_pair_item(const BwdParams& p, int L, uint32_t rank, PairItem& it) {
   int r;
   contract_role(p, L, it.role, r);
@@ -518,7 +526,7 @@ __device__ __forceinline__ bool decode_pair_item(const BwdParams& p, int L, uint
     it.b = bh / p.Hkv;
     it.hq = it.hkv * p.group;
   }
-  if (p.varlen) {
+  if constexpr (VARLEN) {
     it.q_row0 = p.cu_q[it.b];
     it.q_len = p.cu_q[it.b + 1] - it.q_row0;
     it.kv_row0 = p.cu_k[it.b];
@@ -556,14 +564,14 @@ __device__ __forceinline__ bool decode_pair_item(const BwdParams& p, int L, uint
 // the bytes per multiply-add are about 60 % of a single CTA's.  The peer's
 // warp 5 relays its "stage landed" events to the leader's full barriers; the
 // leader's commits arrive in both CTAs.
-template <int NCH>
+template <int NCH, bool VARLEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     ffpa_bwd_contract_kernel(const __grid_constant__ BwdParams p) {
   constexpr int NG = (NCH + 3) / 4;   // 256-column groups (the last may have 128)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   PairItem it;
-  if (!decode_pair_item(p, blockIdx.x >> 1, rank, it)) return;   // same answer in both CTAs
+  if (!decode_pair_item<VARLEN>(p, blockIdx.x >> 1, rank, it)) return;   // same answer in both CTAs
   const bool dq_role = it.role == BWD_ROLE_DQ;
   const int T = it.n_iter;
   const bool fp16 = p.fp16 != 0;
@@ -644,8 +652,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         }
         const bool real = qt < it.n_qt && kt < bwd_stored_tiles(qt, it.q_len, it.kv_len, p.causal);
         if (!real) return p.ws_zero;
-        const long long blk = stored_block(p, it.b, head, it.q_len, it.kv_len, qt, kt);
-        return block_in_workspace(p, blk) ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
+        const long long blk = stored_block<VARLEN>(p, it.b, head, it.q_len, it.kv_len, qt, kt);
+        return block_in_workspace<VARLEN>(p, blk) ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
       };
       // The stored blocks come from DRAM: for D >= 384 each is requested into
       // L2 this many steps before its copy into the ring (measured at D = 512:
@@ -675,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           // 256-column group: chunks 4g + 2 rank, +1; a 128-column tail: chunk 4g + rank.
           const int c0 = (4 * g + 4 <= NCH) ? 4 * g + 2 * (int)rank : 4 * g + (int)rank;
           if (dst) {
-            if (p.varlen)
+            if constexpr (VARLEN)
               tma_load_4d(dst, bmap, fb, 0, (dq_role ? it.kv_row0 : it.q_row0) + b_row, c0, b_head);
             else
               tma_load_5d(dst, bmap, fb, 0, b_row, c0, b_head, it.b);
@@ -838,14 +846,16 @@ template <int NCH>
 static ffpa_status launch_tiles_t(const BwdParams& P, int score_items, int contract_items, size_t smem_s,
                                   size_t smem_c, cudaStream_t stream) {
   if (score_items > 0) {
-    auto ks = P.mask != nullptr ? ffpa_bwd_scores_kernel<NCH, true> : ffpa_bwd_scores_kernel<NCH, false>;
+    auto ks = P.varlen           ? ffpa_bwd_scores_kernel<NCH, false, true>
+              : P.mask != nullptr ? ffpa_bwd_scores_kernel<NCH, true, false>
+                                  : ffpa_bwd_scores_kernel<NCH, false, false>;
     const ffpa_status st = set_smem_attr_once(reinterpret_cast<const void*>(ks), P.device, static_cast<int>(smem_s));
     if (st != FFPA_OK) return st;
     ks<<<score_items, TS_THREADS, smem_s, stream>>>(P);
     if (cudaGetLastError() != cudaSuccess) return FFPA_ERR_CUDA;
   }
   if (contract_items > 0) {
-    auto kc = ffpa_bwd_contract_kernel<NCH>;
+    auto kc = P.varlen ? ffpa_bwd_contract_kernel<NCH, true> : ffpa_bwd_contract_kernel<NCH, false>;
     const ffpa_status st = set_smem_attr_once(reinterpret_cast<const void*>(kc), P.device, static_cast<int>(smem_c));
     if (st != FFPA_OK) return st;
     kc<<<2 * contract_items, TC_THREADS, smem_c, stream>>>(P);

@@ -352,10 +352,12 @@ static __device__ __forceinline__ bool wait_bounded_inl(uint32_t bar, uint32_t p
                                                         bool cluster = false) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    // Suspended waiting keeps idle warps from taking issue slots away from
-    // the MMA and TMA threads that share their SM sub-partition.
-    if (cluster ? mbar_try_wait_sleep_cluster(bar, parity, 20000u)
-                : mbar_try_wait_sleep(bar, parity, 20000u))
+    // try_wait without a suspend-time hint (the instruction still waits a
+    // hardware-chosen while before it reports an incomplete phase): the
+    // waiting warp resumes sooner after the phase completes than a suspended
+    // one (measured on GB300: D=512 forward 1173 -> 1204 TFLOPS, causal GQA
+    // 1063 -> 1075, backward 1.315 -> 1.309 ms).
+    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
       return true;
     if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
