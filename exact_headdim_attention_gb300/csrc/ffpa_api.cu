@@ -870,6 +870,11 @@ ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const vo
     const uint64_t sd[4] = {(uint64_t)do_str[2] * 2, 128, (uint64_t)do_str[1] * 2, (uint64_t)do_str[0] * 2};
     if ((st = encode_map(&P.tm_q, tdt, 5, q, dq5, sq, box)) != FFPA_OK) return st;
     if ((st = encode_map(&P.tm_do, tdt, 5, dout, dq5, sd, box)) != FFPA_OK) return st;
+    if (tiles) {   // output stores of the contraction: box 64 x 32 rows
+      const uint32_t obox[5] = {64, 32, 1, 1, 1};
+      const uint64_t sdq[4] = {(uint64_t)dq_str[2] * 2, 128, (uint64_t)dq_str[1] * 2, (uint64_t)dq_str[0] * 2};
+      if ((st = encode_map(&P.tm_dq, tdt, 5, dq, dq5, sdq, obox)) != FFPA_OK) return st;
+    }
   }
   if (any_k) {
     const uint64_t dk5[5] = {64, (uint64_t)Nkv, nch, (uint64_t)Hkv, (uint64_t)B};
@@ -877,6 +882,13 @@ ffpa_status ffpa_bwd_ws_ex(const void* q, const void* k, const void* v, const vo
     const uint64_t sv[4] = {(uint64_t)v_str[2] * 2, 128, (uint64_t)v_str[1] * 2, (uint64_t)v_str[0] * 2};
     if ((st = encode_map(&P.tm_k, tdt, 5, k, dk5, sk, box)) != FFPA_OK) return st;
     if ((st = encode_map(&P.tm_v, tdt, 5, v, dk5, sv, box)) != FFPA_OK) return st;
+    if (tiles) {
+      const uint32_t obox[5] = {64, 32, 1, 1, 1};
+      const uint64_t sdk[4] = {(uint64_t)dk_str[2] * 2, 128, (uint64_t)dk_str[1] * 2, (uint64_t)dk_str[0] * 2};
+      const uint64_t sdv[4] = {(uint64_t)dv_str[2] * 2, 128, (uint64_t)dv_str[1] * 2, (uint64_t)dv_str[0] * 2};
+      if ((st = encode_map(&P.tm_dk, tdt, 5, dk, dk5, sdk, obox)) != FFPA_OK) return st;
+      if ((st = encode_map(&P.tm_dv, tdt, 5, dv, dk5, sdv, obox)) != FFPA_OK) return st;
+    }
   }
   P.o = o;
   P.dout = dout;

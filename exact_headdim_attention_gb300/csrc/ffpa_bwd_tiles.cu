@@ -761,9 +761,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     // Warp w's 32 rows go through ring slot w (idle once the accumulator is
-    // complete): thread t writes its row's 16-bit values there (16-byte unit
-    // x of row t at unit x ^ (t & 7), conflict-free), then the warp stores
-    // the rows one by one, each warp store covering 512 contiguous bytes.
+    // complete).  Dense: tensor stores of 32-row boxes.  Varlen (a box could
+    // reach into the next sequence's rows): thread t writes its row's 16-bit
+    // values there (16-byte unit x of row t at unit x ^ (t & 7),
+    // conflict-free), then the warp stores the rows one by one, each warp
+    // store covering 512 contiguous bytes.
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
     if (T > 0) {
@@ -771,7 +773,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       ok = __all_sync(0xffffffffu, w);
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && !VARLEN) {
+      // Dense: per 64-column chunk a 32-row x 128-byte box of the slot
+      // (4 KB, 128-byte swizzle: unit u of row t at u ^ (t & 7)), written out
+      // by tensor stores; the rows past the tensor's end are not written.
+      const uint32_t stage = ring_u32 + warp * SLOT_BYTES;
+      const uint32_t sw = (uint32_t)(lane & 7);
+#pragma unroll 1
+      for (int c0 = 0; c0 < NCH * DK; c0 += 64) {
+        uint32_t va[32], vb[32];
+        if (T > 0) {
+          tmem_ld32(lane_base + c0, va);
+          tmem_ld32(lane_base + c0 + 32, vb);
+          tmem_wait_ld();
+          reg_fence(va);
+          reg_fence(vb);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) va[c] = vb[c] = 0u;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 2 * c;
+          const float a0 = __uint_as_float(e < 32 ? va[e] : vb[e - 32]);
+          const float a1 = __uint_as_float(e + 1 < 32 ? va[e + 1] : vb[e + 1 - 32]);
+          pk[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+        }
+        const uint32_t box = stage + (uint32_t)(c0 / 64) * 4096u + lane * 128u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(box + (((uint32_t)q ^ sw) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int row0 = it.my_tile * BM + warp * 32;
+      if (lane == 0 && row0 < (dq_role ? it.q_len : it.kv_len)) {
+        const CUtensorMap* om = dq_role ? &p.tm_dq : it.role == BWD_ROLE_DV ? &p.tm_dv : &p.tm_dk;
+        const int head = dq_role ? it.hq : it.hkv;
+#pragma unroll 1
+        for (int c = 0; c < NCH; ++c) tma_store_5d(om, stage + (uint32_t)c * 4096u, 0, row0, c, head, it.b);
+        bulk_commit_group();
+        bulk_wait_read_all();   // the slot is read before the CTA may exit
+      }
+      __syncwarp();
+    } else if (ok) {
       constexpr int ROWB = NCH * DK * 2;   // bytes of one output row
       constexpr int UNITS = ROWB / 16;
       const uint32_t stage = ring_u32 + warp * SLOT_BYTES;

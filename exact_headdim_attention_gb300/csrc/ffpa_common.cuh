@@ -188,6 +188,11 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  // dQ, dK, dV with box 64 x 32 rows (the stored-tile contraction's output
+  // stores, dense layout).
+  CUtensorMap tm_dq;
+  CUtensorMap tm_dk;
+  CUtensorMap tm_dv;
   const void* o;
   const void* dout;
   const float* lse;
