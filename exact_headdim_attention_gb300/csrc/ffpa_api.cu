@@ -749,6 +749,13 @@ ffpa_status ffpa_fwd_ex(const void* q, const void* k, const void* v, void* o, fl
       const uint32_t bv[5] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1, 1};
       if ((st = encode_map(&P.tm_v, tdt, 5, v, dk, sv, bv)) != FFPA_OK) return st;
     }
+    if (kn == Kern::SPLIT && P.split_c == 2 && P.q_res && Nq > 0) {
+      // The column-split pair kernel stores O through 32-row boxes.
+      const uint64_t so[4] = {(uint64_t)o_str[2] * 2, 128, (uint64_t)o_str[1] * 2, (uint64_t)o_str[0] * 2};
+      const uint32_t bo[5] = {64, 32, 1, 1, 1};
+      if ((st = encode_map(&P.tm_o, tdt, 5, o, dq, so, bo)) != FFPA_OK) return st;
+      P.o_tma = 1;
+    }
   }
   P.o = o;
   P.lse = lse;

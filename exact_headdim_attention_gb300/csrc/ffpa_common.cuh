@@ -246,6 +246,10 @@ struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  // O with box 64 x 32 rows: the column-split kernel's output stores (dense
+  // layout; o_tma = 1 when encoded).
+  CUtensorMap tm_o;
+  int o_tma;
   void* o;
   float* lse;
   const void* mask;
@@ -532,6 +536,61 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
     else
       li = ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
     p.lse[li] = lse;
+  }
+}
+
+// store_output for the dense layout through tensor stores: the warp's 32
+// rows are staged at `stage` (1 KB aligned, 4 KB per 64 columns) as 32-row
+// boxes with the 128-byte swizzle (unit u of row t at u ^ (t & 7)), and one
+// thread writes them with p.tm_o (rows past Nq and the zero padding
+// columns past D are not written).  The LSE as store_output.
+__device__ __forceinline__ void store_output_boxes(const Params& p, const Item& it, bool have_o,
+                                                   uint32_t lane_base, int warp, int lane, int row,
+                                                   bool row_valid, float l_sum, float m_ref, uint32_t stage) {
+  const bool fp16 = p.fp16 != 0;
+  const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+  const uint32_t sw = (uint32_t)(lane & 7);
+  for (int c0 = 0; c0 < it.dv; c0 += 64) {
+    uint32_t va[32], vb[32];
+    if (have_o) {
+      tmem_ld32(lane_base + c0, va);
+      tmem_ld32(lane_base + c0 + 32, vb);
+      tmem_wait_ld();
+      reg_fence(va);
+      reg_fence(vb);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) va[c] = vb[c] = 0u;
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int e = 2 * c;
+      const float a0 = __uint_as_float(e < 32 ? va[e] : vb[e - 32]) * inv_l;
+      const float a1 = __uint_as_float(e + 1 < 32 ? va[e + 1] : vb[e + 1 - 32]) * inv_l;
+      pk[c] = fp16 ? pack_f16(a0, a1) : pack_bf16(a0, a1);
+    }
+    const uint32_t box = stage + (uint32_t)(c0 / 64) * 4096u + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(box + (((uint32_t)q ^ sw) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  const int row0 = it.q0 + 32 * warp;
+  if (lane == 0 && row0 < it.q_len) {
+    const int nch = (p.D + DK - 1) / DK;
+    for (int c = 0; c < it.dv / 64; ++c) {
+      const int chunk = it.col_lo / 64 + c;
+      if (chunk < nch) tma_store_5d(&p.tm_o, stage + (uint32_t)c * 4096u, 0, row0, chunk, it.hq, it.b);
+    }
+    bulk_commit_group();
+    bulk_wait_read_all();   // the staging area is read before the CTA may exit
+  }
+  __syncwarp();
+  if (row_valid && p.lse != nullptr && it.slice == 0) {
+    const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+    p.lse[((long long)it.b * p.Hq + it.hq) * p.Nq + row] = lse;
   }
 }
 

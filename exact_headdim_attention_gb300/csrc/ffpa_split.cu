@@ -509,7 +509,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
         if (ok) l_sum += ld_shared_f32(smem_u32(&lbuf[r]));
       }
     }
-    if (ok || T == 0) store_output<VARLEN>(p, it, T > 0, lane_base, row, row_valid, l_sum, m_ref);
+    if (ok || T == 0) {
+      // Dense: the ring is idle once the last products are done; 16 KB per
+      // warp of it stage the output boxes for tensor stores.
+      if (!VARLEN && p.o_tma)
+        store_output_boxes(p, it, T > 0, lane_base, warp, lane, row, row_valid, l_sum, m_ref,
+                           ring_u32 + (uint32_t)warp * 16384u);
+      else
+        store_output<VARLEN>(p, it, T > 0, lane_base, row, row_valid, l_sum, m_ref);
+    }
     if (r == 0 && ok && T > 0) {
       // Before this CTA may exit: the peer has read every P tile copied to it.
       const int n_own = (T - own0 + 1) >> 1;
