@@ -306,6 +306,13 @@ def test_bwd_full_size_d512_sampled(workspace):
              workspace=workspace)
 
 
+@pytest.mark.parametrize("D", [128, 256, 384])
+def test_bwd_full_size_tiles_sampled(D):
+    """B1 H16 N4096 at the other stored-tile head dims (one workspace block
+    per tile, D/64 chunks per operand) on sampled rows."""
+    _sampled(1, 16, 16, 4096, D, seed=44 + D, causal=False, q_heads=[0, 9, 15], kv_heads=[4])
+
+
 def test_bwd_gqa_causal_d512_sampled():
     _sampled(1, 8, 2, 2048, 512, seed=42, causal=True, q_heads=[1, 6], kv_heads=[1])
 
@@ -441,6 +448,45 @@ def test_bwd_varlen_tiles_cross_fewer_keys():
     causal: the first rows see no key and get zero gradients)."""
     varlen_bwd_case([200, 33, 300], [150, 40, 500], 2, 1, 512, seed=91, causal=True)
     varlen_bwd_case([200, 33, 300], [150, 40, 500], 2, 2, 256, seed=92, causal=False)
+
+
+@pytest.mark.parametrize("workspace", ["auto", None])
+def test_bwd_varlen_full_size_sampled(workspace):
+    """The packed causal workload (8 sequences of 512..4096 rows, Hq16 Hkv4,
+    D512) at full size: dQ rows of every query head of every sequence, dK/dV
+    rows of one KV head in the shortest and in the longest sequence (the
+    oracle's cost grows with the group's rows times the sequence length).
+    Each sequence is its own dense causal problem for the oracle."""
+    w = wl.varlen_causal()
+    m = wl.materialize(w)
+    q, k, v, cu, lens = m["q"], m["k"], m["v"], m["cu_q"], m["seqlens"]
+    g = torch.Generator().manual_seed(w.seed + 2)
+    dout = torch.randn(q.shape, generator=g).to(q.dtype)
+    qd, kd, vd, dod, cud = (t.to(DEV) for t in (q, k, v, dout, cu))
+    o, lse = pkg.ffpa_fwd_varlen(qd, kd, vd, cud, None, max(lens), max(lens), causal=True,
+                                 enable_gqa=True, return_lse=True)
+    dq, dk, dv = pkg.ffpa_bwd_varlen(dod, qd, kd, vd, o, lse, cud, None, max(lens), max(lens),
+                                     causal=True, enable_gqa=True, workspace=workspace)
+    device_ok()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    by_len = sorted(range(len(lens)), key=lambda s: lens[s])
+    kv_head = {by_len[0]: 0, by_len[-1]: w.Hkv - 1}
+    for s, L in enumerate(lens):
+        a = int(cu[s])
+        dense = lambda t: t[a:a + L].permute(1, 0, 2).unsqueeze(0)   # [1, H, L, D] view
+        edge = [0, 1, 127, 128, L - 129, L - 1]
+        q_rows = edge + torch.randint(0, L, (8,), generator=g).tolist()
+        qr = [h * L + i for h in range(w.Hq) for i in q_rows]
+        k_rows = edge + torch.randint(0, L, (16,), generator=g).tolist() if s in kv_head else []
+        kr = [kv_head[s] * L + j for j in k_rows]
+        rq, rk, rv = oracle.attn_bwd_rows(dense(q), dense(k), dense(v), dense(dout), qr, kr,
+                                          is_causal=True)
+        tag = f"varlen full size seq {s} (L={L})"
+        check_grad(torch.stack([dq[a + i, h] for h in range(w.Hq) for i in q_rows]), rq, f"{tag} dQ")
+        if kr:
+            hk = kv_head[s]
+            check_grad(torch.stack([dk[a + j, hk] for j in k_rows]), rk, f"{tag} dK head {hk}")
+            check_grad(torch.stack([dv[a + j, hk] for j in k_rows]), rv, f"{tag} dV head {hk}")
 
 
 def test_bwd_varlen_small_workspace_reports_invalid():
