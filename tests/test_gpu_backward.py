@@ -58,8 +58,8 @@ def draw(B, Hq, Hkv, Nq, Nkv, D, seed, dtype=torch.bfloat16):
 
 def gpu_backward(q, k, v, dout, causal=False, scale=None, mask=None, workspace="auto"):
     """Forward then backward on the GPU, as a training step would run them.
-    workspace="auto" takes the stored-tile path where it applies (D = 256,
-    384, 512), None the slice kernels."""
+    workspace="auto" takes the stored-tile path where it applies (D = 128,
+    256, 384, 512), None the slice kernels."""
     gqa = q.shape[1] != k.shape[1]
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, dout))
     md = None if mask is None else mask.to(DEV)
@@ -146,7 +146,7 @@ def test_bwd_single_key(Nq, D):
 
 
 # ------------------------------------------------------------------ stored tiles vs slices
-# D = 256, 384, 512 take the stored-tile path by default; the same cases on
+# D = 128, 256, 384, 512 take the stored-tile path by default; the same cases on
 # the slice kernels (workspace=None) keep both paths checked.
 @pytest.mark.parametrize("D,causal", [(256, False), (384, True), (512, False), (512, True)])
 def test_bwd_sliced_path(D, causal):
@@ -454,9 +454,10 @@ def test_bwd_varlen_tiles_cross_fewer_keys():
 def test_bwd_varlen_full_size_sampled(workspace):
     """The packed causal workload (8 sequences of 512..4096 rows, Hq16 Hkv4,
     D512) at full size: dQ rows of every query head of every sequence, dK/dV
-    rows of one KV head in the shortest and in the longest sequence (the
-    oracle's cost grows with the group's rows times the sequence length).
-    Each sequence is its own dense causal problem for the oracle."""
+    rows of every KV head in the shortest sequence and of the last KV head in
+    the longest (the oracle's cost per KV head grows with the group's rows
+    times the sequence length).  Each sequence is its own dense causal
+    problem for the oracle."""
     w = wl.varlen_causal()
     m = wl.materialize(w)
     q, k, v, cu, lens = m["q"], m["k"], m["v"], m["cu_q"], m["seqlens"]
@@ -470,23 +471,23 @@ def test_bwd_varlen_full_size_sampled(workspace):
     device_ok()
     dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
     by_len = sorted(range(len(lens)), key=lambda s: lens[s])
-    kv_head = {by_len[0]: 0, by_len[-1]: w.Hkv - 1}
+    kv_heads = {by_len[0]: list(range(w.Hkv)), by_len[-1]: [w.Hkv - 1]}
     for s, L in enumerate(lens):
         a = int(cu[s])
         dense = lambda t: t[a:a + L].permute(1, 0, 2).unsqueeze(0)   # [1, H, L, D] view
         edge = [0, 1, 127, 128, L - 129, L - 1]
         q_rows = edge + torch.randint(0, L, (8,), generator=g).tolist()
         qr = [h * L + i for h in range(w.Hq) for i in q_rows]
-        k_rows = edge + torch.randint(0, L, (16,), generator=g).tolist() if s in kv_head else []
-        kr = [kv_head[s] * L + j for j in k_rows]
+        hks = kv_heads.get(s, [])
+        k_rows = edge + torch.randint(0, L, (16,), generator=g).tolist() if hks else []
+        kr = [hk * L + j for hk in hks for j in k_rows]
         rq, rk, rv = oracle.attn_bwd_rows(dense(q), dense(k), dense(v), dense(dout), qr, kr,
                                           is_causal=True)
         tag = f"varlen full size seq {s} (L={L})"
         check_grad(torch.stack([dq[a + i, h] for h in range(w.Hq) for i in q_rows]), rq, f"{tag} dQ")
         if kr:
-            hk = kv_head[s]
-            check_grad(torch.stack([dk[a + j, hk] for j in k_rows]), rk, f"{tag} dK head {hk}")
-            check_grad(torch.stack([dv[a + j, hk] for j in k_rows]), rv, f"{tag} dV head {hk}")
+            check_grad(torch.stack([dk[a + j, hk] for hk in hks for j in k_rows]), rk, f"{tag} dK heads {hks}")
+            check_grad(torch.stack([dv[a + j, hk] for hk in hks for j in k_rows]), rv, f"{tag} dV heads {hks}")
 
 
 def test_bwd_varlen_small_workspace_reports_invalid():
