@@ -655,10 +655,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         const long long blk = stored_block<VARLEN>(p, it.b, head, it.q_len, it.kv_len, qt, kt);
         return block_in_workspace<VARLEN>(p, blk) ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
       };
-      // The stored blocks come from DRAM: for D >= 384 each is requested into
-      // L2 this many steps before its copy into the ring (measured at D = 512:
-      // 743 -> 725 us per launch; none at D = 256, whose steps are half as long).
-      constexpr int PF = NCH >= 6 ? 6 : 0;
+      // The stored blocks come from DRAM: each is requested into L2 this many
+      // steps before its copy into the ring.  Measured on GB300 (B1 H16 N4096):
+      // D = 512, about 20 us less per launch with 6 steps (9 steps: 1046 instead
+      // of 1052 TFLOPS for the whole backward); D = 128, 416 -> 433 TFLOPS
+      // with 2 steps (3: 431, 4: 429, 6: 423); D = 256, 830 without and 803
+      // with 3 steps: none there.
+      constexpr int PF = NCH >= 6 ? 6 : NCH == 2 ? 2 : 0;
       for (int i = 0; i < PF && i < T; ++i) {
         int br, hd;
         prefetch_l2_bulk(step(i, br, hd), P_TILE_BYTES);
