@@ -656,12 +656,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
         return block_in_workspace<VARLEN>(p, blk) ? static_cast<const void*>(abase + (blk << 15)) : p.ws_zero;
       };
       // The stored blocks come from DRAM: each is requested into L2 this many
-      // steps before its copy into the ring.  Measured on GB300 (B1 H16 N4096):
-      // D = 512, about 20 us less per launch with 6 steps (9 steps: 1046 instead
-      // of 1052 TFLOPS for the whole backward); D = 128, 416 -> 433 TFLOPS
-      // with 2 steps (3: 431, 4: 429, 6: 423); D = 256, 830 without and 803
-      // with 3 steps: none there.
-      constexpr int PF = NCH >= 6 ? 6 : NCH == 2 ? 2 : 0;
+      // steps before its copy into the ring.  Measured on GB300 (TFLOPS of the
+      // whole backward, B1 N4096; same-box A/B, two rounds): D = 512 1047 with
+      // 6 steps, 1052 with 2 (3: 1052, 4: 1051, 5: 1050, 8: 1046), causal GQA
+      // Hq16 Hkv4 949 -> 980; D = 384 893 -> 895; D = 128 416 -> 433 (3: 431,
+      // 6: 423); D = 256 831 without, 807 with 2 steps, 809 with 1: none there.
+      constexpr int PF = NCH == 4 ? 0 : 2;
       for (int i = 0; i < PF && i < T; ++i) {
         int br, hd;
         prefetch_l2_bulk(step(i, br, hd), P_TILE_BYTES);
