@@ -1220,6 +1220,15 @@ ffpa_status ffpa_fwd_varlen_ex(const void* q, const void* k, const void* v, void
     const uint32_t bv[4] = {64, (uint32_t)P.vk, (uint32_t)P.vchunks, 1};
     if ((st = encode_map(&P.tm_v, tdt, 4, v, dk, sv, bv)) != FFPA_OK) return st;
   }
+  if (kn == Kern::SPLIT && P.split_c == 2 && P.q_res && Tq > 0) {
+    // The column-split pair kernel stores the O tiles that lie inside their
+    // sequence through 32-row boxes of the packed rows.
+    const uint64_t dq[4] = {64, (uint64_t)Tq, nch, (uint64_t)Hq};
+    const uint64_t so[3] = {(uint64_t)o_str[0] * 2, 128, (uint64_t)o_str[1] * 2};
+    const uint32_t bo[4] = {64, 32, 1, 1};
+    if ((st = encode_map(&P.tm_o, tdt, 4, o, dq, so, bo)) != FFPA_OK) return st;
+    P.o_tma = 1;
+  }
   P.o = o;
   P.lse = lse;
   P.mask = nullptr;

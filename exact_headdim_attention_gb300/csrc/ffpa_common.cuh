@@ -544,6 +544,7 @@ __device__ __forceinline__ void store_output(const Params& p, const Item& it, bo
 // boxes with the 128-byte swizzle (unit u of row t at u ^ (t & 7)), and one
 // thread writes them with p.tm_o (rows past Nq and the zero padding
 // columns past D are not written).  The LSE as store_output.
+template <bool VARLEN>
 __device__ __forceinline__ void store_output_boxes(const Params& p, const Item& it, bool have_o,
                                                    uint32_t lane_base, int warp, int lane, int row,
                                                    bool row_valid, float l_sum, float m_ref, uint32_t stage) {
@@ -582,7 +583,11 @@ __device__ __forceinline__ void store_output_boxes(const Params& p, const Item& 
     const int nch = (p.D + DK - 1) / DK;
     for (int c = 0; c < it.dv / 64; ++c) {
       const int chunk = it.col_lo / 64 + c;
-      if (chunk < nch) tma_store_5d(&p.tm_o, stage + (uint32_t)c * 4096u, 0, row0, chunk, it.hq, it.b);
+      if (chunk >= nch) continue;
+      if (VARLEN)
+        tma_store_4d(&p.tm_o, stage + (uint32_t)c * 4096u, 0, it.q_row0 + row0, chunk, it.hq);
+      else
+        tma_store_5d(&p.tm_o, stage + (uint32_t)c * 4096u, 0, row0, chunk, it.hq, it.b);
     }
     bulk_commit_group();
     bulk_wait_read_all();   // the staging area is read before the CTA may exit
@@ -590,7 +595,9 @@ __device__ __forceinline__ void store_output_boxes(const Params& p, const Item& 
   __syncwarp();
   if (row_valid && p.lse != nullptr && it.slice == 0) {
     const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
-    p.lse[((long long)it.b * p.Hq + it.hq) * p.Nq + row] = lse;
+    const long long li = VARLEN ? (long long)it.hq * p.Tq + it.q_row0 + row
+                                : ((long long)it.b * p.Hq + it.hq) * p.Nq + row;
+    p.lse[li] = lse;
   }
 }
 

@@ -510,11 +510,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(SPLIT_THREADS, 1)
       }
     }
     if (ok || T == 0) {
-      // Dense: the ring is idle once the last products are done; 16 KB per
-      // warp of it stage the output boxes for tensor stores.
-      if (!VARLEN && p.o_tma)
-        store_output_boxes(p, it, T > 0, lane_base, warp, lane, row, row_valid, l_sum, m_ref,
-                           ring_u32 + (uint32_t)warp * 16384u);
+      // The ring is idle once the last products are done; 16 KB per warp of
+      // it stage the output boxes for tensor stores.  Varlen: only a tile
+      // whose 128 rows all lie in its sequence (a box must not reach into
+      // the next sequence's rows).
+      if (p.o_tma && (!VARLEN || it.q0 + BM <= it.q_len))
+        store_output_boxes<VARLEN>(p, it, T > 0, lane_base, warp, lane, row, row_valid, l_sum, m_ref,
+                                   ring_u32 + (uint32_t)warp * 16384u);
       else
         store_output<VARLEN>(p, it, T > 0, lane_base, row, row_valid, l_sum, m_ref);
     }
