@@ -301,8 +301,9 @@ def _sampled(B, Hq, Hkv, N, D, seed, causal, q_heads, kv_heads, n_rows=48, works
 @pytest.mark.parametrize("workspace", ["auto", None])
 def test_bwd_full_size_d512_sampled(workspace):
     """The self-attention workload B1 H16 N4096 D512 on sampled rows (stored
-    tiles, as the benchmark runs it, and the slice kernels)."""
-    _sampled(1, 16, 16, 4096, 512, seed=41, causal=False, q_heads=[0, 15], kv_heads=[7],
+    tiles, as the benchmark runs it, and the slice kernels): dQ rows of every
+    head, dK/dV rows of the first, a middle and the last head."""
+    _sampled(1, 16, 16, 4096, 512, seed=41, causal=False, q_heads=list(range(16)), kv_heads=[0, 7, 15],
              workspace=workspace)
 
 
@@ -310,11 +311,11 @@ def test_bwd_full_size_d512_sampled(workspace):
 def test_bwd_full_size_tiles_sampled(D):
     """B1 H16 N4096 at the other stored-tile head dims (one workspace block
     per tile, D/64 chunks per operand) on sampled rows."""
-    _sampled(1, 16, 16, 4096, D, seed=44 + D, causal=False, q_heads=[0, 9, 15], kv_heads=[4])
+    _sampled(1, 16, 16, 4096, D, seed=44 + D, causal=False, q_heads=list(range(16)), kv_heads=[0, 15])
 
 
 def test_bwd_gqa_causal_d512_sampled():
-    _sampled(1, 8, 2, 2048, 512, seed=42, causal=True, q_heads=[1, 6], kv_heads=[1])
+    _sampled(1, 8, 2, 2048, 512, seed=42, causal=True, q_heads=list(range(8)), kv_heads=[0, 1])
 
 
 # ------------------------------------------------------------------ autograd
