@@ -5,7 +5,6 @@ or index, a transposed operand or a wrong convention anywhere in the oracle.
 The mistakes are planted in temporary copies compiled on the CPU; the
 committed oracle is untouched.
 """
-import shutil
 from pathlib import Path
 
 import pytest
